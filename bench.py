@@ -1,0 +1,409 @@
+"""Benchmark: NVFP4 decode-attention KV-tokens/s and HBM GB/s (% of peak); append tokens/s.
+
+Workload (one attention layer): 4 sequences x 131,072 cached tokens + 1 new token each, 24 query /
+4 KV heads, head_dim 128, 64-token pages placed by a seeded permutation of a 40,000-page pool,
+RoPE on 32 dims (theta 1e7), bf16 inputs ~ N(0,1) with K/Q outlier channels x12.
+
+A step is one pass of the whole hot path: the fused quantize-append of the step's new tokens
+(Q, K, V) and the split-K decode attention over the whole cache (two kernel launches). The step
+re-appends the same positions, so every step sees the same cache. The KV read per step (302 MB)
+is larger than L2 (129 MB), so no L2 flush is needed between steps.
+
+`value` is device time with inputs resident in HBM; `e2e` adds, every step, the host->device
+copy of the new tokens from pinned memory, the split-K plan upload, and the device->host copy of
+the attention output. `roofline` covers the decode-attention kernel (events around each launch).
+`--impl reference` times the CPU oracle on a bounded sample of the same workload.
+
+Multi-GPU: the path has no exchange step, so N GPUs run N independent replicas (weak scaling);
+value = units of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+sys.path.insert(0, os.path.join(ROOT, "tests"))
+
+METRIC = "NVFP4 decode attn KV-tokens/s & HBM GB/s (% of peak); append tokens/s"
+UNIT = "KV-tokens/s"
+WORKLOAD = "steady_decode: 4 seqs x 131072 cached + 1 new token, Hq 24 / Hkv 4, d 128, page 64, 40k-page pool"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sms.append(float(f[1]))
+                maxes.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def decode_traffic_profile(rows_bytes):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "decode_attn_steady_decode.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    src = os.path.join(ROOT, "bit_kv_cache_03_gb300", "csrc", "decode.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if d.get("decode_cu_sha256_16") != h:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def oracle_sample(w, reps_target_s=10.0, max_reps=3):
+    """The CPU oracle on a bounded sample of the step: the new token of sequence 0 quantised
+    (Q/K/V) and its 24 heads' attention over all 131,073 keys of that sequence."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    s = 0
+    L = int(w.seq_lens[s])
+    table = oracle.rope_table(w.max_pos, w.rot_dim, w.theta, w.pos_scale)
+    k = w.k_rows(s, 0, L)
+    v = w.v_rows(s, 0, L)
+    pos = np.repeat(np.arange(L, dtype=np.int32), w.kv_heads)
+    # the cached part is state, not step work: quantised before the clock starts
+    kc, ks = oracle.quantize_rows(k[:-1].reshape(-1, 128), pos[:-w.kv_heads], True, table, w.rot_dim)
+    vc, vs = oracle.quantize_rows(v[:-1].reshape(-1, 128), None, False, None, 0)
+    q = w.q_rows(s, L - 1, 1)
+    nthreads = oracle.num_threads()
+
+    def one():
+        kn, ksn = oracle.quantize_rows(k[-1:].reshape(-1, 128), pos[-w.kv_heads:], True, table,
+                                       w.rot_dim)
+        vn, vsn = oracle.quantize_rows(v[-1:].reshape(-1, 128), None, False, None, 0)
+        qc, qs = oracle.quantize_rows(q.reshape(-1, 128),
+                                      np.full(w.q_heads, L - 1, np.int32), True, table, w.rot_dim)
+        KC = np.concatenate([kc, kn]); KS = np.concatenate([ks, ksn])
+        VC = np.concatenate([vc, vn]); VS = np.concatenate([vs, vsn])
+        rows = (np.zeros(w.q_heads, np.int32), np.zeros(w.q_heads, np.int32),
+                np.arange(w.q_heads, dtype=np.int32))
+        oracle.attention_rows(w.q_heads, w.kv_heads, 1, True, w.sm_scale, np.array([L], np.int32),
+                              np.array([0], np.int64), qc, qs, KC, KS, VC, VS, *rows)
+
+    t0 = time.perf_counter()
+    one()
+    dt = time.perf_counter() - t0
+    reps = 1
+    extra = max(0, min(max_reps - 1, int(reps_target_s / max(dt, 1e-3)) - 1))
+    t0 = time.perf_counter()
+    for _ in range(extra):
+        one()
+    if extra:
+        dt = (time.perf_counter() - t0) / extra
+        reps += extra
+    return {"value": L / dt, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": f"1 of 4 sequences ({L} KV tokens, 24 query heads, 1 new token: "
+                      f"quantise + fp64 attention), {reps} reps, {dt:.2f} s each"}
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample of the workload.
+
+    Each step: quantise sequence 0's new token (24 Q heads, 4 K and 4 V heads) and run the fp64
+    attention of one query head (cycling over the 24) over the first 1024 keys of that sequence.
+    One KV-token unit is one key seen by all 24 query heads, so a step covers 1024 / 24 units."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import synth
+    w = synth.steady_decode()
+    L = 1024
+    table = oracle.rope_table(w.max_pos, w.rot_dim, w.theta, w.pos_scale)
+    k = w.k_rows(0, 0, L)
+    v = w.v_rows(0, 0, L)
+    pos = np.repeat(np.arange(L, dtype=np.int32), w.kv_heads)
+    kc, ks = oracle.quantize_rows(k[:-1].reshape(-1, 128), pos[:-w.kv_heads], True, table,
+                                  w.rot_dim)
+    vc, vs = oracle.quantize_rows(v[:-1].reshape(-1, 128), None, False, None, 0)
+    q = w.q_rows(0, L - 1, 1)
+
+    def step(h):
+        kn, ksn = oracle.quantize_rows(k[-1:].reshape(-1, 128), pos[-w.kv_heads:], True, table,
+                                       w.rot_dim, 1)
+        vn, vsn = oracle.quantize_rows(v[-1:].reshape(-1, 128), None, False, None, 0, 1)
+        qc, qs = oracle.quantize_rows(q.reshape(-1, 128), np.full(w.q_heads, L - 1, np.int32),
+                                      True, table, w.rot_dim, 1)
+        rows = (np.zeros(1, np.int32), np.zeros(1, np.int32), np.array([h], np.int32))
+        oracle.attention_rows(w.q_heads, w.kv_heads, 1, True, w.sm_scale,
+                              np.array([L], np.int32), np.array([0], np.int64), qc, qs,
+                              np.concatenate([kc, kn]), np.concatenate([ks, ksn]),
+                              np.concatenate([vc, vn]), np.concatenate([vs, vsn]), *rows, 1)
+
+    for i in range(args.warmup):
+        step(i % w.q_heads)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i % w.q_heads)
+    dt = (time.perf_counter() - t0) / args.steps
+    units = L / w.q_heads
+    value = units / dt
+    sample = (f"per step: sequence 0, one of 24 query heads, fp64 attention over the first {L} "
+              f"keys + quantisation of the new token ({units:.1f} KV-token units), 1 thread")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_cuda(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import bit_kv_cache_03_gb300 as kv
+    import synth
+    from kvrun import GpuRun
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    w = synth.steady_decode()
+    g = GpuRun(w, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    g.cache.plan(w.seq_lens, w.q_len, w.chunk_tokens)
+
+    # ---- bulk append throughput (tokens with Q, K, V: the prefill-chunk shape) ----
+    Tb = 16384
+    qb = torch.randn(Tb, w.q_heads, 128, device=dev).to(torch.bfloat16)
+    kb = torch.randn(Tb, w.kv_heads, 128, device=dev).to(torch.bfloat16)
+    vb = torch.randn(Tb, w.kv_heads, 128, device=dev).to(torch.bfloat16)
+    sidb = torch.zeros(Tb, dtype=torch.int32, device=dev)
+    posb = torch.arange(Tb, dtype=torch.int32, device=dev)
+    qcb, qsb = g.cache.quantized_q_buffers(Tb)
+    spare = kv.PagedNVFP4Cache(Tb // 64, np.arange(Tb // 64, dtype=np.int32)[None], Tb,
+                               w.q_heads, w.kv_heads, w.rot_dim, device=dev)
+    for _ in range(3):
+        spare.append(kb, vb, sidb, posb, q=qb, q_codes=qcb, q_scales=qsb)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    e0.record(stream)
+    for _ in range(reps):
+        spare.append(kb, vb, sidb, posb, q=qb, q_codes=qcb, q_scales=qsb)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    append_s = e0.elapsed_time(e1) / 1e3 / reps
+    append_tps = Tb / append_s
+    append_bytes = Tb * ((w.q_heads + 2 * w.kv_heads) * 256 + (w.q_heads + 2 * w.kv_heads) * 72)
+    del spare, qb, kb, vb
+
+    # ---- timed decode steps (device-resident inputs) ----
+    for _ in range(args.warmup):
+        g.step(plan=False)
+    torch.cuda.synchronize(dev)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    t_begin.record(stream)
+    for i in range(args.steps):
+        g.cache.append(g.k, g.v, g.sid, g.pos, q=g.q, q_codes=g.q_codes, q_scales=g.q_scales)
+        starts[i].record(stream)
+        g.cache.attend(g.q_codes, g.q_scales, g.out, causal=w.causal, sm_scale=w.sm_scale)
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed = t_begin.elapsed_time(t_end) / 1e3
+    attn_times = [s.elapsed_time(e) / 1e3 for s, e in zip(starts, ends)]
+    attn_avg = sum(attn_times) / len(attn_times)
+    assert g.status() == 0, f"device status {g.status():#x}"
+
+    # ---- end to end through the public API, host buffers ----
+    q_h = torch.from_numpy(np.ascontiguousarray(w.new_tokens()[0]).view(np.int16)).pin_memory()
+    k_h = torch.from_numpy(np.ascontiguousarray(w.new_tokens()[1]).view(np.int16)).pin_memory()
+    v_h = torch.from_numpy(np.ascontiguousarray(w.new_tokens()[2]).view(np.int16)).pin_memory()
+    sid_h = torch.from_numpy(w.new_tokens()[3]).pin_memory()
+    pos_h = torch.from_numpy(w.new_tokens()[4]).pin_memory()
+    out_h = torch.empty(g.out.numel(), dtype=torch.float32).pin_memory()
+    q_d = torch.empty_like(q_h, device=dev)
+    k_d = torch.empty_like(k_h, device=dev)
+    v_d = torch.empty_like(v_h, device=dev)
+    sid_d = torch.empty_like(sid_h, device=dev)
+    pos_d = torch.empty_like(pos_h, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, sid_h, pos_h))
+    d2h = out_h.numel() * 4
+    e2e_steps = max(10, min(args.steps, 2000))
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True); k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True); sid_d.copy_(sid_h, non_blocking=True)
+        pos_d.copy_(pos_h, non_blocking=True)
+        g.cache.append(k_d.view(torch.bfloat16), v_d.view(torch.bfloat16), sid_d, pos_d,
+                       q=q_d.view(torch.bfloat16), q_codes=g.q_codes, q_scales=g.q_scales)
+        g.cache.plan(w.seq_lens, w.q_len, w.chunk_tokens)
+        g.cache.attend(g.q_codes, g.q_scales, g.out, causal=w.causal, sm_scale=w.sm_scale)
+        out_h.copy_(g.out, non_blocking=True)
+
+    for _ in range(5):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_elapsed = time.perf_counter() - t0
+
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([elapsed, e2e_elapsed], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed, e2e_elapsed = float(tt[0]), float(tt[1])
+    if rank != 0:
+        return
+
+    kv_tokens = int(w.seq_lens.sum())
+    value = world * kv_tokens * args.steps / elapsed
+    e2e_value = world * kv_tokens * e2e_steps / e2e_elapsed
+    n_pages = int(sum((int(l) + 63) // 64 for l in w.seq_lens))
+    T = w.num_seqs * w.q_len
+    attn_bytes = (kv_tokens * w.kv_heads * 144 + T * w.q_heads * 72 + n_pages * 4 +
+                  T * w.q_heads * 128 * 4)
+    peak, peak_kind = measured_peaks()
+    achieved = attn_bytes / attn_avg / 1e9
+    traffic = decode_traffic_profile(attn_bytes)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "kv_tokens_per_step": kv_tokens,
+                   "kv_bytes_per_step": kv_tokens * w.kv_heads * 144,
+                   "l2": "inputs larger than L2 (302 MB of KV per step vs 129 MB L2), no flush",
+                   "chunk_tokens": w.chunk_tokens, "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "hbm_gbs_attn": achieved,
+        "hbm_frac_attn_of_measured": achieved / peak,
+        "hbm_frac_attn_of_nominal_7900": achieved / 7900.0,
+        "attn_us": attn_avg * 1e6,
+        "attn_kv_tokens_per_s": kv_tokens / attn_avg,
+        "append_tokens_per_s": append_tps,
+        "append_gbs": append_bytes / append_s / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "decode_kernel (split-K NVFP4 attention, merge fused)",
+                     "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": attn_bytes},
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "includes": "pinned H2D of new Q/K/V + ids, append, plan upload, attention, D2H of output"},
+        "gpu_launches": 2 * args.steps,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(w)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    import __graft_entry__
+    __graft_entry__.build()
+    run_cuda(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+"""NVFP4 KV cache for GB300: Python binding of the C ABI in include/kv_nvfp4.h.
+
+Argument marshalling only: every step of the path runs in the CUDA library
+(``_build/libkvnvfp4.so``, built from ``csrc/`` for sm_103a). Importing this package loads that
+library and fails loudly if it is missing; there is no CPU fallback.
+
+Method: prismix.dev/news/833001997676, sections "NVFP4 KV cache (from scratch)" and "YaRN context
+extension" (NVFP4 K/V with E4M3 block scales, Hadamard-rotated K and Q, fused append, NVFP4 Q.K^T,
+V dequantised for P.V, 144 bytes per token per KV head, linear RoPE position scaling).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build_mod
+
+_LIB_PATH = _build_mod.LIB_PATH
+
+KV_NVFP4_OK = 0
+KV_NVFP4_EINVAL = -1
+KV_NVFP4_ECUDA = -2
+KV_NVFP4_ENOSPACE = -3
+DEV_BAD_PAGE, DEV_BAD_POS, DEV_BAD_SEQ, DEV_BAD_ROPE, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
+
+
+class Layout(ctypes.Structure):
+    """kv_nvfp4_layout"""
+    _fields_ = [("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("rot_dim", ctypes.c_int32)]
+
+
+class PlanInfo(ctypes.Structure):
+    """kv_nvfp4_plan_info"""
+    _fields_ = [("num_seqs", ctypes.c_int32), ("q_len", ctypes.c_int32),
+                ("chunk_pages", ctypes.c_int32), ("num_chunks", ctypes.c_int32),
+                ("num_row_groups", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("num_partials", ctypes.c_int32), ("max_chunks", ctypes.c_int32),
+                ("max_seq_len", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("total_kv_tokens", ctypes.c_int64),
+                ("off_seqinfo", ctypes.c_uint64), ("off_items", ctypes.c_uint64),
+                ("off_counters", ctypes.c_uint64), ("off_partials", ctypes.c_uint64),
+                ("workspace_bytes", ctypes.c_uint64)]
+
+
+class KVNVFP4Error(RuntimeError):
+    pass
+
+
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_F64 = ctypes.c_double
+_SIG = {
+    "kv_nvfp4_status_string": ([_I32], ctypes.c_char_p),
+    "kv_nvfp4_version": ([], _I32),
+    "kv_nvfp4_layout_check": ([ctypes.POINTER(Layout)], _I32),
+    "kv_nvfp4_page_bytes": ([ctypes.POINTER(Layout)], ctypes.c_size_t),
+    "kv_nvfp4_pool_plane_bytes": ([ctypes.POINTER(Layout), _I32, ctypes.POINTER(ctypes.c_size_t),
+                                   ctypes.POINTER(ctypes.c_size_t)], _I32),
+    "kv_nvfp4_rope_table_bytes": ([_I32, _I32], ctypes.c_size_t),
+    "kv_nvfp4_rope_table_fill_host": ([_P, _I32, _I32, _F64, _F64], _I32),
+    "kv_nvfp4_rope_table_init": ([_P, _I32, _I32, _F64, _F64, _P], _I32),
+    "kv_nvfp4_append": ([ctypes.POINTER(Layout), _P, _P, _P, _P, _P, _I32, _P, _I32, _P, _I32,
+                         _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P], _I32),
+    "kv_nvfp4_plan_workspace_bytes": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32,
+                                       ctypes.POINTER(ctypes.c_size_t)], _I32),
+    "kv_nvfp4_plan": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _P, ctypes.c_size_t,
+                       ctypes.POINTER(PlanInfo), _P], _I32),
+    "kv_nvfp4_decode_attn": ([ctypes.POINTER(Layout), ctypes.POINTER(PlanInfo), _P, _P, _P, _I32,
+                              ctypes.c_float, _P, _P, _P, _P, _I32, _P, _I32, _P, _P, _P], _I32),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded CUDA library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise KVNVFP4Error(
+                f"CUDA library {_LIB_PATH} is missing: run "
+                "`python -c 'import __graft_entry__ as g; g.build()'` (nvcc, sm_103a) first")
+        L = ctypes.CDLL(_LIB_PATH)
+        for name, (args, res) in _SIG.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _check(status: int, what: str):
+    if status != KV_NVFP4_OK:
+        msg = lib().kv_nvfp4_status_string(status).decode()
+        raise KVNVFP4Error(f"{what}: {msg} ({status})")
+
+
+def _ptr(x) -> int | None:
+    """Device/host address of a tensor-like (torch tensor, numpy array) or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x)}")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_layout(num_q_heads=24, num_kv_heads=4, head_dim=128, page_size=64, rot_dim=32) -> Layout:
+    L = Layout(num_q_heads, num_kv_heads, head_dim, page_size, rot_dim)
+    _check(lib().kv_nvfp4_layout_check(ctypes.byref(L)), "kv_nvfp4_layout_check")
+    return L
+
+
+# ---- the C ABI, name for name -----------------------------------------------------------------
+
+def kv_nvfp4_version() -> int:
+    return int(lib().kv_nvfp4_version())
+
+
+def kv_nvfp4_page_bytes(layout: Layout) -> int:
+    return int(lib().kv_nvfp4_page_bytes(ctypes.byref(layout)))
+
+
+def kv_nvfp4_pool_plane_bytes(layout: Layout, num_pages: int):
+    c, s = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().kv_nvfp4_pool_plane_bytes(ctypes.byref(layout), num_pages, ctypes.byref(c),
+                                           ctypes.byref(s)), "kv_nvfp4_pool_plane_bytes")
+    return c.value, s.value
+
+
+def kv_nvfp4_rope_table_bytes(max_pos: int, rot_dim: int) -> int:
+    return int(lib().kv_nvfp4_rope_table_bytes(max_pos, rot_dim))
+
+
+def kv_nvfp4_rope_table_fill_host(h_table, max_pos, rot_dim, theta, pos_scale):
+    _check(lib().kv_nvfp4_rope_table_fill_host(_ptr(h_table), max_pos, rot_dim, theta, pos_scale),
+           "kv_nvfp4_rope_table_fill_host")
+
+
+def kv_nvfp4_rope_table_init(d_table, max_pos, rot_dim, theta, pos_scale, stream=None):
+    _check(lib().kv_nvfp4_rope_table_init(_ptr(d_table), max_pos, rot_dim, theta, pos_scale,
+                                          _stream(stream)), "kv_nvfp4_rope_table_init")
+
+
+def kv_nvfp4_append(layout, q, k, v, seq_ids, positions, T, rope_table, rope_max_pos,
+                    block_table, num_seqs, max_pages, num_pages, k_codes, k_scales, v_codes,
+                    v_scales, q_codes=None, q_scales=None, status=None, stream=None):
+    _check(lib().kv_nvfp4_append(
+        ctypes.byref(layout), _ptr(q), _ptr(k), _ptr(v), _ptr(seq_ids), _ptr(positions), T,
+        _ptr(rope_table), rope_max_pos, _ptr(block_table), num_seqs, max_pages, num_pages,
+        _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), _ptr(q_codes),
+        _ptr(q_scales), _ptr(status), _stream(stream)), "kv_nvfp4_append")
+
+
+def kv_nvfp4_plan_workspace_bytes(layout, seq_lens, q_len, chunk_tokens) -> int:
+    import numpy as np
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    n = ctypes.c_size_t()
+    _check(lib().kv_nvfp4_plan_workspace_bytes(ctypes.byref(layout), sl.ctypes.data, len(sl),
+                                               q_len, chunk_tokens, ctypes.byref(n)),
+           "kv_nvfp4_plan_workspace_bytes")
+    return n.value
+
+
+def kv_nvfp4_plan(layout, seq_lens, q_len, chunk_tokens, workspace, ws_bytes,
+                  stream=None) -> PlanInfo:
+    import numpy as np
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    info = PlanInfo()
+    _check(lib().kv_nvfp4_plan(ctypes.byref(layout), sl.ctypes.data, len(sl), q_len,
+                               chunk_tokens, _ptr(workspace), ws_bytes, ctypes.byref(info),
+                               _stream(stream)), "kv_nvfp4_plan")
+    return info
+
+
+def kv_nvfp4_decode_attn(layout, plan: PlanInfo, workspace, q_codes, q_scales, causal, sm_scale,
+                         k_codes, k_scales, v_codes, v_scales, num_pages, block_table, max_pages,
+                         out, status=None, stream=None):
+    _check(lib().kv_nvfp4_decode_attn(
+        ctypes.byref(layout), ctypes.byref(plan), _ptr(workspace), _ptr(q_codes), _ptr(q_scales),
+        int(causal), float(sm_scale), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes),
+        _ptr(v_scales), num_pages, _ptr(block_table), max_pages, _ptr(out), _ptr(status),
+        _stream(stream)), "kv_nvfp4_decode_attn")
+
+
+from .cache import PagedNVFP4Cache  # noqa: E402  (device buffers for one layer, allocated by torch)

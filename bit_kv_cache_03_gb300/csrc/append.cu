@@ -1,0 +1,234 @@
+// Fused quantize-append: RoPE -> normalised Walsh-Hadamard rotation -> NVFP4 for Q and K rows,
+// NVFP4 only for V rows, stored into the paged pool (K, V) or the Q buffer.
+//
+// Source: prismix.dev/news/833001997676, section "NVFP4 KV cache (from scratch)" (Hadamard
+// rotation of K and Q before quantisation, V unrotated, E2M1 codes with one E4M3 scale per 16
+// elements, row-major scales, current K/V quantised as they are generated) and section "YaRN
+// context extension" (theta 1e7, 25 % rotary dims, linear position scaling).
+//
+// Mapping: one warp per 128-element row, lane l holds elements 4l..4l+3 (one 8-byte load).
+//   RoPE pairs (i, i + rot_dim/2) sit in lanes l and l + rot_dim/8: one shuffle.
+//   Hadamard: stages h = 1, 2 inside the lane, h = 4..64 as xor-shuffles over lane bits 0..4.
+//   A 16-element scale block is a group of four lanes: two xor-shuffles give its amax.
+// Every fp32 step that feeds a code is rounded exactly as the definition states (explicit _rn
+// intrinsics, no contraction), so codes and scales are bit-identical to a plain CPU evaluation.
+// Each warp handles kRowsPerWarp rows and issues all of their loads before computing, to keep
+// enough bytes in flight for an HBM-bound kernel.
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "nvfp4_device.cuh"
+
+namespace kvnvfp4 {
+
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+constexpr int kRowsPerWarp = 4;
+
+struct AppendParams {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  const int32_t* seq_ids;
+  const int32_t* positions;
+  int64_t T;
+  const float* rope;
+  int32_t rope_max_pos;
+  int32_t rot_dim;
+  const int32_t* block_table;
+  int32_t num_seqs;
+  int32_t max_pages;
+  int32_t num_pages;
+  uint8_t* k_codes;
+  uint8_t* k_scales;
+  uint8_t* v_codes;
+  uint8_t* v_scales;
+  uint8_t* q_codes;
+  uint8_t* q_scales;
+  int32_t Hq;   // 0 when q is absent
+  int32_t Hkv;
+  int32_t* status;
+};
+
+struct RowTarget {
+  const uint16_t* src;  // bf16 row
+  uint8_t* codes;       // 64-byte destination, or nullptr to skip the row
+  uint8_t* scales;      // 8-byte destination
+  int32_t pos;          // position, for RoPE
+  bool rotate;
+};
+
+__device__ __forceinline__ RowTarget locate_row(const AppendParams& p, int64_t row, int lane) {
+  RowTarget r{nullptr, nullptr, nullptr, 0, false};
+  const int32_t per_tok = p.Hq + 2 * p.Hkv;
+  const int64_t t = row / per_tok;
+  const int32_t w = (int32_t)(row - t * per_tok);
+  const int32_t seq = p.seq_ids[t];
+  const int32_t pos = p.positions[t];
+  bool bad = false;
+  if (seq < 0 || seq >= p.num_seqs) {
+    if (lane == 0) flag_status(p.status, KV_NVFP4_DEV_BAD_SEQ);
+    bad = true;
+  }
+  if (pos < 0 || pos >= p.max_pages * kPage) {
+    if (lane == 0) flag_status(p.status, KV_NVFP4_DEV_BAD_POS);
+    bad = true;
+  }
+  if (bad) return r;
+  r.pos = pos;
+  if (w < p.Hq) {  // Q row
+    r.src = p.q + (t * p.Hq + w) * kHeadDim;
+    r.codes = p.q_codes + (t * p.Hq + w) * kCodeBytes;
+    r.scales = p.q_scales + (t * p.Hq + w) * kScaleBytes;
+    r.rotate = true;
+  } else {
+    const int32_t kv = w - p.Hq;
+    const bool is_k = kv < p.Hkv;
+    const int32_t h = is_k ? kv : kv - p.Hkv;
+    const int32_t page = p.block_table[(int64_t)seq * p.max_pages + pos / kPage];
+    if (page < 0 || page >= p.num_pages) {
+      if (lane == 0) flag_status(p.status, KV_NVFP4_DEV_BAD_PAGE);
+      return r;
+    }
+    const int64_t slot = ((int64_t)page * p.Hkv + h) * kPage + pos % kPage;
+    r.src = (is_k ? p.k : p.v) + (t * p.Hkv + h) * kHeadDim;
+    r.codes = (is_k ? p.k_codes : p.v_codes) + slot * kCodeBytes;
+    r.scales = (is_k ? p.k_scales : p.v_scales) + slot * kScaleBytes;
+    r.rotate = is_k;
+  }
+  if (r.rotate && p.rot_dim > 0 && pos >= p.rope_max_pos) {
+    if (lane == 0) flag_status(p.status, KV_NVFP4_DEV_BAD_ROPE);
+    r.codes = nullptr;
+  }
+  return r;
+}
+
+__device__ __forceinline__ uint2 ldg_nc_u2(const void* ptr) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(ptr));
+  return v;
+}
+
+__device__ __forceinline__ void quantize_store_row(float (&x)[4], const RowTarget& r,
+                                                   const AppendParams& p, int lane) {
+  if (r.rotate) {
+    // --- RoPE on the first rot_dim dims (pairs i, i + rot_dim/2) ---
+    const int rot = p.rot_dim;
+    if (rot > 0) {
+      const int half_lanes = rot >> 3;           // lanes holding dims [0, rot/2)
+      const bool lower = lane < half_lanes;
+      const int src = lower ? lane + half_lanes : lane - half_lanes;
+      float y[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) y[e] = __shfl_sync(0xffffffffu, x[e], src & 31);
+      if (lane < 2 * half_lanes) {
+        const int i0 = 4 * (lower ? lane : lane - half_lanes);
+        const float* row = p.rope + (int64_t)r.pos * rot;
+        const float4 c = *reinterpret_cast<const float4*>(row + i0);
+        const float4 s = *reinterpret_cast<const float4*>(row + (rot >> 1) + i0);
+        const float cc[4] = {c.x, c.y, c.z, c.w};
+        const float ss[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          // lower lane holds a = x_i, partner b = x_{i+half}: a c - b s
+          // upper lane holds b = x_{i+half}, partner a = x_i:  b c + a s
+          x[e] = lower ? __fsub_rn(__fmul_rn(x[e], cc[e]), __fmul_rn(y[e], ss[e]))
+                       : __fadd_rn(__fmul_rn(x[e], cc[e]), __fmul_rn(y[e], ss[e]));
+        }
+      }
+    }
+    // --- Walsh-Hadamard, stages h = 1, 2, 4, ..., 64 ---
+    {
+      float a = x[0], b = x[1];
+      x[0] = __fadd_rn(a, b); x[1] = __fsub_rn(a, b);
+      a = x[2]; b = x[3];
+      x[2] = __fadd_rn(a, b); x[3] = __fsub_rn(a, b);
+      a = x[0]; b = x[2];
+      x[0] = __fadd_rn(a, b); x[2] = __fsub_rn(a, b);
+      a = x[1]; b = x[3];
+      x[1] = __fadd_rn(a, b); x[3] = __fsub_rn(a, b);
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const bool upper = (lane & m) != 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
+        x[e] = upper ? __fsub_rn(o, x[e]) : __fadd_rn(x[e], o);
+      }
+    }
+    const float kNorm = __uint_as_float(0x3DB504F3u);  // rn(2^-3.5) = rn(1/sqrt(128))
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = __fmul_rn(x[e], kNorm);
+  }
+
+  // --- NVFP4: block of 16 = 4 lanes ---
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const uint32_t sc = e4m3_encode_rne_sat(__fdiv_rn(amax, 6.0f));
+  const float sd = e4m3_decode_pos(sc);
+  uint32_t packed = 0;
+  if (sd != 0.0f) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) packed |= e2m1_encode_rne_sat(__fdiv_rn(x[e], sd)) << (4 * e);
+  }
+  if (r.codes != nullptr) {
+    *reinterpret_cast<uint16_t*>(r.codes + 2 * lane) = (uint16_t)packed;
+    if ((lane & 3) == 0) r.scales[lane >> 2] = (uint8_t)sc;
+  }
+}
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const AppendParams p) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t rows = p.T * (int64_t)(p.Hq + 2 * p.Hkv);
+  const int64_t row0 = ((int64_t)blockIdx.x * kWarpsPerBlock + warp) * kRowsPerWarp;
+  RowTarget tg[kRowsPerWarp];
+  uint2 raw[kRowsPerWarp];
+#pragma unroll
+  for (int j = 0; j < kRowsPerWarp; ++j) {
+    tg[j].codes = nullptr;
+    raw[j] = make_uint2(0u, 0u);
+    if (row0 + j < rows) {
+      tg[j] = locate_row(p, row0 + j, lane);
+      if (tg[j].codes != nullptr) raw[j] = ldg_nc_u2(tg[j].src + 4 * lane);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kRowsPerWarp; ++j) {
+    if (tg[j].codes == nullptr) continue;  // warp-uniform: every lane saw the same row
+    float x[4];
+    x[0] = __uint_as_float(raw[j].x << 16);
+    x[1] = __uint_as_float(raw[j].x & 0xFFFF0000u);
+    x[2] = __uint_as_float(raw[j].y << 16);
+    x[3] = __uint_as_float(raw[j].y & 0xFFFF0000u);
+    quantize_store_row(x, tg[j], p, lane);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          const int32_t* seq_ids, const int32_t* positions, int64_t T,
+                          const float* rope, int32_t rope_max_pos, int32_t rot_dim,
+                          const int32_t* block_table, int32_t num_seqs, int32_t max_pages,
+                          int32_t num_pages, uint8_t* k_codes, uint8_t* k_scales,
+                          uint8_t* v_codes, uint8_t* v_scales, uint8_t* q_codes,
+                          uint8_t* q_scales, int32_t Hq, int32_t Hkv, int32_t* status,
+                          cudaStream_t stream) {
+  AppendParams p{q,         k,        v,       seq_ids, positions, T,       rope,
+                 rope_max_pos, rot_dim, block_table, num_seqs, max_pages, num_pages, k_codes,
+                 k_scales,  v_codes,  v_scales, q_codes, q_scales,  q ? Hq : 0, Hkv, status};
+  const int64_t rows = T * (int64_t)(p.Hq + 2 * Hkv);
+  const int64_t per_block = (int64_t)kWarpsPerBlock * kRowsPerWarp;
+  const int64_t blocks = (rows + per_block - 1) / per_block;
+  if (blocks == 0) return cudaSuccess;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  append_kernel<<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvnvfp4

@@ -1,0 +1,226 @@
+// Device helpers shared by the NVFP4 kernels (sm_103a): format encoders/decoders written from
+// the E2M1/E4M3 definitions, and thin inline-PTX wrappers (mbarrier, bulk async copy, warp MMA,
+// conversions).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kv_nvfp4.h"
+
+namespace kvnvfp4 {
+
+constexpr int kHeadDim = 128;
+constexpr int kPage = 64;
+constexpr int kCodeBytes = 64;   // 128 x 4 bit
+constexpr int kScaleBytes = 8;   // 128 / 16 E4M3 scales
+
+// ---------------------------------------------------------------------------------------------
+// Formats. E4M3 ("fn"): bias 7, subnormal step 2^-9, max finite 448 (0x7E). E2M1: bias 1, values
+// {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
+// ---------------------------------------------------------------------------------------------
+
+// Round a finite t >= 0 to the nearest E4M3 value, ties to even, saturating at 448.
+__device__ __forceinline__ uint32_t e4m3_encode_rne_sat(float t) {
+  if (!(t > 0.0f)) return 0u;
+  if (t >= 448.0f) return 0x7Eu;
+  if (t < 0.015625f) {                          // below 2^-6: subnormal grid m * 2^-9
+    return (uint32_t)__float2int_rn(__fmul_rn(t, 512.0f));  // exact scaling, RNE; 8 -> 2^-6
+  }
+  const uint32_t b = __float_as_uint(t);
+  const int e = (int)(b >> 23) - 127;           // -6 .. 8
+  uint32_t r = (b >> 20) & 7u;                  // top 3 mantissa bits
+  const uint32_t rem = b & 0xFFFFFu;
+  if (rem > 0x80000u || (rem == 0x80000u && (r & 1u))) ++r;  // a carry into r = 8 bumps e
+  const uint32_t code = (uint32_t)((e + 7) << 3) + r;
+  return code > 0x7Eu ? 0x7Eu : code;
+}
+
+// Exact value of a non-NaN E4M3 code with the sign bit clear.
+__device__ __forceinline__ float e4m3_decode_pos(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  if (e == 0u) return __fmul_rn((float)m, 0.001953125f);  // m * 2^-9, exact
+  return __uint_as_float(((e + 120u) << 23) | (m << 20));  // 2^(e-7) * (1 + m/8)
+}
+
+// E2M1 code of x (round to nearest, ties to the even code, saturate at 6, sign kept). The
+// midpoints of the grid are 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5; at a midpoint the even code
+// wins, which makes the comparison strict where the lower neighbour is even and inclusive where
+// the upper neighbour is even.
+__device__ __forceinline__ uint32_t e2m1_encode_rne_sat(float x) {
+  const float a = fabsf(x);
+  uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
+               (a >= 3.5f) + (a > 5.0f);
+  return c | ((__float_as_uint(x) >> 28) & 8u);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Conversions via the hardware converters (PTX cvt, sm_100+ family).
+// ---------------------------------------------------------------------------------------------
+
+// Four bytes of packed E2M1 pairs -> four f16x2 (low nibble -> low half).
+__device__ __forceinline__ void cvt_e2m1x8_f16(uint32_t w, uint32_t& r0, uint32_t& r1,
+                                               uint32_t& r2, uint32_t& r3) {
+  asm("{\n.reg .b8 b0, b1, b2, b3;\n"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+      : "r"(w));
+}
+
+// Two E4M3 bytes (low byte -> low half) -> f16x2.
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16(uint32_t two_bytes) {
+  uint32_t r;
+  const uint16_t h = (uint16_t)two_bytes;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+  return r;
+}
+
+// (lo, hi) fp32 -> f16x2, round to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) {
+  float f;
+  asm("{\n.reg .b16 l, h;\nmov.b32 {l, h}, %1;\ncvt.f32.f16 %0, l;\n}" : "=f"(f) : "r"(h2));
+  return f;
+}
+__device__ __forceinline__ float f16_hi_to_f32(uint32_t h2) {
+  float f;
+  asm("{\n.reg .b16 l, h;\nmov.b32 {l, h}, %1;\ncvt.f32.f16 %0, h;\n}" : "=f"(f) : "r"(h2));
+  return f;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Broadcast the low / high f16 of a pair to both halves.
+__device__ __forceinline__ uint32_t dup_lo(uint32_t h2) { return __byte_perm(h2, 0, 0x1010); }
+__device__ __forceinline__ uint32_t dup_hi(uint32_t h2) { return __byte_perm(h2, 0, 0x3232); }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Warp-level MMA m16n8k16, f16 inputs, f32 accumulate, and the 8x8 b16 transpose.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Shared-memory access and mbarrier / bulk-copy wrappers.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds8(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}" ::"r"(
+                   bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase with the given parity to complete, for at most ~2 s of wall time. Returns
+// false on timeout (the caller records KV_NVFP4_DEV_TIMEOUT and carries on).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > 2000000000ull) return false;
+  }
+}
+
+// Bulk (non-tensor) async copy global -> shared, completing on an mbarrier. Both addresses
+// 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void flag_status(int32_t* status, int32_t bits) {
+  if (status != nullptr) atomicOr(status, bits);
+}
+
+}  // namespace kvnvfp4

@@ -1,0 +1,197 @@
+/* NVFP4 KV cache for GB300 (sm_103a): fused quantize-append and paged GQA attention.
+ *
+ * C ABI. Every pointer is a plain host or device pointer as stated per argument; no framework
+ * types cross this boundary. CUDA streams are passed as `void *` holding a cudaStream_t
+ * (NULL = the legacy default stream). All device work is asynchronous on that stream.
+ *
+ * Method sources (web pages, cited by address and section):
+ *   [NVFP4] prismix.dev/news/833001997676, section "NVFP4 KV cache (from scratch)":
+ *           4-bit E2M1 codes with one E4M3 scale per 16 elements for K and V, scales in natural
+ *           row-major order, a Hadamard rotation of K (and Q) before quantisation, V unrotated,
+ *           Q and K both quantised for the Q.K^T product, V dequantised for P.V, the current
+ *           token's K/V quantised in the decode path with no separate pass, and 144 bytes per
+ *           token per KV head.
+ *   [YaRN]  same page, section "YaRN context extension": theta = 1e7, 25 % of the head dims
+ *           rotary, linear position scaling.
+ *
+ * Data layout (all byte planes, caller-allocated, 16-byte aligned):
+ *   Pool planes, one page = 64 token slots:
+ *     k_codes  [num_pages][num_kv_heads][64][64]  E2M1 codes; element 2j in the low nibble of
+ *                                                 byte j, element 2j+1 in the high nibble
+ *     k_scales [num_pages][num_kv_heads][64][8]   E4M3 scale b covers elements 16b..16b+15
+ *     v_codes, v_scales: same shapes.
+ *   => 64 + 8 bytes for K and again for V: 144 bytes per token per KV head [NVFP4].
+ *   Token `pos` of sequence `s` lives in page block_table[s * max_pages + pos / 64], slot
+ *   pos % 64. K rows are stored after RoPE and the normalised Hadamard rotation; V rows raw.
+ *   Quantised Q: q_codes [tokens][num_q_heads][64], q_scales [tokens][num_q_heads][8], after
+ *   RoPE and rotation, in the same encoding.
+ *
+ * Ownership: the caller allocates and frees every device buffer. No entry point allocates
+ * device memory. A plan workspace belongs to the stream it was planned on: reuse or overwrite
+ * it only after the attention call that reads it has completed on that stream, and do not run
+ * two attention calls with the same workspace concurrently.
+ *
+ * Errors: every entry point returns a kv_nvfp4_status. Host-checkable faults return
+ * KV_NVFP4_EINVAL before any launch. Launch failures return KV_NVFP4_ECUDA. Data-dependent
+ * faults found on the device (a page id outside the pool, a position beyond the page table or
+ * the RoPE table, a sequence id out of range) set bits (KV_NVFP4_DEV_*) in the caller's int32
+ * `d_status` word with an atomic OR, and the offending row or page is skipped; pass NULL to
+ * ignore them. The library never traps and never spins without a bound.
+ */
+#ifndef KV_NVFP4_H
+#define KV_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t kv_nvfp4_status;
+#define KV_NVFP4_OK 0
+#define KV_NVFP4_EINVAL (-1)
+#define KV_NVFP4_ECUDA (-2)
+#define KV_NVFP4_ENOSPACE (-3)
+
+/* Bits written to *d_status by device code. */
+#define KV_NVFP4_DEV_BAD_PAGE 0x1     /* block_table entry outside [0, num_pages) */
+#define KV_NVFP4_DEV_BAD_POS 0x2      /* position < 0 or >= max_pages * 64 */
+#define KV_NVFP4_DEV_BAD_SEQ 0x4      /* sequence id outside [0, num_seqs) */
+#define KV_NVFP4_DEV_BAD_ROPE 0x8     /* position >= rope_max_pos for a rotated row */
+#define KV_NVFP4_DEV_TIMEOUT 0x10     /* an internal barrier wait hit its time limit */
+
+/* Model geometry of one attention layer. This build supports head_dim = 128 and
+ * page_size = 64; num_q_heads must be a multiple of num_kv_heads with a group of at most 8;
+ * rot_dim is even, a multiple of 8 and at most 128 (0 disables RoPE). */
+typedef struct kv_nvfp4_layout {
+  int32_t num_q_heads;  /* 24 in the pages' model */
+  int32_t num_kv_heads; /* 4 */
+  int32_t head_dim;     /* 128 */
+  int32_t page_size;    /* 64 tokens */
+  int32_t rot_dim;      /* 32 = 25 % of 128 [YaRN] */
+} kv_nvfp4_layout;
+
+/* Filled by kv_nvfp4_plan; passed unchanged to kv_nvfp4_decode_attn. */
+typedef struct kv_nvfp4_plan_info {
+  int32_t num_seqs;
+  int32_t q_len;
+  int32_t chunk_pages;     /* split-K chunk, in pages */
+  int32_t num_chunks;      /* chunks summed over sequences */
+  int32_t num_row_groups;  /* ceil(group * q_len / 8): query-row tiles per (sequence, kv head) */
+  int32_t num_kv_heads;
+  int32_t num_partials;    /* partial-result slots used by split sequences */
+  int32_t max_chunks;      /* largest chunk count of one sequence */
+  int32_t max_seq_len;     /* longest sequence; must fit max_pages * 64 at attention time */
+  int32_t reserved;
+  int64_t total_kv_tokens; /* sum of seq_lens */
+  uint64_t off_seqinfo, off_items, off_counters, off_partials; /* byte offsets in workspace */
+  uint64_t workspace_bytes;
+} kv_nvfp4_plan_info;
+
+/* Human-readable name of a status code (static string). */
+const char *kv_nvfp4_status_string(kv_nvfp4_status status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int32_t kv_nvfp4_version(void);
+
+/* Validates a layout; KV_NVFP4_OK or KV_NVFP4_EINVAL. */
+kv_nvfp4_status kv_nvfp4_layout_check(const kv_nvfp4_layout *layout);
+
+/* Bytes of one pool page over all KV heads, K and V, codes and scales:
+ * 64 * 144 * num_kv_heads (36,864 for 4 KV heads) [NVFP4]. 0 on an invalid layout. */
+size_t kv_nvfp4_page_bytes(const kv_nvfp4_layout *layout);
+
+/* Sizes of one code plane and one scale plane for a pool of num_pages pages. */
+kv_nvfp4_status kv_nvfp4_pool_plane_bytes(const kv_nvfp4_layout *layout, int32_t num_pages,
+                                          size_t *code_plane_bytes, size_t *scale_plane_bytes);
+
+/* ---- RoPE table [YaRN] ----------------------------------------------------------------------
+ * fp32 table [max_pos][rot_dim]: entries 0..rot_dim/2-1 are cos, rot_dim/2..rot_dim-1 are sin,
+ * of angle (pos / pos_scale) * theta^(-2i/rot_dim), evaluated in double on the host and rounded
+ * once to fp32. Dimension i < rot_dim/2 rotates with dimension i + rot_dim/2. pos_scale is the
+ * linear position-scaling factor (1 = none; 600000/262144 stretches a 262k model to 600k). */
+size_t kv_nvfp4_rope_table_bytes(int32_t max_pos, int32_t rot_dim);
+
+/* Fills a HOST buffer of kv_nvfp4_rope_table_bytes bytes. No CUDA call. */
+kv_nvfp4_status kv_nvfp4_rope_table_fill_host(float *h_table, int32_t max_pos, int32_t rot_dim,
+                                              double theta, double pos_scale);
+
+/* Computes the table on the host and copies it into DEVICE memory d_table on `stream`. The
+ * host staging copy is consumed before return. */
+kv_nvfp4_status kv_nvfp4_rope_table_init(float *d_table, int32_t max_pos, int32_t rot_dim,
+                                         double theta, double pos_scale, void *stream);
+
+/* ---- Fused quantize-append [NVFP4: Hadamard rotation, quantisation, fused append] ---------
+ * For each of T tokens: every Q head (if q != NULL) and every K head gets RoPE on its first
+ * rot_dim dims, the normalised 128-point Walsh-Hadamard rotation (Sylvester order, stages
+ * h = 1..64, then a multiply by fp32 rn(2^-3.5)), and NVFP4 quantisation; every V head gets the
+ * quantisation only. Quantisation per 16 elements: scale = E4M3 round-to-nearest-even of
+ * amax/6, saturating at 448; code = E2M1 round-to-nearest-even of x / scale, saturating at 6,
+ * sign kept; a block whose scale is 0 stores zero codes. K/V rows go into their page slots,
+ * Q rows into q_codes/q_scales at the token's index.
+ *   q, k, v:        DEVICE bf16 [T][num_q_heads][128], [T][num_kv_heads][128] (q may be NULL,
+ *                   then q_codes/q_scales are ignored)
+ *   d_seq_ids:      DEVICE int32 [T], sequence of each token, in [0, num_seqs)
+ *   d_positions:    DEVICE int32 [T], absolute position of each token in its sequence
+ *   d_rope_table:   DEVICE fp32 table from kv_nvfp4_rope_table_init, rope_max_pos rows
+ *   d_block_table:  DEVICE int32 [num_seqs][max_pages]
+ *   k_/v_codes/scales: DEVICE pool planes of num_pages pages (see layout above)
+ *   q_codes/q_scales: DEVICE [T][num_q_heads][64] / [T][num_q_heads][8]
+ *   d_status:       DEVICE int32 or NULL
+ * One kernel launch. T = 0 is a no-op. */
+kv_nvfp4_status kv_nvfp4_append(const kv_nvfp4_layout *layout, const void *q, const void *k,
+                                const void *v, const int32_t *d_seq_ids,
+                                const int32_t *d_positions, int32_t T, const float *d_rope_table,
+                                int32_t rope_max_pos, const int32_t *d_block_table,
+                                int32_t num_seqs, int32_t max_pages, int32_t num_pages,
+                                uint8_t *k_codes, uint8_t *k_scales, uint8_t *v_codes,
+                                uint8_t *v_scales, uint8_t *q_codes, uint8_t *q_scales,
+                                int32_t *d_status, void *stream);
+
+/* ---- Page-table / split-K setup ------------------------------------------------------------
+ * Sizes and builds the work list of one attention call from HOST sequence lengths (after the
+ * append, i.e. including the q_len new tokens). Sequences are cut into chunks of chunk_tokens
+ * keys (a positive multiple of 64; 1024 suits decode, a chunk as long as the sequence turns the
+ * split off); each (chunk, kv head, tile of 8 query rows) is one work item, and the chunks of
+ * one sequence are merged by a log-sum-exp combine. The workspace holds one partial result of
+ * 4160 bytes per work item of every sequence that has more than one chunk. */
+kv_nvfp4_status kv_nvfp4_plan_workspace_bytes(const kv_nvfp4_layout *layout,
+                                              const int32_t *h_seq_lens, int32_t num_seqs,
+                                              int32_t q_len, int32_t chunk_tokens,
+                                              size_t *bytes);
+
+/* Writes the work list into DEVICE memory d_workspace (ws_bytes at least the size above) on
+ * `stream`, zeroes the merge counters, and fills *info (HOST). Every seq_len must be >= q_len
+ * and >= 1. */
+kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout *layout, const int32_t *h_seq_lens,
+                              int32_t num_seqs, int32_t q_len, int32_t chunk_tokens,
+                              void *d_workspace, size_t ws_bytes, kv_nvfp4_plan_info *info,
+                              void *stream);
+
+/* ---- Paged GQA decode / speculative-verify attention [NVFP4: NVFP4 Q.K^T, V dequantised]
+ * For every sequence s and each of its q_len query tokens i (position seq_len - q_len + i) and
+ * every query head h (kv head h / (num_q_heads / num_kv_heads)):
+ *   out = sum_t softmax_t(sm_scale * qhat . khat_t) * vhat_t
+ * over keys t < seq_len, restricted to t <= seq_len - q_len + i when causal != 0, where qhat,
+ * khat, vhat are the dequantised NVFP4 rows (code value times block scale). Scores and the
+ * softmax run in fp32 with split-K over the plan's chunks.
+ *   plan, d_workspace: from kv_nvfp4_plan (same stream)
+ *   q_codes/q_scales: DEVICE [num_seqs * q_len][num_q_heads][64 | 8], sequence-major
+ *   sm_scale:       softmax scale; <= 0 selects 1/sqrt(head_dim)
+ *   out:            DEVICE fp32 [num_seqs * q_len][num_q_heads][128]
+ * One kernel launch. */
+kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout *layout,
+                                     const kv_nvfp4_plan_info *plan, void *d_workspace,
+                                     const uint8_t *q_codes, const uint8_t *q_scales,
+                                     int32_t causal, float sm_scale, const uint8_t *k_codes,
+                                     const uint8_t *k_scales, const uint8_t *v_codes,
+                                     const uint8_t *v_scales, int32_t num_pages,
+                                     const int32_t *d_block_table, int32_t max_pages, float *out,
+                                     int32_t *d_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KV_NVFP4_H */

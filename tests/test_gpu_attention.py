@@ -1,0 +1,69 @@
+"""Attention parity of the CUDA path against the oracle on small workloads (GPU)."""
+import numpy as np
+import pytest
+
+import synth
+from kvrun import MAX_ABS_TOL, REL_L2_TOL, GpuRun, OracleRun, attention_errors
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _check(w, chunk=None, steps=1):
+    g = GpuRun(w)
+    outs = []
+    for _ in range(steps):
+        g.step(chunk_tokens=chunk)
+        torch.cuda.synchronize()
+        outs.append(g.output())
+    assert g.status() == 0
+    ref = OracleRun(w).attention().reshape(outs[0].shape)
+    for out in outs:
+        max_abs, rel = attention_errors(out, ref)
+        assert max_abs <= MAX_ABS_TOL and rel <= REL_L2_TOL, (max_abs, rel)
+    for out in outs[1:]:
+        assert np.array_equal(out, outs[0])  # repeat calls reuse the workspace counters
+    return outs[0], ref
+
+
+@pytest.mark.parametrize("lens,q_len,causal,chunk", [
+    ([0, 5, 63, 64, 65, 200, 1000], 1, True, 1024),
+    ([0, 5, 63, 64, 65, 200, 1000], 1, True, 128),       # split-K with the ticket merge
+    ([10, 700, 1500], 3, True, 192),
+    ([10, 700, 1500], 3, False, 192),
+    ([2000, 37], 8, True, 256),                          # verify-shaped: 48 rows, 6 row tiles
+    ([5000], 1, True, 64),                               # one page per chunk, 79 chunks
+])
+def test_attention_small(lens, q_len, causal, chunk):
+    w = synth.Workload("small", lens, q_len=q_len, causal=causal, seed=len(lens) + q_len,
+                       chunk_tokens=chunk, pool_pages=sum((c + q_len + 63) // 64 for c in lens) + 5)
+    _check(w, chunk=chunk, steps=2)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (4, 4), (16, 2), (7, 7)])
+def test_attention_other_group_sizes(Hq, Hkv):
+    w = synth.Workload("groups", [300, 1200], q_len=2, seed=Hq * 10 + Hkv, q_heads=Hq,
+                       kv_heads=Hkv, chunk_tokens=256)
+    _check(w, chunk=256)
+
+
+def test_attention_position_scaling_and_full_rotation():
+    w = synth.Workload("scaled", [3000], q_len=4, seed=5, rot_dim=128,
+                       pos_scale=600000.0 / 262144.0, chunk_tokens=512)
+    _check(w, chunk=512)
+
+
+def test_attention_skips_bad_pages_and_flags_them():
+    import bit_kv_cache_03_gb300 as kv
+    w = synth.Workload("badpage", [500], q_len=1, seed=3, pool_pages=12)
+    g = GpuRun(w)
+    g.step()
+    torch.cuda.synchronize()
+    assert g.status() == 0
+    # corrupt one entry of the block table, re-run attention only
+    bt = g.cache.block_table
+    bt[0, 2] = 10 ** 6
+    g.cache.attend(g.q_codes, g.q_scales, g.out, causal=True, sm_scale=w.sm_scale)
+    torch.cuda.synchronize()
+    assert g.status() & kv.DEV_BAD_PAGE
+    assert np.all(np.isfinite(g.output()))
