@@ -55,11 +55,14 @@ def _append_crafted(Hq, Hkv, T, seed, rot_dim=32):
     import bit_kv_cache_03_gb300 as kv
     cache = kv.PagedNVFP4Cache(pages + 3, bt, T, Hq or 4, Hkv, rot_dim)
     dev = cache.device
-    to_dev = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    def to_dev(a, heads):
+        t = torch.from_numpy(a.reshape(T, heads, 128).view(np.int16))
+        return t.to(dev).view(torch.bfloat16)
     pos = np.arange(T, dtype=np.int32)
     qc, qs = cache.quantized_q_buffers(T)
-    cache.append(to_dev(rows_k), to_dev(rows_v), torch.zeros(T, dtype=torch.int32, device=dev),
-                 torch.from_numpy(pos).to(dev), q=to_dev(rows_q) if Hq else None,
+    cache.append(to_dev(rows_k, Hkv), to_dev(rows_v, Hkv),
+                 torch.zeros(T, dtype=torch.int32, device=dev),
+                 torch.from_numpy(pos).to(dev), q=to_dev(rows_q, Hq) if Hq else None,
                  q_codes=qc, q_scales=qs)
     torch.cuda.synchronize()
     assert int(cache.status.item()) == 0
