@@ -36,6 +36,7 @@ sys.path.insert(0, os.path.join(ROOT, "tests"))
 
 METRIC = "NVFP4 decode attn KV-tokens/s & HBM GB/s (% of peak); append tokens/s"
 UNIT = "KV-tokens/s"
+CHUNK = 64  # split-K granularity: one page, so the plan balances CTAs to the page
 WORKLOAD = "steady_decode: 4 seqs x 131072 cached + 1 new token, Hq 24 / Hkv 4, d 128, page 64, 40k-page pool"
 
 
@@ -242,9 +243,22 @@ def run_cuda(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     w = synth.steady_decode()
+    if args.seqs != 4:
+        w = synth.Workload(f"steady_decode_{args.seqs}x128k", [131072] * args.seqs, q_len=1,
+                           pool_pages=40000)
     g = GpuRun(w, device=dev)
     stream = torch.cuda.current_stream(dev)
-    g.cache.plan(w.seq_lens, w.q_len, w.chunk_tokens)
+    g.cache.plan(w.seq_lens, w.q_len, w.causal, CHUNK)
+
+    if args.profile:
+        # short run for the profiler: warm-up and the timed steps only
+        for _ in range(args.warmup + args.steps):
+            g.cache.append(g.k, g.v, g.sid, g.pos, q=g.q, q_codes=g.q_codes, q_scales=g.q_scales)
+            g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
+        torch.cuda.synchronize(dev)
+        assert g.status() == 0
+        print(json.dumps({"profile_run": True, "seqs": w.num_seqs, "steps": args.steps}))
+        return
 
     # ---- bulk append throughput (tokens with Q, K, V: the prefill-chunk shape) ----
     Tb = 16384
@@ -272,7 +286,8 @@ def run_cuda(args, world, rank, local):
 
     # ---- timed decode steps (device-resident inputs) ----
     for _ in range(args.warmup):
-        g.step(plan=False)
+        g.cache.append(g.k, g.v, g.sid, g.pos, q=g.q, q_codes=g.q_codes, q_scales=g.q_scales)
+        g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
     torch.cuda.synchronize(dev)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -287,7 +302,7 @@ def run_cuda(args, world, rank, local):
     for i in range(args.steps):
         g.cache.append(g.k, g.v, g.sid, g.pos, q=g.q, q_codes=g.q_codes, q_scales=g.q_scales)
         starts[i].record(stream)
-        g.cache.attend(g.q_codes, g.q_scales, g.out, causal=w.causal, sm_scale=w.sm_scale)
+        g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
         ends[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize(dev)
@@ -321,8 +336,8 @@ def run_cuda(args, world, rank, local):
         pos_d.copy_(pos_h, non_blocking=True)
         g.cache.append(k_d.view(torch.bfloat16), v_d.view(torch.bfloat16), sid_d, pos_d,
                        q=q_d.view(torch.bfloat16), q_codes=g.q_codes, q_scales=g.q_scales)
-        g.cache.plan(w.seq_lens, w.q_len, w.chunk_tokens)
-        g.cache.attend(g.q_codes, g.q_scales, g.out, causal=w.causal, sm_scale=w.sm_scale)
+        g.cache.plan(w.seq_lens, w.q_len, w.causal, CHUNK)
+        g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
         out_h.copy_(g.out, non_blocking=True)
 
     for _ in range(5):
@@ -362,7 +377,7 @@ def run_cuda(args, world, rank, local):
         "config": {"workload": WORKLOAD, "kv_tokens_per_step": kv_tokens,
                    "kv_bytes_per_step": kv_tokens * w.kv_heads * 144,
                    "l2": "inputs larger than L2 (302 MB of KV per step vs 129 MB L2), no flush",
-                   "chunk_tokens": w.chunk_tokens, "parallelism": "replicas" if world > 1 else "1 GPU"},
+                   "chunk_tokens": CHUNK, "parallelism": "replicas" if world > 1 else "1 GPU"},
         "hbm_gbs_attn": achieved,
         "hbm_frac_attn_of_measured": achieved / peak,
         "hbm_frac_attn_of_nominal_7900": achieved / 7900.0,
@@ -393,6 +408,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seqs", type=int, default=4, help="sequences of 131072 tokens (profiling)")
+    ap.add_argument("--profile", action="store_true",
+                    help="warm-up + steps only, no extra measurements (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

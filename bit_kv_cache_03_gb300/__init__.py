@@ -33,15 +33,12 @@ class Layout(ctypes.Structure):
 
 class PlanInfo(ctypes.Structure):
     """kv_nvfp4_plan_info"""
-    _fields_ = [("num_seqs", ctypes.c_int32), ("q_len", ctypes.c_int32),
-                ("chunk_pages", ctypes.c_int32), ("num_chunks", ctypes.c_int32),
-                ("num_row_groups", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
-                ("num_partials", ctypes.c_int32), ("max_chunks", ctypes.c_int32),
-                ("max_seq_len", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("total_kv_tokens", ctypes.c_int64),
-                ("off_seqinfo", ctypes.c_uint64), ("off_items", ctypes.c_uint64),
-                ("off_counters", ctypes.c_uint64), ("off_partials", ctypes.c_uint64),
-                ("workspace_bytes", ctypes.c_uint64)]
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_seqs", "q_len", "causal", "chunk_pages", "num_kv_heads", "num_row_groups",
+        "num_groups", "num_segments", "num_partials", "grid", "max_seq_len", "reserved")] + [
+        ("total_kv_tokens", ctypes.c_int64), ("total_pages", ctypes.c_int64)] + [
+        (n, ctypes.c_uint64) for n in ("off_groups", "off_segments", "off_cta", "off_counters",
+                                       "off_partials", "workspace_bytes")]
 
 
 class KVNVFP4Error(RuntimeError):
@@ -63,11 +60,13 @@ _SIG = {
     "kv_nvfp4_rope_table_init": ([_P, _I32, _I32, _F64, _F64, _P], _I32),
     "kv_nvfp4_append": ([ctypes.POINTER(Layout), _P, _P, _P, _P, _P, _I32, _P, _I32, _P, _I32,
                          _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P], _I32),
-    "kv_nvfp4_plan_workspace_bytes": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32,
+    "kv_nvfp4_plan_workspace_bytes": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32,
                                        ctypes.POINTER(ctypes.c_size_t)], _I32),
-    "kv_nvfp4_plan": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _P, ctypes.c_size_t,
+    "kv_nvfp4_plan": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32, _P, ctypes.c_size_t,
                        ctypes.POINTER(PlanInfo), _P], _I32),
-    "kv_nvfp4_decode_attn": ([ctypes.POINTER(Layout), ctypes.POINTER(PlanInfo), _P, _P, _P, _I32,
+    "kv_nvfp4_plan_host": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32, _I32, _P,
+                            ctypes.c_size_t, ctypes.POINTER(PlanInfo)], _I32),
+    "kv_nvfp4_decode_attn": ([ctypes.POINTER(Layout), ctypes.POINTER(PlanInfo), _P, _P, _P,
                               ctypes.c_float, _P, _P, _P, _P, _I32, _P, _I32, _P, _P, _P], _I32),
 }
 
@@ -170,35 +169,59 @@ def kv_nvfp4_append(layout, q, k, v, seq_ids, positions, T, rope_table, rope_max
         _ptr(q_scales), _ptr(status), _stream(stream)), "kv_nvfp4_append")
 
 
-def kv_nvfp4_plan_workspace_bytes(layout, seq_lens, q_len, chunk_tokens) -> int:
+def kv_nvfp4_plan_workspace_bytes(layout, seq_lens, q_len, causal, chunk_tokens) -> int:
     import numpy as np
     sl = np.ascontiguousarray(seq_lens, np.int32)
     n = ctypes.c_size_t()
     _check(lib().kv_nvfp4_plan_workspace_bytes(ctypes.byref(layout), sl.ctypes.data, len(sl),
-                                               q_len, chunk_tokens, ctypes.byref(n)),
+                                               q_len, int(causal), chunk_tokens, ctypes.byref(n)),
            "kv_nvfp4_plan_workspace_bytes")
     return n.value
 
 
-def kv_nvfp4_plan(layout, seq_lens, q_len, chunk_tokens, workspace, ws_bytes,
+def kv_nvfp4_plan(layout, seq_lens, q_len, causal, chunk_tokens, workspace, ws_bytes,
                   stream=None) -> PlanInfo:
     import numpy as np
     sl = np.ascontiguousarray(seq_lens, np.int32)
     info = PlanInfo()
-    _check(lib().kv_nvfp4_plan(ctypes.byref(layout), sl.ctypes.data, len(sl), q_len,
+    _check(lib().kv_nvfp4_plan(ctypes.byref(layout), sl.ctypes.data, len(sl), q_len, int(causal),
                                chunk_tokens, _ptr(workspace), ws_bytes, ctypes.byref(info),
                                _stream(stream)), "kv_nvfp4_plan")
     return info
 
 
-def kv_nvfp4_decode_attn(layout, plan: PlanInfo, workspace, q_codes, q_scales, causal, sm_scale,
+def kv_nvfp4_plan_host(layout, seq_lens, q_len, causal, chunk_tokens, num_ctas):
+    """Host image of the plan tables for `num_ctas` CTAs: (info, groups [n,8], segments [n,4],
+    cta ranges [num_ctas+1]) as numpy arrays."""
+    import numpy as np
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    info = PlanInfo()
+    size = 1 << 16
+    while True:
+        buf = np.zeros(size, np.uint8)
+        st = lib().kv_nvfp4_plan_host(ctypes.byref(layout), sl.ctypes.data, len(sl), q_len,
+                                      int(causal), chunk_tokens, num_ctas, buf.ctypes.data, size,
+                                      ctypes.byref(info))
+        if st == KV_NVFP4_ENOSPACE:
+            size *= 4
+            continue
+        _check(st, "kv_nvfp4_plan_host")
+        break
+    i32 = buf.view(np.int32)
+    groups = i32[info.off_groups // 4: info.off_groups // 4 + 8 * info.num_groups].reshape(-1, 8)
+    segs = i32[info.off_segments // 4: info.off_segments // 4 + 4 * info.num_segments].reshape(-1, 4)
+    cta = i32[info.off_cta // 4: info.off_cta // 4 + info.grid + 1]
+    return info, groups.copy(), segs.copy(), cta.copy()
+
+
+def kv_nvfp4_decode_attn(layout, plan: PlanInfo, workspace, q_codes, q_scales, sm_scale,
                          k_codes, k_scales, v_codes, v_scales, num_pages, block_table, max_pages,
                          out, status=None, stream=None):
     _check(lib().kv_nvfp4_decode_attn(
         ctypes.byref(layout), ctypes.byref(plan), _ptr(workspace), _ptr(q_codes), _ptr(q_scales),
-        int(causal), float(sm_scale), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes),
-        _ptr(v_scales), num_pages, _ptr(block_table), max_pages, _ptr(out), _ptr(status),
-        _stream(stream)), "kv_nvfp4_decode_attn")
+        float(sm_scale), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), num_pages,
+        _ptr(block_table), max_pages, _ptr(out), _ptr(status), _stream(stream)),
+        "kv_nvfp4_decode_attn")
 
 
 from .cache import PagedNVFP4Cache  # noqa: E402  (device buffers for one layer, allocated by torch)

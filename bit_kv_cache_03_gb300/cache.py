@@ -55,18 +55,18 @@ class PagedNVFP4Cache:
                 torch.empty(T * H * 8, dtype=torch.uint8, device=self.device))
 
     # -- split-K plan + attention -----------------------------------------------------------
-    def plan(self, seq_lens, q_len, chunk_tokens=1024, stream=None):
-        need = kv_nvfp4_plan_workspace_bytes(self.layout, seq_lens, q_len, chunk_tokens)
+    def plan(self, seq_lens, q_len, causal=True, chunk_tokens=1024, stream=None):
+        need = kv_nvfp4_plan_workspace_bytes(self.layout, seq_lens, q_len, causal, chunk_tokens)
         if self.workspace is None or self.workspace.numel() < need:
             self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
-        self.plan_info = kv_nvfp4_plan(self.layout, seq_lens, q_len, chunk_tokens, self.workspace,
-                                       self.workspace.numel(), stream)
+        self.plan_info = kv_nvfp4_plan(self.layout, seq_lens, q_len, causal, chunk_tokens,
+                                       self.workspace, self.workspace.numel(), stream)
         return self.plan_info
 
-    def attend(self, q_codes, q_scales, out, causal=True, sm_scale=None, stream=None):
+    def attend(self, q_codes, q_scales, out, sm_scale=None, stream=None):
         if sm_scale is None:
             sm_scale = 1.0 / math.sqrt(128)
         kv_nvfp4_decode_attn(self.layout, self.plan_info, self.workspace, q_codes, q_scales,
-                             causal, sm_scale, self.k_codes, self.k_scales, self.v_codes,
-                             self.v_scales, self.num_pages, self.block_table, self.max_pages, out,
-                             self.status, stream)
+                             sm_scale, self.k_codes, self.k_scales, self.v_codes, self.v_scales,
+                             self.num_pages, self.block_table, self.max_pages, out, self.status,
+                             stream)

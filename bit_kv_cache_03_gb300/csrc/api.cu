@@ -1,6 +1,7 @@
 // C ABI of the NVFP4 KV-cache library: argument validation, the RoPE table, the split-K plan,
 // and the kernel launches. Declarations and contracts are in include/kv_nvfp4.h.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -22,16 +23,17 @@ cudaError_t launch_append(const uint16_t* q, const uint16_t* k, const uint16_t* 
 cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const uint8_t* k_codes,
                           const uint8_t* k_scales, const uint8_t* v_codes,
                           const uint8_t* v_scales, const int32_t* block_table, int32_t max_pages,
-                          int32_t num_pages, const void* seqinfo, const void* items,
-                          int32_t* counters, float* partials, float* out, int32_t* status,
-                          int32_t Hq, int32_t Hkv, int32_t q_len, int32_t causal, int32_t n_rg,
-                          int32_t total_items, float sm_scale, int num_sms, cudaStream_t stream);
+                          int32_t num_pages, const void* groups, const void* segments,
+                          const int32_t* cta_seg, int32_t* counters, float* partials, float* out,
+                          int32_t* status, int32_t Hq, int32_t Hkv, int32_t q_len, int32_t causal,
+                          int32_t grid, float sm_scale, cudaStream_t stream);
 }  // namespace kvnvfp4
 
 namespace {
 
-constexpr int kRowsPerItem = 8;   // query rows per decode work item
+constexpr int kRowsPerItem = 8;   // query rows per attention work group
 constexpr int kPartFloats = kRowsPerItem * 128 + 2 * kRowsPerItem;
+constexpr int kMaxGridForSizing = 1024;  // workspace sizing when no device is visible
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -48,51 +50,126 @@ int num_sms_current_device() {
 
 uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
-// Layout of a plan workspace for the given lengths; also validates them.
-kv_nvfp4_status plan_layout(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, int32_t num_seqs,
-                            int32_t q_len, int32_t chunk_tokens, kv_nvfp4_plan_info* info) {
+// The split-K work list. Groups are (sequence, kv head, 8-row query tile) in that order; each
+// group's visited pages are cut into chunks of chunk_pages, and the chunk stream of all groups is
+// dealt out to `grid` CTAs in contiguous ranges of about total_pages / grid pages each.
+struct PlanBuild {
+  kv_nvfp4_plan_info info;
+  std::vector<int32_t> groups;    // 8 ints per group
+  std::vector<int32_t> segments;  // 4 ints per segment
+  std::vector<int32_t> cta_seg;   // grid + 1
+};
+
+kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, int32_t num_seqs,
+                           int32_t q_len, int32_t causal, int32_t chunk_tokens, int32_t num_sms,
+                           PlanBuild* pb) {
   if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK) return KV_NVFP4_EINVAL;
-  if (h_seq_lens == nullptr || num_seqs <= 0 || q_len <= 0) return KV_NVFP4_EINVAL;
+  if (h_seq_lens == nullptr || num_seqs <= 0 || q_len <= 0 || num_sms <= 0) return KV_NVFP4_EINVAL;
   if (chunk_tokens <= 0 || chunk_tokens % L->page_size != 0) return KV_NVFP4_EINVAL;
+  const int32_t P = L->page_size;
   const int32_t G = L->num_q_heads / L->num_kv_heads;
   const int64_t rows = (int64_t)G * q_len;
   const int64_t n_rg = (rows + kRowsPerItem - 1) / kRowsPerItem;
-  if (n_rg > (1 << 20)) return KV_NVFP4_EINVAL;
-  const int32_t chunk_pages = chunk_tokens / L->page_size;
-  int64_t chunks = 0, partials = 0, max_chunks = 0, total = 0, max_len = 0;
+  const int32_t chunk_pages = chunk_tokens / P;
+  const int64_t n_groups = (int64_t)num_seqs * L->num_kv_heads * n_rg;
+  if (n_groups > (1 << 26)) return KV_NVFP4_EINVAL;
+  int64_t total_pages = 0, total_chunks = 0, total_tok = 0, max_len = 0;
+  std::vector<int32_t> gpages((size_t)n_groups);
   for (int32_t s = 0; s < num_seqs; ++s) {
     const int32_t len = h_seq_lens[s];
     if (len < q_len || len < 1) return KV_NVFP4_EINVAL;
-    const int64_t pages = (len + L->page_size - 1) / L->page_size;
-    const int64_t nc = (pages + chunk_pages - 1) / chunk_pages;
-    chunks += nc;
-    if (nc > 1) partials += nc * L->num_kv_heads * n_rg;
-    if (nc > max_chunks) max_chunks = nc;
-    total += len;
+    total_tok += len;
     if (len > max_len) max_len = len;
+    for (int32_t h = 0; h < L->num_kv_heads; ++h) {
+      for (int64_t rg = 0; rg < n_rg; ++rg) {
+        int64_t vis = len;  // keys any row of the tile can see
+        if (causal) {
+          const int64_t last_row = std::min<int64_t>(rows - 1, rg * kRowsPerItem + kRowsPerItem - 1);
+          vis = (int64_t)(len - q_len) + last_row / G + 1;
+        }
+        const int64_t pages = (vis + P - 1) / P;
+        gpages[(size_t)(((int64_t)s * L->num_kv_heads + h) * n_rg + rg)] = (int32_t)pages;
+        total_pages += pages;
+        total_chunks += (pages + chunk_pages - 1) / chunk_pages;
+      }
+    }
   }
-  if (chunks * L->num_kv_heads * n_rg > 0x7FFFFFFF || partials > 0x7FFFFFFF)
-    return KV_NVFP4_EINVAL;
+  const int64_t grid = std::min<int64_t>(num_sms, total_chunks);
+  pb->groups.assign((size_t)n_groups * 8, 0);
+  pb->segments.clear();
+  pb->cta_seg.assign((size_t)grid + 1, 0);
+  std::vector<int32_t> seg_count((size_t)n_groups, 0);
+  // deal chunks to CTAs: CTA c closes once the pages dealt so far reach (c+1) * total / grid
+  int64_t cta = 0, dealt = 0;
+  for (int64_t gi = 0; gi < n_groups; ++gi) {
+    const int32_t pages = gpages[(size_t)gi];
+    int32_t lo = 0;
+    while (lo < pages) {
+      // extend this segment chunk by chunk while the CTA is below its quota
+      int32_t hi = lo;
+      while (hi < pages) {
+        hi = std::min(pages, hi + chunk_pages);
+        const int64_t quota = (cta + 1) * total_pages / grid;
+        if (cta < grid - 1 && dealt + (hi - lo) >= quota) break;
+      }
+      pb->segments.push_back((int32_t)gi);
+      pb->segments.push_back(lo);
+      pb->segments.push_back(hi);
+      pb->segments.push_back(-1);
+      seg_count[(size_t)gi] += 1;
+      dealt += hi - lo;
+      lo = hi;
+      const int64_t quota = (cta + 1) * total_pages / grid;
+      if (cta < grid - 1 && dealt >= quota) {
+        ++cta;
+        pb->cta_seg[(size_t)cta] = (int32_t)(pb->segments.size() / 4);
+      }
+    }
+  }
+  const int64_t n_seg = (int64_t)pb->segments.size() / 4;
+  for (int64_t c = cta + 1; c <= grid; ++c) pb->cta_seg[(size_t)c] = (int32_t)n_seg;
+  // partial slots, contiguous per group in segment order
+  int64_t parts = 0;
+  std::vector<int32_t> first_part((size_t)n_groups, -1);
+  for (int64_t si = 0; si < n_seg; ++si) {
+    const int32_t gi = pb->segments[(size_t)si * 4];
+    if (seg_count[(size_t)gi] > 1) {
+      if (first_part[(size_t)gi] < 0) first_part[(size_t)gi] = (int32_t)parts;
+      pb->segments[(size_t)si * 4 + 3] = (int32_t)parts++;
+    }
+  }
+  for (int64_t gi = 0; gi < n_groups; ++gi) {
+    const int64_t rg = gi % n_rg, h = (gi / n_rg) % L->num_kv_heads, s = gi / n_rg / L->num_kv_heads;
+    int32_t* g = &pb->groups[(size_t)gi * 8];
+    g[0] = (int32_t)s; g[1] = (int32_t)h; g[2] = (int32_t)rg; g[3] = h_seq_lens[s];
+    g[4] = seg_count[(size_t)gi]; g[5] = first_part[(size_t)gi]; g[6] = gpages[(size_t)gi]; g[7] = 0;
+  }
+  kv_nvfp4_plan_info* info = &pb->info;
   std::memset(info, 0, sizeof(*info));
   info->num_seqs = num_seqs;
   info->q_len = q_len;
+  info->causal = causal ? 1 : 0;
   info->chunk_pages = chunk_pages;
-  info->num_chunks = (int32_t)chunks;
-  info->num_row_groups = (int32_t)n_rg;
   info->num_kv_heads = L->num_kv_heads;
-  info->num_partials = (int32_t)partials;
-  info->max_chunks = (int32_t)max_chunks;
-  info->total_kv_tokens = total;
+  info->num_row_groups = (int32_t)n_rg;
+  info->num_groups = (int32_t)n_groups;
+  info->num_segments = (int32_t)n_seg;
+  info->num_partials = (int32_t)parts;
+  info->grid = (int32_t)grid;
   info->max_seq_len = (int32_t)max_len;
+  info->total_kv_tokens = total_tok;
+  info->total_pages = total_pages;
   uint64_t off = 0;
-  info->off_seqinfo = off;
-  off = align_up(off + 16ull * num_seqs, 256);
-  info->off_items = off;
-  off = align_up(off + 16ull * chunks, 256);
+  info->off_groups = off;
+  off = align_up(off + 32ull * n_groups, 256);
+  info->off_segments = off;
+  off = align_up(off + 16ull * n_seg, 256);
+  info->off_cta = off;
+  off = align_up(off + 4ull * (grid + 1), 256);
   info->off_counters = off;
-  off = align_up(off + 4ull * num_seqs * L->num_kv_heads * n_rg, 256);
+  off = align_up(off + 4ull * n_groups, 256);
   info->off_partials = off;
-  off = align_up(off + 4ull * kPartFloats * partials, 256);
+  off = align_up(off + 4ull * kPartFloats * parts, 256);
   info->workspace_bytes = off;
   return KV_NVFP4_OK;
 }
@@ -209,49 +286,57 @@ kv_nvfp4_status kv_nvfp4_append(const kv_nvfp4_layout* L, const void* q, const v
 }
 
 kv_nvfp4_status kv_nvfp4_plan_workspace_bytes(const kv_nvfp4_layout* L, const int32_t* h_seq_lens,
-                                              int32_t num_seqs, int32_t q_len,
+                                              int32_t num_seqs, int32_t q_len, int32_t causal,
                                               int32_t chunk_tokens, size_t* bytes) {
   if (bytes == nullptr) return KV_NVFP4_EINVAL;
-  kv_nvfp4_plan_info info;
-  const kv_nvfp4_status s = plan_layout(L, h_seq_lens, num_seqs, q_len, chunk_tokens, &info);
+  int num_sms = num_sms_current_device();
+  if (num_sms <= 0) num_sms = kMaxGridForSizing;  // no device: size for the largest grid
+  PlanBuild pb;
+  const kv_nvfp4_status s =
+      plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_sms, &pb);
   if (s != KV_NVFP4_OK) return s;
-  *bytes = (size_t)info.workspace_bytes;
+  *bytes = (size_t)pb.info.workspace_bytes;
+  return KV_NVFP4_OK;
+}
+
+kv_nvfp4_status kv_nvfp4_plan_host(const kv_nvfp4_layout* L, const int32_t* h_seq_lens,
+                                   int32_t num_seqs, int32_t q_len, int32_t causal,
+                                   int32_t chunk_tokens, int32_t num_ctas, void* h_workspace,
+                                   size_t ws_bytes, kv_nvfp4_plan_info* info) {
+  if (info == nullptr || h_workspace == nullptr || num_ctas <= 0) return KV_NVFP4_EINVAL;
+  PlanBuild pb;
+  const kv_nvfp4_status s =
+      plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_ctas, &pb);
+  if (s != KV_NVFP4_OK) return s;
+  const kv_nvfp4_plan_info& pi = pb.info;
+  if (ws_bytes < pi.workspace_bytes) return KV_NVFP4_ENOSPACE;
+  char* h = (char*)h_workspace;
+  std::memset(h, 0, (size_t)pi.off_partials);
+  std::memcpy(h + pi.off_groups, pb.groups.data(), pb.groups.size() * 4);
+  std::memcpy(h + pi.off_segments, pb.segments.data(), pb.segments.size() * 4);
+  std::memcpy(h + pi.off_cta, pb.cta_seg.data(), pb.cta_seg.size() * 4);
+  *info = pi;
   return KV_NVFP4_OK;
 }
 
 kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout* L, const int32_t* h_seq_lens,
-                              int32_t num_seqs, int32_t q_len, int32_t chunk_tokens,
-                              void* d_workspace, size_t ws_bytes, kv_nvfp4_plan_info* info,
-                              void* stream) {
+                              int32_t num_seqs, int32_t q_len, int32_t causal,
+                              int32_t chunk_tokens, void* d_workspace, size_t ws_bytes,
+                              kv_nvfp4_plan_info* info, void* stream) {
   if (info == nullptr || d_workspace == nullptr || !aligned16(d_workspace)) return KV_NVFP4_EINVAL;
-  kv_nvfp4_plan_info pi;
-  const kv_nvfp4_status s = plan_layout(L, h_seq_lens, num_seqs, q_len, chunk_tokens, &pi);
+  const int num_sms = num_sms_current_device();
+  if (num_sms <= 0) return KV_NVFP4_ECUDA;
+  PlanBuild pb;
+  const kv_nvfp4_status s =
+      plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_sms, &pb);
   if (s != KV_NVFP4_OK) return s;
+  const kv_nvfp4_plan_info& pi = pb.info;
   if (ws_bytes < pi.workspace_bytes) return KV_NVFP4_ENOSPACE;
-  // host image of the seqinfo + items region
+  // host image of the tables (everything before the tickets), one copy
   std::vector<int32_t> host((size_t)(pi.off_counters / 4), 0);
-  int32_t* seqinfo = host.data() + pi.off_seqinfo / 4;
-  int32_t* items = host.data() + pi.off_items / 4;
-  int64_t ci = 0, part = 0;
-  const int32_t P = L->page_size;
-  for (int32_t sq = 0; sq < num_seqs; ++sq) {
-    const int32_t len = h_seq_lens[sq];
-    const int32_t pages = (len + P - 1) / P;
-    const int32_t nc = (pages + pi.chunk_pages - 1) / pi.chunk_pages;
-    seqinfo[4 * sq + 0] = len;
-    seqinfo[4 * sq + 1] = nc;
-    seqinfo[4 * sq + 2] = (int32_t)part;
-    seqinfo[4 * sq + 3] = 0;
-    if (nc > 1) part += (int64_t)nc * L->num_kv_heads * pi.num_row_groups;
-    for (int32_t c = 0; c < nc; ++c, ++ci) {
-      const int32_t pb = c * pi.chunk_pages;
-      const int32_t np = (pages - pb < pi.chunk_pages) ? pages - pb : pi.chunk_pages;
-      items[4 * ci + 0] = sq;
-      items[4 * ci + 1] = pb;
-      items[4 * ci + 2] = np;
-      items[4 * ci + 3] = c;
-    }
-  }
+  std::memcpy(host.data() + pi.off_groups / 4, pb.groups.data(), pb.groups.size() * 4);
+  std::memcpy(host.data() + pi.off_segments / 4, pb.segments.data(), pb.segments.size() * 4);
+  std::memcpy(host.data() + pi.off_cta / 4, pb.cta_seg.data(), pb.cta_seg.size() * 4);
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemcpyAsync(d_workspace, host.data(), host.size() * 4, cudaMemcpyHostToDevice, st) !=
       cudaSuccess)
@@ -265,14 +350,15 @@ kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout* L, const int32_t* h_seq_len
 
 kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout* L, const kv_nvfp4_plan_info* plan,
                                      void* d_workspace, const uint8_t* q_codes,
-                                     const uint8_t* q_scales, int32_t causal, float sm_scale,
+                                     const uint8_t* q_scales, float sm_scale,
                                      const uint8_t* k_codes, const uint8_t* k_scales,
                                      const uint8_t* v_codes, const uint8_t* v_scales,
                                      int32_t num_pages, const int32_t* d_block_table,
                                      int32_t max_pages, float* out, int32_t* d_status,
                                      void* stream) {
   if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || plan == nullptr) return KV_NVFP4_EINVAL;
-  if (plan->num_kv_heads != L->num_kv_heads || plan->num_seqs <= 0 || plan->q_len <= 0)
+  if (plan->num_kv_heads != L->num_kv_heads || plan->num_seqs <= 0 || plan->q_len <= 0 ||
+      plan->grid <= 0)
     return KV_NVFP4_EINVAL;
   if (!d_workspace || !q_codes || !q_scales || !k_codes || !k_scales || !v_codes || !v_scales ||
       !d_block_table || !out || num_pages <= 0 || max_pages <= 0)
@@ -282,17 +368,14 @@ kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout* L, const kv_nvfp4_pl
   const void* ptrs[] = {d_workspace, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out};
   for (const void* p : ptrs)
     if (!aligned16(p)) return KV_NVFP4_EINVAL;
-  const int num_sms = num_sms_current_device();
-  if (num_sms <= 0) return KV_NVFP4_ECUDA;
   if (!(sm_scale > 0.0f)) sm_scale = 1.0f / std::sqrt((float)L->head_dim);
   char* ws = (char*)d_workspace;
-  const int64_t total = (int64_t)plan->num_chunks * plan->num_kv_heads * plan->num_row_groups;
   const cudaError_t e = kvnvfp4::launch_decode(
       q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, d_block_table, max_pages,
-      num_pages, ws + plan->off_seqinfo, ws + plan->off_items,
-      (int32_t*)(ws + plan->off_counters), (float*)(ws + plan->off_partials), out, d_status,
-      L->num_q_heads, L->num_kv_heads, plan->q_len, causal ? 1 : 0, plan->num_row_groups,
-      (int32_t)total, sm_scale, num_sms, (cudaStream_t)stream);
+      num_pages, ws + plan->off_groups, ws + plan->off_segments,
+      (const int32_t*)(ws + plan->off_cta), (int32_t*)(ws + plan->off_counters),
+      (float*)(ws + plan->off_partials), out, d_status, L->num_q_heads, L->num_kv_heads,
+      plan->q_len, plan->causal, plan->grid, sm_scale, (cudaStream_t)stream);
   return e == cudaSuccess ? KV_NVFP4_OK : KV_NVFP4_ECUDA;
 }
 

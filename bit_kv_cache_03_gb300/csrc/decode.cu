@@ -5,13 +5,18 @@
 // scales. Split-K with an fp32 log-sum-exp merge is this library's design (the pages run long
 // contexts from a paged pool and say nothing about the kernel's decomposition).
 //
-// Work item = (sequence chunk of <= chunk_pages pages, kv head, tile of 8 query rows). A row is
-// (query token, head in the GQA group), row = token * group + head_in_group.
+// Work decomposition: a group is (sequence, kv head, tile of 8 query rows); a row is (query token,
+// head in the GQA group), row = token * group + head_in_group. The plan lays the groups' pages
+// (cut into split-K chunks) end to end and hands every CTA (one persistent CTA per SM) an equal
+// share of that page stream; a CTA's share is one or more segments, each a contiguous page
+// range of one group. Within a segment the CTA's state carries across chunks (online softmax);
+// at the end of a segment it writes either the final rows (the group lies in one CTA) or one
+// (m, l, O) partial, and the CTA that takes the group's last ticket combines its partials.
 //
-// Per CTA (persistent, one per SM): warp 8 is the producer; one lane streams every page of the
-// CTA's items into a 16-slot shared-memory ring with bulk async copies (K codes 4 KiB, K scales
-// 512 B, V codes 4 KiB, V scales 512 B per page and head), each slot guarded by a full and an
-// empty mbarrier. Warps 0..7 consume pages round-robin within an item.
+// Per CTA: warp 8 is the producer; lane 0 streams every page of the CTA's segments into a
+// 16-slot shared-memory ring with bulk async copies (K codes 4 KiB, K scales 512 B, V codes
+// 4 KiB, V scales 512 B per page and head), each slot guarded by a full and an empty mbarrier.
+// Warps 0..7 consume the segment's pages round-robin.
 //
 // Per page and warp, the product runs on the warp-level tensor path with keys as the M
 // dimension (16 keys per MMA) and the 8 query rows as N:
@@ -24,9 +29,8 @@
 // dims (the same one for both operands), chosen so that each thread reads contiguous bytes.
 //
 // Softmax: running max per row, exp2 with log2(e) folded into the scale, rescale of the
-// accumulator only when the max grows. At the end of an item the 8 warps' states are merged in
-// shared memory; a split sequence writes (m, l, O) to its partial slot, takes a ticket, and the
-// CTA that completes the last chunk combines all partials (no waiting on other CTAs).
+// accumulator only when the max grows. At the end of a segment the 8 warps' states are merged
+// in shared memory; merging never waits on another CTA.
 
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -46,8 +50,9 @@ constexpr int kRows = 8;                           // query rows per work item
 constexpr int kPartFloats = kRows * 128 + 2 * kRows;  // O[8][128], m[8], l[8]
 constexpr int kRingBytes = kSlots * kSlotBytes;
 constexpr int kBarOff = kRingBytes;                // 2 * kSlots mbarriers
-constexpr int kMergeOff = kBarOff + 2 * kSlots * 8;
-constexpr int kMergeFloats = kConsumerWarps * (kRows * 128 + 2 * kRows);
+constexpr int kSlotPidOff = kBarOff + 2 * kSlots * 8;   // int32 page id per slot
+constexpr int kMergeOff = kSlotPidOff + kSlots * 4;
+constexpr int kMergeFloats = kConsumerWarps * kPartFloats;
 constexpr int kFlagOff = kMergeOff + kMergeFloats * 4;
 constexpr int kSmemBytes = kFlagOff + 16;
 
@@ -61,78 +66,72 @@ struct DecodeParams {
   const int32_t* block_table;
   int32_t max_pages;
   int32_t num_pages;
-  const int4* seqinfo;   // {len, n_chunks, part_base, 0}
-  const int4* items;     // {seq, page_begin, n_pages, chunk}
-  int32_t* counters;     // [num_seqs][Hkv][n_rg]
+  const int4* groups;    // 2 x int4 per group: {seq, kvh, rg, len}, {n_seg, first_part, pages, 0}
+  const int4* segments;  // {group, page_lo, page_hi, part_slot or -1}
+  const int32_t* cta_seg;  // [grid + 1]: segments of CTA b are [cta_seg[b], cta_seg[b+1])
+  int32_t* counters;     // [num_groups], merge tickets
   float* partials;       // [num_partials][kPartFloats]
   float* out;
   int32_t* status;
-  int32_t Hq, Hkv, G, q_len, causal, n_rg;
-  int32_t total_items;
+  int32_t Hq, Hkv, G, q_len, causal;
   float c2;              // sm_scale * log2(e)
 };
 
-struct ItemDesc {
-  int seq, page_begin, n_pages, chunk, kvh, rg;
-  int len, n_chunks, part_base;
-};
-
-__device__ __forceinline__ ItemDesc decode_item(const DecodeParams& p, int it) {
-  ItemDesc d;
-  d.rg = it % p.n_rg;
-  const int t = it / p.n_rg;
-  d.kvh = t % p.Hkv;
-  const int ci = t / p.Hkv;
-  const int4 item = p.items[ci];
-  d.seq = item.x;
-  d.page_begin = item.y;
-  d.n_pages = item.z;
-  d.chunk = item.w;
-  const int4 si = p.seqinfo[d.seq];
-  d.len = si.x;
-  d.n_chunks = si.y;
-  d.part_base = si.z;
-  return d;
-}
-
 // --------------------------------------------------------------------------------------------
-// Producer: one thread streams pages into the ring.
+// Producer warp: lane 0 streams the CTA's pages into the ring; the other lanes help load page
+// ids 32 at a time. The page id (or -1 for an id outside the pool) is published in shared
+// memory before the slot's full barrier is armed, so consumers never read the block table.
 // --------------------------------------------------------------------------------------------
-__device__ void producer(const DecodeParams& p, uint8_t* smem) {
+__device__ void producer(const DecodeParams& p, uint8_t* smem, int lane) {
   const uint32_t ring = smem_u32(smem);
   const uint32_t bars = smem_u32(smem + kBarOff);
+  volatile int32_t* slot_pid = reinterpret_cast<volatile int32_t*>(smem + kSlotPidOff);
   uint32_t k = 0;
   bool timed_out = false;
-  for (int it = blockIdx.x; it < p.total_items; it += gridDim.x) {
-    const ItemDesc d = decode_item(p, it);
-    for (int j = 0; j < d.n_pages; ++j, ++k) {
-      const uint32_t slot = k % kSlots;
-      const uint32_t full = bars + 8 * slot;
-      const uint32_t empty = bars + 8 * (kSlots + slot);
-      if (k >= kSlots) {
-        if (!mbar_wait_bounded(empty, ((k / kSlots) - 1) & 1)) timed_out = true;
+  const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
+  for (int s = s_begin; s < s_end; ++s) {
+    const int4 seg = p.segments[s];
+    const int4 g0 = p.groups[2 * seg.x];
+    const int seq = g0.x, kvh = g0.y;
+    for (int p0 = seg.y; p0 < seg.z; p0 += 32) {
+      const int n = min(32, seg.z - p0);
+      const int32_t mine = (lane < n) ? p.block_table[(int64_t)seq * p.max_pages + p0 + lane] : -1;
+      for (int j = 0; j < n; ++j, ++k) {
+        const int32_t pid = __shfl_sync(0xffffffffu, mine, j);
+        if (lane == 0) {
+          const uint32_t slot = k % kSlots;
+          const uint32_t full = bars + 8 * slot;
+          if (k >= kSlots) {
+            if (!mbar_wait_bounded(bars + 8 * (kSlots + slot), ((k / kSlots) - 1) & 1))
+              timed_out = true;
+          }
+          const bool valid = pid >= 0 && pid < p.num_pages;
+          slot_pid[slot] = valid ? pid : -1;
+          if (valid) {
+            const int64_t head = (int64_t)pid * p.Hkv + kvh;
+            const uint32_t dst = ring + slot * kSlotBytes;
+            mbar_arrive_expect_tx(full, kSlotBytes);
+            bulk_g2s(dst + kKcOff, p.k_codes + head * 4096, 4096, full);
+            bulk_g2s(dst + kKsOff, p.k_scales + head * 512, 512, full);
+            bulk_g2s(dst + kVcOff, p.v_codes + head * 4096, 4096, full);
+            bulk_g2s(dst + kVsOff, p.v_scales + head * 512, 512, full);
+          } else {
+            mbar_arrive(full);  // completes the phase with no data; consumers skip the page
+          }
+        }
+        __syncwarp();
       }
-      const int32_t pid = p.block_table[(int64_t)d.seq * p.max_pages + d.page_begin + j];
-      if (pid < 0 || pid >= p.num_pages) {
-        mbar_arrive(full);  // completes the phase with no data; consumers skip the page
-        continue;
-      }
-      const int64_t head = (int64_t)pid * p.Hkv + d.kvh;
-      const uint32_t dst = ring + slot * kSlotBytes;
-      mbar_arrive_expect_tx(full, kSlotBytes);
-      bulk_g2s(dst + kKcOff, p.k_codes + head * 4096, 4096, full);
-      bulk_g2s(dst + kKsOff, p.k_scales + head * 512, 512, full);
-      bulk_g2s(dst + kVcOff, p.v_codes + head * 4096, 4096, full);
-      bulk_g2s(dst + kVsOff, p.v_scales + head * 512, 512, full);
     }
   }
-  // Drain: make sure no copy into this CTA's shared memory is still in flight at exit.
-  const uint32_t issued = k;
-  for (uint32_t s = 0; s < kSlots && s < issued; ++s) {
-    const uint32_t last = issued - 1 - ((issued - 1 - s) % kSlots);  // last use of slot s
-    if (!mbar_wait_bounded(bars + 8 * (last % kSlots), (last / kSlots) & 1)) timed_out = true;
+  if (lane == 0) {
+    // Drain: no copy into this CTA's shared memory may still be in flight at exit.
+    const uint32_t issued = k;
+    for (uint32_t s = 0; s < kSlots && s < issued; ++s) {
+      const uint32_t last = issued - 1 - ((issued - 1 - s) % kSlots);  // last use of slot s
+      if (!mbar_wait_bounded(bars + 8 * (last % kSlots), (last / kSlots) & 1)) timed_out = true;
+    }
+    if (timed_out) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
   }
-  if (timed_out) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
 
 // --------------------------------------------------------------------------------------------
@@ -275,27 +274,39 @@ __device__ __forceinline__ void process_page(WarpState& st, uint32_t slot_addr, 
   }
 }
 
+__device__ __forceinline__ void store_out(const DecodeParams& p, int seq, int kvh, int r, int dim,
+                                          float v) {
+  const int tok = r / p.G, hq = kvh * p.G + r % p.G;
+  p.out[(((int64_t)seq * p.q_len + tok) * p.Hq + hq) * 128 + dim] = v;
+}
+
 __device__ void consumer(const DecodeParams& p, uint8_t* smem, int warp, int lane) {
   const int g = lane >> 2, t = lane & 3;
   const uint32_t ring = smem_u32(smem);
   const uint32_t bars = smem_u32(smem + kBarOff);
+  const volatile int32_t* slot_pid = reinterpret_cast<const volatile int32_t*>(smem + kSlotPidOff);
   float* mrg = reinterpret_cast<float*>(smem + kMergeOff);
   volatile int* flag = reinterpret_cast<volatile int*>(smem + kFlagOff);
   const int ctid = warp * 32 + lane;  // 0 .. 255 over consumer threads
   const int rows_total = p.G * p.q_len;
   uint32_t kbase = 0;
   bool timed_out = false;
+  const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
 
-  for (int it = blockIdx.x; it < p.total_items; it += gridDim.x) {
-    const ItemDesc d = decode_item(p, it);
-    const int row0 = d.rg * kRows;
-    const int L0 = d.len - p.q_len;
+  for (int s = s_begin; s < s_end; ++s) {
+    const int4 seg = p.segments[s];
+    const int4 g0 = p.groups[2 * seg.x];
+    const int4 g1 = p.groups[2 * seg.x + 1];
+    const int seq = g0.x, kvh = g0.y, rg = g0.z, len = g0.w;
+    const int n_seg = g1.x, first_part = g1.y;
+    const int row0 = rg * kRows;
+    const int L0 = len - p.q_len;
     // visibility limit (largest visible key position) of rows 2t, 2t+1; -1 for padding rows
     int lim[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int r = row0 + 2 * t + e;
-      lim[e] = (r < rows_total) ? (p.causal ? L0 + r / p.G : d.len - 1) : -1;
+      lim[e] = (r < rows_total) ? (p.causal ? L0 + r / p.G : len - 1) : -1;
     }
     WarpState st;
 #pragma unroll
@@ -308,10 +319,10 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, int warp, int lan
       uint4 qc = make_uint4(0u, 0u, 0u, 0u);
       uint32_t qs = 0;
       if (r < rows_total) {
-        const int tok = r / p.G, hq = d.kvh * p.G + r % p.G;
-        const int64_t qrow = ((int64_t)d.seq * p.q_len + tok) * p.Hq + hq;
+        const int tok = r / p.G, hq = kvh * p.G + r % p.G;
+        const int64_t qrow = ((int64_t)seq * p.q_len + tok) * p.Hq + hq;
         qc = *reinterpret_cast<const uint4*>(p.q_codes + qrow * 64 + 16 * t);
-        qs = (uint32_t)p.q_scales[qrow * 8 + 2 * t] | ((uint32_t)p.q_scales[qrow * 8 + 2 * t + 1] << 8);
+        qs = *reinterpret_cast<const uint16_t*>(p.q_scales + qrow * 8 + 2 * t);
       }
       const uint32_t sh = cvt_e4m3x2_f16(qs);
       const uint32_t s0 = dup_lo(sh), s1 = dup_hi(sh);
@@ -327,22 +338,22 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, int warp, int lan
         st.qf[2 * w + 1][1] = hmul2(a3, sc);
       }
     }
-    // pages of this item: warp w takes pages w, w + 8, ...
-    for (int j = warp; j < d.n_pages; j += kConsumerWarps) {
+    // pages of this segment: warp w takes pages w, w + 8, ...
+    const int n_pages = seg.z - seg.y;
+    for (int j = warp; j < n_pages; j += kConsumerWarps) {
       const uint32_t k = kbase + j;
       const uint32_t slot = k % kSlots;
       if (!mbar_wait_bounded(bars + 8 * slot, (k / kSlots) & 1)) timed_out = true;
-      const int32_t pid = p.block_table[(int64_t)d.seq * p.max_pages + d.page_begin + j];
-      if (pid >= 0 && pid < p.num_pages) {
-        const int kp0 = (d.page_begin + j) * kPage;
-        process_page(st, ring + slot * kSlotBytes, kp0, d.len, lim[0], lim[1], p.c2, g, t);
+      if (slot_pid[slot] >= 0) {
+        const int kp0 = (seg.y + j) * kPage;
+        process_page(st, ring + slot * kSlotBytes, kp0, len, lim[0], lim[1], p.c2, g, t);
       } else if (lane == 0) {
         flag_status(p.status, KV_NVFP4_DEV_BAD_PAGE);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bars + 8 * (kSlots + slot));
     }
-    kbase += d.n_pages;
+    kbase += n_pages;
 
     // ---- merge the 8 warps' states in shared memory ----
     float l0 = st.l[0], l1 = st.l[1];
@@ -351,7 +362,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, int warp, int lan
       l0 += __shfl_xor_sync(0xffffffffu, l0, m);
       l1 += __shfl_xor_sync(0xffffffffu, l1, m);
     }
-    float* Ow = mrg + warp * (kRows * 128 + 2 * kRows);  // [dim][8 rows], then m[8], l[8]
+    float* Ow = mrg + warp * kPartFloats;  // [dim][8 rows], then m[8], l[8]
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int dA = 16 * g + i, dB = dA + 8;
@@ -366,22 +377,20 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, int warp, int lan
     }
     named_barrier_sync(1, kConsumerWarps * 32);
 
-    const bool split = d.n_chunks > 1;
-    float* part = split ? p.partials + (int64_t)(d.part_base + (d.chunk * p.Hkv + d.kvh) * p.n_rg + d.rg) * kPartFloats
-                        : nullptr;
+    const bool split = n_seg > 1;
+    float* part = split ? p.partials + (int64_t)seg.w * kPartFloats : nullptr;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int idx = ctid + 256 * e;   // (row, dim) with row = idx / 128
+      const int idx = ctid + 256 * e;   // (row, dim): row = idx / 128
       const int row = idx >> 7, dim = idx & 127;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w)
-        M = fmaxf(M, mrg[w * (kRows * 128 + 2 * kRows) + kRows * 128 + row]);
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg[w * kPartFloats + kRows * 128 + row]);
       float L = 0.f, O = 0.f;
       if (M != -INFINITY) {
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
-          const float* base = mrg + w * (kRows * 128 + 2 * kRows);
+          const float* base = mrg + w * kPartFloats;
           const float mw = base[kRows * 128 + row];
           const float f = (mw == -INFINITY) ? 0.f : fast_exp2((mw - M) * p.c2);
           L += f * base[kRows * 128 + kRows + row];
@@ -396,27 +405,25 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, int warp, int lan
           part[kRows * 128 + kRows + row] = L;
         }
       } else if (r < rows_total && L > 0.f) {
-        const int tok = r / p.G, hq = d.kvh * p.G + r % p.G;
-        p.out[(((int64_t)d.seq * p.q_len + tok) * p.Hq + hq) * 128 + dim] = O / L;
+        store_out(p, seq, kvh, r, dim, O / L);
       }
     }
     if (split) {
-      // ---- ticket: the CTA finishing the last chunk of (seq, kv head, row tile) merges ----
+      // ---- ticket: the CTA that finishes the group's last segment combines all partials ----
       __threadfence();  // this thread's partial writes, visible device-wide before the ticket
       named_barrier_sync(1, kConsumerWarps * 32);
       if (ctid == 0) {
         __threadfence();
-        int32_t* ctr = p.counters + ((int64_t)d.seq * p.Hkv + d.kvh) * p.n_rg + d.rg;
+        int32_t* ctr = p.counters + seg.x;
         const int ticket = atomicAdd(ctr, 1);
-        const int last = (ticket == d.n_chunks - 1);
+        const int last = (ticket == n_seg - 1);
         if (last) *ctr = 0;  // ready for the next call on this workspace
         *flag = last;
       }
       named_barrier_sync(1, kConsumerWarps * 32);
       if (*flag) {
         __threadfence();
-        const float* pb = p.partials + (int64_t)(d.part_base + d.kvh * p.n_rg + d.rg) * kPartFloats;
-        const int64_t cstride = (int64_t)p.Hkv * p.n_rg * kPartFloats;
+        const float* pb = p.partials + (int64_t)first_part * kPartFloats;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int idx = ctid + 256 * e;
@@ -424,21 +431,20 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, int warp, int lan
           const int r = row0 + row;
           if (r >= rows_total) continue;
           float M = -INFINITY;
-          for (int c = 0; c < d.n_chunks; ++c) M = fmaxf(M, __ldcg(pb + c * cstride + kRows * 128 + row));
+          for (int c = 0; c < n_seg; ++c) M = fmaxf(M, __ldcg(pb + c * kPartFloats + kRows * 128 + row));
           float L = 0.f, O = 0.f;
-          for (int c = 0; c < d.n_chunks; ++c) {
-            const float* q = pb + c * cstride;
+          for (int c = 0; c < n_seg; ++c) {
+            const float* q = pb + c * kPartFloats;
             const float mc = __ldcg(q + kRows * 128 + row);
             const float f = (mc == -INFINITY) ? 0.f : fast_exp2((mc - M) * p.c2);
             L += f * __ldcg(q + kRows * 128 + kRows + row);
             O += f * __ldcg(q + row * 128 + dim);
           }
-          const int tok = r / p.G, hq = d.kvh * p.G + r % p.G;
-          if (L > 0.f) p.out[(((int64_t)d.seq * p.q_len + tok) * p.Hq + hq) * 128 + dim] = O / L;
+          if (L > 0.f) store_out(p, seq, kvh, r, dim, O / L);
         }
       }
     }
-    named_barrier_sync(1, kConsumerWarps * 32);  // merge area reused by the next item
+    named_barrier_sync(1, kConsumerWarps * 32);  // merge area reused by the next segment
   }
   if (timed_out && lane == 0) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
@@ -456,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   }
   __syncthreads();
   if (warp == kConsumerWarps) {
-    if (lane == 0) producer(p, smem);
+    producer(p, smem, lane);
     return;
   }
   consumer(p, smem, warp, lane);
@@ -469,11 +475,11 @@ int decode_smem_bytes() { return kSmemBytes; }
 cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const uint8_t* k_codes,
                           const uint8_t* k_scales, const uint8_t* v_codes,
                           const uint8_t* v_scales, const int32_t* block_table, int32_t max_pages,
-                          int32_t num_pages, const void* seqinfo, const void* items,
-                          int32_t* counters, float* partials, float* out, int32_t* status,
-                          int32_t Hq, int32_t Hkv, int32_t q_len, int32_t causal, int32_t n_rg,
-                          int32_t total_items, float sm_scale, int num_sms, cudaStream_t stream) {
-  static bool attr_done = false;  // per process; the attribute is per function, not per device
+                          int32_t num_pages, const void* groups, const void* segments,
+                          const int32_t* cta_seg, int32_t* counters, float* partials, float* out,
+                          int32_t* status, int32_t Hq, int32_t Hkv, int32_t q_len, int32_t causal,
+                          int32_t grid, float sm_scale, cudaStream_t stream) {
+  static bool attr_done = false;  // the attribute belongs to the function, set once per process
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
@@ -484,14 +490,13 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
   p.q_codes = q_codes; p.q_scales = q_scales;
   p.k_codes = k_codes; p.k_scales = k_scales; p.v_codes = v_codes; p.v_scales = v_scales;
   p.block_table = block_table; p.max_pages = max_pages; p.num_pages = num_pages;
-  p.seqinfo = reinterpret_cast<const int4*>(seqinfo);
-  p.items = reinterpret_cast<const int4*>(items);
+  p.groups = reinterpret_cast<const int4*>(groups);
+  p.segments = reinterpret_cast<const int4*>(segments);
+  p.cta_seg = cta_seg;
   p.counters = counters; p.partials = partials; p.out = out; p.status = status;
-  p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.q_len = q_len; p.causal = causal; p.n_rg = n_rg;
-  p.total_items = total_items;
+  p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.q_len = q_len; p.causal = causal;
   p.c2 = sm_scale * 1.4426950408889634f;
-  if (total_items <= 0) return cudaSuccess;
-  const int grid = total_items < num_sms ? total_items : num_sms;
+  if (grid <= 0) return cudaSuccess;
   decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }

@@ -72,20 +72,27 @@ typedef struct kv_nvfp4_layout {
   int32_t rot_dim;      /* 32 = 25 % of 128 [YaRN] */
 } kv_nvfp4_layout;
 
-/* Filled by kv_nvfp4_plan; passed unchanged to kv_nvfp4_decode_attn. */
+/* Filled by kv_nvfp4_plan; passed unchanged to kv_nvfp4_decode_attn. A group is one
+ * (sequence, kv head, tile of 8 query rows); its keys are split into chunks of chunk_pages
+ * pages, and the chunks of all groups are shared out over `grid` CTAs in contiguous, page-balanced
+ * ranges (one range may hold several chunks of a group, which the CTA combines as it goes). */
 typedef struct kv_nvfp4_plan_info {
   int32_t num_seqs;
   int32_t q_len;
-  int32_t chunk_pages;     /* split-K chunk, in pages */
-  int32_t num_chunks;      /* chunks summed over sequences */
-  int32_t num_row_groups;  /* ceil(group * q_len / 8): query-row tiles per (sequence, kv head) */
+  int32_t causal;          /* causal masking among the q_len new tokens (pages past the last
+                              visible key of a row tile are not visited) */
+  int32_t chunk_pages;     /* split-K granularity, in pages */
   int32_t num_kv_heads;
-  int32_t num_partials;    /* partial-result slots used by split sequences */
-  int32_t max_chunks;      /* largest chunk count of one sequence */
+  int32_t num_row_groups;  /* ceil(group * q_len / 8) row tiles per (sequence, kv head) */
+  int32_t num_groups;      /* num_seqs * num_kv_heads * num_row_groups */
+  int32_t num_segments;    /* contiguous (group, page range) pieces over all CTAs */
+  int32_t num_partials;    /* partial-result slots (segments of groups split over CTAs) */
+  int32_t grid;            /* CTAs of the attention launch, at most the SM count */
   int32_t max_seq_len;     /* longest sequence; must fit max_pages * 64 at attention time */
   int32_t reserved;
   int64_t total_kv_tokens; /* sum of seq_lens */
-  uint64_t off_seqinfo, off_items, off_counters, off_partials; /* byte offsets in workspace */
+  int64_t total_pages;     /* pages visited by one attention call, summed over groups */
+  uint64_t off_groups, off_segments, off_cta, off_counters, off_partials; /* byte offsets */
   uint64_t workspace_bytes;
 } kv_nvfp4_plan_info;
 
@@ -151,29 +158,40 @@ kv_nvfp4_status kv_nvfp4_append(const kv_nvfp4_layout *layout, const void *q, co
 
 /* ---- Page-table / split-K setup ------------------------------------------------------------
  * Sizes and builds the work list of one attention call from HOST sequence lengths (after the
- * append, i.e. including the q_len new tokens). Sequences are cut into chunks of chunk_tokens
- * keys (a positive multiple of 64; 1024 suits decode, a chunk as long as the sequence turns the
- * split off); each (chunk, kv head, tile of 8 query rows) is one work item, and the chunks of
- * one sequence are merged by a log-sum-exp combine. The workspace holds one partial result of
- * 4160 bytes per work item of every sequence that has more than one chunk. */
+ * append, i.e. including the q_len new tokens). chunk_tokens (a positive multiple of 64) is the
+ * split-K granularity: a sequence is only ever cut between chunks. 1024 suits long-context
+ * decode; 64 lets the plan balance the CTAs to the page. The workspace holds the group and
+ * segment tables, one int32 ticket per group, and one 4160-byte (m, l, O) partial per segment
+ * of every group that spans more than one CTA. */
 kv_nvfp4_status kv_nvfp4_plan_workspace_bytes(const kv_nvfp4_layout *layout,
                                               const int32_t *h_seq_lens, int32_t num_seqs,
-                                              int32_t q_len, int32_t chunk_tokens,
-                                              size_t *bytes);
+                                              int32_t q_len, int32_t causal,
+                                              int32_t chunk_tokens, size_t *bytes);
+
+/* Host-only variant of kv_nvfp4_plan for a given CTA count: writes the image of the workspace
+ * tables (groups, segments, per-CTA segment ranges, zeroed tickets; everything before
+ * info->off_partials) into HOST memory h_workspace and fills *info. No CUDA call. Layout of the
+ * image: groups are 8 int32 {seq, kv_head, row_tile, seq_len, n_segments, first_partial,
+ * pages, 0}; segments are 4 int32 {group, page_lo, page_hi, partial or -1}; CTA b owns
+ * segments [cta[b], cta[b+1]). */
+kv_nvfp4_status kv_nvfp4_plan_host(const kv_nvfp4_layout *layout, const int32_t *h_seq_lens,
+                                   int32_t num_seqs, int32_t q_len, int32_t causal,
+                                   int32_t chunk_tokens, int32_t num_ctas, void *h_workspace,
+                                   size_t ws_bytes, kv_nvfp4_plan_info *info);
 
 /* Writes the work list into DEVICE memory d_workspace (ws_bytes at least the size above) on
- * `stream`, zeroes the merge counters, and fills *info (HOST). Every seq_len must be >= q_len
- * and >= 1. */
+ * `stream`, zeroes the merge tickets, and fills *info (HOST). Every seq_len must be >= q_len
+ * and >= 1. The CTA count is taken from the current device's SM count. */
 kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout *layout, const int32_t *h_seq_lens,
-                              int32_t num_seqs, int32_t q_len, int32_t chunk_tokens,
-                              void *d_workspace, size_t ws_bytes, kv_nvfp4_plan_info *info,
-                              void *stream);
+                              int32_t num_seqs, int32_t q_len, int32_t causal,
+                              int32_t chunk_tokens, void *d_workspace, size_t ws_bytes,
+                              kv_nvfp4_plan_info *info, void *stream);
 
 /* ---- Paged GQA decode / speculative-verify attention [NVFP4: NVFP4 Q.K^T, V dequantised]
  * For every sequence s and each of its q_len query tokens i (position seq_len - q_len + i) and
  * every query head h (kv head h / (num_q_heads / num_kv_heads)):
  *   out = sum_t softmax_t(sm_scale * qhat . khat_t) * vhat_t
- * over keys t < seq_len, restricted to t <= seq_len - q_len + i when causal != 0, where qhat,
+ * over keys t < seq_len, restricted to t <= seq_len - q_len + i when the plan is causal, where qhat,
  * khat, vhat are the dequantised NVFP4 rows (code value times block scale). Scores and the
  * softmax run in fp32 with split-K over the plan's chunks.
  *   plan, d_workspace: from kv_nvfp4_plan (same stream)
@@ -184,7 +202,7 @@ kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout *layout, const int32_t *h_se
 kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout *layout,
                                      const kv_nvfp4_plan_info *plan, void *d_workspace,
                                      const uint8_t *q_codes, const uint8_t *q_scales,
-                                     int32_t causal, float sm_scale, const uint8_t *k_codes,
+                                     float sm_scale, const uint8_t *k_codes,
                                      const uint8_t *k_scales, const uint8_t *v_codes,
                                      const uint8_t *v_scales, int32_t num_pages,
                                      const int32_t *d_block_table, int32_t max_pages, float *out,

@@ -60,9 +60,8 @@ class GpuRun:
         self.cache.append(self.k, self.v, self.sid, self.pos, q=self.q, q_codes=self.q_codes,
                           q_scales=self.q_scales)
         if plan:
-            self.cache.plan(w.seq_lens, w.q_len, chunk_tokens or w.chunk_tokens)
-        self.cache.attend(self.q_codes, self.q_scales, self.out, causal=w.causal,
-                          sm_scale=w.sm_scale)
+            self.cache.plan(w.seq_lens, w.q_len, w.causal, chunk_tokens or w.chunk_tokens)
+        self.cache.attend(self.q_codes, self.q_scales, self.out, sm_scale=w.sm_scale)
 
     def status(self) -> int:
         return int(self.cache.status.item())

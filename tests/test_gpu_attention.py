@@ -63,7 +63,7 @@ def test_attention_skips_bad_pages_and_flags_them():
     # corrupt one entry of the block table, re-run attention only
     bt = g.cache.block_table
     bt[0, 2] = 10 ** 6
-    g.cache.attend(g.q_codes, g.q_scales, g.out, causal=True, sm_scale=w.sm_scale)
+    g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
     torch.cuda.synchronize()
     assert g.status() & kv.DEV_BAD_PAGE
     assert np.all(np.isfinite(g.output()))

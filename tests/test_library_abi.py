@@ -63,21 +63,22 @@ def test_rope_host_table_bit_identical_to_oracle(kv):
 
 def test_plan_sizes_and_validation(kv):
     L = kv.make_layout()
-    n = kv.kv_nvfp4_plan_workspace_bytes(L, [4097], 1, 1024)
+    n = kv.kv_nvfp4_plan_workspace_bytes(L, [4097], 1, True, 1024)
     assert n > 0
-    # 4 x 131073 tokens, 1024-token chunks: 129 chunks each, 4 heads, 1 row tile, 4160 B partials
-    n2 = kv.kv_nvfp4_plan_workspace_bytes(L, [131073] * 4, 1, 1024)
-    assert n2 >= 4 * 129 * 4 * 4160
+    # 4 x 131073 tokens, 16 groups spread over many CTAs: every group is split, one 4160 B
+    # partial per segment
+    n2 = kv.kv_nvfp4_plan_workspace_bytes(L, [131073] * 4, 1, True, 1024)
+    assert n2 >= 16 * 2 * 4160
     lib = kv.lib()
     sl = np.array([5, 3], np.int32)
     size = ctypes.c_size_t()
     # seq_len < q_len, chunk not a multiple of 64, null workspace: all rejected without CUDA
-    assert lib.kv_nvfp4_plan_workspace_bytes(ctypes.byref(L), sl.ctypes.data, 2, 4, 1024,
+    assert lib.kv_nvfp4_plan_workspace_bytes(ctypes.byref(L), sl.ctypes.data, 2, 4, 1, 1024,
                                              ctypes.byref(size)) == kv.KV_NVFP4_EINVAL
-    assert lib.kv_nvfp4_plan_workspace_bytes(ctypes.byref(L), sl.ctypes.data, 2, 1, 100,
+    assert lib.kv_nvfp4_plan_workspace_bytes(ctypes.byref(L), sl.ctypes.data, 2, 1, 1, 100,
                                              ctypes.byref(size)) == kv.KV_NVFP4_EINVAL
     info = kv.PlanInfo()
-    assert lib.kv_nvfp4_plan(ctypes.byref(L), sl.ctypes.data, 2, 1, 1024, None, 0,
+    assert lib.kv_nvfp4_plan(ctypes.byref(L), sl.ctypes.data, 2, 1, 1, 1024, None, 0,
                              ctypes.byref(info), None) == kv.KV_NVFP4_EINVAL
 
 
@@ -94,7 +95,58 @@ def test_entry_points_reject_bad_arguments_before_cuda(kv):
     assert lib.kv_nvfp4_append(ctypes.byref(L), *([None] * 5), 0, None, 1, None, 1, 1, 1,
                                *([None] * 8), None) == kv.KV_NVFP4_OK
     info = kv.PlanInfo()
-    assert lib.kv_nvfp4_decode_attn(ctypes.byref(L), ctypes.byref(info), None, None, None, 1,
+    assert lib.kv_nvfp4_decode_attn(ctypes.byref(L), ctypes.byref(info), None, None, None,
                                     0.0, None, None, None, None, 1, None, 1, None, None,
                                     None) == kv.KV_NVFP4_EINVAL
     assert kv.lib().kv_nvfp4_status_string(-1) == b"invalid argument"
+
+
+@pytest.mark.parametrize("lens,q_len,causal,chunk,ctas", [
+    ([131073] * 4, 1, True, 64, 152), ([131073] * 4, 1, True, 1024, 152),
+    ([5, 70, 1000, 200000], 1, True, 1024, 152), ([100008] * 4, 8, True, 1024, 152),
+    ([3], 1, True, 64, 152), ([600064], 8192, True, 64, 152), ([2000, 37], 8, False, 256, 7),
+])
+def test_plan_covers_every_visible_page_once_and_balances(kv, lens, q_len, causal, chunk, ctas):
+    L = kv.make_layout()
+    info, groups, segs, cta = kv.kv_nvfp4_plan_host(L, lens, q_len, causal, chunk, ctas)
+    G = 6
+    n_rg = (G * q_len + 7) // 8
+    assert info.num_groups == len(lens) * 4 * n_rg == len(groups)
+    # expected visited pages per group: up to the last key any row of the tile can see
+    gi = np.arange(len(groups))
+    s_, h_, rg_ = groups[:, 0], groups[:, 1], groups[:, 2]
+    assert np.array_equal(gi, (s_ * 4 + h_) * n_rg + rg_)
+    assert np.array_equal(groups[:, 3], np.asarray(lens)[s_])
+    last_row = np.minimum(G * q_len - 1, 8 * rg_ + 7)
+    vis = (groups[:, 3] - q_len + last_row // G + 1) if causal else groups[:, 3]
+    assert np.array_equal(groups[:, 6], (vis + 63) // 64)
+    # segments tile each group's [0, pages) exactly, in order, cut only at chunk boundaries
+    cp = chunk // 64
+    covered = {}
+    for g, lo, hi, part in segs:
+        assert lo < hi
+        assert lo % cp == 0 and (hi % cp == 0 or hi == groups[g][6])
+        covered.setdefault(g, []).append((lo, hi))
+    for gi, rngs in covered.items():
+        assert rngs[0][0] == 0 and rngs[-1][1] == groups[gi][6]
+        assert all(a[1] == b[0] for a, b in zip(rngs, rngs[1:]))
+        assert len(rngs) == groups[gi][4]
+    assert set(covered) == set(range(info.num_groups))
+    # CTA ranges are contiguous; per-CTA load within one chunk of the mean
+    assert cta[0] == 0 and cta[-1] == info.num_segments and np.all(np.diff(cta) >= 0)
+    seg_pages = (segs[:, 2] - segs[:, 1]).astype(np.int64)
+    csum = np.concatenate([[0], np.cumsum(seg_pages)])
+    load = csum[cta[1:]] - csum[cta[:-1]]
+    assert load.sum() == info.total_pages
+    mean = info.total_pages / info.grid
+    assert load.max() <= mean + cp + 1
+    # partial slots: split groups get contiguous slots, unsplit groups none
+    by_group = {}
+    for seg in segs:
+        by_group.setdefault(int(seg[0]), []).append(int(seg[3]))
+    for gi, (s, h, rg, ln, nseg, fp, pages, _) in enumerate(groups):
+        parts = by_group[gi]
+        if nseg > 1:
+            assert parts == list(range(fp, fp + nseg))
+        else:
+            assert parts == [-1]
