@@ -16,9 +16,10 @@
 // Per CTA: warp 8 is the producer; lane 0 streams every page of the CTA's segments into a
 // 16-slot shared-memory ring with bulk async copies (K codes 4 KiB, K scales 512 B, V codes
 // 4 KiB, V scales 512 B per page and head), each slot guarded by a full and an empty mbarrier.
-// Warps 0..7 consume the segment's pages round-robin.
+// Warps 0..11 consume: three groups of four warps take the segment's pages round-robin, and the
+// four warps of a group split a page into 16-key sub-tiles (empty barrier count 4).
 //
-// Per page and warp, the product runs on the warp-level tensor path with keys as the M
+// Per 16-key sub-tile and warp, the product runs on the warp-level tensor path with keys as the M
 // dimension (16 keys per MMA) and the 8 query rows as N:
 //   S^T[key][row] = sum_d Khat[key][d] Qhat[row][d]        (8 x m16n8k16, k = 16 dims per step)
 //   O^T[dim][row] += sum_key Vhat^T[dim][key] P^T[key][row] (8 m-tiles of 16 dims)
@@ -29,7 +30,7 @@
 // dims (the same one for both operands), chosen so that each thread reads contiguous bytes.
 //
 // Softmax: running max per row, exp2 with log2(e) folded into the scale, rescale of the
-// accumulator only when the max grows. At the end of a segment the 8 warps' states are merged
+// accumulator only when the max grows. At the end of a segment the 12 warps' states are merged
 // in shared memory; merging never waits on another CTA.
 
 #include <cstdint>
@@ -41,7 +42,8 @@ namespace kvnvfp4 {
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kGroups = 3;                     // pages processed concurrently per CTA
+constexpr int kConsumerWarps = 4 * kGroups;     // four warps (16-key sub-tiles) per page
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kSlots = 16;
 constexpr int kKcOff = 0, kKsOff = 4096, kVcOff = 4608, kVsOff = 8704;
@@ -144,15 +146,15 @@ struct WarpState {
   uint32_t qf[8][2];  // Q B-fragments for k-steps 0..7
 };
 
-__device__ __forceinline__ void process_page(WarpState& st, uint32_t slot_addr, int kp0, int len,
-                                             int lim0, int lim1, float c2, int g, int t) {
+__device__ __forceinline__ void process_subtile(WarpState& st, uint32_t slot_addr, int sub, int kp0,
+                                                int len, int lim0, int lim1, float c2, int g,
+                                                int t) {
   const uint32_t kc = slot_addr + kKcOff, ks = slot_addr + kKsOff;
   const uint32_t vc = slot_addr + kVcOff, vs = slot_addr + kVsOff;
 
-  // ---- scores: S^T for 4 sub-tiles of 16 keys ----
-  float S[4][4];
-#pragma unroll
-  for (int sub = 0; sub < 4; ++sub) {
+  // ---- scores S^T for keys 16*sub .. 16*sub+15 of the page ----
+  float S[4] = {0.f, 0.f, 0.f, 0.f};
+  {
     const int ka = 16 * sub + g, kb = ka + 8;
     const uint4 ca = lds128(kc + ka * 64 + 16 * t);
     const uint4 cb = lds128(kc + kb * 64 + 16 * t);
@@ -163,9 +165,10 @@ __device__ __forceinline__ void process_page(WarpState& st, uint32_t slot_addr, 
     const uint32_t sah = cvt_e4m3x2_f16(sa), sbh = cvt_e4m3x2_f16(sb);
     const uint32_t sa0 = dup_lo(sah), sa1 = dup_hi(sah);
     const uint32_t sb0 = dup_lo(sbh), sb1 = dup_hi(sbh);
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
     const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
     const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
+    // two independent accumulators (even / odd k-steps) halve the MMA dependency chain
+    float c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
@@ -174,24 +177,22 @@ __device__ __forceinline__ void process_page(WarpState& st, uint32_t slot_addr, 
       const uint32_t sA = (w < 2) ? sa0 : sa1;  // bytes 0..7 of the 16 -> block 2t, 8..15 -> 2t+1
       const uint32_t sB = (w < 2) ? sb0 : sb1;
       // step s = 2w uses bytes (0,1) of word w, step 2w+1 bytes (2,3)
-      mma_f16_16816(c, hmul2(a0, sA), hmul2(b0, sB), hmul2(a1, sA), hmul2(b1, sB),
+      mma_f16_16816(S, hmul2(a0, sA), hmul2(b0, sB), hmul2(a1, sA), hmul2(b1, sB),
                     st.qf[2 * w][0], st.qf[2 * w][1]);
-      mma_f16_16816(c, hmul2(a2, sA), hmul2(b2, sB), hmul2(a3, sA), hmul2(b3, sB),
+      mma_f16_16816(c1, hmul2(a2, sA), hmul2(b2, sB), hmul2(a3, sA), hmul2(b3, sB),
                     st.qf[2 * w + 1][0], st.qf[2 * w + 1][1]);
     }
-    S[sub][0] = c[0]; S[sub][1] = c[1]; S[sub][2] = c[2]; S[sub][3] = c[3];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) S[e] += c1[e];
   }
 
-  // ---- online softmax over this page ----
+  // ---- online softmax over these 16 keys ----
+  const int kpa = kp0 + 16 * sub + g, kpb = kpa + 8;
   float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-  for (int sub = 0; sub < 4; ++sub) {
-    const int kpa = kp0 + 16 * sub + g, kpb = kpa + 8;
-    if (kpa <= lim0) mx0 = fmaxf(mx0, S[sub][0]);
-    if (kpa <= lim1) mx1 = fmaxf(mx1, S[sub][1]);
-    if (kpb <= lim0) mx0 = fmaxf(mx0, S[sub][2]);
-    if (kpb <= lim1) mx1 = fmaxf(mx1, S[sub][3]);
-  }
+  if (kpa <= lim0) mx0 = S[0];
+  if (kpa <= lim1) mx1 = S[1];
+  if (kpb <= lim0) mx0 = fmaxf(mx0, S[2]);
+  if (kpb <= lim1) mx1 = fmaxf(mx1, S[3]);
 #pragma unroll
   for (int m = 4; m < 32; m <<= 1) {
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, m));
@@ -211,66 +212,60 @@ __device__ __forceinline__ void process_page(WarpState& st, uint32_t slot_addr, 
     st.l[1] *= alpha;
     st.m[1] = mx1;
   }
-  const float m0 = st.m[0], m1 = st.m[1];
+  const float p0 = (kpa <= lim0) ? fast_exp2((S[0] - st.m[0]) * c2) : 0.f;
+  const float p1 = (kpa <= lim1) ? fast_exp2((S[1] - st.m[1]) * c2) : 0.f;
+  const float p2 = (kpb <= lim0) ? fast_exp2((S[2] - st.m[0]) * c2) : 0.f;
+  const float p3 = (kpb <= lim1) ? fast_exp2((S[3] - st.m[1]) * c2) : 0.f;
+  st.l[0] += p0 + p2;
+  st.l[1] += p1 + p3;
+  // P as f16 hi + lo, transposed into the B layout (keys along k)
+  const uint32_t h01 = pack_f16x2(p0, p1);
+  const uint32_t h23 = pack_f16x2(p2, p3);
+  const uint32_t l01 = pack_f16x2(p0 - f16_lo_to_f32(h01), p1 - f16_hi_to_f32(h01));
+  const uint32_t l23 = pack_f16x2(p2 - f16_lo_to_f32(h23), p3 - f16_hi_to_f32(h23));
+  const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+  const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
 
+  // ---- V^T fragments: keys (2t, 2t+1) and (2t+8, 2t+9) of the sub-tile, dims of block g ----
+  const int v0 = 16 * sub + 2 * t;
+  const uint2 w0 = lds64(vc + v0 * 64 + 8 * g);
+  const uint2 w1 = lds64(vc + (v0 + 1) * 64 + 8 * g);
+  const uint2 w2 = lds64(vc + (v0 + 8) * 64 + 8 * g);
+  const uint2 w3 = lds64(vc + (v0 + 9) * 64 + 8 * g);
+  uint32_t s0 = lds8(vs + v0 * 8 + g), s1 = lds8(vs + (v0 + 1) * 8 + g);
+  uint32_t s2 = lds8(vs + (v0 + 8) * 8 + g), s3 = lds8(vs + (v0 + 9) * 8 + g);
+  if (kp0 + v0 >= len) s0 = 0;
+  if (kp0 + v0 + 1 >= len) s1 = 0;
+  if (kp0 + v0 + 8 >= len) s2 = 0;
+  if (kp0 + v0 + 9 >= len) s3 = 0;
+  const uint32_t sp01 = cvt_e4m3x2_f16(s0 | (s1 << 8));
+  const uint32_t sp23 = cvt_e4m3x2_f16(s2 | (s3 << 8));
+  // interleave the nibbles of two keys: byte k of `e` = (dim 2k of key b) << 4 | (dim 2k of
+  // key a); `o` likewise for dim 2k+1
+  const uint32_t e0 = (w0.x & 0x0F0F0F0Fu) | ((w1.x & 0x0F0F0F0Fu) << 4);
+  const uint32_t o0 = ((w0.x >> 4) & 0x0F0F0F0Fu) | (w1.x & 0xF0F0F0F0u);
+  const uint32_t e1 = (w0.y & 0x0F0F0F0Fu) | ((w1.y & 0x0F0F0F0Fu) << 4);
+  const uint32_t o1 = ((w0.y >> 4) & 0x0F0F0F0Fu) | (w1.y & 0xF0F0F0F0u);
+  const uint32_t e2 = (w2.x & 0x0F0F0F0Fu) | ((w3.x & 0x0F0F0F0Fu) << 4);
+  const uint32_t o2 = ((w2.x >> 4) & 0x0F0F0F0Fu) | (w3.x & 0xF0F0F0F0u);
+  const uint32_t e3 = (w2.y & 0x0F0F0F0Fu) | ((w3.y & 0x0F0F0F0Fu) << 4);
+  const uint32_t o3 = ((w2.y >> 4) & 0x0F0F0F0Fu) | (w3.y & 0xF0F0F0F0u);
+  // D01[j] = (Vhat[key v0][16g+j], Vhat[key v0+1][16g+j]) for j = 0..15, likewise D23
+  uint32_t D01[16], D23[16];
+  cvt_e2m1x8_f16(e0, D01[0], D01[2], D01[4], D01[6]);
+  cvt_e2m1x8_f16(o0, D01[1], D01[3], D01[5], D01[7]);
+  cvt_e2m1x8_f16(e1, D01[8], D01[10], D01[12], D01[14]);
+  cvt_e2m1x8_f16(o1, D01[9], D01[11], D01[13], D01[15]);
+  cvt_e2m1x8_f16(e2, D23[0], D23[2], D23[4], D23[6]);
+  cvt_e2m1x8_f16(o2, D23[1], D23[3], D23[5], D23[7]);
+  cvt_e2m1x8_f16(e3, D23[8], D23[10], D23[12], D23[14]);
+  cvt_e2m1x8_f16(o3, D23[9], D23[11], D23[13], D23[15]);
 #pragma unroll
-  for (int sub = 0; sub < 4; ++sub) {
-    const int kpa = kp0 + 16 * sub + g, kpb = kpa + 8;
-    const float p0 = (kpa <= lim0) ? fast_exp2((S[sub][0] - m0) * c2) : 0.f;
-    const float p1 = (kpa <= lim1) ? fast_exp2((S[sub][1] - m1) * c2) : 0.f;
-    const float p2 = (kpb <= lim0) ? fast_exp2((S[sub][2] - m0) * c2) : 0.f;
-    const float p3 = (kpb <= lim1) ? fast_exp2((S[sub][3] - m1) * c2) : 0.f;
-    st.l[0] += p0 + p2;
-    st.l[1] += p1 + p3;
-    // P as f16 hi + lo, transposed into the B layout (keys along k)
-    const uint32_t h01 = pack_f16x2(p0, p1);
-    const uint32_t h23 = pack_f16x2(p2, p3);
-    const uint32_t l01 = pack_f16x2(p0 - f16_lo_to_f32(h01), p1 - f16_hi_to_f32(h01));
-    const uint32_t l23 = pack_f16x2(p2 - f16_lo_to_f32(h23), p3 - f16_hi_to_f32(h23));
-    const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-    const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-
-    // ---- V^T fragments: keys (2t, 2t+1) and (2t+8, 2t+9), dims of block g ----
-    const int v0 = 16 * sub + 2 * t;
-    const uint2 w0 = lds64(vc + v0 * 64 + 8 * g);
-    const uint2 w1 = lds64(vc + (v0 + 1) * 64 + 8 * g);
-    const uint2 w2 = lds64(vc + (v0 + 8) * 64 + 8 * g);
-    const uint2 w3 = lds64(vc + (v0 + 9) * 64 + 8 * g);
-    uint32_t s0 = lds8(vs + v0 * 8 + g), s1 = lds8(vs + (v0 + 1) * 8 + g);
-    uint32_t s2 = lds8(vs + (v0 + 8) * 8 + g), s3 = lds8(vs + (v0 + 9) * 8 + g);
-    if (kp0 + v0 >= len) s0 = 0;
-    if (kp0 + v0 + 1 >= len) s1 = 0;
-    if (kp0 + v0 + 8 >= len) s2 = 0;
-    if (kp0 + v0 + 9 >= len) s3 = 0;
-    const uint32_t sp01 = cvt_e4m3x2_f16(s0 | (s1 << 8));
-    const uint32_t sp23 = cvt_e4m3x2_f16(s2 | (s3 << 8));
-    // interleave the nibbles of two keys: byte k of `ev` = (dim 2k of key b) << 4 | (dim 2k of
-    // key a); `od` likewise for dim 2k+1
-    const uint32_t e0 = (w0.x & 0x0F0F0F0Fu) | ((w1.x & 0x0F0F0F0Fu) << 4);
-    const uint32_t o0 = ((w0.x >> 4) & 0x0F0F0F0Fu) | (w1.x & 0xF0F0F0F0u);
-    const uint32_t e1 = (w0.y & 0x0F0F0F0Fu) | ((w1.y & 0x0F0F0F0Fu) << 4);
-    const uint32_t o1 = ((w0.y >> 4) & 0x0F0F0F0Fu) | (w1.y & 0xF0F0F0F0u);
-    const uint32_t e2 = (w2.x & 0x0F0F0F0Fu) | ((w3.x & 0x0F0F0F0Fu) << 4);
-    const uint32_t o2 = ((w2.x >> 4) & 0x0F0F0F0Fu) | (w3.x & 0xF0F0F0F0u);
-    const uint32_t e3 = (w2.y & 0x0F0F0F0Fu) | ((w3.y & 0x0F0F0F0Fu) << 4);
-    const uint32_t o3 = ((w2.y >> 4) & 0x0F0F0F0Fu) | (w3.y & 0xF0F0F0F0u);
-    // D01[j] = (Vhat[key v0][16g+j], Vhat[key v0+1][16g+j]) for j = 0..15, likewise D23
-    uint32_t D01[16], D23[16];
-    cvt_e2m1x8_f16(e0, D01[0], D01[2], D01[4], D01[6]);
-    cvt_e2m1x8_f16(o0, D01[1], D01[3], D01[5], D01[7]);
-    cvt_e2m1x8_f16(e1, D01[8], D01[10], D01[12], D01[14]);
-    cvt_e2m1x8_f16(o1, D01[9], D01[11], D01[13], D01[15]);
-    cvt_e2m1x8_f16(e2, D23[0], D23[2], D23[4], D23[6]);
-    cvt_e2m1x8_f16(o2, D23[1], D23[3], D23[5], D23[7]);
-    cvt_e2m1x8_f16(e3, D23[8], D23[10], D23[12], D23[14]);
-    cvt_e2m1x8_f16(o3, D23[9], D23[11], D23[13], D23[15]);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t a0 = hmul2(D01[i], sp01), a1 = hmul2(D01[8 + i], sp01);
-      const uint32_t a2 = hmul2(D23[i], sp23), a3 = hmul2(D23[8 + i], sp23);
-      mma_f16_16816(st.o[i], a0, a1, a2, a3, bh0, bh1);
-      mma_f16_16816(st.o[i], a0, a1, a2, a3, bl0, bl1);
-    }
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t a0 = hmul2(D01[i], sp01), a1 = hmul2(D01[8 + i], sp01);
+    const uint32_t a2 = hmul2(D23[i], sp23), a3 = hmul2(D23[8 + i], sp23);
+    mma_f16_16816(st.o[i], a0, a1, a2, a3, bh0, bh1);
+    mma_f16_16816(st.o[i], a0, a1, a2, a3, bl0, bl1);
   }
 }
 
@@ -287,7 +282,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, int warp, int lan
   const volatile int32_t* slot_pid = reinterpret_cast<const volatile int32_t*>(smem + kSlotPidOff);
   float* mrg = reinterpret_cast<float*>(smem + kMergeOff);
   volatile int* flag = reinterpret_cast<volatile int*>(smem + kFlagOff);
-  const int ctid = warp * 32 + lane;  // 0 .. 255 over consumer threads
+  const int ctid = warp * 32 + lane;  // consumer thread index
   const int rows_total = p.G * p.q_len;
   uint32_t kbase = 0;
   bool timed_out = false;
@@ -338,16 +333,18 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, int warp, int lan
         st.qf[2 * w + 1][1] = hmul2(a3, sc);
       }
     }
-    // pages of this segment: warp w takes pages w, w + 8, ...
+    // pages of this segment: warp group q = warp / 4 takes pages q, q + kGroups, ...; the four
+    // warps of a group split each page into four 16-key sub-tiles
     const int n_pages = seg.z - seg.y;
-    for (int j = warp; j < n_pages; j += kConsumerWarps) {
+    const int grp = warp >> 2, sub = warp & 3;
+    for (int j = grp; j < n_pages; j += kGroups) {
       const uint32_t k = kbase + j;
       const uint32_t slot = k % kSlots;
       if (!mbar_wait_bounded(bars + 8 * slot, (k / kSlots) & 1)) timed_out = true;
       if (slot_pid[slot] >= 0) {
         const int kp0 = (seg.y + j) * kPage;
-        process_page(st, ring + slot * kSlotBytes, kp0, len, lim[0], lim[1], p.c2, g, t);
-      } else if (lane == 0) {
+        process_subtile(st, ring + slot * kSlotBytes, sub, kp0, len, lim[0], lim[1], p.c2, g, t);
+      } else if (lane == 0 && sub == 0) {
         flag_status(p.status, KV_NVFP4_DEV_BAD_PAGE);
       }
       __syncwarp();
@@ -355,7 +352,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, int warp, int lan
     }
     kbase += n_pages;
 
-    // ---- merge the 8 warps' states in shared memory ----
+    // ---- merge the consumer warps' states in shared memory ----
     float l0 = st.l[0], l1 = st.l[1];
 #pragma unroll
     for (int m = 4; m < 32; m <<= 1) {
@@ -379,9 +376,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, int warp, int lan
 
     const bool split = n_seg > 1;
     float* part = split ? p.partials + (int64_t)seg.w * kPartFloats : nullptr;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int idx = ctid + 256 * e;   // (row, dim): row = idx / 128
+    for (int idx = ctid; idx < kRows * 128; idx += kConsumerWarps * 32) {  // (row, dim)
       const int row = idx >> 7, dim = idx & 127;
       float M = -INFINITY;
 #pragma unroll
@@ -424,9 +419,7 @@ __device__ void consumer(const DecodeParams& p, uint8_t* smem, int warp, int lan
       if (*flag) {
         __threadfence();
         const float* pb = p.partials + (int64_t)first_part * kPartFloats;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int idx = ctid + 256 * e;
+        for (int idx = ctid; idx < kRows * 128; idx += kConsumerWarps * 32) {
           const int row = idx >> 7, dim = idx & 127;
           const int r = row0 + row;
           if (r >= rows_total) continue;
@@ -456,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     const uint32_t bars = smem_u32(smem + kBarOff);
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(bars + 8 * s, 1);
-      mbar_init(bars + 8 * (kSlots + s), 1);
+      mbar_init(bars + 8 * (kSlots + s), 4);  // released by the page's four warps
     }
     fence_mbar_init();
   }
