@@ -13,7 +13,7 @@
 // at the end of a segment it writes either the final rows (the group lies in one CTA) or one
 // (m, l, O) partial, and the CTA that takes the group's last ticket combines its partials.
 //
-// Per CTA: warp 8 is the producer; lane 0 streams every page of the CTA's segments into a
+// Per CTA: the last warp is the producer; lane 0 streams every page of the CTA's segments into a
 // 16-slot shared-memory ring with bulk async copies (K codes 4 KiB, K scales 512 B, V codes
 // 4 KiB, V scales 512 B per page and head), each slot guarded by a full and an empty mbarrier.
 // Warps 0..11 consume: three groups of four warps take the segment's pages round-robin, and the
