@@ -53,13 +53,13 @@ _SIG = {
     "kv_nvfp4_version": ([], _I32),
     "kv_nvfp4_layout_check": ([ctypes.POINTER(Layout)], _I32),
     "kv_nvfp4_page_bytes": ([ctypes.POINTER(Layout)], ctypes.c_size_t),
-    "kv_nvfp4_pool_plane_bytes": ([ctypes.POINTER(Layout), _I32, ctypes.POINTER(ctypes.c_size_t),
-                                   ctypes.POINTER(ctypes.c_size_t)], _I32),
+    "kv_nvfp4_pool_bytes": ([ctypes.POINTER(Layout), _I32, ctypes.POINTER(ctypes.c_size_t)],
+                            _I32),
     "kv_nvfp4_rope_table_bytes": ([_I32, _I32], ctypes.c_size_t),
     "kv_nvfp4_rope_table_fill_host": ([_P, _I32, _I32, _F64, _F64], _I32),
     "kv_nvfp4_rope_table_init": ([_P, _I32, _I32, _F64, _F64, _P], _I32),
     "kv_nvfp4_append": ([ctypes.POINTER(Layout), _P, _P, _P, _P, _P, _I32, _P, _I32, _P, _I32,
-                         _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P], _I32),
+                         _I32, _I32, _P, _P, _P, _P, _P], _I32),
     "kv_nvfp4_plan_workspace_bytes": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32,
                                        ctypes.POINTER(ctypes.c_size_t)], _I32),
     "kv_nvfp4_plan": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32, _P, ctypes.c_size_t,
@@ -67,7 +67,7 @@ _SIG = {
     "kv_nvfp4_plan_host": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32, _I32, _P,
                             ctypes.c_size_t, ctypes.POINTER(PlanInfo)], _I32),
     "kv_nvfp4_decode_attn": ([ctypes.POINTER(Layout), ctypes.POINTER(PlanInfo), _P, _P, _P,
-                              ctypes.c_float, _P, _P, _P, _P, _I32, _P, _I32, _P, _P, _P], _I32),
+                              ctypes.c_float, _P, _I32, _P, _I32, _P, _P, _P], _I32),
 }
 
 _lib = None
@@ -138,11 +138,11 @@ def kv_nvfp4_page_bytes(layout: Layout) -> int:
     return int(lib().kv_nvfp4_page_bytes(ctypes.byref(layout)))
 
 
-def kv_nvfp4_pool_plane_bytes(layout: Layout, num_pages: int):
-    c, s = ctypes.c_size_t(), ctypes.c_size_t()
-    _check(lib().kv_nvfp4_pool_plane_bytes(ctypes.byref(layout), num_pages, ctypes.byref(c),
-                                           ctypes.byref(s)), "kv_nvfp4_pool_plane_bytes")
-    return c.value, s.value
+def kv_nvfp4_pool_bytes(layout: Layout, num_pages: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().kv_nvfp4_pool_bytes(ctypes.byref(layout), num_pages, ctypes.byref(n)),
+           "kv_nvfp4_pool_bytes")
+    return n.value
 
 
 def kv_nvfp4_rope_table_bytes(max_pos: int, rot_dim: int) -> int:
@@ -160,13 +160,13 @@ def kv_nvfp4_rope_table_init(d_table, max_pos, rot_dim, theta, pos_scale, stream
 
 
 def kv_nvfp4_append(layout, q, k, v, seq_ids, positions, T, rope_table, rope_max_pos,
-                    block_table, num_seqs, max_pages, num_pages, k_codes, k_scales, v_codes,
-                    v_scales, q_codes=None, q_scales=None, status=None, stream=None):
+                    block_table, num_seqs, max_pages, num_pages, pool, q_codes=None,
+                    q_scales=None, status=None, stream=None):
     _check(lib().kv_nvfp4_append(
         ctypes.byref(layout), _ptr(q), _ptr(k), _ptr(v), _ptr(seq_ids), _ptr(positions), T,
         _ptr(rope_table), rope_max_pos, _ptr(block_table), num_seqs, max_pages, num_pages,
-        _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), _ptr(q_codes),
-        _ptr(q_scales), _ptr(status), _stream(stream)), "kv_nvfp4_append")
+        _ptr(pool), _ptr(q_codes), _ptr(q_scales), _ptr(status), _stream(stream)),
+        "kv_nvfp4_append")
 
 
 def kv_nvfp4_plan_workspace_bytes(layout, seq_lens, q_len, causal, chunk_tokens) -> int:
@@ -214,14 +214,12 @@ def kv_nvfp4_plan_host(layout, seq_lens, q_len, causal, chunk_tokens, num_ctas):
     return info, groups.copy(), segs.copy(), cta.copy()
 
 
-def kv_nvfp4_decode_attn(layout, plan: PlanInfo, workspace, q_codes, q_scales, sm_scale,
-                         k_codes, k_scales, v_codes, v_scales, num_pages, block_table, max_pages,
-                         out, status=None, stream=None):
+def kv_nvfp4_decode_attn(layout, plan: PlanInfo, workspace, q_codes, q_scales, sm_scale, pool,
+                         num_pages, block_table, max_pages, out, status=None, stream=None):
     _check(lib().kv_nvfp4_decode_attn(
         ctypes.byref(layout), ctypes.byref(plan), _ptr(workspace), _ptr(q_codes), _ptr(q_scales),
-        float(sm_scale), _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales), num_pages,
-        _ptr(block_table), max_pages, _ptr(out), _ptr(status), _stream(stream)),
-        "kv_nvfp4_decode_attn")
+        float(sm_scale), _ptr(pool), num_pages, _ptr(block_table), max_pages, _ptr(out),
+        _ptr(status), _stream(stream)), "kv_nvfp4_decode_attn")
 
 
 from .cache import PagedNVFP4Cache  # noqa: E402  (device buffers for one layer, allocated by torch)

@@ -10,24 +10,20 @@ import numpy as np
 import torch
 
 from . import (kv_nvfp4_append, kv_nvfp4_decode_attn, kv_nvfp4_plan,
-               kv_nvfp4_plan_workspace_bytes, kv_nvfp4_pool_plane_bytes,
-               kv_nvfp4_rope_table_init, make_layout)
+               kv_nvfp4_plan_workspace_bytes, kv_nvfp4_pool_bytes, kv_nvfp4_rope_table_init,
+               make_layout)
 
 
 class PagedNVFP4Cache:
-    """Pool planes, block table, RoPE table and status word for one layer on one GPU."""
+    """Page pool, block table, RoPE table and status word for one layer on one GPU."""
 
     def __init__(self, num_pages, block_table, max_pos, num_q_heads=24, num_kv_heads=4,
                  rot_dim=32, theta=1e7, pos_scale=1.0, device="cuda"):
         self.layout = make_layout(num_q_heads, num_kv_heads, 128, 64, rot_dim)
         self.device = torch.device(device)
         self.num_pages = int(num_pages)
-        cb, sb = kv_nvfp4_pool_plane_bytes(self.layout, self.num_pages)
-        u8 = dict(dtype=torch.uint8, device=self.device)
-        self.k_codes = torch.empty(cb, **u8)
-        self.k_scales = torch.empty(sb, **u8)
-        self.v_codes = torch.empty(cb, **u8)
-        self.v_scales = torch.empty(sb, **u8)
+        self.pool = torch.empty(kv_nvfp4_pool_bytes(self.layout, self.num_pages),
+                                dtype=torch.uint8, device=self.device)
         bt = np.ascontiguousarray(block_table, np.int32)
         self.num_seqs, self.max_pages = bt.shape
         self.block_table = torch.from_numpy(bt).to(self.device)
@@ -46,8 +42,7 @@ class PagedNVFP4Cache:
         T = int(k.shape[0])
         kv_nvfp4_append(self.layout, q, k, v, seq_ids, positions, T, self.rope, self.max_pos,
                         self.block_table, self.num_seqs, self.max_pages, self.num_pages,
-                        self.k_codes, self.k_scales, self.v_codes, self.v_scales, q_codes,
-                        q_scales, self.status, stream)
+                        self.pool, q_codes, q_scales, self.status, stream)
 
     def quantized_q_buffers(self, T):
         H = self.layout.num_q_heads
@@ -67,6 +62,5 @@ class PagedNVFP4Cache:
         if sm_scale is None:
             sm_scale = 1.0 / math.sqrt(128)
         kv_nvfp4_decode_attn(self.layout, self.plan_info, self.workspace, q_codes, q_scales,
-                             sm_scale, self.k_codes, self.k_scales, self.v_codes, self.v_scales,
-                             self.num_pages, self.block_table, self.max_pages, out, self.status,
-                             stream)
+                             sm_scale, self.pool, self.num_pages, self.block_table, self.max_pages,
+                             out, self.status, stream)

@@ -16,23 +16,22 @@ cudaError_t launch_append(const uint16_t* q, const uint16_t* k, const uint16_t* 
                           const int32_t* seq_ids, const int32_t* positions, int64_t T,
                           const float* rope, int32_t rope_max_pos, int32_t rot_dim,
                           const int32_t* block_table, int32_t num_seqs, int32_t max_pages,
-                          int32_t num_pages, uint8_t* k_codes, uint8_t* k_scales,
-                          uint8_t* v_codes, uint8_t* v_scales, uint8_t* q_codes,
+                          int32_t num_pages, uint8_t* pool, uint8_t* q_codes,
                           uint8_t* q_scales, int32_t Hq, int32_t Hkv, int32_t* status,
                           cudaStream_t stream);
-cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const uint8_t* k_codes,
-                          const uint8_t* k_scales, const uint8_t* v_codes,
-                          const uint8_t* v_scales, const int32_t* block_table, int32_t max_pages,
-                          int32_t num_pages, const void* groups, const void* segments,
-                          const int32_t* cta_seg, int32_t* counters, float* partials, float* out,
-                          int32_t* status, int32_t Hq, int32_t Hkv, int32_t q_len, int32_t causal,
-                          int32_t grid, float sm_scale, cudaStream_t stream);
+cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const uint8_t* pool,
+                          const int32_t* block_table, int32_t max_pages, int32_t num_pages,
+                          const void* groups, const void* segments, const int32_t* cta_seg,
+                          int32_t* counters, float* partials, float* out, int32_t* status,
+                          int32_t Hq, int32_t Hkv, int32_t q_len, int32_t causal, int32_t grid,
+                          float sm_scale, cudaStream_t stream);
 }  // namespace kvnvfp4
 
 namespace {
 
-constexpr int kRowsPerItem = 8;   // query rows per attention work group
-constexpr int kPartFloats = kRowsPerItem * 128 + 2 * kRowsPerItem;
+constexpr int kRowsPerItem = 8;   // query rows per KV head in one attention work group
+constexpr int kPartHeadFloats = kRowsPerItem * 128 + 2 * kRowsPerItem;  // O[8][128], m[8], l[8]
+constexpr int kMaxAttnKvHeads = 4;  // the attention kernel stages every head of a page
 constexpr int kMaxGridForSizing = 1024;  // workspace sizing when no device is visible
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -71,7 +70,7 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
   const int64_t rows = (int64_t)G * q_len;
   const int64_t n_rg = (rows + kRowsPerItem - 1) / kRowsPerItem;
   const int32_t chunk_pages = chunk_tokens / P;
-  const int64_t n_groups = (int64_t)num_seqs * L->num_kv_heads * n_rg;
+  const int64_t n_groups = (int64_t)num_seqs * n_rg;
   if (n_groups > (1 << 26)) return KV_NVFP4_EINVAL;
   int64_t total_pages = 0, total_chunks = 0, total_tok = 0, max_len = 0;
   std::vector<int32_t> gpages((size_t)n_groups);
@@ -80,18 +79,16 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
     if (len < q_len || len < 1) return KV_NVFP4_EINVAL;
     total_tok += len;
     if (len > max_len) max_len = len;
-    for (int32_t h = 0; h < L->num_kv_heads; ++h) {
-      for (int64_t rg = 0; rg < n_rg; ++rg) {
-        int64_t vis = len;  // keys any row of the tile can see
-        if (causal) {
-          const int64_t last_row = std::min<int64_t>(rows - 1, rg * kRowsPerItem + kRowsPerItem - 1);
-          vis = (int64_t)(len - q_len) + last_row / G + 1;
-        }
-        const int64_t pages = (vis + P - 1) / P;
-        gpages[(size_t)(((int64_t)s * L->num_kv_heads + h) * n_rg + rg)] = (int32_t)pages;
-        total_pages += pages;
-        total_chunks += (pages + chunk_pages - 1) / chunk_pages;
+    for (int64_t rg = 0; rg < n_rg; ++rg) {
+      int64_t vis = len;  // keys any row of the tile can see
+      if (causal) {
+        const int64_t last_row = std::min<int64_t>(rows - 1, rg * kRowsPerItem + kRowsPerItem - 1);
+        vis = (int64_t)(len - q_len) + last_row / G + 1;
       }
+      const int64_t pages = (vis + P - 1) / P;
+      gpages[(size_t)((int64_t)s * n_rg + rg)] = (int32_t)pages;
+      total_pages += pages;
+      total_chunks += (pages + chunk_pages - 1) / chunk_pages;
     }
   }
   const int64_t grid = std::min<int64_t>(num_sms, total_chunks);
@@ -139,9 +136,9 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
     }
   }
   for (int64_t gi = 0; gi < n_groups; ++gi) {
-    const int64_t rg = gi % n_rg, h = (gi / n_rg) % L->num_kv_heads, s = gi / n_rg / L->num_kv_heads;
+    const int64_t rg = gi % n_rg, s = gi / n_rg;
     int32_t* g = &pb->groups[(size_t)gi * 8];
-    g[0] = (int32_t)s; g[1] = (int32_t)h; g[2] = (int32_t)rg; g[3] = h_seq_lens[s];
+    g[0] = (int32_t)s; g[1] = 0; g[2] = (int32_t)rg; g[3] = h_seq_lens[s];
     g[4] = seg_count[(size_t)gi]; g[5] = first_part[(size_t)gi]; g[6] = gpages[(size_t)gi]; g[7] = 0;
   }
   kv_nvfp4_plan_info* info = &pb->info;
@@ -169,7 +166,7 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
   info->off_counters = off;
   off = align_up(off + 4ull * n_groups, 256);
   info->off_partials = off;
-  off = align_up(off + 4ull * kPartFloats * parts, 256);
+  off = align_up(off + 4ull * kPartHeadFloats * L->num_kv_heads * parts, 256);
   info->workspace_bytes = off;
   return KV_NVFP4_OK;
 }
@@ -221,12 +218,11 @@ size_t kv_nvfp4_page_bytes(const kv_nvfp4_layout* L) {
   return (size_t)L->page_size * 2 * (64 + 8) * (size_t)L->num_kv_heads;
 }
 
-kv_nvfp4_status kv_nvfp4_pool_plane_bytes(const kv_nvfp4_layout* L, int32_t num_pages,
-                                          size_t* code_bytes, size_t* scale_bytes) {
-  if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || num_pages < 0) return KV_NVFP4_EINVAL;
-  const size_t slots = (size_t)num_pages * L->num_kv_heads * L->page_size;
-  if (code_bytes) *code_bytes = slots * 64;
-  if (scale_bytes) *scale_bytes = slots * 8;
+kv_nvfp4_status kv_nvfp4_pool_bytes(const kv_nvfp4_layout* L, int32_t num_pages,
+                                    size_t* bytes) {
+  if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || num_pages < 0 || bytes == nullptr)
+    return KV_NVFP4_EINVAL;
+  *bytes = (size_t)num_pages * kv_nvfp4_page_bytes(L);
   return KV_NVFP4_OK;
 }
 
@@ -264,23 +260,21 @@ kv_nvfp4_status kv_nvfp4_append(const kv_nvfp4_layout* L, const void* q, const v
                                 const int32_t* d_positions, int32_t T, const float* d_rope_table,
                                 int32_t rope_max_pos, const int32_t* d_block_table,
                                 int32_t num_seqs, int32_t max_pages, int32_t num_pages,
-                                uint8_t* k_codes, uint8_t* k_scales, uint8_t* v_codes,
-                                uint8_t* v_scales, uint8_t* q_codes, uint8_t* q_scales,
+                                uint8_t* pool, uint8_t* q_codes, uint8_t* q_scales,
                                 int32_t* d_status, void* stream) {
   if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK) return KV_NVFP4_EINVAL;
   if (T < 0 || num_seqs <= 0 || max_pages <= 0 || num_pages <= 0) return KV_NVFP4_EINVAL;
   if (T == 0) return KV_NVFP4_OK;
-  if (!k || !v || !d_seq_ids || !d_positions || !d_block_table || !k_codes || !k_scales ||
-      !v_codes || !v_scales)
-    return KV_NVFP4_EINVAL;
+  if (!k || !v || !d_seq_ids || !d_positions || !d_block_table || !pool) return KV_NVFP4_EINVAL;
   if (q && (!q_codes || !q_scales)) return KV_NVFP4_EINVAL;
   if (L->rot_dim > 0 && (!d_rope_table || rope_max_pos <= 0 || !aligned16(d_rope_table)))
     return KV_NVFP4_EINVAL;
-  if (!aligned16(k) || !aligned16(v) || (q && !aligned16(q))) return KV_NVFP4_EINVAL;
+  if (!aligned16(k) || !aligned16(v) || (q && !aligned16(q)) || !aligned16(pool))
+    return KV_NVFP4_EINVAL;
   const cudaError_t e = kvnvfp4::launch_append(
       (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, d_seq_ids, d_positions, T,
       d_rope_table, rope_max_pos, L->rot_dim, d_block_table, num_seqs, max_pages, num_pages,
-      k_codes, k_scales, v_codes, v_scales, q_codes, q_scales, L->num_q_heads, L->num_kv_heads,
+      pool, q_codes, q_scales, L->num_q_heads, L->num_kv_heads,
       d_status, (cudaStream_t)stream);
   return e == cudaSuccess ? KV_NVFP4_OK : KV_NVFP4_ECUDA;
 }
@@ -350,32 +344,31 @@ kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout* L, const int32_t* h_seq_len
 
 kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout* L, const kv_nvfp4_plan_info* plan,
                                      void* d_workspace, const uint8_t* q_codes,
-                                     const uint8_t* q_scales, float sm_scale,
-                                     const uint8_t* k_codes, const uint8_t* k_scales,
-                                     const uint8_t* v_codes, const uint8_t* v_scales,
+                                     const uint8_t* q_scales, float sm_scale, const uint8_t* pool,
                                      int32_t num_pages, const int32_t* d_block_table,
                                      int32_t max_pages, float* out, int32_t* d_status,
                                      void* stream) {
   if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || plan == nullptr) return KV_NVFP4_EINVAL;
+  if (L->num_kv_heads > kMaxAttnKvHeads) return KV_NVFP4_EINVAL;
   if (plan->num_kv_heads != L->num_kv_heads || plan->num_seqs <= 0 || plan->q_len <= 0 ||
       plan->grid <= 0)
     return KV_NVFP4_EINVAL;
-  if (!d_workspace || !q_codes || !q_scales || !k_codes || !k_scales || !v_codes || !v_scales ||
-      !d_block_table || !out || num_pages <= 0 || max_pages <= 0)
+  if (!d_workspace || !q_codes || !q_scales || !pool || !d_block_table || !out ||
+      num_pages <= 0 || max_pages <= 0)
     return KV_NVFP4_EINVAL;
   // every page index the work list touches must lie inside the block table's rows
   if ((int64_t)plan->max_seq_len > (int64_t)max_pages * L->page_size) return KV_NVFP4_EINVAL;
-  const void* ptrs[] = {d_workspace, q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, out};
+  const void* ptrs[] = {d_workspace, q_codes, q_scales, pool, out};
   for (const void* p : ptrs)
     if (!aligned16(p)) return KV_NVFP4_EINVAL;
   if (!(sm_scale > 0.0f)) sm_scale = 1.0f / std::sqrt((float)L->head_dim);
   char* ws = (char*)d_workspace;
   const cudaError_t e = kvnvfp4::launch_decode(
-      q_codes, q_scales, k_codes, k_scales, v_codes, v_scales, d_block_table, max_pages,
-      num_pages, ws + plan->off_groups, ws + plan->off_segments,
-      (const int32_t*)(ws + plan->off_cta), (int32_t*)(ws + plan->off_counters),
-      (float*)(ws + plan->off_partials), out, d_status, L->num_q_heads, L->num_kv_heads,
-      plan->q_len, plan->causal, plan->grid, sm_scale, (cudaStream_t)stream);
+      q_codes, q_scales, pool, d_block_table, max_pages, num_pages, ws + plan->off_groups,
+      ws + plan->off_segments, (const int32_t*)(ws + plan->off_cta),
+      (int32_t*)(ws + plan->off_counters), (float*)(ws + plan->off_partials), out, d_status,
+      L->num_q_heads, L->num_kv_heads, plan->q_len, plan->causal, plan->grid, sm_scale,
+      (cudaStream_t)stream);
   return e == cudaSuccess ? KV_NVFP4_OK : KV_NVFP4_ECUDA;
 }
 

@@ -41,10 +41,7 @@ struct AppendParams {
   int32_t num_seqs;
   int32_t max_pages;
   int32_t num_pages;
-  uint8_t* k_codes;
-  uint8_t* k_scales;
-  uint8_t* v_codes;
-  uint8_t* v_scales;
+  uint8_t* pool;         // num_pages blocks of Hkv * 9216 bytes
   uint8_t* q_codes;
   uint8_t* q_scales;
   int32_t Hq;   // 0 when q is absent
@@ -54,14 +51,15 @@ struct AppendParams {
 
 struct RowTarget {
   const uint16_t* src;  // bf16 row
-  uint8_t* codes;       // 64-byte destination, or nullptr to skip the row
+  uint8_t* codes;       // code destination, or nullptr to skip the row
   uint8_t* scales;      // 8-byte destination
   int32_t pos;          // position, for RoPE
   bool rotate;
+  bool tiled;           // K codes: 16-byte pieces 128 bytes apart (tensor-core tile order)
 };
 
 __device__ __forceinline__ RowTarget locate_row(const AppendParams& p, int64_t row, int lane) {
-  RowTarget r{nullptr, nullptr, nullptr, 0, false};
+  RowTarget r{nullptr, nullptr, nullptr, 0, false, false};
   const int32_t per_tok = p.Hq + 2 * p.Hkv;
   const int64_t t = row / per_tok;
   const int32_t w = (int32_t)(row - t * per_tok);
@@ -92,10 +90,18 @@ __device__ __forceinline__ RowTarget locate_row(const AppendParams& p, int64_t r
       if (lane == 0) flag_status(p.status, KV_NVFP4_DEV_BAD_PAGE);
       return r;
     }
-    const int64_t slot = ((int64_t)page * p.Hkv + h) * kPage + pos % kPage;
+    // page block: [K codes H*4096 (tiled)][K scales H*512][V codes H*4096][V scales H*512]
+    uint8_t* blk = p.pool + (int64_t)page * p.Hkv * 9216;
+    const int k = pos % kPage;
     r.src = (is_k ? p.k : p.v) + (t * p.Hkv + h) * kHeadDim;
-    r.codes = (is_k ? p.k_codes : p.v_codes) + slot * kCodeBytes;
-    r.scales = (is_k ? p.k_scales : p.v_scales) + slot * kScaleBytes;
+    if (is_k) {
+      r.codes = blk + h * 4096 + (k >> 3) * 512 + (k & 7) * 16;  // + chunk * 128 + byte % 16
+      r.scales = blk + p.Hkv * 4096 + h * 512 + k * 8;
+    } else {
+      r.codes = blk + p.Hkv * 4608 + h * 4096 + k * 64;
+      r.scales = blk + p.Hkv * 8704 + h * 512 + k * 8;
+    }
+    r.tiled = is_k;
     r.rotate = is_k;
   }
   if (r.rotate && p.rot_dim > 0 && pos >= p.rope_max_pos) {
@@ -176,7 +182,9 @@ __device__ __forceinline__ void quantize_store_row(float (&x)[4], const RowTarge
     for (int e = 0; e < 4; ++e) packed |= e2m1_encode_rne_sat(__fdiv_rn(x[e], sd)) << (4 * e);
   }
   if (r.codes != nullptr) {
-    *reinterpret_cast<uint16_t*>(r.codes + 2 * lane) = (uint16_t)packed;
+    // lane l holds code bytes 2l, 2l+1 of the row: 16-byte piece l / 8, offset (2l) % 16
+    uint8_t* dst = r.tiled ? r.codes + (lane >> 3) * 128 + ((2 * lane) & 15) : r.codes + 2 * lane;
+    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
     if ((lane & 3) == 0) r.scales[lane >> 2] = (uint8_t)sc;
   }
 }
@@ -215,13 +223,12 @@ cudaError_t launch_append(const uint16_t* q, const uint16_t* k, const uint16_t* 
                           const int32_t* seq_ids, const int32_t* positions, int64_t T,
                           const float* rope, int32_t rope_max_pos, int32_t rot_dim,
                           const int32_t* block_table, int32_t num_seqs, int32_t max_pages,
-                          int32_t num_pages, uint8_t* k_codes, uint8_t* k_scales,
-                          uint8_t* v_codes, uint8_t* v_scales, uint8_t* q_codes,
+                          int32_t num_pages, uint8_t* pool, uint8_t* q_codes,
                           uint8_t* q_scales, int32_t Hq, int32_t Hkv, int32_t* status,
                           cudaStream_t stream) {
-  AppendParams p{q,         k,        v,       seq_ids, positions, T,       rope,
-                 rope_max_pos, rot_dim, block_table, num_seqs, max_pages, num_pages, k_codes,
-                 k_scales,  v_codes,  v_scales, q_codes, q_scales,  q ? Hq : 0, Hkv, status};
+  AppendParams p{q,       k,         v,           seq_ids,  positions, T,
+                 rope,    rope_max_pos, rot_dim,  block_table, num_seqs, max_pages,
+                 num_pages, pool,    q_codes,     q_scales, q ? Hq : 0, Hkv, status};
   const int64_t rows = T * (int64_t)(p.Hq + 2 * Hkv);
   const int64_t per_block = (int64_t)kWarpsPerBlock * kRowsPerWarp;
   const int64_t blocks = (rows + per_block - 1) / per_block;

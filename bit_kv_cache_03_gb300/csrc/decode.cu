@@ -1,37 +1,36 @@
-// Paged GQA decode / speculative-verify attention over the NVFP4 cache, with split-K.
+// Paged GQA decode / speculative-verify attention over the NVFP4 cache, on the tcgen05 tensor
+// cores, with split-K.
 //
-// Source: prismix.dev/news/833001997676, section "NVFP4 KV cache (from scratch)": Q.K^T from
-// NVFP4 Q and K with their E4M3 block scales, V dequantised for the P.V product, row-major KV
-// scales. Split-K with an fp32 log-sum-exp merge is this library's design (the pages run long
-// contexts from a paged pool and say nothing about the kernel's decomposition).
+// Source: prismix.dev/news/833001997676, section "NVFP4 KV cache (from scratch)": the Q.K^T
+// product in NVFP4 with E4M3 block scales (both Q and K quantised), V dequantised for the P.V
+// product, row-major KV scales. The split-K decomposition and the fp32 log-sum-exp merge are this
+// library's design; the pages say nothing about the kernel's decomposition.
 //
-// Work decomposition: a group is (sequence, kv head, tile of 8 query rows); a row is (query token,
-// head in the GQA group), row = token * group + head_in_group. The plan lays the groups' pages
-// (cut into split-K chunks) end to end and hands every CTA (one persistent CTA per SM) an equal
-// share of that page stream; a CTA's share is one or more segments, each a contiguous page
-// range of one group. Within a segment the CTA's state carries across chunks (online softmax);
-// at the end of a segment it writes either the final rows (the group lies in one CTA) or one
-// (m, l, O) partial, and the CTA that takes the group's last ticket combines its partials.
+// Work decomposition. A group is (sequence, tile of 8 query rows) over every KV head; a row is
+// (query token, head in the GQA group). The plan lays the groups' pages end to end and gives each
+// persistent CTA (one per SM) a contiguous, page-balanced share: one or more segments, each a page
+// range of one group. A CTA's softmax state carries across the pages of a segment; a group that
+// spans CTAs leaves one (m, l, O) partial per segment and the CTA taking its last ticket merges.
 //
-// Per CTA: the last warp is the producer; lane 0 streams every page of the CTA's segments into a
-// 16-slot shared-memory ring with bulk async copies (K codes 4 KiB, K scales 512 B, V codes
-// 4 KiB, V scales 512 B per page and head), each slot guarded by a full and an empty mbarrier.
-// Warps 0..11 consume: three groups of four warps take the segment's pages round-robin, and the
-// four warps of a group split a page into 16-key sub-tiles (empty barrier count 4).
+// One page = 64 keys of every KV head, a 9216 x H byte block moved by ONE bulk async copy.
 //
-// Per 16-key sub-tile and warp, the product runs on the warp-level tensor path with keys as the M
-// dimension (16 keys per MMA) and the 8 query rows as N:
-//   S^T[key][row] = sum_d Khat[key][d] Qhat[row][d]        (8 x m16n8k16, k = 16 dims per step)
-//   O^T[dim][row] += sum_key Vhat^T[dim][key] P^T[key][row] (8 m-tiles of 16 dims)
-// Khat, Vhat and Qhat are the NVFP4 values converted to f16 (E2M1 * E4M3 has at most 6
-// significant bits and lies in [2^-10, 2688], so it is exact in f16); products accumulate in
-// fp32. P is fed as an f16 hi/lo pair (p = hi + lo to ~2^-22 relative), so the P.V product
-// carries fp32-level precision. The dims inside an MMA are a fixed permutation of the head
-// dims (the same one for both operands), chosen so that each thread reads contiguous bytes.
+// Per page, with KV heads taken in pairs (2p, 2p+1):
+//   Q.K^T: tcgen05.mma kind::mxf4nvf4, block_scale.scale_vec::4X (E2M1 x E2M1, UE4M3 scale per
+//     16 elements), M = 128 = 64 keys of head 2p over 64 keys of head 2p+1, N = 16 = 8 query rows
+//     of head 2p then 8 of head 2p+1, K = 64 per instruction (two per 128-dim row). The K codes
+//     are stored in the pool in the tensor core's 8-row x 16-byte tile order, so the page lands in
+//     shared memory ready for the MMA; scales go to TMEM in the replicated 32-lane x 4-column
+//     layout. Cross terms (head 2p keys x head 2p+1 rows) are computed and ignored.
+//   softmax: 4 warps read S from TMEM (one key per lane), fp32 online softmax with a lazily
+//     raised running max, P written to shared memory as f16 hi + lo.
+//   P.V: 8 warps dequantise V (E2M1 x E4M3 is exact in f16) into an MN-major shared tile; one
+//     thread issues tcgen05.mma kind::f16 with M = 128 dims, N = 16 (P hi in columns 0..7, P lo in
+//     8..15), K = 16 keys per instruction, accumulating O^T per head in TMEM.
 //
-// Softmax: running max per row, exp2 with log2(e) folded into the scale, rescale of the
-// accumulator only when the max grows. At the end of a segment the 12 warps' states are merged
-// in shared memory; merging never waits on another CTA.
+// Warp roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner, warps 2..5
+// softmax / scale factors / epilogue (TMEM lane quadrants 2, 3, 0, 1), warps 6..13 V dequant.
+// Every wait is an mbarrier wait bounded in time; on a timeout the kernel records
+// KV_NVFP4_DEV_TIMEOUT and carries on, so it cannot hang.
 
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -42,83 +41,144 @@ namespace kvnvfp4 {
 
 namespace {
 
-constexpr int kGroups = 3;                     // pages processed concurrently per CTA
-constexpr int kConsumerWarps = 4 * kGroups;     // four warps (16-key sub-tiles) per page
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kSlots = 16;
-constexpr int kKcOff = 0, kKsOff = 4096, kVcOff = 4608, kVsOff = 8704;
-constexpr int kSlotBytes = 9216;
-constexpr int kRows = 8;                           // query rows per work item
-constexpr int kPartFloats = kRows * 128 + 2 * kRows;  // O[8][128], m[8], l[8]
-constexpr int kRingBytes = kSlots * kSlotBytes;
-constexpr int kBarOff = kRingBytes;                // 2 * kSlots mbarriers
-constexpr int kSlotPidOff = kBarOff + 2 * kSlots * 8;   // int32 page id per slot
-constexpr int kMergeOff = kSlotPidOff + kSlots * 4;
-constexpr int kMergeFloats = kConsumerWarps * kPartFloats;
-constexpr int kFlagOff = kMergeOff + kMergeFloats * 4;
-constexpr int kSmemBytes = kFlagOff + 16;
+constexpr int kMaxHkv = 4;
+constexpr int kStages = 4;
+constexpr int kStageBytes = kMaxHkv * 9216;        // one page block of up to 4 heads
+constexpr int kVhSlots = 3;                        // dequantised V tiles (one head-page each)
+constexpr int kVhBytes = 64 * 128 * 2;             // 64 keys x 128 dims x f16
+constexpr int kPBytes = kMaxHkv * 2048;            // per page: per head P hi (1 KB) + lo (1 KB)
+constexpr int kQBytes = 2 * 1024;                  // two head pairs x 16 rows x 64 B
+constexpr int kRows = 8;                           // query rows per head per group
+constexpr int kPartHeadFloats = kRows * 128 + 2 * kRows;  // O[8][128], m[8], l[8]
+
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpSoftmax0 = 2, kWarpDequant0 = 6;
+constexpr int kDequantWarps = 8;
+constexpr int kThreads = (kWarpDequant0 + kDequantWarps) * 32;
+
+// shared memory map
+constexpr int kOffStage = 0;
+constexpr int kOffVh = kOffStage + kStages * kStageBytes;
+constexpr int kOffP = kOffVh + kVhSlots * kVhBytes;
+constexpr int kOffQ = kOffP + 2 * kPBytes;
+constexpr int kOffBars = kOffQ + kQBytes;
+// barrier indices
+constexpr int kBarStageFull = 0;                    // [kStages]
+constexpr int kBarStageEmpty = kBarStageFull + kStages;
+constexpr int kBarSfaFull = kBarStageEmpty + kStages;  // [2]
+constexpr int kBarQkDone = kBarSfaFull + 2;         // [2]
+constexpr int kBarSFree = kBarQkDone + 2;           // [2]
+constexpr int kBarPFull = kBarSFree + 2;            // [2]
+constexpr int kBarPvDone = kBarPFull + 2;           // [2]
+constexpr int kBarVhFull = kBarPvDone + 2;          // [kVhSlots]
+constexpr int kBarVhFree = kBarVhFull + kVhSlots;   // [kVhSlots]
+constexpr int kBarQReady = kBarVhFree + kVhSlots;
+constexpr int kBarOFree = kBarQReady + 1;
+constexpr int kNumBars = kBarOFree + 1;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+// misc: stage page ids, tmem base, flags (need-max per page parity x warp, rescale per
+// half, ticket), reduction scratch, per-head alpha / mu / L
+constexpr int kOffStagePid = kOffMisc;
+constexpr int kOffTmemSlot = kOffStagePid + 4 * kStages;
+constexpr int kOffFlags = kOffTmemSlot + 16;
+constexpr int kOffRed = kOffFlags + 128;            // float [4 quadrants][2 pairs][8 rows]
+constexpr int kOffAlpha = kOffRed + 4 * 2 * kRows * 4;  // float [kMaxHkv][8]: rescale / mu / L
+constexpr int kOffMu = kOffAlpha + kMaxHkv * kRows * 4;
+constexpr int kOffL = kOffMu + kMaxHkv * kRows * 4;
+constexpr int kSmemBytes = kOffL + kMaxHkv * kRows * 4 + 64;
+
+// TMEM columns
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0;      // [2 buffers][2 pairs][16]
+constexpr uint32_t kColO = 64;     // [4 heads][16]
+constexpr uint32_t kColSfa = 128;  // [2 buffers][2 pairs][2 k-halves][4]
+constexpr uint32_t kColSfb = 160;  // [2 pairs][2 k-halves][4]
+
+// instruction descriptors (dense, no negation):
+//   QK: A, B = E2M1 (format 1) K-major, scale type UE4M3, N = 16, M = 128
+//   PV: D = f32, A, B = f16, both MN-major, N = 16, M = 128
+constexpr uint32_t kIdescQK = (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdescPV = (1u << 4) | (1u << 15) | (1u << 16) | ((16u >> 3) << 17) |
+                              ((128u >> 4) << 24);
+
+constexpr float kLazyMaxLog2 = 8.0f;  // the running max is raised only past a 2^8 margin
 
 struct DecodeParams {
   const uint8_t* q_codes;
   const uint8_t* q_scales;
-  const uint8_t* k_codes;
-  const uint8_t* k_scales;
-  const uint8_t* v_codes;
-  const uint8_t* v_scales;
+  const uint8_t* pool;
   const int32_t* block_table;
   int32_t max_pages;
   int32_t num_pages;
-  const int4* groups;    // 2 x int4 per group: {seq, kvh, rg, len}, {n_seg, first_part, pages, 0}
-  const int4* segments;  // {group, page_lo, page_hi, part_slot or -1}
-  const int32_t* cta_seg;  // [grid + 1]: segments of CTA b are [cta_seg[b], cta_seg[b+1])
-  int32_t* counters;     // [num_groups], merge tickets
-  float* partials;       // [num_partials][kPartFloats]
+  const int4* groups;      // 2 x int4 per group: {seq, 0, rg, len}, {n_seg, first_part, pages, 0}
+  const int4* segments;    // {group, page_lo, page_hi, part_slot or -1}
+  const int32_t* cta_seg;  // [grid + 1]
+  int32_t* counters;       // [num_groups] merge tickets
+  float* partials;         // [num_partials][Hkv][kPartHeadFloats]
   float* out;
   int32_t* status;
   int32_t Hq, Hkv, G, q_len, causal;
-  float c2;              // sm_scale * log2(e)
+  float c2;                // sm_scale * log2(e)
 };
 
+struct SegInfo {
+  int seq, rg, len, n_seg, first_part, lo, hi, part, group;
+};
+
+__device__ __forceinline__ SegInfo load_seg(const DecodeParams& p, int s) {
+  const int4 seg = p.segments[s];
+  const int4 g0 = p.groups[2 * seg.x];
+  const int4 g1 = p.groups[2 * seg.x + 1];
+  SegInfo r;
+  r.group = seg.x; r.lo = seg.y; r.hi = seg.z; r.part = seg.w;
+  r.seq = g0.x; r.rg = g0.z; r.len = g0.w;
+  r.n_seg = g1.x; r.first_part = g1.y;
+  return r;
+}
+
+// Bounded wait: after a thread has once hit the time limit its later waits do not block, so a
+// kernel whose pipeline lost a signal still ends promptly (with KV_NVFP4_DEV_TIMEOUT set).
+__device__ __forceinline__ void wait_bar(uint32_t bar, uint32_t parity, bool& timed_out) {
+  if (timed_out) {
+    (void)mbar_try_wait(bar, parity);
+    return;
+  }
+  if (!mbar_wait_bounded(bar, parity)) timed_out = true;
+}
+
 // --------------------------------------------------------------------------------------------
-// Producer warp: lane 0 streams the CTA's pages into the ring; the other lanes help load page
-// ids 32 at a time. The page id (or -1 for an id outside the pool) is published in shared
-// memory before the slot's full barrier is armed, so consumers never read the block table.
+// Producer warp: lane 0 streams the CTA's pages (all KV heads of a page in one bulk copy) into a
+// kStages ring; the other lanes load page ids 32 at a time. The page id (or -1 when it lies
+// outside the pool) is published in shared memory before the stage's full barrier is armed.
 // --------------------------------------------------------------------------------------------
 __device__ void producer(const DecodeParams& p, uint8_t* smem, int lane) {
-  const uint32_t ring = smem_u32(smem);
-  const uint32_t bars = smem_u32(smem + kBarOff);
-  volatile int32_t* slot_pid = reinterpret_cast<volatile int32_t*>(smem + kSlotPidOff);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + kOffBars;
+  volatile int32_t* stage_pid = reinterpret_cast<volatile int32_t*>(smem + kOffStagePid);
+  const uint32_t blk_bytes = (uint32_t)p.Hkv * 9216u;
   uint32_t k = 0;
   bool timed_out = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
   for (int s = s_begin; s < s_end; ++s) {
-    const int4 seg = p.segments[s];
-    const int4 g0 = p.groups[2 * seg.x];
-    const int seq = g0.x, kvh = g0.y;
-    for (int p0 = seg.y; p0 < seg.z; p0 += 32) {
-      const int n = min(32, seg.z - p0);
-      const int32_t mine = (lane < n) ? p.block_table[(int64_t)seq * p.max_pages + p0 + lane] : -1;
+    const SegInfo sg = load_seg(p, s);
+    for (int p0 = sg.lo; p0 < sg.hi; p0 += 32) {
+      const int n = min(32, sg.hi - p0);
+      const int32_t mine =
+          (lane < n) ? p.block_table[(int64_t)sg.seq * p.max_pages + p0 + lane] : -1;
       for (int j = 0; j < n; ++j, ++k) {
         const int32_t pid = __shfl_sync(0xffffffffu, mine, j);
         if (lane == 0) {
-          const uint32_t slot = k % kSlots;
-          const uint32_t full = bars + 8 * slot;
-          if (k >= kSlots) {
-            if (!mbar_wait_bounded(bars + 8 * (kSlots + slot), ((k / kSlots) - 1) & 1))
-              timed_out = true;
-          }
+          const uint32_t st = k % kStages;
+          if (k >= kStages)
+            wait_bar(bars + 8 * (kBarStageEmpty + st), ((k / kStages) - 1) & 1, timed_out);
           const bool valid = pid >= 0 && pid < p.num_pages;
-          slot_pid[slot] = valid ? pid : -1;
+          stage_pid[st] = valid ? pid : -1;
+          const uint32_t full = bars + 8 * (kBarStageFull + st);
           if (valid) {
-            const int64_t head = (int64_t)pid * p.Hkv + kvh;
-            const uint32_t dst = ring + slot * kSlotBytes;
-            mbar_arrive_expect_tx(full, kSlotBytes);
-            bulk_g2s(dst + kKcOff, p.k_codes + head * 4096, 4096, full);
-            bulk_g2s(dst + kKsOff, p.k_scales + head * 512, 512, full);
-            bulk_g2s(dst + kVcOff, p.v_codes + head * 4096, 4096, full);
-            bulk_g2s(dst + kVsOff, p.v_scales + head * 512, 512, full);
+            mbar_arrive_expect_tx(full, blk_bytes);
+            bulk_g2s(sbase + kOffStage + st * kStageBytes, p.pool + (int64_t)pid * blk_bytes,
+                     blk_bytes, full);
           } else {
-            mbar_arrive(full);  // completes the phase with no data; consumers skip the page
+            mbar_arrive(full);
           }
         }
         __syncwarp();
@@ -126,352 +186,514 @@ __device__ void producer(const DecodeParams& p, uint8_t* smem, int lane) {
     }
   }
   if (lane == 0) {
-    // Drain: no copy into this CTA's shared memory may still be in flight at exit.
-    const uint32_t issued = k;
-    for (uint32_t s = 0; s < kSlots && s < issued; ++s) {
-      const uint32_t last = issued - 1 - ((issued - 1 - s) % kSlots);  // last use of slot s
-      if (!mbar_wait_bounded(bars + 8 * (last % kSlots), (last / kSlots) & 1)) timed_out = true;
+    // no copy into this CTA's shared memory may still be in flight at exit
+    for (uint32_t st = 0; st < kStages && st < k; ++st) {
+      const uint32_t last = k - 1 - ((k - 1 - st) % kStages);
+      wait_bar(bars + 8 * (kBarStageFull + st), (last / kStages) & 1, timed_out);
     }
     if (timed_out) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
   }
 }
 
 // --------------------------------------------------------------------------------------------
-// Consumer warp: one page (64 keys) against the item's 8 query rows.
+// MMA issuer (one thread).
 // --------------------------------------------------------------------------------------------
-struct WarpState {
-  float o[8][4];   // O^T fragments: m-tile i -> dims 16g+i (c0,c1) and 16g+8+i (c2,c3)
-  float m[2];      // running max (raw dot-product units) of rows 2t, 2t+1
-  float l[2];      // per-thread partial sums of p for rows 2t, 2t+1
-  uint32_t qf[8][2];  // Q B-fragments for k-steps 0..7
-};
-
-__device__ __forceinline__ void process_subtile(WarpState& st, uint32_t slot_addr, int sub, int kp0,
-                                                int len, int lim0, int lim1, float c2, int g,
-                                                int t) {
-  const uint32_t kc = slot_addr + kKcOff, ks = slot_addr + kKsOff;
-  const uint32_t vc = slot_addr + kVcOff, vs = slot_addr + kVsOff;
-
-  // ---- scores S^T for keys 16*sub .. 16*sub+15 of the page ----
-  float S[4] = {0.f, 0.f, 0.f, 0.f};
-  {
-    const int ka = 16 * sub + g, kb = ka + 8;
-    const uint4 ca = lds128(kc + ka * 64 + 16 * t);
-    const uint4 cb = lds128(kc + kb * 64 + 16 * t);
-    uint32_t sa = lds16(ks + ka * 8 + 2 * t);
-    uint32_t sb = lds16(ks + kb * 8 + 2 * t);
-    if (kp0 + ka >= len) sa = 0;  // keys past the end may hold stale bytes: force them to 0
-    if (kp0 + kb >= len) sb = 0;
-    const uint32_t sah = cvt_e4m3x2_f16(sa), sbh = cvt_e4m3x2_f16(sb);
-    const uint32_t sa0 = dup_lo(sah), sa1 = dup_hi(sah);
-    const uint32_t sb0 = dup_lo(sbh), sb1 = dup_hi(sbh);
-    const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
-    const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
-    // two independent accumulators (even / odd k-steps) halve the MMA dependency chain
-    float c1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-      cvt_e2m1x8_f16(wa[w], a0, a1, a2, a3);
-      cvt_e2m1x8_f16(wb[w], b0, b1, b2, b3);
-      const uint32_t sA = (w < 2) ? sa0 : sa1;  // bytes 0..7 of the 16 -> block 2t, 8..15 -> 2t+1
-      const uint32_t sB = (w < 2) ? sb0 : sb1;
-      // step s = 2w uses bytes (0,1) of word w, step 2w+1 bytes (2,3)
-      mma_f16_16816(S, hmul2(a0, sA), hmul2(b0, sB), hmul2(a1, sA), hmul2(b1, sB),
-                    st.qf[2 * w][0], st.qf[2 * w][1]);
-      mma_f16_16816(c1, hmul2(a2, sA), hmul2(b2, sB), hmul2(a3, sA), hmul2(b3, sB),
-                    st.qf[2 * w + 1][0], st.qf[2 * w + 1][1]);
+__device__ __forceinline__ void issue_qk(const DecodeParams& p, uint32_t sbase, uint32_t tbase,
+                                         uint32_t k, int npairs, bool& timed_out) {
+  const uint32_t bars = sbase + kOffBars;
+  const uint32_t st = k % kStages, b = k & 1;
+  wait_bar(bars + 8 * (kBarStageFull + st), (k / kStages) & 1, timed_out);
+  wait_bar(bars + 8 * (kBarSfaFull + b), (k >> 1) & 1, timed_out);
+  if (k >= 2) wait_bar(bars + 8 * (kBarSFree + b), ((k >> 1) - 1) & 1, timed_out);
+  tc_fence_after();
+  const uint32_t kc = sbase + kOffStage + st * kStageBytes;
+  const uint32_t qb = sbase + kOffQ;
+  for (int pr = 0; pr < npairs; ++pr) {
+    for (int kh = 0; kh < 2; ++kh) {
+      const uint64_t ad = smem_desc(kc + pr * 8192 + kh * 256, 128, 512);
+      const uint64_t bd = smem_desc(qb + pr * 1024 + kh * 256, 128, 512);
+      mma_nvf4_ss(tbase + kColS + b * 32 + pr * 16, ad, bd, kIdescQK,
+                  tbase + kColSfa + b * 16 + pr * 8 + kh * 4, tbase + kColSfb + pr * 8 + kh * 4,
+                  (uint32_t)kh);
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) S[e] += c1[e];
   }
-
-  // ---- online softmax over these 16 keys ----
-  const int kpa = kp0 + 16 * sub + g, kpb = kpa + 8;
-  float mx0 = -INFINITY, mx1 = -INFINITY;
-  if (kpa <= lim0) mx0 = S[0];
-  if (kpa <= lim1) mx1 = S[1];
-  if (kpb <= lim0) mx0 = fmaxf(mx0, S[2]);
-  if (kpb <= lim1) mx1 = fmaxf(mx1, S[3]);
-#pragma unroll
-  for (int m = 4; m < 32; m <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, m));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, m));
-  }
-  if (mx0 > st.m[0]) {
-    const float alpha = (st.m[0] == -INFINITY) ? 0.f : fast_exp2((st.m[0] - mx0) * c2);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { st.o[i][0] *= alpha; st.o[i][2] *= alpha; }
-    st.l[0] *= alpha;
-    st.m[0] = mx0;
-  }
-  if (mx1 > st.m[1]) {
-    const float alpha = (st.m[1] == -INFINITY) ? 0.f : fast_exp2((st.m[1] - mx1) * c2);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { st.o[i][1] *= alpha; st.o[i][3] *= alpha; }
-    st.l[1] *= alpha;
-    st.m[1] = mx1;
-  }
-  const float p0 = (kpa <= lim0) ? fast_exp2((S[0] - st.m[0]) * c2) : 0.f;
-  const float p1 = (kpa <= lim1) ? fast_exp2((S[1] - st.m[1]) * c2) : 0.f;
-  const float p2 = (kpb <= lim0) ? fast_exp2((S[2] - st.m[0]) * c2) : 0.f;
-  const float p3 = (kpb <= lim1) ? fast_exp2((S[3] - st.m[1]) * c2) : 0.f;
-  st.l[0] += p0 + p2;
-  st.l[1] += p1 + p3;
-  // P as f16 hi + lo, transposed into the B layout (keys along k)
-  const uint32_t h01 = pack_f16x2(p0, p1);
-  const uint32_t h23 = pack_f16x2(p2, p3);
-  const uint32_t l01 = pack_f16x2(p0 - f16_lo_to_f32(h01), p1 - f16_hi_to_f32(h01));
-  const uint32_t l23 = pack_f16x2(p2 - f16_lo_to_f32(h23), p3 - f16_hi_to_f32(h23));
-  const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
-  const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
-
-  // ---- V^T fragments: keys (2t, 2t+1) and (2t+8, 2t+9) of the sub-tile, dims of block g ----
-  const int v0 = 16 * sub + 2 * t;
-  const uint2 w0 = lds64(vc + v0 * 64 + 8 * g);
-  const uint2 w1 = lds64(vc + (v0 + 1) * 64 + 8 * g);
-  const uint2 w2 = lds64(vc + (v0 + 8) * 64 + 8 * g);
-  const uint2 w3 = lds64(vc + (v0 + 9) * 64 + 8 * g);
-  uint32_t s0 = lds8(vs + v0 * 8 + g), s1 = lds8(vs + (v0 + 1) * 8 + g);
-  uint32_t s2 = lds8(vs + (v0 + 8) * 8 + g), s3 = lds8(vs + (v0 + 9) * 8 + g);
-  if (kp0 + v0 >= len) s0 = 0;
-  if (kp0 + v0 + 1 >= len) s1 = 0;
-  if (kp0 + v0 + 8 >= len) s2 = 0;
-  if (kp0 + v0 + 9 >= len) s3 = 0;
-  const uint32_t sp01 = cvt_e4m3x2_f16(s0 | (s1 << 8));
-  const uint32_t sp23 = cvt_e4m3x2_f16(s2 | (s3 << 8));
-  // interleave the nibbles of two keys: byte k of `e` = (dim 2k of key b) << 4 | (dim 2k of
-  // key a); `o` likewise for dim 2k+1
-  const uint32_t e0 = (w0.x & 0x0F0F0F0Fu) | ((w1.x & 0x0F0F0F0Fu) << 4);
-  const uint32_t o0 = ((w0.x >> 4) & 0x0F0F0F0Fu) | (w1.x & 0xF0F0F0F0u);
-  const uint32_t e1 = (w0.y & 0x0F0F0F0Fu) | ((w1.y & 0x0F0F0F0Fu) << 4);
-  const uint32_t o1 = ((w0.y >> 4) & 0x0F0F0F0Fu) | (w1.y & 0xF0F0F0F0u);
-  const uint32_t e2 = (w2.x & 0x0F0F0F0Fu) | ((w3.x & 0x0F0F0F0Fu) << 4);
-  const uint32_t o2 = ((w2.x >> 4) & 0x0F0F0F0Fu) | (w3.x & 0xF0F0F0F0u);
-  const uint32_t e3 = (w2.y & 0x0F0F0F0Fu) | ((w3.y & 0x0F0F0F0Fu) << 4);
-  const uint32_t o3 = ((w2.y >> 4) & 0x0F0F0F0Fu) | (w3.y & 0xF0F0F0F0u);
-  // D01[j] = (Vhat[key v0][16g+j], Vhat[key v0+1][16g+j]) for j = 0..15, likewise D23
-  uint32_t D01[16], D23[16];
-  cvt_e2m1x8_f16(e0, D01[0], D01[2], D01[4], D01[6]);
-  cvt_e2m1x8_f16(o0, D01[1], D01[3], D01[5], D01[7]);
-  cvt_e2m1x8_f16(e1, D01[8], D01[10], D01[12], D01[14]);
-  cvt_e2m1x8_f16(o1, D01[9], D01[11], D01[13], D01[15]);
-  cvt_e2m1x8_f16(e2, D23[0], D23[2], D23[4], D23[6]);
-  cvt_e2m1x8_f16(o2, D23[1], D23[3], D23[5], D23[7]);
-  cvt_e2m1x8_f16(e3, D23[8], D23[10], D23[12], D23[14]);
-  cvt_e2m1x8_f16(o3, D23[9], D23[11], D23[13], D23[15]);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t a0 = hmul2(D01[i], sp01), a1 = hmul2(D01[8 + i], sp01);
-    const uint32_t a2 = hmul2(D23[i], sp23), a3 = hmul2(D23[8 + i], sp23);
-    mma_f16_16816(st.o[i], a0, a1, a2, a3, bh0, bh1);
-    mma_f16_16816(st.o[i], a0, a1, a2, a3, bl0, bl1);
-  }
+  mma_commit(bars + 8 * (kBarQkDone + b));
+  mma_commit(bars + 8 * (kBarStageEmpty + st));  // K codes consumed once the QK MMAs complete
 }
 
-__device__ __forceinline__ void store_out(const DecodeParams& p, int seq, int kvh, int r, int dim,
-                                          float v) {
-  const int tok = r / p.G, hq = kvh * p.G + r % p.G;
-  p.out[(((int64_t)seq * p.q_len + tok) * p.Hq + hq) * 128 + dim] = v;
-}
-
-__device__ void consumer(const DecodeParams& p, uint8_t* smem, int warp, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  const uint32_t ring = smem_u32(smem);
-  const uint32_t bars = smem_u32(smem + kBarOff);
-  const volatile int32_t* slot_pid = reinterpret_cast<const volatile int32_t*>(smem + kSlotPidOff);
-  float* mrg = reinterpret_cast<float*>(smem + kMergeOff);
-  volatile int* flag = reinterpret_cast<volatile int*>(smem + kFlagOff);
-  const int ctid = warp * 32 + lane;  // consumer thread index
-  const int rows_total = p.G * p.q_len;
-  uint32_t kbase = 0;
+__device__ void mma_issuer(const DecodeParams& p, uint8_t* smem, uint32_t tbase) {
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + kOffBars;
+  const int npairs = (p.Hkv + 1) >> 1;
+  uint32_t k = 0, hp = 0, sgi = 0;
   bool timed_out = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
+  for (int s = s_begin; s < s_end; ++s, ++sgi) {
+    const SegInfo sg = load_seg(p, s);
+    const int n = sg.hi - sg.lo;
+    wait_bar(bars + 8 * kBarQReady, sgi & 1, timed_out);  // Q tile and its scales for this group
+    issue_qk(p, sbase, tbase, k, npairs, timed_out);
+    for (int j = 0; j < n; ++j, ++k) {
+      if (j + 1 < n) issue_qk(p, sbase, tbase, k + 1, npairs, timed_out);
+      const uint32_t b = k & 1;
+      wait_bar(bars + 8 * (kBarPFull + b), (k >> 1) & 1, timed_out);
+      if (j == 0 && sgi > 0) wait_bar(bars + 8 * kBarOFree, (sgi - 1) & 1, timed_out);
+      tc_fence_after();
+      for (int h = 0; h < p.Hkv; ++h, ++hp) {
+        const uint32_t slot = hp % kVhSlots;
+        wait_bar(bars + 8 * (kBarVhFull + slot), (hp / kVhSlots) & 1, timed_out);
+        tc_fence_after();
+        const uint32_t vh = sbase + kOffVh + slot * kVhBytes;
+        const uint32_t pb = sbase + kOffP + b * kPBytes + h * 2048;
+        for (int i = 0; i < 4; ++i) {  // 16 keys per instruction
+          const uint64_t ad = smem_desc(vh + i * 4096, 2048, 128);
+          const uint64_t bd = smem_desc(pb + i * 256, 128, 1024);
+          mma_f16_ss(tbase + kColO + h * 16, ad, bd, kIdescPV, (j > 0 || i > 0) ? 1u : 0u);
+        }
+        mma_commit(bars + 8 * (kBarVhFree + slot));
+      }
+      mma_commit(bars + 8 * (kBarPvDone + b));
+    }
+  }
+  if (timed_out) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
+}
 
-  for (int s = s_begin; s < s_end; ++s) {
-    const int4 seg = p.segments[s];
-    const int4 g0 = p.groups[2 * seg.x];
-    const int4 g1 = p.groups[2 * seg.x + 1];
-    const int seq = g0.x, kvh = g0.y, rg = g0.z, len = g0.w;
-    const int n_seg = g1.x, first_part = g1.y;
-    const int row0 = rg * kRows;
-    const int L0 = len - p.q_len;
-    // visibility limit (largest visible key position) of rows 2t, 2t+1; -1 for padding rows
-    int lim[2];
+// --------------------------------------------------------------------------------------------
+// Softmax warps (4 warps, TMEM lane quadrant qd = warp % 4). For S a lane holds one key: TMEM
+// lane L = 32 qd + lane is key L % 64 of head 2 pr + L / 64 in pair pr. For O a lane holds one
+// head dim.
+// --------------------------------------------------------------------------------------------
+struct SoftmaxCtx {
+  const DecodeParams* p;
+  uint8_t* smem;
+  uint32_t sbase, bars, tbase, lane_base;
+  int lane, qd, sw, half, key, npairs;
+  bool timed_out;
+};
+
+// Scale factors of page k's K rows into TMEM (replicated 32-lane x 4-column layout: lane i,
+// column j holds the 4 scales of MMA row 32 j + i); releases the stage's K scales.
+__device__ __forceinline__ void write_sfa(SoftmaxCtx& c, uint32_t k, int page, int len) {
+  const DecodeParams& p = *c.p;
+  const uint32_t st = k % kStages, b = k & 1;
+  wait_bar(c.bars + 8 * (kBarStageFull + st), (k / kStages) & 1, c.timed_out);
+  if (k >= 2) wait_bar(c.bars + 8 * (kBarQkDone + b), ((k >> 1) - 1) & 1, c.timed_out);
+  const bool pvalid = reinterpret_cast<volatile int32_t*>(c.smem + kOffStagePid)[st] >= 0;
+  const uint32_t ks = c.sbase + kOffStage + st * kStageBytes + p.Hkv * 4096;
+  const int kp0 = page * 64;
+  uint32_t sf[16];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int r = row0 + 2 * t + e;
-      lim[e] = (r < rows_total) ? (p.causal ? L0 + r / p.G : len - 1) : -1;
+  for (int pr = 0; pr < 2; ++pr) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int hh = 2 * pr + (j >> 1), kk = 32 * (j & 1) + c.lane;
+      uint2 v = make_uint2(0u, 0u);
+      if (hh < p.Hkv && pvalid && kp0 + kk < len) v = lds64(ks + hh * 512 + kk * 8);
+      sf[pr * 8 + j] = v.x;      // k-half 0: scales of dims 0..63
+      sf[pr * 8 + 4 + j] = v.y;  // k-half 1: dims 64..127
     }
-    WarpState st;
+  }
+  tmem_st16(c.tbase + c.lane_base + kColSfa + b * 16, sf);
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (c.lane == 0) {
+    mbar_arrive(c.bars + 8 * (kBarSfaFull + b));
+    mbar_arrive(c.bars + 8 * (kBarStageEmpty + st));
+  }
+}
+
+__device__ __forceinline__ void store_row(const DecodeParams& p, int seq, int hh, int r, int dim,
+                                          float v) {
+  const int tok = r / p.G, qh = hh * p.G + r % p.G;
+  p.out[(((int64_t)seq * p.q_len + tok) * p.Hq + qh) * 128 + dim] = v;
+}
+
+__device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tbase, int warp,
+                              int lane) {
+  SoftmaxCtx c;
+  c.p = &p; c.smem = smem; c.sbase = smem_u32(smem); c.bars = c.sbase + kOffBars;
+  c.tbase = tbase; c.lane = lane; c.qd = warp & 3; c.sw = warp - kWarpSoftmax0;
+  c.lane_base = (uint32_t)(c.qd * 32) << 16;
+  c.half = c.qd >> 1;                 // TMEM lanes 64..127 hold the odd head of a pair
+  c.key = (c.qd * 32 + lane) & 63;
+  c.npairs = (p.Hkv + 1) >> 1;
+  c.timed_out = false;
+  const int dim = c.qd * 32 + lane;   // this thread's head dim in O
+  const int t128 = c.sw * 32 + lane;  // 0..127
+  const int rows_total = p.G * p.q_len;
+  const float thr = kLazyMaxLog2 / p.c2;
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + kOffFlags);
+  volatile float* red = reinterpret_cast<volatile float*>(smem + kOffRed);
+  volatile float* alpha_s = reinterpret_cast<volatile float*>(smem + kOffAlpha);
+  volatile float* mu_s = reinterpret_cast<volatile float*>(smem + kOffMu);
+  volatile float* l_s = reinterpret_cast<volatile float*>(smem + kOffL);
+  const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kOffStagePid);
+  uint32_t k = 0, sgi = 0;
+  const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
+
+  for (int s = s_begin; s < s_end; ++s, ++sgi) {
+    const SegInfo sg = load_seg(p, s);
+    const int n = sg.hi - sg.lo;
+    const int row0 = sg.rg * kRows;
+    const int L0 = sg.len - p.q_len;
+    int lim[kRows];  // largest visible key position of each row; -1 for padding rows
 #pragma unroll
-    for (int i = 0; i < 8; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
-    st.m[0] = st.m[1] = -INFINITY;
-    st.l[0] = st.l[1] = 0.f;
+    for (int i = 0; i < kRows; ++i) {
+      const int r = row0 + i;
+      lim[i] = (r < rows_total) ? (p.causal ? L0 + r / p.G : sg.len - 1) : -1;
+    }
+    // ---- Q tile (B operand of Q.K^T) and its scale factors for this group ----
     {
-      // Q fragments of row g: dims 32t + 4s + {0,1} and + {2,3} for k-step s
-      const int r = row0 + g;
-      uint4 qc = make_uint4(0u, 0u, 0u, 0u);
-      uint32_t qs = 0;
-      if (r < rows_total) {
-        const int tok = r / p.G, hq = kvh * p.G + r % p.G;
-        const int64_t qrow = ((int64_t)seq * p.q_len + tok) * p.Hq + hq;
-        qc = *reinterpret_cast<const uint4*>(p.q_codes + qrow * 64 + 16 * t);
-        qs = *reinterpret_cast<const uint16_t*>(p.q_scales + qrow * 8 + 2 * t);
+      const int pr = t128 >> 6, nrow = (t128 >> 2) & 15, ch = t128 & 3;
+      const int hh = 2 * pr + (nrow >> 3), r = row0 + (nrow & 7);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (hh < p.Hkv && r < rows_total) {
+        const int64_t qrow = ((int64_t)sg.seq * p.q_len + r / p.G) * p.Hq + hh * p.G + r % p.G;
+        v = *reinterpret_cast<const uint4*>(p.q_codes + qrow * 64 + 16 * ch);
       }
-      const uint32_t sh = cvt_e4m3x2_f16(qs);
-      const uint32_t s0 = dup_lo(sh), s1 = dup_hi(sh);
-      const uint32_t wq[4] = {qc.x, qc.y, qc.z, qc.w};
+      sts128(c.sbase + kOffQ + pr * 1024 + (nrow >> 3) * 512 + ch * 128 + (nrow & 7) * 16, v.x,
+             v.y, v.z, v.w);
+      uint32_t sf[16];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        uint32_t a0, a1, a2, a3;
-        cvt_e2m1x8_f16(wq[w], a0, a1, a2, a3);
-        const uint32_t sc = (w < 2) ? s0 : s1;
-        st.qf[2 * w][0] = hmul2(a0, sc);
-        st.qf[2 * w][1] = hmul2(a1, sc);
-        st.qf[2 * w + 1][0] = hmul2(a2, sc);
-        st.qf[2 * w + 1][1] = hmul2(a3, sc);
+      for (int q = 0; q < 16; ++q) sf[q] = 0u;
+      if (lane < 16) {
+#pragma unroll
+        for (int pr2 = 0; pr2 < 2; ++pr2) {
+          const int h2 = 2 * pr2 + (lane >> 3), r2 = row0 + (lane & 7);
+          if (h2 < p.Hkv && r2 < rows_total) {
+            const int64_t qrow =
+                ((int64_t)sg.seq * p.q_len + r2 / p.G) * p.Hq + h2 * p.G + r2 % p.G;
+            const uint2 qs = *reinterpret_cast<const uint2*>(p.q_scales + qrow * 8);
+            sf[pr2 * 8 + 0] = qs.x;
+            sf[pr2 * 8 + 4] = qs.y;
+          }
+        }
+      }
+      tmem_st16(tbase + c.lane_base + kColSfb, sf);
+      tmem_wait_st();
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bars + 8 * kBarQReady);
+    }
+    float mu[2][kRows], lp[2][kRows];  // running max (raw score units), partial row sums
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr)
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) { mu[pr][i] = -INFINITY; lp[pr][i] = 0.f; }
+
+    write_sfa(c, k, sg.lo, sg.len);
+    for (int j = 0; j < n; ++j, ++k) {
+      if (j + 1 < n) write_sfa(c, k + 1, sg.lo + j + 1, sg.len);
+      const uint32_t b = k & 1, st = k % kStages;
+      wait_bar(c.bars + 8 * (kBarQkDone + b), (k >> 1) & 1, c.timed_out);
+      tc_fence_after();
+      uint32_t sr[2][8];
+#pragma unroll
+      for (int pr = 0; pr < 2; ++pr) {
+        if (pr < c.npairs) tmem_ld8(tbase + c.lane_base + kColS + b * 32 + pr * 16 + c.half * 8, sr[pr]);
+        else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) sr[pr][i] = 0u;
+        }
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bars + 8 * (kBarSFree + b));
+
+      const bool pvalid = stage_pid[st] >= 0;
+      const int kp = (sg.lo + j) * 64 + c.key;
+      float sv[2][kRows];
+      bool need = false;
+#pragma unroll
+      for (int pr = 0; pr < 2; ++pr) {
+        const bool hv = pr < c.npairs && 2 * pr + c.half < p.Hkv && pvalid;
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+          const bool v = hv && kp <= lim[i];
+          sv[pr][i] = v ? __uint_as_float(sr[pr][i]) : -INFINITY;
+          if (v && sv[pr][i] > mu[pr][i] + thr) need = true;
+        }
+      }
+      const int any_need = __any_sync(0xffffffffu, need) ? 1 : 0;
+      if (lane == 0) flags[(k & 1) * 8 + c.sw] = any_need;
+      named_barrier_sync(1, 128);
+      const int fb = (k & 1) * 8;
+      if (flags[fb] | flags[fb + 1] | flags[fb + 2] | flags[fb + 3]) {
+        // raise the running max where the page beats it by more than the margin
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr)
+#pragma unroll
+          for (int i = 0; i < kRows; ++i) {
+            const float m = ord2f(__reduce_max_sync(0xffffffffu, f2ord(sv[pr][i])));
+            if (lane == 0) red[(c.qd * 2 + pr) * 8 + i] = m;
+          }
+        named_barrier_sync(1, 128);
+        bool rescale = false;
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr)
+#pragma unroll
+          for (int i = 0; i < kRows; ++i) {
+            const float pm = fmaxf(red[((2 * c.half) * 2 + pr) * 8 + i],
+                                   red[((2 * c.half + 1) * 2 + pr) * 8 + i]);
+            float a = 1.f;
+            if (pm > mu[pr][i] + thr) {
+              if (mu[pr][i] != -INFINITY) {
+                a = fast_exp2((mu[pr][i] - pm) * p.c2);
+                rescale = true;
+              }
+              mu[pr][i] = pm;
+              lp[pr][i] *= a;
+            }
+            if (lane == 0 && (c.qd & 1) == 0 && 2 * pr + c.half < kMaxHkv)
+              alpha_s[(2 * pr + c.half) * 8 + i] = a;
+          }
+        if (lane == 0 && (c.qd & 1) == 0) flags[16 + c.half] = rescale ? 1 : 0;
+        named_barrier_sync(1, 128);
+        if (flags[16] | flags[17]) {
+          // O holds every earlier page of this segment: wait for those P.V products first
+          if (j > 0) {
+            wait_bar(c.bars + 8 * (kBarPvDone + ((k - 1) & 1)), ((k - 1) >> 1) & 1, c.timed_out);
+            tc_fence_after();
+          }
+          for (int h = 0; h < p.Hkv; ++h) {
+            uint32_t o[16];
+            tmem_ld16(tbase + c.lane_base + kColO + h * 16, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < kRows; ++i) {
+              const float a = alpha_s[h * 8 + i];
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
+              o[8 + i] = __float_as_uint(__uint_as_float(o[8 + i]) * a);
+            }
+            tmem_st16(tbase + c.lane_base + kColO + h * 16, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // ---- P = exp2((s - mu) c2) as f16 hi + lo, B operand of P.V (rows contiguous per key) ----
+      if (k >= 2) wait_bar(c.bars + 8 * (kBarPvDone + b), ((k >> 1) - 1) & 1, c.timed_out);
+#pragma unroll
+      for (int pr = 0; pr < 2; ++pr) {
+        const int hh = 2 * pr + c.half;
+        if (pr >= c.npairs || hh >= p.Hkv) continue;
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int i = 0; i < kRows; i += 2) {
+          const float p0 = (sv[pr][i] != -INFINITY) ? fast_exp2((sv[pr][i] - mu[pr][i]) * p.c2) : 0.f;
+          const float p1 =
+              (sv[pr][i + 1] != -INFINITY) ? fast_exp2((sv[pr][i + 1] - mu[pr][i + 1]) * p.c2) : 0.f;
+          lp[pr][i] += p0;
+          lp[pr][i + 1] += p1;
+          hi[i / 2] = pack_f16x2(p0, p1);
+          lo[i / 2] = pack_f16x2(p0 - f16_lo_to_f32(hi[i / 2]), p1 - f16_hi_to_f32(hi[i / 2]));
+        }
+        const uint32_t a = c.sbase + kOffP + b * kPBytes + hh * 2048 + (c.key >> 3) * 128 +
+                           (c.key & 7) * 16;
+        sts128(a, hi[0], hi[1], hi[2], hi[3]);
+        sts128(a + 1024, lo[0], lo[1], lo[2], lo[3]);
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bars + 8 * (kBarPFull + b));
+    }
+    // ---- segment epilogue: O^T from TMEM (one head dim per lane), row sums, output ----
+    const uint32_t kl = k - 1;  // last page of this segment
+    wait_bar(c.bars + 8 * (kBarPvDone + (kl & 1)), (kl >> 1) & 1, c.timed_out);
+    tc_fence_after();
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr)
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        float v = lp[pr][i];
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+        if (lane == 0) red[(c.qd * 2 + pr) * 8 + i] = v;
+        if (lane == 0 && (c.qd & 1) == 0) mu_s[(2 * pr + c.half) * 8 + i] = mu[pr][i];
+      }
+    named_barrier_sync(1, 128);
+    if (t128 < kMaxHkv * kRows) {
+      const int hh = t128 >> 3, i = t128 & 7, pr = hh >> 1, hf = hh & 1;
+      l_s[t128] = red[((2 * hf) * 2 + pr) * 8 + i] + red[((2 * hf + 1) * 2 + pr) * 8 + i];
+    }
+    named_barrier_sync(1, 128);
+    const bool split = sg.n_seg > 1;
+    const int part_stride = p.Hkv * kPartHeadFloats;
+    for (int h = 0; h < p.Hkv; ++h) {
+      uint32_t o[16];
+      tmem_ld16(tbase + c.lane_base + kColO + h * 16, o);
+      tmem_wait_ld();
+      float* part = split ? p.partials + (int64_t)sg.part * part_stride + h * kPartHeadFloats
+                          : nullptr;
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        const int r = row0 + i;
+        const float ov = __uint_as_float(o[i]) + __uint_as_float(o[8 + i]);  // P hi + P lo
+        const float Ls = l_s[h * 8 + i];
+        if (split) {
+          if (r < rows_total) part[i * 128 + dim] = ov;
+          if (dim == 0) {
+            part[kRows * 128 + i] = mu_s[h * 8 + i];
+            part[kRows * 128 + kRows + i] = Ls;
+          }
+        } else if (r < rows_total && Ls > 0.f) {
+          store_row(p, sg.seq, h, r, dim, ov / Ls);
+        }
       }
     }
-    // pages of this segment: warp group q = warp / 4 takes pages q, q + kGroups, ...; the four
-    // warps of a group split each page into four 16-key sub-tiles
-    const int n_pages = seg.z - seg.y;
-    const int grp = warp >> 2, sub = warp & 3;
-    for (int j = grp; j < n_pages; j += kGroups) {
-      const uint32_t k = kbase + j;
-      const uint32_t slot = k % kSlots;
-      if (!mbar_wait_bounded(bars + 8 * slot, (k / kSlots) & 1)) timed_out = true;
-      if (slot_pid[slot] >= 0) {
-        const int kp0 = (seg.y + j) * kPage;
-        process_subtile(st, ring + slot * kSlotBytes, sub, kp0, len, lim[0], lim[1], p.c2, g, t);
-      } else if (lane == 0 && sub == 0) {
-        flag_status(p.status, KV_NVFP4_DEV_BAD_PAGE);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bars + 8 * kBarOFree);
+    if (split) {
+      // the CTA that completes the group's last segment combines all of its partials
+      __threadfence();
+      named_barrier_sync(1, 128);
+      if (t128 == 0) {
+        __threadfence();
+        const int ticket = atomicAdd(p.counters + sg.group, 1);
+        const int last = ticket == sg.n_seg - 1;
+        if (last) p.counters[sg.group] = 0;  // ready for the next call on this workspace
+        flags[24] = last;
+      }
+      named_barrier_sync(1, 128);
+      if (flags[24]) {
+        __threadfence();
+        const float* pb = p.partials + (int64_t)sg.first_part * part_stride;
+        for (int h = 0; h < p.Hkv; ++h) {
+          for (int i = 0; i < kRows; ++i) {
+            const int r = row0 + i;
+            if (r >= rows_total) continue;
+            const float* ph = pb + h * kPartHeadFloats;
+            float M = -INFINITY;
+            for (int q = 0; q < sg.n_seg; ++q)
+              M = fmaxf(M, __ldcg(ph + (int64_t)q * part_stride + kRows * 128 + i));
+            float Lt = 0.f, Ot = 0.f;
+            for (int q = 0; q < sg.n_seg; ++q) {
+              const float* pq = ph + (int64_t)q * part_stride;
+              const float mq = __ldcg(pq + kRows * 128 + i);
+              const float f = (mq == -INFINITY) ? 0.f : fast_exp2((mq - M) * p.c2);
+              Lt += f * __ldcg(pq + kRows * 128 + kRows + i);
+              Ot += f * __ldcg(pq + i * 128 + dim);
+            }
+            if (Lt > 0.f) store_row(p, sg.seq, h, r, dim, Ot / Lt);
+          }
+        }
+      }
+    }
+    named_barrier_sync(1, 128);  // scratch reused by the next segment
+  }
+  if (c.timed_out && lane == 0) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
+}
+
+// --------------------------------------------------------------------------------------------
+// Dequant warps: V codes x E4M3 scales -> f16 V^T tile (MN-major: 8 dims x 8 keys core tiles).
+// Warp wd takes keys 8 wd .. 8 wd + 7 of every head, each lane one key and one 32-dim quarter; the
+// quarter is rotated by key so that shared-memory reads and writes are free of bank conflicts.
+// --------------------------------------------------------------------------------------------
+__device__ void dequant_warps(const DecodeParams& p, uint8_t* smem, int warp, int lane) {
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + kOffBars;
+  const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kOffStagePid);
+  const int wd = warp - kWarpDequant0;
+  const int key = 8 * wd + (lane & 7);
+  const int quarter = ((lane >> 3) + ((lane & 7) >> 1)) & 3;
+  uint32_t k = 0, hp = 0;
+  bool timed_out = false;
+  const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
+  for (int s = s_begin; s < s_end; ++s) {
+    const SegInfo sg = load_seg(p, s);
+    for (int page = sg.lo; page < sg.hi; ++page, ++k) {
+      const uint32_t st = k % kStages;
+      wait_bar(bars + 8 * (kBarStageFull + st), (k / kStages) & 1, timed_out);
+      const bool kvalid = stage_pid[st] >= 0 && page * 64 + key < sg.len;
+      const uint32_t stage = sbase + kOffStage + st * kStageBytes;
+      for (int h = 0; h < p.Hkv; ++h, ++hp) {
+        const uint32_t slot = hp % kVhSlots;
+        if (hp >= kVhSlots) wait_bar(bars + 8 * (kBarVhFree + slot), ((hp / kVhSlots) - 1) & 1, timed_out);
+        const uint4 cw = lds128(stage + p.Hkv * 4608 + h * 4096 + key * 64 + 16 * quarter);
+        const uint32_t sc = kvalid ? lds16(stage + p.Hkv * 8704 + h * 512 + key * 8 + 2 * quarter) : 0u;
+        const uint32_t sh = cvt_e4m3x2_f16(sc);
+        const uint32_t s0 = dup_lo(sh), s1 = dup_hi(sh);
+        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+        const uint32_t vh = sbase + kOffVh + slot * kVhBytes + (key >> 3) * 2048 + (key & 7) * 16;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t r0, r1, r2, r3;
+          cvt_e2m1x8_f16(words[q], r0, r1, r2, r3);
+          const uint32_t sq = q < 2 ? s0 : s1;  // dims 32 quarter + 8 q .. : block 2 quarter + q / 2
+          sts128(vh + (4 * quarter + q) * 128, hmul2(r0, sq), hmul2(r1, sq), hmul2(r2, sq),
+                 hmul2(r3, sq));
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * (kBarVhFull + slot));
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8 * (kSlots + slot));
+      if (lane == 0) mbar_arrive(bars + 8 * (kBarStageEmpty + st));
     }
-    kbase += n_pages;
-
-    // ---- merge the consumer warps' states in shared memory ----
-    float l0 = st.l[0], l1 = st.l[1];
-#pragma unroll
-    for (int m = 4; m < 32; m <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, m);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, m);
-    }
-    float* Ow = mrg + warp * kPartFloats;  // [dim][8 rows], then m[8], l[8]
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int dA = 16 * g + i, dB = dA + 8;
-      *reinterpret_cast<float2*>(Ow + dA * kRows + 2 * t) = make_float2(st.o[i][0], st.o[i][1]);
-      *reinterpret_cast<float2*>(Ow + dB * kRows + 2 * t) = make_float2(st.o[i][2], st.o[i][3]);
-    }
-    if (g == 0) {
-      Ow[kRows * 128 + 2 * t] = st.m[0];
-      Ow[kRows * 128 + 2 * t + 1] = st.m[1];
-      Ow[kRows * 128 + kRows + 2 * t] = l0;
-      Ow[kRows * 128 + kRows + 2 * t + 1] = l1;
-    }
-    named_barrier_sync(1, kConsumerWarps * 32);
-
-    const bool split = n_seg > 1;
-    float* part = split ? p.partials + (int64_t)seg.w * kPartFloats : nullptr;
-    for (int idx = ctid; idx < kRows * 128; idx += kConsumerWarps * 32) {  // (row, dim)
-      const int row = idx >> 7, dim = idx & 127;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg[w * kPartFloats + kRows * 128 + row]);
-      float L = 0.f, O = 0.f;
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-          const float* base = mrg + w * kPartFloats;
-          const float mw = base[kRows * 128 + row];
-          const float f = (mw == -INFINITY) ? 0.f : fast_exp2((mw - M) * p.c2);
-          L += f * base[kRows * 128 + kRows + row];
-          O += f * base[dim * kRows + row];
-        }
-      }
-      const int r = row0 + row;
-      if (split) {
-        part[row * 128 + dim] = O;
-        if (dim == 0) {
-          part[kRows * 128 + row] = M;
-          part[kRows * 128 + kRows + row] = L;
-        }
-      } else if (r < rows_total && L > 0.f) {
-        store_out(p, seq, kvh, r, dim, O / L);
-      }
-    }
-    if (split) {
-      // ---- ticket: the CTA that finishes the group's last segment combines all partials ----
-      __threadfence();  // this thread's partial writes, visible device-wide before the ticket
-      named_barrier_sync(1, kConsumerWarps * 32);
-      if (ctid == 0) {
-        __threadfence();
-        int32_t* ctr = p.counters + seg.x;
-        const int ticket = atomicAdd(ctr, 1);
-        const int last = (ticket == n_seg - 1);
-        if (last) *ctr = 0;  // ready for the next call on this workspace
-        *flag = last;
-      }
-      named_barrier_sync(1, kConsumerWarps * 32);
-      if (*flag) {
-        __threadfence();
-        const float* pb = p.partials + (int64_t)first_part * kPartFloats;
-        for (int idx = ctid; idx < kRows * 128; idx += kConsumerWarps * 32) {
-          const int row = idx >> 7, dim = idx & 127;
-          const int r = row0 + row;
-          if (r >= rows_total) continue;
-          float M = -INFINITY;
-          for (int c = 0; c < n_seg; ++c) M = fmaxf(M, __ldcg(pb + c * kPartFloats + kRows * 128 + row));
-          float L = 0.f, O = 0.f;
-          for (int c = 0; c < n_seg; ++c) {
-            const float* q = pb + c * kPartFloats;
-            const float mc = __ldcg(q + kRows * 128 + row);
-            const float f = (mc == -INFINITY) ? 0.f : fast_exp2((mc - M) * p.c2);
-            L += f * __ldcg(q + kRows * 128 + kRows + row);
-            O += f * __ldcg(q + row * 128 + dim);
-          }
-          if (L > 0.f) store_out(p, seq, kvh, r, dim, O / L);
-        }
-      }
-    }
-    named_barrier_sync(1, kConsumerWarps * 32);  // merge area reused by the next segment
   }
   if (timed_out && lane == 0) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
+__global__ void __maxnreg__(144) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bars = smem_u32(smem + kOffBars);
   if (threadIdx.x == 0) {
-    const uint32_t bars = smem_u32(smem + kBarOff);
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(bars + 8 * s, 1);
-      mbar_init(bars + 8 * (kSlots + s), 4);  // released by the page's four warps
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bars + 8 * (kBarStageFull + s), 1);
+      mbar_init(bars + 8 * (kBarStageEmpty + s), 4 + kDequantWarps + 1);
     }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bars + 8 * (kBarSfaFull + b), 4);
+      mbar_init(bars + 8 * (kBarQkDone + b), 1);
+      mbar_init(bars + 8 * (kBarSFree + b), 4);
+      mbar_init(bars + 8 * (kBarPFull + b), 4);
+      mbar_init(bars + 8 * (kBarPvDone + b), 1);
+    }
+    for (int v = 0; v < kVhSlots; ++v) {
+      mbar_init(bars + 8 * (kBarVhFull + v), kDequantWarps);
+      mbar_init(bars + 8 * (kBarVhFree + v), 1);
+    }
+    mbar_init(bars + 8 * kBarQReady, 4);
+    mbar_init(bars + 8 * kBarOFree, 4);
     fence_mbar_init();
   }
+  if (warp == kWarpMma) tmem_alloc(smem_u32(smem + kOffTmemSlot), kTmemCols);
+  tc_fence_before();
   __syncthreads();
-  if (warp == kConsumerWarps) {
+  tc_fence_after();
+  const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
+
+  if (warp == kWarpProducer) {
     producer(p, smem, lane);
-    return;
+  } else if (warp == kWarpMma) {
+    if (lane == 0) mma_issuer(p, smem, tbase);
+  } else if (warp < kWarpDequant0) {
+    softmax_warps(p, smem, tbase, warp, lane);
+  } else {
+    dequant_warps(p, smem, warp, lane);
   }
-  consumer(p, smem, warp, lane);
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tbase, kTmemCols);
 }
 
 }  // namespace
 
 int decode_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const uint8_t* k_codes,
-                          const uint8_t* k_scales, const uint8_t* v_codes,
-                          const uint8_t* v_scales, const int32_t* block_table, int32_t max_pages,
-                          int32_t num_pages, const void* groups, const void* segments,
-                          const int32_t* cta_seg, int32_t* counters, float* partials, float* out,
-                          int32_t* status, int32_t Hq, int32_t Hkv, int32_t q_len, int32_t causal,
-                          int32_t grid, float sm_scale, cudaStream_t stream) {
+cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const uint8_t* pool,
+                          const int32_t* block_table, int32_t max_pages, int32_t num_pages,
+                          const void* groups, const void* segments, const int32_t* cta_seg,
+                          int32_t* counters, float* partials, float* out, int32_t* status,
+                          int32_t Hq, int32_t Hkv, int32_t q_len, int32_t causal, int32_t grid,
+                          float sm_scale, cudaStream_t stream) {
   static bool attr_done = false;  // the attribute belongs to the function, set once per process
   if (!attr_done) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -479,9 +701,9 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
+  if (Hkv < 1 || Hkv > kMaxHkv) return cudaErrorInvalidValue;
   DecodeParams p;
-  p.q_codes = q_codes; p.q_scales = q_scales;
-  p.k_codes = k_codes; p.k_scales = k_scales; p.v_codes = v_codes; p.v_scales = v_scales;
+  p.q_codes = q_codes; p.q_scales = q_scales; p.pool = pool;
   p.block_table = block_table; p.max_pages = max_pages; p.num_pages = num_pages;
   p.groups = reinterpret_cast<const int4*>(groups);
   p.segments = reinterpret_cast<const int4*>(segments);

@@ -14,17 +14,22 @@
  *   [YaRN]  same page, section "YaRN context extension": theta = 1e7, 25 % of the head dims
  *           rotary, linear position scaling.
  *
- * Data layout (all byte planes, caller-allocated, 16-byte aligned):
- *   Pool planes, one page = 64 token slots:
- *     k_codes  [num_pages][num_kv_heads][64][64]  E2M1 codes; element 2j in the low nibble of
- *                                                 byte j, element 2j+1 in the high nibble
- *     k_scales [num_pages][num_kv_heads][64][8]   E4M3 scale b covers elements 16b..16b+15
- *     v_codes, v_scales: same shapes.
- *   => 64 + 8 bytes for K and again for V: 144 bytes per token per KV head [NVFP4].
+ * Data layout (caller-allocated device memory, 16-byte aligned):
+ *   Pool: num_pages blocks of kv_nvfp4_page_bytes() = num_kv_heads * 9216 bytes, one block per
+ *   page of 64 token slots holding every KV head. Within a block (H = num_kv_heads):
+ *     [0, 4096 H)          K codes, head h at 4096 h, in the tensor-core tile order: byte j
+ *                          (0..63) of slot k sits at (k / 8) * 512 + (j / 16) * 128 +
+ *                          (k % 8) * 16 + (j % 16), i.e. 8-slot x 16-byte core tiles
+ *     [4096 H, 4608 H)     K scales, head h at 4096 H + 512 h: slot k at 8 k (row-major)
+ *     [4608 H, 8704 H)     V codes, head h at 4608 H + 4096 h: slot k at 64 k (row-major)
+ *     [8704 H, 9216 H)     V scales, head h at 8704 H + 512 h: slot k at 8 k (row-major)
+ *   A 64-byte code row holds 128 E2M1 codes: element 2j in the low nibble of byte j, element
+ *   2j+1 in the high nibble. A scale row holds 8 E4M3 scales; scale b covers elements
+ *   16b..16b+15. => 64 + 8 bytes for K and again for V: 144 bytes per token per KV head.
  *   Token `pos` of sequence `s` lives in page block_table[s * max_pages + pos / 64], slot
  *   pos % 64. K rows are stored after RoPE and the normalised Hadamard rotation; V rows raw.
- *   Quantised Q: q_codes [tokens][num_q_heads][64], q_scales [tokens][num_q_heads][8], after
- *   RoPE and rotation, in the same encoding.
+ *   Quantised Q: q_codes [tokens][num_q_heads][64] (row-major), q_scales
+ *   [tokens][num_q_heads][8], after RoPE and rotation, in the same encoding.
  *
  * Ownership: the caller allocates and frees every device buffer. No entry point allocates
  * device memory. A plan workspace belongs to the stream it was planned on: reuse or overwrite
@@ -73,9 +78,11 @@ typedef struct kv_nvfp4_layout {
 } kv_nvfp4_layout;
 
 /* Filled by kv_nvfp4_plan; passed unchanged to kv_nvfp4_decode_attn. A group is one
- * (sequence, kv head, tile of 8 query rows); its keys are split into chunks of chunk_pages
- * pages, and the chunks of all groups are shared out over `grid` CTAs in contiguous, page-balanced
- * ranges (one range may hold several chunks of a group, which the CTA combines as it goes). */
+ * (sequence, tile of 8 query rows per KV head), covering every KV head; its pages are split into
+ * chunks of chunk_pages pages, and the chunks of all groups are shared out over `grid` CTAs in
+ * contiguous, page-balanced ranges (one range may hold several chunks of a group, which the CTA
+ * combines as it goes). A row is (query token, head within the GQA group): row = token * group +
+ * head_in_group. */
 typedef struct kv_nvfp4_plan_info {
   int32_t num_seqs;
   int32_t q_len;
@@ -83,8 +90,8 @@ typedef struct kv_nvfp4_plan_info {
                               visible key of a row tile are not visited) */
   int32_t chunk_pages;     /* split-K granularity, in pages */
   int32_t num_kv_heads;
-  int32_t num_row_groups;  /* ceil(group * q_len / 8) row tiles per (sequence, kv head) */
-  int32_t num_groups;      /* num_seqs * num_kv_heads * num_row_groups */
+  int32_t num_row_groups;  /* ceil(group * q_len / 8) row tiles per sequence */
+  int32_t num_groups;      /* num_seqs * num_row_groups */
   int32_t num_segments;    /* contiguous (group, page range) pieces over all CTAs */
   int32_t num_partials;    /* partial-result slots (segments of groups split over CTAs) */
   int32_t grid;            /* CTAs of the attention launch, at most the SM count */
@@ -109,9 +116,9 @@ kv_nvfp4_status kv_nvfp4_layout_check(const kv_nvfp4_layout *layout);
  * 64 * 144 * num_kv_heads (36,864 for 4 KV heads) [NVFP4]. 0 on an invalid layout. */
 size_t kv_nvfp4_page_bytes(const kv_nvfp4_layout *layout);
 
-/* Sizes of one code plane and one scale plane for a pool of num_pages pages. */
-kv_nvfp4_status kv_nvfp4_pool_plane_bytes(const kv_nvfp4_layout *layout, int32_t num_pages,
-                                          size_t *code_plane_bytes, size_t *scale_plane_bytes);
+/* Bytes of a pool of num_pages pages (num_pages * kv_nvfp4_page_bytes). */
+kv_nvfp4_status kv_nvfp4_pool_bytes(const kv_nvfp4_layout *layout, int32_t num_pages,
+                                    size_t *bytes);
 
 /* ---- RoPE table [YaRN] ----------------------------------------------------------------------
  * fp32 table [max_pos][rot_dim]: entries 0..rot_dim/2-1 are cos, rot_dim/2..rot_dim-1 are sin,
@@ -143,7 +150,7 @@ kv_nvfp4_status kv_nvfp4_rope_table_init(float *d_table, int32_t max_pos, int32_
  *   d_positions:    DEVICE int32 [T], absolute position of each token in its sequence
  *   d_rope_table:   DEVICE fp32 table from kv_nvfp4_rope_table_init, rope_max_pos rows
  *   d_block_table:  DEVICE int32 [num_seqs][max_pages]
- *   k_/v_codes/scales: DEVICE pool planes of num_pages pages (see layout above)
+ *   pool:           DEVICE pool of num_pages pages (see layout above)
  *   q_codes/q_scales: DEVICE [T][num_q_heads][64] / [T][num_q_heads][8]
  *   d_status:       DEVICE int32 or NULL
  * One kernel launch. T = 0 is a no-op. */
@@ -152,8 +159,7 @@ kv_nvfp4_status kv_nvfp4_append(const kv_nvfp4_layout *layout, const void *q, co
                                 const int32_t *d_positions, int32_t T, const float *d_rope_table,
                                 int32_t rope_max_pos, const int32_t *d_block_table,
                                 int32_t num_seqs, int32_t max_pages, int32_t num_pages,
-                                uint8_t *k_codes, uint8_t *k_scales, uint8_t *v_codes,
-                                uint8_t *v_scales, uint8_t *q_codes, uint8_t *q_scales,
+                                uint8_t *pool, uint8_t *q_codes, uint8_t *q_scales,
                                 int32_t *d_status, void *stream);
 
 /* ---- Page-table / split-K setup ------------------------------------------------------------
@@ -171,8 +177,7 @@ kv_nvfp4_status kv_nvfp4_plan_workspace_bytes(const kv_nvfp4_layout *layout,
 /* Host-only variant of kv_nvfp4_plan for a given CTA count: writes the image of the workspace
  * tables (groups, segments, per-CTA segment ranges, zeroed tickets; everything before
  * info->off_partials) into HOST memory h_workspace and fills *info. No CUDA call. Layout of the
- * image: groups are 8 int32 {seq, kv_head, row_tile, seq_len, n_segments, first_partial,
- * pages, 0}; segments are 4 int32 {group, page_lo, page_hi, partial or -1}; CTA b owns
+ * image: groups are 8 int32 {seq, 0, row_tile, seq_len, n_segments, first_partial, pages, 0}; segments are 4 int32 {group, page_lo, page_hi, partial or -1}; CTA b owns
  * segments [cta[b], cta[b+1]). */
 kv_nvfp4_status kv_nvfp4_plan_host(const kv_nvfp4_layout *layout, const int32_t *h_seq_lens,
                                    int32_t num_seqs, int32_t q_len, int32_t causal,
@@ -181,7 +186,9 @@ kv_nvfp4_status kv_nvfp4_plan_host(const kv_nvfp4_layout *layout, const int32_t 
 
 /* Writes the work list into DEVICE memory d_workspace (ws_bytes at least the size above) on
  * `stream`, zeroes the merge tickets, and fills *info (HOST). Every seq_len must be >= q_len
- * and >= 1. The CTA count is taken from the current device's SM count. */
+ * and >= 1. The CTA count is taken from the current device's SM count. The workspace holds
+ * one (m, l, O) partial of num_kv_heads * 4160 bytes per segment of a group spread over several
+ * CTAs. */
 kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout *layout, const int32_t *h_seq_lens,
                               int32_t num_seqs, int32_t q_len, int32_t causal,
                               int32_t chunk_tokens, void *d_workspace, size_t ws_bytes,
@@ -197,14 +204,13 @@ kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout *layout, const int32_t *h_se
  *   plan, d_workspace: from kv_nvfp4_plan (same stream)
  *   q_codes/q_scales: DEVICE [num_seqs * q_len][num_q_heads][64 | 8], sequence-major
  *   sm_scale:       softmax scale; <= 0 selects 1/sqrt(head_dim)
+ *   pool, num_pages, d_block_table, max_pages: as for kv_nvfp4_append
  *   out:            DEVICE fp32 [num_seqs * q_len][num_q_heads][128]
- * One kernel launch. */
+ * Supports num_kv_heads <= 4 (every head of a page is staged together). One kernel launch. */
 kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout *layout,
                                      const kv_nvfp4_plan_info *plan, void *d_workspace,
                                      const uint8_t *q_codes, const uint8_t *q_scales,
-                                     float sm_scale, const uint8_t *k_codes,
-                                     const uint8_t *k_scales, const uint8_t *v_codes,
-                                     const uint8_t *v_scales, int32_t num_pages,
+                                     float sm_scale, const uint8_t *pool, int32_t num_pages,
                                      const int32_t *d_block_table, int32_t max_pages, float *out,
                                      int32_t *d_status, void *stream);
 

@@ -75,7 +75,7 @@ def _declare(L):
     L.orc_quantize_rows.restype = None
     L.orc_dequant_rows.argtypes = [_P, _P, _I64, _P]
     L.orc_dequant_rows.restype = None
-    L.orc_paged_gather.argtypes = [_P, _P, _I32, _I32, _P, _I32, _I32, _I32, _I32, _P, _P]
+    L.orc_paged_gather.argtypes = [_P, _I32, _I32, _P, _I32, _I32, _I32, _I32, _P, _P, _P, _P]
     L.orc_paged_gather.restype = _I64
     L.orc_attention_rows.argtypes = [_I32, _I32, _I32, _I32, _F64, _P, _P, _P, _P, _P, _P, _P,
                                      _P, _I64, _P, _P, _P, _P, _I32]
@@ -175,17 +175,18 @@ def dequant_rows(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     return out
 
 
-def paged_gather(pool_codes, pool_scales, num_pages, kv_heads, block_table, seq, pos0, n_tok):
-    """Read tokens [pos0, pos0+n_tok) of one sequence out of pool planes laid out as
-    [page][kv_head][64 slots][64 | 8 bytes]. Returns (codes [n,H,64], scales [n,H,8], bad)."""
-    pc = np.ascontiguousarray(pool_codes, dtype=np.uint8)
-    ps = np.ascontiguousarray(pool_scales, dtype=np.uint8)
+def paged_gather(pool, num_pages, kv_heads, block_table, seq, pos0, n_tok):
+    """Read tokens [pos0, pos0+n_tok) of one sequence out of a pool of page blocks (layout in
+    kv_oracle.cpp). Returns (k_codes [n,H,64], k_scales [n,H,8], v_codes, v_scales, bad)."""
+    pl = np.ascontiguousarray(pool, dtype=np.uint8)
     bt = np.ascontiguousarray(block_table, dtype=np.int32)
-    codes = np.empty((n_tok, kv_heads, 64), np.uint8)
-    scales = np.empty((n_tok, kv_heads, 8), np.uint8)
-    bad = lib().orc_paged_gather(_ptr(pc), _ptr(ps), num_pages, kv_heads, _ptr(bt), bt.shape[1],
-                                 seq, pos0, n_tok, _ptr(codes), _ptr(scales))
-    return codes, scales, int(bad)
+    kc = np.empty((n_tok, kv_heads, 64), np.uint8)
+    ks = np.empty((n_tok, kv_heads, 8), np.uint8)
+    vc = np.empty((n_tok, kv_heads, 64), np.uint8)
+    vs = np.empty((n_tok, kv_heads, 8), np.uint8)
+    bad = lib().orc_paged_gather(_ptr(pl), num_pages, kv_heads, _ptr(bt), bt.shape[1], seq, pos0,
+                                 n_tok, _ptr(kc), _ptr(ks), _ptr(vc), _ptr(vs))
+    return kc, ks, vc, vs, int(bad)
 
 
 def attention_rows(q_heads, kv_heads, q_len, causal, sm_scale, seq_lens, tok_off,

@@ -236,32 +236,44 @@ void orc_dequant_rows(const uint8_t* codes, const uint8_t* scales, int64_t n_row
 }
 
 // ---------------------------------------------------------------------------------------------
-// Paged store: the pool planes are [page][kv_head][64 slots][64 code bytes] and
-// [page][kv_head][64 slots][8 scale bytes]; token `pos` of sequence `s` lives in page
-// block_table[s * max_pages + pos / 64], slot pos % 64. This gathers a contiguous
-// [n_tok][kv_heads][...] view out of a pool so that it can be compared with oracle arrays.
-// Returns the number of rows whose page id was outside [0, num_pages).
+// Paged layout. A pool is num_pages blocks of H * 9216 bytes (H = kv_heads), one block per page
+// of 64 token slots holding every head: [K codes, H x 4096][K scales, H x 512][V codes, H x 4096]
+// [V scales, H x 512]. K codes of head h are kept in 8-slot x 16-byte tiles: byte j of slot k is
+// at h*4096 + (k/8)*512 + (j/16)*128 + (k%8)*16 + (j%16). Scales and V codes are row-major per
+// slot. Token `pos` of sequence `seq` lives in page block_table[seq * max_pages + pos / 64], slot
+// pos % 64. This gathers rows [n_tok][kv_heads][64 | 8] back out of a pool so that they can be
+// compared with oracle arrays. Returns the number of rows whose page id was outside the pool.
 // ---------------------------------------------------------------------------------------------
-int64_t orc_paged_gather(const uint8_t* pool_codes, const uint8_t* pool_scales, int32_t num_pages,
-                         int32_t kv_heads, const int32_t* block_table, int32_t max_pages,
-                         int32_t seq, int32_t pos0, int32_t n_tok, uint8_t* codes_out,
-                         uint8_t* scales_out) {
+int64_t orc_paged_gather(const uint8_t* pool, int32_t num_pages, int32_t kv_heads,
+                         const int32_t* block_table, int32_t max_pages, int32_t seq,
+                         int32_t pos0, int32_t n_tok, uint8_t* k_codes, uint8_t* k_scales,
+                         uint8_t* v_codes, uint8_t* v_scales) {
   int64_t bad = 0;
+  const int64_t H = kv_heads;
   for (int32_t i = 0; i < n_tok; ++i) {
     const int32_t pos = pos0 + i;
     const int32_t page = block_table[(int64_t)seq * max_pages + pos / 64];
+    const int32_t k = pos % 64;
     for (int32_t h = 0; h < kv_heads; ++h) {
-      uint8_t* c = codes_out + ((int64_t)i * kv_heads + h) * 64;
-      uint8_t* s = scales_out + ((int64_t)i * kv_heads + h) * 8;
+      const int64_t row = (int64_t)i * kv_heads + h;
+      uint8_t* kc = k_codes + row * 64;
+      uint8_t* ks = k_scales + row * 8;
+      uint8_t* vc = v_codes + row * 64;
+      uint8_t* vs = v_scales + row * 8;
       if (page < 0 || page >= num_pages) {
-        std::memset(c, 0, 64);
-        std::memset(s, 0, 8);
+        std::memset(kc, 0, 64);
+        std::memset(ks, 0, 8);
+        std::memset(vc, 0, 64);
+        std::memset(vs, 0, 8);
         ++bad;
         continue;
       }
-      const int64_t slot = ((int64_t)page * kv_heads + h) * 64 + pos % 64;
-      std::memcpy(c, pool_codes + slot * 64, 64);
-      std::memcpy(s, pool_scales + slot * 8, 8);
+      const uint8_t* blk = pool + (int64_t)page * H * 9216;
+      for (int j = 0; j < 64; ++j)
+        kc[j] = blk[h * 4096 + (k / 8) * 512 + (j / 16) * 128 + (k % 8) * 16 + (j % 16)];
+      std::memcpy(ks, blk + H * 4096 + h * 512 + k * 8, 8);
+      std::memcpy(vc, blk + H * 4608 + h * 4096 + k * 64, 64);
+      std::memcpy(vs, blk + H * 8704 + h * 512 + k * 8, 8);
     }
   }
   return bad;

@@ -75,9 +75,7 @@ class GpuRun:
                 self.q_scales.view(self.T, H, 8).cpu().numpy())
 
     def pool(self):
-        c = self.cache
-        return (c.k_codes.cpu().numpy(), c.k_scales.cpu().numpy(), c.v_codes.cpu().numpy(),
-                c.v_scales.cpu().numpy())
+        return self.cache.pool.cpu().numpy()
 
 
 # ------------------------------------------------------------------------------------------------
@@ -167,20 +165,20 @@ def cosine(a: np.ndarray, b: np.ndarray) -> float:
 
 def compare_pool(g: GpuRun, o: OracleRun):
     """Bit-exact comparison of every K/V row of the workload as stored in the GPU pool.
-    Returns the number of mismatching rows per plane."""
+    Returns the number of mismatching rows per kind."""
     w = g.w
-    kc, ks, vc, vs = g.pool()
+    pool = g.pool()
     bad = {"k_codes": 0, "k_scales": 0, "v_codes": 0, "v_scales": 0}
     for s in range(w.num_seqs):
         L = int(w.seq_lens[s])
         o0 = o.tok_off[s]
-        c, sc, nbad = oracle.paged_gather(kc, ks, w.pool_pages, w.kv_heads, w.block_table, s, 0, L)
+        kc, ks, vc, vs, nbad = oracle.paged_gather(pool, w.pool_pages, w.kv_heads, w.block_table,
+                                                   s, 0, L)
         assert nbad == 0
-        bad["k_codes"] += int(np.any(c != o.kc[o0:o0 + L], axis=-1).sum())
-        bad["k_scales"] += int(np.any(sc != o.ks[o0:o0 + L], axis=-1).sum())
-        c, sc, nbad = oracle.paged_gather(vc, vs, w.pool_pages, w.kv_heads, w.block_table, s, 0, L)
-        bad["v_codes"] += int(np.any(c != o.vc[o0:o0 + L], axis=-1).sum())
-        bad["v_scales"] += int(np.any(sc != o.vs[o0:o0 + L], axis=-1).sum())
+        bad["k_codes"] += int(np.any(kc != o.kc[o0:o0 + L], axis=-1).sum())
+        bad["k_scales"] += int(np.any(ks != o.ks[o0:o0 + L], axis=-1).sum())
+        bad["v_codes"] += int(np.any(vc != o.vc[o0:o0 + L], axis=-1).sum())
+        bad["v_scales"] += int(np.any(vs != o.vs[o0:o0 + L], axis=-1).sum())
     return bad
 
 

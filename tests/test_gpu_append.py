@@ -69,10 +69,7 @@ def _append_crafted(Hq, Hkv, T, seed, rot_dim=32):
     table = oracle.rope_table(T, rot_dim, 1e7, 1.0)
     ek, eks = oracle.quantize_rows(rows_k, np.repeat(pos, Hkv), True, table, rot_dim)
     ev, evs = oracle.quantize_rows(rows_v, None, False, None, 0)
-    kc, ks, _ = oracle.paged_gather(cache.k_codes.cpu().numpy(), cache.k_scales.cpu().numpy(),
-                                    pages + 3, Hkv, bt, 0, 0, T)
-    vc, vs, _ = oracle.paged_gather(cache.v_codes.cpu().numpy(), cache.v_scales.cpu().numpy(),
-                                    pages + 3, Hkv, bt, 0, 0, T)
+    kc, ks, vc, vs, _ = oracle.paged_gather(cache.pool.cpu().numpy(), pages + 3, Hkv, bt, 0, 0, T)
     assert np.array_equal(kc.reshape(-1, 64), ek) and np.array_equal(ks.reshape(-1, 8), eks)
     assert np.array_equal(vc.reshape(-1, 64), ev) and np.array_equal(vs.reshape(-1, 8), evs)
     if Hq:
@@ -109,14 +106,24 @@ def test_append_reports_bad_rows_and_skips_them():
     T = 4
     k = torch.randn(T, 4, 128, device=dev).to(torch.bfloat16)
     v = torch.randn(T, 4, 128, device=dev).to(torch.bfloat16)
-    cache.k_codes.fill_(0xAB)
+    cache.pool.fill_(0xAB)
     sid = torch.tensor([0, 1, 5, 0], dtype=torch.int32, device=dev)      # seq 5 does not exist
     pos = torch.tensor([3, 70, 1, 200], dtype=torch.int32, device=dev)   # 70 -> page 99; 200 beyond
     cache.append(k, v, sid, pos)
     torch.cuda.synchronize()
     st = int(cache.status.item())
     assert st & kv.DEV_BAD_PAGE and st & kv.DEV_BAD_SEQ and st & kv.DEV_BAD_POS
-    codes = cache.k_codes.view(3, 4, 64, 64).cpu().numpy()
-    assert np.any(codes[0, :, 3] != 0xAB)           # the one valid token was written
-    untouched = codes.copy(); untouched[0, :, 3] = 0xAB
-    assert np.all(untouched == 0xAB)                 # nothing else was
+    pool = cache.pool.cpu().numpy()
+    changed = np.nonzero(pool != 0xAB)[0]
+    # only page 0, slot 3 of every head was written (codes, scales of K and V)
+    kc, ks, vc, vs, _ = oracle.paged_gather(pool, 3, 4, np.array([[0]], np.int32), 0, 3, 1)
+    assert changed.size > 0 and changed.max() < 4 * 9216
+    expected = set()
+    for h in range(4):
+        for j in range(64):
+            expected.add(h * 4096 + (3 // 8) * 512 + (j // 16) * 128 + (3 % 8) * 16 + j % 16)
+            expected.add(4 * 4608 + h * 4096 + 3 * 64 + j)
+        for j in range(8):
+            expected.add(4 * 4096 + h * 512 + 3 * 8 + j)
+            expected.add(4 * 8704 + h * 512 + 3 * 8 + j)
+    assert set(changed.tolist()) <= expected

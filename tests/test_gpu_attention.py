@@ -40,7 +40,7 @@ def test_attention_small(lens, q_len, causal, chunk):
     _check(w, chunk=chunk, steps=2)
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (4, 4), (16, 2), (7, 7)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 1), (4, 4), (16, 2), (9, 3), (3, 3)])
 def test_attention_other_group_sizes(Hq, Hkv):
     w = synth.Workload("groups", [300, 1200], q_len=2, seed=Hq * 10 + Hkv, q_heads=Hq,
                        kv_heads=Hkv, chunk_tokens=256)

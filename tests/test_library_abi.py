@@ -35,12 +35,11 @@ def test_exports_every_declared_symbol(kv):
         assert hasattr(raw, n), f"{n} declared in the header but not exported"
 
 
-def test_page_and_plane_bytes(kv):
+def test_page_and_pool_bytes(kv):
     L = kv.make_layout()
     assert kv.kv_nvfp4_page_bytes(L) == 64 * 144 * 4 == 36864
-    c, s = kv.kv_nvfp4_pool_plane_bytes(L, 10)
-    assert c == 10 * 4 * 64 * 64 and s == 10 * 4 * 64 * 8
-    assert (c + s) * 2 // (10 * 4 * 64) == 144
+    n = kv.kv_nvfp4_pool_bytes(L, 10)
+    assert n == 10 * 36864 and n // (10 * 4 * 64) == 144
 
 
 @pytest.mark.parametrize("bad", [dict(head_dim=64), dict(page_size=32), dict(num_q_heads=10),
@@ -65,10 +64,10 @@ def test_plan_sizes_and_validation(kv):
     L = kv.make_layout()
     n = kv.kv_nvfp4_plan_workspace_bytes(L, [4097], 1, True, 1024)
     assert n > 0
-    # 4 x 131073 tokens, 16 groups spread over many CTAs: every group is split, one 4160 B
-    # partial per segment
+    # 4 x 131073 tokens, 4 groups spread over many CTAs: every group is split, one partial of
+    # 4 heads x 4160 B per segment
     n2 = kv.kv_nvfp4_plan_workspace_bytes(L, [131073] * 4, 1, True, 1024)
-    assert n2 >= 16 * 2 * 4160
+    assert n2 >= 4 * 2 * 4 * 4160
     lib = kv.lib()
     sl = np.array([5, 3], np.int32)
     size = ctypes.c_size_t()
@@ -87,17 +86,20 @@ def test_entry_points_reject_bad_arguments_before_cuda(kv):
     L = kv.make_layout()
     bad = kv.Layout(24, 4, 64, 64, 32)
     assert lib.kv_nvfp4_append(ctypes.byref(bad), *([None] * 5), 1, None, 1, None, 1, 1, 1,
-                               *([None] * 8), None) == kv.KV_NVFP4_EINVAL
+                               *([None] * 5)) == kv.KV_NVFP4_EINVAL
     # null K pointer
     assert lib.kv_nvfp4_append(ctypes.byref(L), *([None] * 5), 1, None, 1, None, 1, 1, 1,
-                               *([None] * 8), None) == kv.KV_NVFP4_EINVAL
+                               *([None] * 5)) == kv.KV_NVFP4_EINVAL
     # T = 0 is a no-op that needs no buffers
     assert lib.kv_nvfp4_append(ctypes.byref(L), *([None] * 5), 0, None, 1, None, 1, 1, 1,
-                               *([None] * 8), None) == kv.KV_NVFP4_OK
+                               *([None] * 5)) == kv.KV_NVFP4_OK
     info = kv.PlanInfo()
     assert lib.kv_nvfp4_decode_attn(ctypes.byref(L), ctypes.byref(info), None, None, None,
-                                    0.0, None, None, None, None, 1, None, 1, None, None,
-                                    None) == kv.KV_NVFP4_EINVAL
+                                    0.0, None, 1, None, 1, None, None, None) == kv.KV_NVFP4_EINVAL
+    # more than four KV heads per page is rejected by the attention entry point
+    L8 = kv.make_layout(8, 8)
+    assert lib.kv_nvfp4_decode_attn(ctypes.byref(L8), ctypes.byref(info), None, None, None,
+                                    0.0, None, 1, None, 1, None, None, None) == kv.KV_NVFP4_EINVAL
     assert kv.lib().kv_nvfp4_status_string(-1) == b"invalid argument"
 
 
@@ -111,11 +113,12 @@ def test_plan_covers_every_visible_page_once_and_balances(kv, lens, q_len, causa
     info, groups, segs, cta = kv.kv_nvfp4_plan_host(L, lens, q_len, causal, chunk, ctas)
     G = 6
     n_rg = (G * q_len + 7) // 8
-    assert info.num_groups == len(lens) * 4 * n_rg == len(groups)
+    assert info.num_groups == len(lens) * n_rg == len(groups)
     # expected visited pages per group: up to the last key any row of the tile can see
     gi = np.arange(len(groups))
-    s_, h_, rg_ = groups[:, 0], groups[:, 1], groups[:, 2]
-    assert np.array_equal(gi, (s_ * 4 + h_) * n_rg + rg_)
+    s_, rg_ = groups[:, 0], groups[:, 2]
+    assert np.all(groups[:, 1] == 0)
+    assert np.array_equal(gi, s_ * n_rg + rg_)
     assert np.array_equal(groups[:, 3], np.asarray(lens)[s_])
     last_row = np.minimum(G * q_len - 1, 8 * rg_ + 7)
     vis = (groups[:, 3] - q_len + last_row // G + 1) if causal else groups[:, 3]

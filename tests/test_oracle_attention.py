@@ -134,24 +134,32 @@ def test_quantize_rows_composes_rope_fwht_quant():
 
 
 def test_paged_gather_layout():
-    # pool planes [page][head][slot][bytes]: fill every slot with a pattern naming it
+    # fill every byte of a pool with a value naming (page, region, head, slot, byte) per the
+    # documented block layout, then check the gather returns each slot's own bytes
     P, H = 6, 3
-    codes = np.zeros((P, H, 64, 64), np.uint8)
-    scales = np.zeros((P, H, 64, 8), np.uint8)
+    blk = H * 9216
+    pool = np.zeros(P * blk, np.uint8)
     for p in range(P):
+        b = pool[p * blk:(p + 1) * blk]
         for h in range(H):
-            for s in range(64):
-                codes[p, h, s, 0], codes[p, h, s, 1], codes[p, h, s, 2] = p, h, s
-                scales[p, h, s, 0], scales[p, h, s, 1] = p * 10 + h, s
+            for k in range(64):
+                for j in range(64):
+                    b[h * 4096 + (k // 8) * 512 + (j // 16) * 128 + (k % 8) * 16 + j % 16] = (p * 7 + h * 3 + k + j) % 251
+                    b[H * 4608 + h * 4096 + k * 64 + j] = (p * 5 + h + 2 * k + j) % 253
+                for j in range(8):
+                    b[H * 4096 + h * 512 + k * 8 + j] = (p + h * 11 + k + 3 * j) % 241
+                    b[H * 8704 + h * 512 + k * 8 + j] = (p * 13 + h + k + j) % 239
     bt = np.array([[4, 1, 5], [0, 2, 3]], np.int32)
-    c, s, bad = oracle.paged_gather(codes, scales, P, H, bt, 1, 60, 70)
+    kc, ks, vc, vs, bad = oracle.paged_gather(pool, P, H, bt, 1, 60, 70)
     assert bad == 0
     for i in range(70):
         pos = 60 + i
-        page = bt[1, pos // 64]
+        p, k = bt[1, pos // 64], pos % 64
         for h in range(H):
-            assert tuple(c[i, h, :3]) == (page, h, pos % 64)
-            assert tuple(s[i, h, :2]) == (page * 10 + h, pos % 64)
+            assert list(kc[i, h]) == [(p * 7 + h * 3 + k + j) % 251 for j in range(64)]
+            assert list(vc[i, h]) == [(p * 5 + h + 2 * k + j) % 253 for j in range(64)]
+            assert list(ks[i, h]) == [(p + h * 11 + k + 3 * j) % 241 for j in range(8)]
+            assert list(vs[i, h]) == [(p * 13 + h + k + j) % 239 for j in range(8)]
     bt2 = np.array([[4, 9]], np.int32)
-    _, _, bad = oracle.paged_gather(codes, scales, P, H, bt2, 0, 0, 100)
+    *_, bad = oracle.paged_gather(pool, P, H, bt2, 0, 0, 100)
     assert bad == (100 - 64) * H
