@@ -51,6 +51,7 @@ _F64 = ctypes.c_double
 _SIG = {
     "kv_nvfp4_status_string": ([_I32], ctypes.c_char_p),
     "kv_nvfp4_version": ([], _I32),
+    "kv_nvfp4_last_cuda_error": ([], ctypes.c_char_p),
     "kv_nvfp4_layout_check": ([ctypes.POINTER(Layout)], _I32),
     "kv_nvfp4_page_bytes": ([ctypes.POINTER(Layout)], ctypes.c_size_t),
     "kv_nvfp4_pool_bytes": ([ctypes.POINTER(Layout), _I32, ctypes.POINTER(ctypes.c_size_t)],
@@ -97,6 +98,8 @@ def library_path() -> str:
 def _check(status: int, what: str):
     if status != KV_NVFP4_OK:
         msg = lib().kv_nvfp4_status_string(status).decode()
+        if status == KV_NVFP4_ECUDA:
+            msg += ": " + lib().kv_nvfp4_last_cuda_error().decode()
         raise KVNVFP4Error(f"{what}: {msg} ({status})")
 
 

@@ -34,6 +34,14 @@ constexpr int kPartHeadFloats = kRowsPerItem * 128 + 2 * kRowsPerItem;  // O[8][
 constexpr int kMaxAttnKvHeads = 4;  // the attention kernel stages every head of a page
 constexpr int kMaxGridForSizing = 1024;  // workspace sizing when no device is visible
 
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+kv_nvfp4_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return KV_NVFP4_OK;
+  g_last_cuda_error = e;
+  return KV_NVFP4_ECUDA;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int num_sms_current_device() {
@@ -203,6 +211,8 @@ const char* kv_nvfp4_status_string(kv_nvfp4_status s) {
 
 int32_t kv_nvfp4_version(void) { return 10000; }
 
+const char* kv_nvfp4_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
+
 kv_nvfp4_status kv_nvfp4_layout_check(const kv_nvfp4_layout* L) {
   if (L == nullptr) return KV_NVFP4_EINVAL;
   if (L->head_dim != 128 || L->page_size != 64) return KV_NVFP4_EINVAL;
@@ -248,10 +258,10 @@ kv_nvfp4_status kv_nvfp4_rope_table_init(float* d_table, int32_t max_pos, int32_
   std::vector<float> h((size_t)max_pos * rot_dim);
   rope_fill(h.data(), max_pos, rot_dim, theta, pos_scale);
   // pageable source: the runtime stages it before returning, so `h` may be freed afterwards
-  if (cudaMemcpyAsync(d_table, h.data(), h.size() * sizeof(float), cudaMemcpyHostToDevice,
-                      (cudaStream_t)stream) != cudaSuccess)
-    return KV_NVFP4_ECUDA;
-  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KV_NVFP4_ECUDA;
+  cudaError_t e = cudaMemcpyAsync(d_table, h.data(), h.size() * sizeof(float),
+                                  cudaMemcpyHostToDevice, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e);
   return KV_NVFP4_OK;
 }
 
@@ -276,7 +286,7 @@ kv_nvfp4_status kv_nvfp4_append(const kv_nvfp4_layout* L, const void* q, const v
       d_rope_table, rope_max_pos, L->rot_dim, d_block_table, num_seqs, max_pages, num_pages,
       pool, q_codes, q_scales, L->num_q_heads, L->num_kv_heads,
       d_status, (cudaStream_t)stream);
-  return e == cudaSuccess ? KV_NVFP4_OK : KV_NVFP4_ECUDA;
+  return cuda_status(e);
 }
 
 kv_nvfp4_status kv_nvfp4_plan_workspace_bytes(const kv_nvfp4_layout* L, const int32_t* h_seq_lens,
@@ -319,7 +329,7 @@ kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout* L, const int32_t* h_seq_len
                               kv_nvfp4_plan_info* info, void* stream) {
   if (info == nullptr || d_workspace == nullptr || !aligned16(d_workspace)) return KV_NVFP4_EINVAL;
   const int num_sms = num_sms_current_device();
-  if (num_sms <= 0) return KV_NVFP4_ECUDA;
+  if (num_sms <= 0) return cuda_status(cudaErrorNoDevice);
   PlanBuild pb;
   const kv_nvfp4_status s =
       plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_sms, &pb);
@@ -332,12 +342,11 @@ kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout* L, const int32_t* h_seq_len
   std::memcpy(host.data() + pi.off_segments / 4, pb.segments.data(), pb.segments.size() * 4);
   std::memcpy(host.data() + pi.off_cta / 4, pb.cta_seg.data(), pb.cta_seg.size() * 4);
   cudaStream_t st = (cudaStream_t)stream;
-  if (cudaMemcpyAsync(d_workspace, host.data(), host.size() * 4, cudaMemcpyHostToDevice, st) !=
-      cudaSuccess)
-    return KV_NVFP4_ECUDA;
+  cudaError_t e =
+      cudaMemcpyAsync(d_workspace, host.data(), host.size() * 4, cudaMemcpyHostToDevice, st);
   const size_t ctr_bytes = (size_t)(pi.off_partials - pi.off_counters);
-  if (cudaMemsetAsync((char*)d_workspace + pi.off_counters, 0, ctr_bytes, st) != cudaSuccess)
-    return KV_NVFP4_ECUDA;
+  if (e == cudaSuccess) e = cudaMemsetAsync((char*)d_workspace + pi.off_counters, 0, ctr_bytes, st);
+  if (e != cudaSuccess) return cuda_status(e);
   *info = pi;
   return KV_NVFP4_OK;
 }
@@ -369,7 +378,7 @@ kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout* L, const kv_nvfp4_pl
       (int32_t*)(ws + plan->off_counters), (float*)(ws + plan->off_partials), out, d_status,
       L->num_q_heads, L->num_kv_heads, plan->q_len, plan->causal, plan->grid, sm_scale,
       (cudaStream_t)stream);
-  return e == cudaSuccess ? KV_NVFP4_OK : KV_NVFP4_ECUDA;
+  return cuda_status(e);
 }
 
 }  // extern "C"

@@ -337,12 +337,11 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
     const int n = sg.hi - sg.lo;
     const int row0 = sg.rg * kRows;
     const int L0 = sg.len - p.q_len;
-    int lim[kRows];  // largest visible key position of each row; -1 for padding rows
-#pragma unroll
-    for (int i = 0; i < kRows; ++i) {
+    // largest visible key position of row i of the tile (-1 for a padding row)
+    auto lim = [&](int i) -> int {
       const int r = row0 + i;
-      lim[i] = (r < rows_total) ? (p.causal ? L0 + r / p.G : sg.len - 1) : -1;
-    }
+      return (r < rows_total) ? (p.causal ? L0 + r / p.G : sg.len - 1) : -1;
+    };
     // ---- Q tile (B operand of Q.K^T) and its scale factors for this group ----
     {
       const int pr = t128 >> 6, nrow = (t128 >> 2) & 15, ch = t128 & 3;
@@ -405,18 +404,20 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
 
       const bool pvalid = stage_pid[st] >= 0;
       const int kp = (sg.lo + j) * 64 + c.key;
-      float sv[2][kRows];
+      uint32_t vmask = 0;  // bit pr * 8 + i: key visible to row i of this pair's head
       bool need = false;
 #pragma unroll
       for (int pr = 0; pr < 2; ++pr) {
         const bool hv = pr < c.npairs && 2 * pr + c.half < p.Hkv && pvalid;
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
-          const bool v = hv && kp <= lim[i];
-          sv[pr][i] = v ? __uint_as_float(sr[pr][i]) : -INFINITY;
-          if (v && sv[pr][i] > mu[pr][i] + thr) need = true;
+          if (hv && kp <= lim(i)) {
+            vmask |= 1u << (pr * 8 + i);
+            if (__uint_as_float(sr[pr][i]) > mu[pr][i] + thr) need = true;
+          }
         }
       }
+#define SV(pr, i) (((vmask >> ((pr) * 8 + (i))) & 1u) ? __uint_as_float(sr[pr][i]) : -INFINITY)
       const int any_need = __any_sync(0xffffffffu, need) ? 1 : 0;
       if (lane == 0) flags[(k & 1) * 8 + c.sw] = any_need;
       named_barrier_sync(1, 128);
@@ -427,7 +428,7 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
         for (int pr = 0; pr < 2; ++pr)
 #pragma unroll
           for (int i = 0; i < kRows; ++i) {
-            const float m = ord2f(__reduce_max_sync(0xffffffffu, f2ord(sv[pr][i])));
+            const float m = ord2f(__reduce_max_sync(0xffffffffu, f2ord(SV(pr, i))));
             if (lane == 0) red[(c.qd * 2 + pr) * 8 + i] = m;
           }
         named_barrier_sync(1, 128);
@@ -458,17 +459,16 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
             wait_bar(c.bars + 8 * (kBarPvDone + ((k - 1) & 1)), ((k - 1) >> 1) & 1, c.timed_out);
             tc_fence_after();
           }
-          for (int h = 0; h < p.Hkv; ++h) {
-            uint32_t o[16];
-            tmem_ld16(tbase + c.lane_base + kColO + h * 16, o);
+          // 8 columns at a time (P hi part, then P lo part) keeps the register footprint small
+          for (int q = 0; q < 2 * p.Hkv; ++q) {
+            const int h = q >> 1;
+            uint32_t o[8];
+            tmem_ld8(tbase + c.lane_base + kColO + q * 8, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < kRows; ++i) {
-              const float a = alpha_s[h * 8 + i];
-              o[i] = __float_as_uint(__uint_as_float(o[i]) * a);
-              o[8 + i] = __float_as_uint(__uint_as_float(o[8 + i]) * a);
-            }
-            tmem_st16(tbase + c.lane_base + kColO + h * 16, o);
+            for (int i = 0; i < kRows; ++i)
+              o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha_s[h * 8 + i]);
+            tmem_st8(tbase + c.lane_base + kColO + q * 8, o);
           }
           tmem_wait_st();
         }
@@ -482,9 +482,11 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int i = 0; i < kRows; i += 2) {
-          const float p0 = (sv[pr][i] != -INFINITY) ? fast_exp2((sv[pr][i] - mu[pr][i]) * p.c2) : 0.f;
-          const float p1 =
-              (sv[pr][i + 1] != -INFINITY) ? fast_exp2((sv[pr][i + 1] - mu[pr][i + 1]) * p.c2) : 0.f;
+          const float p0 = ((vmask >> (pr * 8 + i)) & 1u)
+                               ? fast_exp2((__uint_as_float(sr[pr][i]) - mu[pr][i]) * p.c2) : 0.f;
+          const float p1 = ((vmask >> (pr * 8 + i + 1)) & 1u)
+                               ? fast_exp2((__uint_as_float(sr[pr][i + 1]) - mu[pr][i + 1]) * p.c2)
+                               : 0.f;
           lp[pr][i] += p0;
           lp[pr][i + 1] += p1;
           hi[i / 2] = pack_f16x2(p0, p1);
@@ -499,6 +501,7 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bars + 8 * (kBarPFull + b));
+#undef SV
     }
     // ---- segment epilogue: O^T from TMEM (one head dim per lane), row sums, output ----
     const uint32_t kl = k - 1;  // last page of this segment
@@ -638,7 +641,7 @@ __device__ void dequant_warps(const DecodeParams& p, uint8_t* smem, int warp, in
   if (timed_out && lane == 0) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
 
-__global__ void __maxnreg__(144) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bars = smem_u32(smem + kOffBars);

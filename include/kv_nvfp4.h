@@ -106,6 +106,9 @@ typedef struct kv_nvfp4_plan_info {
 /* Human-readable name of a status code (static string). */
 const char *kv_nvfp4_status_string(kv_nvfp4_status status);
 
+/* Description of the CUDA error behind this thread's most recent KV_NVFP4_ECUDA (static string). */
+const char *kv_nvfp4_last_cuda_error(void);
+
 /* Library version as major * 10000 + minor * 100 + patch. */
 int32_t kv_nvfp4_version(void);
 
