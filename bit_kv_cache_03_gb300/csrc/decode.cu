@@ -178,6 +178,7 @@ __device__ void producer(const DecodeParams& p, uint8_t* smem, int lane) {
             bulk_g2s(sbase + kOffStage + st * kStageBytes, p.pool + (int64_t)pid * blk_bytes,
                      blk_bytes, full);
           } else {
+            flag_status(p.status, KV_NVFP4_DEV_BAD_PAGE);  // the page is skipped (P = 0, V = 0)
             mbar_arrive(full);
           }
         }
