@@ -21,11 +21,15 @@
 //     are stored in the pool in the tensor core's 8-row x 16-byte tile order, so the page lands in
 //     shared memory ready for the MMA; scales go to TMEM in the replicated 32-lane x 4-column
 //     layout. Cross terms (head 2p keys x head 2p+1 rows) are computed and ignored.
-//   softmax: 4 warps read S from TMEM (one key per lane), fp32 online softmax with a lazily
-//     raised running max, P written to shared memory as f16 hi + lo.
+//   softmax: 4 warps read S from TMEM (one key per lane), take the exact page max per (head, row)
+//     (warp max reduction + one exchange between the two warps holding a head), keep an fp32
+//     running max and row sums, and write P = exp2((s - max) log2e scale) <= 1 to shared memory as
+//     f16 hi + lo.
 //   P.V: 8 warps dequantise V (E2M1 x E4M3 is exact in f16) into an MN-major shared tile; one
 //     thread issues tcgen05.mma kind::f16 with M = 128 dims, N = 16 (P hi in columns 0..7, P lo in
-//     8..15), K = 16 keys per instruction, accumulating O^T per head in TMEM.
+//     8..15), K = 16 keys per instruction, into a per-page TMEM accumulator (4 slots). Two pages
+//     later the softmax warps fold that page into the running O^T (O = O * alpha + O_page), so a
+//     rising max never stalls the tensor-core pipeline on a rescale.
 //
 // Warp roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner, warps 2..5
 // softmax / scale factors / epilogue (TMEM lane quadrants 2, 3, 0, 1), warps 6..13 V dequant.
@@ -71,27 +75,29 @@ constexpr int kBarPFull = kBarSFree + 2;            // [2]
 constexpr int kBarPvDone = kBarPFull + 2;           // [2]
 constexpr int kBarVhFull = kBarPvDone + 2;          // [kVhSlots]
 constexpr int kBarVhFree = kBarVhFull + kVhSlots;   // [kVhSlots]
+constexpr int kOSlots = 4;                          // per-page P.V accumulators in TMEM
 constexpr int kBarQReady = kBarVhFree + kVhSlots;
-constexpr int kBarOFree = kBarQReady + 1;
-constexpr int kNumBars = kBarOFree + 1;
+constexpr int kBarOFree = kBarQReady + 1;            // [kOSlots]: page accumulator folded
+constexpr int kNumBars = kBarOFree + kOSlots;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 // misc: stage page ids, tmem base, flags (need-max per page parity x warp, rescale per
 // half, ticket), reduction scratch, per-head alpha / mu / L
 constexpr int kOffStagePid = kOffMisc;
 constexpr int kOffTmemSlot = kOffStagePid + 4 * kStages;
 constexpr int kOffFlags = kOffTmemSlot + 16;
-constexpr int kOffRed = kOffFlags + 128;            // float [4 quadrants][2 pairs][8 rows]
-constexpr int kOffAlpha = kOffRed + 4 * 2 * kRows * 4;  // float [kMaxHkv][8]: rescale / mu / L
-constexpr int kOffMu = kOffAlpha + kMaxHkv * kRows * 4;
+constexpr int kOffRed = kOffFlags + 128;  // float [3][4 quadrants][2 pairs][8 rows]: page max x2, sums
+constexpr int kOffAlpha = kOffRed + 3 * 4 * 2 * kRows * 4;  // float [kOSlots][kMaxHkv][8]
+constexpr int kOffMu = kOffAlpha + kOSlots * kMaxHkv * kRows * 4;
 constexpr int kOffL = kOffMu + kMaxHkv * kRows * 4;
 constexpr int kSmemBytes = kOffL + kMaxHkv * kRows * 4 + 64;
 
 // TMEM columns
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0;      // [2 buffers][2 pairs][16]
-constexpr uint32_t kColO = 64;     // [4 heads][16]
-constexpr uint32_t kColSfa = 128;  // [2 buffers][2 pairs][2 k-halves][4]
-constexpr uint32_t kColSfb = 160;  // [2 pairs][2 k-halves][4]
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;        // [2 buffers][2 pairs][16]
+constexpr uint32_t kColSfa = 64;     // [2 buffers][2 pairs][2 k-halves][4]
+constexpr uint32_t kColSfb = 96;     // [2 pairs][2 k-halves][4]
+constexpr uint32_t kColOMain = 128;  // running O^T: [4 heads][16] (hi + lo halves)
+constexpr uint32_t kColOPage = 192;  // per-page O^T: [kOSlots][4 heads][16]
 
 // instruction descriptors (dense, no negation):
 //   QK: A, B = E2M1 (format 1) K-major, scale type UE4M3, N = 16, M = 128
@@ -99,8 +105,6 @@ constexpr uint32_t kColSfb = 160;  // [2 pairs][2 k-halves][4]
 constexpr uint32_t kIdescQK = (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t kIdescPV = (1u << 4) | (1u << 15) | (1u << 16) | ((16u >> 3) << 17) |
                               ((128u >> 4) << 24);
-
-constexpr float kLazyMaxLog2 = 8.0f;  // the running max is raised only past a 2^8 margin
 
 struct DecodeParams {
   const uint8_t* q_codes;
@@ -236,9 +240,9 @@ __device__ void mma_issuer(const DecodeParams& p, uint8_t* smem, uint32_t tbase)
     issue_qk(p, sbase, tbase, k, npairs, timed_out);
     for (int j = 0; j < n; ++j, ++k) {
       if (j + 1 < n) issue_qk(p, sbase, tbase, k + 1, npairs, timed_out);
-      const uint32_t b = k & 1;
+      const uint32_t b = k & 1, os = k % kOSlots;
       wait_bar(bars + 8 * (kBarPFull + b), (k >> 1) & 1, timed_out);
-      if (j == 0 && sgi > 0) wait_bar(bars + 8 * kBarOFree, (sgi - 1) & 1, timed_out);
+      if (k >= kOSlots) wait_bar(bars + 8 * (kBarOFree + os), ((k / kOSlots) - 1) & 1, timed_out);
       tc_fence_after();
       for (int h = 0; h < p.Hkv; ++h, ++hp) {
         const uint32_t slot = hp % kVhSlots;
@@ -249,7 +253,7 @@ __device__ void mma_issuer(const DecodeParams& p, uint8_t* smem, uint32_t tbase)
         for (int i = 0; i < 4; ++i) {  // 16 keys per instruction
           const uint64_t ad = smem_desc(vh + i * 4096, 2048, 128);
           const uint64_t bd = smem_desc(pb + i * 256, 128, 1024);
-          mma_f16_ss(tbase + kColO + h * 16, ad, bd, kIdescPV, (j > 0 || i > 0) ? 1u : 0u);
+          mma_f16_ss(tbase + kColOPage + os * 64 + h * 16, ad, bd, kIdescPV, i > 0 ? 1u : 0u);
         }
         mma_commit(bars + 8 * (kBarVhFree + slot));
       }
@@ -310,6 +314,32 @@ __device__ __forceinline__ void store_row(const DecodeParams& p, int seq, int hh
   p.out[(((int64_t)seq * p.q_len + tok) * p.Hq + qh) * 128 + dim] = v;
 }
 
+// Fold page j's P.V accumulator into the running O^T (one head dim per lane):
+// O = O * alpha_j + O_page(j), alpha_j = 2^((mu_{j-1} - mu_j) c2) per (head, row). P hi and P lo
+// were accumulated in columns 0..7 and 8..15; they are summed here.
+__device__ __forceinline__ void fold_page(SoftmaxCtx& c, uint32_t j, bool first) {
+  const DecodeParams& p = *c.p;
+  const volatile float* alpha = reinterpret_cast<const volatile float*>(c.smem + kOffAlpha) +
+                                (j % kOSlots) * kMaxHkv * kRows;
+  for (int h = 0; h < p.Hkv; ++h) {
+    uint32_t pg[16];
+    tmem_ld16(c.tbase + c.lane_base + kColOPage + (j % kOSlots) * 64 + h * 16, pg);
+    uint32_t om[8];
+    if (!first) tmem_ld8(c.tbase + c.lane_base + kColOMain + h * 16, om);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+      const float v = __uint_as_float(pg[i]) + __uint_as_float(pg[8 + i]);
+      om[i] = __float_as_uint(first ? v : fmaf(__uint_as_float(om[i]), alpha[h * kRows + i], v));
+    }
+    tmem_st8(c.tbase + c.lane_base + kColOMain + h * 16, om);
+  }
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (c.lane == 0) mbar_arrive(c.bars + 8 * (kBarOFree + j % kOSlots));
+}
+
 __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tbase, int warp,
                               int lane) {
   SoftmaxCtx c;
@@ -323,17 +353,16 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
   const int dim = c.qd * 32 + lane;   // this thread's head dim in O
   const int t128 = c.sw * 32 + lane;  // 0..127
   const int rows_total = p.G * p.q_len;
-  const float thr = kLazyMaxLog2 / p.c2;
   volatile int* flags = reinterpret_cast<volatile int*>(smem + kOffFlags);
   volatile float* red = reinterpret_cast<volatile float*>(smem + kOffRed);
   volatile float* alpha_s = reinterpret_cast<volatile float*>(smem + kOffAlpha);
   volatile float* mu_s = reinterpret_cast<volatile float*>(smem + kOffMu);
   volatile float* l_s = reinterpret_cast<volatile float*>(smem + kOffL);
   const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kOffStagePid);
-  uint32_t k = 0, sgi = 0;
+  uint32_t k = 0;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
 
-  for (int s = s_begin; s < s_end; ++s, ++sgi) {
+  for (int s = s_begin; s < s_end; ++s) {
     const SegInfo sg = load_seg(p, s);
     const int n = sg.hi - sg.lo;
     const int row0 = sg.rg * kRows;
@@ -384,6 +413,7 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
       for (int i = 0; i < kRows; ++i) { mu[pr][i] = -INFINITY; lp[pr][i] = 0.f; }
 
     write_sfa(c, k, sg.lo, sg.len);
+    const uint32_t k0 = k;
     for (int j = 0; j < n; ++j, ++k) {
       if (j + 1 < n) write_sfa(c, k + 1, sg.lo + j + 1, sg.len);
       const uint32_t b = k & 1, st = k % kStages;
@@ -403,78 +433,42 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bars + 8 * (kBarSFree + b));
 
+      // ---- exact page max per (head, row): warp reduction, then across the two warps of a head
       const bool pvalid = stage_pid[st] >= 0;
       const int kp = (sg.lo + j) * 64 + c.key;
       uint32_t vmask = 0;  // bit pr * 8 + i: key visible to row i of this pair's head
-      bool need = false;
 #pragma unroll
       for (int pr = 0; pr < 2; ++pr) {
         const bool hv = pr < c.npairs && 2 * pr + c.half < p.Hkv && pvalid;
 #pragma unroll
+        for (int i = 0; i < kRows; ++i)
+          if (hv && kp <= lim(i)) vmask |= 1u << (pr * 8 + i);
+      }
+      volatile float* rb = red + (k & 1) * 64;
+#pragma unroll
+      for (int pr = 0; pr < 2; ++pr)
+#pragma unroll
         for (int i = 0; i < kRows; ++i) {
-          if (hv && kp <= lim(i)) {
-            vmask |= 1u << (pr * 8 + i);
-            if (__uint_as_float(sr[pr][i]) > mu[pr][i] + thr) need = true;
-          }
+          const float x = ((vmask >> (pr * 8 + i)) & 1u) ? __uint_as_float(sr[pr][i]) : -INFINITY;
+          const float m = ord2f(__reduce_max_sync(0xffffffffu, f2ord(x)));
+          if (lane == 0) rb[(c.qd * 2 + pr) * 8 + i] = m;
         }
-      }
-#define SV(pr, i) (((vmask >> ((pr) * 8 + (i))) & 1u) ? __uint_as_float(sr[pr][i]) : -INFINITY)
-      const int any_need = __any_sync(0xffffffffu, need) ? 1 : 0;
-      if (lane == 0) flags[(k & 1) * 8 + c.sw] = any_need;
       named_barrier_sync(1, 128);
-      const int fb = (k & 1) * 8;
-      if (flags[fb] | flags[fb + 1] | flags[fb + 2] | flags[fb + 3]) {
-        // raise the running max where the page beats it by more than the margin
+      float* alpha_page = const_cast<float*>(alpha_s) + (k % kOSlots) * kMaxHkv * kRows;
 #pragma unroll
-        for (int pr = 0; pr < 2; ++pr)
+      for (int pr = 0; pr < 2; ++pr)
 #pragma unroll
-          for (int i = 0; i < kRows; ++i) {
-            const float m = ord2f(__reduce_max_sync(0xffffffffu, f2ord(SV(pr, i))));
-            if (lane == 0) red[(c.qd * 2 + pr) * 8 + i] = m;
-          }
-        named_barrier_sync(1, 128);
-        bool rescale = false;
-#pragma unroll
-        for (int pr = 0; pr < 2; ++pr)
-#pragma unroll
-          for (int i = 0; i < kRows; ++i) {
-            const float pm = fmaxf(red[((2 * c.half) * 2 + pr) * 8 + i],
-                                   red[((2 * c.half + 1) * 2 + pr) * 8 + i]);
-            float a = 1.f;
-            if (pm > mu[pr][i] + thr) {
-              if (mu[pr][i] != -INFINITY) {
-                a = fast_exp2((mu[pr][i] - pm) * p.c2);
-                rescale = true;
-              }
-              mu[pr][i] = pm;
-              lp[pr][i] *= a;
-            }
-            if (lane == 0 && (c.qd & 1) == 0 && 2 * pr + c.half < kMaxHkv)
-              alpha_s[(2 * pr + c.half) * 8 + i] = a;
-          }
-        if (lane == 0 && (c.qd & 1) == 0) flags[16 + c.half] = rescale ? 1 : 0;
-        named_barrier_sync(1, 128);
-        if (flags[16] | flags[17]) {
-          // O holds every earlier page of this segment: wait for those P.V products first
-          if (j > 0) {
-            wait_bar(c.bars + 8 * (kBarPvDone + ((k - 1) & 1)), ((k - 1) >> 1) & 1, c.timed_out);
-            tc_fence_after();
-          }
-          // 8 columns at a time (P hi part, then P lo part) keeps the register footprint small
-          for (int q = 0; q < 2 * p.Hkv; ++q) {
-            const int h = q >> 1;
-            uint32_t o[8];
-            tmem_ld8(tbase + c.lane_base + kColO + q * 8, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < kRows; ++i)
-              o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha_s[h * 8 + i]);
-            tmem_st8(tbase + c.lane_base + kColO + q * 8, o);
-          }
-          tmem_wait_st();
+        for (int i = 0; i < kRows; ++i) {
+          const float pm = fmaxf(rb[((2 * c.half) * 2 + pr) * 8 + i],
+                                 rb[((2 * c.half + 1) * 2 + pr) * 8 + i]);
+          const float mn = fmaxf(mu[pr][i], pm);
+          const float a = (mn == -INFINITY) ? 1.f : fast_exp2((mu[pr][i] - mn) * p.c2);
+          mu[pr][i] = mn;
+          lp[pr][i] *= a;
+          if (lane == 0 && (c.qd & 1) == 0 && 2 * pr + c.half < kMaxHkv)
+            alpha_page[(2 * pr + c.half) * kRows + i] = a;
         }
-      }
-      // ---- P = exp2((s - mu) c2) as f16 hi + lo, B operand of P.V (rows contiguous per key) ----
+      // ---- P = exp2((s - mu) c2) <= 1 as f16 hi + lo, B operand of P.V (rows contiguous per key)
       if (k >= 2) wait_bar(c.bars + 8 * (kBarPvDone + b), ((k >> 1) - 1) & 1, c.timed_out);
 #pragma unroll
       for (int pr = 0; pr < 2; ++pr) {
@@ -502,12 +496,18 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bars + 8 * (kBarPFull + b));
-#undef SV
+      // ---- fold the page two back (its P.V completed: the wait above covered it) ----
+      if (j >= 2) {
+        tc_fence_after();
+        fold_page(c, k - 2, k - 2 == k0);
+      }
     }
-    // ---- segment epilogue: O^T from TMEM (one head dim per lane), row sums, output ----
-    const uint32_t kl = k - 1;  // last page of this segment
-    wait_bar(c.bars + 8 * (kBarPvDone + (kl & 1)), (kl >> 1) & 1, c.timed_out);
-    tc_fence_after();
+    // ---- segment epilogue: fold the last pages, then O^T (one head dim per lane) / row sums ----
+    for (uint32_t jj = (n >= 2 ? k - 2 : k0); jj < k; ++jj) {
+      wait_bar(c.bars + 8 * (kBarPvDone + (jj & 1)), (jj >> 1) & 1, c.timed_out);
+      tc_fence_after();
+      fold_page(c, jj, jj == k0);
+    }
 #pragma unroll
     for (int pr = 0; pr < 2; ++pr)
 #pragma unroll
@@ -515,27 +515,27 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
         float v = lp[pr][i];
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
-        if (lane == 0) red[(c.qd * 2 + pr) * 8 + i] = v;
+        if (lane == 0) red[128 + (c.qd * 2 + pr) * 8 + i] = v;
         if (lane == 0 && (c.qd & 1) == 0) mu_s[(2 * pr + c.half) * 8 + i] = mu[pr][i];
       }
     named_barrier_sync(1, 128);
     if (t128 < kMaxHkv * kRows) {
       const int hh = t128 >> 3, i = t128 & 7, pr = hh >> 1, hf = hh & 1;
-      l_s[t128] = red[((2 * hf) * 2 + pr) * 8 + i] + red[((2 * hf + 1) * 2 + pr) * 8 + i];
+      l_s[t128] = red[128 + ((2 * hf) * 2 + pr) * 8 + i] + red[128 + ((2 * hf + 1) * 2 + pr) * 8 + i];
     }
     named_barrier_sync(1, 128);
     const bool split = sg.n_seg > 1;
     const int part_stride = p.Hkv * kPartHeadFloats;
     for (int h = 0; h < p.Hkv; ++h) {
-      uint32_t o[16];
-      tmem_ld16(tbase + c.lane_base + kColO + h * 16, o);
+      uint32_t o[8];
+      tmem_ld8(tbase + c.lane_base + kColOMain + h * 16, o);
       tmem_wait_ld();
       float* part = split ? p.partials + (int64_t)sg.part * part_stride + h * kPartHeadFloats
                           : nullptr;
 #pragma unroll
       for (int i = 0; i < kRows; ++i) {
         const int r = row0 + i;
-        const float ov = __uint_as_float(o[i]) + __uint_as_float(o[8 + i]);  // P hi + P lo
+        const float ov = __uint_as_float(o[i]);
         const float Ls = l_s[h * 8 + i];
         if (split) {
           if (r < rows_total) part[i * 128 + dim] = ov;
@@ -549,8 +549,6 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
       }
     }
     tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(c.bars + 8 * kBarOFree);
     if (split) {
       // the CTA that completes the group's last segment combines all of its partials
       __threadfence();
@@ -663,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
       mbar_init(bars + 8 * (kBarVhFree + v), 1);
     }
     mbar_init(bars + 8 * kBarQReady, 4);
-    mbar_init(bars + 8 * kBarOFree, 4);
+    for (int o = 0; o < kOSlots; ++o) mbar_init(bars + 8 * (kBarOFree + o), 4);
     fence_mbar_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(smem + kOffTmemSlot), kTmemCols);
