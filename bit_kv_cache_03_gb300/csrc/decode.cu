@@ -21,18 +21,19 @@
 //     are stored in the pool in the tensor core's 8-row x 16-byte tile order, so the page lands in
 //     shared memory ready for the MMA; scales go to TMEM in the replicated 32-lane x 4-column
 //     layout. Cross terms (head 2p keys x head 2p+1 rows) are computed and ignored.
-//   softmax: 4 warps read S from TMEM (one key per lane), take the exact page max per (head, row)
+//   softmax: 8 warps read S from TMEM (one key per lane), take the exact page max per (head, row)
 //     (warp max reduction + one exchange between the two warps holding a head), keep an fp32
 //     running max and row sums, and write P = exp2((s - max) log2e scale) <= 1 to shared memory as
 //     f16 hi + lo.
-//   P.V: 8 warps dequantise V (E2M1 x E4M3 is exact in f16) into an MN-major shared tile; one
+//   P.V: 4 warps dequantise V (E2M1 x E4M3 is exact in f16) into an MN-major shared tile; one
 //     thread issues tcgen05.mma kind::f16 with M = 128 dims, N = 16 (P hi in columns 0..7, P lo in
 //     8..15), K = 16 keys per instruction, into a per-page TMEM accumulator (4 slots). Two pages
 //     later the softmax warps fold that page into the running O^T (O = O * alpha + O_page), so a
 //     rising max never stalls the tensor-core pipeline on a rescale.
 //
-// Warp roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner, warps 2..5
-// softmax / scale factors / epilogue (TMEM lane quadrants 2, 3, 0, 1), warps 6..13 V dequant.
+// Warp roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner, warps 2..9
+// softmax / scale factors / epilogue (two groups of four, one per KV-head pair, covering the TMEM
+// lane quadrants 2, 3, 0, 1), warps 10..13 V dequant.
 // Every wait is an mbarrier wait bounded in time; on a timeout the kernel records
 // KV_NVFP4_DEV_TIMEOUT and carries on, so it cannot hang.
 
@@ -55,8 +56,8 @@ constexpr int kQBytes = 2 * 1024;                  // two head pairs x 16 rows x
 constexpr int kRows = 8;                           // query rows per head per group
 constexpr int kPartHeadFloats = kRows * 128 + 2 * kRows;  // O[8][128], m[8], l[8]
 
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpSoftmax0 = 2, kWarpDequant0 = 6;
-constexpr int kDequantWarps = 8;
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpSoftmax0 = 2, kWarpDequant0 = 10;
+constexpr int kDequantWarps = 4;
 constexpr int kThreads = (kWarpDequant0 + kDequantWarps) * 32;
 
 // shared memory map
@@ -264,20 +265,23 @@ __device__ void mma_issuer(const DecodeParams& p, uint8_t* smem, uint32_t tbase)
 }
 
 // --------------------------------------------------------------------------------------------
-// Softmax warps (4 warps, TMEM lane quadrant qd = warp % 4). For S a lane holds one key: TMEM
-// lane L = 32 qd + lane is key L % 64 of head 2 pr + L / 64 in pair pr. For O a lane holds one
-// head dim.
+// Softmax warps: 8 warps, two groups of four. Group pr works on KV-head pair pr; within a group
+// the four warps cover the four TMEM lane quadrants (qd = warp % 4). For S a lane holds one key:
+// TMEM lane L = 32 qd + lane is key L % 64 of head 2 pr + L / 64. For O a lane holds one head dim.
 // --------------------------------------------------------------------------------------------
+constexpr int kSoftmaxWarps = 8;
+
 struct SoftmaxCtx {
   const DecodeParams* p;
   uint8_t* smem;
   uint32_t sbase, bars, tbase, lane_base;
-  int lane, qd, sw, half, key, npairs;
+  int lane, qd, pr, half, key, head, gt;  // gt: thread index within the pair group (0..127)
+  bool active;                            // the pair has a real head for this thread's half
   bool timed_out;
 };
 
-// Scale factors of page k's K rows into TMEM (replicated 32-lane x 4-column layout: lane i,
-// column j holds the 4 scales of MMA row 32 j + i); releases the stage's K scales.
+// Scale factors of page k's K rows of this warp's pair into TMEM (replicated 32-lane x 4-column
+// layout: lane i, column j holds the 4 scales of MMA row 32 j + i); releases the stage's K scales.
 __device__ __forceinline__ void write_sfa(SoftmaxCtx& c, uint32_t k, int page, int len) {
   const DecodeParams& p = *c.p;
   const uint32_t st = k % kStages, b = k & 1;
@@ -286,19 +290,16 @@ __device__ __forceinline__ void write_sfa(SoftmaxCtx& c, uint32_t k, int page, i
   const bool pvalid = reinterpret_cast<volatile int32_t*>(c.smem + kOffStagePid)[st] >= 0;
   const uint32_t ks = c.sbase + kOffStage + st * kStageBytes + p.Hkv * 4096;
   const int kp0 = page * 64;
-  uint32_t sf[16];
+  uint32_t sf[8];
 #pragma unroll
-  for (int pr = 0; pr < 2; ++pr) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int hh = 2 * pr + (j >> 1), kk = 32 * (j & 1) + c.lane;
-      uint2 v = make_uint2(0u, 0u);
-      if (hh < p.Hkv && pvalid && kp0 + kk < len) v = lds64(ks + hh * 512 + kk * 8);
-      sf[pr * 8 + j] = v.x;      // k-half 0: scales of dims 0..63
-      sf[pr * 8 + 4 + j] = v.y;  // k-half 1: dims 64..127
-    }
+  for (int j = 0; j < 4; ++j) {
+    const int hh = 2 * c.pr + (j >> 1), kk = 32 * (j & 1) + c.lane;
+    uint2 v = make_uint2(0u, 0u);
+    if (hh < p.Hkv && pvalid && kp0 + kk < len) v = lds64(ks + hh * 512 + kk * 8);
+    sf[j] = v.x;      // k-half 0: scales of dims 0..63
+    sf[4 + j] = v.y;  // k-half 1: dims 64..127
   }
-  tmem_st16(c.tbase + c.lane_base + kColSfa + b * 16, sf);
+  tmem_st8(c.tbase + c.lane_base + kColSfa + b * 16 + c.pr * 8, sf);
   tmem_wait_st();
   tc_fence_before();
   __syncwarp();
@@ -308,23 +309,19 @@ __device__ __forceinline__ void write_sfa(SoftmaxCtx& c, uint32_t k, int page, i
   }
 }
 
-__device__ __forceinline__ void store_row(const DecodeParams& p, int seq, int hh, int r, int dim,
-                                          float v) {
-  const int tok = r / p.G, qh = hh * p.G + r % p.G;
-  p.out[(((int64_t)seq * p.q_len + tok) * p.Hq + qh) * 128 + dim] = v;
-}
-
-// Fold page j's P.V accumulator into the running O^T (one head dim per lane):
+// Fold page j's P.V accumulator into the running O^T of this warp's pair (one dim per lane):
 // O = O * alpha_j + O_page(j), alpha_j = 2^((mu_{j-1} - mu_j) c2) per (head, row). P hi and P lo
-// were accumulated in columns 0..7 and 8..15; they are summed here.
+// were accumulated in columns 0..7 and 8..15 and are summed here.
 __device__ __forceinline__ void fold_page(SoftmaxCtx& c, uint32_t j, bool first) {
   const DecodeParams& p = *c.p;
   const volatile float* alpha = reinterpret_cast<const volatile float*>(c.smem + kOffAlpha) +
                                 (j % kOSlots) * kMaxHkv * kRows;
-  for (int h = 0; h < p.Hkv; ++h) {
-    uint32_t pg[16];
+#pragma unroll 1
+  for (int e = 0; e < 2; ++e) {
+    const int h = 2 * c.pr + e;
+    if (h >= p.Hkv) continue;
+    uint32_t pg[16], om[8];
     tmem_ld16(c.tbase + c.lane_base + kColOPage + (j % kOSlots) * 64 + h * 16, pg);
-    uint32_t om[8];
     if (!first) tmem_ld8(c.tbase + c.lane_base + kColOMain + h * 16, om);
     tmem_wait_ld();
 #pragma unroll
@@ -340,21 +337,30 @@ __device__ __forceinline__ void fold_page(SoftmaxCtx& c, uint32_t j, bool first)
   if (c.lane == 0) mbar_arrive(c.bars + 8 * (kBarOFree + j % kOSlots));
 }
 
+__device__ __forceinline__ void store_row(const DecodeParams& p, int seq, int hh, int r, int dim,
+                                          float v) {
+  const int tok = r / p.G, qh = hh * p.G + r % p.G;
+  p.out[(((int64_t)seq * p.q_len + tok) * p.Hq + qh) * 128 + dim] = v;
+}
+
 __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tbase, int warp,
                               int lane) {
   SoftmaxCtx c;
   c.p = &p; c.smem = smem; c.sbase = smem_u32(smem); c.bars = c.sbase + kOffBars;
-  c.tbase = tbase; c.lane = lane; c.qd = warp & 3; c.sw = warp - kWarpSoftmax0;
+  c.tbase = tbase; c.lane = lane; c.qd = warp & 3;
+  c.pr = (warp - kWarpSoftmax0) >> 2;
   c.lane_base = (uint32_t)(c.qd * 32) << 16;
-  c.half = c.qd >> 1;                 // TMEM lanes 64..127 hold the odd head of a pair
+  c.half = c.qd >> 1;                 // TMEM lanes 64..127 hold the odd head of the pair
   c.key = (c.qd * 32 + lane) & 63;
-  c.npairs = (p.Hkv + 1) >> 1;
+  c.head = 2 * c.pr + c.half;
+  c.active = c.head < p.Hkv;
+  c.gt = ((warp - kWarpSoftmax0) & 3) * 32 + lane;
   c.timed_out = false;
   const int dim = c.qd * 32 + lane;   // this thread's head dim in O
-  const int t128 = c.sw * 32 + lane;  // 0..127
+  const uint32_t gbar = 1 + c.pr;     // named barrier of this pair group (128 threads)
   const int rows_total = p.G * p.q_len;
   volatile int* flags = reinterpret_cast<volatile int*>(smem + kOffFlags);
-  volatile float* red = reinterpret_cast<volatile float*>(smem + kOffRed);
+  volatile float* red = reinterpret_cast<volatile float*>(smem + kOffRed) + c.pr * 96;
   volatile float* alpha_s = reinterpret_cast<volatile float*>(smem + kOffAlpha);
   volatile float* mu_s = reinterpret_cast<volatile float*>(smem + kOffMu);
   volatile float* l_s = reinterpret_cast<volatile float*>(smem + kOffL);
@@ -372,45 +378,41 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
       const int r = row0 + i;
       return (r < rows_total) ? (p.causal ? L0 + r / p.G : sg.len - 1) : -1;
     };
-    // ---- Q tile (B operand of Q.K^T) and its scale factors for this group ----
-    {
-      const int pr = t128 >> 6, nrow = (t128 >> 2) & 15, ch = t128 & 3;
-      const int hh = 2 * pr + (nrow >> 3), r = row0 + (nrow & 7);
+    // ---- this pair's Q tile (B operand of Q.K^T) and its scale factors ----
+    if (c.gt < 64) {
+      const int nrow = c.gt >> 2, ch = c.gt & 3;
+      const int hh = 2 * c.pr + (nrow >> 3), r = row0 + (nrow & 7);
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (hh < p.Hkv && r < rows_total) {
         const int64_t qrow = ((int64_t)sg.seq * p.q_len + r / p.G) * p.Hq + hh * p.G + r % p.G;
         v = *reinterpret_cast<const uint4*>(p.q_codes + qrow * 64 + 16 * ch);
       }
-      sts128(c.sbase + kOffQ + pr * 1024 + (nrow >> 3) * 512 + ch * 128 + (nrow & 7) * 16, v.x,
+      sts128(c.sbase + kOffQ + c.pr * 1024 + (nrow >> 3) * 512 + ch * 128 + (nrow & 7) * 16, v.x,
              v.y, v.z, v.w);
-      uint32_t sf[16];
+    }
+    {
+      uint32_t sf[8];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) sf[q] = 0u;
+      for (int q = 0; q < 8; ++q) sf[q] = 0u;
       if (lane < 16) {
-#pragma unroll
-        for (int pr2 = 0; pr2 < 2; ++pr2) {
-          const int h2 = 2 * pr2 + (lane >> 3), r2 = row0 + (lane & 7);
-          if (h2 < p.Hkv && r2 < rows_total) {
-            const int64_t qrow =
-                ((int64_t)sg.seq * p.q_len + r2 / p.G) * p.Hq + h2 * p.G + r2 % p.G;
-            const uint2 qs = *reinterpret_cast<const uint2*>(p.q_scales + qrow * 8);
-            sf[pr2 * 8 + 0] = qs.x;
-            sf[pr2 * 8 + 4] = qs.y;
-          }
+        const int h2 = 2 * c.pr + (lane >> 3), r2 = row0 + (lane & 7);
+        if (h2 < p.Hkv && r2 < rows_total) {
+          const int64_t qrow = ((int64_t)sg.seq * p.q_len + r2 / p.G) * p.Hq + h2 * p.G + r2 % p.G;
+          const uint2 qs = *reinterpret_cast<const uint2*>(p.q_scales + qrow * 8);
+          sf[0] = qs.x;
+          sf[4] = qs.y;
         }
       }
-      tmem_st16(tbase + c.lane_base + kColSfb, sf);
+      tmem_st8(tbase + c.lane_base + kColSfb + c.pr * 8, sf);
       tmem_wait_st();
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bars + 8 * kBarQReady);
     }
-    float mu[2][kRows], lp[2][kRows];  // running max (raw score units), partial row sums
+    float mu[kRows], lp[kRows];  // running max (raw score units) and partial row sums, own head
 #pragma unroll
-    for (int pr = 0; pr < 2; ++pr)
-#pragma unroll
-      for (int i = 0; i < kRows; ++i) { mu[pr][i] = -INFINITY; lp[pr][i] = 0.f; }
+    for (int i = 0; i < kRows; ++i) { mu[i] = -INFINITY; lp[i] = 0.f; }
 
     write_sfa(c, k, sg.lo, sg.len);
     const uint32_t k0 = k;
@@ -419,75 +421,53 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
       const uint32_t b = k & 1, st = k % kStages;
       wait_bar(c.bars + 8 * (kBarQkDone + b), (k >> 1) & 1, c.timed_out);
       tc_fence_after();
-      uint32_t sr[2][8];
-#pragma unroll
-      for (int pr = 0; pr < 2; ++pr) {
-        if (pr < c.npairs) tmem_ld8(tbase + c.lane_base + kColS + b * 32 + pr * 16 + c.half * 8, sr[pr]);
-        else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) sr[pr][i] = 0u;
-        }
-      }
+      uint32_t sr[8];
+      tmem_ld8(tbase + c.lane_base + kColS + b * 32 + c.pr * 16 + c.half * 8, sr);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bars + 8 * (kBarSFree + b));
 
-      // ---- exact page max per (head, row): warp reduction, then across the two warps of a head
-      const bool pvalid = stage_pid[st] >= 0;
+      // ---- exact page max per row: warp reduction, then across the two warps of the head ----
+      const bool hv = c.active && stage_pid[st] >= 0;
       const int kp = (sg.lo + j) * 64 + c.key;
-      uint32_t vmask = 0;  // bit pr * 8 + i: key visible to row i of this pair's head
+      uint32_t vmask = 0;  // bit i: key visible to row i
 #pragma unroll
-      for (int pr = 0; pr < 2; ++pr) {
-        const bool hv = pr < c.npairs && 2 * pr + c.half < p.Hkv && pvalid;
+      for (int i = 0; i < kRows; ++i)
+        if (hv && kp <= lim(i)) vmask |= 1u << i;
+      volatile float* rb = red + (k & 1) * 32;
 #pragma unroll
-        for (int i = 0; i < kRows; ++i)
-          if (hv && kp <= lim(i)) vmask |= 1u << (pr * 8 + i);
+      for (int i = 0; i < kRows; ++i) {
+        const float x = ((vmask >> i) & 1u) ? __uint_as_float(sr[i]) : -INFINITY;
+        const float m = ord2f(__reduce_max_sync(0xffffffffu, f2ord(x)));
+        if (lane == 0) rb[c.qd * 8 + i] = m;
       }
-      volatile float* rb = red + (k & 1) * 64;
-#pragma unroll
-      for (int pr = 0; pr < 2; ++pr)
-#pragma unroll
-        for (int i = 0; i < kRows; ++i) {
-          const float x = ((vmask >> (pr * 8 + i)) & 1u) ? __uint_as_float(sr[pr][i]) : -INFINITY;
-          const float m = ord2f(__reduce_max_sync(0xffffffffu, f2ord(x)));
-          if (lane == 0) rb[(c.qd * 2 + pr) * 8 + i] = m;
-        }
-      named_barrier_sync(1, 128);
+      named_barrier_sync(gbar, 128);
       float* alpha_page = const_cast<float*>(alpha_s) + (k % kOSlots) * kMaxHkv * kRows;
 #pragma unroll
-      for (int pr = 0; pr < 2; ++pr)
-#pragma unroll
-        for (int i = 0; i < kRows; ++i) {
-          const float pm = fmaxf(rb[((2 * c.half) * 2 + pr) * 8 + i],
-                                 rb[((2 * c.half + 1) * 2 + pr) * 8 + i]);
-          const float mn = fmaxf(mu[pr][i], pm);
-          const float a = (mn == -INFINITY) ? 1.f : fast_exp2((mu[pr][i] - mn) * p.c2);
-          mu[pr][i] = mn;
-          lp[pr][i] *= a;
-          if (lane == 0 && (c.qd & 1) == 0 && 2 * pr + c.half < kMaxHkv)
-            alpha_page[(2 * pr + c.half) * kRows + i] = a;
-        }
+      for (int i = 0; i < kRows; ++i) {
+        const float pm = fmaxf(rb[(2 * c.half) * 8 + i], rb[(2 * c.half + 1) * 8 + i]);
+        const float mn = fmaxf(mu[i], pm);
+        const float a = (mn == -INFINITY) ? 1.f : fast_exp2((mu[i] - mn) * p.c2);
+        mu[i] = mn;
+        lp[i] *= a;
+        if (lane == 0 && (c.qd & 1) == 0 && c.head < kMaxHkv) alpha_page[c.head * kRows + i] = a;
+      }
       // ---- P = exp2((s - mu) c2) <= 1 as f16 hi + lo, B operand of P.V (rows contiguous per key)
       if (k >= 2) wait_bar(c.bars + 8 * (kBarPvDone + b), ((k >> 1) - 1) & 1, c.timed_out);
-#pragma unroll
-      for (int pr = 0; pr < 2; ++pr) {
-        const int hh = 2 * pr + c.half;
-        if (pr >= c.npairs || hh >= p.Hkv) continue;
+      if (c.active) {
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int i = 0; i < kRows; i += 2) {
-          const float p0 = ((vmask >> (pr * 8 + i)) & 1u)
-                               ? fast_exp2((__uint_as_float(sr[pr][i]) - mu[pr][i]) * p.c2) : 0.f;
-          const float p1 = ((vmask >> (pr * 8 + i + 1)) & 1u)
-                               ? fast_exp2((__uint_as_float(sr[pr][i + 1]) - mu[pr][i + 1]) * p.c2)
-                               : 0.f;
-          lp[pr][i] += p0;
-          lp[pr][i + 1] += p1;
+          const float p0 = ((vmask >> i) & 1u) ? fast_exp2((__uint_as_float(sr[i]) - mu[i]) * p.c2) : 0.f;
+          const float p1 =
+              ((vmask >> (i + 1)) & 1u) ? fast_exp2((__uint_as_float(sr[i + 1]) - mu[i + 1]) * p.c2) : 0.f;
+          lp[i] += p0;
+          lp[i + 1] += p1;
           hi[i / 2] = pack_f16x2(p0, p1);
           lo[i / 2] = pack_f16x2(p0 - f16_lo_to_f32(hi[i / 2]), p1 - f16_hi_to_f32(hi[i / 2]));
         }
-        const uint32_t a = c.sbase + kOffP + b * kPBytes + hh * 2048 + (c.key >> 3) * 128 +
+        const uint32_t a = c.sbase + kOffP + b * kPBytes + c.head * 2048 + (c.key >> 3) * 128 +
                            (c.key & 7) * 16;
         sts128(a, hi[0], hi[1], hi[2], hi[3]);
         sts128(a + 1024, lo[0], lo[1], lo[2], lo[3]);
@@ -502,31 +482,32 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
         fold_page(c, k - 2, k - 2 == k0);
       }
     }
-    // ---- segment epilogue: fold the last pages, then O^T (one head dim per lane) / row sums ----
+    // ---- segment epilogue: fold the last pages, row sums, then O^T (one head dim per lane) ----
     for (uint32_t jj = (n >= 2 ? k - 2 : k0); jj < k; ++jj) {
       wait_bar(c.bars + 8 * (kBarPvDone + (jj & 1)), (jj >> 1) & 1, c.timed_out);
       tc_fence_after();
       fold_page(c, jj, jj == k0);
     }
 #pragma unroll
-    for (int pr = 0; pr < 2; ++pr)
+    for (int i = 0; i < kRows; ++i) {
+      float v = lp[i];
 #pragma unroll
-      for (int i = 0; i < kRows; ++i) {
-        float v = lp[pr][i];
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
-        if (lane == 0) red[128 + (c.qd * 2 + pr) * 8 + i] = v;
-        if (lane == 0 && (c.qd & 1) == 0) mu_s[(2 * pr + c.half) * 8 + i] = mu[pr][i];
-      }
-    named_barrier_sync(1, 128);
-    if (t128 < kMaxHkv * kRows) {
-      const int hh = t128 >> 3, i = t128 & 7, pr = hh >> 1, hf = hh & 1;
-      l_s[t128] = red[128 + ((2 * hf) * 2 + pr) * 8 + i] + red[128 + ((2 * hf + 1) * 2 + pr) * 8 + i];
+      for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+      if (lane == 0) red[64 + c.qd * 8 + i] = v;
+      if (lane == 0 && (c.qd & 1) == 0 && c.head < kMaxHkv) mu_s[c.head * 8 + i] = mu[i];
     }
-    named_barrier_sync(1, 128);
+    named_barrier_sync(gbar, 128);
+    if (c.gt < 16) {
+      const int hf = c.gt >> 3, i = c.gt & 7, hh = 2 * c.pr + hf;
+      l_s[hh * 8 + i] = red[64 + (2 * hf) * 8 + i] + red[64 + (2 * hf + 1) * 8 + i];
+    }
+    named_barrier_sync(gbar, 128);
     const bool split = sg.n_seg > 1;
     const int part_stride = p.Hkv * kPartHeadFloats;
-    for (int h = 0; h < p.Hkv; ++h) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int h = 2 * c.pr + e;
+      if (h >= p.Hkv) continue;
       uint32_t o[8];
       tmem_ld8(tbase + c.lane_base + kColOMain + h * 16, o);
       tmem_wait_ld();
@@ -548,23 +529,24 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
         }
       }
     }
-    tc_fence_before();
     if (split) {
       // the CTA that completes the group's last segment combines all of its partials
       __threadfence();
-      named_barrier_sync(1, 128);
-      if (t128 == 0) {
+      named_barrier_sync(3, 32 * kSoftmaxWarps);
+      if (c.pr == 0 && c.gt == 0) {
         __threadfence();
         const int ticket = atomicAdd(p.counters + sg.group, 1);
         const int last = ticket == sg.n_seg - 1;
         if (last) p.counters[sg.group] = 0;  // ready for the next call on this workspace
         flags[24] = last;
       }
-      named_barrier_sync(1, 128);
+      named_barrier_sync(3, 32 * kSoftmaxWarps);
       if (flags[24]) {
         __threadfence();
         const float* pb = p.partials + (int64_t)sg.first_part * part_stride;
-        for (int h = 0; h < p.Hkv; ++h) {
+        for (int e = 0; e < 2; ++e) {
+          const int h = 2 * c.pr + e;
+          if (h >= p.Hkv) continue;
           for (int i = 0; i < kRows; ++i) {
             const int r = row0 + i;
             if (r >= rows_total) continue;
@@ -585,23 +567,24 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
         }
       }
     }
-    named_barrier_sync(1, 128);  // scratch reused by the next segment
+    named_barrier_sync(3, 32 * kSoftmaxWarps);  // scratch reused by the next segment
   }
   if (c.timed_out && lane == 0) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
 
 // --------------------------------------------------------------------------------------------
 // Dequant warps: V codes x E4M3 scales -> f16 V^T tile (MN-major: 8 dims x 8 keys core tiles).
-// Warp wd takes keys 8 wd .. 8 wd + 7 of every head, each lane one key and one 32-dim quarter; the
-// quarter is rotated by key so that shared-memory reads and writes are free of bank conflicts.
+// Warp wd takes keys 16 wd .. 16 wd + 15 of every head (two groups of 8), each lane one key and one
+// 32-dim quarter per group; the quarter is rotated by key so that shared-memory reads and writes
+// are free of bank conflicts.
 // --------------------------------------------------------------------------------------------
 __device__ void dequant_warps(const DecodeParams& p, uint8_t* smem, int warp, int lane) {
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kOffBars;
   const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kOffStagePid);
   const int wd = warp - kWarpDequant0;
-  const int key = 8 * wd + (lane & 7);
   const int quarter = ((lane >> 3) + ((lane & 7) >> 1)) & 3;
+  constexpr int kRounds = 64 / (8 * kDequantWarps);  // 8-key groups per warp and head
   uint32_t k = 0, hp = 0;
   bool timed_out = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
@@ -610,24 +593,29 @@ __device__ void dequant_warps(const DecodeParams& p, uint8_t* smem, int warp, in
     for (int page = sg.lo; page < sg.hi; ++page, ++k) {
       const uint32_t st = k % kStages;
       wait_bar(bars + 8 * (kBarStageFull + st), (k / kStages) & 1, timed_out);
-      const bool kvalid = stage_pid[st] >= 0 && page * 64 + key < sg.len;
+      const bool pvalid = stage_pid[st] >= 0;
       const uint32_t stage = sbase + kOffStage + st * kStageBytes;
       for (int h = 0; h < p.Hkv; ++h, ++hp) {
         const uint32_t slot = hp % kVhSlots;
         if (hp >= kVhSlots) wait_bar(bars + 8 * (kBarVhFree + slot), ((hp / kVhSlots) - 1) & 1, timed_out);
-        const uint4 cw = lds128(stage + p.Hkv * 4608 + h * 4096 + key * 64 + 16 * quarter);
-        const uint32_t sc = kvalid ? lds16(stage + p.Hkv * 8704 + h * 512 + key * 8 + 2 * quarter) : 0u;
-        const uint32_t sh = cvt_e4m3x2_f16(sc);
-        const uint32_t s0 = dup_lo(sh), s1 = dup_hi(sh);
-        const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-        const uint32_t vh = sbase + kOffVh + slot * kVhBytes + (key >> 3) * 2048 + (key & 7) * 16;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t r0, r1, r2, r3;
-          cvt_e2m1x8_f16(words[q], r0, r1, r2, r3);
-          const uint32_t sq = q < 2 ? s0 : s1;  // dims 32 quarter + 8 q .. : block 2 quarter + q / 2
-          sts128(vh + (4 * quarter + q) * 128, hmul2(r0, sq), hmul2(r1, sq), hmul2(r2, sq),
-                 hmul2(r3, sq));
+        for (int rd = 0; rd < kRounds; ++rd) {
+          const int key = 8 * (kRounds * wd + rd) + (lane & 7);
+          const bool kvalid = pvalid && page * 64 + key < sg.len;
+          const uint4 cw = lds128(stage + p.Hkv * 4608 + h * 4096 + key * 64 + 16 * quarter);
+          const uint32_t sc = kvalid ? lds16(stage + p.Hkv * 8704 + h * 512 + key * 8 + 2 * quarter) : 0u;
+          const uint32_t sh = cvt_e4m3x2_f16(sc);
+          const uint32_t s0 = dup_lo(sh), s1 = dup_hi(sh);
+          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+          const uint32_t vh = sbase + kOffVh + slot * kVhBytes + (key >> 3) * 2048 + (key & 7) * 16;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t r0, r1, r2, r3;
+            cvt_e2m1x8_f16(words[q], r0, r1, r2, r3);
+            const uint32_t sq = q < 2 ? s0 : s1;  // dims 32 quarter + 8 q .. : block 2 quarter + q / 2
+            sts128(vh + (4 * quarter + q) * 128, hmul2(r0, sq), hmul2(r1, sq), hmul2(r2, sq),
+                   hmul2(r3, sq));
+          }
         }
         fence_async_smem();
         __syncwarp();
@@ -647,21 +635,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bars + 8 * (kBarStageFull + s), 1);
-      mbar_init(bars + 8 * (kBarStageEmpty + s), 4 + kDequantWarps + 1);
+      mbar_init(bars + 8 * (kBarStageEmpty + s), 8 + kDequantWarps + 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bars + 8 * (kBarSfaFull + b), 4);
+      mbar_init(bars + 8 * (kBarSfaFull + b), 8);
       mbar_init(bars + 8 * (kBarQkDone + b), 1);
-      mbar_init(bars + 8 * (kBarSFree + b), 4);
-      mbar_init(bars + 8 * (kBarPFull + b), 4);
+      mbar_init(bars + 8 * (kBarSFree + b), 8);
+      mbar_init(bars + 8 * (kBarPFull + b), 8);
       mbar_init(bars + 8 * (kBarPvDone + b), 1);
     }
     for (int v = 0; v < kVhSlots; ++v) {
       mbar_init(bars + 8 * (kBarVhFull + v), kDequantWarps);
       mbar_init(bars + 8 * (kBarVhFree + v), 1);
     }
-    mbar_init(bars + 8 * kBarQReady, 4);
-    for (int o = 0; o < kOSlots; ++o) mbar_init(bars + 8 * (kBarOFree + o), 4);
+    mbar_init(bars + 8 * kBarQReady, 8);
+    for (int o = 0; o < kOSlots; ++o) mbar_init(bars + 8 * (kBarOFree + o), 8);
     fence_mbar_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(smem + kOffTmemSlot), kTmemCols);
