@@ -31,9 +31,9 @@
 //     later the softmax warps fold that page into the running O^T (O = O * alpha + O_page), so a
 //     rising max never stalls the tensor-core pipeline on a rescale.
 //
-// Warp roles (448 threads): warp 0 TMA producer, warp 1 MMA issuer and TMEM owner, warps 2..9
-// softmax / scale factors / epilogue (two groups of four, one per KV-head pair, covering the TMEM
-// lane quadrants 2, 3, 0, 1), warps 10..13 V dequant.
+// Warp roles (480 threads): warp 0 TMA producer, warp 1 Q.K^T issuer and TMEM owner, warp 2 P.V
+// issuer, warps 3..10 softmax / scale factors / epilogue (two groups of four, one per KV-head pair,
+// covering the four TMEM lane quadrants), warps 11..14 V dequant.
 // Every wait is an mbarrier wait bounded in time; on a timeout the kernel records
 // KV_NVFP4_DEV_TIMEOUT and carries on, so it cannot hang.
 
@@ -47,16 +47,16 @@ namespace kvnvfp4 {
 namespace {
 
 constexpr int kMaxHkv = 4;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kStageBytes = kMaxHkv * 9216;        // one page block of up to 4 heads
-constexpr int kVhSlots = 3;                        // dequantised V tiles (one head-page each)
+constexpr int kVhSlots = 5;                        // dequantised V tiles (one head-page each)
 constexpr int kVhBytes = 64 * 128 * 2;             // 64 keys x 128 dims x f16
 constexpr int kPBytes = kMaxHkv * 2048;            // per page: per head P hi (1 KB) + lo (1 KB)
 constexpr int kQBytes = 2 * 1024;                  // two head pairs x 16 rows x 64 B
 constexpr int kRows = 8;                           // query rows per head per group
 constexpr int kPartHeadFloats = kRows * 128 + 2 * kRows;  // O[8][128], m[8], l[8]
 
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpSoftmax0 = 2, kWarpDequant0 = 10;
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpPv = 2, kWarpSoftmax0 = 3, kWarpDequant0 = 11;
 constexpr int kDequantWarps = 4;
 constexpr int kThreads = (kWarpDequant0 + kDequantWarps) * 32;
 
@@ -202,7 +202,7 @@ __device__ void producer(const DecodeParams& p, uint8_t* smem, int lane) {
 }
 
 // --------------------------------------------------------------------------------------------
-// MMA issuer (one thread).
+// MMA issue (one thread each for Q.K^T and for P.V).
 // --------------------------------------------------------------------------------------------
 __device__ __forceinline__ void issue_qk(const DecodeParams& p, uint32_t sbase, uint32_t tbase,
                                          uint32_t k, int npairs, bool& timed_out) {
@@ -227,20 +227,33 @@ __device__ __forceinline__ void issue_qk(const DecodeParams& p, uint32_t sbase, 
   mma_commit(bars + 8 * (kBarStageEmpty + st));  // K codes consumed once the QK MMAs complete
 }
 
-__device__ void mma_issuer(const DecodeParams& p, uint8_t* smem, uint32_t tbase) {
+// Q.K^T issuer: runs ahead of the softmax as far as the stage ring, the scale-factor buffers and
+// the two S buffers allow.
+__device__ void qk_issuer(const DecodeParams& p, uint8_t* smem, uint32_t tbase) {
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kOffBars;
   const int npairs = (p.Hkv + 1) >> 1;
-  uint32_t k = 0, hp = 0, sgi = 0;
+  uint32_t k = 0, sgi = 0;
   bool timed_out = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
   for (int s = s_begin; s < s_end; ++s, ++sgi) {
     const SegInfo sg = load_seg(p, s);
-    const int n = sg.hi - sg.lo;
     wait_bar(bars + 8 * kBarQReady, sgi & 1, timed_out);  // Q tile and its scales for this group
-    issue_qk(p, sbase, tbase, k, npairs, timed_out);
-    for (int j = 0; j < n; ++j, ++k) {
-      if (j + 1 < n) issue_qk(p, sbase, tbase, k + 1, npairs, timed_out);
+    for (int j = 0; j < sg.hi - sg.lo; ++j, ++k) issue_qk(p, sbase, tbase, k, npairs, timed_out);
+  }
+  if (timed_out) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
+}
+
+// P.V issuer: per page and head, four MMAs (16 keys each) into the page's TMEM accumulator.
+__device__ void pv_issuer(const DecodeParams& p, uint8_t* smem, uint32_t tbase) {
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + kOffBars;
+  uint32_t k = 0, hp = 0;
+  bool timed_out = false;
+  const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
+  for (int s = s_begin; s < s_end; ++s) {
+    const SegInfo sg = load_seg(p, s);
+    for (int j = 0; j < sg.hi - sg.lo; ++j, ++k) {
       const uint32_t b = k & 1, os = k % kOSlots;
       wait_bar(bars + 8 * (kBarPFull + b), (k >> 1) & 1, timed_out);
       if (k >= kOSlots) wait_bar(bars + 8 * (kBarOFree + os), ((k / kOSlots) - 1) & 1, timed_out);
@@ -661,7 +674,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
   if (warp == kWarpProducer) {
     producer(p, smem, lane);
   } else if (warp == kWarpMma) {
-    if (lane == 0) mma_issuer(p, smem, tbase);
+    if (lane == 0) qk_issuer(p, smem, tbase);
+  } else if (warp == kWarpPv) {
+    if (lane == 0) pv_issuer(p, smem, tbase);
   } else if (warp < kWarpDequant0) {
     softmax_warps(p, smem, tbase, warp, lane);
   } else {
