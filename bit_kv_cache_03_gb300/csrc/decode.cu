@@ -1,5 +1,4 @@
-// Paged GQA decode / speculative-verify attention over the NVFP4 cache, on the tcgen05 tensor
-// cores, with split-K.
+// Paged GQA decode / speculative-verify attention over the NVFP4 cache, with split-K.
 //
 // Source: prismix.dev/news/833001997676, section "NVFP4 KV cache (from scratch)": the Q.K^T
 // product in NVFP4 with E4M3 block scales (both Q and K quantised), V dequantised for the P.V
@@ -14,27 +13,29 @@
 //
 // One page = 64 keys of every KV head, a 9216 x H byte block moved by ONE bulk async copy.
 //
-// Per page, with KV heads taken in pairs (2p, 2p+1):
-//   Q.K^T: tcgen05.mma kind::mxf4nvf4, block_scale.scale_vec::4X (E2M1 x E2M1, UE4M3 scale per
-//     16 elements), M = 128 = 64 keys of head 2p over 64 keys of head 2p+1, N = 16 = 8 query rows
-//     of head 2p then 8 of head 2p+1, K = 64 per instruction (two per 128-dim row). The K codes
-//     are stored in the pool in the tensor core's 8-row x 16-byte tile order, so the page lands in
-//     shared memory ready for the MMA; scales go to TMEM in the replicated 32-lane x 4-column
-//     layout. Cross terms (head 2p keys x head 2p+1 rows) are computed and ignored.
-//   softmax: 8 warps read S from TMEM (one key per lane), take the exact page max per (head, row)
-//     (warp max reduction + one exchange between the two warps holding a head), keep an fp32
-//     running max and row sums, and write P = exp2((s - max) log2e scale) <= 1 to shared memory as
-//     f16 hi + lo.
-//   P.V: 4 warps dequantise V (E2M1 x E4M3 is exact in f16) into an MN-major shared tile; one
-//     thread issues tcgen05.mma kind::f16 with M = 128 dims, N = 16 (P hi in columns 0..7, P lo in
-//     8..15), K = 16 keys per instruction, into a per-page TMEM accumulator (4 slots). Two pages
-//     later the softmax warps fold that page into the running O^T (O = O * alpha + O_page), so a
-//     rising max never stalls the tensor-core pipeline on a rescale.
+// Q.K^T on the tcgen05 tensor cores: kind::mxf4nvf4, block_scale.scale_vec::4X (E2M1 x E2M1 with
+// a UE4M3 scale per 16 elements), M = 128 = 64 keys of head 2p over 64 keys of head 2p+1, N = 16 =
+// 8 query rows of head 2p then 8 of head 2p+1, K = 64 per instruction (two per 128-dim row). The
+// K codes are stored in the pool in the tensor core's 8-row x 16-byte tile order, so the page
+// lands in shared memory ready for the MMA; the K scales go to TMEM in the replicated 32-lane x
+// 4-column layout. Cross terms (head 2p keys x head 2p+1 rows) are computed and ignored. Four
+// MMAs per page for four KV heads.
 //
-// Warp roles (480 threads): warp 0 TMA producer, warp 1 Q.K^T issuer and TMEM owner, warp 2 P.V
-// issuer, warps 3..10 softmax / scale factors / epilogue (two groups of four, one per KV-head pair,
-// covering the four TMEM lane quadrants), warps 11..14 V dequant.
-// Every wait is an mbarrier wait bounded in time; on a timeout the kernel records
+// Softmax and P.V in eight attention warps. Warp (pair p, TMEM lane quadrant q) owns head
+// 2p + q / 2 and keys 32 (q % 2) .. 32 (q % 2) + 31 of every page, with its own running max, row
+// sums and O accumulator; the two warps of a head merge once, at the end of a segment. Per page a
+// warp reads its S slice from TMEM (one key per lane), takes the page max per row with warp
+// reductions, rescales its accumulator when a max grows, and writes P = exp2((s - m) log2e scale)
+// <= 1 as an f16 hi + lo pair to a private shared tile. The P.V product runs on the warp-level
+// tensor path (mma.sync m16n8k16, f32 accumulate) with the query rows as M (rows 0..7 P hi, rows
+// 8..15 P lo, so the pair costs nothing extra), 16 keys as K and 8 head dims as N. P comes in
+// with transposing ldmatrix; V goes from its E2M1 codes straight into B fragments: the nibbles of
+// two keys are interleaved into one byte per dim, converted with cvt.e2m1x2 and multiplied by the
+// two keys' E4M3 scales (E2M1 x E4M3 is exact in f16). Within a 16-key step the keys are taken in
+// a fixed permutation, the same for P and V, that keeps the shared-memory reads conflict-free.
+//
+// Warp roles (320 threads): warp 0 bulk-copy producer, warp 1 Q.K^T issuer and TMEM owner, warps
+// 2..9 attention. Every wait is an mbarrier wait bounded in time; on a timeout the kernel records
 // KV_NVFP4_DEV_TIMEOUT and carries on, so it cannot hang.
 
 #include <cstdint>
@@ -47,65 +48,56 @@ namespace kvnvfp4 {
 namespace {
 
 constexpr int kMaxHkv = 4;
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr int kStageBytes = kMaxHkv * 9216;        // one page block of up to 4 heads
-constexpr int kVhSlots = 5;                        // dequantised V tiles (one head-page each)
-constexpr int kVhBytes = 64 * 128 * 2;             // 64 keys x 128 dims x f16
-constexpr int kPBytes = kMaxHkv * 2048;            // per page: per head P hi (1 KB) + lo (1 KB)
 constexpr int kQBytes = 2 * 1024;                  // two head pairs x 16 rows x 64 B
 constexpr int kRows = 8;                           // query rows per head per group
 constexpr int kPartHeadFloats = kRows * 128 + 2 * kRows;  // O[8][128], m[8], l[8]
 
-constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpPv = 2, kWarpSoftmax0 = 3, kWarpDequant0 = 11;
-constexpr int kDequantWarps = 4;
-constexpr int kThreads = (kWarpDequant0 + kDequantWarps) * 32;
+constexpr int kWarpProducer = 0, kWarpMma = 1, kWarpAttn0 = 2;
+constexpr int kAttnWarps = 8;
+constexpr int kThreads = (kWarpAttn0 + kAttnWarps) * 32;
+// Register bound: three warps share one SM sub-partition's 16K registers, so <= 168 per thread.
+constexpr int kBoundThreads = 384;
+
+constexpr int kPsBytes = 1024;                     // per attention warp: 32 keys x (hi 16 B, lo 16 B)
+constexpr int kMergeHeadBytes = 8 * 32 * 16 + 2 * kRows * 4;  // O: 8 float4 per lane; m[8], l[8]
 
 // shared memory map
 constexpr int kOffStage = 0;
-constexpr int kOffVh = kOffStage + kStages * kStageBytes;
-constexpr int kOffP = kOffVh + kVhSlots * kVhBytes;
-constexpr int kOffQ = kOffP + 2 * kPBytes;
-constexpr int kOffBars = kOffQ + kQBytes;
+constexpr int kOffPs = kOffStage + kStages * kStageBytes;
+constexpr int kOffQ = kOffPs + kAttnWarps * kPsBytes;
+constexpr int kOffMerge = kOffQ + kQBytes;
+constexpr int kOffBars = kOffMerge + kMaxHkv * kMergeHeadBytes;
 // barrier indices
-constexpr int kBarStageFull = 0;                    // [kStages]
-constexpr int kBarStageEmpty = kBarStageFull + kStages;
+constexpr int kBarStageFull = 0;                       // [kStages]
+constexpr int kBarStageEmpty = kBarStageFull + kStages;  // [kStages]
 constexpr int kBarSfaFull = kBarStageEmpty + kStages;  // [2]
-constexpr int kBarQkDone = kBarSfaFull + 2;         // [2]
-constexpr int kBarSFree = kBarQkDone + 2;           // [2]
-constexpr int kBarPFull = kBarSFree + 2;            // [2]
-constexpr int kBarPvDone = kBarPFull + 2;           // [2]
-constexpr int kBarVhFull = kBarPvDone + 2;          // [kVhSlots]
-constexpr int kBarVhFree = kBarVhFull + kVhSlots;   // [kVhSlots]
-constexpr int kOSlots = 4;                          // per-page P.V accumulators in TMEM
-constexpr int kBarQReady = kBarVhFree + kVhSlots;
-constexpr int kBarOFree = kBarQReady + 1;            // [kOSlots]: page accumulator folded
-constexpr int kNumBars = kBarOFree + kOSlots;
+constexpr int kBarQkDone = kBarSfaFull + 2;            // [2]
+constexpr int kBarSFree = kBarQkDone + 2;              // [2]
+constexpr int kBarQReady = kBarSFree + 2;
+constexpr int kNumBars = kBarQReady + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-// misc: stage page ids, tmem base, flags (need-max per page parity x warp, rescale per
-// half, ticket), reduction scratch, per-head alpha / mu / L
+// misc: stage page ids, tmem base, flags (ticket result)
 constexpr int kOffStagePid = kOffMisc;
-constexpr int kOffTmemSlot = kOffStagePid + 4 * kStages;
+constexpr int kOffTmemSlot = kOffStagePid + 4 * 8;
 constexpr int kOffFlags = kOffTmemSlot + 16;
-constexpr int kOffRed = kOffFlags + 128;  // float [3][4 quadrants][2 pairs][8 rows]: page max x2, sums
-constexpr int kOffAlpha = kOffRed + 3 * 4 * 2 * kRows * 4;  // float [kOSlots][kMaxHkv][8]
-constexpr int kOffMu = kOffAlpha + kOSlots * kMaxHkv * kRows * 4;
-constexpr int kOffL = kOffMu + kMaxHkv * kRows * 4;
-constexpr int kSmemBytes = kOffL + kMaxHkv * kRows * 4 + 64;
+constexpr int kSmemBytes = kOffFlags + 128;
+static_assert(kStages <= 8, "stage page-id slots");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // TMEM columns
-constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemCols = 128;
 constexpr uint32_t kColS = 0;        // [2 buffers][2 pairs][16]
 constexpr uint32_t kColSfa = 64;     // [2 buffers][2 pairs][2 k-halves][4]
 constexpr uint32_t kColSfb = 96;     // [2 pairs][2 k-halves][4]
-constexpr uint32_t kColOMain = 128;  // running O^T: [4 heads][16] (hi + lo halves)
-constexpr uint32_t kColOPage = 192;  // per-page O^T: [kOSlots][4 heads][16]
 
-// instruction descriptors (dense, no negation):
-//   QK: A, B = E2M1 (format 1) K-major, scale type UE4M3, N = 16, M = 128
-//   PV: D = f32, A, B = f16, both MN-major, N = 16, M = 128
+// instruction descriptor (dense, no negation): A, B = E2M1 (format 1) K-major, scale type UE4M3,
+// N = 16, M = 128
 constexpr uint32_t kIdescQK = (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
-constexpr uint32_t kIdescPV = (1u << 4) | (1u << 15) | (1u << 16) | ((16u >> 3) << 17) |
-                              ((128u >> 4) << 24);
+
+// named barriers: 3 = all attention warps, 4 + h = the two warps of KV head h
+constexpr uint32_t kNbAttn = 3, kNbHead0 = 4;
 
 struct DecodeParams {
   const uint8_t* q_codes;
@@ -244,58 +236,25 @@ __device__ void qk_issuer(const DecodeParams& p, uint8_t* smem, uint32_t tbase) 
   if (timed_out) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
 
-// P.V issuer: per page and head, four MMAs (16 keys each) into the page's TMEM accumulator.
-__device__ void pv_issuer(const DecodeParams& p, uint8_t* smem, uint32_t tbase) {
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t bars = sbase + kOffBars;
-  uint32_t k = 0, hp = 0;
-  bool timed_out = false;
-  const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
-  for (int s = s_begin; s < s_end; ++s) {
-    const SegInfo sg = load_seg(p, s);
-    for (int j = 0; j < sg.hi - sg.lo; ++j, ++k) {
-      const uint32_t b = k & 1, os = k % kOSlots;
-      wait_bar(bars + 8 * (kBarPFull + b), (k >> 1) & 1, timed_out);
-      if (k >= kOSlots) wait_bar(bars + 8 * (kBarOFree + os), ((k / kOSlots) - 1) & 1, timed_out);
-      tc_fence_after();
-      for (int h = 0; h < p.Hkv; ++h, ++hp) {
-        const uint32_t slot = hp % kVhSlots;
-        wait_bar(bars + 8 * (kBarVhFull + slot), (hp / kVhSlots) & 1, timed_out);
-        tc_fence_after();
-        const uint32_t vh = sbase + kOffVh + slot * kVhBytes;
-        const uint32_t pb = sbase + kOffP + b * kPBytes + h * 2048;
-        for (int i = 0; i < 4; ++i) {  // 16 keys per instruction
-          const uint64_t ad = smem_desc(vh + i * 4096, 2048, 128);
-          const uint64_t bd = smem_desc(pb + i * 256, 128, 1024);
-          mma_f16_ss(tbase + kColOPage + os * 64 + h * 16, ad, bd, kIdescPV, i > 0 ? 1u : 0u);
-        }
-        mma_commit(bars + 8 * (kBarVhFree + slot));
-      }
-      mma_commit(bars + 8 * (kBarPvDone + b));
-    }
-  }
-  if (timed_out) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
-}
 
 // --------------------------------------------------------------------------------------------
-// Softmax warps: 8 warps, two groups of four. Group pr works on KV-head pair pr; within a group
-// the four warps cover the four TMEM lane quadrants (qd = warp % 4). For S a lane holds one key:
-// TMEM lane L = 32 qd + lane is key L % 64 of head 2 pr + L / 64. For O a lane holds one head dim.
+// Attention warps: 8 warps, two groups of four. Group pr works on KV-head pair pr; within a group
+// the four warps cover the four TMEM lane quadrants (qd = warp % 4). TMEM lane L = 32 qd + lane
+// holds key L % 64 of head 2 pr + L / 64, so warp (pr, qd) owns head 2 pr + qd / 2 and keys
+// 32 (qd % 2) .. 32 (qd % 2) + 31 of every page.
 // --------------------------------------------------------------------------------------------
-constexpr int kSoftmaxWarps = 8;
-
-struct SoftmaxCtx {
+struct AttnCtx {
   const DecodeParams* p;
   uint8_t* smem;
   uint32_t sbase, bars, tbase, lane_base;
-  int lane, qd, pr, half, key, head, gt;  // gt: thread index within the pair group (0..127)
-  bool active;                            // the pair has a real head for this thread's half
+  int lane, qd, pr, head, key0, gt;  // gt: thread index within the pair group (0..127)
+  bool active;                       // the warp's head exists (Hkv may be odd)
   bool timed_out;
 };
 
 // Scale factors of page k's K rows of this warp's pair into TMEM (replicated 32-lane x 4-column
-// layout: lane i, column j holds the 4 scales of MMA row 32 j + i); releases the stage's K scales.
-__device__ __forceinline__ void write_sfa(SoftmaxCtx& c, uint32_t k, int page, int len) {
+// layout: lane i, column j holds the 4 scales of MMA row 32 j + i).
+__device__ __forceinline__ void write_sfa(AttnCtx& c, uint32_t k, int page, int len) {
   const DecodeParams& p = *c.p;
   const uint32_t st = k % kStages, b = k & 1;
   wait_bar(c.bars + 8 * (kBarStageFull + st), (k / kStages) & 1, c.timed_out);
@@ -316,67 +275,56 @@ __device__ __forceinline__ void write_sfa(SoftmaxCtx& c, uint32_t k, int page, i
   tmem_wait_st();
   tc_fence_before();
   __syncwarp();
-  if (c.lane == 0) {
-    mbar_arrive(c.bars + 8 * (kBarSfaFull + b));
-    mbar_arrive(c.bars + 8 * (kBarStageEmpty + st));
-  }
+  if (c.lane == 0) mbar_arrive(c.bars + 8 * (kBarSfaFull + b));
 }
 
-// Fold page j's P.V accumulator into the running O^T of this warp's pair (one dim per lane):
-// O = O * alpha_j + O_page(j), alpha_j = 2^((mu_{j-1} - mu_j) c2) per (head, row). P hi and P lo
-// were accumulated in columns 0..7 and 8..15 and are summed here.
-__device__ __forceinline__ void fold_page(SoftmaxCtx& c, uint32_t j, bool first) {
-  const DecodeParams& p = *c.p;
-  const volatile float* alpha = reinterpret_cast<const volatile float*>(c.smem + kOffAlpha) +
-                                (j % kOSlots) * kMaxHkv * kRows;
-#pragma unroll 1
-  for (int e = 0; e < 2; ++e) {
-    const int h = 2 * c.pr + e;
-    if (h >= p.Hkv) continue;
-    uint32_t pg[16], om[8];
-    tmem_ld16(c.tbase + c.lane_base + kColOPage + (j % kOSlots) * 64 + h * 16, pg);
-    if (!first) tmem_ld8(c.tbase + c.lane_base + kColOMain + h * 16, om);
-    tmem_wait_ld();
+// Byte address of the hi (half 0) or lo (half 1) P row of warp-local key `key` in a warp's P tile:
+// four keys per 128-byte line, the 32-byte slots and 16-byte halves permuted by line so that both
+// the row stores and the transposing ldmatrix reads are free of bank conflicts.
+__device__ __forceinline__ uint32_t p_addr(uint32_t base, int key, int half) {
+  const int q = key >> 2;
+  return base + q * 128 + 32 * ((key & 3) ^ (q & 3)) + 16 * (half ^ (q & 1));
+}
+
+__device__ __forceinline__ float pick8(const float (&v)[kRows], int i) {
+  float r = v[0];
 #pragma unroll
-    for (int i = 0; i < kRows; ++i) {
-      const float v = __uint_as_float(pg[i]) + __uint_as_float(pg[8 + i]);
-      om[i] = __float_as_uint(first ? v : fmaf(__uint_as_float(om[i]), alpha[h * kRows + i], v));
-    }
-    tmem_st8(c.tbase + c.lane_base + kColOMain + h * 16, om);
-  }
-  tmem_wait_st();
-  tc_fence_before();
-  __syncwarp();
-  if (c.lane == 0) mbar_arrive(c.bars + 8 * (kBarOFree + j % kOSlots));
+  for (int j = 1; j < kRows; ++j) r = (i == j) ? v[j] : r;
+  return r;
 }
 
-__device__ __forceinline__ void store_row(const DecodeParams& p, int seq, int hh, int r, int dim,
-                                          float v) {
-  const int tok = r / p.G, qh = hh * p.G + r % p.G;
-  p.out[(((int64_t)seq * p.q_len + tok) * p.Hq + qh) * 128 + dim] = v;
-}
-
-__device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tbase, int warp,
-                              int lane) {
-  SoftmaxCtx c;
+__device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t tbase, int warp,
+                                int lane) {
+  AttnCtx c;
   c.p = &p; c.smem = smem; c.sbase = smem_u32(smem); c.bars = c.sbase + kOffBars;
   c.tbase = tbase; c.lane = lane; c.qd = warp & 3;
-  c.pr = (warp - kWarpSoftmax0) >> 2;
+  const int aw = warp - kWarpAttn0;
+  c.pr = aw >> 2;
   c.lane_base = (uint32_t)(c.qd * 32) << 16;
-  c.half = c.qd >> 1;                 // TMEM lanes 64..127 hold the odd head of the pair
-  c.key = (c.qd * 32 + lane) & 63;
-  c.head = 2 * c.pr + c.half;
+  const int half = c.qd >> 1;         // TMEM lanes 64..127 hold the odd head of the pair
+  c.head = 2 * c.pr + half;
+  c.key0 = 32 * (c.qd & 1);
   c.active = c.head < p.Hkv;
-  c.gt = ((warp - kWarpSoftmax0) & 3) * 32 + lane;
+  c.gt = (aw & 3) * 32 + lane;
   c.timed_out = false;
-  const int dim = c.qd * 32 + lane;   // this thread's head dim in O
-  const uint32_t gbar = 1 + c.pr;     // named barrier of this pair group (128 threads)
+  const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates
+  const uint32_t ps = c.sbase + kOffPs + aw * kPsBytes;
+  // ldmatrix rows of this lane: matrix mi = lane / 8 is (P hi | P lo) x (k 0..7 | k 8..15); the
+  // fragment k index maps to a warp-local key by the permutation below (also used for V)
+  uint32_t lm_addr0, lm_addr1;
+  {
+    const int mi = lane >> 3, kidx = (mi >> 1) * 8 + (lane & 7), tt = (kidx & 7) >> 1;
+    const int local = 4 * tt + ((kidx >> 3) << 1) + ((kidx & 1) ^ (tt & 1));
+    lm_addr0 = p_addr(ps, local, mi & 1);
+    lm_addr1 = p_addr(ps, 16 + local, mi & 1);
+  }
+  // B fragment keys of this lane within a 16-key step: k = 2t, 2t+1, 2t+8, 2t+9 -> keys
+  // 4t + {0,1,2,3} with the pair order flipped for odd t (so lanes t and t+1 read different banks)
+  const int vk0 = 4 * t + (t & 1), vk1 = 4 * t + 1 - (t & 1);
+  const int vk2 = vk0 + 2, vk3 = vk1 + 2;
   const int rows_total = p.G * p.q_len;
+  const float c2 = p.c2;
   volatile int* flags = reinterpret_cast<volatile int*>(smem + kOffFlags);
-  volatile float* red = reinterpret_cast<volatile float*>(smem + kOffRed) + c.pr * 96;
-  volatile float* alpha_s = reinterpret_cast<volatile float*>(smem + kOffAlpha);
-  volatile float* mu_s = reinterpret_cast<volatile float*>(smem + kOffMu);
-  volatile float* l_s = reinterpret_cast<volatile float*>(smem + kOffL);
   const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kOffStagePid);
   uint32_t k = 0;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
@@ -386,11 +334,16 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
     const int n = sg.hi - sg.lo;
     const int row0 = sg.rg * kRows;
     const int L0 = sg.len - p.q_len;
-    // largest visible key position of row i of the tile (-1 for a padding row)
-    auto lim = [&](int i) -> int {
-      const int r = row0 + i;
-      return (r < rows_total) ? (p.causal ? L0 + r / p.G : sg.len - 1) : -1;
-    };
+    // largest visible key position of row lane % 8 of the tile (-1 for a padding row); rows are
+    // ordered by token, so row 0 has the smallest limit
+    int mylim;
+    {
+      const int r = row0 + (lane & 7);
+      mylim = (r < rows_total) ? (p.causal ? L0 + r / p.G : sg.len - 1) : -1;
+    }
+    const int lim_min = __shfl_sync(0xffffffffu, mylim, 0);
+    const uint32_t rows_mask = __ballot_sync(0xffffffffu, mylim >= 0) & 0xFFu;
+
     // ---- this pair's Q tile (B operand of Q.K^T) and its scale factors ----
     if (c.gt < 64) {
       const int nrow = c.gt >> 2, ch = c.gt & 3;
@@ -423,246 +376,271 @@ __device__ void softmax_warps(const DecodeParams& p, uint8_t* smem, uint32_t tba
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bars + 8 * kBarQReady);
     }
-    float mu[kRows], lp[kRows];  // running max (raw score units) and partial row sums, own head
+
+    // running max (raw score units) and per-lane partial row sums, replicated per row
+    float m[kRows], lp[kRows];
 #pragma unroll
-    for (int i = 0; i < kRows; ++i) { mu[i] = -INFINITY; lp[i] = 0.f; }
+    for (int i = 0; i < kRows; ++i) { m[i] = -INFINITY; lp[i] = 0.f; }
+    // O accumulator: acc[dd] is the m16n8 tile of dims 16 n + dd (n = fragment column); rows
+    // 0..7 take P hi, rows 8..15 P lo
+    float acc[16][4];
+#pragma unroll
+    for (int dd = 0; dd < 16; ++dd)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[dd][q] = 0.f;
 
     write_sfa(c, k, sg.lo, sg.len);
-    const uint32_t k0 = k;
     for (int j = 0; j < n; ++j, ++k) {
       if (j + 1 < n) write_sfa(c, k + 1, sg.lo + j + 1, sg.len);
       const uint32_t b = k & 1, st = k % kStages;
       wait_bar(c.bars + 8 * (kBarQkDone + b), (k >> 1) & 1, c.timed_out);
       tc_fence_after();
       uint32_t sr[8];
-      tmem_ld8(tbase + c.lane_base + kColS + b * 32 + c.pr * 16 + c.half * 8, sr);
+      tmem_ld8(tbase + c.lane_base + kColS + b * 32 + c.pr * 16 + half * 8, sr);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bars + 8 * (kBarSFree + b));
 
-      // ---- exact page max per row: warp reduction, then across the two warps of the head ----
-      const bool hv = c.active && stage_pid[st] >= 0;
-      const int kp = (sg.lo + j) * 64 + c.key;
-      uint32_t vmask = 0;  // bit i: key visible to row i
-#pragma unroll
-      for (int i = 0; i < kRows; ++i)
-        if (hv && kp <= lim(i)) vmask |= 1u << i;
-      volatile float* rb = red + (k & 1) * 32;
-#pragma unroll
-      for (int i = 0; i < kRows; ++i) {
-        const float x = ((vmask >> i) & 1u) ? __uint_as_float(sr[i]) : -INFINITY;
-        const float m = ord2f(__reduce_max_sync(0xffffffffu, f2ord(x)));
-        if (lane == 0) rb[c.qd * 8 + i] = m;
-      }
-      named_barrier_sync(gbar, 128);
-      float* alpha_page = const_cast<float*>(alpha_s) + (k % kOSlots) * kMaxHkv * kRows;
-#pragma unroll
-      for (int i = 0; i < kRows; ++i) {
-        const float pm = fmaxf(rb[(2 * c.half) * 8 + i], rb[(2 * c.half + 1) * 8 + i]);
-        const float mn = fmaxf(mu[i], pm);
-        const float a = (mn == -INFINITY) ? 1.f : fast_exp2((mu[i] - mn) * p.c2);
-        mu[i] = mn;
-        lp[i] *= a;
-        if (lane == 0 && (c.qd & 1) == 0 && c.head < kMaxHkv) alpha_page[c.head * kRows + i] = a;
-      }
-      // ---- P = exp2((s - mu) c2) <= 1 as f16 hi + lo, B operand of P.V (rows contiguous per key)
-      if (k >= 2) wait_bar(c.bars + 8 * (kBarPvDone + b), ((k >> 1) - 1) & 1, c.timed_out);
+      const int page = sg.lo + j;
+      const bool pvalid = stage_pid[st] >= 0;
       if (c.active) {
+        // ---- visibility of this lane's key to each row ----
+        uint32_t vmask = 0;
+        if (pvalid) {
+          if (page * 64 + 63 <= lim_min) {
+            vmask = rows_mask;
+          } else {
+            const int kp = page * 64 + c.key0 + lane;
+#pragma unroll
+            for (int i = 0; i < kRows; ++i)
+              if (kp <= __shfl_sync(0xffffffffu, mylim, i)) vmask |= 1u << i;
+          }
+        }
+        // ---- page max per row over the warp's 32 keys; rescale when it grows ----
+        float alpha_g = 1.f;
+        bool grow = false;
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+          const float x = ((vmask >> i) & 1u) ? __uint_as_float(sr[i]) : -INFINITY;
+          const float pm = ord2f(__reduce_max_sync(0xffffffffu, f2ord(x)));
+          if (pm > m[i]) {  // warp-uniform
+            const float a = fast_exp2((m[i] - pm) * c2);  // 0 when m was -inf
+            lp[i] *= a;
+            m[i] = pm;
+            grow = true;
+            if (g == i) alpha_g = a;
+          }
+        }
+        if (grow) {
+#pragma unroll
+          for (int dd = 0; dd < 16; ++dd)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[dd][q] *= alpha_g;
+        }
+        // ---- P = exp2((s - m) c2) <= 1 as f16 hi + lo into the warp's P tile ----
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int i = 0; i < kRows; i += 2) {
-          const float p0 = ((vmask >> i) & 1u) ? fast_exp2((__uint_as_float(sr[i]) - mu[i]) * p.c2) : 0.f;
+          const float p0 = ((vmask >> i) & 1u) ? fast_exp2((__uint_as_float(sr[i]) - m[i]) * c2) : 0.f;
           const float p1 =
-              ((vmask >> (i + 1)) & 1u) ? fast_exp2((__uint_as_float(sr[i + 1]) - mu[i + 1]) * p.c2) : 0.f;
+              ((vmask >> (i + 1)) & 1u) ? fast_exp2((__uint_as_float(sr[i + 1]) - m[i + 1]) * c2) : 0.f;
           lp[i] += p0;
           lp[i + 1] += p1;
           hi[i / 2] = pack_f16x2(p0, p1);
           lo[i / 2] = pack_f16x2(p0 - f16_lo_to_f32(hi[i / 2]), p1 - f16_hi_to_f32(hi[i / 2]));
         }
-        const uint32_t a = c.sbase + kOffP + b * kPBytes + c.head * 2048 + (c.key >> 3) * 128 +
-                           (c.key & 7) * 16;
-        sts128(a, hi[0], hi[1], hi[2], hi[3]);
-        sts128(a + 1024, lo[0], lo[1], lo[2], lo[3]);
+        sts128(p_addr(ps, lane, 0), hi[0], hi[1], hi[2], hi[3]);
+        sts128(p_addr(ps, lane, 1), lo[0], lo[1], lo[2], lo[3]);
+        __syncwarp();
+
+        // ---- O += P V over the warp's 32 keys: two 16-key steps ----
+        const uint32_t stage = c.sbase + kOffStage + st * kStageBytes;
+        const uint32_t vc = stage + p.Hkv * 4608 + c.head * 4096 + 8 * g;  // codes of dims 16 g ..
+        const uint32_t vs = stage + p.Hkv * 8704 + c.head * 512 + g;       // scale of block g
+        const int kv_lim = pvalid ? sg.len - page * 64 : 0;                 // keys < kv_lim are real
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(ks ? lm_addr1 : lm_addr0, a0, a1, a2, a3);
+          const int kb = c.key0 + 16 * ks;
+          const uint2 w0 = lds64(vc + (kb + vk0) * 64), w1 = lds64(vc + (kb + vk1) * 64);
+          const uint2 w2 = lds64(vc + (kb + vk2) * 64), w3 = lds64(vc + (kb + vk3) * 64);
+          // a key past the end or on a skipped page gets scale 0 (its codes are stale bytes)
+          const uint32_t s0 = kb + vk0 < kv_lim ? lds8(vs + (kb + vk0) * 8) : 0u;
+          const uint32_t s1 = kb + vk1 < kv_lim ? lds8(vs + (kb + vk1) * 8) : 0u;
+          const uint32_t s2 = kb + vk2 < kv_lim ? lds8(vs + (kb + vk2) * 8) : 0u;
+          const uint32_t s3 = kb + vk3 < kv_lim ? lds8(vs + (kb + vk3) * 8) : 0u;
+          const uint32_t sc01 = cvt_e4m3x2_f16(s0 | (s1 << 8));
+          const uint32_t sc23 = cvt_e4m3x2_f16(s2 | (s3 << 8));
+#pragma unroll
+          for (int w = 0; w < 2; ++w) {  // dims 16 g + 8 w .. 16 g + 8 w + 7
+            const uint32_t x0 = w ? w0.y : w0.x, x1 = w ? w1.y : w1.x;
+            const uint32_t x2 = w ? w2.y : w2.x, x3 = w ? w3.y : w3.x;
+            // one byte per dim holding the nibbles of two keys: (key A low, key B high)
+            const uint32_t ze01 = (x0 & 0x0F0F0F0Fu) | ((x1 << 4) & 0xF0F0F0F0u);
+            const uint32_t zo01 = ((x0 >> 4) & 0x0F0F0F0Fu) | (x1 & 0xF0F0F0F0u);
+            const uint32_t ze23 = (x2 & 0x0F0F0F0Fu) | ((x3 << 4) & 0xF0F0F0F0u);
+            const uint32_t zo23 = ((x2 >> 4) & 0x0F0F0F0Fu) | (x3 & 0xF0F0F0F0u);
+            uint32_t e0[4], o0[4], e2[4], o2[4];
+            cvt_e2m1x8_f16(ze01, e0[0], e0[1], e0[2], e0[3]);
+            cvt_e2m1x8_f16(zo01, o0[0], o0[1], o0[2], o0[3]);
+            cvt_e2m1x8_f16(ze23, e2[0], e2[1], e2[2], e2[3]);
+            cvt_e2m1x8_f16(zo23, o2[0], o2[1], o2[2], o2[3]);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              mma16816(acc[8 * w + 2 * jj], a0, a1, a2, a3, hmul2(e0[jj], sc01), hmul2(e2[jj], sc23));
+              mma16816(acc[8 * w + 2 * jj + 1], a0, a1, a2, a3, hmul2(o0[jj], sc01),
+                       hmul2(o2[jj], sc23));
+            }
+          }
+        }
       }
-      fence_async_smem();
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bars + 8 * (kBarPFull + b));
-      // ---- fold the page two back (its P.V completed: the wait above covered it) ----
-      if (j >= 2) {
-        tc_fence_after();
-        fold_page(c, k - 2, k - 2 == k0);
-      }
+      if (lane == 0) mbar_arrive(c.bars + 8 * (kBarStageEmpty + st));
     }
-    // ---- segment epilogue: fold the last pages, row sums, then O^T (one head dim per lane) ----
-    for (uint32_t jj = (n >= 2 ? k - 2 : k0); jj < k; ++jj) {
-      wait_bar(c.bars + 8 * (kBarPvDone + (jj & 1)), (jj >> 1) & 1, c.timed_out);
-      tc_fence_after();
-      fold_page(c, jj, jj == k0);
-    }
+
+    // ---- segment end: row sums, then the two warps of each head merge ----
 #pragma unroll
     for (int i = 0; i < kRows; ++i) {
       float v = lp[i];
 #pragma unroll
-      for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
-      if (lane == 0) red[64 + c.qd * 8 + i] = v;
-      if (lane == 0 && (c.qd & 1) == 0 && c.head < kMaxHkv) mu_s[c.head * 8 + i] = mu[i];
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      lp[i] = v;
     }
-    named_barrier_sync(gbar, 128);
-    if (c.gt < 16) {
-      const int hf = c.gt >> 3, i = c.gt & 7, hh = 2 * c.pr + hf;
-      l_s[hh * 8 + i] = red[64 + (2 * hf) * 8 + i] + red[64 + (2 * hf + 1) * 8 + i];
-    }
-    named_barrier_sync(gbar, 128);
     const bool split = sg.n_seg > 1;
     const int part_stride = p.Hkv * kPartHeadFloats;
+    if (c.active) {
+      // lane (g, t) holds row g, dims 32 t .. 32 t + 31: value v < 16 is tile v column 2t (dim
+      // 32 t + v), v >= 16 is tile v - 16 column 2t + 1 (dim 32 t + v); hi and lo rows summed
+      const uint32_t mg = c.sbase + kOffMerge + c.head * kMergeHeadBytes;
+      volatile float* mml =
+          reinterpret_cast<volatile float*>(smem + kOffMerge + c.head * kMergeHeadBytes + 8 * 32 * 16);
+      const uint32_t hb = kNbHead0 + c.head;
+      if (c.qd & 1) {
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int h = 2 * c.pr + e;
-      if (h >= p.Hkv) continue;
-      uint32_t o[8];
-      tmem_ld8(tbase + c.lane_base + kColOMain + h * 16, o);
-      tmem_wait_ld();
-      float* part = split ? p.partials + (int64_t)sg.part * part_stride + h * kPartHeadFloats
-                          : nullptr;
+        for (int q = 0; q < 8; ++q) {
+          float o[4];
 #pragma unroll
-      for (int i = 0; i < kRows; ++i) {
-        const int r = row0 + i;
-        const float ov = __uint_as_float(o[i]);
-        const float Ls = l_s[h * 8 + i];
-        if (split) {
-          if (r < rows_total) part[i * 128 + dim] = ov;
-          if (dim == 0) {
-            part[kRows * 128 + i] = mu_s[h * 8 + i];
-            part[kRows * 128 + kRows + i] = Ls;
+          for (int e = 0; e < 4; ++e) {
+            const int v = 4 * q + e;
+            o[e] = v < 16 ? acc[v][0] + acc[v][2] : acc[v - 16][1] + acc[v - 16][3];
           }
-        } else if (r < rows_total && Ls > 0.f) {
-          store_row(p, sg.seq, h, r, dim, ov / Ls);
+          sts128(mg + (q * 32 + lane) * 16, __float_as_uint(o[0]), __float_as_uint(o[1]),
+                 __float_as_uint(o[2]), __float_as_uint(o[3]));
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int i = 0; i < kRows; ++i) { mml[i] = m[i]; mml[kRows + i] = lp[i]; }
+        }
+        named_barrier_sync(hb, 64);  // state written
+        named_barrier_sync(hb, 64);  // state read: the area is free for the next segment
+      } else {
+        named_barrier_sync(hb, 64);
+        const float m1 = pick8(m, g), l1 = pick8(lp, g);
+        const float m2 = mml[g], l2 = mml[kRows + g];
+        const float M = fmaxf(m1, m2);
+        const float f1 = (m1 == -INFINITY) ? 0.f : fast_exp2((m1 - M) * c2);
+        const float f2 = (m2 == -INFINITY) ? 0.f : fast_exp2((m2 - M) * c2);
+        const float L = f1 * l1 + f2 * l2;
+        float o[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 u = lds128(mg + (q * 32 + lane) * 16);
+          const float other[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                  __uint_as_float(u.w)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int v = 4 * q + e;
+            const float mine = v < 16 ? acc[v][0] + acc[v][2] : acc[v - 16][1] + acc[v - 16][3];
+            o[v] = f1 * mine + f2 * other[e];
+          }
+        }
+        named_barrier_sync(hb, 64);
+        const int r = row0 + g;
+        if (split) {
+          float* part = p.partials + (int64_t)sg.part * part_stride + c.head * kPartHeadFloats;
+          float4* dst = reinterpret_cast<float4*>(part + g * 128 + 32 * t);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+          if (t == 0) {
+            part[kRows * 128 + g] = M;
+            part[kRows * 128 + kRows + g] = L;
+          }
+        } else if (r < rows_total && L > 0.f) {
+          const int tok = r / p.G, qh = c.head * p.G + r % p.G;
+          float4* dst = reinterpret_cast<float4*>(
+              p.out + (((int64_t)sg.seq * p.q_len + tok) * p.Hq + qh) * 128 + 32 * t);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(o[4 * q] / L, o[4 * q + 1] / L, o[4 * q + 2] / L, o[4 * q + 3] / L);
         }
       }
     }
     if (split) {
       // the CTA that completes the group's last segment combines all of its partials
       __threadfence();
-      named_barrier_sync(3, 32 * kSoftmaxWarps);
-      if (c.pr == 0 && c.gt == 0) {
+      named_barrier_sync(kNbAttn, 32 * kAttnWarps);
+      if (aw == 0 && lane == 0) {
         __threadfence();
         const int ticket = atomicAdd(p.counters + sg.group, 1);
         const int last = ticket == sg.n_seg - 1;
         if (last) p.counters[sg.group] = 0;  // ready for the next call on this workspace
         flags[24] = last;
       }
-      named_barrier_sync(3, 32 * kSoftmaxWarps);
+      named_barrier_sync(kNbAttn, 32 * kAttnWarps);
       if (flags[24]) {
         __threadfence();
         const float* pb = p.partials + (int64_t)sg.first_part * part_stride;
-        for (int e = 0; e < 2; ++e) {
-          const int h = 2 * c.pr + e;
-          if (h >= p.Hkv) continue;
-          for (int i = 0; i < kRows; ++i) {
-            const int r = row0 + i;
-            if (r >= rows_total) continue;
-            const float* ph = pb + h * kPartHeadFloats;
-            float M = -INFINITY;
-            for (int q = 0; q < sg.n_seg; ++q)
-              M = fmaxf(M, __ldcg(ph + (int64_t)q * part_stride + kRows * 128 + i));
-            float Lt = 0.f, Ot = 0.f;
-            for (int q = 0; q < sg.n_seg; ++q) {
-              const float* pq = ph + (int64_t)q * part_stride;
-              const float mq = __ldcg(pq + kRows * 128 + i);
-              const float f = (mq == -INFINITY) ? 0.f : fast_exp2((mq - M) * p.c2);
-              Lt += f * __ldcg(pq + kRows * 128 + kRows + i);
-              Ot += f * __ldcg(pq + i * 128 + dim);
-            }
-            if (Lt > 0.f) store_row(p, sg.seq, h, r, dim, Ot / Lt);
+        const int items = p.Hkv * kRows * 32;  // (head, row, 4 dims)
+        for (int it = aw * 32 + lane; it < items; it += 32 * kAttnWarps) {
+          const int h = it / (kRows * 32), i = (it >> 5) % kRows, d4 = it & 31;
+          const int r = row0 + i;
+          if (r >= rows_total) continue;
+          const float* ph = pb + h * kPartHeadFloats;
+          float M = -INFINITY;
+          for (int q = 0; q < sg.n_seg; ++q)
+            M = fmaxf(M, __ldcg(ph + (int64_t)q * part_stride + kRows * 128 + i));
+          float Lt = 0.f;
+          float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int q = 0; q < sg.n_seg; ++q) {
+            const float* pq = ph + (int64_t)q * part_stride;
+            const float mq = __ldcg(pq + kRows * 128 + i);
+            const float f = (mq == -INFINITY) ? 0.f : fast_exp2((mq - M) * c2);
+            Lt += f * __ldcg(pq + kRows * 128 + kRows + i);
+            const float4 ov = __ldcg(reinterpret_cast<const float4*>(pq + i * 128 + 4 * d4));
+            Ot.x += f * ov.x; Ot.y += f * ov.y; Ot.z += f * ov.z; Ot.w += f * ov.w;
+          }
+          if (Lt > 0.f) {
+            const int tok = r / p.G, qh = h * p.G + r % p.G;
+            float4* dst = reinterpret_cast<float4*>(
+                p.out + (((int64_t)sg.seq * p.q_len + tok) * p.Hq + qh) * 128 + 4 * d4);
+            *dst = make_float4(Ot.x / Lt, Ot.y / Lt, Ot.z / Lt, Ot.w / Lt);
           }
         }
       }
+      named_barrier_sync(kNbAttn, 32 * kAttnWarps);  // the ticket flag is reused
     }
-    named_barrier_sync(3, 32 * kSoftmaxWarps);  // scratch reused by the next segment
   }
   if (c.timed_out && lane == 0) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
 
-// --------------------------------------------------------------------------------------------
-// Dequant warps: V codes x E4M3 scales -> f16 V^T tile (MN-major: 8 dims x 8 keys core tiles).
-// Warp wd takes keys 16 wd .. 16 wd + 15 of every head (two groups of 8), each lane one key and one
-// 32-dim quarter per group; the quarter is rotated by key so that shared-memory reads and writes
-// are free of bank conflicts.
-// --------------------------------------------------------------------------------------------
-__device__ void dequant_warps(const DecodeParams& p, uint8_t* smem, int warp, int lane) {
-  const uint32_t sbase = smem_u32(smem);
-  const uint32_t bars = sbase + kOffBars;
-  const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kOffStagePid);
-  const int wd = warp - kWarpDequant0;
-  const int quarter = ((lane >> 3) + ((lane & 7) >> 1)) & 3;
-  constexpr int kRounds = 64 / (8 * kDequantWarps);  // 8-key groups per warp and head
-  uint32_t k = 0, hp = 0;
-  bool timed_out = false;
-  const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
-  for (int s = s_begin; s < s_end; ++s) {
-    const SegInfo sg = load_seg(p, s);
-    for (int page = sg.lo; page < sg.hi; ++page, ++k) {
-      const uint32_t st = k % kStages;
-      wait_bar(bars + 8 * (kBarStageFull + st), (k / kStages) & 1, timed_out);
-      const bool pvalid = stage_pid[st] >= 0;
-      const uint32_t stage = sbase + kOffStage + st * kStageBytes;
-      for (int h = 0; h < p.Hkv; ++h, ++hp) {
-        const uint32_t slot = hp % kVhSlots;
-        if (hp >= kVhSlots) wait_bar(bars + 8 * (kBarVhFree + slot), ((hp / kVhSlots) - 1) & 1, timed_out);
-#pragma unroll
-        for (int rd = 0; rd < kRounds; ++rd) {
-          const int key = 8 * (kRounds * wd + rd) + (lane & 7);
-          const bool kvalid = pvalid && page * 64 + key < sg.len;
-          const uint4 cw = lds128(stage + p.Hkv * 4608 + h * 4096 + key * 64 + 16 * quarter);
-          const uint32_t sc = kvalid ? lds16(stage + p.Hkv * 8704 + h * 512 + key * 8 + 2 * quarter) : 0u;
-          const uint32_t sh = cvt_e4m3x2_f16(sc);
-          const uint32_t s0 = dup_lo(sh), s1 = dup_hi(sh);
-          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-          const uint32_t vh = sbase + kOffVh + slot * kVhBytes + (key >> 3) * 2048 + (key & 7) * 16;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t r0, r1, r2, r3;
-            cvt_e2m1x8_f16(words[q], r0, r1, r2, r3);
-            const uint32_t sq = q < 2 ? s0 : s1;  // dims 32 quarter + 8 q .. : block 2 quarter + q / 2
-            sts128(vh + (4 * quarter + q) * 128, hmul2(r0, sq), hmul2(r1, sq), hmul2(r2, sq),
-                   hmul2(r3, sq));
-          }
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars + 8 * (kBarVhFull + slot));
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8 * (kBarStageEmpty + st));
-    }
-  }
-  if (timed_out && lane == 0) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
-}
-
-__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bars = smem_u32(smem + kOffBars);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bars + 8 * (kBarStageFull + s), 1);
-      mbar_init(bars + 8 * (kBarStageEmpty + s), 8 + kDequantWarps + 1);
+      mbar_init(bars + 8 * (kBarStageEmpty + s), 1 + kAttnWarps);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bars + 8 * (kBarSfaFull + b), 8);
+      mbar_init(bars + 8 * (kBarSfaFull + b), kAttnWarps);
       mbar_init(bars + 8 * (kBarQkDone + b), 1);
-      mbar_init(bars + 8 * (kBarSFree + b), 8);
-      mbar_init(bars + 8 * (kBarPFull + b), 8);
-      mbar_init(bars + 8 * (kBarPvDone + b), 1);
+      mbar_init(bars + 8 * (kBarSFree + b), kAttnWarps);
     }
-    for (int v = 0; v < kVhSlots; ++v) {
-      mbar_init(bars + 8 * (kBarVhFull + v), kDequantWarps);
-      mbar_init(bars + 8 * (kBarVhFree + v), 1);
-    }
-    mbar_init(bars + 8 * kBarQReady, 8);
-    for (int o = 0; o < kOSlots; ++o) mbar_init(bars + 8 * (kBarOFree + o), 8);
+    mbar_init(bars + 8 * kBarQReady, kAttnWarps);
     fence_mbar_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(smem + kOffTmemSlot), kTmemCols);
@@ -675,12 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecodeParams 
     producer(p, smem, lane);
   } else if (warp == kWarpMma) {
     if (lane == 0) qk_issuer(p, smem, tbase);
-  } else if (warp == kWarpPv) {
-    if (lane == 0) pv_issuer(p, smem, tbase);
-  } else if (warp < kWarpDequant0) {
-    softmax_warps(p, smem, tbase, warp, lane);
   } else {
-    dequant_warps(p, smem, warp, lane);
+    attention_warps(p, smem, tbase, warp, lane);
   }
 
   tc_fence_before();
