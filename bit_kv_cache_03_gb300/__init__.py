@@ -35,9 +35,9 @@ class PlanInfo(ctypes.Structure):
     """kv_nvfp4_plan_info"""
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_seqs", "q_len", "causal", "chunk_pages", "num_kv_heads", "num_row_groups",
-        "num_groups", "num_segments", "num_partials", "grid", "max_seq_len", "reserved")] + [
+        "num_groups", "num_segments", "num_partials", "grid", "max_seq_len", "num_split_groups")] + [
         ("total_kv_tokens", ctypes.c_int64), ("total_pages", ctypes.c_int64)] + [
-        (n, ctypes.c_uint64) for n in ("off_groups", "off_segments", "off_cta", "off_counters",
+        (n, ctypes.c_uint64) for n in ("off_groups", "off_segments", "off_cta", "off_split",
                                        "off_partials", "workspace_bytes")]
 
 
@@ -195,7 +195,7 @@ def kv_nvfp4_plan(layout, seq_lens, q_len, causal, chunk_tokens, workspace, ws_b
 
 def kv_nvfp4_plan_host(layout, seq_lens, q_len, causal, chunk_tokens, num_ctas):
     """Host image of the plan tables for `num_ctas` CTAs: (info, groups [n,8], segments [n,4],
-    cta ranges [num_ctas+1]) as numpy arrays."""
+    cta ranges [num_ctas+1], split-group list [num_split_groups]) as numpy arrays."""
     import numpy as np
     sl = np.ascontiguousarray(seq_lens, np.int32)
     info = PlanInfo()
@@ -214,7 +214,8 @@ def kv_nvfp4_plan_host(layout, seq_lens, q_len, causal, chunk_tokens, num_ctas):
     groups = i32[info.off_groups // 4: info.off_groups // 4 + 8 * info.num_groups].reshape(-1, 8)
     segs = i32[info.off_segments // 4: info.off_segments // 4 + 4 * info.num_segments].reshape(-1, 4)
     cta = i32[info.off_cta // 4: info.off_cta // 4 + info.grid + 1]
-    return info, groups.copy(), segs.copy(), cta.copy()
+    split = i32[info.off_split // 4: info.off_split // 4 + info.num_split_groups]
+    return info, groups.copy(), segs.copy(), cta.copy(), split.copy()
 
 
 def kv_nvfp4_decode_attn(layout, plan: PlanInfo, workspace, q_codes, q_scales, sm_scale, pool,

@@ -22,7 +22,8 @@ cudaError_t launch_append(const uint16_t* q, const uint16_t* k, const uint16_t* 
 cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const uint8_t* pool,
                           const int32_t* block_table, int32_t max_pages, int32_t num_pages,
                           const void* groups, const void* segments, const int32_t* cta_seg,
-                          int32_t* counters, float* partials, float* out, int32_t* status,
+                          const int32_t* split_groups, int32_t num_split, float* partials,
+                          float* out, int32_t* status,
                           int32_t Hq, int32_t Hkv, int32_t q_len, int32_t causal, int32_t grid,
                           float sm_scale, cudaStream_t stream);
 }  // namespace kvnvfp4
@@ -65,6 +66,7 @@ struct PlanBuild {
   std::vector<int32_t> groups;    // 8 ints per group
   std::vector<int32_t> segments;  // 4 ints per segment
   std::vector<int32_t> cta_seg;   // grid + 1
+  std::vector<int32_t> split;     // indices of the groups with more than one segment
 };
 
 kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, int32_t num_seqs,
@@ -133,7 +135,8 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
   }
   const int64_t n_seg = (int64_t)pb->segments.size() / 4;
   for (int64_t c = cta + 1; c <= grid; ++c) pb->cta_seg[(size_t)c] = (int32_t)n_seg;
-  // partial slots, contiguous per group in segment order
+  // partial slots, contiguous per group in segment order; the split groups, in group order, are
+  // the work list of the merge launch
   int64_t parts = 0;
   std::vector<int32_t> first_part((size_t)n_groups, -1);
   for (int64_t si = 0; si < n_seg; ++si) {
@@ -143,6 +146,9 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
       pb->segments[(size_t)si * 4 + 3] = (int32_t)parts++;
     }
   }
+  pb->split.clear();
+  for (int64_t gi = 0; gi < n_groups; ++gi)
+    if (seg_count[(size_t)gi] > 1) pb->split.push_back((int32_t)gi);
   for (int64_t gi = 0; gi < n_groups; ++gi) {
     const int64_t rg = gi % n_rg, s = gi / n_rg;
     int32_t* g = &pb->groups[(size_t)gi * 8];
@@ -160,6 +166,7 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
   info->num_groups = (int32_t)n_groups;
   info->num_segments = (int32_t)n_seg;
   info->num_partials = (int32_t)parts;
+  info->num_split_groups = (int32_t)pb->split.size();
   info->grid = (int32_t)grid;
   info->max_seq_len = (int32_t)max_len;
   info->total_kv_tokens = total_tok;
@@ -171,8 +178,8 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
   off = align_up(off + 16ull * n_seg, 256);
   info->off_cta = off;
   off = align_up(off + 4ull * (grid + 1), 256);
-  info->off_counters = off;
-  off = align_up(off + 4ull * n_groups, 256);
+  info->off_split = off;
+  off = align_up(off + 4ull * pb->split.size(), 256);
   info->off_partials = off;
   off = align_up(off + 4ull * kPartHeadFloats * L->num_kv_heads * parts, 256);
   info->workspace_bytes = off;
@@ -319,6 +326,7 @@ kv_nvfp4_status kv_nvfp4_plan_host(const kv_nvfp4_layout* L, const int32_t* h_se
   std::memcpy(h + pi.off_groups, pb.groups.data(), pb.groups.size() * 4);
   std::memcpy(h + pi.off_segments, pb.segments.data(), pb.segments.size() * 4);
   std::memcpy(h + pi.off_cta, pb.cta_seg.data(), pb.cta_seg.size() * 4);
+  std::memcpy(h + pi.off_split, pb.split.data(), pb.split.size() * 4);
   *info = pi;
   return KV_NVFP4_OK;
 }
@@ -336,16 +344,15 @@ kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout* L, const int32_t* h_seq_len
   if (s != KV_NVFP4_OK) return s;
   const kv_nvfp4_plan_info& pi = pb.info;
   if (ws_bytes < pi.workspace_bytes) return KV_NVFP4_ENOSPACE;
-  // host image of the tables (everything before the tickets), one copy
-  std::vector<int32_t> host((size_t)(pi.off_counters / 4), 0);
+  // host image of the tables (everything before the partials), one copy
+  std::vector<int32_t> host((size_t)(pi.off_partials / 4), 0);
   std::memcpy(host.data() + pi.off_groups / 4, pb.groups.data(), pb.groups.size() * 4);
   std::memcpy(host.data() + pi.off_segments / 4, pb.segments.data(), pb.segments.size() * 4);
   std::memcpy(host.data() + pi.off_cta / 4, pb.cta_seg.data(), pb.cta_seg.size() * 4);
+  std::memcpy(host.data() + pi.off_split / 4, pb.split.data(), pb.split.size() * 4);
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e =
       cudaMemcpyAsync(d_workspace, host.data(), host.size() * 4, cudaMemcpyHostToDevice, st);
-  const size_t ctr_bytes = (size_t)(pi.off_partials - pi.off_counters);
-  if (e == cudaSuccess) e = cudaMemsetAsync((char*)d_workspace + pi.off_counters, 0, ctr_bytes, st);
   if (e != cudaSuccess) return cuda_status(e);
   *info = pi;
   return KV_NVFP4_OK;
@@ -375,7 +382,8 @@ kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout* L, const kv_nvfp4_pl
   const cudaError_t e = kvnvfp4::launch_decode(
       q_codes, q_scales, pool, d_block_table, max_pages, num_pages, ws + plan->off_groups,
       ws + plan->off_segments, (const int32_t*)(ws + plan->off_cta),
-      (int32_t*)(ws + plan->off_counters), (float*)(ws + plan->off_partials), out, d_status,
+      (const int32_t*)(ws + plan->off_split), plan->num_split_groups,
+      (float*)(ws + plan->off_partials), out, d_status,
       L->num_q_heads, L->num_kv_heads, plan->q_len, plan->causal, plan->grid, sm_scale,
       (cudaStream_t)stream);
   return cuda_status(e);

@@ -9,7 +9,8 @@
 // (query token, head in the GQA group). The plan lays the groups' pages end to end and gives each
 // persistent CTA (one per SM) a contiguous, page-balanced share: one or more segments, each a page
 // range of one group. A CTA's softmax state carries across the pages of a segment; a group that
-// spans CTAs leaves one (m, l, O) partial per segment and the CTA taking its last ticket merges.
+// spans CTAs leaves one (m, l, O) partial per segment, and a second launch merges the partials of
+// every split group in parallel.
 //
 // One page = 64 keys of every KV head, a 9216 x H byte block moved by ONE bulk async copy.
 //
@@ -65,24 +66,23 @@ constexpr int kMergeHeadBytes = 8 * 32 * 16 + 2 * kRows * 4;  // O: 8 float4 per
 
 // shared memory map
 constexpr int kOffStage = 0;
-constexpr int kOffPs = kOffStage + kStages * kStageBytes;
+constexpr int kOffSfStage = kOffStage + kStages * kStageBytes;  // [2][pair][k-half][32 rows x 16 B]
+constexpr int kOffPs = kOffSfStage + 2 * 2048;
 constexpr int kOffQ = kOffPs + kAttnWarps * kPsBytes;
 constexpr int kOffMerge = kOffQ + kQBytes;
 constexpr int kOffBars = kOffMerge + kMaxHkv * kMergeHeadBytes;
 // barrier indices
 constexpr int kBarStageFull = 0;                       // [kStages]
 constexpr int kBarStageEmpty = kBarStageFull + kStages;  // [kStages]
-constexpr int kBarSfaFull = kBarStageEmpty + kStages;  // [2]
-constexpr int kBarQkDone = kBarSfaFull + 2;            // [2]
+constexpr int kBarQkDone = kBarStageEmpty + kStages;   // [2]
 constexpr int kBarSFree = kBarQkDone + 2;              // [2]
 constexpr int kBarQReady = kBarSFree + 2;
 constexpr int kNumBars = kBarQReady + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
-// misc: stage page ids, tmem base, flags (ticket result)
+// misc: stage page ids, tmem base
 constexpr int kOffStagePid = kOffMisc;
 constexpr int kOffTmemSlot = kOffStagePid + 4 * 8;
-constexpr int kOffFlags = kOffTmemSlot + 16;
-constexpr int kSmemBytes = kOffFlags + 128;
+constexpr int kSmemBytes = kOffTmemSlot + 16;
 static_assert(kStages <= 8, "stage page-id slots");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
@@ -96,8 +96,8 @@ constexpr uint32_t kColSfb = 96;     // [2 pairs][2 k-halves][4]
 // N = 16, M = 128
 constexpr uint32_t kIdescQK = (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 
-// named barriers: 3 = all attention warps, 4 + h = the two warps of KV head h
-constexpr uint32_t kNbAttn = 3, kNbHead0 = 4;
+// named barriers: 4 + h = the two warps of KV head h
+constexpr uint32_t kNbHead0 = 4;
 
 struct DecodeParams {
   const uint8_t* q_codes;
@@ -109,7 +109,6 @@ struct DecodeParams {
   const int4* groups;      // 2 x int4 per group: {seq, 0, rg, len}, {n_seg, first_part, pages, 0}
   const int4* segments;    // {group, page_lo, page_hi, part_slot or -1}
   const int32_t* cta_seg;  // [grid + 1]
-  int32_t* counters;       // [num_groups] merge tickets
   float* partials;         // [num_partials][Hkv][kPartHeadFloats]
   float* out;
   int32_t* status;
@@ -194,36 +193,17 @@ __device__ void producer(const DecodeParams& p, uint8_t* smem, int lane) {
 }
 
 // --------------------------------------------------------------------------------------------
-// MMA issue (one thread each for Q.K^T and for P.V).
+// Q.K^T warp. Per page the 32 lanes gather the page's K scales into the order of the MMA's scale
+// factors (row i of a (pair, k-half) tile holds the 4-byte scale groups of MMA rows i, 32 + i,
+// 64 + i, 96 + i) in a shared staging tile; lane 0 copies the tiles into TMEM with tcgen05.cp
+// (replicated to the four lane quadrants) and issues the MMAs, which the tensor pipe runs after
+// the copies. The warp runs ahead of the attention warps as far as the stage ring and the two S
+// buffers allow.
 // --------------------------------------------------------------------------------------------
-__device__ __forceinline__ void issue_qk(const DecodeParams& p, uint32_t sbase, uint32_t tbase,
-                                         uint32_t k, int npairs, bool& timed_out) {
-  const uint32_t bars = sbase + kOffBars;
-  const uint32_t st = k % kStages, b = k & 1;
-  wait_bar(bars + 8 * (kBarStageFull + st), (k / kStages) & 1, timed_out);
-  wait_bar(bars + 8 * (kBarSfaFull + b), (k >> 1) & 1, timed_out);
-  if (k >= 2) wait_bar(bars + 8 * (kBarSFree + b), ((k >> 1) - 1) & 1, timed_out);
-  tc_fence_after();
-  const uint32_t kc = sbase + kOffStage + st * kStageBytes;
-  const uint32_t qb = sbase + kOffQ;
-  for (int pr = 0; pr < npairs; ++pr) {
-    for (int kh = 0; kh < 2; ++kh) {
-      const uint64_t ad = smem_desc(kc + pr * 8192 + kh * 256, 128, 512);
-      const uint64_t bd = smem_desc(qb + pr * 1024 + kh * 256, 128, 512);
-      mma_nvf4_ss(tbase + kColS + b * 32 + pr * 16, ad, bd, kIdescQK,
-                  tbase + kColSfa + b * 16 + pr * 8 + kh * 4, tbase + kColSfb + pr * 8 + kh * 4,
-                  (uint32_t)kh);
-    }
-  }
-  mma_commit(bars + 8 * (kBarQkDone + b));
-  mma_commit(bars + 8 * (kBarStageEmpty + st));  // K codes consumed once the QK MMAs complete
-}
-
-// Q.K^T issuer: runs ahead of the softmax as far as the stage ring, the scale-factor buffers and
-// the two S buffers allow.
-__device__ void qk_issuer(const DecodeParams& p, uint8_t* smem, uint32_t tbase) {
+__device__ void qk_warp(const DecodeParams& p, uint8_t* smem, uint32_t tbase, int lane) {
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kOffBars;
+  const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kOffStagePid);
   const int npairs = (p.Hkv + 1) >> 1;
   uint32_t k = 0, sgi = 0;
   bool timed_out = false;
@@ -231,11 +211,54 @@ __device__ void qk_issuer(const DecodeParams& p, uint8_t* smem, uint32_t tbase) 
   for (int s = s_begin; s < s_end; ++s, ++sgi) {
     const SegInfo sg = load_seg(p, s);
     wait_bar(bars + 8 * kBarQReady, sgi & 1, timed_out);  // Q tile and its scales for this group
-    for (int j = 0; j < sg.hi - sg.lo; ++j, ++k) issue_qk(p, sbase, tbase, k, npairs, timed_out);
+    for (int j = 0; j < sg.hi - sg.lo; ++j, ++k) {
+      const uint32_t st = k % kStages, b = k & 1;
+      wait_bar(bars + 8 * (kBarStageFull + st), (k / kStages) & 1, timed_out);
+      // S buffer b free: the attention warps have read S of page k - 2, so that page's MMAs and
+      // scale copies are complete and staging tile b may be rewritten
+      if (k >= 2) wait_bar(bars + 8 * (kBarSFree + b), ((k >> 1) - 1) & 1, timed_out);
+      const uint32_t stage = sbase + kOffStage + st * kStageBytes;
+      const uint32_t sfs = sbase + kOffSfStage + b * 2048;
+      const int kv_lim = stage_pid[st] >= 0 ? sg.len - (sg.lo + j) * 64 : 0;  // keys < kv_lim real
+      for (int pr = 0; pr < npairs; ++pr) {
+        uint32_t w0[4], w1[4];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int hh = 2 * pr + (jj >> 1), key = 32 * (jj & 1) + lane;
+          uint2 v = make_uint2(0u, 0u);
+          if (hh < p.Hkv && key < kv_lim) v = lds64(stage + p.Hkv * 4096 + hh * 512 + key * 8);
+          w0[jj] = v.x;  // k-half 0: scales of dims 0..63
+          w1[jj] = v.y;  // k-half 1: dims 64..127
+        }
+        sts128(sfs + (pr * 2) * 512 + lane * 16, w0[0], w0[1], w0[2], w0[3]);
+        sts128(sfs + (pr * 2 + 1) * 512 + lane * 16, w1[0], w1[1], w1[2], w1[3]);
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tc_fence_after();
+        for (int pr = 0; pr < npairs; ++pr)
+          for (int kh = 0; kh < 2; ++kh)
+            tmem_cp_32x128b_x4(tbase + kColSfa + b * 16 + pr * 8 + kh * 4,
+                               smem_desc(sfs + (pr * 2 + kh) * 512, 16, 128));
+        const uint32_t qb = sbase + kOffQ;
+        for (int pr = 0; pr < npairs; ++pr) {
+          for (int kh = 0; kh < 2; ++kh) {
+            const uint64_t ad = smem_desc(stage + pr * 8192 + kh * 256, 128, 512);
+            const uint64_t bd = smem_desc(qb + pr * 1024 + kh * 256, 128, 512);
+            mma_nvf4_ss(tbase + kColS + b * 32 + pr * 16, ad, bd, kIdescQK,
+                        tbase + kColSfa + b * 16 + pr * 8 + kh * 4,
+                        tbase + kColSfb + pr * 8 + kh * 4, (uint32_t)kh);
+          }
+        }
+        mma_commit(bars + 8 * (kBarQkDone + b));
+        mma_commit(bars + 8 * (kBarStageEmpty + st));  // K codes consumed once the MMAs complete
+      }
+      __syncwarp();
+    }
   }
   if (timed_out) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
-
 
 // --------------------------------------------------------------------------------------------
 // Attention warps: 8 warps, two groups of four. Group pr works on KV-head pair pr; within a group
@@ -247,36 +270,10 @@ struct AttnCtx {
   const DecodeParams* p;
   uint8_t* smem;
   uint32_t sbase, bars, tbase, lane_base;
-  int lane, qd, pr, head, key0, gt;  // gt: thread index within the pair group (0..127)
+  int lane, qd, pr, half, head, key0, gt;  // gt: thread index within the pair group (0..127)
   bool active;                       // the warp's head exists (Hkv may be odd)
   bool timed_out;
 };
-
-// Scale factors of page k's K rows of this warp's pair into TMEM (replicated 32-lane x 4-column
-// layout: lane i, column j holds the 4 scales of MMA row 32 j + i).
-__device__ __forceinline__ void write_sfa(AttnCtx& c, uint32_t k, int page, int len) {
-  const DecodeParams& p = *c.p;
-  const uint32_t st = k % kStages, b = k & 1;
-  wait_bar(c.bars + 8 * (kBarStageFull + st), (k / kStages) & 1, c.timed_out);
-  if (k >= 2) wait_bar(c.bars + 8 * (kBarQkDone + b), ((k >> 1) - 1) & 1, c.timed_out);
-  const bool pvalid = reinterpret_cast<volatile int32_t*>(c.smem + kOffStagePid)[st] >= 0;
-  const uint32_t ks = c.sbase + kOffStage + st * kStageBytes + p.Hkv * 4096;
-  const int kp0 = page * 64;
-  uint32_t sf[8];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int hh = 2 * c.pr + (j >> 1), kk = 32 * (j & 1) + c.lane;
-    uint2 v = make_uint2(0u, 0u);
-    if (hh < p.Hkv && pvalid && kp0 + kk < len) v = lds64(ks + hh * 512 + kk * 8);
-    sf[j] = v.x;      // k-half 0: scales of dims 0..63
-    sf[4 + j] = v.y;  // k-half 1: dims 64..127
-  }
-  tmem_st8(c.tbase + c.lane_base + kColSfa + b * 16 + c.pr * 8, sf);
-  tmem_wait_st();
-  tc_fence_before();
-  __syncwarp();
-  if (c.lane == 0) mbar_arrive(c.bars + 8 * (kBarSfaFull + b));
-}
 
 // Byte address of the hi (half 0) or lo (half 1) P row of warp-local key `key` in a warp's P tile:
 // four keys per 128-byte line, the 32-byte slots and 16-byte halves permuted by line so that both
@@ -293,6 +290,123 @@ __device__ __forceinline__ float pick8(const float (&v)[kRows], int i) {
   return r;
 }
 
+// Visibility of keys to the rows of the segment's row tile.
+struct RowVis {
+  int mylim;           // largest visible key position of row lane % 8 (-1 for a padding row)
+  int lim_min;         // the smallest limit over the real rows (that of row 0)
+  uint32_t rows_mask;  // bit i: row i is a real row
+};
+
+// Wait for page kk's scores and start loading this warp's slice (one key per lane, 8 rows).
+__device__ __forceinline__ void s_issue(AttnCtx& c, uint32_t kk, uint32_t (&sr)[8]) {
+  const uint32_t b = kk & 1;
+  wait_bar(c.bars + 8 * (kBarQkDone + b), (kk >> 1) & 1, c.timed_out);
+  tc_fence_after();
+  tmem_ld8(c.tbase + c.lane_base + kColS + b * 32 + c.pr * 16 + c.half * 8, sr);
+}
+
+// Finish loading page kk's scores, release the S buffer, and turn the scores into P in the P tile
+// at pt: page max per row over the warp's 32 keys (warp reductions), running max and row-sum
+// update, P = exp2((s - m) c2) <= 1 as f16 hi + lo. Returns whether a max grew (then alpha_g is
+// the factor for row g of the accumulator). kv_lim: keys of the page below it are real (0 when
+// the page was skipped).
+__device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, int page, int len,
+                                          const RowVis& rv, uint32_t (&sr)[8], float (&m)[kRows],
+                                          float (&lp)[kRows], uint32_t pt, int g, float c2,
+                                          float& alpha_g, int& kv_lim) {
+  tmem_wait_ld_regs(sr);
+  tc_fence_before();
+  __syncwarp();
+  if (c.lane == 0) mbar_arrive(c.bars + 8 * (kBarSFree + (kk & 1)));
+  const uint32_t st = kk % kStages;
+  // the Q.K^T warp saw this stage land; waiting here as well makes the V bytes and the page id
+  // visible to this warp (the wait returns at once)
+  wait_bar(c.bars + 8 * (kBarStageFull + st), (kk / kStages) & 1, c.timed_out);
+  const bool pvalid = reinterpret_cast<const volatile int32_t*>(c.smem + kOffStagePid)[st] >= 0;
+  kv_lim = pvalid ? len - page * 64 : 0;
+  if (!c.active) return false;
+  uint32_t vmask = 0;  // bit i: this lane's key is visible to row i
+  if (pvalid) {
+    if (page * 64 + 63 <= rv.lim_min) {
+      vmask = rv.rows_mask;
+    } else {
+      const int kp = page * 64 + c.key0 + c.lane;
+#pragma unroll
+      for (int i = 0; i < kRows; ++i)
+        if (kp <= __shfl_sync(0xffffffffu, rv.mylim, i)) vmask |= 1u << i;
+    }
+  }
+  int pmi[kRows];
+#pragma unroll
+  for (int i = 0; i < kRows; ++i)
+    pmi[i] = __reduce_max_sync(0xffffffffu,
+                               f2ord(((vmask >> i) & 1u) ? __uint_as_float(sr[i]) : -INFINITY));
+  float alpha[kRows];
+  bool grow = false;  // warp-uniform: every lane holds the same maxima
+#pragma unroll
+  for (int i = 0; i < kRows; ++i) {
+    const float mn = fmaxf(m[i], ord2f(pmi[i]));
+    alpha[i] = (mn == m[i]) ? 1.f : fast_exp2((m[i] - mn) * c2);  // 0 when m was -inf
+    grow |= mn != m[i];
+    lp[i] *= alpha[i];
+    m[i] = mn;
+  }
+  alpha_g = pick8(alpha, g);
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int i = 0; i < kRows; i += 2) {
+    const float p0 = ((vmask >> i) & 1u) ? fast_exp2((__uint_as_float(sr[i]) - m[i]) * c2) : 0.f;
+    const float p1 =
+        ((vmask >> (i + 1)) & 1u) ? fast_exp2((__uint_as_float(sr[i + 1]) - m[i + 1]) * c2) : 0.f;
+    lp[i] += p0;
+    lp[i + 1] += p1;
+    hi[i / 2] = pack_f16x2(p0, p1);
+    lo[i / 2] = pack_f16x2(p0 - f16_lo_to_f32(hi[i / 2]), p1 - f16_hi_to_f32(hi[i / 2]));
+  }
+  sts128(p_addr(pt, c.lane, 0), hi[0], hi[1], hi[2], hi[3]);
+  sts128(p_addr(pt, c.lane, 1), lo[0], lo[1], lo[2], lo[3]);
+  return grow;
+}
+
+// One 16-key step of O += P V for this warp: P from the P tile through transposing ldmatrix (lm:
+// this lane's row address), V codes of the lane's four keys (vk0, vk1, vk0 + 2, vk1 + 2 within the
+// step) and dims 16 g .. 16 g + 15, decoded into B fragments; a key at or past kv_lim gets scale 0
+// (its code bytes are stale).
+__device__ __forceinline__ void pv_step(int kb, uint32_t lm, uint32_t vc, uint32_t vs, int kv_lim,
+                                        int vk0, int vk1, float (&acc)[16][4]) {
+  uint32_t a0, a1, a2, a3;
+  ldsm_x4_trans(lm, a0, a1, a2, a3);
+  const int vk2 = vk0 + 2, vk3 = vk1 + 2;
+  const uint2 w0 = lds64(vc + (kb + vk0) * 64), w1 = lds64(vc + (kb + vk1) * 64);
+  const uint2 w2 = lds64(vc + (kb + vk2) * 64), w3 = lds64(vc + (kb + vk3) * 64);
+  const uint32_t s0 = kb + vk0 < kv_lim ? lds8(vs + (kb + vk0) * 8) : 0u;
+  const uint32_t s1 = kb + vk1 < kv_lim ? lds8(vs + (kb + vk1) * 8) : 0u;
+  const uint32_t s2 = kb + vk2 < kv_lim ? lds8(vs + (kb + vk2) * 8) : 0u;
+  const uint32_t s3 = kb + vk3 < kv_lim ? lds8(vs + (kb + vk3) * 8) : 0u;
+  const uint32_t sc01 = cvt_e4m3x2_f16(s0 | (s1 << 8));
+  const uint32_t sc23 = cvt_e4m3x2_f16(s2 | (s3 << 8));
+#pragma unroll
+  for (int w = 0; w < 2; ++w) {  // dims 16 g + 8 w .. 16 g + 8 w + 7
+    const uint32_t x0 = w ? w0.y : w0.x, x1 = w ? w1.y : w1.x;
+    const uint32_t x2 = w ? w2.y : w2.x, x3 = w ? w3.y : w3.x;
+    // one byte per dim holding the nibbles of two keys: (first key low, second key high)
+    const uint32_t ze01 = (x0 & 0x0F0F0F0Fu) | ((x1 << 4) & 0xF0F0F0F0u);
+    const uint32_t zo01 = ((x0 >> 4) & 0x0F0F0F0Fu) | (x1 & 0xF0F0F0F0u);
+    const uint32_t ze23 = (x2 & 0x0F0F0F0Fu) | ((x3 << 4) & 0xF0F0F0F0u);
+    const uint32_t zo23 = ((x2 >> 4) & 0x0F0F0F0Fu) | (x3 & 0xF0F0F0F0u);
+    uint32_t e0[4], o0[4], e2[4], o2[4];
+    cvt_e2m1x8_f16(ze01, e0[0], e0[1], e0[2], e0[3]);
+    cvt_e2m1x8_f16(zo01, o0[0], o0[1], o0[2], o0[3]);
+    cvt_e2m1x8_f16(ze23, e2[0], e2[1], e2[2], e2[3]);
+    cvt_e2m1x8_f16(zo23, o2[0], o2[1], o2[2], o2[3]);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      mma16816(acc[8 * w + 2 * jj], a0, a1, a2, a3, hmul2(e0[jj], sc01), hmul2(e2[jj], sc23));
+      mma16816(acc[8 * w + 2 * jj + 1], a0, a1, a2, a3, hmul2(o0[jj], sc01), hmul2(o2[jj], sc23));
+    }
+  }
+}
+
 __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t tbase, int warp,
                                 int lane) {
   AttnCtx c;
@@ -301,8 +415,8 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
   const int aw = warp - kWarpAttn0;
   c.pr = aw >> 2;
   c.lane_base = (uint32_t)(c.qd * 32) << 16;
-  const int half = c.qd >> 1;         // TMEM lanes 64..127 hold the odd head of the pair
-  c.head = 2 * c.pr + half;
+  c.half = c.qd >> 1;                 // TMEM lanes 64..127 hold the odd head of the pair
+  c.head = 2 * c.pr + c.half;
   c.key0 = 32 * (c.qd & 1);
   c.active = c.head < p.Hkv;
   c.gt = (aw & 3) * 32 + lane;
@@ -321,11 +435,8 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
   // B fragment keys of this lane within a 16-key step: k = 2t, 2t+1, 2t+8, 2t+9 -> keys
   // 4t + {0,1,2,3} with the pair order flipped for odd t (so lanes t and t+1 read different banks)
   const int vk0 = 4 * t + (t & 1), vk1 = 4 * t + 1 - (t & 1);
-  const int vk2 = vk0 + 2, vk3 = vk1 + 2;
   const int rows_total = p.G * p.q_len;
   const float c2 = p.c2;
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + kOffFlags);
-  const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kOffStagePid);
   uint32_t k = 0;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
 
@@ -389,112 +500,29 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[dd][q] = 0.f;
 
-    write_sfa(c, k, sg.lo, sg.len);
+    // Per page: scores -> running max, row sums and P (one P tile), accumulator rescale when a
+    // max grew, then two 16-key steps of O += P V.
+    const RowVis rv{mylim, lim_min, rows_mask};
     for (int j = 0; j < n; ++j, ++k) {
-      if (j + 1 < n) write_sfa(c, k + 1, sg.lo + j + 1, sg.len);
-      const uint32_t b = k & 1, st = k % kStages;
-      wait_bar(c.bars + 8 * (kBarQkDone + b), (k >> 1) & 1, c.timed_out);
-      tc_fence_after();
+      const uint32_t st = k % kStages;
       uint32_t sr[8];
-      tmem_ld8(tbase + c.lane_base + kColS + b * 32 + c.pr * 16 + half * 8, sr);
-      tmem_wait_ld();
-      tc_fence_before();
+      float alpha_g = 1.f;
+      int kv_lim = 0;
+      s_issue(c, k, sr);
+      const bool grow = s_softmax(c, k, sg.lo + j, sg.len, rv, sr, m, lp, ps, g, c2, alpha_g, kv_lim);
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bars + 8 * (kBarSFree + b));
-
-      const int page = sg.lo + j;
-      const bool pvalid = stage_pid[st] >= 0;
+      if (grow) {
+#pragma unroll
+        for (int dd = 0; dd < 16; ++dd)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[dd][q] *= alpha_g;
+      }
       if (c.active) {
-        // ---- visibility of this lane's key to each row ----
-        uint32_t vmask = 0;
-        if (pvalid) {
-          if (page * 64 + 63 <= lim_min) {
-            vmask = rows_mask;
-          } else {
-            const int kp = page * 64 + c.key0 + lane;
-#pragma unroll
-            for (int i = 0; i < kRows; ++i)
-              if (kp <= __shfl_sync(0xffffffffu, mylim, i)) vmask |= 1u << i;
-          }
-        }
-        // ---- page max per row over the warp's 32 keys; rescale when it grows ----
-        float alpha_g = 1.f;
-        bool grow = false;
-#pragma unroll
-        for (int i = 0; i < kRows; ++i) {
-          const float x = ((vmask >> i) & 1u) ? __uint_as_float(sr[i]) : -INFINITY;
-          const float pm = ord2f(__reduce_max_sync(0xffffffffu, f2ord(x)));
-          if (pm > m[i]) {  // warp-uniform
-            const float a = fast_exp2((m[i] - pm) * c2);  // 0 when m was -inf
-            lp[i] *= a;
-            m[i] = pm;
-            grow = true;
-            if (g == i) alpha_g = a;
-          }
-        }
-        if (grow) {
-#pragma unroll
-          for (int dd = 0; dd < 16; ++dd)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[dd][q] *= alpha_g;
-        }
-        // ---- P = exp2((s - m) c2) <= 1 as f16 hi + lo into the warp's P tile ----
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int i = 0; i < kRows; i += 2) {
-          const float p0 = ((vmask >> i) & 1u) ? fast_exp2((__uint_as_float(sr[i]) - m[i]) * c2) : 0.f;
-          const float p1 =
-              ((vmask >> (i + 1)) & 1u) ? fast_exp2((__uint_as_float(sr[i + 1]) - m[i + 1]) * c2) : 0.f;
-          lp[i] += p0;
-          lp[i + 1] += p1;
-          hi[i / 2] = pack_f16x2(p0, p1);
-          lo[i / 2] = pack_f16x2(p0 - f16_lo_to_f32(hi[i / 2]), p1 - f16_hi_to_f32(hi[i / 2]));
-        }
-        sts128(p_addr(ps, lane, 0), hi[0], hi[1], hi[2], hi[3]);
-        sts128(p_addr(ps, lane, 1), lo[0], lo[1], lo[2], lo[3]);
-        __syncwarp();
-
-        // ---- O += P V over the warp's 32 keys: two 16-key steps ----
         const uint32_t stage = c.sbase + kOffStage + st * kStageBytes;
         const uint32_t vc = stage + p.Hkv * 4608 + c.head * 4096 + 8 * g;  // codes of dims 16 g ..
         const uint32_t vs = stage + p.Hkv * 8704 + c.head * 512 + g;       // scale of block g
-        const int kv_lim = pvalid ? sg.len - page * 64 : 0;                 // keys < kv_lim are real
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_trans(ks ? lm_addr1 : lm_addr0, a0, a1, a2, a3);
-          const int kb = c.key0 + 16 * ks;
-          const uint2 w0 = lds64(vc + (kb + vk0) * 64), w1 = lds64(vc + (kb + vk1) * 64);
-          const uint2 w2 = lds64(vc + (kb + vk2) * 64), w3 = lds64(vc + (kb + vk3) * 64);
-          // a key past the end or on a skipped page gets scale 0 (its codes are stale bytes)
-          const uint32_t s0 = kb + vk0 < kv_lim ? lds8(vs + (kb + vk0) * 8) : 0u;
-          const uint32_t s1 = kb + vk1 < kv_lim ? lds8(vs + (kb + vk1) * 8) : 0u;
-          const uint32_t s2 = kb + vk2 < kv_lim ? lds8(vs + (kb + vk2) * 8) : 0u;
-          const uint32_t s3 = kb + vk3 < kv_lim ? lds8(vs + (kb + vk3) * 8) : 0u;
-          const uint32_t sc01 = cvt_e4m3x2_f16(s0 | (s1 << 8));
-          const uint32_t sc23 = cvt_e4m3x2_f16(s2 | (s3 << 8));
-#pragma unroll
-          for (int w = 0; w < 2; ++w) {  // dims 16 g + 8 w .. 16 g + 8 w + 7
-            const uint32_t x0 = w ? w0.y : w0.x, x1 = w ? w1.y : w1.x;
-            const uint32_t x2 = w ? w2.y : w2.x, x3 = w ? w3.y : w3.x;
-            // one byte per dim holding the nibbles of two keys: (key A low, key B high)
-            const uint32_t ze01 = (x0 & 0x0F0F0F0Fu) | ((x1 << 4) & 0xF0F0F0F0u);
-            const uint32_t zo01 = ((x0 >> 4) & 0x0F0F0F0Fu) | (x1 & 0xF0F0F0F0u);
-            const uint32_t ze23 = (x2 & 0x0F0F0F0Fu) | ((x3 << 4) & 0xF0F0F0F0u);
-            const uint32_t zo23 = ((x2 >> 4) & 0x0F0F0F0Fu) | (x3 & 0xF0F0F0F0u);
-            uint32_t e0[4], o0[4], e2[4], o2[4];
-            cvt_e2m1x8_f16(ze01, e0[0], e0[1], e0[2], e0[3]);
-            cvt_e2m1x8_f16(zo01, o0[0], o0[1], o0[2], o0[3]);
-            cvt_e2m1x8_f16(ze23, e2[0], e2[1], e2[2], e2[3]);
-            cvt_e2m1x8_f16(zo23, o2[0], o2[1], o2[2], o2[3]);
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              mma16816(acc[8 * w + 2 * jj], a0, a1, a2, a3, hmul2(e0[jj], sc01), hmul2(e2[jj], sc23));
-              mma16816(acc[8 * w + 2 * jj + 1], a0, a1, a2, a3, hmul2(o0[jj], sc01),
-                       hmul2(o2[jj], sc23));
-            }
-          }
-        }
+        pv_step(c.key0, lm_addr0, vc, vs, kv_lim, vk0, vk1, acc);
+        pv_step(c.key0 + 16, lm_addr1, vc, vs, kv_lim, vk0, vk1, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bars + 8 * (kBarStageEmpty + st));
@@ -578,50 +606,6 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
         }
       }
     }
-    if (split) {
-      // the CTA that completes the group's last segment combines all of its partials
-      __threadfence();
-      named_barrier_sync(kNbAttn, 32 * kAttnWarps);
-      if (aw == 0 && lane == 0) {
-        __threadfence();
-        const int ticket = atomicAdd(p.counters + sg.group, 1);
-        const int last = ticket == sg.n_seg - 1;
-        if (last) p.counters[sg.group] = 0;  // ready for the next call on this workspace
-        flags[24] = last;
-      }
-      named_barrier_sync(kNbAttn, 32 * kAttnWarps);
-      if (flags[24]) {
-        __threadfence();
-        const float* pb = p.partials + (int64_t)sg.first_part * part_stride;
-        const int items = p.Hkv * kRows * 32;  // (head, row, 4 dims)
-        for (int it = aw * 32 + lane; it < items; it += 32 * kAttnWarps) {
-          const int h = it / (kRows * 32), i = (it >> 5) % kRows, d4 = it & 31;
-          const int r = row0 + i;
-          if (r >= rows_total) continue;
-          const float* ph = pb + h * kPartHeadFloats;
-          float M = -INFINITY;
-          for (int q = 0; q < sg.n_seg; ++q)
-            M = fmaxf(M, __ldcg(ph + (int64_t)q * part_stride + kRows * 128 + i));
-          float Lt = 0.f;
-          float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int q = 0; q < sg.n_seg; ++q) {
-            const float* pq = ph + (int64_t)q * part_stride;
-            const float mq = __ldcg(pq + kRows * 128 + i);
-            const float f = (mq == -INFINITY) ? 0.f : fast_exp2((mq - M) * c2);
-            Lt += f * __ldcg(pq + kRows * 128 + kRows + i);
-            const float4 ov = __ldcg(reinterpret_cast<const float4*>(pq + i * 128 + 4 * d4));
-            Ot.x += f * ov.x; Ot.y += f * ov.y; Ot.z += f * ov.z; Ot.w += f * ov.w;
-          }
-          if (Lt > 0.f) {
-            const int tok = r / p.G, qh = h * p.G + r % p.G;
-            float4* dst = reinterpret_cast<float4*>(
-                p.out + (((int64_t)sg.seq * p.q_len + tok) * p.Hq + qh) * 128 + 4 * d4);
-            *dst = make_float4(Ot.x / Lt, Ot.y / Lt, Ot.z / Lt, Ot.w / Lt);
-          }
-        }
-      }
-      named_barrier_sync(kNbAttn, 32 * kAttnWarps);  // the ticket flag is reused
-    }
   }
   if (c.timed_out && lane == 0) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
@@ -636,7 +620,6 @@ __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodePa
       mbar_init(bars + 8 * (kBarStageEmpty + s), 1 + kAttnWarps);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bars + 8 * (kBarSfaFull + b), kAttnWarps);
       mbar_init(bars + 8 * (kBarQkDone + b), 1);
       mbar_init(bars + 8 * (kBarSFree + b), kAttnWarps);
     }
@@ -652,7 +635,7 @@ __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodePa
   if (warp == kWarpProducer) {
     producer(p, smem, lane);
   } else if (warp == kWarpMma) {
-    if (lane == 0) qk_issuer(p, smem, tbase);
+    qk_warp(p, smem, tbase, lane);
   } else {
     attention_warps(p, smem, tbase, warp, lane);
   }
@@ -663,6 +646,73 @@ __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodePa
   if (warp == kWarpMma) tmem_dealloc(tbase, kTmemCols);
 }
 
+// --------------------------------------------------------------------------------------------
+// Split-K merge (second launch). One CTA per (split group, KV head, row of the tile); its 256
+// threads are 8 slices of the group's partials x 32 four-dim columns, so the partial reads of all
+// groups run in parallel across the GPU:
+//   M = max_q m_q,  L = sum_q 2^((m_q - M) c2) l_q,  o = sum_q 2^((m_q - M) c2) O_q / L.
+// --------------------------------------------------------------------------------------------
+struct MergeParams {
+  const int4* groups;
+  const int32_t* split;    // [num_split] group indices
+  const float* partials;   // [num_partials][Hkv][kPartHeadFloats]
+  float* out;
+  int32_t Hq, Hkv, G, q_len;
+  float c2;
+};
+
+__global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
+  __shared__ float s_m[8], s_l[8];
+  __shared__ float4 s_o[8][32];
+  const int gi = p.split[blockIdx.x];
+  const int h = blockIdx.y / kRows, i = blockIdx.y % kRows;
+  const int4 g0 = p.groups[2 * gi], g1 = p.groups[2 * gi + 1];
+  const int r = g0.z * kRows + i;
+  if (r >= p.G * p.q_len) return;  // padding row of the last tile (uniform over the CTA)
+  const int n_seg = g1.x;
+  const int slice = threadIdx.x >> 5, d4 = threadIdx.x & 31;
+  const int64_t stride = (int64_t)p.Hkv * kPartHeadFloats;
+  const float* base = p.partials + (int64_t)g1.y * stride + h * kPartHeadFloats;
+  float mx = -INFINITY;
+  for (int q = slice; q < n_seg; q += 8) mx = fmaxf(mx, __ldcg(base + q * stride + kRows * 128 + i));
+  if (d4 == 0) s_m[slice] = mx;
+  __syncthreads();
+  float M = s_m[0];
+#pragma unroll
+  for (int j = 1; j < 8; ++j) M = fmaxf(M, s_m[j]);
+  float L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int q = slice; q < n_seg; q += 8) {
+    const float* pq = base + q * stride;
+    const float mq = __ldcg(pq + kRows * 128 + i);
+    const float lq = __ldcg(pq + kRows * 128 + kRows + i);
+    const float4 ov = __ldcg(reinterpret_cast<const float4*>(pq + i * 128) + d4);
+    const float f = (mq == -INFINITY) ? 0.f : fast_exp2((mq - M) * p.c2);
+    L += f * lq;
+    O.x += f * ov.x; O.y += f * ov.y; O.z += f * ov.z; O.w += f * ov.w;
+  }
+  s_o[slice][d4] = O;
+  if (d4 == 0) s_l[slice] = L;
+  __syncthreads();
+  if (slice == 0) {
+    float Lt = 0.f;
+    float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      Lt += s_l[j];
+      const float4 v = s_o[j][d4];
+      Ot.x += v.x; Ot.y += v.y; Ot.z += v.z; Ot.w += v.w;
+    }
+    if (Lt > 0.f) {
+      const int tok = r / p.G, qh = h * p.G + r % p.G;
+      float4* dst = reinterpret_cast<float4*>(
+          p.out + (((int64_t)g0.x * p.q_len + tok) * p.Hq + qh) * 128 + 4 * d4);
+      *dst = make_float4(Ot.x / Lt, Ot.y / Lt, Ot.z / Lt, Ot.w / Lt);
+    }
+  }
+}
+
 }  // namespace
 
 int decode_smem_bytes() { return kSmemBytes; }
@@ -670,7 +720,8 @@ int decode_smem_bytes() { return kSmemBytes; }
 cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const uint8_t* pool,
                           const int32_t* block_table, int32_t max_pages, int32_t num_pages,
                           const void* groups, const void* segments, const int32_t* cta_seg,
-                          int32_t* counters, float* partials, float* out, int32_t* status,
+                          const int32_t* split_groups, int32_t num_split, float* partials,
+                          float* out, int32_t* status,
                           int32_t Hq, int32_t Hkv, int32_t q_len, int32_t causal, int32_t grid,
                           float sm_scale, cudaStream_t stream) {
   static bool attr_done = false;  // the attribute belongs to the function, set once per process
@@ -687,11 +738,17 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
   p.groups = reinterpret_cast<const int4*>(groups);
   p.segments = reinterpret_cast<const int4*>(segments);
   p.cta_seg = cta_seg;
-  p.counters = counters; p.partials = partials; p.out = out; p.status = status;
+  p.partials = partials; p.out = out; p.status = status;
   p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.q_len = q_len; p.causal = causal;
   p.c2 = sm_scale * 1.4426950408889634f;
   if (grid <= 0) return cudaSuccess;
   decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || num_split <= 0) return e;
+  MergeParams mp;
+  mp.groups = p.groups; mp.split = split_groups; mp.partials = partials; mp.out = out;
+  mp.Hq = Hq; mp.Hkv = Hkv; mp.G = p.G; mp.q_len = q_len; mp.c2 = p.c2;
+  merge_kernel<<<dim3((unsigned)num_split, (unsigned)(Hkv * kRows)), 256, 0, stream>>>(mp);
   return cudaGetLastError();
 }
 

@@ -301,6 +301,13 @@ __device__ __forceinline__ void mma_nvf4_ss(uint32_t d_tmem, uint64_t a_desc, ui
 }
 
 // Arrive once on an mbarrier when every previously issued tcgen05.mma of this thread completes.
+// Shared memory -> TMEM copy of a 32-row x 16-byte tile (row i to lane i, four 32-bit columns),
+// replicated to all four lane quadrants; ordered before later MMAs issued by the same thread.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    bar)
@@ -336,6 +343,15 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
                "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
                "r"(r[7])
+               : "memory");
+}
+// Wait for this thread's TMEM loads, tying the loaded registers to the wait so that no use of
+// them is scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7])
+               :
                : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() {

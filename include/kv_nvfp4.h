@@ -96,10 +96,10 @@ typedef struct kv_nvfp4_plan_info {
   int32_t num_partials;    /* partial-result slots (segments of groups split over CTAs) */
   int32_t grid;            /* CTAs of the attention launch, at most the SM count */
   int32_t max_seq_len;     /* longest sequence; must fit max_pages * 64 at attention time */
-  int32_t reserved;
+  int32_t num_split_groups; /* groups split over several CTAs (merged by a second launch) */
   int64_t total_kv_tokens; /* sum of seq_lens */
   int64_t total_pages;     /* pages visited by one attention call, summed over groups */
-  uint64_t off_groups, off_segments, off_cta, off_counters, off_partials; /* byte offsets */
+  uint64_t off_groups, off_segments, off_cta, off_split, off_partials; /* byte offsets */
   uint64_t workspace_bytes;
 } kv_nvfp4_plan_info;
 
@@ -170,25 +170,26 @@ kv_nvfp4_status kv_nvfp4_append(const kv_nvfp4_layout *layout, const void *q, co
  * append, i.e. including the q_len new tokens). chunk_tokens (a positive multiple of 64) is the
  * split-K granularity: a sequence is only ever cut between chunks. 1024 suits long-context
  * decode; 64 lets the plan balance the CTAs to the page. The workspace holds the group and
- * segment tables, one int32 ticket per group, and one 4160-byte (m, l, O) partial per segment
- * of every group that spans more than one CTA. */
+ * segment tables, the list of split groups (those that span more than one CTA), and one
+ * 4160-byte (m, l, O) partial per KV head and segment of every split group. */
 kv_nvfp4_status kv_nvfp4_plan_workspace_bytes(const kv_nvfp4_layout *layout,
                                               const int32_t *h_seq_lens, int32_t num_seqs,
                                               int32_t q_len, int32_t causal,
                                               int32_t chunk_tokens, size_t *bytes);
 
 /* Host-only variant of kv_nvfp4_plan for a given CTA count: writes the image of the workspace
- * tables (groups, segments, per-CTA segment ranges, zeroed tickets; everything before
+ * tables (groups, segments, per-CTA segment ranges, split-group list; everything before
  * info->off_partials) into HOST memory h_workspace and fills *info. No CUDA call. Layout of the
- * image: groups are 8 int32 {seq, 0, row_tile, seq_len, n_segments, first_partial, pages, 0}; segments are 4 int32 {group, page_lo, page_hi, partial or -1}; CTA b owns
- * segments [cta[b], cta[b+1]). */
+ * image: groups are 8 int32 {seq, 0, row_tile, seq_len, n_segments, first_partial, pages, 0};
+ * segments are 4 int32 {group, page_lo, page_hi, partial or -1}; CTA b owns segments
+ * [cta[b], cta[b+1]); the split list holds info->num_split_groups group indices in order. */
 kv_nvfp4_status kv_nvfp4_plan_host(const kv_nvfp4_layout *layout, const int32_t *h_seq_lens,
                                    int32_t num_seqs, int32_t q_len, int32_t causal,
                                    int32_t chunk_tokens, int32_t num_ctas, void *h_workspace,
                                    size_t ws_bytes, kv_nvfp4_plan_info *info);
 
 /* Writes the work list into DEVICE memory d_workspace (ws_bytes at least the size above) on
- * `stream`, zeroes the merge tickets, and fills *info (HOST). Every seq_len must be >= q_len
+ * `stream` (one host-to-device copy) and fills *info (HOST). Every seq_len must be >= q_len
  * and >= 1. The CTA count is taken from the current device's SM count. The workspace holds
  * one (m, l, O) partial of num_kv_heads * 4160 bytes per segment of a group spread over several
  * CTAs. */
@@ -209,7 +210,10 @@ kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout *layout, const int32_t *h_se
  *   sm_scale:       softmax scale; <= 0 selects 1/sqrt(head_dim)
  *   pool, num_pages, d_block_table, max_pages: as for kv_nvfp4_append
  *   out:            DEVICE fp32 [num_seqs * q_len][num_q_heads][128]
- * Supports num_kv_heads <= 4 (every head of a page is staged together). One kernel launch. */
+ * Supports num_kv_heads <= 4 (every head of a page is staged together). Two kernel launches on
+ * `stream`: the attention kernel (one persistent CTA per SM), then, when the plan has split groups,
+ * the merge of their partials (one CTA per split group, KV head and row). The workspace may be
+ * reused by the next call on the same stream; calls that overlap on one workspace race. */
 kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout *layout,
                                      const kv_nvfp4_plan_info *plan, void *d_workspace,
                                      const uint8_t *q_codes, const uint8_t *q_scales,

@@ -22,7 +22,7 @@ def _check(w, chunk=None, steps=1):
         max_abs, rel = attention_errors(out, ref)
         assert max_abs <= MAX_ABS_TOL and rel <= REL_L2_TOL, (max_abs, rel)
     for out in outs[1:]:
-        assert np.array_equal(out, outs[0])  # repeat calls reuse the workspace counters
+        assert np.array_equal(out, outs[0])  # repeat calls on one workspace give the same result
     return outs[0], ref
 
 

@@ -110,7 +110,7 @@ def test_entry_points_reject_bad_arguments_before_cuda(kv):
 ])
 def test_plan_covers_every_visible_page_once_and_balances(kv, lens, q_len, causal, chunk, ctas):
     L = kv.make_layout()
-    info, groups, segs, cta = kv.kv_nvfp4_plan_host(L, lens, q_len, causal, chunk, ctas)
+    info, groups, segs, cta, split = kv.kv_nvfp4_plan_host(L, lens, q_len, causal, chunk, ctas)
     G = 6
     n_rg = (G * q_len + 7) // 8
     assert info.num_groups == len(lens) * n_rg == len(groups)
@@ -153,3 +153,7 @@ def test_plan_covers_every_visible_page_once_and_balances(kv, lens, q_len, causa
             assert parts == list(range(fp, fp + nseg))
         else:
             assert parts == [-1]
+    # the merge launch's work list: exactly the split groups, in group order
+    assert np.array_equal(split, np.flatnonzero(groups[:, 4] > 1))
+    assert info.num_split_groups == len(split)
+    assert info.off_split % 16 == 0 and info.off_partials % 16 == 0
