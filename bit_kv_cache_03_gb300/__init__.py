@@ -69,6 +69,8 @@ _SIG = {
                             ctypes.c_size_t, ctypes.POINTER(PlanInfo)], _I32),
     "kv_nvfp4_decode_attn": ([ctypes.POINTER(Layout), ctypes.POINTER(PlanInfo), _P, _P, _P,
                               ctypes.c_float, _P, _I32, _P, _I32, _P, _P, _P], _I32),
+    "kv_nvfp4_decode_attn_noalloc": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32, _P, _P,
+                                      ctypes.c_float, _P, _I32, _P, _I32, _P, _P, _P], _I32),
 }
 
 _lib = None
@@ -224,6 +226,19 @@ def kv_nvfp4_decode_attn(layout, plan: PlanInfo, workspace, q_codes, q_scales, s
         ctypes.byref(layout), ctypes.byref(plan), _ptr(workspace), _ptr(q_codes), _ptr(q_scales),
         float(sm_scale), _ptr(pool), num_pages, _ptr(block_table), max_pages, _ptr(out),
         _ptr(status), _stream(stream)), "kv_nvfp4_decode_attn")
+
+
+def kv_nvfp4_decode_attn_noalloc(layout, seq_lens, q_len, causal, chunk_tokens, q_codes, q_scales,
+                                 sm_scale, pool, num_pages, block_table, max_pages, out,
+                                 status=None, stream=None):
+    """Plan + decode attention with the library's fixed device buffer as the workspace, for
+    callers that cannot allocate device memory (KV_NVFP4_ENOSPACE when the plan does not fit)."""
+    import numpy as np
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    _check(lib().kv_nvfp4_decode_attn_noalloc(
+        ctypes.byref(layout), sl.ctypes.data, len(sl), q_len, int(causal), chunk_tokens,
+        _ptr(q_codes), _ptr(q_scales), float(sm_scale), _ptr(pool), num_pages, _ptr(block_table),
+        max_pages, _ptr(out), _ptr(status), _stream(stream)), "kv_nvfp4_decode_attn_noalloc")
 
 
 from .cache import PagedNVFP4Cache  # noqa: E402  (device buffers for one layer, allocated by torch)

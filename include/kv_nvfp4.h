@@ -221,6 +221,35 @@ kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout *layout,
                                      const int32_t *d_block_table, int32_t max_pages, float *out,
                                      int32_t *d_status, void *stream);
 
+/* ---- Decode attention without caller-provided device memory ----------------------------------
+ * No counterpart in the pages: an addition of this library for callers that cannot allocate
+ * device memory, such as an inference engine that reserves all of the GPU's memory for its own
+ * arena at start-up and passes a layer only its inputs and outputs, or a plug-in running under an
+ * allocator it does not control, where cudaMalloc fails or stalls every stream on the device.
+ *
+ * Same result as kv_nvfp4_plan followed by kv_nvfp4_decode_attn (same arguments, same kernels),
+ * but the workspace is a fixed buffer of KV_NVFP4_NOALLOC_SCRATCH_BYTES inside the library, held
+ * on every GPU that loads the library until the process exits; nothing is allocated on the device.
+ *   h_seq_lens, num_seqs, q_len, causal, chunk_tokens: as for kv_nvfp4_plan (HOST lengths)
+ *   the rest: as for kv_nvfp4_decode_attn
+ * Returns KV_NVFP4_ENOSPACE, before any GPU work, when the plan's workspace
+ * (kv_nvfp4_plan_workspace_bytes) exceeds the buffer; callers then use the workspace path.
+ * The first call on a device looks up the buffer's device address (with that device current)
+ * and keeps it; make that first call before any stream capture. Every call shares the buffer:
+ * each rewrites its work list before its kernels read it and nothing in it has to start at zero,
+ * but calls whose kernels overlap on the GPU (other streams, other host threads) corrupt each
+ * other's results and must be serialised by the caller. */
+#define KV_NVFP4_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+kv_nvfp4_status kv_nvfp4_decode_attn_noalloc(const kv_nvfp4_layout *layout,
+                                             const int32_t *h_seq_lens, int32_t num_seqs,
+                                             int32_t q_len, int32_t causal, int32_t chunk_tokens,
+                                             const uint8_t *q_codes, const uint8_t *q_scales,
+                                             float sm_scale, const uint8_t *pool,
+                                             int32_t num_pages, const int32_t *d_block_table,
+                                             int32_t max_pages, float *out, int32_t *d_status,
+                                             void *stream);
+
 #ifdef __cplusplus
 }
 #endif
