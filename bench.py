@@ -387,14 +387,15 @@ def run_cuda(args, world, rank, local):
         "append_gbs": append_bytes / append_s / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "decode_kernel (split-K NVFP4 attention, merge fused)",
+                     "kernel": "decode_kernel + merge_kernel (one kv_nvfp4_decode_attn call, "
+                               "CUDA events around the call)",
                      "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": attn_bytes},
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "includes": "pinned H2D of new Q/K/V + ids, append, plan upload, attention, D2H of output"},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 3 * args.steps,  # append, attention, split-K merge
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(w)
