@@ -51,6 +51,7 @@ namespace {
 constexpr int kMaxHkv = 4;
 constexpr int kStages = 5;
 constexpr int kStageBytes = kMaxHkv * 9216;        // one page block of up to 4 heads
+constexpr int kSBufs = 4;                          // score (S) buffers in TMEM
 constexpr int kQBytes = 2 * 1024;                  // two head pairs x 16 rows x 64 B
 constexpr int kRows = 8;                           // query rows per head per group
 constexpr int kPartHeadFloats = kRows * 128 + 2 * kRows;  // O[8][128], m[8], l[8]
@@ -66,17 +67,17 @@ constexpr int kMergeHeadBytes = 8 * 32 * 16 + 2 * kRows * 4;  // O: 8 float4 per
 
 // shared memory map
 constexpr int kOffStage = 0;
-constexpr int kOffSfStage = kOffStage + kStages * kStageBytes;  // [2][pair][k-half][32 rows x 16 B]
-constexpr int kOffPs = kOffSfStage + 2 * 2048;
+constexpr int kOffSfStage = kOffStage + kStages * kStageBytes;  // [kSBufs][pair][k-half][32 x 16 B]
+constexpr int kOffPs = kOffSfStage + kSBufs * 2048;
 constexpr int kOffQ = kOffPs + kAttnWarps * kPsBytes;
 constexpr int kOffMerge = kOffQ + kQBytes;
 constexpr int kOffBars = kOffMerge + kMaxHkv * kMergeHeadBytes;
 // barrier indices
 constexpr int kBarStageFull = 0;                       // [kStages]
 constexpr int kBarStageEmpty = kBarStageFull + kStages;  // [kStages]
-constexpr int kBarQkDone = kBarStageEmpty + kStages;   // [2]
-constexpr int kBarSFree = kBarQkDone + 2;              // [2]
-constexpr int kBarQReady = kBarSFree + 2;
+constexpr int kBarQkDone = kBarStageEmpty + kStages;   // [kSBufs]
+constexpr int kBarSFree = kBarQkDone + kSBufs;         // [kSBufs]
+constexpr int kBarQReady = kBarSFree + kSBufs;
 constexpr int kNumBars = kBarQReady + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 // misc: stage page ids, tmem base
@@ -87,10 +88,11 @@ static_assert(kStages <= 8, "stage page-id slots");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // TMEM columns
-constexpr uint32_t kTmemCols = 128;
-constexpr uint32_t kColS = 0;        // [2 buffers][2 pairs][16]
-constexpr uint32_t kColSfa = 64;     // [2 buffers][2 pairs][2 k-halves][4]
-constexpr uint32_t kColSfb = 96;     // [2 pairs][2 k-halves][4]
+constexpr uint32_t kColS = 0;                 // [kSBufs][2 pairs][16]
+constexpr uint32_t kColSfa = 32 * kSBufs;     // [kSBufs][2 pairs][2 k-halves][4]
+constexpr uint32_t kColSfb = 48 * kSBufs;     // [2 pairs][2 k-halves][4]
+constexpr uint32_t kTmemCols = kColSfb + 16 <= 128 ? 128 : 256;  // a power of two >= 32
+static_assert(kColSfb + 16 <= 256, "TMEM columns");
 
 // instruction descriptor (dense, no negation): A, B = E2M1 (format 1) K-major, scale type UE4M3,
 // N = 16, M = 128
@@ -212,11 +214,11 @@ __device__ void qk_warp(const DecodeParams& p, uint8_t* smem, uint32_t tbase, in
     const SegInfo sg = load_seg(p, s);
     wait_bar(bars + 8 * kBarQReady, sgi & 1, timed_out);  // Q tile and its scales for this group
     for (int j = 0; j < sg.hi - sg.lo; ++j, ++k) {
-      const uint32_t st = k % kStages, b = k & 1;
+      const uint32_t st = k % kStages, b = k % kSBufs;
       wait_bar(bars + 8 * (kBarStageFull + st), (k / kStages) & 1, timed_out);
-      // S buffer b free: the attention warps have read S of page k - 2, so that page's MMAs and
-      // scale copies are complete and staging tile b may be rewritten
-      if (k >= 2) wait_bar(bars + 8 * (kBarSFree + b), ((k >> 1) - 1) & 1, timed_out);
+      // S buffer b free: the attention warps have read S of page k - kSBufs, so that page's MMAs
+      // and scale copies are complete and staging tile b may be rewritten
+      if (k >= kSBufs) wait_bar(bars + 8 * (kBarSFree + b), ((k / kSBufs) - 1) & 1, timed_out);
       const uint32_t stage = sbase + kOffStage + st * kStageBytes;
       const uint32_t sfs = sbase + kOffSfStage + b * 2048;
       const int kv_lim = stage_pid[st] >= 0 ? sg.len - (sg.lo + j) * 64 : 0;  // keys < kv_lim real
@@ -299,8 +301,8 @@ struct RowVis {
 
 // Wait for page kk's scores and start loading this warp's slice (one key per lane, 8 rows).
 __device__ __forceinline__ void s_issue(AttnCtx& c, uint32_t kk, uint32_t (&sr)[8]) {
-  const uint32_t b = kk & 1;
-  wait_bar(c.bars + 8 * (kBarQkDone + b), (kk >> 1) & 1, c.timed_out);
+  const uint32_t b = kk % kSBufs;
+  wait_bar(c.bars + 8 * (kBarQkDone + b), (kk / kSBufs) & 1, c.timed_out);
   tc_fence_after();
   tmem_ld8(c.tbase + c.lane_base + kColS + b * 32 + c.pr * 16 + c.half * 8, sr);
 }
@@ -317,7 +319,7 @@ __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, int page, int
   tmem_wait_ld_regs(sr);
   tc_fence_before();
   __syncwarp();
-  if (c.lane == 0) mbar_arrive(c.bars + 8 * (kBarSFree + (kk & 1)));
+  if (c.lane == 0) mbar_arrive(c.bars + 8 * (kBarSFree + kk % kSBufs));
   const uint32_t st = kk % kStages;
   // the Q.K^T warp saw this stage land; waiting here as well makes the V bytes and the page id
   // visible to this warp (the wait returns at once)
@@ -336,22 +338,25 @@ __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, int page, int
         if (kp <= __shfl_sync(0xffffffffu, rv.mylim, i)) vmask |= 1u << i;
     }
   }
-  int pmi[kRows];
+  float pm[kRows];
 #pragma unroll
   for (int i = 0; i < kRows; ++i)
-    pmi[i] = __reduce_max_sync(0xffffffffu,
-                               f2ord(((vmask >> i) & 1u) ? __uint_as_float(sr[i]) : -INFINITY));
-  float alpha[kRows];
+    pm[i] = warp_max_f32(((vmask >> i) & 1u) ? __uint_as_float(sr[i]) : -INFINITY);
   bool grow = false;  // warp-uniform: every lane holds the same maxima
 #pragma unroll
-  for (int i = 0; i < kRows; ++i) {
-    const float mn = fmaxf(m[i], ord2f(pmi[i]));
-    alpha[i] = (mn == m[i]) ? 1.f : fast_exp2((m[i] - mn) * c2);  // 0 when m was -inf
-    grow |= mn != m[i];
-    lp[i] *= alpha[i];
-    m[i] = mn;
+  for (int i = 0; i < kRows; ++i) grow |= pm[i] > m[i];
+  alpha_g = 1.f;
+  if (grow) {  // rare once the running maxima have settled
+    float alpha[kRows];
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+      const float mn = fmaxf(m[i], pm[i]);
+      alpha[i] = (mn == m[i]) ? 1.f : fast_exp2((m[i] - mn) * c2);  // 0 when m was -inf
+      lp[i] *= alpha[i];
+      m[i] = mn;
+    }
+    alpha_g = pick8(alpha, g);
   }
-  alpha_g = pick8(alpha, g);
   uint32_t hi[4], lo[4];
 #pragma unroll
   for (int i = 0; i < kRows; i += 2) {
@@ -368,41 +373,55 @@ __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, int page, int
   return grow;
 }
 
-// One 16-key step of O += P V for this warp: P from the P tile through transposing ldmatrix (lm:
-// this lane's row address), V codes of the lane's four keys (vk0, vk1, vk0 + 2, vk1 + 2 within the
-// step) and dims 16 g .. 16 g + 15, decoded into B fragments; a key at or past kv_lim gets scale 0
-// (its code bytes are stale).
-__device__ __forceinline__ void pv_step(int kb, uint32_t lm, uint32_t vc, uint32_t vs, int kv_lim,
-                                        int vk0, int vk1, float (&acc)[16][4]) {
-  uint32_t a0, a1, a2, a3;
-  ldsm_x4_trans(lm, a0, a1, a2, a3);
-  const int vk2 = vk0 + 2, vk3 = vk1 + 2;
-  const uint2 w0 = lds64(vc + (kb + vk0) * 64), w1 = lds64(vc + (kb + vk1) * 64);
-  const uint2 w2 = lds64(vc + (kb + vk2) * 64), w3 = lds64(vc + (kb + vk3) * 64);
-  const uint32_t s0 = kb + vk0 < kv_lim ? lds8(vs + (kb + vk0) * 8) : 0u;
-  const uint32_t s1 = kb + vk1 < kv_lim ? lds8(vs + (kb + vk1) * 8) : 0u;
-  const uint32_t s2 = kb + vk2 < kv_lim ? lds8(vs + (kb + vk2) * 8) : 0u;
-  const uint32_t s3 = kb + vk3 < kv_lim ? lds8(vs + (kb + vk3) * 8) : 0u;
-  const uint32_t sc01 = cvt_e4m3x2_f16(s0 | (s1 << 8));
-  const uint32_t sc23 = cvt_e4m3x2_f16(s2 | (s3 << 8));
+// O += P V over the warp's 32 keys of a page, two 16-key steps. P comes from the P tile through
+// transposing ldmatrix (lm0, lm1: this lane's row addresses for the two steps); V codes of the
+// lane's four keys per step (vk0, vk1, vk0 + 2, vk1 + 2) and dims 16 g .. 16 g + 15 are decoded
+// into B fragments: one byte per dim holding the nibbles of two keys (first key low), converted
+// by cvt.e2m1x2 and multiplied by the two keys' E4M3 scales. A key at or past kv_lim gets scale 0
+// (its code bytes are stale). All shared loads of the page are issued before the arithmetic.
+__device__ __forceinline__ void pv_page(const uint8_t* sm, uint32_t lm0, uint32_t lm1, uint32_t vco,
+                                        uint32_t vso, int key0, int kv_lim, int vk0, int vk1,
+                                        float (&acc)[16][4]) {
+  uint32_t a[2][4];
+  ldsm_x4_trans(lm0, a[0][0], a[0][1], a[0][2], a[0][3]);
+  ldsm_x4_trans(lm1, a[1][0], a[1][1], a[1][2], a[1][3]);
+  uint2 wv[2][4];
+  uint32_t sc[2][2];
 #pragma unroll
-  for (int w = 0; w < 2; ++w) {  // dims 16 g + 8 w .. 16 g + 8 w + 7
-    const uint32_t x0 = w ? w0.y : w0.x, x1 = w ? w1.y : w1.x;
-    const uint32_t x2 = w ? w2.y : w2.x, x3 = w ? w3.y : w3.x;
-    // one byte per dim holding the nibbles of two keys: (first key low, second key high)
-    const uint32_t ze01 = (x0 & 0x0F0F0F0Fu) | ((x1 << 4) & 0xF0F0F0F0u);
-    const uint32_t zo01 = ((x0 >> 4) & 0x0F0F0F0Fu) | (x1 & 0xF0F0F0F0u);
-    const uint32_t ze23 = (x2 & 0x0F0F0F0Fu) | ((x3 << 4) & 0xF0F0F0F0u);
-    const uint32_t zo23 = ((x2 >> 4) & 0x0F0F0F0Fu) | (x3 & 0xF0F0F0F0u);
-    uint32_t e0[4], o0[4], e2[4], o2[4];
-    cvt_e2m1x8_f16(ze01, e0[0], e0[1], e0[2], e0[3]);
-    cvt_e2m1x8_f16(zo01, o0[0], o0[1], o0[2], o0[3]);
-    cvt_e2m1x8_f16(ze23, e2[0], e2[1], e2[2], e2[3]);
-    cvt_e2m1x8_f16(zo23, o2[0], o2[1], o2[2], o2[3]);
+  for (int ks = 0; ks < 2; ++ks) {
+    const int kb = key0 + 16 * ks;
+    const int kk[4] = {kb + vk0, kb + vk1, kb + vk0 + 2, kb + vk1 + 2};
+    uint32_t s[4];
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      mma16816(acc[8 * w + 2 * jj], a0, a1, a2, a3, hmul2(e0[jj], sc01), hmul2(e2[jj], sc23));
-      mma16816(acc[8 * w + 2 * jj + 1], a0, a1, a2, a3, hmul2(o0[jj], sc01), hmul2(o2[jj], sc23));
+    for (int e = 0; e < 4; ++e) {
+      wv[ks][e] = *reinterpret_cast<const uint2*>(sm + vco + kk[e] * 64);
+      s[e] = kk[e] < kv_lim ? (uint32_t)sm[vso + kk[e] * 8] : 0u;
+    }
+    sc[ks][0] = cvt_e4m3x2_f16(s[0] | (s[1] << 8));
+    sc[ks][1] = cvt_e4m3x2_f16(s[2] | (s[3] << 8));
+  }
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const uint32_t x0 = w ? wv[ks][0].y : wv[ks][0].x, x1 = w ? wv[ks][1].y : wv[ks][1].x;
+      const uint32_t x2 = w ? wv[ks][2].y : wv[ks][2].x, x3 = w ? wv[ks][3].y : wv[ks][3].x;
+      const uint32_t ze01 = (x0 & 0x0F0F0F0Fu) | ((x1 << 4) & 0xF0F0F0F0u);
+      const uint32_t zo01 = ((x0 >> 4) & 0x0F0F0F0Fu) | (x1 & 0xF0F0F0F0u);
+      const uint32_t ze23 = (x2 & 0x0F0F0F0Fu) | ((x3 << 4) & 0xF0F0F0F0u);
+      const uint32_t zo23 = ((x2 >> 4) & 0x0F0F0F0Fu) | (x3 & 0xF0F0F0F0u);
+      uint32_t e0[4], o0[4], e2[4], o2[4];
+      cvt_e2m1x8_f16(ze01, e0[0], e0[1], e0[2], e0[3]);
+      cvt_e2m1x8_f16(zo01, o0[0], o0[1], o0[2], o0[3]);
+      cvt_e2m1x8_f16(ze23, e2[0], e2[1], e2[2], e2[3]);
+      cvt_e2m1x8_f16(zo23, o2[0], o2[1], o2[2], o2[3]);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        mma16816(acc[8 * w + 2 * jj], a[ks][0], a[ks][1], a[ks][2], a[ks][3],
+                 hmul2(e0[jj], sc[ks][0]), hmul2(e2[jj], sc[ks][1]));
+        mma16816(acc[8 * w + 2 * jj + 1], a[ks][0], a[ks][1], a[ks][2], a[ks][3],
+                 hmul2(o0[jj], sc[ks][0]), hmul2(o2[jj], sc[ks][1]));
+      }
     }
   }
 }
@@ -521,8 +540,7 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
         const uint32_t stage = c.sbase + kOffStage + st * kStageBytes;
         const uint32_t vc = stage + p.Hkv * 4608 + c.head * 4096 + 8 * g;  // codes of dims 16 g ..
         const uint32_t vs = stage + p.Hkv * 8704 + c.head * 512 + g;       // scale of block g
-        pv_step(c.key0, lm_addr0, vc, vs, kv_lim, vk0, vk1, acc);
-        pv_step(c.key0 + 16, lm_addr1, vc, vs, kv_lim, vk0, vk1, acc);
+        pv_page(smem, lm_addr0, lm_addr1, vc - c.sbase, vs - c.sbase, c.key0, kv_lim, vk0, vk1, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bars + 8 * (kBarStageEmpty + st));
@@ -619,7 +637,7 @@ __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodePa
       mbar_init(bars + 8 * (kBarStageFull + s), 1);
       mbar_init(bars + 8 * (kBarStageEmpty + s), 1 + kAttnWarps);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kSBufs; ++b) {
       mbar_init(bars + 8 * (kBarQkDone + b), 1);
       mbar_init(bars + 8 * (kBarSFree + b), kAttnWarps);
     }

@@ -366,6 +366,13 @@ __device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint3
                : "memory");
 }
 
+// Maximum of a float over the 32 lanes of the warp (finite values and -inf).
+__device__ __forceinline__ float warp_max_f32(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // Order-preserving map of finite floats (and -inf) to signed ints, for integer max reductions.
 __device__ __forceinline__ int f2ord(float x) {
   const int b = __float_as_int(x);
