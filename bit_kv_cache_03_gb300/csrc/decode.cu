@@ -312,6 +312,7 @@ __device__ __forceinline__ void s_issue(AttnCtx& c, uint32_t kk, uint32_t (&sr)[
 // update, P = exp2((s - m) c2) <= 1 as f16 hi + lo. Returns whether a max grew (then alpha_g is
 // the factor for row g of the accumulator). kv_lim: keys of the page below it are real (0 when
 // the page was skipped).
+template <int NR>
 __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, int page, int len,
                                           const RowVis& rv, uint32_t (&sr)[8], float (&m)[kRows],
                                           float (&lp)[kRows], uint32_t pt, int g, float c2,
@@ -334,22 +335,24 @@ __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, int page, int
     } else {
       const int kp = page * 64 + c.key0 + c.lane;
 #pragma unroll
-      for (int i = 0; i < kRows; ++i)
+      for (int i = 0; i < NR; ++i)
         if (kp <= __shfl_sync(0xffffffffu, rv.mylim, i)) vmask |= 1u << i;
     }
   }
-  float pm[kRows];
+  float pm[NR];
 #pragma unroll
-  for (int i = 0; i < kRows; ++i)
+  for (int i = 0; i < NR; ++i)
     pm[i] = warp_max_f32(((vmask >> i) & 1u) ? __uint_as_float(sr[i]) : -INFINITY);
   bool grow = false;  // warp-uniform: every lane holds the same maxima
 #pragma unroll
-  for (int i = 0; i < kRows; ++i) grow |= pm[i] > m[i];
+  for (int i = 0; i < NR; ++i) grow |= pm[i] > m[i];
   alpha_g = 1.f;
   if (grow) {  // rare once the running maxima have settled
     float alpha[kRows];
 #pragma unroll
-    for (int i = 0; i < kRows; ++i) {
+    for (int i = NR; i < kRows; ++i) alpha[i] = 1.f;
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
       const float mn = fmaxf(m[i], pm[i]);
       alpha[i] = (mn == m[i]) ? 1.f : fast_exp2((m[i] - mn) * c2);  // 0 when m was -inf
       lp[i] *= alpha[i];
@@ -360,9 +363,10 @@ __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, int page, int
   uint32_t hi[4], lo[4];
 #pragma unroll
   for (int i = 0; i < kRows; i += 2) {
-    const float p0 = ((vmask >> i) & 1u) ? fast_exp2((__uint_as_float(sr[i]) - m[i]) * c2) : 0.f;
-    const float p1 =
-        ((vmask >> (i + 1)) & 1u) ? fast_exp2((__uint_as_float(sr[i + 1]) - m[i + 1]) * c2) : 0.f;
+    const float p0 = (i < NR && ((vmask >> i) & 1u))
+                         ? fast_exp2((__uint_as_float(sr[i]) - m[i]) * c2) : 0.f;
+    const float p1 = (i + 1 < NR && ((vmask >> (i + 1)) & 1u))
+                         ? fast_exp2((__uint_as_float(sr[i + 1]) - m[i + 1]) * c2) : 0.f;
     lp[i] += p0;
     lp[i + 1] += p1;
     hi[i / 2] = pack_f16x2(p0, p1);
@@ -426,6 +430,7 @@ __device__ __forceinline__ void pv_page(const uint8_t* sm, uint32_t lm0, uint32_
   }
 }
 
+template <int NR>
 __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t tbase, int warp,
                                 int lane) {
   AttnCtx c;
@@ -528,7 +533,7 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
       float alpha_g = 1.f;
       int kv_lim = 0;
       s_issue(c, k, sr);
-      const bool grow = s_softmax(c, k, sg.lo + j, sg.len, rv, sr, m, lp, ps, g, c2, alpha_g, kv_lim);
+      const bool grow = s_softmax<NR>(c, k, sg.lo + j, sg.len, rv, sr, m, lp, ps, g, c2, alpha_g, kv_lim);
       __syncwarp();
       if (grow) {
 #pragma unroll
@@ -628,10 +633,15 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
   if (c.timed_out && lane == 0) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
 
+// NR: query rows computed per head (6 when no tile has more real rows, else all 8)
+template <int NR>
 __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t bars = smem_u32(smem + kOffBars);
+  // the split-K merge launched after this kernel may be scheduled now; it waits for this grid's
+  // completion before it reads anything this kernel writes
+  asm volatile("griddepcontrol.launch_dependents;");
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bars + 8 * (kBarStageFull + s), 1);
@@ -655,7 +665,7 @@ __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodePa
   } else if (warp == kWarpMma) {
     qk_warp(p, smem, tbase, lane);
   } else {
-    attention_warps(p, smem, tbase, warp, lane);
+    attention_warps<NR>(p, smem, tbase, warp, lane);
   }
 
   tc_fence_before();
@@ -682,23 +692,20 @@ struct MergeParams {
 __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
   __shared__ float s_m[8], s_l[8];
   __shared__ float4 s_o[8][32];
-  const int gi = p.split[blockIdx.x];
+  const int gi = p.split[blockIdx.x];  // plan tables: written before the attention launch
   const int h = blockIdx.y / kRows, i = blockIdx.y % kRows;
   const int4 g0 = p.groups[2 * gi], g1 = p.groups[2 * gi + 1];
   const int r = g0.z * kRows + i;
+  // launched as a programmatic dependent of the attention kernel: its partials are visible only
+  // after this wait (which returns when that grid has completed and flushed)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (r >= p.G * p.q_len) return;  // padding row of the last tile (uniform over the CTA)
   const int n_seg = g1.x;
   const int slice = threadIdx.x >> 5, d4 = threadIdx.x & 31;
   const int64_t stride = (int64_t)p.Hkv * kPartHeadFloats;
   const float* base = p.partials + (int64_t)g1.y * stride + h * kPartHeadFloats;
-  float mx = -INFINITY;
-  for (int q = slice; q < n_seg; q += 8) mx = fmaxf(mx, __ldcg(base + q * stride + kRows * 128 + i));
-  if (d4 == 0) s_m[slice] = mx;
-  __syncthreads();
-  float M = s_m[0];
-#pragma unroll
-  for (int j = 1; j < 8; ++j) M = fmaxf(M, s_m[j]);
-  float L = 0.f;
+  // one pass per slice with a running max; slices combined below
+  float M = -INFINITY, L = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int q = slice; q < n_seg; q += 8) {
@@ -706,21 +713,30 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
     const float mq = __ldcg(pq + kRows * 128 + i);
     const float lq = __ldcg(pq + kRows * 128 + kRows + i);
     const float4 ov = __ldcg(reinterpret_cast<const float4*>(pq + i * 128) + d4);
-    const float f = (mq == -INFINITY) ? 0.f : fast_exp2((mq - M) * p.c2);
-    L += f * lq;
-    O.x += f * ov.x; O.y += f * ov.y; O.z += f * ov.z; O.w += f * ov.w;
+    if (mq == -INFINITY) continue;  // a segment with no visible key
+    const float mn = fmaxf(M, mq);
+    const float a = fast_exp2((M - mn) * p.c2), f = fast_exp2((mq - mn) * p.c2);  // a = 0 at start
+    M = mn;
+    L = L * a + f * lq;
+    O.x = O.x * a + f * ov.x; O.y = O.y * a + f * ov.y;
+    O.z = O.z * a + f * ov.z; O.w = O.w * a + f * ov.w;
   }
   s_o[slice][d4] = O;
-  if (d4 == 0) s_l[slice] = L;
+  if (d4 == 0) { s_m[slice] = M; s_l[slice] = L; }
   __syncthreads();
   if (slice == 0) {
+    float Mt = s_m[0];
+#pragma unroll
+    for (int j = 1; j < 8; ++j) Mt = fmaxf(Mt, s_m[j]);
     float Lt = 0.f;
     float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      Lt += s_l[j];
+      if (s_m[j] == -INFINITY) continue;
+      const float f = fast_exp2((s_m[j] - Mt) * p.c2);
       const float4 v = s_o[j][d4];
-      Ot.x += v.x; Ot.y += v.y; Ot.z += v.z; Ot.w += v.w;
+      Lt += f * s_l[j];
+      Ot.x += f * v.x; Ot.y += f * v.y; Ot.z += f * v.z; Ot.w += f * v.w;
     }
     if (Lt > 0.f) {
       const int tok = r / p.G, qh = h * p.G + r % p.G;
@@ -742,10 +758,14 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
                           float* out, int32_t* status,
                           int32_t Hq, int32_t Hkv, int32_t q_len, int32_t causal, int32_t grid,
                           float sm_scale, cudaStream_t stream) {
-  static bool attr_done = false;  // the attribute belongs to the function, set once per process
+  // the attribute belongs to each instantiation, set once per process
+  static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -760,14 +780,29 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
   p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.q_len = q_len; p.causal = causal;
   p.c2 = sm_scale * 1.4426950408889634f;
   if (grid <= 0) return cudaSuccess;
-  decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+  // every tile has at most G * q_len real rows: with six or fewer, rows 6 and 7 are never computed
+  if (p.G * q_len <= 6)
+    decode_kernel<6><<<grid, kThreads, kSmemBytes, stream>>>(p);
+  else
+    decode_kernel<8><<<grid, kThreads, kSmemBytes, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || num_split <= 0) return e;
   MergeParams mp;
   mp.groups = p.groups; mp.split = split_groups; mp.partials = partials; mp.out = out;
   mp.Hq = Hq; mp.Hkv = Hkv; mp.G = p.G; mp.q_len = q_len; mp.c2 = p.c2;
-  merge_kernel<<<dim3((unsigned)num_split, (unsigned)(Hkv * kRows)), 256, 0, stream>>>(mp);
-  return cudaGetLastError();
+  // programmatic dependent launch: the merge grid is set up while the attention kernel runs and
+  // waits (griddepcontrol.wait) for it to complete before reading the partials
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_split, (unsigned)(Hkv * kRows));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge_kernel, mp);
 }
 
 }  // namespace kvnvfp4
