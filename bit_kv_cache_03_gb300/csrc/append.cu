@@ -190,6 +190,12 @@ __device__ __forceinline__ void quantize_store_row(float (&x)[4], const RowTarge
 }
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const AppendParams p) {
+  // Launched as a programmatic dependent of the previous kernel on the stream (e.g. the attention
+  // of the previous step, which reads the pool): wait for it before touching memory, then let the
+  // next kernel (the attention of this step) start its launch while this one runs; that kernel
+  // waits for this one in turn before reading the pool.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int64_t rows = p.T * (int64_t)(p.Hq + 2 * p.Hkv);
@@ -234,8 +240,17 @@ cudaError_t launch_append(const uint16_t* q, const uint16_t* k, const uint16_t* 
   const int64_t blocks = (rows + per_block - 1) / per_block;
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  append_kernel<<<(unsigned)blocks, kWarpsPerBlock * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kWarpsPerBlock * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, append_kernel, p);
 }
 
 }  // namespace kvnvfp4

@@ -658,6 +658,10 @@ __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodePa
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // launched as a programmatic dependent of the previous kernel on the stream (the append that
+  // wrote this step's pool rows and Q, or the previous call's merge, which reads the partials this
+  // kernel rewrites): everything above overlapped its tail; nothing below runs before it completes
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
 
   if (warp == kWarpProducer) {
@@ -692,6 +696,7 @@ struct MergeParams {
 __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
   __shared__ float s_m[8], s_l[8];
   __shared__ float4 s_o[8][32];
+  asm volatile("griddepcontrol.launch_dependents;");  // the next kernel may begin its launch
   const int gi = p.split[blockIdx.x];  // plan tables: written before the attention launch
   const int h = blockIdx.y / kRows, i = blockIdx.y % kRows;
   const int4 g0 = p.groups[2 * gi], g1 = p.groups[2 * gi + 1];
@@ -780,11 +785,24 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
   p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.q_len = q_len; p.causal = causal;
   p.c2 = sm_scale * 1.4426950408889634f;
   if (grid <= 0) return cudaSuccess;
-  // every tile has at most G * q_len real rows: with six or fewer, rows 6 and 7 are never computed
-  if (p.G * q_len <= 6)
-    decode_kernel<6><<<grid, kThreads, kSmemBytes, stream>>>(p);
-  else
-    decode_kernel<8><<<grid, kThreads, kSmemBytes, stream>>>(p);
+  // programmatic dependent launch: the kernel is set up while the previous kernel on the stream
+  // finishes, and waits for it (griddepcontrol.wait) before touching memory
+  {
+    cudaLaunchConfig_t dc = {};
+    dc.gridDim = dim3((unsigned)grid);
+    dc.blockDim = dim3(kThreads);
+    dc.dynamicSmemBytes = kSmemBytes;
+    dc.stream = stream;
+    cudaLaunchAttribute da[1];
+    da[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    da[0].val.programmaticStreamSerializationAllowed = 1;
+    dc.attrs = da;
+    dc.numAttrs = 1;
+    // every tile has at most G * q_len real rows: with six or fewer, rows 6 and 7 are never computed
+    const cudaError_t le = (p.G * q_len <= 6) ? cudaLaunchKernelEx(&dc, decode_kernel<6>, p)
+                                              : cudaLaunchKernelEx(&dc, decode_kernel<8>, p);
+    if (le != cudaSuccess) return le;
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || num_split <= 0) return e;
   MergeParams mp;
