@@ -5,13 +5,15 @@ Workload (one attention layer): 4 sequences x 131,072 cached tokens + 1 new toke
 RoPE on 32 dims (theta 1e7), bf16 inputs ~ N(0,1) with K/Q outlier channels x12.
 
 A step is one pass of the whole hot path: the fused quantize-append of the step's new tokens
-(Q, K, V) and the split-K decode attention over the whole cache (two kernel launches). The step
+(Q, K, V) and the split-K decode attention over the whole cache (three kernel launches: append,
+attention, merge). The step
 re-appends the same positions, so every step sees the same cache. The KV read per step (302 MB)
 is larger than L2 (129 MB), so no L2 flush is needed between steps.
 
 `value` is device time with inputs resident in HBM; `e2e` adds, every step, the host->device
 copy of the new tokens from pinned memory, the split-K plan upload, and the device->host copy of
-the attention output. `roofline` covers the decode-attention kernel (events around each launch).
+the attention output. `roofline` covers one decode-attention call (attention + merge kernels),
+timed with CUDA events around back-to-back calls.
 `--impl reference` times the CPU oracle on a bounded sample of the same workload.
 
 Multi-GPU: the path has no exchange step, so N GPUs run N independent replicas (weak scaling);
@@ -38,6 +40,23 @@ METRIC = "NVFP4 decode attn KV-tokens/s & HBM GB/s (% of peak); append tokens/s"
 UNIT = "KV-tokens/s"
 CHUNK = 64  # split-K granularity: one page, so the plan balances CTAs to the page
 WORKLOAD = "steady_decode: 4 seqs x 131072 cached + 1 new token, Hq 24 / Hkv 4, d 128, page 64, 40k-page pool"
+
+
+def max_over_ranks(values, device=None):
+    """Each value's maximum over all ranks of the initialised process group (as is at N = 1)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def replica_throughput(world, units_per_rank, steps, elapsed_max):
+    """Whole-job throughput of N independent replicas: the units all ranks processed divided by
+    the slowest rank's time."""
+    return world * units_per_rank * steps / elapsed_max
 
 
 def _dist():
@@ -356,17 +375,13 @@ def run_cuda(args, world, rank, local):
     torch.cuda.synchronize(dev)
     e2e_elapsed = time.perf_counter() - t0
 
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([elapsed, e2e_elapsed], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed, e2e_elapsed = float(tt[0]), float(tt[1])
+    elapsed, e2e_elapsed = max_over_ranks([elapsed, e2e_elapsed], dev)
     if rank != 0:
         return
 
     kv_tokens = int(w.seq_lens.sum())
-    value = world * kv_tokens * args.steps / elapsed
-    e2e_value = world * kv_tokens * e2e_steps / e2e_elapsed
+    value = replica_throughput(world, kv_tokens, args.steps, elapsed)
+    e2e_value = replica_throughput(world, kv_tokens, e2e_steps, e2e_elapsed)
     n_pages = int(sum((int(l) + 63) // 64 for l in w.seq_lens))
     T = w.num_seqs * w.q_len
     attn_bytes = (kv_tokens * w.kv_heads * 144 + T * w.q_heads * 72 + n_pages * 4 +
