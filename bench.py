@@ -4,16 +4,18 @@ Workload (one attention layer): 4 sequences x 131,072 cached tokens + 1 new toke
 4 KV heads, head_dim 128, 64-token pages placed by a seeded permutation of a 40,000-page pool,
 RoPE on 32 dims (theta 1e7), bf16 inputs ~ N(0,1) with K/Q outlier channels x12.
 
-A step is one pass of the whole hot path: the fused quantize-append of the step's new tokens
-(Q, K, V) and the split-K decode attention over the whole cache (three kernel launches: append,
-attention, merge). The step
-re-appends the same positions, so every step sees the same cache. The KV read per step (302 MB)
+A step is one pass of the whole hot path: one kv_nvfp4_decode_step call, which quantises the
+step's new tokens (Q, K, V: RoPE, Hadamard rotation, NVFP4), stores their K/V rows into the pool
+and runs the split-K decode attention over the whole cache (two kernel launches: the attention
+kernel with the append inside it, and the split-K merge). The step re-appends the same positions,
+so every step sees the same cache. The same step as two calls (kv_nvfp4_append, then
+kv_nvfp4_decode_attn: three launches) and the attention call alone are timed beside it. The KV read per step (302 MB)
 is larger than L2 (129 MB), so no L2 flush is needed between steps.
 
 `value` is device time with inputs resident in HBM; `e2e` adds, every step, the host->device
 copy of the new tokens from pinned memory, the split-K plan upload, and the device->host copy of
-the attention output. `roofline` covers one decode-attention call (attention + merge kernels),
-timed with CUDA events around back-to-back calls.
+the attention output. `roofline` covers the step call (attention kernel + merge kernel), timed
+with CUDA events around the back-to-back steps.
 `--impl reference` times the CPU oracle on a bounded sample of the same workload.
 
 Multi-GPU: the path has no exchange step, so N GPUs run N independent replicas (weak scaling);
@@ -129,8 +131,8 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def decode_traffic_profile(rows_bytes):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
+def decode_traffic_profile():
+    """DRAM bytes per step launch from the committed ncu summary, if it was taken on the
     current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", "decode_attn_steady_decode.json")
     if not os.path.exists(p):
@@ -272,8 +274,7 @@ def run_cuda(args, world, rank, local):
     if args.profile:
         # short run for the profiler: warm-up and the timed steps only
         for _ in range(args.warmup + args.steps):
-            g.cache.append(g.k, g.v, g.sid, g.pos, q=g.q, q_codes=g.q_codes, q_scales=g.q_scales)
-            g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
+            g.cache.decode_step(g.q, g.k, g.v, g.out, g.q_codes, g.q_scales, sm_scale=w.sm_scale)
         torch.cuda.synchronize(dev)
         assert g.status() == 0
         print(json.dumps({"profile_run": True, "seqs": w.num_seqs, "steps": args.steps}))
@@ -304,64 +305,67 @@ def run_cuda(args, world, rank, local):
     del spare, qb, kb, vb
 
     # ---- timed decode steps (device-resident inputs) ----
-    for _ in range(args.warmup):
+    def fused_step():
+        g.cache.decode_step(g.q, g.k, g.v, g.out, g.q_codes, g.q_scales, sm_scale=w.sm_scale)
+
+    def two_call_step():
         g.cache.append(g.k, g.v, g.sid, g.pos, q=g.q, q_codes=g.q_codes, q_scales=g.q_scales)
         g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
+
+    def attn_only():
+        g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
+
+    def back_to_back(fn, n):
+        # no event between the kernels of a step, so each kernel's launch overlaps the previous
+        # one's tail as it would in a serving loop
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / 1e3
+
+    for fn in (two_call_step, attn_only, fused_step):
+        for _ in range(args.warmup):
+            fn()
     torch.cuda.synchronize(dev)
-    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a_begin, a_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    attn_steps = max(10, min(args.steps, 5000))
+    side_steps = max(10, min(args.steps, 5000))
     clocks = ClockSampler(local)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)  # let the sampler start before the timed region
-    # whole steps, back to back (no event between the kernels of a step, so each kernel's launch
-    # overlaps the previous one's tail as it would in a serving loop)
-    t_begin.record(stream)
-    for i in range(args.steps):
-        g.cache.append(g.k, g.v, g.sid, g.pos, q=g.q, q_codes=g.q_codes, q_scales=g.q_scales)
-        g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
-    t_end.record(stream)
-    torch.cuda.synchronize(dev)
-    # the attention call alone (attention + split-K merge kernels), back to back, for the roofline
-    a_begin.record(stream)
-    for i in range(attn_steps):
-        g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
-    a_end.record(stream)
+    elapsed = back_to_back(fused_step, args.steps)
+    two_call_avg = back_to_back(two_call_step, side_steps) / side_steps
+    attn_avg = back_to_back(attn_only, side_steps) / side_steps
+    fused_step()  # leave the step's output and quantised Q in place
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
-    elapsed = t_begin.elapsed_time(t_end) / 1e3
-    attn_avg = a_begin.elapsed_time(a_end) / 1e3 / attn_steps
+    step_avg = elapsed / args.steps
     assert g.status() == 0, f"device status {g.status():#x}"
 
     # ---- end to end through the public API, host buffers ----
     q_h = torch.from_numpy(np.ascontiguousarray(w.new_tokens()[0]).view(np.int16)).pin_memory()
     k_h = torch.from_numpy(np.ascontiguousarray(w.new_tokens()[1]).view(np.int16)).pin_memory()
     v_h = torch.from_numpy(np.ascontiguousarray(w.new_tokens()[2]).view(np.int16)).pin_memory()
-    sid_h = torch.from_numpy(w.new_tokens()[3]).pin_memory()
-    pos_h = torch.from_numpy(w.new_tokens()[4]).pin_memory()
     out_h = torch.empty(g.out.numel(), dtype=torch.float32).pin_memory()
     q_d = torch.empty_like(q_h, device=dev)
     k_d = torch.empty_like(k_h, device=dev)
     v_d = torch.empty_like(v_h, device=dev)
-    sid_d = torch.empty_like(sid_h, device=dev)
-    pos_d = torch.empty_like(pos_h, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, sid_h, pos_h))
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
     d2h = out_h.numel() * 4
     e2e_steps = max(10, min(args.steps, 2000))
 
     def e2e_step():
         q_d.copy_(q_h, non_blocking=True); k_d.copy_(k_h, non_blocking=True)
-        v_d.copy_(v_h, non_blocking=True); sid_d.copy_(sid_h, non_blocking=True)
-        pos_d.copy_(pos_h, non_blocking=True)
-        g.cache.append(k_d.view(torch.bfloat16), v_d.view(torch.bfloat16), sid_d, pos_d,
-                       q=q_d.view(torch.bfloat16), q_codes=g.q_codes, q_scales=g.q_scales)
+        v_d.copy_(v_h, non_blocking=True)
         g.cache.plan(w.seq_lens, w.q_len, w.causal, CHUNK)
-        g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
+        g.cache.decode_step(q_d.view(torch.bfloat16), k_d.view(torch.bfloat16),
+                            v_d.view(torch.bfloat16), g.out, sm_scale=w.sm_scale)
         out_h.copy_(g.out, non_blocking=True)
 
     for _ in range(5):
@@ -384,11 +388,16 @@ def run_cuda(args, world, rank, local):
     e2e_value = replica_throughput(world, kv_tokens, e2e_steps, e2e_elapsed)
     n_pages = int(sum((int(l) + 63) // 64 for l in w.seq_lens))
     T = w.num_seqs * w.q_len
+    # one attention call: every cached K/V row, the quantised Q, the block table, the fp32 output
     attn_bytes = (kv_tokens * w.kv_heads * 144 + T * w.q_heads * 72 + n_pages * 4 +
                   T * w.q_heads * 128 * 4)
+    # one step call: the same, with the new rows read in bf16 and their K/V (and Q) codes written
+    step_bytes = (kv_tokens * w.kv_heads * 144 + T * (w.q_heads + 2 * w.kv_heads) * 256 +
+                  T * (w.q_heads + 2 * w.kv_heads) * 72 + n_pages * 4 + T * w.q_heads * 128 * 4)
     peak, peak_kind = measured_peaks()
-    achieved = attn_bytes / attn_avg / 1e9
-    traffic = decode_traffic_profile(attn_bytes)
+    achieved = step_bytes / step_avg / 1e9
+    attn_gbs = attn_bytes / attn_avg / 1e9
+    traffic = decode_traffic_profile()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
@@ -398,24 +407,26 @@ def run_cuda(args, world, rank, local):
                    "kv_bytes_per_step": kv_tokens * w.kv_heads * 144,
                    "l2": "inputs larger than L2 (302 MB of KV per step vs 129 MB L2), no flush",
                    "chunk_tokens": CHUNK, "parallelism": "replicas" if world > 1 else "1 GPU"},
-        "hbm_gbs_attn": achieved,
-        "hbm_frac_attn_of_measured": achieved / peak,
-        "hbm_frac_attn_of_nominal_7900": achieved / 7900.0,
-        "attn_us": attn_avg * 1e6,
-        "attn_kv_tokens_per_s": kv_tokens / attn_avg,
+        "step_us": step_avg * 1e6,
+        "two_call_step_us": two_call_avg * 1e6,
+        "attn_only_us": attn_avg * 1e6,
+        "hbm_gbs_attn_only": attn_gbs,
+        "hbm_frac_attn_only_of_measured": attn_gbs / peak,
+        "hbm_frac_step_of_nominal_7900": achieved / 7900.0,
         "append_tokens_per_s": append_tps,
         "append_gbs": append_bytes / append_s / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "decode_kernel + merge_kernel (one kv_nvfp4_decode_attn call; "
-                               "CUDA events around %d back-to-back calls)" % attn_steps,
+                     "kernel": "decode_kernel<6,fused> + merge_kernel (one kv_nvfp4_decode_step "
+                               "call; CUDA events around the %d back-to-back timed steps)"
+                               % args.steps,
                      "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": attn_bytes},
+                     "algorithmic_bytes_per_launch": step_bytes},
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                "includes": "pinned H2D of new Q/K/V + ids, append, plan upload, attention, D2H of output"},
-        "gpu_launches": 3 * args.steps,  # per timed step: append, attention, split-K merge
+                "includes": "pinned H2D of new Q/K/V, plan upload, step call, D2H of output"},
+        "gpu_launches": 2 * args.steps,  # per timed step: the attention kernel, split-K merge
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(w)

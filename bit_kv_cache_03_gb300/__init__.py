@@ -69,6 +69,8 @@ _SIG = {
                             ctypes.c_size_t, ctypes.POINTER(PlanInfo)], _I32),
     "kv_nvfp4_decode_attn": ([ctypes.POINTER(Layout), ctypes.POINTER(PlanInfo), _P, _P, _P,
                               ctypes.c_float, _P, _I32, _P, _I32, _P, _P, _P], _I32),
+    "kv_nvfp4_decode_step": ([ctypes.POINTER(Layout), ctypes.POINTER(PlanInfo), _P, _P, _P, _P, _P,
+                              _I32, _P, _I32, _I32, _P, _P, _P, ctypes.c_float, _P, _P, _P], _I32),
     "kv_nvfp4_decode_attn_noalloc": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32, _P, _P,
                                       ctypes.c_float, _P, _I32, _P, _I32, _P, _P, _P], _I32),
 }
@@ -226,6 +228,17 @@ def kv_nvfp4_decode_attn(layout, plan: PlanInfo, workspace, q_codes, q_scales, s
         ctypes.byref(layout), ctypes.byref(plan), _ptr(workspace), _ptr(q_codes), _ptr(q_scales),
         float(sm_scale), _ptr(pool), num_pages, _ptr(block_table), max_pages, _ptr(out),
         _ptr(status), _stream(stream)), "kv_nvfp4_decode_attn")
+
+
+def kv_nvfp4_decode_step(layout, plan: PlanInfo, workspace, q, k, v, rope, rope_max_pos,
+                         block_table, max_pages, num_pages, pool, q_codes_out, q_scales_out,
+                         sm_scale, out, status=None, stream=None):
+    """Append of the step's new tokens and decode attention in one launch (see the header)."""
+    _check(lib().kv_nvfp4_decode_step(
+        ctypes.byref(layout), ctypes.byref(plan), _ptr(workspace), _ptr(q), _ptr(k), _ptr(v),
+        _ptr(rope), rope_max_pos, _ptr(block_table), max_pages, num_pages, _ptr(pool),
+        _ptr(q_codes_out), _ptr(q_scales_out), float(sm_scale), _ptr(out), _ptr(status),
+        _stream(stream)), "kv_nvfp4_decode_step")
 
 
 def kv_nvfp4_decode_attn_noalloc(layout, seq_lens, q_len, causal, chunk_tokens, q_codes, q_scales,

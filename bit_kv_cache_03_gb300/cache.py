@@ -9,7 +9,7 @@ import math
 import numpy as np
 import torch
 
-from . import (kv_nvfp4_append, kv_nvfp4_decode_attn, kv_nvfp4_plan,
+from . import (kv_nvfp4_append, kv_nvfp4_decode_attn, kv_nvfp4_decode_step, kv_nvfp4_plan,
                kv_nvfp4_plan_workspace_bytes, kv_nvfp4_pool_bytes, kv_nvfp4_rope_table_init,
                make_layout)
 
@@ -64,3 +64,13 @@ class PagedNVFP4Cache:
         kv_nvfp4_decode_attn(self.layout, self.plan_info, self.workspace, q_codes, q_scales,
                              sm_scale, self.pool, self.num_pages, self.block_table, self.max_pages,
                              out, self.status, stream)
+
+    # -- append of the step's new tokens + attention, one launch ------------------------------
+    def decode_step(self, q, k, v, out, q_codes=None, q_scales=None, sm_scale=None, stream=None):
+        """New tokens of every sequence (sequence-major rows, at the last q_len positions of the
+        lengths given to the last plan) appended and attended in one kernel launch."""
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(128)
+        kv_nvfp4_decode_step(self.layout, self.plan_info, self.workspace, q, k, v, self.rope,
+                             self.max_pos, self.block_table, self.max_pages, self.num_pages,
+                             self.pool, q_codes, q_scales, sm_scale, out, self.status, stream)

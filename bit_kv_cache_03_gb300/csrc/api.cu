@@ -25,7 +25,10 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
                           const int32_t* split_groups, int32_t num_split, float* partials,
                           float* out, int32_t* status,
                           int32_t Hq, int32_t Hkv, int32_t q_len, int32_t causal, int32_t grid,
-                          float sm_scale, cudaStream_t stream);
+                          float sm_scale, const uint16_t* q_new, const uint16_t* k_new,
+                          const uint16_t* v_new, const float* rope, int32_t rope_max_pos,
+                          int32_t rot_dim, uint8_t* pool_w, uint8_t* q_codes_out,
+                          uint8_t* q_scales_out, cudaStream_t stream);
 }  // namespace kvnvfp4
 
 namespace {
@@ -385,7 +388,45 @@ kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout* L, const kv_nvfp4_pl
       (const int32_t*)(ws + plan->off_split), plan->num_split_groups,
       (float*)(ws + plan->off_partials), out, d_status,
       L->num_q_heads, L->num_kv_heads, plan->q_len, plan->causal, plan->grid, sm_scale,
-      (cudaStream_t)stream);
+      nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, nullptr, nullptr, (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
+kv_nvfp4_status kv_nvfp4_decode_step(const kv_nvfp4_layout* L, const kv_nvfp4_plan_info* plan,
+                                     void* d_workspace, const void* q, const void* k,
+                                     const void* v, const float* d_rope_table,
+                                     int32_t rope_max_pos, const int32_t* d_block_table,
+                                     int32_t max_pages, int32_t num_pages, uint8_t* pool,
+                                     uint8_t* q_codes_out, uint8_t* q_scales_out, float sm_scale,
+                                     float* out, int32_t* d_status, void* stream) {
+  if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || plan == nullptr) return KV_NVFP4_EINVAL;
+  if (L->num_kv_heads > kMaxAttnKvHeads) return KV_NVFP4_EINVAL;
+  if (plan->num_kv_heads != L->num_kv_heads || plan->num_seqs <= 0 || plan->q_len <= 0 ||
+      plan->grid <= 0)
+    return KV_NVFP4_EINVAL;
+  // one row tile per sequence: each new row is encoded and stored by exactly one CTA
+  if ((int64_t)(L->num_q_heads / L->num_kv_heads) * plan->q_len > kRowsPerItem)
+    return KV_NVFP4_EINVAL;
+  if (!d_workspace || !q || !k || !v || !pool || !d_block_table || !out || num_pages <= 0 ||
+      max_pages <= 0)
+    return KV_NVFP4_EINVAL;
+  if ((q_codes_out == nullptr) != (q_scales_out == nullptr)) return KV_NVFP4_EINVAL;
+  if (L->rot_dim > 0 && (!d_rope_table || rope_max_pos <= 0 || !aligned16(d_rope_table)))
+    return KV_NVFP4_EINVAL;
+  if ((int64_t)plan->max_seq_len > (int64_t)max_pages * L->page_size) return KV_NVFP4_EINVAL;
+  const void* ptrs[] = {d_workspace, q, k, v, pool, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return KV_NVFP4_EINVAL;
+  if (!(sm_scale > 0.0f)) sm_scale = 1.0f / std::sqrt((float)L->head_dim);
+  char* ws = (char*)d_workspace;
+  const cudaError_t e = kvnvfp4::launch_decode(
+      nullptr, nullptr, pool, d_block_table, max_pages, num_pages, ws + plan->off_groups,
+      ws + plan->off_segments, (const int32_t*)(ws + plan->off_cta),
+      (const int32_t*)(ws + plan->off_split), plan->num_split_groups,
+      (float*)(ws + plan->off_partials), out, d_status,
+      L->num_q_heads, L->num_kv_heads, plan->q_len, plan->causal, plan->grid, sm_scale,
+      (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, d_rope_table, rope_max_pos,
+      L->rot_dim, pool, q_codes_out, q_scales_out, (cudaStream_t)stream);
   return cuda_status(e);
 }
 

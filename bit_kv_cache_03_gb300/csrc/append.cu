@@ -111,76 +111,13 @@ __device__ __forceinline__ RowTarget locate_row(const AppendParams& p, int64_t r
   return r;
 }
 
-__device__ __forceinline__ uint2 ldg_nc_u2(const void* ptr) {
-  uint2 v;
-  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(ptr));
-  return v;
-}
-
 __device__ __forceinline__ void quantize_store_row(float (&x)[4], const RowTarget& r,
                                                    const AppendParams& p, int lane) {
-  if (r.rotate) {
-    // --- RoPE on the first rot_dim dims (pairs i, i + rot_dim/2) ---
-    const int rot = p.rot_dim;
-    if (rot > 0) {
-      const int half_lanes = rot >> 3;           // lanes holding dims [0, rot/2)
-      const bool lower = lane < half_lanes;
-      const int src = lower ? lane + half_lanes : lane - half_lanes;
-      float y[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) y[e] = __shfl_sync(0xffffffffu, x[e], src & 31);
-      if (lane < 2 * half_lanes) {
-        const int i0 = 4 * (lower ? lane : lane - half_lanes);
-        const float* row = p.rope + (int64_t)r.pos * rot;
-        const float4 c = *reinterpret_cast<const float4*>(row + i0);
-        const float4 s = *reinterpret_cast<const float4*>(row + (rot >> 1) + i0);
-        const float cc[4] = {c.x, c.y, c.z, c.w};
-        const float ss[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          // lower lane holds a = x_i, partner b = x_{i+half}: a c - b s
-          // upper lane holds b = x_{i+half}, partner a = x_i:  b c + a s
-          x[e] = lower ? __fsub_rn(__fmul_rn(x[e], cc[e]), __fmul_rn(y[e], ss[e]))
-                       : __fadd_rn(__fmul_rn(x[e], cc[e]), __fmul_rn(y[e], ss[e]));
-        }
-      }
-    }
-    // --- Walsh-Hadamard, stages h = 1, 2, 4, ..., 64 ---
-    {
-      float a = x[0], b = x[1];
-      x[0] = __fadd_rn(a, b); x[1] = __fsub_rn(a, b);
-      a = x[2]; b = x[3];
-      x[2] = __fadd_rn(a, b); x[3] = __fsub_rn(a, b);
-      a = x[0]; b = x[2];
-      x[0] = __fadd_rn(a, b); x[2] = __fsub_rn(a, b);
-      a = x[1]; b = x[3];
-      x[1] = __fadd_rn(a, b); x[3] = __fsub_rn(a, b);
-    }
-#pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-      const bool upper = (lane & m) != 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
-        x[e] = upper ? __fsub_rn(o, x[e]) : __fadd_rn(x[e], o);
-      }
-    }
-    const float kNorm = __uint_as_float(0x3DB504F3u);  // rn(2^-3.5) = rn(1/sqrt(128))
-#pragma unroll
-    for (int e = 0; e < 4; ++e) x[e] = __fmul_rn(x[e], kNorm);
-  }
-
-  // --- NVFP4: block of 16 = 4 lanes ---
-  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  const uint32_t sc = e4m3_encode_rne_sat(__fdiv_rn(amax, 6.0f));
-  const float sd = e4m3_decode_pos(sc);
-  uint32_t packed = 0;
-  if (sd != 0.0f) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) packed |= e2m1_encode_rne_sat(__fdiv_rn(x[e], sd)) << (4 * e);
-  }
+  // a row past the RoPE table is flagged and not stored: do not read the table for it either
+  const float* rope_row = (r.rotate && p.rot_dim > 0 && r.codes != nullptr)
+                              ? p.rope + (int64_t)r.pos * p.rot_dim : nullptr;
+  uint32_t sc;
+  const uint32_t packed = nvfp4_encode_row(x, r.rotate, rope_row, p.rot_dim, lane, sc);
   if (r.codes != nullptr) {
     // lane l holds code bytes 2l, 2l+1 of the row: 16-byte piece l / 8, offset (2l) % 16
     uint8_t* dst = r.tiled ? r.codes + (lane >> 3) * 128 + ((2 * lane) & 15) : r.codes + 2 * lane;

@@ -78,12 +78,14 @@ constexpr int kBarStageEmpty = kBarStageFull + kStages;  // [kStages]
 constexpr int kBarQkDone = kBarStageEmpty + kStages;   // [kSBufs]
 constexpr int kBarSFree = kBarQkDone + kSBufs;         // [kSBufs]
 constexpr int kBarQReady = kBarSFree + kSBufs;
-constexpr int kNumBars = kBarQReady + 1;
+constexpr int kBarKvReady = kBarQReady + 1;  // fused append: the segment's new K/V rows are written
+constexpr int kNumBars = kBarKvReady + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 // misc: stage page ids, tmem base
 constexpr int kOffStagePid = kOffMisc;
 constexpr int kOffTmemSlot = kOffStagePid + 4 * 8;
-constexpr int kSmemBytes = kOffTmemSlot + 16;
+constexpr int kOffQsc = kOffTmemSlot + 16;   // fused append: Q scales [2 pairs][16 rows][8]
+constexpr int kSmemBytes = kOffQsc + 2 * 16 * 8;
 static_assert(kStages <= 8, "stage page-id slots");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
@@ -98,8 +100,8 @@ static_assert(kColSfb + 16 <= 256, "TMEM columns");
 // N = 16, M = 128
 constexpr uint32_t kIdescQK = (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 
-// named barriers: 4 + h = the two warps of KV head h
-constexpr uint32_t kNbHead0 = 4;
+// named barriers: 3 = the attention warps, 4 + h = the two warps of KV head h
+constexpr uint32_t kNbAttn = 3, kNbHead0 = 4;
 
 struct DecodeParams {
   const uint8_t* q_codes;
@@ -116,6 +118,15 @@ struct DecodeParams {
   int32_t* status;
   int32_t Hq, Hkv, G, q_len, causal;
   float c2;                // sm_scale * log2(e)
+  // fused append (kv_nvfp4_decode_step): the step's new tokens, bf16, sequence-major
+  const uint16_t* q_new;   // [num_seqs * q_len][Hq][128]
+  const uint16_t* k_new;   // [num_seqs * q_len][Hkv][128]
+  const uint16_t* v_new;
+  const float* rope;       // [rope_max_pos][rot_dim]
+  int32_t rope_max_pos, rot_dim;
+  uint8_t* pool_w;         // the pool, receiving the new K/V rows
+  uint8_t* q_codes_out;    // optional copy of the encoded Q rows, or null
+  uint8_t* q_scales_out;
 };
 
 struct SegInfo {
@@ -148,16 +159,21 @@ __device__ __forceinline__ void wait_bar(uint32_t bar, uint32_t parity, bool& ti
 // kStages ring; the other lanes load page ids 32 at a time. The page id (or -1 when it lies
 // outside the pool) is published in shared memory before the stage's full barrier is armed.
 // --------------------------------------------------------------------------------------------
+template <bool FUSED>
 __device__ void producer(const DecodeParams& p, uint8_t* smem, int lane) {
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kOffBars;
   volatile int32_t* stage_pid = reinterpret_cast<volatile int32_t*>(smem + kOffStagePid);
   const uint32_t blk_bytes = (uint32_t)p.Hkv * 9216u;
-  uint32_t k = 0;
+  uint32_t k = 0, kvr = 0;
   bool timed_out = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
   for (int s = s_begin; s < s_end; ++s) {
     const SegInfo sg = load_seg(p, s);
+    // fused append: pages from this one on hold the step's new rows, written by this CTA's
+    // attention warps at the segment's start; copy them only after that
+    const int first_new_page = FUSED ? (sg.len - p.q_len) / kPage : 0x7fffffff;
+    bool new_written = false;
     for (int p0 = sg.lo; p0 < sg.hi; p0 += 32) {
       const int n = min(32, sg.hi - p0);
       const int32_t mine =
@@ -168,6 +184,11 @@ __device__ void producer(const DecodeParams& p, uint8_t* smem, int lane) {
           const uint32_t st = k % kStages;
           if (k >= kStages)
             wait_bar(bars + 8 * (kBarStageEmpty + st), ((k / kStages) - 1) & 1, timed_out);
+          if (FUSED && !new_written && p0 + j >= first_new_page) {
+            wait_bar(bars + 8 * kBarKvReady, kvr & 1, timed_out);
+            ++kvr;
+            new_written = true;
+          }
           const bool valid = pid >= 0 && pid < p.num_pages;
           stage_pid[st] = valid ? pid : -1;
           const uint32_t full = bars + 8 * (kBarStageFull + st);
@@ -430,7 +451,157 @@ __device__ __forceinline__ void pv_page(const uint8_t* sm, uint32_t lm0, uint32_
   }
 }
 
-template <int NR>
+// Fused append (kv_nvfp4_decode_step), at the start of a segment: the tile's Q rows are encoded
+// from bf16 (RoPE, Hadamard rotation, NVFP4: the append's arithmetic) straight into the Q tile,
+// their scales into the staging rows at kOffQsc, and the step's new K/V rows that fall on this
+// segment's pages into the pool. After a proxy fence the producer may copy those pages. The new
+// tokens of sequence s are rows s * q_len .. s * q_len + q_len - 1 of q, k, v, at positions
+// len - q_len .. len - 1; a sequence has one row tile here, so one CTA writes each new row.
+// One new K or V row of the step, fetched (bf16 values, RoPE factors, page id) before it is
+// encoded and stored.
+struct NewKvRow {
+  uint2 raw;
+  float4 c, s;
+  int32_t pid;
+  int pos, h;
+  bool is_k;
+};
+
+__device__ __forceinline__ void new_kv_fetch(const DecodeParams& p, const SegInfo& sg, int ri,
+                                             int t0, int lane, NewKvRow& r) {
+  const int tok = t0 + ri / (2 * p.Hkv), w = ri % (2 * p.Hkv);
+  r.is_k = w < p.Hkv;
+  r.h = r.is_k ? w : w - p.Hkv;
+  r.pos = sg.len - p.q_len + tok;
+  r.pid = p.block_table[(int64_t)sg.seq * p.max_pages + r.pos / kPage];
+  r.raw = ldg_nc_u2((r.is_k ? p.k_new : p.v_new) +
+                    (((int64_t)sg.seq * p.q_len + tok) * p.Hkv + r.h) * kHeadDim + 4 * lane);
+  const bool rope = r.is_k && p.rot_dim > 0 && r.pos < p.rope_max_pos;
+  rope_fetch(rope ? p.rope + (int64_t)r.pos * p.rot_dim : nullptr, p.rot_dim, lane, r.c, r.s);
+}
+
+__device__ __forceinline__ void new_kv_store(const DecodeParams& p, const NewKvRow& r, int lane) {
+  if (r.pid < 0 || r.pid >= p.num_pages) {  // the producer skips (and flags) the page as well
+    if (lane == 0) flag_status(p.status, KV_NVFP4_DEV_BAD_PAGE);
+    return;
+  }
+  if (r.is_k && p.rot_dim > 0 && r.pos >= p.rope_max_pos) {
+    if (lane == 0) flag_status(p.status, KV_NVFP4_DEV_BAD_ROPE);
+    return;
+  }
+  float x[4] = {__uint_as_float(r.raw.x << 16), __uint_as_float(r.raw.x & 0xFFFF0000u),
+                __uint_as_float(r.raw.y << 16), __uint_as_float(r.raw.y & 0xFFFF0000u)};
+  uint32_t sc;
+  const uint32_t packed =
+      nvfp4_encode_row_fetched(x, r.is_k, r.is_k && p.rot_dim > 0, r.c, r.s, p.rot_dim, lane, sc);
+  // page block: [K codes H*4096 (tile order)][K scales H*512][V codes H*4096][V scales H*512]
+  uint8_t* blk = p.pool_w + (int64_t)r.pid * p.Hkv * 9216;
+  const int slot = r.pos % kPage;
+  uint8_t* codes;
+  uint8_t* scales;
+  if (r.is_k) {
+    codes = blk + r.h * 4096 + (slot >> 3) * 512 + (slot & 7) * 16 + (lane >> 3) * 128 +
+            ((2 * lane) & 15);
+    scales = blk + p.Hkv * 4096 + r.h * 512 + slot * 8;
+  } else {
+    codes = blk + p.Hkv * 4608 + r.h * 4096 + slot * 64 + 2 * lane;
+    scales = blk + p.Hkv * 8704 + r.h * 512 + slot * 8;
+  }
+  *reinterpret_cast<uint16_t*>(codes) = (uint16_t)packed;
+  if ((lane & 3) == 0) scales[lane >> 2] = (uint8_t)sc;
+}
+
+// Fused step, per segment, by the attention warps: the segment's Q tile encoded from the bf16
+// rows into shared memory (and, by the first segment of the group, into q_codes_out), and the
+// step's new K/V rows that fall on the segment's pages stored into the pool. Every global load is
+// issued before any arithmetic: while the other CTAs stream the cache, one load takes about a
+// microsecond, and a chain of them would hold back the segment's first QK.
+__device__ __forceinline__ void fused_prologue(const DecodeParams& p, const SegInfo& sg,
+                                               uint8_t* smem, uint32_t sbase, uint32_t bars,
+                                               int aw, int lane) {
+  const int rows_total = p.G * p.q_len;
+  const int row0 = sg.rg * kRows;
+  const bool q_out = p.q_codes_out != nullptr && (sg.n_seg == 1 || sg.part == sg.first_part);
+  uint8_t* qsc = smem + kOffQsc;
+  const int pr = aw >> 2;
+  // tile rows 4 (aw % 4) .. + 3 of pair aw / 4
+  uint2 qraw[4];
+  float4 qc[4], qs[4];
+  int64_t qtrow[4];
+  int qstate[4];  // 0: padding row, 1: row past the RoPE table, 2: row to encode
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const int nrow = 4 * (aw & 3) + jj;
+    const int hh = 2 * pr + (nrow >> 3), r = row0 + (nrow & 7);
+    qraw[jj] = make_uint2(0u, 0u);
+    qc[jj] = qs[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
+    qtrow[jj] = 0;
+    qstate[jj] = 0;
+    if (hh < p.Hkv && r < rows_total) {  // warp-uniform
+      const int tok = r / p.G, qh = hh * p.G + r % p.G;
+      qtrow[jj] = ((int64_t)sg.seq * p.q_len + tok) * p.Hq + qh;
+      const int pos = sg.len - p.q_len + tok;
+      const bool rope_ok = p.rot_dim == 0 || pos < p.rope_max_pos;
+      qstate[jj] = rope_ok ? 2 : 1;
+      if (rope_ok) {
+        qraw[jj] = ldg_nc_u2(p.q_new + qtrow[jj] * kHeadDim + 4 * lane);
+        rope_fetch(p.rot_dim > 0 ? p.rope + (int64_t)pos * p.rot_dim : nullptr, p.rot_dim, lane,
+                   qc[jj], qs[jj]);
+      }
+    }
+  }
+  // the step's new K and V rows on this segment's pages; the first one of this warp fetched now
+  const int first_pos = sg.len - p.q_len;
+  const int t0 = max(0, sg.lo * kPage - first_pos), t1 = min(p.q_len, sg.hi * kPage - first_pos);
+  const int nrows = t1 > t0 ? (t1 - t0) * 2 * p.Hkv : 0;
+  NewKvRow kv;
+  if (aw < nrows) new_kv_fetch(p, sg, aw, t0, lane, kv);
+
+  // the four rows in lockstep; a padding row or one past the RoPE table holds zeros and encodes
+  // to zero codes and a zero scale
+  float qx[4][4];
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    qx[jj][0] = __uint_as_float(qraw[jj].x << 16);
+    qx[jj][1] = __uint_as_float(qraw[jj].x & 0xFFFF0000u);
+    qx[jj][2] = __uint_as_float(qraw[jj].y << 16);
+    qx[jj][3] = __uint_as_float(qraw[jj].y & 0xFFFF0000u);
+  }
+  uint32_t qpk[4], qsc4[4];
+  nvfp4_encode_rows<4>(qx, true, p.rot_dim > 0, qc, qs, p.rot_dim, lane, qpk, qsc4);
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const int nrow = 4 * (aw & 3) + jj;
+    if (qstate[jj] == 2 && q_out) {
+      *reinterpret_cast<uint16_t*>(p.q_codes_out + qtrow[jj] * kCodeBytes + 2 * lane) =
+          (uint16_t)qpk[jj];
+      if ((lane & 3) == 0) p.q_scales_out[qtrow[jj] * kScaleBytes + (lane >> 2)] = (uint8_t)qsc4[jj];
+    } else if (qstate[jj] == 1) {  // a position past the RoPE table: flagged, the row scores zero
+      if (lane == 0) flag_status(p.status, KV_NVFP4_DEV_BAD_ROPE);
+    }
+    // tensor-core tile order: lane l's code bytes 2l, 2l + 1 sit in 16-byte piece l / 8
+    sts16(sbase + kOffQ + pr * 1024 + (nrow >> 3) * 512 + (lane >> 3) * 128 + (nrow & 7) * 16 +
+              ((2 * lane) & 15),
+          qpk[jj]);
+    if ((lane & 3) == 0) qsc[(pr * 16 + nrow) * 8 + (lane >> 2)] = (uint8_t)qsc4[jj];
+  }
+  if (aw < nrows) new_kv_store(p, kv, lane);
+#pragma unroll 1
+  for (int ri = aw + kAttnWarps; ri < nrows; ri += kAttnWarps) {  // more than 8 new rows
+    new_kv_fetch(p, sg, ri, t0, lane, kv);
+    new_kv_store(p, kv, lane);
+  }
+  // the pool rows visible to this CTA's bulk copies (async proxy) before the producer copies their
+  // page; the Q tile and its staged scales complete before the scale factors are read
+  if (nrows > 0) {
+    __threadfence();
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+  }
+  named_barrier_sync(kNbAttn, 32 * kAttnWarps);
+  if (nrows > 0 && aw == 0 && lane == 0) mbar_arrive(bars + 8 * kBarKvReady);
+}
+
+template <int NR, bool FUSED>
 __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t tbase, int warp,
                                 int lane) {
   AttnCtx c;
@@ -480,7 +651,9 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
     const uint32_t rows_mask = __ballot_sync(0xffffffffu, mylim >= 0) & 0xFFu;
 
     // ---- this pair's Q tile (B operand of Q.K^T) and its scale factors ----
-    if (c.gt < 64) {
+    if (FUSED) {
+      fused_prologue(p, sg, smem, c.sbase, c.bars, aw, lane);
+    } else if (c.gt < 64) {
       const int nrow = c.gt >> 2, ch = c.gt & 3;
       const int hh = 2 * c.pr + (nrow >> 3), r = row0 + (nrow & 7);
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -495,7 +668,13 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
       uint32_t sf[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) sf[q] = 0u;
-      if (lane < 16) {
+      if (FUSED) {  // scales staged by the prologue, rows of pair c.pr in tile order
+        if (lane < 16) {
+          const uint2 qs = *reinterpret_cast<const uint2*>(smem + kOffQsc + (c.pr * 16 + lane) * 8);
+          sf[0] = qs.x;
+          sf[4] = qs.y;
+        }
+      } else if (lane < 16) {
         const int h2 = 2 * c.pr + (lane >> 3), r2 = row0 + (lane & 7);
         if (h2 < p.Hkv && r2 < rows_total) {
           const int64_t qrow = ((int64_t)sg.seq * p.q_len + r2 / p.G) * p.Hq + h2 * p.G + r2 % p.G;
@@ -633,8 +812,9 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
   if (c.timed_out && lane == 0) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
 
-// NR: query rows computed per head (6 when no tile has more real rows, else all 8)
-template <int NR>
+// NR: query rows computed per head (6 when no tile has more real rows, else all 8); FUSED: the
+// step's append is done in the kernel (kv_nvfp4_decode_step)
+template <int NR, bool FUSED>
 __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -652,6 +832,7 @@ __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodePa
       mbar_init(bars + 8 * (kBarSFree + b), kAttnWarps);
     }
     mbar_init(bars + 8 * kBarQReady, kAttnWarps);
+    mbar_init(bars + 8 * kBarKvReady, 1);
     fence_mbar_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(smem + kOffTmemSlot), kTmemCols);
@@ -665,11 +846,11 @@ __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodePa
   const uint32_t tbase = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmemSlot);
 
   if (warp == kWarpProducer) {
-    producer(p, smem, lane);
+    producer<FUSED>(p, smem, lane);
   } else if (warp == kWarpMma) {
     qk_warp(p, smem, tbase, lane);
   } else {
-    attention_warps<NR>(p, smem, tbase, warp, lane);
+    attention_warps<NR, FUSED>(p, smem, tbase, warp, lane);
   }
 
   tc_fence_before();
@@ -762,15 +943,19 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
                           const int32_t* split_groups, int32_t num_split, float* partials,
                           float* out, int32_t* status,
                           int32_t Hq, int32_t Hkv, int32_t q_len, int32_t causal, int32_t grid,
-                          float sm_scale, cudaStream_t stream) {
+                          float sm_scale, const uint16_t* q_new, const uint16_t* k_new,
+                          const uint16_t* v_new, const float* rope, int32_t rope_max_pos,
+                          int32_t rot_dim, uint8_t* pool_w, uint8_t* q_codes_out,
+                          uint8_t* q_scales_out, cudaStream_t stream) {
   // the attribute belongs to each instantiation, set once per process
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemBytes);
+    cudaError_t e = cudaSuccess;
+    const void* kernels[] = {(const void*)decode_kernel<8, false>, (const void*)decode_kernel<6, false>,
+                             (const void*)decode_kernel<8, true>, (const void*)decode_kernel<6, true>};
+    for (const void* kf : kernels)
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -784,6 +969,10 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
   p.partials = partials; p.out = out; p.status = status;
   p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv; p.q_len = q_len; p.causal = causal;
   p.c2 = sm_scale * 1.4426950408889634f;
+  p.q_new = q_new; p.k_new = k_new; p.v_new = v_new; p.rope = rope;
+  p.rope_max_pos = rope_max_pos; p.rot_dim = rot_dim; p.pool_w = pool_w;
+  p.q_codes_out = q_codes_out; p.q_scales_out = q_scales_out;
+  const bool fused = q_new != nullptr;
   if (grid <= 0) return cudaSuccess;
   // programmatic dependent launch: the kernel is set up while the previous kernel on the stream
   // finishes, and waits for it (griddepcontrol.wait) before touching memory
@@ -799,8 +988,12 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
     dc.attrs = da;
     dc.numAttrs = 1;
     // every tile has at most G * q_len real rows: with six or fewer, rows 6 and 7 are never computed
-    const cudaError_t le = (p.G * q_len <= 6) ? cudaLaunchKernelEx(&dc, decode_kernel<6>, p)
-                                              : cudaLaunchKernelEx(&dc, decode_kernel<8>, p);
+    const bool six = p.G * q_len <= 6;
+    const cudaError_t le =
+        fused ? (six ? cudaLaunchKernelEx(&dc, decode_kernel<6, true>, p)
+                     : cudaLaunchKernelEx(&dc, decode_kernel<8, true>, p))
+              : (six ? cudaLaunchKernelEx(&dc, decode_kernel<6, false>, p)
+                     : cudaLaunchKernelEx(&dc, decode_kernel<8, false>, p));
     if (le != cudaSuccess) return le;
   }
   cudaError_t e = cudaGetLastError();

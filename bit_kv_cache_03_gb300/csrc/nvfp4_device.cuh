@@ -20,22 +20,6 @@ constexpr int kScaleBytes = 8;   // 128 / 16 E4M3 scales
 // {0, 0.5, 1, 1.5, 2, 3, 4, 6}.
 // ---------------------------------------------------------------------------------------------
 
-// Round a finite t >= 0 to the nearest E4M3 value, ties to even, saturating at 448.
-__device__ __forceinline__ uint32_t e4m3_encode_rne_sat(float t) {
-  if (!(t > 0.0f)) return 0u;
-  if (t >= 448.0f) return 0x7Eu;
-  if (t < 0.015625f) {                          // below 2^-6: subnormal grid m * 2^-9
-    return (uint32_t)__float2int_rn(__fmul_rn(t, 512.0f));  // exact scaling, RNE; 8 -> 2^-6
-  }
-  const uint32_t b = __float_as_uint(t);
-  const int e = (int)(b >> 23) - 127;           // -6 .. 8
-  uint32_t r = (b >> 20) & 7u;                  // top 3 mantissa bits
-  const uint32_t rem = b & 0xFFFFFu;
-  if (rem > 0x80000u || (rem == 0x80000u && (r & 1u))) ++r;  // a carry into r = 8 bumps e
-  const uint32_t code = (uint32_t)((e + 7) << 3) + r;
-  return code > 0x7Eu ? 0x7Eu : code;
-}
-
 // Exact value of a non-NaN E4M3 code with the sign bit clear.
 __device__ __forceinline__ float e4m3_decode_pos(uint32_t c) {
   const uint32_t e = (c >> 3) & 15u, m = c & 7u;
@@ -43,15 +27,168 @@ __device__ __forceinline__ float e4m3_decode_pos(uint32_t c) {
   return __uint_as_float(((e + 120u) << 23) | (m << 20));  // 2^(e-7) * (1 + m/8)
 }
 
-// E2M1 code of x (round to nearest, ties to the even code, saturate at 6, sign kept). The
-// midpoints of the grid are 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5; at a midpoint the even code
-// wins, which makes the comparison strict where the lower neighbour is even and inclusive where
-// the upper neighbour is even.
-__device__ __forceinline__ uint32_t e2m1_encode_rne_sat(float x) {
-  const float a = fabsf(x);
-  uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
-               (a >= 3.5f) + (a > 5.0f);
-  return c | ((__float_as_uint(x) >> 28) & 8u);
+// Two f32 -> two E2M1 codes with the sm_100-family converter: round to nearest, ties to the even
+// code, saturating at 6, sign kept (a negative value that rounds to zero gives the negative-zero
+// code 8). a goes to bits 4..7, b to bits 0..3.
+__device__ __forceinline__ uint32_t e2m1x2_from_f32(float a, float b) {
+  uint32_t r;
+  asm("{\n.reg .b8 d;\ncvt.rn.satfinite.e2m1x2.f32 d, %1, %2;\ncvt.u32.u8 %0, d;\n}"
+      : "=r"(r)
+      : "f"(a), "f"(b));
+  return r;
+}
+
+// Two f32 >= 0 -> two E4M3 codes with the converter: round to nearest, ties to even, saturating at
+// 448 (0x7E). a goes to bits 8..15, b to bits 0..7.
+__device__ __forceinline__ uint32_t e4m3x2_from_f32(float a, float b) {
+  uint32_t r;
+  asm("{\n.reg .b16 d;\ncvt.rn.satfinite.e4m3x2.f32 d, %1, %2;\ncvt.u32.u16 %0, d;\n}"
+      : "=r"(r)
+      : "f"(a), "f"(b));
+  return r;
+}
+
+// x / b rounded to nearest from r = the correctly rounded 1 / b: q0 = x r, then one correction
+// with the exact residual x - q0 b (Markstein's division step). The result is the correctly
+// rounded quotient whenever that is a normal number; a subnormal quotient may be off by an ulp,
+// which moves no E4M3 or E2M1 code (it is far below their smallest rounding threshold).
+__device__ __forceinline__ float div_rn_by(float x, float b, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float res = __fmaf_rn(-q0, b, x);
+  return __fmaf_rn(res, r, q0);
+}
+
+// This lane's RoPE factors for a row at angle-table row `rope_row` (cos of its 4 dims, then sin):
+// lanes below rot/4 hold dims of a rotated pair, the others (and a null row) get zeros. Kept apart
+// from the encode so that a caller can issue the loads of several rows before any arithmetic.
+__device__ __forceinline__ void rope_fetch(const float* rope_row, int rot, int lane, float4& c,
+                                           float4& s) {
+  c = make_float4(0.f, 0.f, 0.f, 0.f);
+  s = c;
+  const int half_lanes = rot >> 3;  // lanes holding dims [0, rot/2)
+  if (rope_row != nullptr && lane < 2 * half_lanes) {
+    const int i0 = 4 * (lane < half_lanes ? lane : lane - half_lanes);
+    c = *reinterpret_cast<const float4*>(rope_row + i0);
+    s = *reinterpret_cast<const float4*>(rope_row + (rot >> 1) + i0);
+  }
+}
+
+// R rows of nvfp4_encode_row, advanced in lockstep (every step taken for all R rows before the
+// next), with the RoPE factors already fetched (rope_fetch). Each row goes through exactly the
+// operations of the one-row encode, so its codes and scale do not depend on R; the R independent
+// chains of shuffles and divisions hide one another's latency. `rope` says whether the rows take
+// RoPE at all.
+template <int R>
+__device__ __forceinline__ void nvfp4_encode_rows(float (&x)[R][4], bool rotate, bool rope,
+                                                  const float4 (&c)[R], const float4 (&s)[R],
+                                                  int rot, int lane, uint32_t (&packed)[R],
+                                                  uint32_t (&sc)[R]) {
+  if (rotate) {
+    // --- RoPE on the first rot_dim dims (pairs i, i + rot_dim/2) ---
+    if (rope) {
+      const int half_lanes = rot >> 3;           // lanes holding dims [0, rot/2)
+      const bool lower = lane < half_lanes;
+      const bool paired = lane < 2 * half_lanes;
+      const int src = lower ? lane + half_lanes : lane - half_lanes;
+      const float ysg = lower ? -1.0f : 1.0f;
+      float y[R][4];
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[r][e] = __shfl_sync(0xffffffffu, x[r][e], src & 31);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float cc[4] = {c[r].x, c[r].y, c[r].z, c[r].w};
+        const float ss[4] = {s[r].x, s[r].y, s[r].z, s[r].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          // lower lane holds a = x_i, partner b = x_{i+half}: a c - b s
+          // upper lane holds b = x_{i+half}, partner a = x_i:  b c + a s
+          // (-b) s = -(b s) exactly, so both are one add of two rounded products
+          const float v = __fadd_rn(__fmul_rn(x[r][e], cc[e]), __fmul_rn(ysg * y[r][e], ss[e]));
+          x[r][e] = paired ? v : x[r][e];
+        }
+      }
+    }
+    // --- Walsh-Hadamard, stages h = 1, 2, 4, ..., 64 ---
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float a = x[r][0], b = x[r][1];
+      x[r][0] = __fadd_rn(a, b); x[r][1] = __fsub_rn(a, b);
+      a = x[r][2]; b = x[r][3];
+      x[r][2] = __fadd_rn(a, b); x[r][3] = __fsub_rn(a, b);
+      a = x[r][0]; b = x[r][2];
+      x[r][0] = __fadd_rn(a, b); x[r][2] = __fsub_rn(a, b);
+      a = x[r][1]; b = x[r][3];
+      x[r][1] = __fadd_rn(a, b); x[r][3] = __fsub_rn(a, b);
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const float sgn = (lane & m) != 0 ? -1.0f : 1.0f;
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          // upper lane: o - x, lower lane: x + o; (+-1) x is exact, so one fma rounds as they do
+          const float o = __shfl_xor_sync(0xffffffffu, x[r][e], m);
+          x[r][e] = __fmaf_rn(sgn, x[r][e], o);
+        }
+    }
+    const float kNorm = __uint_as_float(0x3DB504F3u);  // rn(2^-3.5) = rn(1/sqrt(128))
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[r][e] = __fmul_rn(x[r][e], kNorm);
+  }
+
+  // --- NVFP4: block of 16 = 4 lanes ---
+  float amax[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    amax[r] = fmaxf(fmaxf(fabsf(x[r][0]), fabsf(x[r][1])), fmaxf(fabsf(x[r][2]), fabsf(x[r][3])));
+#pragma unroll
+  for (int r = 0; r < R; ++r) amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], 1));
+#pragma unroll
+  for (int r = 0; r < R; ++r) amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], 2));
+  // scale = RNE_sat_E4M3(amax / 6), codes = RNE_sat_E2M1(x / scale), each quotient rounded to
+  // fp32 first, exactly as the definition reads
+  const float r6 = __frcp_rn(6.0f);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    sc[r] = e4m3x2_from_f32(0.0f, div_rn_by(amax[r], 6.0f, r6)) & 0xFFu;
+    const float sd = e4m3_decode_pos(sc[r]);
+    const float rs = __frcp_rn(sd);
+    float q[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) q[e] = copysignf(div_rn_by(x[r][e], sd, rs), x[r][e]);
+    const uint32_t pk = e2m1x2_from_f32(q[1], q[0]) | (e2m1x2_from_f32(q[3], q[2]) << 8);
+    packed[r] = sd != 0.0f ? pk : 0u;  // an all-zero block: zero scale, zero codes
+  }
+}
+
+__device__ __forceinline__ uint32_t nvfp4_encode_row_fetched(float (&x)[4], bool rotate, bool rope,
+                                                             float4 c, float4 s, int rot, int lane,
+                                                             uint32_t& sc) {
+  float xr[1][4] = {{x[0], x[1], x[2], x[3]}};
+  const float4 cr[1] = {c}, sr[1] = {s};
+  uint32_t packed[1], scr[1];
+  nvfp4_encode_rows<1>(xr, rotate, rope, cr, sr, rot, lane, packed, scr);
+  sc = scr[0];
+  return packed[0];
+}
+
+// One 128-element row held by a warp, lane l holding elements 4l..4l+3, encoded as the method
+// prescribes: for Q and K rows (rotate) RoPE on the first `rot` dims (pairs i, i + rot/2, angle
+// table row `rope_row`, skipped when null) and the normalised Walsh-Hadamard rotation; then NVFP4
+// (E4M3 scale per 16 elements = RNE of amax / 6, E2M1 codes = RNE of x / scale). Every fp32 step
+// rounds once, exactly as written (explicit _rn intrinsics). Returns this lane's 4 codes (element
+// 4l + e in bits 4e..4e+3) and sets sc to the scale of its 16-element block.
+__device__ __forceinline__ uint32_t nvfp4_encode_row(float (&x)[4], bool rotate,
+                                                     const float* rope_row, int rot, int lane,
+                                                     uint32_t& sc) {
+  float4 c, s;
+  rope_fetch(rotate ? rope_row : nullptr, rot, lane, c, s);
+  return nvfp4_encode_row_fetched(x, rotate, rope_row != nullptr, c, s, rot, lane, sc);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -158,6 +295,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+__device__ __forceinline__ void sts16(uint32_t a, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((uint16_t)v) : "memory");
+}
+// 8 bytes from global memory through the read-only path.
+__device__ __forceinline__ uint2 ldg_nc_u2(const void* ptr) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(ptr));
+  return v;
+}
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -221,6 +221,31 @@ kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout *layout,
                                      const int32_t *d_block_table, int32_t max_pages, float *out,
                                      int32_t *d_status, void *stream);
 
+/* ---- Fused decode step [NVFP4: the decode path quantises the current K/V as it runs] -----------
+ * One launch doing what kv_nvfp4_append (of the step's new tokens, with Q) followed by
+ * kv_nvfp4_decode_attn does, with bit-identical pool bytes and output: the new tokens are encoded
+ * (RoPE, Hadamard rotation, NVFP4) inside the attention kernel, the K/V rows stored into the pool
+ * by the CTA that reads their page, and the Q rows used straight from shared memory.
+ *   plan, d_workspace: from kv_nvfp4_plan over the lengths INCLUDING the new tokens (same stream)
+ *   q, k, v:   DEVICE bf16 [num_seqs * q_len][num_q_heads | num_kv_heads][128], sequence-major:
+ *              row s * q_len + i is new token i of sequence s, at position seq_len_s - q_len + i
+ *   d_rope_table, rope_max_pos, d_block_table, max_pages, num_pages, pool: as for the append
+ *   q_codes_out, q_scales_out: optional (both or neither) DEVICE copy of the encoded Q rows,
+ *              [num_seqs * q_len][num_q_heads][64 | 8]
+ *   sm_scale, out, d_status: as for kv_nvfp4_decode_attn
+ * Requires (num_q_heads / num_kv_heads) * q_len <= 8 (one 8-row tile per sequence: decode with
+ * GQA groups up to 8); larger verify or prefill steps use the two calls. Status bits as for both
+ * calls (a bad page or position skips the row). One kernel launch, plus the split-K merge launch
+ * when the plan has split groups. */
+kv_nvfp4_status kv_nvfp4_decode_step(const kv_nvfp4_layout *layout,
+                                     const kv_nvfp4_plan_info *plan, void *d_workspace,
+                                     const void *q, const void *k, const void *v,
+                                     const float *d_rope_table, int32_t rope_max_pos,
+                                     const int32_t *d_block_table, int32_t max_pages,
+                                     int32_t num_pages, uint8_t *pool, uint8_t *q_codes_out,
+                                     uint8_t *q_scales_out, float sm_scale, float *out,
+                                     int32_t *d_status, void *stream);
+
 /* ---- Decode attention without caller-provided device memory ----------------------------------
  * No counterpart in the pages: an addition of this library for callers that cannot allocate
  * device memory, such as an inference engine that reserves all of the GPU's memory for its own

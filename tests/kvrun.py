@@ -63,6 +63,15 @@ class GpuRun:
             self.cache.plan(w.seq_lens, w.q_len, w.causal, chunk_tokens or w.chunk_tokens)
         self.cache.attend(self.q_codes, self.q_scales, self.out, sm_scale=w.sm_scale)
 
+    def step_fused(self, chunk_tokens=None, plan=True, q_out=True):
+        """The same step through kv_nvfp4_decode_step: the append of the new tokens inside the
+        attention launch (requires group * q_len <= 8)."""
+        w, c = self.w, self.cache
+        if plan:
+            c.plan(w.seq_lens, w.q_len, w.causal, chunk_tokens or w.chunk_tokens)
+        c.decode_step(self.q, self.k, self.v, self.out, self.q_codes if q_out else None,
+                      self.q_scales if q_out else None, sm_scale=w.sm_scale)
+
     def status(self) -> int:
         return int(self.cache.status.item())
 

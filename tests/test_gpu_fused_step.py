@@ -1,0 +1,66 @@
+"""kv_nvfp4_decode_step (append inside the attention launch) against the two-call path and the
+oracle (GPU): bit-identical pool bytes and Q codes, identical output, oracle parity."""
+import numpy as np
+import pytest
+
+import synth
+from kvrun import MAX_ABS_TOL, REL_L2_TOL, GpuRun, OracleRun, attention_errors, compare_pool
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _pair(w, chunk):
+    a, b = GpuRun(w), GpuRun(w)
+    a.step(chunk_tokens=chunk)        # kv_nvfp4_append, then kv_nvfp4_decode_attn
+    b.step_fused(chunk_tokens=chunk)  # kv_nvfp4_decode_step
+    torch.cuda.synchronize()
+    return a, b
+
+
+@pytest.mark.parametrize("lens,q_len,Hq,Hkv,chunk", [
+    ([0, 5, 63, 64, 65, 200, 1000], 1, 24, 4, 1024),
+    ([0, 5, 63, 64, 65, 200, 1000], 1, 24, 4, 64),     # split groups: the merge launch too
+    ([130, 700, 1500], 2, 8, 2, 128),                  # 2 new tokens x GQA 4 = 8 rows
+    ([300, 1200], 1, 8, 1, 256),                       # GQA 8: all 8 rows computed
+    ([100, 2000], 1, 9, 3, 256),                       # odd number of KV heads
+    ([4000], 4, 4, 4, 512),                            # 4 new tokens, no GQA, page boundary
+])
+def test_fused_step_matches_two_calls_and_oracle(lens, q_len, Hq, Hkv, chunk):
+    w = synth.Workload("fused", lens, q_len=q_len, seed=7 + q_len + Hkv, q_heads=Hq, kv_heads=Hkv,
+                       chunk_tokens=chunk, pool_pages=sum((c + q_len + 63) // 64 for c in lens) + 3)
+    a, b = _pair(w, chunk)
+    assert a.status() == 0 and b.status() == 0
+    o = OracleRun(w)
+    bad = compare_pool(b, o)               # every cached and new code byte, bit-exact
+    assert all(v == 0 for v in bad.values()), bad
+    qa, qb = a.q_quant(), b.q_quant()
+    assert np.array_equal(qa[0], qb[0]) and np.array_equal(qa[1], qb[1])
+    assert np.array_equal(a.output(), b.output())
+    max_abs, rel = attention_errors(b.output(), o.attention().reshape(b.output().shape))
+    assert max_abs <= MAX_ABS_TOL and rel <= REL_L2_TOL, (max_abs, rel)
+    # a second step on the same cache rewrites the same rows: same result
+    b.step_fused(chunk_tokens=chunk, q_out=False)
+    torch.cuda.synchronize()
+    assert np.array_equal(a.output(), b.output()) and b.status() == 0
+
+
+def test_fused_step_rejects_more_than_one_row_tile():
+    import bit_kv_cache_03_gb300 as kv
+    w = synth.Workload("fused_bad", [500], q_len=2, seed=3, chunk_tokens=256)  # 2 x GQA 6 = 12 rows
+    g = GpuRun(w)
+    g.cache.plan(w.seq_lens, w.q_len, w.causal, 256)
+    with pytest.raises(kv.KVNVFP4Error, match=r"\(-1\)"):
+        g.step_fused(plan=False)
+
+
+def test_fused_step_flags_a_page_outside_the_pool():
+    import bit_kv_cache_03_gb300 as kv
+    w = synth.Workload("fused_badpage", [500], q_len=1, seed=4, pool_pages=12)
+    g = GpuRun(w)
+    bt = g.cache.block_table.clone()
+    g.cache.block_table[0, 500 // 64] = 10 ** 6  # the page of the new token
+    g.step_fused()
+    torch.cuda.synchronize()
+    assert g.status() & kv.DEV_BAD_PAGE
+    g.cache.block_table.copy_(bt)
