@@ -62,6 +62,14 @@ constexpr int kThreads = (kWarpAttn0 + kAttnWarps) * 32;
 // Register bound: three warps share one SM sub-partition's 16K registers, so <= 168 per thread.
 constexpr int kBoundThreads = 384;
 
+// Fused step: at the start of each segment the producer fills one stage slot (the step slot) with
+// the segment sequence's bf16 Q rows, new K and V rows and RoPE rows, ahead of the segment's pages,
+// so the prologue that encodes them reads shared memory only. Offsets within the slot; the sizes
+// are bounded by (Hq / Hkv) q_len <= 8: at most 32 Q rows, 32 K and 32 V rows of 256 B, 8 RoPE
+// rows of up to 512 B.
+constexpr int kStepQ = 0, kStepK = 8192, kStepV = 16384, kStepRope = 24576;
+static_assert(kStepRope + 8 * 128 * 4 <= kMaxHkv * 9216, "step slot larger than a stage");
+
 constexpr int kPsBytes = 1024;                     // per attention warp: 32 keys x (hi 16 B, lo 16 B)
 constexpr int kMergeHeadBytes = 8 * 32 * 16 + 2 * kRows * 4;  // O: 8 float4 per lane; m[8], l[8]
 
@@ -170,6 +178,29 @@ __device__ void producer(const DecodeParams& p, uint8_t* smem, int lane) {
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
   for (int s = s_begin; s < s_end; ++s) {
     const SegInfo sg = load_seg(p, s);
+    if (FUSED) {  // the segment's step slot (bf16 Q, new K/V and RoPE rows of its sequence)
+      if (lane == 0) {
+        const uint32_t st = k % kStages;
+        if (k >= kStages)
+          wait_bar(bars + 8 * (kBarStageEmpty + st), ((k / kStages) - 1) & 1, timed_out);
+        stage_pid[st] = -1;
+        const int first_pos = sg.len - p.q_len;
+        const uint32_t qb = (uint32_t)(p.q_len * p.Hq) * 256u, kb = (uint32_t)(p.q_len * p.Hkv) * 256u;
+        // RoPE rows that exist in the table (a row past it is flagged by the prologue)
+        const int nrope = p.rot_dim > 0 ? max(0, min(p.q_len, p.rope_max_pos - first_pos)) : 0;
+        const uint32_t rb = (uint32_t)(nrope * p.rot_dim) * 4u;
+        const uint32_t full = bars + 8 * (kBarStageFull + st);
+        const uint32_t dst = sbase + kOffStage + st * kStageBytes;
+        const int64_t tok0 = (int64_t)sg.seq * p.q_len;
+        mbar_arrive_expect_tx(full, qb + 2u * kb + rb);
+        bulk_g2s(dst + kStepQ, p.q_new + tok0 * p.Hq * kHeadDim, qb, full);
+        bulk_g2s(dst + kStepK, p.k_new + tok0 * p.Hkv * kHeadDim, kb, full);
+        bulk_g2s(dst + kStepV, p.v_new + tok0 * p.Hkv * kHeadDim, kb, full);
+        if (rb > 0u) bulk_g2s(dst + kStepRope, p.rope + (int64_t)first_pos * p.rot_dim, rb, full);
+      }
+      ++k;
+      __syncwarp();
+    }
     // fused append: pages from this one on hold the step's new rows, written by this CTA's
     // attention warps at the segment's start; copy them only after that
     const int first_new_page = FUSED ? (sg.len - p.q_len) / kPage : 0x7fffffff;
@@ -223,20 +254,29 @@ __device__ void producer(const DecodeParams& p, uint8_t* smem, int lane) {
 // the copies. The warp runs ahead of the attention warps as far as the stage ring and the two S
 // buffers allow.
 // --------------------------------------------------------------------------------------------
+template <bool FUSED>
 __device__ void qk_warp(const DecodeParams& p, uint8_t* smem, uint32_t tbase, int lane) {
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kOffBars;
   const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kOffStagePid);
   const int npairs = (p.Hkv + 1) >> 1;
-  uint32_t k = 0, sgi = 0;
+  uint32_t k = 0, ks = 0, sgi = 0;  // pages (S buffers), stage slots, segments
   bool timed_out = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
   for (int s = s_begin; s < s_end; ++s, ++sgi) {
     const SegInfo sg = load_seg(p, s);
+    if (FUSED) {
+      // this warp's share of releasing the step slot; waiting for the slot first orders the
+      // arrival after the slot's previous use was released (as for a page slot)
+      const uint32_t st = ks % kStages;
+      wait_bar(bars + 8 * (kBarStageFull + st), (ks / kStages) & 1, timed_out);
+      if (lane == 0) mbar_arrive(bars + 8 * (kBarStageEmpty + st));
+      ++ks;
+    }
     wait_bar(bars + 8 * kBarQReady, sgi & 1, timed_out);  // Q tile and its scales for this group
-    for (int j = 0; j < sg.hi - sg.lo; ++j, ++k) {
-      const uint32_t st = k % kStages, b = k % kSBufs;
-      wait_bar(bars + 8 * (kBarStageFull + st), (k / kStages) & 1, timed_out);
+    for (int j = 0; j < sg.hi - sg.lo; ++j, ++k, ++ks) {
+      const uint32_t st = ks % kStages, b = k % kSBufs;
+      wait_bar(bars + 8 * (kBarStageFull + st), (ks / kStages) & 1, timed_out);
       // S buffer b free: the attention warps have read S of page k - kSBufs, so that page's MMAs
       // and scale copies are complete and staging tile b may be rewritten
       if (k >= kSBufs) wait_bar(bars + 8 * (kBarSFree + b), ((k / kSBufs) - 1) & 1, timed_out);
@@ -334,7 +374,7 @@ __device__ __forceinline__ void s_issue(AttnCtx& c, uint32_t kk, uint32_t (&sr)[
 // the factor for row g of the accumulator). kv_lim: keys of the page below it are real (0 when
 // the page was skipped).
 template <int NR>
-__device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, int page, int len,
+__device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, uint32_t kst, int page, int len,
                                           const RowVis& rv, uint32_t (&sr)[8], float (&m)[kRows],
                                           float (&lp)[kRows], uint32_t pt, int g, float c2,
                                           float& alpha_g, int& kv_lim) {
@@ -342,10 +382,10 @@ __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, int page, int
   tc_fence_before();
   __syncwarp();
   if (c.lane == 0) mbar_arrive(c.bars + 8 * (kBarSFree + kk % kSBufs));
-  const uint32_t st = kk % kStages;
+  const uint32_t st = kst % kStages;
   // the Q.K^T warp saw this stage land; waiting here as well makes the V bytes and the page id
   // visible to this warp (the wait returns at once)
-  wait_bar(c.bars + 8 * (kBarStageFull + st), (kk / kStages) & 1, c.timed_out);
+  wait_bar(c.bars + 8 * (kBarStageFull + st), (kst / kStages) & 1, c.timed_out);
   const bool pvalid = reinterpret_cast<const volatile int32_t*>(c.smem + kOffStagePid)[st] >= 0;
   kv_lim = pvalid ? len - page * 64 : 0;
   if (!c.active) return false;
@@ -467,17 +507,19 @@ struct NewKvRow {
   bool is_k;
 };
 
-__device__ __forceinline__ void new_kv_fetch(const DecodeParams& p, const SegInfo& sg, int ri,
-                                             int t0, int lane, NewKvRow& r) {
+__device__ __forceinline__ void new_kv_fetch(const DecodeParams& p, const SegInfo& sg,
+                                             const uint8_t* slot, int ri, int t0, int lane,
+                                             NewKvRow& r) {
   const int tok = t0 + ri / (2 * p.Hkv), w = ri % (2 * p.Hkv);
   r.is_k = w < p.Hkv;
   r.h = r.is_k ? w : w - p.Hkv;
   r.pos = sg.len - p.q_len + tok;
   r.pid = p.block_table[(int64_t)sg.seq * p.max_pages + r.pos / kPage];
-  r.raw = ldg_nc_u2((r.is_k ? p.k_new : p.v_new) +
-                    (((int64_t)sg.seq * p.q_len + tok) * p.Hkv + r.h) * kHeadDim + 4 * lane);
+  r.raw = *reinterpret_cast<const uint2*>(slot + (r.is_k ? kStepK : kStepV) +
+                                          (tok * p.Hkv + r.h) * 256 + 8 * lane);
   const bool rope = r.is_k && p.rot_dim > 0 && r.pos < p.rope_max_pos;
-  rope_fetch(rope ? p.rope + (int64_t)r.pos * p.rot_dim : nullptr, p.rot_dim, lane, r.c, r.s);
+  rope_fetch(rope ? reinterpret_cast<const float*>(slot + kStepRope) + tok * p.rot_dim : nullptr,
+             p.rot_dim, lane, r.c, r.s);
 }
 
 __device__ __forceinline__ void new_kv_store(const DecodeParams& p, const NewKvRow& r, int lane) {
@@ -513,12 +555,14 @@ __device__ __forceinline__ void new_kv_store(const DecodeParams& p, const NewKvR
 
 // Fused step, per segment, by the attention warps: the segment's Q tile encoded from the bf16
 // rows into shared memory (and, by the first segment of the group, into q_codes_out), and the
-// step's new K/V rows that fall on the segment's pages stored into the pool. Every global load is
-// issued before any arithmetic: while the other CTAs stream the cache, one load takes about a
-// microsecond, and a chain of them would hold back the segment's first QK.
-__device__ __forceinline__ void fused_prologue(const DecodeParams& p, const SegInfo& sg,
-                                               uint8_t* smem, uint32_t sbase, uint32_t bars,
-                                               int aw, int lane) {
+// step's new K/V rows that fall on the segment's pages stored into the pool. The bf16 rows and
+// RoPE rows come from the step slot, which the producer filled ahead of the segment; the one
+// global load left is the page id of a new row (while the other CTAs stream the cache, a global
+// load takes about a microsecond, and the segment's first QK waits for this prologue). Kept out of
+// line: inlined, it made the page loop that follows about 4 % slower (measured).
+__device__ __noinline__ void fused_prologue(const DecodeParams& p, const SegInfo& sg,
+                                               uint8_t* smem, const uint8_t* slot, uint32_t sbase,
+                                               uint32_t bars, int aw, int lane) {
   const int rows_total = p.G * p.q_len;
   const int row0 = sg.rg * kRows;
   const bool q_out = p.q_codes_out != nullptr && (sg.n_seg == 1 || sg.part == sg.first_part);
@@ -544,9 +588,10 @@ __device__ __forceinline__ void fused_prologue(const DecodeParams& p, const SegI
       const bool rope_ok = p.rot_dim == 0 || pos < p.rope_max_pos;
       qstate[jj] = rope_ok ? 2 : 1;
       if (rope_ok) {
-        qraw[jj] = ldg_nc_u2(p.q_new + qtrow[jj] * kHeadDim + 4 * lane);
-        rope_fetch(p.rot_dim > 0 ? p.rope + (int64_t)pos * p.rot_dim : nullptr, p.rot_dim, lane,
-                   qc[jj], qs[jj]);
+        qraw[jj] = *reinterpret_cast<const uint2*>(slot + kStepQ + (tok * p.Hq + qh) * 256 + 8 * lane);
+        rope_fetch(p.rot_dim > 0 ? reinterpret_cast<const float*>(slot + kStepRope) + tok * p.rot_dim
+                                 : nullptr,
+                   p.rot_dim, lane, qc[jj], qs[jj]);
       }
     }
   }
@@ -555,7 +600,7 @@ __device__ __forceinline__ void fused_prologue(const DecodeParams& p, const SegI
   const int t0 = max(0, sg.lo * kPage - first_pos), t1 = min(p.q_len, sg.hi * kPage - first_pos);
   const int nrows = t1 > t0 ? (t1 - t0) * 2 * p.Hkv : 0;
   NewKvRow kv;
-  if (aw < nrows) new_kv_fetch(p, sg, aw, t0, lane, kv);
+  if (aw < nrows) new_kv_fetch(p, sg, slot, aw, t0, lane, kv);
 
   // the four rows in lockstep; a padding row or one past the RoPE table holds zeros and encodes
   // to zero codes and a zero scale
@@ -588,7 +633,7 @@ __device__ __forceinline__ void fused_prologue(const DecodeParams& p, const SegI
   if (aw < nrows) new_kv_store(p, kv, lane);
 #pragma unroll 1
   for (int ri = aw + kAttnWarps; ri < nrows; ri += kAttnWarps) {  // more than 8 new rows
-    new_kv_fetch(p, sg, ri, t0, lane, kv);
+    new_kv_fetch(p, sg, slot, ri, t0, lane, kv);
     new_kv_store(p, kv, lane);
   }
   // the pool rows visible to this CTA's bulk copies (async proxy) before the producer copies their
@@ -632,7 +677,7 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
   const int vk0 = 4 * t + (t & 1), vk1 = 4 * t + 1 - (t & 1);
   const int rows_total = p.G * p.q_len;
   const float c2 = p.c2;
-  uint32_t k = 0;
+  uint32_t k = 0, ks = 0;  // pages (S buffers), stage slots
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
 
   for (int s = s_begin; s < s_end; ++s) {
@@ -652,7 +697,11 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
 
     // ---- this pair's Q tile (B operand of Q.K^T) and its scale factors ----
     if (FUSED) {
-      fused_prologue(p, sg, smem, c.sbase, c.bars, aw, lane);
+      const uint32_t st = ks % kStages;
+      wait_bar(c.bars + 8 * (kBarStageFull + st), (ks / kStages) & 1, c.timed_out);
+      fused_prologue(p, sg, smem, smem + kOffStage + st * kStageBytes, c.sbase, c.bars, aw, lane);
+      if (lane == 0) mbar_arrive(c.bars + 8 * (kBarStageEmpty + st));  // slot read by this warp
+      ++ks;
     } else if (c.gt < 64) {
       const int nrow = c.gt >> 2, ch = c.gt & 3;
       const int hh = 2 * c.pr + (nrow >> 3), r = row0 + (nrow & 7);
@@ -706,13 +755,14 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
     // Per page: scores -> running max, row sums and P (one P tile), accumulator rescale when a
     // max grew, then two 16-key steps of O += P V.
     const RowVis rv{mylim, lim_min, rows_mask};
-    for (int j = 0; j < n; ++j, ++k) {
-      const uint32_t st = k % kStages;
+    for (int j = 0; j < n; ++j, ++k, ++ks) {
+      const uint32_t st = ks % kStages;
       uint32_t sr[8];
       float alpha_g = 1.f;
       int kv_lim = 0;
       s_issue(c, k, sr);
-      const bool grow = s_softmax<NR>(c, k, sg.lo + j, sg.len, rv, sr, m, lp, ps, g, c2, alpha_g, kv_lim);
+      const bool grow =
+          s_softmax<NR>(c, k, ks, sg.lo + j, sg.len, rv, sr, m, lp, ps, g, c2, alpha_g, kv_lim);
       __syncwarp();
       if (grow) {
 #pragma unroll
@@ -848,7 +898,7 @@ __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodePa
   if (warp == kWarpProducer) {
     producer<FUSED>(p, smem, lane);
   } else if (warp == kWarpMma) {
-    qk_warp(p, smem, tbase, lane);
+    qk_warp<FUSED>(p, smem, tbase, lane);
   } else {
     attention_warps<NR, FUSED>(p, smem, tbase, warp, lane);
   }
