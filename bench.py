@@ -134,7 +134,7 @@ def measured_peaks():
 def decode_traffic_profile():
     """DRAM bytes per step launch from the committed ncu summary, if it was taken on the
     current kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", "decode_attn_steady_decode.json")
+    p = os.path.join(ROOT, "profiles", "decode_step_steady_decode.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
