@@ -7,6 +7,8 @@ of ``bench.py`` do. The oracle shares no code with the CUDA path.
 Every function states the page passage it restates:
   [NVFP4] prismix.dev/news/833001997676, section "NVFP4 KV cache (from scratch)".
   [YaRN]  prismix.dev/news/833001997676, section "YaRN context extension".
+  [Spill] prismix.dev/news/833001997676, section "Multi-level prefix reuse with host-KV safety
+          net".
 """
 from __future__ import annotations
 
@@ -87,6 +89,10 @@ def _declare(L):
               "orc_bytes_per_token_head_bf16"):
         getattr(L, n).argtypes = [_I32]
         getattr(L, n).restype = _I32
+    L.orc_spill_pages.argtypes = [_P, _I32, _I32, _P, _I32, _P]
+    L.orc_spill_pages.restype = _I64
+    L.orc_restore_pages.argtypes = [_P, _I32, _I32, _P, _I32, _P]
+    L.orc_restore_pages.restype = _I64
     L.orc_num_threads.argtypes = []
     L.orc_num_threads.restype = _I32
 
@@ -187,6 +193,27 @@ def paged_gather(pool, num_pages, kv_heads, block_table, seq, pos0, n_tok):
     bad = lib().orc_paged_gather(_ptr(pl), num_pages, kv_heads, _ptr(bt), bt.shape[1], seq, pos0,
                                  n_tok, _ptr(kc), _ptr(ks), _ptr(vc), _ptr(vs))
     return kc, ks, vc, vs, int(bad)
+
+
+def spill_pages(pool, num_pages, kv_heads, page_ids, arena):
+    """[Spill] arena slot i <- pool page page_ids[i] (whole page blocks); a page id outside the
+    pool is skipped, its slot left as it was. Writes into `arena` in place; returns the number of
+    skipped ids."""
+    pl = np.ascontiguousarray(pool, dtype=np.uint8)
+    ids = np.ascontiguousarray(page_ids, dtype=np.int32)
+    assert arena.dtype == np.uint8 and arena.flags.c_contiguous
+    return int(lib().orc_spill_pages(_ptr(pl), num_pages, kv_heads, _ptr(ids), len(ids),
+                                     _ptr(arena)))
+
+
+def restore_pages(pool, num_pages, kv_heads, page_ids, arena):
+    """[Spill] pool page page_ids[i] <- arena slot i; a page id outside the pool is skipped.
+    Writes into `pool` in place; returns the number of skipped ids."""
+    ar = np.ascontiguousarray(arena, dtype=np.uint8)
+    ids = np.ascontiguousarray(page_ids, dtype=np.int32)
+    assert pool.dtype == np.uint8 and pool.flags.c_contiguous
+    return int(lib().orc_restore_pages(_ptr(pool), num_pages, kv_heads, _ptr(ids), len(ids),
+                                       _ptr(ar)))
 
 
 def attention_rows(q_heads, kv_heads, q_len, causal, sm_scale, seq_lens, tok_off,

@@ -380,6 +380,52 @@ void orc_attention_ref_rows(int32_t q_heads, int32_t kv_heads, int32_t q_len, in
 // Storage cost per token per KV head for head_dim 128 [NVFP4 "Result"]: NVFP4 = codes + E4M3
 // scales for K and for V; int8 = 128 bytes + one fp32 scale, for K and V; bf16 = 2 bytes/elem.
 // ---------------------------------------------------------------------------------------------
+// ---------------------------------------------------------------------------------------------
+// Page spill and restore (prismix.dev/news/833001997676, section "Multi-level prefix reuse with
+// host-KV safety net": cache pages copied out to host memory and copied back when needed). A page
+// block holds every KV head's K and V codes and scales for its 64 slots, so moving a page is a
+// byte copy of the whole block: per head, 64 slots x (64 code bytes + 8 scale bytes) for K and the
+// same for V.
+//   spill:   arena slot i  <- pool page page_ids[i]
+//   restore: pool page page_ids[i] <- arena slot i
+// A page id outside [0, num_pages) is counted and its copy skipped (the destination is left as it
+// was). Returns the number of skipped ids.
+// ---------------------------------------------------------------------------------------------
+static int64_t orc_page_block_bytes(int32_t kv_heads) {
+  const int64_t slot_bytes = 128 / 2 + 128 / 16;  // E2M1 codes + E4M3 scales of one row
+  return (int64_t)kv_heads * 2 * 64 * slot_bytes;
+}
+
+int64_t orc_spill_pages(const uint8_t* pool, int32_t num_pages, int32_t kv_heads,
+                        const int32_t* page_ids, int32_t n, uint8_t* arena) {
+  const int64_t pb = orc_page_block_bytes(kv_heads);
+  int64_t bad = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t id = page_ids[i];
+    if (id < 0 || id >= num_pages) {
+      ++bad;
+      continue;
+    }
+    std::memcpy(arena + (int64_t)i * pb, pool + (int64_t)id * pb, (size_t)pb);
+  }
+  return bad;
+}
+
+int64_t orc_restore_pages(uint8_t* pool, int32_t num_pages, int32_t kv_heads,
+                          const int32_t* page_ids, int32_t n, const uint8_t* arena) {
+  const int64_t pb = orc_page_block_bytes(kv_heads);
+  int64_t bad = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t id = page_ids[i];
+    if (id < 0 || id >= num_pages) {
+      ++bad;
+      continue;
+    }
+    std::memcpy(pool + (int64_t)id * pb, arena + (int64_t)i * pb, (size_t)pb);
+  }
+  return bad;
+}
+
 int32_t orc_bytes_per_token_head_nvfp4(int32_t head_dim) { return 2 * (head_dim / 2 + head_dim / 16); }
 int32_t orc_bytes_per_token_head_int8(int32_t head_dim) { return 2 * (head_dim + 4); }
 int32_t orc_bytes_per_token_head_bf16(int32_t head_dim) { return 2 * head_dim * 2; }
