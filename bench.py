@@ -250,6 +250,52 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def spill_restore(g, dev, stream, reps=5):
+    """Page spill and restore of every page the cache uses (8196 pages, 302 MB) to and from a
+    page-locked host arena, against a plain contiguous copy of the same bytes over the same link.
+    The restore writes each page back to its own id, so the cache is unchanged."""
+    import numpy as np
+    import torch
+
+    import bit_kv_cache_03_gb300 as kv
+    c = g.cache
+    w = g.w
+    bt = c.block_table.cpu().numpy()
+    used = np.concatenate([bt[s, :(int(w.seq_lens[s]) + 63) // 64] for s in range(w.num_seqs)])
+    n = len(used)
+    pb = kv.kv_nvfp4_page_bytes(c.layout)
+    ids = torch.from_numpy(used.astype(np.int32)).to(dev)
+    arena = torch.empty(n * pb, dtype=torch.uint8).pin_memory()
+    scratch = torch.empty(n * pb, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / 1e3 / reps
+
+    t_spill = timed(lambda: kv.kv_nvfp4_spill_pages(c.layout, c.pool, c.num_pages, ids, n, arena,
+                                                    c.status))
+    t_restore = timed(lambda: kv.kv_nvfp4_restore_pages(c.layout, arena, ids, n, c.pool,
+                                                        c.num_pages, c.status))
+    t_d2h = timed(lambda: arena.copy_(scratch, non_blocking=True))
+    t_h2d = timed(lambda: scratch.copy_(arena, non_blocking=True))
+    assert g.status() == 0, f"device status {g.status():#x}"
+    b = n * pb
+    return {"pages": n, "bytes": b,
+            "spill_pages_per_s": n / t_spill, "spill_gbs": b / t_spill / 1e9,
+            "restore_pages_per_s": n / t_restore, "restore_gbs": b / t_restore / 1e9,
+            "copy_d2h_gbs": b / t_d2h / 1e9, "copy_h2d_gbs": b / t_h2d / 1e9,
+            "spill_frac_of_copy": t_d2h / t_spill, "restore_frac_of_copy": t_h2d / t_restore,
+            "note": "scattered pool pages <-> page-locked host arena by one kernel launch; copy = "
+                    "one contiguous cudaMemcpyAsync of the same bytes"}
+
+
 def run_cuda(args, world, rank, local):
     import numpy as np
     import torch
@@ -379,6 +425,8 @@ def run_cuda(args, world, rank, local):
     torch.cuda.synchronize(dev)
     e2e_elapsed = time.perf_counter() - t0
 
+    spill = spill_restore(g, dev, stream)
+
     elapsed, e2e_elapsed = max_over_ranks([elapsed, e2e_elapsed], dev)
     if rank != 0:
         return
@@ -427,6 +475,7 @@ def run_cuda(args, world, rank, local):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "includes": "pinned H2D of new Q/K/V, plan upload, step call, D2H of output"},
         "gpu_launches": 2 * args.steps,  # per timed step: the attention kernel, split-K merge
+        "spill": spill,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(w)

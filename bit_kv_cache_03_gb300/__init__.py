@@ -73,6 +73,8 @@ _SIG = {
                               _I32, _P, _I32, _I32, _P, _P, _P, ctypes.c_float, _P, _P, _P], _I32),
     "kv_nvfp4_decode_attn_noalloc": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32, _P, _P,
                                       ctypes.c_float, _P, _I32, _P, _I32, _P, _P, _P], _I32),
+    "kv_nvfp4_spill_pages": ([ctypes.POINTER(Layout), _P, _I32, _P, _I32, _P, _P, _P], _I32),
+    "kv_nvfp4_restore_pages": ([ctypes.POINTER(Layout), _P, _P, _I32, _P, _I32, _P, _P], _I32),
 }
 
 _lib = None
@@ -239,6 +241,22 @@ def kv_nvfp4_decode_step(layout, plan: PlanInfo, workspace, q, k, v, rope, rope_
         _ptr(rope), rope_max_pos, _ptr(block_table), max_pages, num_pages, _ptr(pool),
         _ptr(q_codes_out), _ptr(q_scales_out), float(sm_scale), _ptr(out), _ptr(status),
         _stream(stream)), "kv_nvfp4_decode_step")
+
+
+def kv_nvfp4_spill_pages(layout, pool, num_pages, page_ids, n, arena, status=None, stream=None):
+    """Arena slot i <- pool page page_ids[i] (page_ids on the device; arena page-locked host
+    memory or device memory, n page blocks)."""
+    _check(lib().kv_nvfp4_spill_pages(ctypes.byref(layout), _ptr(pool), num_pages, _ptr(page_ids),
+                                      n, _ptr(arena), _ptr(status), _stream(stream)),
+           "kv_nvfp4_spill_pages")
+
+
+def kv_nvfp4_restore_pages(layout, arena, page_ids, n, pool, num_pages, status=None,
+                           stream=None):
+    """Pool page page_ids[i] <- arena slot i."""
+    _check(lib().kv_nvfp4_restore_pages(ctypes.byref(layout), _ptr(arena), _ptr(page_ids), n,
+                                        _ptr(pool), num_pages, _ptr(status), _stream(stream)),
+           "kv_nvfp4_restore_pages")
 
 
 def kv_nvfp4_decode_attn_noalloc(layout, seq_lens, q_len, causal, chunk_tokens, q_codes, q_scales,

@@ -29,6 +29,9 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
                           const uint16_t* v_new, const float* rope, int32_t rope_max_pos,
                           int32_t rot_dim, uint8_t* pool_w, uint8_t* q_codes_out,
                           uint8_t* q_scales_out, cudaStream_t stream);
+cudaError_t launch_page_copy(bool spill, const uint8_t* src, uint8_t* dst, const int32_t* ids,
+                             int32_t n, int32_t num_pages, uint32_t page_bytes, int sms,
+                             int32_t* status, cudaStream_t stream);
 }  // namespace kvnvfp4
 
 namespace {
@@ -207,6 +210,51 @@ void rope_fill(float* t, int32_t max_pos, int32_t rot_dim, double theta, double 
 
 }  // namespace
 
+// ---- page spill / restore ----------------------------------------------------------------------
+namespace {
+
+// Device address of an arena: page-locked host memory (its mapped device address) or device
+// memory. Pageable host memory, which the GPU cannot address on every system, is refused.
+kv_nvfp4_status arena_device_address(const void* arena, const void** dev) {
+  cudaPointerAttributes a{};
+  const cudaError_t e = cudaPointerGetAttributes(&a, arena);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // the query's error is not a launch error: do not leave it set
+    return e == cudaErrorInvalidValue ? KV_NVFP4_EINVAL : cuda_status(e);
+  }
+  if (a.type == cudaMemoryTypeHost) {
+    if (a.devicePointer == nullptr) return KV_NVFP4_EINVAL;
+    *dev = a.devicePointer;
+    return KV_NVFP4_OK;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *dev = arena;
+    return KV_NVFP4_OK;
+  }
+  return KV_NVFP4_EINVAL;  // cudaMemoryTypeUnregistered: pageable host memory
+}
+
+kv_nvfp4_status page_copy(const kv_nvfp4_layout* L, bool spill, const uint8_t* pool,
+                          int32_t num_pages, const int32_t* d_page_ids, int32_t n,
+                          const uint8_t* arena, int32_t* d_status, void* stream) {
+  if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || n < 0) return KV_NVFP4_EINVAL;
+  if (n == 0) return KV_NVFP4_OK;
+  if (!pool || !arena || !d_page_ids || num_pages <= 0 || !aligned16(pool) || !aligned16(arena))
+    return KV_NVFP4_EINVAL;
+  const void* arena_dev = nullptr;
+  const kv_nvfp4_status s = arena_device_address(arena, &arena_dev);
+  if (s != KV_NVFP4_OK) return s;
+  const int sms = num_sms_current_device();
+  if (sms <= 0) return cuda_status(cudaErrorNoDevice);
+  const uint32_t pb = (uint32_t)kv_nvfp4_page_bytes(L);
+  const uint8_t* a = static_cast<const uint8_t*>(arena_dev);
+  return cuda_status(kvnvfp4::launch_page_copy(
+      spill, spill ? pool : a, spill ? const_cast<uint8_t*>(a) : const_cast<uint8_t*>(pool),
+      d_page_ids, n, num_pages, pb, sms, d_status, (cudaStream_t)stream));
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* kv_nvfp4_status_string(kv_nvfp4_status s) {
@@ -222,6 +270,19 @@ const char* kv_nvfp4_status_string(kv_nvfp4_status s) {
 int32_t kv_nvfp4_version(void) { return 10000; }
 
 const char* kv_nvfp4_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda_error); }
+
+// ---- page spill / restore ----------------------------------------------------------------------
+kv_nvfp4_status kv_nvfp4_spill_pages(const kv_nvfp4_layout* layout, const uint8_t* pool,
+                                     int32_t num_pages, const int32_t* d_page_ids, int32_t n,
+                                     uint8_t* arena, int32_t* d_status, void* stream) {
+  return page_copy(layout, true, pool, num_pages, d_page_ids, n, arena, d_status, stream);
+}
+
+kv_nvfp4_status kv_nvfp4_restore_pages(const kv_nvfp4_layout* layout, const uint8_t* arena,
+                                       const int32_t* d_page_ids, int32_t n, uint8_t* pool,
+                                       int32_t num_pages, int32_t* d_status, void* stream) {
+  return page_copy(layout, false, pool, num_pages, d_page_ids, n, arena, d_status, stream);
+}
 
 kv_nvfp4_status kv_nvfp4_layout_check(const kv_nvfp4_layout* L) {
   if (L == nullptr) return KV_NVFP4_EINVAL;

@@ -246,6 +246,31 @@ kv_nvfp4_status kv_nvfp4_decode_step(const kv_nvfp4_layout *layout,
                                      uint8_t *q_scales_out, float sm_scale, float *out,
                                      int32_t *d_status, void *stream);
 
+/* ---- Page spill and restore [Spill: cache pages moved out to host memory and back] ----------
+ * prismix.dev/news/833001997676, section "Multi-level prefix reuse with host-KV safety net".
+ * kv_nvfp4_spill_pages:   arena slot i <- pool page d_page_ids[i], for i < n
+ * kv_nvfp4_restore_pages: pool page d_page_ids[i] <- arena slot i
+ * A page block (kv_nvfp4_page_bytes: every KV head's K and V codes and scales of 64 slots) is
+ * self-contained, so a page moves as one byte copy; a restored page may take another page id than
+ * it had, with the block table renamed to match.
+ *   pool:        DEVICE, num_pages page blocks (kv_nvfp4_pool_bytes), 16-byte aligned
+ *   d_page_ids:  DEVICE int32 [n]; an id outside [0, num_pages) sets KV_NVFP4_DEV_BAD_PAGE and its
+ *                copy is skipped (the arena slot, or the pool page, is left as it was). Restore
+ *                ids should be distinct: a repeated id leaves that page holding one of its slots.
+ *   arena:       n * kv_nvfp4_page_bytes bytes, 16-byte aligned, in memory the GPU can address:
+ *                page-locked host memory (cudaHostAlloc, cudaMallocHost, cudaHostRegister: the
+ *                GPU's own loads and stores reach it over the host link) or device memory.
+ *                Pageable host memory is refused with KV_NVFP4_EINVAL.
+ * One kernel launch on `stream`, asynchronous: the caller keeps pool, ids and arena alive, and
+ * does not touch the arena's slots, until the stream has passed the call. n = 0 does nothing.
+ * EINVAL for a bad layout, n < 0, a null or misaligned buffer, or num_pages <= 0. */
+kv_nvfp4_status kv_nvfp4_spill_pages(const kv_nvfp4_layout *layout, const uint8_t *pool,
+                                     int32_t num_pages, const int32_t *d_page_ids, int32_t n,
+                                     uint8_t *arena, int32_t *d_status, void *stream);
+kv_nvfp4_status kv_nvfp4_restore_pages(const kv_nvfp4_layout *layout, const uint8_t *arena,
+                                       const int32_t *d_page_ids, int32_t n, uint8_t *pool,
+                                       int32_t num_pages, int32_t *d_status, void *stream);
+
 /* ---- Decode attention without caller-provided device memory ----------------------------------
  * No counterpart in the pages: an addition of this library for callers that cannot allocate
  * device memory, such as an inference engine that reserves all of the GPU's memory for its own

@@ -157,3 +157,23 @@ def test_plan_covers_every_visible_page_once_and_balances(kv, lens, q_len, causa
     assert np.array_equal(split, np.flatnonzero(groups[:, 4] > 1))
     assert info.num_split_groups == len(split)
     assert info.off_split % 16 == 0 and info.off_partials % 16 == 0
+
+
+def test_spill_restore_reject_bad_arguments_before_cuda(kv):
+    lib = kv.lib()
+    L = kv.make_layout()
+    OK, EINVAL = kv.KV_NVFP4_OK, kv.KV_NVFP4_EINVAL
+    # no pages: nothing to do, no buffer needed
+    assert lib.kv_nvfp4_spill_pages(ctypes.byref(L), None, 1, None, 0, None, None, None) == OK
+    assert lib.kv_nvfp4_restore_pages(ctypes.byref(L), None, None, 0, None, 1, None, None) == OK
+    # negative count, null buffers, misaligned arena or pool, empty pool, bad layout
+    assert lib.kv_nvfp4_spill_pages(ctypes.byref(L), 256, 4, 512, -1, 768, None, None) == EINVAL
+    assert lib.kv_nvfp4_spill_pages(ctypes.byref(L), None, 4, 512, 2, 768, None, None) == EINVAL
+    assert lib.kv_nvfp4_spill_pages(ctypes.byref(L), 256, 4, None, 2, 768, None, None) == EINVAL
+    assert lib.kv_nvfp4_spill_pages(ctypes.byref(L), 256, 4, 512, 2, None, None, None) == EINVAL
+    assert lib.kv_nvfp4_spill_pages(ctypes.byref(L), 256, 4, 512, 2, 777, None, None) == EINVAL
+    assert lib.kv_nvfp4_spill_pages(ctypes.byref(L), 260, 4, 512, 2, 768, None, None) == EINVAL
+    assert lib.kv_nvfp4_spill_pages(ctypes.byref(L), 256, 0, 512, 2, 768, None, None) == EINVAL
+    assert lib.kv_nvfp4_restore_pages(ctypes.byref(L), 776, 512, 2, 256, 4, None, None) == EINVAL
+    bad = kv.Layout(24, 4, 64, 64, 32)
+    assert lib.kv_nvfp4_restore_pages(ctypes.byref(bad), 768, 512, 2, 256, 4, None, None) == EINVAL
