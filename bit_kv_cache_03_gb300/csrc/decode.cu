@@ -27,13 +27,14 @@
 // sums and O accumulator; the two warps of a head merge once, at the end of a segment. Per page a
 // warp reads its S slice from TMEM (one key per lane), takes the page max per row with warp
 // reductions, rescales its accumulator when a max grows, and writes P = exp2((s - m) log2e scale)
-// <= 1 as an f16 hi + lo pair to a private shared tile. The P.V product runs on the warp-level
-// tensor path (mma.sync m16n8k16, f32 accumulate) with the query rows as M (rows 0..7 P hi, rows
-// 8..15 P lo, so the pair costs nothing extra), 16 keys as K and 8 head dims as N. P comes in
-// with transposing ldmatrix; V goes from its E2M1 codes straight into B fragments: the nibbles of
-// two keys are interleaved into one byte per dim, converted with cvt.e2m1x2 and multiplied by the
-// two keys' E4M3 scales (E2M1 x E4M3 is exact in f16). Within a 16-key step the keys are taken in
-// a fixed permutation, the same for P and V, that keeps the shared-memory reads conflict-free.
+// <= 1 in f16 to a private shared tile (f16 keeps 11 significant bits of P; the method's own P.V
+// runs in bf16, with 8). The P.V product runs on the warp-level tensor path (mma.sync m16n8k16,
+// f32 accumulate) with the query rows as M (rows 0..7; rows 8..15 read the tile's zeroed second
+// half), 16 keys as K and 8 head dims as N. P comes in with transposing ldmatrix; V goes from its
+// E2M1 codes straight into B fragments: the nibbles of two keys are interleaved into one byte per
+// dim, converted with cvt.e2m1x2 and multiplied by the two keys' E4M3 scales (E2M1 x E4M3 is
+// exact in f16). Within a 16-key step the keys are taken in a fixed permutation, the same for P
+// and V, that keeps the shared-memory reads conflict-free.
 //
 // Warp roles (320 threads): warp 0 bulk-copy producer, warp 1 Q.K^T issuer and TMEM owner, warps
 // 2..9 attention. Every wait is an mbarrier wait bounded in time; on a timeout the kernel records
@@ -338,9 +339,11 @@ struct AttnCtx {
   bool timed_out;
 };
 
-// Byte address of the hi (half 0) or lo (half 1) P row of warp-local key `key` in a warp's P tile:
-// four keys per 128-byte line, the 32-byte slots and 16-byte halves permuted by line so that both
-// the row stores and the transposing ldmatrix reads are free of bank conflicts.
+// Byte address of the P row (half 0) or of the always-zero row (half 1) of warp-local key `key`
+// in a warp's P tile: four keys per 128-byte line, the 32-byte slots and 16-byte halves permuted
+// by line so that both the row stores and the transposing ldmatrix reads are free of bank
+// conflicts. (Reading the zero half with the same x4 ldmatrix measured faster than loading only
+// the P half and passing zero registers to the MMA.)
 __device__ __forceinline__ uint32_t p_addr(uint32_t base, int key, int half) {
   const int q = key >> 2;
   return base + q * 128 + 32 * ((key & 3) ^ (q & 3)) + 16 * (half ^ (q & 1));
@@ -370,7 +373,7 @@ __device__ __forceinline__ void s_issue(AttnCtx& c, uint32_t kk, uint32_t (&sr)[
 
 // Finish loading page kk's scores, release the S buffer, and turn the scores into P in the P tile
 // at pt: page max per row over the warp's 32 keys (warp reductions), running max and row-sum
-// update, P = exp2((s - m) c2) <= 1 as f16 hi + lo. Returns whether a max grew (then alpha_g is
+// update, P = exp2((s - m) c2) <= 1 in f16. Returns whether a max grew (then alpha_g is
 // the factor for row g of the accumulator). kv_lim: keys of the page below it are real (0 when
 // the page was skipped).
 template <int NR>
@@ -421,7 +424,7 @@ __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, uint32_t kst,
     }
     alpha_g = pick8(alpha, g);
   }
-  uint32_t hi[4], lo[4];
+  uint32_t hi[4];
 #pragma unroll
   for (int i = 0; i < kRows; i += 2) {
     const float p0 = (i < NR && ((vmask >> i) & 1u))
@@ -431,10 +434,8 @@ __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, uint32_t kst,
     lp[i] += p0;
     lp[i + 1] += p1;
     hi[i / 2] = pack_f16x2(p0, p1);
-    lo[i / 2] = pack_f16x2(p0 - f16_lo_to_f32(hi[i / 2]), p1 - f16_hi_to_f32(hi[i / 2]));
   }
   sts128(p_addr(pt, c.lane, 0), hi[0], hi[1], hi[2], hi[3]);
-  sts128(p_addr(pt, c.lane, 1), lo[0], lo[1], lo[2], lo[3]);
   return grow;
 }
 
@@ -663,7 +664,7 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
   c.timed_out = false;
   const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates
   const uint32_t ps = c.sbase + kOffPs + aw * kPsBytes;
-  // ldmatrix rows of this lane: matrix mi = lane / 8 is (P hi | P lo) x (k 0..7 | k 8..15); the
+  // ldmatrix rows of this lane: matrix mi = lane / 8 is (P | zero) x (k 0..7 | k 8..15); the
   // fragment k index maps to a warp-local key by the permutation below (also used for V)
   uint32_t lm_addr0, lm_addr1;
   {
@@ -677,6 +678,8 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
   const int vk0 = 4 * t + (t & 1), vk1 = 4 * t + 1 - (t & 1);
   const int rows_total = p.G * p.q_len;
   const float c2 = p.c2;
+  sts128(p_addr(ps, lane, 1), 0u, 0u, 0u, 0u);  // rows 8..15 of every P.V product: zero
+  __syncwarp();
   uint32_t k = 0, ks = 0;  // pages (S buffers), stage slots
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
 
@@ -745,7 +748,7 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
 #pragma unroll
     for (int i = 0; i < kRows; ++i) { m[i] = -INFINITY; lp[i] = 0.f; }
     // O accumulator: acc[dd] is the m16n8 tile of dims 16 n + dd (n = fragment column); rows
-    // 0..7 take P hi, rows 8..15 P lo
+    // 0..7 are the query rows, rows 8..15 stay zero
     float acc[16][4];
 #pragma unroll
     for (int dd = 0; dd < 16; ++dd)
@@ -792,7 +795,8 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
     const int part_stride = p.Hkv * kPartHeadFloats;
     if (c.active) {
       // lane (g, t) holds row g, dims 32 t .. 32 t + 31: value v < 16 is tile v column 2t (dim
-      // 32 t + v), v >= 16 is tile v - 16 column 2t + 1 (dim 32 t + v); hi and lo rows summed
+      // 32 t + v), v >= 16 is tile v - 16 column 2t + 1 (dim 32 t + v); rows g and g + 8 (zero)
+      // summed
       const uint32_t mg = c.sbase + kOffMerge + c.head * kMergeHeadBytes;
       volatile float* mml =
           reinterpret_cast<volatile float*>(smem + kOffMerge + c.head * kMergeHeadBytes + 8 * 32 * 16);

@@ -223,17 +223,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
-__device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) {
-  float f;
-  asm("{\n.reg .b16 l, h;\nmov.b32 {l, h}, %1;\ncvt.f32.f16 %0, l;\n}" : "=f"(f) : "r"(h2));
-  return f;
-}
-__device__ __forceinline__ float f16_hi_to_f32(uint32_t h2) {
-  float f;
-  asm("{\n.reg .b16 l, h;\nmov.b32 {l, h}, %1;\ncvt.f32.f16 %0, h;\n}" : "=f"(f) : "r"(h2));
-  return f;
-}
-
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
