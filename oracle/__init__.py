@@ -89,6 +89,21 @@ def _declare(L):
               "orc_bytes_per_token_head_bf16"):
         getattr(L, n).argtypes = [_I32]
         getattr(L, n).restype = _I32
+    L.orc_float_to_bf16.argtypes = [ctypes.c_float]
+    L.orc_float_to_bf16.restype = ctypes.c_uint16
+    L.orc_float_to_f16.argtypes = [ctypes.c_float]
+    L.orc_float_to_f16.restype = ctypes.c_uint16
+    L.orc_f16_to_double.argtypes = [ctypes.c_uint16]
+    L.orc_f16_to_double.restype = ctypes.c_double
+    L.orc_int8_quantize_row.argtypes = [_P, _P, _P]
+    L.orc_cmp_row_bytes.argtypes = [_I32, _I32]
+    L.orc_cmp_row_bytes.restype = _I32
+    L.orc_cmp_encode_rows.argtypes = [_I32, _I32, _P, _I64, _P, _P, _I32, _P]
+    L.orc_cmp_decode_rows.argtypes = [_I32, _I32, _P, _I64, _P]
+    L.orc_cmp_paged_gather.argtypes = [_I32, _P, _I32, _I32, _P, _I32, _I32, _I32, _I32, _P, _P]
+    L.orc_cmp_paged_gather.restype = _I64
+    L.orc_attention_f64_rows.argtypes = [_I32, _I32, _I32, _I32, _F64, _P, _P, _P, _P, _P, _I64,
+                                         _P, _P, _P, _P, _I32]
     L.orc_spill_pages.argtypes = [_P, _I32, _I32, _P, _I32, _P]
     L.orc_spill_pages.restype = _I64
     L.orc_restore_pages.argtypes = [_P, _I32, _I32, _P, _I32, _P]
@@ -193,6 +208,83 @@ def paged_gather(pool, num_pages, kv_heads, block_table, seq, pos0, n_tok):
     bad = lib().orc_paged_gather(_ptr(pl), num_pages, kv_heads, _ptr(bt), bt.shape[1], seq, pos0,
                                  n_tok, _ptr(kc), _ptr(ks), _ptr(vc), _ptr(vs))
     return kc, ks, vc, vs, int(bad)
+
+
+# ---- comparator formats [NVFP4 "Result": 144 B vs int8 264 B vs bf16 512 B; upstream NVFP4 K with
+# fp16 V]; fmt 0 = bf16, 1 = int8, 2 = NVFP4 K + fp16 V; kind 0 = Q, 1 = K, 2 = V ----
+CMP_FORMATS = {"bf16": 0, "int8": 1, "k4v16": 2}
+
+
+def float_to_bf16(x: float) -> int:
+    return int(lib().orc_float_to_bf16(float(x)))
+
+
+def float_to_f16(x: float) -> int:
+    return int(lib().orc_float_to_f16(float(x)))
+
+
+def f16_to_double(h: int) -> float:
+    return float(lib().orc_f16_to_double(int(h)))
+
+
+def int8_quantize_row(x: np.ndarray):
+    """Per-row symmetric int8: returns (codes int8 [128], fp32 scale)."""
+    xr = np.ascontiguousarray(x, np.float32)
+    codes = np.empty(128, np.int8)
+    sc = np.empty(1, np.float32)
+    lib().orc_int8_quantize_row(_ptr(xr), _ptr(codes), _ptr(sc))
+    return codes, float(sc[0])
+
+
+def cmp_row_bytes(fmt: int, kind: int) -> int:
+    return int(lib().orc_cmp_row_bytes(fmt, kind))
+
+
+def cmp_encode_rows(fmt, kind, rows_bf16, pos, table, rot_dim) -> np.ndarray:
+    """Comparator row encoding (see kv_oracle.cpp): [n][row bytes] uint8."""
+    r = np.ascontiguousarray(rows_bf16, np.uint16).reshape(-1, 128)
+    n = r.shape[0]
+    p = np.ascontiguousarray(np.broadcast_to(np.asarray(pos if pos is not None else 0, np.int32), (n,)))
+    tbl = np.ascontiguousarray(table if table is not None else np.zeros(1), np.float32)
+    out = np.empty((n, cmp_row_bytes(fmt, kind)), np.uint8)
+    lib().orc_cmp_encode_rows(fmt, kind, _ptr(r), n, _ptr(p), _ptr(tbl), rot_dim, _ptr(out))
+    return out
+
+
+def cmp_decode_rows(fmt, kind, rows: np.ndarray) -> np.ndarray:
+    r = np.ascontiguousarray(rows, np.uint8).reshape(-1, cmp_row_bytes(fmt, kind))
+    out = np.empty((r.shape[0], 128), np.float64)
+    lib().orc_cmp_decode_rows(fmt, kind, _ptr(r), r.shape[0], _ptr(out))
+    return out
+
+
+def cmp_paged_gather(fmt, pool, num_pages, kv_heads, block_table, seq, pos0, n_tok):
+    """Rows of one sequence out of a comparator pool: (k_rows [n,H,kb], v_rows [n,H,vb], bad)."""
+    pl = np.ascontiguousarray(pool, dtype=np.uint8)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    k = np.empty((n_tok, kv_heads, cmp_row_bytes(fmt, 1)), np.uint8)
+    v = np.empty((n_tok, kv_heads, cmp_row_bytes(fmt, 2)), np.uint8)
+    bad = lib().orc_cmp_paged_gather(fmt, _ptr(pl), num_pages, kv_heads, _ptr(bt), bt.shape[1],
+                                     seq, pos0, n_tok, _ptr(k), _ptr(v))
+    return k, v, int(bad)
+
+
+def attention_f64_rows(q_heads, kv_heads, q_len, causal, sm_scale, seq_lens, tok_off, q, k, v,
+                       row_seq, row_tok, row_head, nthreads: int = 0) -> np.ndarray:
+    """fp64 attention over decoded rows (q [rows][128], k / v [tokens * kv_heads][128])."""
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    to = np.ascontiguousarray(tok_off, np.int64)
+    rs = np.ascontiguousarray(row_seq, np.int32)
+    rt = np.ascontiguousarray(row_tok, np.int32)
+    rh = np.ascontiguousarray(row_head, np.int32)
+    qq = np.ascontiguousarray(q, np.float64)
+    kk = np.ascontiguousarray(k, np.float64)
+    vv = np.ascontiguousarray(v, np.float64)
+    out = np.empty((rs.shape[0], 128), np.float32)
+    lib().orc_attention_f64_rows(q_heads, kv_heads, q_len, int(causal), sm_scale, _ptr(sl),
+                                 _ptr(to), _ptr(qq), _ptr(kk), _ptr(vv), rs.shape[0], _ptr(rs),
+                                 _ptr(rt), _ptr(rh), _ptr(out), nthreads)
+    return out
 
 
 def spill_pages(pool, num_pages, kv_heads, page_ids, arena):

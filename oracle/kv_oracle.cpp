@@ -426,6 +426,228 @@ int64_t orc_restore_pages(uint8_t* pool, int32_t num_pages, int32_t kv_heads,
   return bad;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Comparator formats (prismix.dev/news/833001997676, section "NVFP4 KV cache (from scratch)": the
+// 144-byte NVFP4 row against 264 bytes for int8 and 512 for bf16, and the upstream variant with
+// NVFP4 K and fp16 V, no Hadamard rotation). Readings, for the comparators only:
+//   fmt 0 (bf16):  K = bf16(RoPE(k)), V = v (bf16 as given)                    512 B/token/head
+//   fmt 1 (int8):  per row (K after RoPE, V raw) s = amax / 127 in fp32, codes = RNE(x / s)
+//                  clamped to [-127, 127], s stored as fp32; an all-zero row has s = 0  264 B
+//   fmt 2 (k4v16): K = NVFP4 of RoPE(k) (no Hadamard), V = fp16(v)              328 B
+//   Q, every format: bf16(RoPE(q)), unquantised.
+// Row bytes: Q, bf16 and fp16 rows 256; int8 rows 128 codes then the fp32 scale (132); NVFP4 K
+// rows 64 codes then 8 scales (72).
+// Page block: one chunk per KV head in head order; a chunk holds the 64 slots of K, then of V:
+//   bf16:  [K 64 x 256][V 64 x 256]
+//   int8:  [K codes 64 x 128][K scales 64 x 4][V codes 64 x 128][V scales 64 x 4]
+//   k4v16: [K codes 64 x 64][K scales 64 x 8][V 64 x 256]
+// ---------------------------------------------------------------------------------------------
+uint16_t orc_float_to_bf16(float x) {  // round to nearest even; finite x
+  uint32_t b;
+  std::memcpy(&b, &x, 4);
+  const uint32_t lsb = (b >> 16) & 1u;
+  return (uint16_t)((b + 0x7FFFu + lsb) >> 16);
+}
+
+uint16_t orc_float_to_f16(float x) {  // IEEE binary16, round to nearest even, overflow to inf
+  uint32_t b;
+  std::memcpy(&b, &x, 4);
+  const uint16_t sign = (uint16_t)((b >> 16) & 0x8000u);
+  const double a = std::fabs((double)x);
+  if (a == 0.0) return sign;
+  if (a >= 65520.0) return (uint16_t)(sign | 0x7C00u);  // past half an ulp above 65504
+  int e = 0;
+  std::frexp(a, &e);
+  int E = e - 1;  // a in [2^E, 2^(E+1))
+  if (E < -14) {  // subnormal grid k * 2^-24 (k = 1024 is the smallest normal)
+    const double k = std::nearbyint(std::ldexp(a, 24));
+    return (uint16_t)(sign | (uint16_t)k);
+  }
+  double k = std::nearbyint(std::ldexp(a, 10 - E));  // 1024 .. 2048
+  if (k == 2048.0) {
+    k = 1024.0;
+    ++E;
+  }
+  if (E > 15) return (uint16_t)(sign | 0x7C00u);
+  return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(k - 1024.0));
+}
+
+double orc_f16_to_double(uint16_t h) {
+  const int sign = (h >> 15) & 1, E = (h >> 10) & 31, m = h & 1023;
+  double v;
+  if (E == 0) v = std::ldexp((double)m, -24);
+  else if (E == 31) v = m ? NAN : INFINITY;
+  else v = std::ldexp(1024.0 + m, E - 25);
+  return sign ? -v : v;
+}
+
+void orc_int8_quantize_row(const float* x, int8_t* codes, float* scale) {
+  float amax = 0.0f;
+  for (int d = 0; d < 128; ++d) amax = std::fmax(amax, std::fabs(x[d]));
+  const float s = amax / 127.0f;
+  *scale = s;
+  for (int d = 0; d < 128; ++d) {
+    if (s == 0.0f) {
+      codes[d] = 0;
+      continue;
+    }
+    const float q = x[d] / s;
+    double c = std::nearbyint((double)q);  // ties to even (default rounding mode)
+    if (c > 127.0) c = 127.0;
+    if (c < -127.0) c = -127.0;
+    codes[d] = (int8_t)c;
+  }
+}
+
+int32_t orc_cmp_row_bytes(int32_t fmt, int32_t kind) {  // kind 0 = Q, 1 = K, 2 = V
+  if (kind == 0) return 256;
+  if (fmt == 0) return 256;
+  if (fmt == 1) return 132;
+  return kind == 1 ? 72 : 256;
+}
+
+void orc_cmp_encode_rows(int32_t fmt, int32_t kind, const uint16_t* rows, int64_t n_rows,
+                         const int32_t* pos, const float* rope_table, int32_t rot_dim,
+                         uint8_t* out) {
+  const int32_t rb = orc_cmp_row_bytes(fmt, kind);
+  for (int64_t r = 0; r < n_rows; ++r) {
+    float x[128];
+    for (int d = 0; d < 128; ++d) x[d] = orc_bf16_to_float(rows[r * 128 + d]);
+    if (kind != 2 && rot_dim > 0) orc_rope_apply(x, rope_table, pos[r], rot_dim);
+    uint8_t* o = out + r * rb;
+    if (kind == 0 || (fmt == 0 && kind == 1)) {
+      for (int d = 0; d < 128; ++d) {
+        const uint16_t h = orc_float_to_bf16(x[d]);
+        std::memcpy(o + 2 * d, &h, 2);
+      }
+    } else if (fmt == 0) {  // bf16 V: the row as given
+      std::memcpy(o, rows + r * 128, 256);
+    } else if (fmt == 1) {
+      float sc;
+      orc_int8_quantize_row(x, reinterpret_cast<int8_t*>(o), &sc);
+      std::memcpy(o + 128, &sc, 4);
+    } else if (kind == 1) {  // k4v16 K: NVFP4 without the Hadamard rotation
+      orc_quantize_row(x, o, o + 64);
+    } else {  // k4v16 V: fp16
+      for (int d = 0; d < 128; ++d) {
+        const uint16_t h = orc_float_to_f16(x[d]);
+        std::memcpy(o + 2 * d, &h, 2);
+      }
+    }
+  }
+}
+
+void orc_cmp_decode_rows(int32_t fmt, int32_t kind, const uint8_t* in, int64_t n_rows,
+                         double* out) {
+  const int32_t rb = orc_cmp_row_bytes(fmt, kind);
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const uint8_t* row = in + r * rb;
+    double* o = out + r * 128;
+    if (kind == 0 || fmt == 0) {
+      for (int d = 0; d < 128; ++d) {
+        uint16_t h;
+        std::memcpy(&h, row + 2 * d, 2);
+        o[d] = (double)orc_bf16_to_float(h);
+      }
+    } else if (fmt == 1) {
+      float sc;
+      std::memcpy(&sc, row + 128, 4);
+      for (int d = 0; d < 128; ++d) o[d] = (double)(int8_t)row[d] * (double)sc;
+    } else if (kind == 1) {
+      dequant_row(row, row + 64, o);
+    } else {
+      for (int d = 0; d < 128; ++d) {
+        uint16_t h;
+        std::memcpy(&h, row + 2 * d, 2);
+        o[d] = orc_f16_to_double(h);
+      }
+    }
+  }
+}
+
+// Rows [pos0, pos0 + n_tok) of one sequence out of a comparator pool (layout above):
+// k_rows / v_rows [n_tok][kv_heads][row bytes]. Returns the number of rows on pages outside the
+// pool (their bytes are zeroed).
+int64_t orc_cmp_paged_gather(int32_t fmt, const uint8_t* pool, int32_t num_pages,
+                             int32_t kv_heads, const int32_t* block_table, int32_t max_pages,
+                             int32_t seq, int32_t pos0, int32_t n_tok, uint8_t* k_rows,
+                             uint8_t* v_rows) {
+  const int64_t kb = orc_cmp_row_bytes(fmt, 1), vb = orc_cmp_row_bytes(fmt, 2);
+  const int64_t chunk = 64 * (kb + vb);
+  int64_t bad = 0;
+  for (int32_t i = 0; i < n_tok; ++i) {
+    const int32_t pos = pos0 + i;
+    const int32_t page = block_table[(int64_t)seq * max_pages + pos / 64];
+    const int32_t k = pos % 64;
+    for (int32_t h = 0; h < kv_heads; ++h) {
+      uint8_t* ko = k_rows + ((int64_t)i * kv_heads + h) * kb;
+      uint8_t* vo = v_rows + ((int64_t)i * kv_heads + h) * vb;
+      if (page < 0 || page >= num_pages) {
+        std::memset(ko, 0, (size_t)kb);
+        std::memset(vo, 0, (size_t)vb);
+        ++bad;
+        continue;
+      }
+      const uint8_t* c = pool + ((int64_t)page * kv_heads + h) * chunk;
+      if (fmt == 0) {
+        std::memcpy(ko, c + k * 256, 256);
+        std::memcpy(vo, c + 64 * 256 + k * 256, 256);
+      } else if (fmt == 1) {
+        std::memcpy(ko, c + k * 128, 128);
+        std::memcpy(ko + 128, c + 64 * 128 + k * 4, 4);
+        std::memcpy(vo, c + 64 * 132 + k * 128, 128);
+        std::memcpy(vo + 128, c + 64 * 132 + 64 * 128 + k * 4, 4);
+      } else {
+        std::memcpy(ko, c + k * 64, 64);
+        std::memcpy(ko + 64, c + 64 * 64 + k * 8, 8);
+        std::memcpy(vo, c + 64 * 72 + k * 256, 256);
+      }
+    }
+  }
+  return bad;
+}
+
+// fp64 attention over given (already decoded) rows, one output row per (seq, query token, q
+// head): q [(s * q_len + i) * q_heads + head][128], k / v [(tok_off[s] + pos) * kv_heads + h][128].
+// Same visibility and head mapping as orc_attention_rows; result rounded to fp32.
+void orc_attention_f64_rows(int32_t q_heads, int32_t kv_heads, int32_t q_len, int32_t causal,
+                            double sm_scale, const int32_t* seq_lens, const int64_t* tok_off,
+                            const double* q, const double* k, const double* v, int64_t n_rows,
+                            const int32_t* row_seq, const int32_t* row_tok,
+                            const int32_t* row_head, float* out, int32_t nthreads) {
+  const int32_t group = q_heads / kv_heads;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const int32_t s = row_seq[r], i = row_tok[r], head = row_head[r];
+    const int32_t kvh = head / group;
+    const int32_t len = seq_lens[s];
+    const int32_t qpos = len - q_len + i;
+    const int32_t n_vis = causal ? (qpos + 1) : len;
+    const double* qr = q + (((int64_t)s * q_len + i) * q_heads + head) * 128;
+    std::vector<double> score((size_t)n_vis);
+    double mx = -INFINITY;
+    for (int32_t t = 0; t < n_vis; ++t) {
+      const double* kr = k + ((tok_off[s] + t) * kv_heads + kvh) * 128;
+      double dot = 0.0;
+      for (int d = 0; d < 128; ++d) dot += qr[d] * kr[d];
+      score[t] = dot * sm_scale;
+      if (score[t] > mx) mx = score[t];
+    }
+    double acc[128] = {0.0};
+    double denom = 0.0;
+    for (int32_t t = 0; t < n_vis; ++t) {
+      const double p = std::exp(score[t] - mx);
+      denom += p;
+      const double* vr = v + ((tok_off[s] + t) * kv_heads + kvh) * 128;
+      for (int d = 0; d < 128; ++d) acc[d] += p * vr[d];
+    }
+    for (int d = 0; d < 128; ++d) out[r * 128 + d] = (float)(acc[d] / denom);
+  }
+}
+
 int32_t orc_bytes_per_token_head_nvfp4(int32_t head_dim) { return 2 * (head_dim / 2 + head_dim / 16); }
 int32_t orc_bytes_per_token_head_int8(int32_t head_dim) { return 2 * (head_dim + 4); }
 int32_t orc_bytes_per_token_head_bf16(int32_t head_dim) { return 2 * head_dim * 2; }
