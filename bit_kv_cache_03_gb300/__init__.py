@@ -73,6 +73,15 @@ _SIG = {
                               _I32, _P, _I32, _I32, _P, _P, _P, ctypes.c_float, _P, _P, _P], _I32),
     "kv_nvfp4_decode_attn_noalloc": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32, _P, _P,
                                       ctypes.c_float, _P, _I32, _P, _I32, _P, _P, _P], _I32),
+    "kv_cmp_page_bytes": ([ctypes.POINTER(Layout), _I32], ctypes.c_size_t),
+    "kv_cmp_append": ([ctypes.POINTER(Layout), _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _P, _I32,
+                       _I32, _I32, _P, _P, _P, _P], _I32),
+    "kv_cmp_plan_workspace_bytes": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32,
+                                     ctypes.POINTER(ctypes.c_size_t)], _I32),
+    "kv_cmp_plan": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32, _P, ctypes.c_size_t,
+                     ctypes.POINTER(PlanInfo), _P], _I32),
+    "kv_cmp_decode_attn": ([ctypes.POINTER(Layout), _I32, ctypes.POINTER(PlanInfo), _P, _P,
+                            ctypes.c_float, _P, _I32, _P, _I32, _P, _P, _P], _I32),
     "kv_nvfp4_spill_pages": ([ctypes.POINTER(Layout), _P, _I32, _P, _I32, _P, _P, _P], _I32),
     "kv_nvfp4_restore_pages": ([ctypes.POINTER(Layout), _P, _P, _I32, _P, _I32, _P, _P], _I32),
 }
@@ -241,6 +250,52 @@ def kv_nvfp4_decode_step(layout, plan: PlanInfo, workspace, q, k, v, rope, rope_
         _ptr(rope), rope_max_pos, _ptr(block_table), max_pages, num_pages, _ptr(pool),
         _ptr(q_codes_out), _ptr(q_scales_out), float(sm_scale), _ptr(out), _ptr(status),
         _stream(stream)), "kv_nvfp4_decode_step")
+
+
+# ---- comparator formats (bf16, int8, NVFP4 K + fp16 V) ----
+KV_CMP_BF16, KV_CMP_INT8, KV_CMP_K4V16 = 0, 1, 2
+
+
+def kv_cmp_page_bytes(layout, fmt) -> int:
+    return int(lib().kv_cmp_page_bytes(ctypes.byref(layout), fmt))
+
+
+def kv_cmp_append(layout, fmt, q, k, v, seq_ids, positions, T, rope_table, rope_max_pos,
+                  block_table, num_seqs, max_pages, num_pages, pool, q_out=None, status=None,
+                  stream=None):
+    _check(lib().kv_cmp_append(
+        ctypes.byref(layout), fmt, _ptr(q), _ptr(k), _ptr(v), _ptr(seq_ids), _ptr(positions), T,
+        _ptr(rope_table), rope_max_pos, _ptr(block_table), num_seqs, max_pages, num_pages,
+        _ptr(pool), _ptr(q_out), _ptr(status), _stream(stream)), "kv_cmp_append")
+
+
+def kv_cmp_plan_workspace_bytes(layout, seq_lens, q_len, causal, chunk_tokens) -> int:
+    import numpy as np
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    n = ctypes.c_size_t()
+    _check(lib().kv_cmp_plan_workspace_bytes(ctypes.byref(layout), sl.ctypes.data, len(sl), q_len,
+                                             int(causal), chunk_tokens, ctypes.byref(n)),
+           "kv_cmp_plan_workspace_bytes")
+    return n.value
+
+
+def kv_cmp_plan(layout, seq_lens, q_len, causal, chunk_tokens, workspace, ws_bytes,
+                stream=None) -> PlanInfo:
+    import numpy as np
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    info = PlanInfo()
+    _check(lib().kv_cmp_plan(ctypes.byref(layout), sl.ctypes.data, len(sl), q_len, int(causal),
+                             chunk_tokens, _ptr(workspace), ws_bytes, ctypes.byref(info),
+                             _stream(stream)), "kv_cmp_plan")
+    return info
+
+
+def kv_cmp_decode_attn(layout, fmt, plan: PlanInfo, workspace, q_rot, sm_scale, pool, num_pages,
+                       block_table, max_pages, out, status=None, stream=None):
+    _check(lib().kv_cmp_decode_attn(
+        ctypes.byref(layout), fmt, ctypes.byref(plan), _ptr(workspace), _ptr(q_rot),
+        float(sm_scale), _ptr(pool), num_pages, _ptr(block_table), max_pages, _ptr(out),
+        _ptr(status), _stream(stream)), "kv_cmp_decode_attn")
 
 
 def kv_nvfp4_spill_pages(layout, pool, num_pages, page_ids, n, arena, status=None, stream=None):

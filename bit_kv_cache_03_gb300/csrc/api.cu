@@ -29,6 +29,19 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
                           const uint16_t* v_new, const float* rope, int32_t rope_max_pos,
                           int32_t rot_dim, uint8_t* pool_w, uint8_t* q_codes_out,
                           uint8_t* q_scales_out, cudaStream_t stream);
+int cmp_chunk_bytes(int fmt);
+cudaError_t launch_cmp_append(int fmt, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                              const int32_t* seq_ids, const int32_t* positions, int64_t T,
+                              const float* rope, int32_t rope_max_pos, int32_t rot_dim,
+                              const int32_t* block_table, int32_t num_seqs, int32_t max_pages,
+                              int32_t num_pages, uint8_t* pool, uint16_t* q_out, int32_t Hq,
+                              int32_t Hkv, int32_t* status, cudaStream_t stream);
+cudaError_t launch_cmp_decode(int fmt, const uint16_t* q, const uint8_t* pool,
+                              const int32_t* block_table, int32_t max_pages, int32_t num_pages,
+                              const void* groups, const void* segments, const int32_t* cta_seg,
+                              const int32_t* split_groups, int32_t num_split, float* partials,
+                              float* out, int32_t* status, int32_t Hq, int32_t Hkv, int32_t q_len,
+                              int32_t causal, float sm_scale, int32_t grid, cudaStream_t stream);
 cudaError_t launch_page_copy(bool spill, const uint8_t* src, uint8_t* dst, const int32_t* ids,
                              int32_t n, int32_t num_pages, uint32_t page_bytes, int sms,
                              int32_t* status, cudaStream_t stream);
@@ -212,6 +225,32 @@ void rope_fill(float* t, int32_t max_pos, int32_t rot_dim, double theta, double 
 
 // ---- page spill / restore ----------------------------------------------------------------------
 namespace {
+
+// Build the plan for num_ctas CTAs and upload its tables (everything before the partials) into
+// the device workspace with one copy on the stream.
+kv_nvfp4_status plan_upload(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, int32_t num_seqs,
+                            int32_t q_len, int32_t causal, int32_t chunk_tokens, int num_ctas,
+                            void* d_workspace, size_t ws_bytes, kv_nvfp4_plan_info* info,
+                            void* stream) {
+  PlanBuild pb;
+  const kv_nvfp4_status s =
+      plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_ctas, &pb);
+  if (s != KV_NVFP4_OK) return s;
+  const kv_nvfp4_plan_info& pi = pb.info;
+  if (ws_bytes < pi.workspace_bytes) return KV_NVFP4_ENOSPACE;
+  std::vector<int32_t> host((size_t)(pi.off_partials / 4), 0);
+  std::memcpy(host.data() + pi.off_groups / 4, pb.groups.data(), pb.groups.size() * 4);
+  std::memcpy(host.data() + pi.off_segments / 4, pb.segments.data(), pb.segments.size() * 4);
+  std::memcpy(host.data() + pi.off_cta / 4, pb.cta_seg.data(), pb.cta_seg.size() * 4);
+  std::memcpy(host.data() + pi.off_split / 4, pb.split.data(), pb.split.size() * 4);
+  const cudaError_t e = cudaMemcpyAsync(d_workspace, host.data(), host.size() * 4,
+                                        cudaMemcpyHostToDevice, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  *info = pi;
+  return KV_NVFP4_OK;
+}
+
+
 
 // Device address of an arena: page-locked host memory (its mapped device address) or device
 // memory. Pageable host memory, which the GPU cannot address on every system, is refused.
@@ -402,24 +441,8 @@ kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout* L, const int32_t* h_seq_len
   if (info == nullptr || d_workspace == nullptr || !aligned16(d_workspace)) return KV_NVFP4_EINVAL;
   const int num_sms = num_sms_current_device();
   if (num_sms <= 0) return cuda_status(cudaErrorNoDevice);
-  PlanBuild pb;
-  const kv_nvfp4_status s =
-      plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_sms, &pb);
-  if (s != KV_NVFP4_OK) return s;
-  const kv_nvfp4_plan_info& pi = pb.info;
-  if (ws_bytes < pi.workspace_bytes) return KV_NVFP4_ENOSPACE;
-  // host image of the tables (everything before the partials), one copy
-  std::vector<int32_t> host((size_t)(pi.off_partials / 4), 0);
-  std::memcpy(host.data() + pi.off_groups / 4, pb.groups.data(), pb.groups.size() * 4);
-  std::memcpy(host.data() + pi.off_segments / 4, pb.segments.data(), pb.segments.size() * 4);
-  std::memcpy(host.data() + pi.off_cta / 4, pb.cta_seg.data(), pb.cta_seg.size() * 4);
-  std::memcpy(host.data() + pi.off_split / 4, pb.split.data(), pb.split.size() * 4);
-  cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e =
-      cudaMemcpyAsync(d_workspace, host.data(), host.size() * 4, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return cuda_status(e);
-  *info = pi;
-  return KV_NVFP4_OK;
+  return plan_upload(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_sms, d_workspace,
+                     ws_bytes, info, stream);
 }
 
 kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout* L, const kv_nvfp4_plan_info* plan,
@@ -489,6 +512,94 @@ kv_nvfp4_status kv_nvfp4_decode_step(const kv_nvfp4_layout* L, const kv_nvfp4_pl
       (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, d_rope_table, rope_max_pos,
       L->rot_dim, pool, q_codes_out, q_scales_out, (cudaStream_t)stream);
   return cuda_status(e);
+}
+
+
+// ---- comparator formats -----------------------------------------------------------------------
+size_t kv_cmp_page_bytes(const kv_nvfp4_layout* L, int32_t fmt) {
+  if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || fmt < KV_CMP_BF16 || fmt > KV_CMP_K4V16) return 0;
+  return (size_t)L->num_kv_heads * (size_t)kvnvfp4::cmp_chunk_bytes(fmt);
+}
+
+kv_nvfp4_status kv_cmp_append(const kv_nvfp4_layout* L, int32_t fmt, const void* q, const void* k,
+                              const void* v, const int32_t* d_seq_ids, const int32_t* d_positions,
+                              int32_t T, const float* d_rope_table, int32_t rope_max_pos,
+                              const int32_t* d_block_table, int32_t num_seqs, int32_t max_pages,
+                              int32_t num_pages, uint8_t* pool, void* q_out, int32_t* d_status,
+                              void* stream) {
+  if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || fmt < KV_CMP_BF16 || fmt > KV_CMP_K4V16)
+    return KV_NVFP4_EINVAL;
+  if (T < 0 || num_seqs <= 0 || max_pages <= 0 || num_pages <= 0) return KV_NVFP4_EINVAL;
+  if (T == 0) return KV_NVFP4_OK;
+  if (!k || !v || !d_seq_ids || !d_positions || !d_block_table || !pool) return KV_NVFP4_EINVAL;
+  if (q && !q_out) return KV_NVFP4_EINVAL;
+  if (L->rot_dim > 0 && (!d_rope_table || rope_max_pos <= 0 || !aligned16(d_rope_table)))
+    return KV_NVFP4_EINVAL;
+  if (!aligned16(k) || !aligned16(v) || (q && (!aligned16(q) || !aligned16(q_out))) ||
+      !aligned16(pool))
+    return KV_NVFP4_EINVAL;
+  return cuda_status(kvnvfp4::launch_cmp_append(
+      fmt, (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, d_seq_ids, d_positions, T,
+      d_rope_table, rope_max_pos, L->rot_dim, d_block_table, num_seqs, max_pages, num_pages, pool,
+      (uint16_t*)q_out, L->num_q_heads, L->num_kv_heads, d_status, (cudaStream_t)stream));
+}
+
+kv_nvfp4_status kv_cmp_plan_workspace_bytes(const kv_nvfp4_layout* L, const int32_t* h_seq_lens,
+                                            int32_t num_seqs, int32_t q_len, int32_t causal,
+                                            int32_t chunk_tokens, size_t* bytes) {
+  if (bytes == nullptr || kv_nvfp4_layout_check(L) != KV_NVFP4_OK) return KV_NVFP4_EINVAL;
+  int num_sms = num_sms_current_device();
+  if (num_sms <= 0) num_sms = kMaxGridForSizing;
+  const int ctas = num_sms / L->num_kv_heads > 0 ? num_sms / L->num_kv_heads : 1;
+  PlanBuild pb;
+  const kv_nvfp4_status s =
+      plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, ctas, &pb);
+  if (s != KV_NVFP4_OK) return s;
+  *bytes = (size_t)pb.info.workspace_bytes;
+  return KV_NVFP4_OK;
+}
+
+kv_nvfp4_status kv_cmp_plan(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, int32_t num_seqs,
+                            int32_t q_len, int32_t causal, int32_t chunk_tokens,
+                            void* d_workspace, size_t ws_bytes, kv_nvfp4_plan_info* info,
+                            void* stream) {
+  if (info == nullptr || d_workspace == nullptr || !aligned16(d_workspace) ||
+      kv_nvfp4_layout_check(L) != KV_NVFP4_OK)
+    return KV_NVFP4_EINVAL;
+  const int num_sms = num_sms_current_device();
+  if (num_sms <= 0) return cuda_status(cudaErrorNoDevice);
+  const int ctas = num_sms / L->num_kv_heads > 0 ? num_sms / L->num_kv_heads : 1;
+  return plan_upload(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, ctas, d_workspace,
+                     ws_bytes, info, stream);
+}
+
+kv_nvfp4_status kv_cmp_decode_attn(const kv_nvfp4_layout* L, int32_t fmt,
+                                   const kv_nvfp4_plan_info* plan, void* d_workspace,
+                                   const void* q_rot, float sm_scale, const uint8_t* pool,
+                                   int32_t num_pages, const int32_t* d_block_table,
+                                   int32_t max_pages, float* out, int32_t* d_status,
+                                   void* stream) {
+  if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || plan == nullptr || fmt < KV_CMP_BF16 ||
+      fmt > KV_CMP_K4V16)
+    return KV_NVFP4_EINVAL;
+  if (plan->num_kv_heads != L->num_kv_heads || plan->num_seqs <= 0 || plan->q_len <= 0 ||
+      plan->grid <= 0 || L->num_kv_heads > 65535)
+    return KV_NVFP4_EINVAL;
+  if (!d_workspace || !q_rot || !pool || !d_block_table || !out || num_pages <= 0 ||
+      max_pages <= 0)
+    return KV_NVFP4_EINVAL;
+  if ((int64_t)plan->max_seq_len > (int64_t)max_pages * L->page_size) return KV_NVFP4_EINVAL;
+  const void* ptrs[] = {d_workspace, q_rot, pool, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return KV_NVFP4_EINVAL;
+  if (!(sm_scale > 0.0f)) sm_scale = 1.0f / std::sqrt((float)L->head_dim);
+  char* ws = (char*)d_workspace;
+  return cuda_status(kvnvfp4::launch_cmp_decode(
+      fmt, (const uint16_t*)q_rot, pool, d_block_table, max_pages, num_pages,
+      ws + plan->off_groups, ws + plan->off_segments, (const int32_t*)(ws + plan->off_cta),
+      (const int32_t*)(ws + plan->off_split), plan->num_split_groups,
+      (float*)(ws + plan->off_partials), out, d_status, L->num_q_heads, L->num_kv_heads,
+      plan->q_len, plan->causal, sm_scale, plan->grid, (cudaStream_t)stream));
 }
 
 }  // extern "C"

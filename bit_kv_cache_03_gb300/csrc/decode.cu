@@ -155,13 +155,6 @@ __device__ __forceinline__ SegInfo load_seg(const DecodeParams& p, int s) {
 
 // Bounded wait: after a thread has once hit the time limit its later waits do not block, so a
 // kernel whose pipeline lost a signal still ends promptly (with KV_NVFP4_DEV_TIMEOUT set).
-__device__ __forceinline__ void wait_bar(uint32_t bar, uint32_t parity, bool& timed_out) {
-  if (timed_out) {
-    (void)mbar_try_wait(bar, parity);
-    return;
-  }
-  if (!mbar_wait_bounded(bar, parity)) timed_out = true;
-}
 
 // --------------------------------------------------------------------------------------------
 // Producer warp: lane 0 streams the CTA's pages (all KV heads of a page in one bulk copy) into a
@@ -991,6 +984,11 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
 
 int decode_smem_bytes() { return kSmemBytes; }
 
+cudaError_t launch_split_merge(const void* groups, const int32_t* split_groups,
+                               const float* partials, float* out, int32_t Hq, int32_t Hkv,
+                               int32_t G, int32_t q_len, float c2, int32_t num_split,
+                               cudaStream_t stream);
+
 cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const uint8_t* pool,
                           const int32_t* block_table, int32_t max_pages, int32_t num_pages,
                           const void* groups, const void* segments, const int32_t* cta_seg,
@@ -1052,11 +1050,21 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || num_split <= 0) return e;
+  return launch_split_merge(p.groups, split_groups, partials, out, Hq, Hkv, p.G, q_len, p.c2,
+                            num_split, stream);
+}
+
+// The split-K merge launch (also used by the comparator decode): one CTA per (split group, KV
+// head, row of the tile), as a programmatic dependent of the attention kernel before it on the
+// stream (it waits for that grid to complete before reading the partials).
+cudaError_t launch_split_merge(const void* groups, const int32_t* split_groups,
+                               const float* partials, float* out, int32_t Hq, int32_t Hkv,
+                               int32_t G, int32_t q_len, float c2, int32_t num_split,
+                               cudaStream_t stream) {
+  if (num_split <= 0) return cudaSuccess;
   MergeParams mp;
-  mp.groups = p.groups; mp.split = split_groups; mp.partials = partials; mp.out = out;
-  mp.Hq = Hq; mp.Hkv = Hkv; mp.G = p.G; mp.q_len = q_len; mp.c2 = p.c2;
-  // programmatic dependent launch: the merge grid is set up while the attention kernel runs and
-  // waits (griddepcontrol.wait) for it to complete before reading the partials
+  mp.groups = static_cast<const int4*>(groups); mp.split = split_groups; mp.partials = partials;
+  mp.out = out; mp.Hq = Hq; mp.Hkv = Hkv; mp.G = G; mp.q_len = q_len; mp.c2 = c2;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)num_split, (unsigned)(Hkv * kRows));
   cfg.blockDim = dim3(256);

@@ -73,6 +73,37 @@ __device__ __forceinline__ void rope_fetch(const float* rope_row, int rot, int l
   }
 }
 
+// RoPE on the first rot dims of R rows held by a warp (pairs i, i + rot/2; lane l holds elements
+// 4l..4l+3), with this lane's factors from rope_fetch. The products are rounded separately and then
+// added, as the definition reads.
+template <int R>
+__device__ __forceinline__ void rope_rows(float (&x)[R][4], const float4 (&c)[R],
+                                          const float4 (&s)[R], int rot, int lane) {
+  const int half_lanes = rot >> 3;           // lanes holding dims [0, rot/2)
+  const bool lower = lane < half_lanes;
+  const bool paired = lane < 2 * half_lanes;
+  const int src = lower ? lane + half_lanes : lane - half_lanes;
+  const float ysg = lower ? -1.0f : 1.0f;
+  float y[R][4];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) y[r][e] = __shfl_sync(0xffffffffu, x[r][e], src & 31);
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const float cc[4] = {c[r].x, c[r].y, c[r].z, c[r].w};
+    const float ss[4] = {s[r].x, s[r].y, s[r].z, s[r].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      // lower lane holds a = x_i, partner b = x_{i+half}: a c - b s
+      // upper lane holds b = x_{i+half}, partner a = x_i:  b c + a s
+      // (-b) s = -(b s) exactly, so both are one add of two rounded products
+      const float v = __fadd_rn(__fmul_rn(x[r][e], cc[e]), __fmul_rn(ysg * y[r][e], ss[e]));
+      x[r][e] = paired ? v : x[r][e];
+    }
+  }
+}
+
 // R rows of nvfp4_encode_row, advanced in lockstep (every step taken for all R rows before the
 // next), with the RoPE factors already fetched (rope_fetch). Each row goes through exactly the
 // operations of the one-row encode, so its codes and scale do not depend on R; the R independent
@@ -84,32 +115,7 @@ __device__ __forceinline__ void nvfp4_encode_rows(float (&x)[R][4], bool rotate,
                                                   int rot, int lane, uint32_t (&packed)[R],
                                                   uint32_t (&sc)[R]) {
   if (rotate) {
-    // --- RoPE on the first rot_dim dims (pairs i, i + rot_dim/2) ---
-    if (rope) {
-      const int half_lanes = rot >> 3;           // lanes holding dims [0, rot/2)
-      const bool lower = lane < half_lanes;
-      const bool paired = lane < 2 * half_lanes;
-      const int src = lower ? lane + half_lanes : lane - half_lanes;
-      const float ysg = lower ? -1.0f : 1.0f;
-      float y[R][4];
-#pragma unroll
-      for (int r = 0; r < R; ++r)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) y[r][e] = __shfl_sync(0xffffffffu, x[r][e], src & 31);
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float cc[4] = {c[r].x, c[r].y, c[r].z, c[r].w};
-        const float ss[4] = {s[r].x, s[r].y, s[r].z, s[r].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          // lower lane holds a = x_i, partner b = x_{i+half}: a c - b s
-          // upper lane holds b = x_{i+half}, partner a = x_i:  b c + a s
-          // (-b) s = -(b s) exactly, so both are one add of two rounded products
-          const float v = __fadd_rn(__fmul_rn(x[r][e], cc[e]), __fmul_rn(ysg * y[r][e], ss[e]));
-          x[r][e] = paired ? v : x[r][e];
-        }
-      }
-    }
+    if (rope) rope_rows<R>(x, c, s, rot, lane);
     // --- Walsh-Hadamard, stages h = 1, 2, 4, ..., 64 ---
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -357,6 +363,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
     if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > 2000000000ull) return false;
   }
+}
+
+// A bounded wait that records a timeout and then stops waiting (later waits only poll once), so
+// that a kernel whose peer never arrives still runs to its end and reports KV_NVFP4_DEV_TIMEOUT.
+__device__ __forceinline__ void wait_bar(uint32_t bar, uint32_t parity, bool& timed_out) {
+  if (timed_out) {
+    (void)mbar_try_wait(bar, parity);
+    return;
+  }
+  if (!mbar_wait_bounded(bar, parity)) timed_out = true;
 }
 
 // Bulk (non-tensor) async copy global -> shared, completing on an mbarrier. Both addresses

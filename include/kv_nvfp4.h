@@ -246,6 +246,57 @@ kv_nvfp4_status kv_nvfp4_decode_step(const kv_nvfp4_layout *layout,
                                      uint8_t *q_scales_out, float sm_scale, float *out,
                                      int32_t *d_status, void *stream);
 
+/* ---- Comparator KV formats [NVFP4 "Result": 144 B per token per KV head vs 264 int8 vs 512 bf16;
+ * upstream NVFP4 K with fp16 V and no rotation] -------------------------------------------------
+ * prismix.dev/news/833001997676, section "NVFP4 KV cache (from scratch)". Decode attention over
+ * three other KV formats, for byte-count and roofline comparison with the NVFP4 path; not the
+ * method itself. Q is unquantised in all three (bf16 after RoPE).
+ *   KV_CMP_BF16:  K = bf16(RoPE(k)), V = v                                   512 B/token/KV head
+ *   KV_CMP_INT8:  per row (K after RoPE, V raw) s = amax / 127 (fp32), codes = RNE(x / s)
+ *                 clamped to +-127, s stored as fp32                          264 B
+ *   KV_CMP_K4V16: K = NVFP4 of RoPE(k) without the Hadamard rotation, V = fp16(v)   328 B
+ * Pool: num_pages blocks of kv_cmp_page_bytes; a block holds one chunk per KV head (K rows, then
+ * V rows, of its 64 slots; the chunk layouts and the 16-byte unit swizzle inside rows are given
+ * in bit_kv_cache_03_gb300/csrc/compare.cu). */
+#define KV_CMP_BF16 0
+#define KV_CMP_INT8 1
+#define KV_CMP_K4V16 2
+
+/* Bytes of one comparator page (all KV heads); 0 for an invalid layout or format. */
+size_t kv_cmp_page_bytes(const kv_nvfp4_layout *layout, int32_t fmt);
+
+/* Comparator append: as kv_nvfp4_append (same ids, positions, RoPE table, block table, status
+ * bits and errors), writing K/V rows in format `fmt` and, when q is given, the bf16 RoPE'd Q rows
+ * to q_out (DEVICE bf16 [T][num_q_heads][128], 16-byte aligned). One kernel launch. */
+kv_nvfp4_status kv_cmp_append(const kv_nvfp4_layout *layout, int32_t fmt, const void *q,
+                              const void *k, const void *v, const int32_t *d_seq_ids,
+                              const int32_t *d_positions, int32_t T, const float *d_rope_table,
+                              int32_t rope_max_pos, const int32_t *d_block_table,
+                              int32_t num_seqs, int32_t max_pages, int32_t num_pages,
+                              uint8_t *pool, void *q_out, int32_t *d_status, void *stream);
+
+/* Plan for the comparator decode: as kv_nvfp4_plan, for (SM count / num_kv_heads) CTAs, each of
+ * which the decode launches once per KV head. */
+kv_nvfp4_status kv_cmp_plan_workspace_bytes(const kv_nvfp4_layout *layout,
+                                            const int32_t *h_seq_lens, int32_t num_seqs,
+                                            int32_t q_len, int32_t causal, int32_t chunk_tokens,
+                                            size_t *bytes);
+kv_nvfp4_status kv_cmp_plan(const kv_nvfp4_layout *layout, const int32_t *h_seq_lens,
+                            int32_t num_seqs, int32_t q_len, int32_t causal, int32_t chunk_tokens,
+                            void *d_workspace, size_t ws_bytes, kv_nvfp4_plan_info *plan,
+                            void *stream);
+
+/* Comparator decode attention over a pool of format `fmt`: q_rot = the q_out rows of
+ * kv_cmp_append (num_seqs * q_len tokens, sequence-major); plan and workspace from kv_cmp_plan;
+ * out, d_status, sm_scale and the errors as for kv_nvfp4_decode_attn. One kernel launch, plus
+ * the split-K merge launch when the plan has split groups. */
+kv_nvfp4_status kv_cmp_decode_attn(const kv_nvfp4_layout *layout, int32_t fmt,
+                                   const kv_nvfp4_plan_info *plan, void *d_workspace,
+                                   const void *q_rot, float sm_scale, const uint8_t *pool,
+                                   int32_t num_pages, const int32_t *d_block_table,
+                                   int32_t max_pages, float *out, int32_t *d_status,
+                                   void *stream);
+
 /* ---- Page spill and restore [Spill: cache pages moved out to host memory and back] ----------
  * prismix.dev/news/833001997676, section "Multi-level prefix reuse with host-KV safety net".
  * kv_nvfp4_spill_pages:   arena slot i <- pool page d_page_ids[i], for i < n

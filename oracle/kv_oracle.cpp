@@ -441,6 +441,10 @@ int64_t orc_restore_pages(uint8_t* pool, int32_t num_pages, int32_t kv_heads,
 //   bf16:  [K 64 x 256][V 64 x 256]
 //   int8:  [K codes 64 x 128][K scales 64 x 4][V codes 64 x 128][V scales 64 x 4]
 //   k4v16: [K codes 64 x 64][K scales 64 x 8][V 64 x 256]
+// Inside a row, 16-byte unit u of slot k is stored at unit u ^ sw(k) (a layout choice of the
+// comparator kernels, for bank-conflict-free shared-memory reads): bf16 K and V rows and fp16 V
+// rows sw = k & 7; int8 K rows sw = (k & 1) * 4; int8 V rows sw = ((k / 2) & 3) * 2; NVFP4 K
+// codes and every scale are stored plainly.
 // ---------------------------------------------------------------------------------------------
 uint16_t orc_float_to_bf16(float x) {  // round to nearest even; finite x
   uint32_t b;
@@ -565,6 +569,11 @@ void orc_cmp_decode_rows(int32_t fmt, int32_t kind, const uint8_t* in, int64_t n
   }
 }
 
+// One row of `bytes` bytes out of a stored row whose 16-byte units are permuted by u ^ sw.
+static void unswizzle_row(const uint8_t* stored, int32_t bytes, int32_t sw, uint8_t* out) {
+  for (int32_t j = 0; j < bytes; ++j) out[j] = stored[(((j / 16) ^ sw) * 16) + j % 16];
+}
+
 // Rows [pos0, pos0 + n_tok) of one sequence out of a comparator pool (layout above):
 // k_rows / v_rows [n_tok][kv_heads][row bytes]. Returns the number of rows on pages outside the
 // pool (their bytes are zeroed).
@@ -590,17 +599,17 @@ int64_t orc_cmp_paged_gather(int32_t fmt, const uint8_t* pool, int32_t num_pages
       }
       const uint8_t* c = pool + ((int64_t)page * kv_heads + h) * chunk;
       if (fmt == 0) {
-        std::memcpy(ko, c + k * 256, 256);
-        std::memcpy(vo, c + 64 * 256 + k * 256, 256);
+        unswizzle_row(c + k * 256, 256, k & 7, ko);
+        unswizzle_row(c + 64 * 256 + k * 256, 256, k & 7, vo);
       } else if (fmt == 1) {
-        std::memcpy(ko, c + k * 128, 128);
+        unswizzle_row(c + k * 128, 128, (k & 1) * 4, ko);
         std::memcpy(ko + 128, c + 64 * 128 + k * 4, 4);
-        std::memcpy(vo, c + 64 * 132 + k * 128, 128);
+        unswizzle_row(c + 64 * 132 + k * 128, 128, ((k / 2) & 3) * 2, vo);
         std::memcpy(vo + 128, c + 64 * 132 + 64 * 128 + k * 4, 4);
       } else {
         std::memcpy(ko, c + k * 64, 64);
         std::memcpy(ko + 64, c + 64 * 64 + k * 8, 8);
-        std::memcpy(vo, c + 64 * 72 + k * 256, 256);
+        unswizzle_row(c + 64 * 72 + k * 256, 256, k & 7, vo);
       }
     }
   }

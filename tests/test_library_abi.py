@@ -177,3 +177,23 @@ def test_spill_restore_reject_bad_arguments_before_cuda(kv):
     assert lib.kv_nvfp4_restore_pages(ctypes.byref(L), 776, 512, 2, 256, 4, None, None) == EINVAL
     bad = kv.Layout(24, 4, 64, 64, 32)
     assert lib.kv_nvfp4_restore_pages(ctypes.byref(bad), 768, 512, 2, 256, 4, None, None) == EINVAL
+
+
+def test_comparator_sizes_and_rejections_before_cuda(kv):
+    lib = kv.lib()
+    L = kv.make_layout()
+    # per token per KV head: 512 (bf16), 264 (int8), 328 (NVFP4 K + fp16 V); 64 tokens x 4 heads
+    assert [kv.kv_cmp_page_bytes(L, f) for f in (0, 1, 2)] == [64 * 4 * b for b in (512, 264, 328)]
+    assert kv.kv_cmp_page_bytes(L, 3) == 0
+    info = kv.PlanInfo()
+    EINVAL = kv.KV_NVFP4_EINVAL
+    assert lib.kv_cmp_append(ctypes.byref(L), 5, *([None] * 5), 1, None, 1, None, 1, 1, 1,
+                             *([None] * 4)) == EINVAL
+    assert lib.kv_cmp_append(ctypes.byref(L), 0, *([None] * 5), 0, None, 1, None, 1, 1, 1,
+                             *([None] * 4)) == kv.KV_NVFP4_OK  # nothing to append
+    assert lib.kv_cmp_decode_attn(ctypes.byref(L), 0, ctypes.byref(info), None, None, 0.0, None,
+                                  1, None, 1, None, None, None) == EINVAL
+    assert lib.kv_cmp_decode_attn(ctypes.byref(L), 7, ctypes.byref(info), 256, 256, 0.0, 256,
+                                  1, 256, 1, 256, None, None) == EINVAL
+    n = kv.kv_cmp_plan_workspace_bytes(L, [131073] * 4, 1, True, 64)
+    assert n > 0

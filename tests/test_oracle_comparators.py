@@ -133,29 +133,34 @@ def test_encodings_follow_the_pinned_pieces():
 
 @pytest.mark.parametrize("fmt", [0, 1, 2])
 def test_comparator_gather_layout(fmt):
-    # every byte of the pool names (page, head, region, slot, byte); the gather must return each
-    # slot's own bytes in row order
+    # every byte of the pool names (page, head, region, slot, byte), rows stored with their
+    # 16-byte units permuted as the layout states; the gather must return each slot's own bytes
+    # in row order
     P, H = 5, 3
     kb, vb = oracle.cmp_row_bytes(fmt, 1), oracle.cmp_row_bytes(fmt, 2)
     chunk = 64 * (kb + vb)
     pool = np.zeros(P * H * chunk, np.uint8)
     name = lambda p, h, reg, k, j: (p * 31 + h * 17 + reg * 7 + k * 3 + j) % 251
+    def put(c, base, k, sw, vals):  # a row stored with 16-byte unit u at u ^ sw
+        for j, x in enumerate(vals):
+            c[base + (((j // 16) ^ sw) * 16) + j % 16] = x
+
     for p in range(P):
         for h in range(H):
             c = pool[(p * H + h) * chunk:(p * H + h + 1) * chunk]
             for k in range(64):
                 if fmt == 0:
-                    c[k * 256:(k + 1) * 256] = [name(p, h, 0, k, j) for j in range(256)]
-                    c[64 * 256 + k * 256:64 * 256 + (k + 1) * 256] = [name(p, h, 1, k, j) for j in range(256)]
+                    put(c, k * 256, k, k & 7, [name(p, h, 0, k, j) for j in range(256)])
+                    put(c, 64 * 256 + k * 256, k, k & 7, [name(p, h, 1, k, j) for j in range(256)])
                 elif fmt == 1:
-                    c[k * 128:(k + 1) * 128] = [name(p, h, 0, k, j) for j in range(128)]
+                    put(c, k * 128, k, (k & 1) * 4, [name(p, h, 0, k, j) for j in range(128)])
                     c[8192 + k * 4:8192 + k * 4 + 4] = [name(p, h, 0, k, 128 + j) for j in range(4)]
-                    c[8448 + k * 128:8448 + (k + 1) * 128] = [name(p, h, 1, k, j) for j in range(128)]
+                    put(c, 8448 + k * 128, k, ((k // 2) & 3) * 2, [name(p, h, 1, k, j) for j in range(128)])
                     c[16640 + k * 4:16640 + k * 4 + 4] = [name(p, h, 1, k, 128 + j) for j in range(4)]
                 else:
                     c[k * 64:(k + 1) * 64] = [name(p, h, 0, k, j) for j in range(64)]
                     c[4096 + k * 8:4096 + k * 8 + 8] = [name(p, h, 0, k, 64 + j) for j in range(8)]
-                    c[4608 + k * 256:4608 + (k + 1) * 256] = [name(p, h, 1, k, j) for j in range(256)]
+                    put(c, 4608 + k * 256, k, k & 7, [name(p, h, 1, k, j) for j in range(256)])
     bt = np.array([[3, 0, 4], [1, 2, 9]], np.int32)
     k, v, bad = oracle.cmp_paged_gather(fmt, pool, P, H, bt, 0, 40, 100)
     assert bad == 0
