@@ -296,6 +296,72 @@ def spill_restore(g, dev, stream, reps=5):
                     "one contiguous cudaMemcpyAsync of the same bytes"}
 
 
+CMP_NAMES = {0: "bf16", 1: "int8", 2: "nvfp4k_fp16v"}
+CMP_ROW_BYTES = {0: 512, 1: 264, 2: 328}  # K + V bytes per token per KV head
+
+
+def comparators(w, dev, stream, peak, reps=200):
+    """The comparator formats (bf16, int8, NVFP4 K + fp16 V) on the same workload: decode call
+    time, KV-tokens/s and HBM fraction of their own algorithmic bytes."""
+    import numpy as np
+    import torch
+
+    import bit_kv_cache_03_gb300 as kv
+    L = kv.make_layout(w.q_heads, w.kv_heads, 128, 64, w.rot_dim)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    bt = torch.from_numpy(np.ascontiguousarray(w.block_table, np.int32)).to(dev)
+    rope = torch.empty(max(1, w.max_pos * w.rot_dim), dtype=torch.float32, device=dev)
+    kv.kv_nvfp4_rope_table_init(rope, w.max_pos, w.rot_dim, w.theta, w.pos_scale)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    cached = []
+    for s_, c in enumerate(w.cached_lens):
+        k, v, pos = w.cached_tokens(s_, 0, c)
+        cached.append((bf(k), bf(v), torch.full((c,), s_, dtype=torch.int32, device=dev),
+                       torch.from_numpy(pos).to(dev), c))
+    q, k, v, sid, pos = w.new_tokens()
+    T = q.shape[0]
+    qn, kn, vn = bf(q), bf(k), bf(v)
+    sidn, posn = torch.from_numpy(sid).to(dev), torch.from_numpy(pos).to(dev)
+    q_out = torch.empty(T * w.q_heads * 128, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(T * w.q_heads * 128, dtype=torch.float32, device=dev)
+    kv_tokens = int(w.seq_lens.sum())
+    n_pages = int(sum((int(l) + 63) // 64 for l in w.seq_lens))
+    res = {}
+    for fmt in (0, 1, 2):
+        pool = torch.empty(w.pool_pages * kv.kv_cmp_page_bytes(L, fmt), dtype=torch.uint8, device=dev)
+        for (kc, vc, sc, pc, c) in cached:
+            kv.kv_cmp_append(L, fmt, None, kc, vc, sc, pc, c, rope, w.max_pos, bt, w.num_seqs,
+                             w.max_pages, w.pool_pages, pool, None, status)
+        kv.kv_cmp_append(L, fmt, qn, kn, vn, sidn, posn, T, rope, w.max_pos, bt, w.num_seqs,
+                         w.max_pages, w.pool_pages, pool, q_out, status)
+        nws = kv.kv_cmp_plan_workspace_bytes(L, w.seq_lens, w.q_len, w.causal, CHUNK)
+        ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=dev)
+        plan = kv.kv_cmp_plan(L, w.seq_lens, w.q_len, w.causal, CHUNK, ws, nws)
+
+        def call():
+            kv.kv_cmp_decode_attn(L, fmt, plan, ws, q_out, w.sm_scale, pool, w.pool_pages, bt,
+                                  w.max_pages, out, status)
+
+        for _ in range(10):
+            call()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t = e0.elapsed_time(e1) / 1e3 / reps
+        b = (kv_tokens * w.kv_heads * CMP_ROW_BYTES[fmt] + T * w.q_heads * 256 + n_pages * 4 +
+             T * w.q_heads * 128 * 4)
+        res[CMP_NAMES[fmt]] = {"bytes_per_token_kv_head": CMP_ROW_BYTES[fmt],
+                               "attn_us": t * 1e6, "kv_tokens_per_s": kv_tokens / t,
+                               "hbm_gbs": b / t / 1e9, "hbm_frac_of_measured": b / t / 1e9 / peak}
+        del pool, ws
+    assert int(status.item()) == 0, f"comparator status {int(status.item()):#x}"
+    return res
+
+
 def run_cuda(args, world, rank, local):
     import numpy as np
     import torch
@@ -426,6 +492,7 @@ def run_cuda(args, world, rank, local):
     e2e_elapsed = time.perf_counter() - t0
 
     spill = spill_restore(g, dev, stream)
+    cmp = None if args.no_comparators else comparators(w, dev, stream, measured_peaks()[0])
 
     elapsed, e2e_elapsed = max_over_ranks([elapsed, e2e_elapsed], dev)
     if rank != 0:
@@ -476,6 +543,7 @@ def run_cuda(args, world, rank, local):
                 "includes": "pinned H2D of new Q/K/V, plan upload, step call, D2H of output"},
         "gpu_launches": 2 * args.steps,  # per timed step: the attention kernel, split-K merge
         "spill": spill,
+        "comparators": cmp,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(w)
@@ -489,6 +557,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-comparators", action="store_true",
+                    help="skip the bf16 / int8 / NVFP4 K + fp16 V comparator timings")
     ap.add_argument("--seqs", type=int, default=4, help="sequences of 131072 tokens (profiling)")
     ap.add_argument("--profile", action="store_true",
                     help="warm-up + steps only, no extra measurements (for ncu)")
