@@ -29,12 +29,13 @@
 // reductions, rescales its accumulator when a max grows, and writes P = exp2((s - m) log2e scale)
 // <= 1 in f16 to a private shared tile (f16 keeps 11 significant bits of P; the method's own P.V
 // runs in bf16, with 8). The P.V product runs on the warp-level tensor path (mma.sync m16n8k16,
-// f32 accumulate) with the query rows as M (rows 0..7; rows 8..15 read the tile's zeroed second
-// half), 16 keys as K and 8 head dims as N. P comes in with transposing ldmatrix; V goes from its
-// E2M1 codes straight into B fragments: the nibbles of two keys are interleaved into one byte per
-// dim, converted with cvt.e2m1x2 and multiplied by the two keys' E4M3 scales (E2M1 x E4M3 is
-// exact in f16). Within a 16-key step the keys are taken in a fixed permutation, the same for P
-// and V, that keeps the shared-memory reads conflict-free.
+// f32 accumulate), transposed: O^T += V^T P^T, with 16 head dims as M (a lane's rows g and g + 8
+// are two adjacent dims of its 16-dim scale block), 16 keys as K and the 8 query rows as N. P
+// comes in with one transposing ldmatrix per page; V goes from its E2M1 codes straight into A
+// fragments: the nibbles of two keys are interleaved into one byte per dim, converted with
+// cvt.e2m1x2 and multiplied by the two keys' E4M3 scales (E2M1 x E4M3 is exact in f16). Within a
+// 16-key step the keys are taken in a fixed permutation, the same for P and V, that keeps the
+// shared-memory reads conflict-free.
 //
 // Warp roles (320 threads): warp 0 bulk-copy producer, warp 1 Q.K^T issuer and TMEM owner, warps
 // 2..9 attention. Every wait is an mbarrier wait bounded in time; on a timeout the kernel records
@@ -332,11 +333,9 @@ struct AttnCtx {
   bool timed_out;
 };
 
-// Byte address of the P row (half 0) or of the always-zero row (half 1) of warp-local key `key`
-// in a warp's P tile: four keys per 128-byte line, the 32-byte slots and 16-byte halves permuted
-// by line so that both the row stores and the transposing ldmatrix reads are free of bank
-// conflicts. (Reading the zero half with the same x4 ldmatrix measured faster than loading only
-// the P half and passing zero registers to the MMA.)
+// Byte address of the P row (half 0 of a 32-byte slot; half 1 is not used) of warp-local key
+// `key` in a warp's P tile: four keys per 128-byte line, the slots and halves permuted by line so
+// that both the row stores and the transposing ldmatrix reads are free of bank conflicts.
 __device__ __forceinline__ uint32_t p_addr(uint32_t base, int key, int half) {
   const int q = key >> 2;
   return base + q * 128 + 32 * ((key & 3) ^ (q & 3)) + 16 * (half ^ (q & 1));
@@ -366,14 +365,14 @@ __device__ __forceinline__ void s_issue(AttnCtx& c, uint32_t kk, uint32_t (&sr)[
 
 // Finish loading page kk's scores, release the S buffer, and turn the scores into P in the P tile
 // at pt: page max per row over the warp's 32 keys (warp reductions), running max and row-sum
-// update, P = exp2((s - m) c2) <= 1 in f16. Returns whether a max grew (then alpha_g is
-// the factor for row g of the accumulator). kv_lim: keys of the page below it are real (0 when
-// the page was skipped).
+// update, P = exp2((s - m) c2) <= 1 in f16. Returns whether a max grew (then alpha_a and
+// alpha_b are the factors for rows 2t and 2t + 1 of the accumulator). kv_lim: keys of the page
+// below it are real (0 when the page was skipped).
 template <int NR>
 __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, uint32_t kst, int page, int len,
                                           const RowVis& rv, uint32_t (&sr)[8], float (&m)[kRows],
-                                          float (&lp)[kRows], uint32_t pt, int g, float c2,
-                                          float& alpha_g, int& kv_lim) {
+                                          float (&lp)[kRows], uint32_t pt, int t, float c2,
+                                          float& alpha_a, float& alpha_b, int& kv_lim) {
   tmem_wait_ld_regs(sr);
   tc_fence_before();
   __syncwarp();
@@ -403,7 +402,7 @@ __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, uint32_t kst,
   bool grow = false;  // warp-uniform: every lane holds the same maxima
 #pragma unroll
   for (int i = 0; i < NR; ++i) grow |= pm[i] > m[i];
-  alpha_g = 1.f;
+  alpha_a = alpha_b = 1.f;
   if (grow) {  // rare once the running maxima have settled
     float alpha[kRows];
 #pragma unroll
@@ -415,7 +414,8 @@ __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, uint32_t kst,
       lp[i] *= alpha[i];
       m[i] = mn;
     }
-    alpha_g = pick8(alpha, g);
+    alpha_a = pick8(alpha, 2 * t);
+    alpha_b = pick8(alpha, 2 * t + 1);
   }
   uint32_t hi[4];
 #pragma unroll
@@ -438,12 +438,12 @@ __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, uint32_t kst,
 // into B fragments: one byte per dim holding the nibbles of two keys (first key low), converted
 // by cvt.e2m1x2 and multiplied by the two keys' E4M3 scales. A key at or past kv_lim gets scale 0
 // (its code bytes are stale). All shared loads of the page are issued before the arithmetic.
-__device__ __forceinline__ void pv_page(const uint8_t* sm, uint32_t lm0, uint32_t lm1, uint32_t vco,
-                                        uint32_t vso, int key0, int kv_lim, int vk0, int vk1,
-                                        float (&acc)[16][4]) {
-  uint32_t a[2][4];
-  ldsm_x4_trans(lm0, a[0][0], a[0][1], a[0][2], a[0][3]);
-  ldsm_x4_trans(lm1, a[1][0], a[1][1], a[1][2], a[1][3]);
+__device__ __forceinline__ void pv_page(const uint8_t* sm, uint32_t lm, uint32_t vco, uint32_t vso,
+                                        int key0, int kv_lim, int vk0, int vk1,
+                                        float (&acc)[8][4]) {
+  // B fragments (P^T, keys x query rows) of both 16-key steps in one transposing ldmatrix
+  uint32_t b[2][2];
+  ldsm_x4_trans(lm, b[0][0], b[0][1], b[1][0], b[1][1]);
   uint2 wv[2][4];
   uint32_t sc[2][2];
 #pragma unroll
@@ -475,12 +475,9 @@ __device__ __forceinline__ void pv_page(const uint8_t* sm, uint32_t lm0, uint32_
       cvt_e2m1x8_f16(ze23, e2[0], e2[1], e2[2], e2[3]);
       cvt_e2m1x8_f16(zo23, o2[0], o2[1], o2[2], o2[3]);
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        mma16816(acc[8 * w + 2 * jj], a[ks][0], a[ks][1], a[ks][2], a[ks][3],
-                 hmul2(e0[jj], sc[ks][0]), hmul2(e2[jj], sc[ks][1]));
-        mma16816(acc[8 * w + 2 * jj + 1], a[ks][0], a[ks][1], a[ks][2], a[ks][3],
-                 hmul2(o0[jj], sc[ks][0]), hmul2(o2[jj], sc[ks][1]));
-      }
+      for (int jj = 0; jj < 4; ++jj)  // A rows g, g + 8: dims 16 g + 2 m, + 1 (m = 4 w + jj)
+        mma16816(acc[4 * w + jj], hmul2(e0[jj], sc[ks][0]), hmul2(o0[jj], sc[ks][0]),
+                 hmul2(e2[jj], sc[ks][1]), hmul2(o2[jj], sc[ks][1]), b[ks][0], b[ks][1]);
     }
   }
 }
@@ -657,22 +654,20 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
   c.timed_out = false;
   const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates
   const uint32_t ps = c.sbase + kOffPs + aw * kPsBytes;
-  // ldmatrix rows of this lane: matrix mi = lane / 8 is (P | zero) x (k 0..7 | k 8..15); the
-  // fragment k index maps to a warp-local key by the permutation below (also used for V)
-  uint32_t lm_addr0, lm_addr1;
+  // ldmatrix rows of this lane: matrix mi = lane / 8 is 16-key step mi / 2, fragment k indices
+  // 0..7 or 8..15 (mi % 2); the fragment k index maps to a warp-local key by the permutation
+  // below (also used for V)
+  uint32_t lm_addr;
   {
-    const int mi = lane >> 3, kidx = (mi >> 1) * 8 + (lane & 7), tt = (kidx & 7) >> 1;
+    const int mi = lane >> 3, kidx = (mi & 1) * 8 + (lane & 7), tt = (kidx & 7) >> 1;
     const int local = 4 * tt + ((kidx >> 3) << 1) + ((kidx & 1) ^ (tt & 1));
-    lm_addr0 = p_addr(ps, local, mi & 1);
-    lm_addr1 = p_addr(ps, 16 + local, mi & 1);
+    lm_addr = p_addr(ps, 16 * (mi >> 1) + local, 0);
   }
   // B fragment keys of this lane within a 16-key step: k = 2t, 2t+1, 2t+8, 2t+9 -> keys
   // 4t + {0,1,2,3} with the pair order flipped for odd t (so lanes t and t+1 read different banks)
   const int vk0 = 4 * t + (t & 1), vk1 = 4 * t + 1 - (t & 1);
   const int rows_total = p.G * p.q_len;
   const float c2 = p.c2;
-  sts128(p_addr(ps, lane, 1), 0u, 0u, 0u, 0u);  // rows 8..15 of every P.V product: zero
-  __syncwarp();
   uint32_t k = 0, ks = 0;  // pages (S buffers), stage slots
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
 
@@ -742,11 +737,11 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
     for (int i = 0; i < kRows; ++i) { m[i] = -INFINITY; lp[i] = 0.f; }
     // O accumulator: acc[dd] is the m16n8 tile of dims 16 n + dd (n = fragment column); rows
     // 0..7 are the query rows, rows 8..15 stay zero
-    float acc[16][4];
+    float acc[8][4];
 #pragma unroll
-    for (int dd = 0; dd < 16; ++dd)
+    for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-      for (int q = 0; q < 4; ++q) acc[dd][q] = 0.f;
+      for (int q = 0; q < 4; ++q) acc[mt][q] = 0.f;
 
     // Per page: scores -> running max, row sums and P (one P tile), accumulator rescale when a
     // max grew, then two 16-key steps of O += P V.
@@ -754,23 +749,24 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
     for (int j = 0; j < n; ++j, ++k, ++ks) {
       const uint32_t st = ks % kStages;
       uint32_t sr[8];
-      float alpha_g = 1.f;
+      float alpha_a = 1.f, alpha_b = 1.f;
       int kv_lim = 0;
       s_issue(c, k, sr);
-      const bool grow =
-          s_softmax<NR>(c, k, ks, sg.lo + j, sg.len, rv, sr, m, lp, ps, g, c2, alpha_g, kv_lim);
+      const bool grow = s_softmax<NR>(c, k, ks, sg.lo + j, sg.len, rv, sr, m, lp, ps, t, c2,
+                                      alpha_a, alpha_b, kv_lim);
       __syncwarp();
-      if (grow) {
+      if (grow) {  // entries 0, 2: row 2t; entries 1, 3: row 2t + 1
 #pragma unroll
-        for (int dd = 0; dd < 16; ++dd)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[dd][q] *= alpha_g;
+        for (int mt = 0; mt < 8; ++mt) {
+          acc[mt][0] *= alpha_a; acc[mt][2] *= alpha_a;
+          acc[mt][1] *= alpha_b; acc[mt][3] *= alpha_b;
+        }
       }
       if (c.active) {
         const uint32_t stage = c.sbase + kOffStage + st * kStageBytes;
         const uint32_t vc = stage + p.Hkv * 4608 + c.head * 4096 + 8 * g;  // codes of dims 16 g ..
         const uint32_t vs = stage + p.Hkv * 8704 + c.head * 512 + g;       // scale of block g
-        pv_page(smem, lm_addr0, lm_addr1, vc - c.sbase, vs - c.sbase, c.key0, kv_lim, vk0, vk1, acc);
+        pv_page(smem, lm_addr, vc - c.sbase, vs - c.sbase, c.key0, kv_lim, vk0, vk1, acc);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bars + 8 * (kBarStageEmpty + st));
@@ -787,25 +783,17 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
     const bool split = sg.n_seg > 1;
     const int part_stride = p.Hkv * kPartHeadFloats;
     if (c.active) {
-      // lane (g, t) holds row g, dims 32 t .. 32 t + 31: value v < 16 is tile v column 2t (dim
-      // 32 t + v), v >= 16 is tile v - 16 column 2t + 1 (dim 32 t + v); rows g and g + 8 (zero)
-      // summed
+      // lane (g, t) holds rows 2t and 2t + 1, dims 16 g .. 16 g + 15: acc[m][0 | 2] is row 2t,
+      // dims 16 g + 2m | 16 g + 2m + 1; acc[m][1 | 3] the same for row 2t + 1
       const uint32_t mg = c.sbase + kOffMerge + c.head * kMergeHeadBytes;
       volatile float* mml =
           reinterpret_cast<volatile float*>(smem + kOffMerge + c.head * kMergeHeadBytes + 8 * 32 * 16);
       const uint32_t hb = kNbHead0 + c.head;
       if (c.qd & 1) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          float o[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int v = 4 * q + e;
-            o[e] = v < 16 ? acc[v][0] + acc[v][2] : acc[v - 16][1] + acc[v - 16][3];
-          }
-          sts128(mg + (q * 32 + lane) * 16, __float_as_uint(o[0]), __float_as_uint(o[1]),
-                 __float_as_uint(o[2]), __float_as_uint(o[3]));
-        }
+        for (int q = 0; q < 8; ++q)
+          sts128(mg + (q * 32 + lane) * 16, __float_as_uint(acc[q][0]), __float_as_uint(acc[q][1]),
+                 __float_as_uint(acc[q][2]), __float_as_uint(acc[q][3]));
         if (lane == 0) {
 #pragma unroll
           for (int i = 0; i < kRows; ++i) { mml[i] = m[i]; mml[kRows + i] = lp[i]; }
@@ -814,44 +802,50 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
         named_barrier_sync(hb, 64);  // state read: the area is free for the next segment
       } else {
         named_barrier_sync(hb, 64);
-        const float m1 = pick8(m, g), l1 = pick8(lp, g);
-        const float m2 = mml[g], l2 = mml[kRows + g];
-        const float M = fmaxf(m1, m2);
-        const float f1 = (m1 == -INFINITY) ? 0.f : fast_exp2((m1 - M) * c2);
-        const float f2 = (m2 == -INFINITY) ? 0.f : fast_exp2((m2 - M) * c2);
-        const float L = f1 * l1 + f2 * l2;
-        float o[32];
+        float M[2], L[2], f1[2], f2[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int i = 2 * t + hh;
+          const float m1 = pick8(m, i), l1 = pick8(lp, i);
+          const float m2 = mml[i], l2 = mml[kRows + i];
+          M[hh] = fmaxf(m1, m2);
+          f1[hh] = (m1 == -INFINITY) ? 0.f : fast_exp2((m1 - M[hh]) * c2);
+          f2[hh] = (m2 == -INFINITY) ? 0.f : fast_exp2((m2 - M[hh]) * c2);
+          L[hh] = f1[hh] * l1 + f2[hh] * l2;
+        }
+        float o[2][16];  // rows 2t, 2t + 1; dims 16 g .. 16 g + 15
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const uint4 u = lds128(mg + (q * 32 + lane) * 16);
-          const float other[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
-                                  __uint_as_float(u.w)};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int v = 4 * q + e;
-            const float mine = v < 16 ? acc[v][0] + acc[v][2] : acc[v - 16][1] + acc[v - 16][3];
-            o[v] = f1 * mine + f2 * other[e];
-          }
+          o[0][2 * q] = f1[0] * acc[q][0] + f2[0] * __uint_as_float(u.x);
+          o[1][2 * q] = f1[1] * acc[q][1] + f2[1] * __uint_as_float(u.y);
+          o[0][2 * q + 1] = f1[0] * acc[q][2] + f2[0] * __uint_as_float(u.z);
+          o[1][2 * q + 1] = f1[1] * acc[q][3] + f2[1] * __uint_as_float(u.w);
         }
         named_barrier_sync(hb, 64);
-        const int r = row0 + g;
-        if (split) {
-          float* part = p.partials + (int64_t)sg.part * part_stride + c.head * kPartHeadFloats;
-          float4* dst = reinterpret_cast<float4*>(part + g * 128 + 32 * t);
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-          if (t == 0) {
-            part[kRows * 128 + g] = M;
-            part[kRows * 128 + kRows + g] = L;
+        for (int hh = 0; hh < 2; ++hh) {
+          const int i = 2 * t + hh, r = row0 + i;
+          if (split) {
+            float* part = p.partials + (int64_t)sg.part * part_stride + c.head * kPartHeadFloats;
+            float4* dst = reinterpret_cast<float4*>(part + i * 128 + 16 * g);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_float4(o[hh][4 * q], o[hh][4 * q + 1], o[hh][4 * q + 2], o[hh][4 * q + 3]);
+            if (g == 0) {
+              part[kRows * 128 + i] = M[hh];
+              part[kRows * 128 + kRows + i] = L[hh];
+            }
+          } else if (r < rows_total && L[hh] > 0.f) {
+            const int tok = r / p.G, qh = c.head * p.G + r % p.G;
+            float4* dst = reinterpret_cast<float4*>(
+                p.out + (((int64_t)sg.seq * p.q_len + tok) * p.Hq + qh) * 128 + 16 * g);
+            const float inv = 1.f / L[hh];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_float4(o[hh][4 * q] * inv, o[hh][4 * q + 1] * inv,
+                                   o[hh][4 * q + 2] * inv, o[hh][4 * q + 3] * inv);
           }
-        } else if (r < rows_total && L > 0.f) {
-          const int tok = r / p.G, qh = c.head * p.G + r % p.G;
-          float4* dst = reinterpret_cast<float4*>(
-              p.out + (((int64_t)sg.seq * p.q_len + tok) * p.Hq + qh) * 128 + 32 * t);
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(o[4 * q] / L, o[4 * q + 1] / L, o[4 * q + 2] / L, o[4 * q + 3] / L);
         }
       }
     }
