@@ -277,28 +277,29 @@ __device__ void qk_warp(const DecodeParams& p, uint8_t* smem, uint32_t tbase, in
       if (k >= kSBufs) wait_bar(bars + 8 * (kBarSFree + b), ((k / kSBufs) - 1) & 1, timed_out);
       const uint32_t stage = sbase + kOffStage + st * kStageBytes;
       const uint32_t sfs = sbase + kOffSfStage + b * 2048;
-      const int kv_lim = stage_pid[st] >= 0 ? sg.len - (sg.lo + j) * 64 : 0;  // keys < kv_lim real
-      for (int pr = 0; pr < npairs; ++pr) {
-        uint32_t w0[4], w1[4];
+      // K scales: a full head pair's are already in the page in the scale-copy order (32 rows of
+      // 16 bytes per k-half) and are copied straight from the stage; a last unpaired head's
+      // 8-byte rows are widened into the staging tile first (the absent head's half is zero)
+      const bool half_pair = (p.Hkv & 1) != 0;
+      if (half_pair) {
+        const int pr = npairs - 1;
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int hh = 2 * pr + (jj >> 1), key = 32 * (jj & 1) + lane;
-          uint2 v = make_uint2(0u, 0u);
-          if (hh < p.Hkv && key < kv_lim) v = lds64(stage + p.Hkv * 4096 + hh * 512 + key * 8);
-          w0[jj] = v.x;  // k-half 0: scales of dims 0..63
-          w1[jj] = v.y;  // k-half 1: dims 64..127
+        for (int kh = 0; kh < 2; ++kh) {
+          const uint2 v = lds64(stage + p.Hkv * 4096 + pr * 1024 + kh * 256 + lane * 8);
+          sts128(sfs + (pr * 2 + kh) * 512 + lane * 16, v.x, v.y, 0u, 0u);
         }
-        sts128(sfs + (pr * 2) * 512 + lane * 16, w0[0], w0[1], w0[2], w0[3]);
-        sts128(sfs + (pr * 2 + 1) * 512 + lane * 16, w1[0], w1[1], w1[2], w1[3]);
+        fence_async_smem();
       }
-      fence_async_smem();
       __syncwarp();
       if (lane == 0) {
         tc_fence_after();
         for (int pr = 0; pr < npairs; ++pr)
-          for (int kh = 0; kh < 2; ++kh)
-            tmem_cp_32x128b_x4(tbase + kColSfa + b * 16 + pr * 8 + kh * 4,
-                               smem_desc(sfs + (pr * 2 + kh) * 512, 16, 128));
+          for (int kh = 0; kh < 2; ++kh) {
+            const uint32_t src = (half_pair && pr == npairs - 1)
+                                     ? sfs + (pr * 2 + kh) * 512
+                                     : stage + p.Hkv * 4096 + pr * 1024 + kh * 512;
+            tmem_cp_32x128b_x4(tbase + kColSfa + b * 16 + pr * 8 + kh * 4, smem_desc(src, 16, 128));
+          }
         const uint32_t qb = sbase + kOffQ;
         for (int pr = 0; pr < npairs; ++pr) {
           for (int kh = 0; kh < 2; ++kh) {
@@ -531,17 +532,17 @@ __device__ __forceinline__ void new_kv_store(const DecodeParams& p, const NewKvR
   uint8_t* blk = p.pool_w + (int64_t)r.pid * p.Hkv * 9216;
   const int slot = r.pos % kPage;
   uint8_t* codes;
-  uint8_t* scales;
+  uint8_t* scales;  // this lane's block (lane / 4) when lane % 4 == 0
   if (r.is_k) {
     codes = blk + r.h * 4096 + (slot >> 3) * 512 + (slot & 7) * 16 + (lane >> 3) * 128 +
             ((2 * lane) & 15);
-    scales = blk + p.Hkv * 4096 + r.h * 512 + slot * 8;
+    scales = blk + kscale_offset(p.Hkv, r.h, slot, lane >> 4) + ((lane >> 2) & 3);
   } else {
     codes = blk + p.Hkv * 4608 + r.h * 4096 + slot * 64 + 2 * lane;
-    scales = blk + p.Hkv * 8704 + r.h * 512 + slot * 8;
+    scales = blk + p.Hkv * 8704 + r.h * 512 + slot * 8 + (lane >> 2);
   }
   *reinterpret_cast<uint16_t*>(codes) = (uint16_t)packed;
-  if ((lane & 3) == 0) scales[lane >> 2] = (uint8_t)sc;
+  if ((lane & 3) == 0) *scales = (uint8_t)sc;
 }
 
 // Fused step, per segment, by the attention warps: the segment's Q tile encoded from the bf16

@@ -15,6 +15,18 @@ constexpr int kPage = 64;
 constexpr int kCodeBytes = 64;   // 128 x 4 bit
 constexpr int kScaleBytes = 8;   // 128 / 16 E4M3 scales
 
+// Byte offset, within a page block of Hkv heads, of the four K block scales of k-half kh (blocks
+// 4 kh .. 4 kh + 3, dims 64 kh .. 64 kh + 63) of slot `key` of KV head h. The K scales are kept in
+// the order the tensor core's scale-factor copy reads them: for each head pair and k-half, 32
+// rows of 16 bytes, row r holding keys r and r + 32 of the pair's first head, then of its second
+// head. A last unpaired head (odd head count) has 8-byte rows (keys r and r + 32).
+__host__ __device__ __forceinline__ int kscale_offset(int Hkv, int h, int key, int kh) {
+  const int pr = h >> 1, r = key & 31, kk = key >> 5;
+  const int base = Hkv * 4096 + pr * 1024;
+  if (2 * pr + 1 < Hkv) return base + kh * 512 + r * 16 + (h & 1) * 8 + kk * 4;
+  return base + kh * 256 + r * 8 + kk * 4;
+}
+
 // ---------------------------------------------------------------------------------------------
 // Formats. E4M3 ("fn"): bias 7, subnormal step 2^-9, max finite 448 (0x7E). E2M1: bias 1, values
 // {0, 0.5, 1, 1.5, 2, 3, 4, 6}.

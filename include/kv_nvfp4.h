@@ -20,7 +20,11 @@
  *     [0, 4096 H)          K codes, head h at 4096 h, in the tensor-core tile order: byte j
  *                          (0..63) of slot k sits at (k / 8) * 512 + (j / 16) * 128 +
  *                          (k % 8) * 16 + (j % 16), i.e. 8-slot x 16-byte core tiles
- *     [4096 H, 4608 H)     K scales, head h at 4096 H + 512 h: slot k at 8 k (row-major)
+ *     [4096 H, 4608 H)     K scales, in the order the tensor core's scale-factor copy reads them:
+ *                          scale b of slot k of head h is at 4096 H + 1024 (h / 2) + 512 c
+ *                          + 16 (k % 32) + 8 (h % 2) + 4 (k / 32) + b % 4 with c = b / 4, or,
+ *                          for a last head without a partner (odd H), at 4096 H + 1024 (h / 2)
+ *                          + 256 c + 8 (k % 32) + 4 (k / 32) + b % 4
  *     [4608 H, 8704 H)     V codes, head h at 4608 H + 4096 h: slot k at 64 k (row-major)
  *     [8704 H, 9216 H)     V scales, head h at 8704 H + 512 h: slot k at 8 k (row-major)
  *   A 64-byte code row holds 128 E2M1 codes: element 2j in the low nibble of byte j, element

@@ -239,11 +239,17 @@ void orc_dequant_rows(const uint8_t* codes, const uint8_t* scales, int64_t n_row
 // Paged layout. A pool is num_pages blocks of H * 9216 bytes (H = kv_heads), one block per page
 // of 64 token slots holding every head: [K codes, H x 4096][K scales, H x 512][V codes, H x 4096]
 // [V scales, H x 512]. K codes of head h are kept in 8-slot x 16-byte tiles: byte j of slot k is
-// at h*4096 + (k/8)*512 + (j/16)*128 + (k%8)*16 + (j%16). Scales and V codes are row-major per
-// slot. Token `pos` of sequence `seq` lives in page block_table[seq * max_pages + pos / 64], slot
-// pos % 64. This gathers rows [n_tok][kv_heads][64 | 8] back out of a pool so that they can be
-// compared with oracle arrays. Returns the number of rows whose page id was outside the pool.
+// at h*4096 + (k/8)*512 + (j/16)*128 + (k%8)*16 + (j%16). K scale b of slot k of head h sits in
+// the region of head pair h/2 (1024 bytes at H*4096 + (h/2)*1024): with c = b/4 (the 64-dim half)
+// it is at c*512 + (k%32)*16 + (h%2)*8 + (k/32)*4 + b%4 for a full pair, and for a last head
+// without a partner (odd H) at c*256 + (k%32)*8 + (k/32)*4 + b%4. V codes and V scales are
+// row-major per slot. Token `pos` of sequence `seq` lives in page
+// block_table[seq * max_pages + pos / 64], slot pos % 64. This gathers rows
+// [n_tok][kv_heads][64 | 8] back out of a pool so that they can be compared with oracle arrays.
+// Returns the number of rows whose page id was outside the pool.
 // ---------------------------------------------------------------------------------------------
+static int64_t blk_kscale_pair(int64_t H, int32_t h) { return H * 4096 + (int64_t)(h / 2) * 1024; }
+
 int64_t orc_paged_gather(const uint8_t* pool, int32_t num_pages, int32_t kv_heads,
                          const int32_t* block_table, int32_t max_pages, int32_t seq,
                          int32_t pos0, int32_t n_tok, uint8_t* k_codes, uint8_t* k_scales,
@@ -271,7 +277,13 @@ int64_t orc_paged_gather(const uint8_t* pool, int32_t num_pages, int32_t kv_head
       const uint8_t* blk = pool + (int64_t)page * H * 9216;
       for (int j = 0; j < 64; ++j)
         kc[j] = blk[h * 4096 + (k / 8) * 512 + (j / 16) * 128 + (k % 8) * 16 + (j % 16)];
-      std::memcpy(ks, blk + H * 4096 + h * 512 + k * 8, 8);
+      const int64_t pair = blk_kscale_pair(H, h);
+      for (int b = 0; b < 8; ++b) {
+        const int64_t c = b / 4, within = (h % 2 == 1 || h + 1 < H)
+                                              ? c * 512 + (k % 32) * 16 + (h % 2) * 8 + (k / 32) * 4
+                                              : c * 256 + (k % 32) * 8 + (k / 32) * 4;
+        ks[b] = blk[pair + within + b % 4];
+      }
       std::memcpy(vc, blk + H * 4608 + h * 4096 + k * 64, 64);
       std::memcpy(vs, blk + H * 8704 + h * 512 + k * 8, 8);
     }

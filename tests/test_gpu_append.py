@@ -124,6 +124,7 @@ def test_append_reports_bad_rows_and_skips_them():
             expected.add(h * 4096 + (3 // 8) * 512 + (j // 16) * 128 + (3 % 8) * 16 + j % 16)
             expected.add(4 * 4608 + h * 4096 + 3 * 64 + j)
         for j in range(8):
-            expected.add(4 * 4096 + h * 512 + 3 * 8 + j)
+            # K scales in the scale-copy order (4 heads: two full pairs): slot 3, half j // 4
+            expected.add(4 * 4096 + (h // 2) * 1024 + (j // 4) * 512 + 3 * 16 + (h % 2) * 8 + j % 4)
             expected.add(4 * 8704 + h * 512 + 3 * 8 + j)
     assert set(changed.tolist()) <= expected

@@ -7,6 +7,7 @@ mapping, causal offsets, scale), and the joint-rotation invariance of Q.K^T.
 import math
 
 import numpy as np
+import pytest
 import torch
 
 import oracle
@@ -133,10 +134,11 @@ def test_quantize_rows_composes_rope_fwht_quant():
     assert np.array_equal(c, vc[3]) and np.array_equal(s, vs[3])
 
 
-def test_paged_gather_layout():
+@pytest.mark.parametrize("H", [3, 4])
+def test_paged_gather_layout(H):
     # fill every byte of a pool with a value naming (page, region, head, slot, byte) per the
     # documented block layout, then check the gather returns each slot's own bytes
-    P, H = 6, 3
+    P = 6
     blk = H * 9216
     pool = np.zeros(P * blk, np.uint8)
     for p in range(P):
@@ -147,7 +149,14 @@ def test_paged_gather_layout():
                     b[h * 4096 + (k // 8) * 512 + (j // 16) * 128 + (k % 8) * 16 + j % 16] = (p * 7 + h * 3 + k + j) % 251
                     b[H * 4608 + h * 4096 + k * 64 + j] = (p * 5 + h + 2 * k + j) % 253
                 for j in range(8):
-                    b[H * 4096 + h * 512 + k * 8 + j] = (p + h * 11 + k + 3 * j) % 241
+                    # K scale j of slot k: head pair h // 2, half c = j // 4; rows of 16 bytes
+                    # (keys k % 32, both heads) for a full pair, 8 bytes for a last lone head
+                    c, pair = j // 4, H * 4096 + (h // 2) * 1024
+                    if h % 2 == 1 or h + 1 < H:
+                        off = pair + c * 512 + (k % 32) * 16 + (h % 2) * 8 + (k // 32) * 4 + j % 4
+                    else:
+                        off = pair + c * 256 + (k % 32) * 8 + (k // 32) * 4 + j % 4
+                    b[off] = (p + h * 11 + k + 3 * j) % 241
                     b[H * 8704 + h * 512 + k * 8 + j] = (p * 13 + h + k + j) % 239
     bt = np.array([[4, 1, 5], [0, 2, 3]], np.int32)
     kc, ks, vc, vs, bad = oracle.paged_gather(pool, P, H, bt, 1, 60, 70)
