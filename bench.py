@@ -131,6 +131,14 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_bf16_tflops():
+    """Dense bf16 tensor throughput (burst: the tile kernel is timed on its own)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 def decode_traffic_profile():
     """DRAM bytes per step launch from the committed ncu summary, if it was taken on the
     current kernel source (else None)."""
@@ -362,6 +370,59 @@ def comparators(w, dev, stream, peak, reps=200):
     return res
 
 
+def tile_workloads(dev, stream, peak_gbs):
+    """Attention calls of the many-row shapes, which run on the tile kernel: the speculative
+    verify step (4 x 100,008 keys, 8 new tokens: 48 query rows per KV head) and the 600k prefill
+    chunk (8192 new tokens: 196,608 query rows over up to 600,064 keys). Both are parity cases of
+    the GPU tests; here they are timed (the cache populated by the append kernel first)."""
+    import torch
+
+    import synth
+    from kvrun import GpuRun
+    bf16, bf16_kind = measured_bf16_tflops()
+    res = {}
+    for w, chunk, reps in ((synth.spec_verify(), 1024, 200), (synth.prefill_chunk(), 1024, 5)):
+        g = GpuRun(w, device=dev)
+        g.step(chunk_tokens=chunk)  # append the new tokens with Q, plan, attend
+
+        def call():
+            g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        assert g.status() == 0, f"{w.name}: device status {g.status():#x}"
+        t = e0.elapsed_time(e1) / 1e3 / reps
+        T = w.num_seqs * w.q_len
+        kv_tokens = int(w.seq_lens.sum())
+        n_pages = int(sum((int(l) + 63) // 64 for l in w.seq_lens))
+        # (query row, visible key) pairs: Q.K^T and P.V take 2 x 128 flops each per pair
+        vis = 0
+        for L in w.seq_lens:
+            L = int(L)
+            vis += (sum(L - w.q_len + i + 1 for i in range(w.q_len)) if w.causal
+                    else L * w.q_len) * w.q_heads
+        attn_bytes = (kv_tokens * w.kv_heads * 144 + T * w.q_heads * 72 + n_pages * 4 +
+                      T * w.q_heads * 128 * 4)
+        pv_tflops = 2 * 128 * vis / t / 1e12
+        res[w.name] = {
+            "attn_us": t * 1e6, "query_rows": T * w.q_heads, "kv_tokens": kv_tokens,
+            "chunk_tokens": chunk, "kv_tokens_per_s": kv_tokens / t,
+            "hbm_gbs": attn_bytes / t / 1e9, "hbm_frac_of_measured": attn_bytes / t / 1e9 / peak_gbs,
+            "qk_plus_pv_tflops": 2 * pv_tflops, "pv_tflops": pv_tflops,
+            "pv_frac_of_bf16": pv_tflops / bf16, "bf16_peak_tflops": bf16,
+            "bf16_peak_kind": bf16_kind + " (burst)"}
+        del g
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_cuda(args, world, rank, local):
     import numpy as np
     import torch
@@ -375,6 +436,18 @@ def run_cuda(args, world, rank, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if args.profile_tile:
+        # short run of one many-row shape for the profiler: populate, then warm-up + timed calls
+        from kvrun import GpuRun as _G
+        wt = synth.spec_verify() if args.profile_tile == "verify" else synth.prefill_chunk()
+        gt = _G(wt, device=dev)
+        gt.step(chunk_tokens=1024)
+        for _ in range(args.warmup + args.steps):
+            gt.cache.attend(gt.q_codes, gt.q_scales, gt.out, sm_scale=wt.sm_scale)
+        torch.cuda.synchronize(dev)
+        assert gt.status() == 0
+        print(json.dumps({"profile_run": True, "workload": wt.name, "steps": args.steps}))
+        return
     w = synth.steady_decode()
     if args.seqs != 4:
         w = synth.Workload(f"steady_decode_{args.seqs}x128k", [131072] * args.seqs, q_len=1,
@@ -493,6 +566,7 @@ def run_cuda(args, world, rank, local):
 
     spill = spill_restore(g, dev, stream)
     cmp = None if args.no_comparators else comparators(w, dev, stream, measured_peaks()[0])
+    tiles = None if args.no_tile_workloads else tile_workloads(dev, stream, measured_peaks()[0])
 
     elapsed, e2e_elapsed = max_over_ranks([elapsed, e2e_elapsed], dev)
     if rank != 0:
@@ -544,6 +618,7 @@ def run_cuda(args, world, rank, local):
         "gpu_launches": 2 * args.steps,  # per timed step: the attention kernel, split-K merge
         "spill": spill,
         "comparators": cmp,
+        "tile_workloads": tiles,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(w)
@@ -557,6 +632,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-tile", choices=["verify", "prefill"], default=None,
+                    help="short run of the verify or prefill-chunk attention call (profiling)")
+    ap.add_argument("--no-tile-workloads", action="store_true",
+                    help="skip timing the verify and prefill-chunk shapes (tile kernel)")
     ap.add_argument("--no-comparators", action="store_true",
                     help="skip the bf16 / int8 / NVFP4 K + fp16 V comparator timings")
     ap.add_argument("--seqs", type=int, default=4, help="sequences of 131072 tokens (profiling)")

@@ -22,6 +22,7 @@ KV_NVFP4_EINVAL = -1
 KV_NVFP4_ECUDA = -2
 KV_NVFP4_ENOSPACE = -3
 DEV_BAD_PAGE, DEV_BAD_POS, DEV_BAD_SEQ, DEV_BAD_ROPE, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8, 0x10
+NOALLOC_SCRATCH_BYTES = 32 << 20  # KV_NVFP4_NOALLOC_SCRATCH_BYTES
 
 
 class Layout(ctypes.Structure):

@@ -42,6 +42,12 @@ cudaError_t launch_cmp_decode(int fmt, const uint16_t* q, const uint8_t* pool,
                               const int32_t* split_groups, int32_t num_split, float* partials,
                               float* out, int32_t* status, int32_t Hq, int32_t Hkv, int32_t q_len,
                               int32_t causal, float sm_scale, int32_t grid, cudaStream_t stream);
+cudaError_t launch_tile(const uint8_t* q_codes, const uint8_t* q_scales, const uint8_t* pool,
+                        const int32_t* block_table, int32_t max_pages, int32_t num_pages,
+                        const void* groups, const void* segments, const int32_t* cta_seg,
+                        const int32_t* split_groups, int32_t num_split, float* partials,
+                        float* out, int32_t* status, int32_t Hq, int32_t Hkv, int32_t q_len,
+                        int32_t causal, int32_t grid, float sm_scale, cudaStream_t stream);
 cudaError_t launch_page_copy(bool spill, const uint8_t* src, uint8_t* dst, const int32_t* ids,
                              int32_t n, int32_t num_pages, uint32_t page_bytes, int sms,
                              int32_t* status, cudaStream_t stream);
@@ -49,8 +55,17 @@ cudaError_t launch_page_copy(bool spill, const uint8_t* src, uint8_t* dst, const
 
 namespace {
 
-constexpr int kRowsPerItem = 8;   // query rows per KV head in one attention work group
+constexpr int kRowsPerItem = 8;   // query rows per KV head in one decode work group
 constexpr int kPartHeadFloats = kRowsPerItem * 128 + 2 * kRowsPerItem;  // O[8][128], m[8], l[8]
+// Tiles of more rows (speculative verify, prefill chunks) go to the tile kernel: groups of one
+// KV-head pair and 64 rows per head, partials of both heads of the pair per segment.
+constexpr int kTileRows = 64;
+constexpr int kTilePartFloats = 2 * (kTileRows * 128 + 2 * kTileRows);
+
+// The attention kernel a (layout, q_len) pair runs on: more than 8 rows per KV head -> tile kernel.
+bool tile_mode(const kv_nvfp4_layout* L, int32_t q_len) {
+  return (int64_t)(L->num_q_heads / L->num_kv_heads) * q_len > kRowsPerItem;
+}
 constexpr int kMaxAttnKvHeads = 4;  // the attention kernel stages every head of a page
 constexpr int kMaxGridForSizing = 1024;  // workspace sizing when no device is visible
 
@@ -77,7 +92,8 @@ int num_sms_current_device() {
 
 uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
-// The split-K work list. Groups are (sequence, kv head, 8-row query tile) in that order; each
+// The split-K work list. Groups are (sequence, 8-row query tile) over every KV head for the
+// decode kernel, or (sequence, KV-head pair, 64-row tile) for the tile kernel, in that order; each
 // group's visited pages are cut into chunks of chunk_pages, and the chunk stream of all groups is
 // dealt out to `grid` CTAs in contiguous ranges of about total_pages / grid pages each.
 struct PlanBuild {
@@ -90,16 +106,18 @@ struct PlanBuild {
 
 kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, int32_t num_seqs,
                            int32_t q_len, int32_t causal, int32_t chunk_tokens, int32_t num_sms,
-                           PlanBuild* pb) {
+                           bool tile, PlanBuild* pb) {
   if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK) return KV_NVFP4_EINVAL;
   if (h_seq_lens == nullptr || num_seqs <= 0 || q_len <= 0 || num_sms <= 0) return KV_NVFP4_EINVAL;
   if (chunk_tokens <= 0 || chunk_tokens % L->page_size != 0) return KV_NVFP4_EINVAL;
   const int32_t P = L->page_size;
   const int32_t G = L->num_q_heads / L->num_kv_heads;
   const int64_t rows = (int64_t)G * q_len;
-  const int64_t n_rg = (rows + kRowsPerItem - 1) / kRowsPerItem;
+  const int64_t tile_rows = tile ? kTileRows : kRowsPerItem;
+  const int64_t n_rg = (rows + tile_rows - 1) / tile_rows;
+  const int64_t n_pairs = tile ? (L->num_kv_heads + 1) / 2 : 1;  // groups per (sequence, tile)
   const int32_t chunk_pages = chunk_tokens / P;
-  const int64_t n_groups = (int64_t)num_seqs * n_rg;
+  const int64_t n_groups = (int64_t)num_seqs * n_pairs * n_rg;
   if (n_groups > (1 << 26)) return KV_NVFP4_EINVAL;
   int64_t total_pages = 0, total_chunks = 0, total_tok = 0, max_len = 0;
   std::vector<int32_t> gpages((size_t)n_groups);
@@ -108,17 +126,18 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
     if (len < q_len || len < 1) return KV_NVFP4_EINVAL;
     total_tok += len;
     if (len > max_len) max_len = len;
-    for (int64_t rg = 0; rg < n_rg; ++rg) {
-      int64_t vis = len;  // keys any row of the tile can see
-      if (causal) {
-        const int64_t last_row = std::min<int64_t>(rows - 1, rg * kRowsPerItem + kRowsPerItem - 1);
-        vis = (int64_t)(len - q_len) + last_row / G + 1;
+    for (int64_t pr = 0; pr < n_pairs; ++pr)
+      for (int64_t rg = 0; rg < n_rg; ++rg) {
+        int64_t vis = len;  // keys any row of the tile can see
+        if (causal) {
+          const int64_t last_row = std::min<int64_t>(rows - 1, rg * tile_rows + tile_rows - 1);
+          vis = (int64_t)(len - q_len) + last_row / G + 1;
+        }
+        const int64_t pages = (vis + P - 1) / P;
+        gpages[(size_t)(((int64_t)s * n_pairs + pr) * n_rg + rg)] = (int32_t)pages;
+        total_pages += pages;
+        total_chunks += (pages + chunk_pages - 1) / chunk_pages;
       }
-      const int64_t pages = (vis + P - 1) / P;
-      gpages[(size_t)((int64_t)s * n_rg + rg)] = (int32_t)pages;
-      total_pages += pages;
-      total_chunks += (pages + chunk_pages - 1) / chunk_pages;
-    }
   }
   const int64_t grid = std::min<int64_t>(num_sms, total_chunks);
   pb->groups.assign((size_t)n_groups * 8, 0);
@@ -169,9 +188,9 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
   for (int64_t gi = 0; gi < n_groups; ++gi)
     if (seg_count[(size_t)gi] > 1) pb->split.push_back((int32_t)gi);
   for (int64_t gi = 0; gi < n_groups; ++gi) {
-    const int64_t rg = gi % n_rg, s = gi / n_rg;
+    const int64_t rg = gi % n_rg, pr = (gi / n_rg) % n_pairs, s = gi / (n_rg * n_pairs);
     int32_t* g = &pb->groups[(size_t)gi * 8];
-    g[0] = (int32_t)s; g[1] = 0; g[2] = (int32_t)rg; g[3] = h_seq_lens[s];
+    g[0] = (int32_t)s; g[1] = (int32_t)pr; g[2] = (int32_t)rg; g[3] = h_seq_lens[s];
     g[4] = seg_count[(size_t)gi]; g[5] = first_part[(size_t)gi]; g[6] = gpages[(size_t)gi]; g[7] = 0;
   }
   kv_nvfp4_plan_info* info = &pb->info;
@@ -200,7 +219,9 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
   info->off_split = off;
   off = align_up(off + 4ull * pb->split.size(), 256);
   info->off_partials = off;
-  off = align_up(off + 4ull * kPartHeadFloats * L->num_kv_heads * parts, 256);
+  const uint64_t part_floats =
+      tile ? (uint64_t)kTilePartFloats : (uint64_t)kPartHeadFloats * L->num_kv_heads;
+  off = align_up(off + 4ull * part_floats * parts, 256);
   info->workspace_bytes = off;
   return KV_NVFP4_OK;
 }
@@ -230,11 +251,11 @@ namespace {
 // the device workspace with one copy on the stream.
 kv_nvfp4_status plan_upload(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, int32_t num_seqs,
                             int32_t q_len, int32_t causal, int32_t chunk_tokens, int num_ctas,
-                            void* d_workspace, size_t ws_bytes, kv_nvfp4_plan_info* info,
-                            void* stream) {
+                            bool tile, void* d_workspace, size_t ws_bytes,
+                            kv_nvfp4_plan_info* info, void* stream) {
   PlanBuild pb;
   const kv_nvfp4_status s =
-      plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_ctas, &pb);
+      plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_ctas, tile, &pb);
   if (s != KV_NVFP4_OK) return s;
   const kv_nvfp4_plan_info& pi = pb.info;
   if (ws_bytes < pi.workspace_bytes) return KV_NVFP4_ENOSPACE;
@@ -405,9 +426,10 @@ kv_nvfp4_status kv_nvfp4_plan_workspace_bytes(const kv_nvfp4_layout* L, const in
   if (bytes == nullptr) return KV_NVFP4_EINVAL;
   int num_sms = num_sms_current_device();
   if (num_sms <= 0) num_sms = kMaxGridForSizing;  // no device: size for the largest grid
+  if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK) return KV_NVFP4_EINVAL;
   PlanBuild pb;
-  const kv_nvfp4_status s =
-      plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_sms, &pb);
+  const kv_nvfp4_status s = plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens,
+                                       num_sms, tile_mode(L, q_len), &pb);
   if (s != KV_NVFP4_OK) return s;
   *bytes = (size_t)pb.info.workspace_bytes;
   return KV_NVFP4_OK;
@@ -418,9 +440,10 @@ kv_nvfp4_status kv_nvfp4_plan_host(const kv_nvfp4_layout* L, const int32_t* h_se
                                    int32_t chunk_tokens, int32_t num_ctas, void* h_workspace,
                                    size_t ws_bytes, kv_nvfp4_plan_info* info) {
   if (info == nullptr || h_workspace == nullptr || num_ctas <= 0) return KV_NVFP4_EINVAL;
+  if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK) return KV_NVFP4_EINVAL;
   PlanBuild pb;
-  const kv_nvfp4_status s =
-      plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_ctas, &pb);
+  const kv_nvfp4_status s = plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens,
+                                       num_ctas, tile_mode(L, q_len), &pb);
   if (s != KV_NVFP4_OK) return s;
   const kv_nvfp4_plan_info& pi = pb.info;
   if (ws_bytes < pi.workspace_bytes) return KV_NVFP4_ENOSPACE;
@@ -439,10 +462,11 @@ kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout* L, const int32_t* h_seq_len
                               int32_t chunk_tokens, void* d_workspace, size_t ws_bytes,
                               kv_nvfp4_plan_info* info, void* stream) {
   if (info == nullptr || d_workspace == nullptr || !aligned16(d_workspace)) return KV_NVFP4_EINVAL;
+  if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK) return KV_NVFP4_EINVAL;
   const int num_sms = num_sms_current_device();
   if (num_sms <= 0) return cuda_status(cudaErrorNoDevice);
-  return plan_upload(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_sms, d_workspace,
-                     ws_bytes, info, stream);
+  return plan_upload(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_sms,
+                     tile_mode(L, q_len), d_workspace, ws_bytes, info, stream);
 }
 
 kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout* L, const kv_nvfp4_plan_info* plan,
@@ -465,14 +489,31 @@ kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout* L, const kv_nvfp4_pl
   for (const void* p : ptrs)
     if (!aligned16(p)) return KV_NVFP4_EINVAL;
   if (!(sm_scale > 0.0f)) sm_scale = 1.0f / std::sqrt((float)L->head_dim);
+  // the plan's tiling must be the one this layout and q_len run on
+  const bool tile = tile_mode(L, plan->q_len);
+  const int64_t rows = (int64_t)(L->num_q_heads / L->num_kv_heads) * plan->q_len;
+  const int64_t tile_rows = tile ? kTileRows : kRowsPerItem;
+  if (plan->num_row_groups != (rows + tile_rows - 1) / tile_rows) return KV_NVFP4_EINVAL;
   char* ws = (char*)d_workspace;
-  const cudaError_t e = kvnvfp4::launch_decode(
-      q_codes, q_scales, pool, d_block_table, max_pages, num_pages, ws + plan->off_groups,
-      ws + plan->off_segments, (const int32_t*)(ws + plan->off_cta),
-      (const int32_t*)(ws + plan->off_split), plan->num_split_groups,
-      (float*)(ws + plan->off_partials), out, d_status,
-      L->num_q_heads, L->num_kv_heads, plan->q_len, plan->causal, plan->grid, sm_scale,
-      nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, nullptr, nullptr, (cudaStream_t)stream);
+  cudaError_t e;
+  if (tile) {
+    e = kvnvfp4::launch_tile(q_codes, q_scales, pool, d_block_table, max_pages, num_pages,
+                             ws + plan->off_groups, ws + plan->off_segments,
+                             (const int32_t*)(ws + plan->off_cta),
+                             (const int32_t*)(ws + plan->off_split), plan->num_split_groups,
+                             (float*)(ws + plan->off_partials), out, d_status, L->num_q_heads,
+                             L->num_kv_heads, plan->q_len, plan->causal, plan->grid, sm_scale,
+                             (cudaStream_t)stream);
+  } else {
+    e = kvnvfp4::launch_decode(
+        q_codes, q_scales, pool, d_block_table, max_pages, num_pages, ws + plan->off_groups,
+        ws + plan->off_segments, (const int32_t*)(ws + plan->off_cta),
+        (const int32_t*)(ws + plan->off_split), plan->num_split_groups,
+        (float*)(ws + plan->off_partials), out, d_status,
+        L->num_q_heads, L->num_kv_heads, plan->q_len, plan->causal, plan->grid, sm_scale,
+        nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, nullptr, nullptr,
+        (cudaStream_t)stream);
+  }
   return cuda_status(e);
 }
 
@@ -553,7 +594,7 @@ kv_nvfp4_status kv_cmp_plan_workspace_bytes(const kv_nvfp4_layout* L, const int3
   const int ctas = num_sms / L->num_kv_heads > 0 ? num_sms / L->num_kv_heads : 1;
   PlanBuild pb;
   const kv_nvfp4_status s =
-      plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, ctas, &pb);
+      plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, ctas, false, &pb);
   if (s != KV_NVFP4_OK) return s;
   *bytes = (size_t)pb.info.workspace_bytes;
   return KV_NVFP4_OK;
@@ -569,8 +610,8 @@ kv_nvfp4_status kv_cmp_plan(const kv_nvfp4_layout* L, const int32_t* h_seq_lens,
   const int num_sms = num_sms_current_device();
   if (num_sms <= 0) return cuda_status(cudaErrorNoDevice);
   const int ctas = num_sms / L->num_kv_heads > 0 ? num_sms / L->num_kv_heads : 1;
-  return plan_upload(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, ctas, d_workspace,
-                     ws_bytes, info, stream);
+  return plan_upload(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, ctas, false,
+                     d_workspace, ws_bytes, info, stream);
 }
 
 kv_nvfp4_status kv_cmp_decode_attn(const kv_nvfp4_layout* L, int32_t fmt,

@@ -81,12 +81,14 @@ typedef struct kv_nvfp4_layout {
   int32_t rot_dim;      /* 32 = 25 % of 128 [YaRN] */
 } kv_nvfp4_layout;
 
-/* Filled by kv_nvfp4_plan; passed unchanged to kv_nvfp4_decode_attn. A group is one
- * (sequence, tile of 8 query rows per KV head), covering every KV head; its pages are split into
- * chunks of chunk_pages pages, and the chunks of all groups are shared out over `grid` CTAs in
+/* Filled by kv_nvfp4_plan; passed unchanged to kv_nvfp4_decode_attn. A row is (query token, head
+ * within the GQA group): row = token * group + head_in_group, group * q_len rows per KV head.
+ * With at most 8 rows per KV head (decode) a group is one (sequence, tile of 8 rows), covering
+ * every KV head; with more (speculative verify, prefill chunks) a group is one (sequence, KV-head
+ * pair, tile of 64 rows per head), run by the tile kernel. A group's pages are split into chunks
+ * of chunk_pages pages, and the chunks of all groups are shared out over `grid` CTAs in
  * contiguous, page-balanced ranges (one range may hold several chunks of a group, which the CTA
- * combines as it goes). A row is (query token, head within the GQA group): row = token * group +
- * head_in_group. */
+ * combines as it goes). */
 typedef struct kv_nvfp4_plan_info {
   int32_t num_seqs;
   int32_t q_len;
@@ -94,8 +96,10 @@ typedef struct kv_nvfp4_plan_info {
                               visible key of a row tile are not visited) */
   int32_t chunk_pages;     /* split-K granularity, in pages */
   int32_t num_kv_heads;
-  int32_t num_row_groups;  /* ceil(group * q_len / 8) row tiles per sequence */
-  int32_t num_groups;      /* num_seqs * num_row_groups */
+  int32_t num_row_groups;  /* row tiles per sequence: ceil(group * q_len / 8), or
+                              ceil(group * q_len / 64) when group * q_len > 8 */
+  int32_t num_groups;      /* num_seqs * num_row_groups, times ceil(num_kv_heads / 2) head
+                              pairs when group * q_len > 8 */
   int32_t num_segments;    /* contiguous (group, page range) pieces over all CTAs */
   int32_t num_partials;    /* partial-result slots (segments of groups split over CTAs) */
   int32_t grid;            /* CTAs of the attention launch, at most the SM count */
@@ -175,7 +179,8 @@ kv_nvfp4_status kv_nvfp4_append(const kv_nvfp4_layout *layout, const void *q, co
  * split-K granularity: a sequence is only ever cut between chunks. 1024 suits long-context
  * decode; 64 lets the plan balance the CTAs to the page. The workspace holds the group and
  * segment tables, the list of split groups (those that span more than one CTA), and one
- * 4160-byte (m, l, O) partial per KV head and segment of every split group. */
+ * (m, l, O) partial per segment of every split group: 4160 bytes per KV head for 8-row tiles,
+ * 2 x 33,280 bytes (both heads of the pair) for 64-row tiles. */
 kv_nvfp4_status kv_nvfp4_plan_workspace_bytes(const kv_nvfp4_layout *layout,
                                               const int32_t *h_seq_lens, int32_t num_seqs,
                                               int32_t q_len, int32_t causal,
@@ -184,7 +189,8 @@ kv_nvfp4_status kv_nvfp4_plan_workspace_bytes(const kv_nvfp4_layout *layout,
 /* Host-only variant of kv_nvfp4_plan for a given CTA count: writes the image of the workspace
  * tables (groups, segments, per-CTA segment ranges, split-group list; everything before
  * info->off_partials) into HOST memory h_workspace and fills *info. No CUDA call. Layout of the
- * image: groups are 8 int32 {seq, 0, row_tile, seq_len, n_segments, first_partial, pages, 0};
+ * image: groups are 8 int32 {seq, pair, row_tile, seq_len, n_segments, first_partial, pages, 0}
+ * (pair = 0 for 8-row tiles, which cover every KV head);
  * segments are 4 int32 {group, page_lo, page_hi, partial or -1}; CTA b owns segments
  * [cta[b], cta[b+1]); the split list holds info->num_split_groups group indices in order. */
 kv_nvfp4_status kv_nvfp4_plan_host(const kv_nvfp4_layout *layout, const int32_t *h_seq_lens,
@@ -195,8 +201,7 @@ kv_nvfp4_status kv_nvfp4_plan_host(const kv_nvfp4_layout *layout, const int32_t 
 /* Writes the work list into DEVICE memory d_workspace (ws_bytes at least the size above) on
  * `stream` (one host-to-device copy) and fills *info (HOST). Every seq_len must be >= q_len
  * and >= 1. The CTA count is taken from the current device's SM count. The workspace holds
- * one (m, l, O) partial of num_kv_heads * 4160 bytes per segment of a group spread over several
- * CTAs. */
+ * one (m, l, O) partial per segment of a group spread over several CTAs (sizes above). */
 kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout *layout, const int32_t *h_seq_lens,
                               int32_t num_seqs, int32_t q_len, int32_t causal,
                               int32_t chunk_tokens, void *d_workspace, size_t ws_bytes,
@@ -216,8 +221,12 @@ kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout *layout, const int32_t *h_se
  *   out:            DEVICE fp32 [num_seqs * q_len][num_q_heads][128]
  * Supports num_kv_heads <= 4 (every head of a page is staged together). Two kernel launches on
  * `stream`: the attention kernel (one persistent CTA per SM), then, when the plan has split groups,
- * the merge of their partials (one CTA per split group, KV head and row). The workspace may be
- * reused by the next call on the same stream; calls that overlap on one workspace race. */
+ * the merge of their partials (one CTA per split group, KV head and row). With at most 8 rows per
+ * KV head the attention kernel is the decode kernel (Q.K^T block-scaled on the tensor cores, P.V
+ * on the warp-level tensor path); with more rows it is the tile kernel (64 rows of each head of a
+ * KV-head pair per tile; Q.K^T block-scaled and P.V in f16, both on the tcgen05 tensor cores, O
+ * accumulated in tensor memory). The workspace may be reused by the next call on the same stream;
+ * calls that overlap on one workspace race. */
 kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout *layout,
                                      const kv_nvfp4_plan_info *plan, void *d_workspace,
                                      const uint8_t *q_codes, const uint8_t *q_scales,
@@ -344,7 +353,7 @@ kv_nvfp4_status kv_nvfp4_restore_pages(const kv_nvfp4_layout *layout, const uint
  * each rewrites its work list before its kernels read it and nothing in it has to start at zero,
  * but calls whose kernels overlap on the GPU (other streams, other host threads) corrupt each
  * other's results and must be serialised by the caller. */
-#define KV_NVFP4_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define KV_NVFP4_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 kv_nvfp4_status kv_nvfp4_decode_attn_noalloc(const kv_nvfp4_layout *layout,
                                              const int32_t *h_seq_lens, int32_t num_seqs,

@@ -67,3 +67,41 @@ def test_attention_skips_bad_pages_and_flags_them():
     torch.cuda.synchronize()
     assert g.status() & kv.DEV_BAD_PAGE
     assert np.all(np.isfinite(g.output()))
+
+
+# More than 8 rows per KV head run on the tile kernel (64 rows of each head of a KV-head pair per
+# tile, both products on the tcgen05 tensor cores).
+@pytest.mark.parametrize("lens,q_len,causal,chunk", [
+    ([300, 2000], 16, True, 256),        # 96 rows: a full 64-row tile and a ragged one
+    ([257, 1000], 12, False, 128),       # 72 rows, every key visible
+    ([3000], 256, True, 64),             # 1536 rows, 24 tiles per pair: many segments per CTA
+    ([64, 65, 129], 2, True, 64),        # 12 rows; sequences ending on and just past a page
+    ([4100], 11, True, 4160),            # one chunk per group: groups not split
+])
+def test_tile_kernel_shapes(lens, q_len, causal, chunk):
+    w = synth.Workload("tile", lens, q_len=q_len, causal=causal, seed=q_len * 7 + len(lens),
+                       chunk_tokens=chunk, pool_pages=sum((c + q_len + 63) // 64 for c in lens) + 3)
+    _check(w, chunk=chunk, steps=2)
+
+
+@pytest.mark.parametrize("Hq,Hkv,q_len", [(8, 1, 5), (9, 3, 5), (16, 2, 3), (6, 3, 9), (12, 4, 4)])
+def test_tile_kernel_group_sizes(Hq, Hkv, q_len):
+    # odd head counts leave the last pair with one head
+    w = synth.Workload("tile_groups", [200, 1300], q_len=q_len, seed=Hq * 10 + Hkv, q_heads=Hq,
+                       kv_heads=Hkv, chunk_tokens=128)
+    _check(w, chunk=128)
+
+
+def test_tile_kernel_skips_bad_pages_and_flags_them():
+    import bit_kv_cache_03_gb300 as kv
+    w = synth.Workload("tile_badpage", [700], q_len=8, seed=11, pool_pages=20)
+    g = GpuRun(w)
+    g.step()
+    torch.cuda.synchronize()
+    assert g.status() == 0
+    bt = g.cache.block_table
+    bt[0, 3] = 10 ** 6
+    g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
+    torch.cuda.synchronize()
+    assert g.status() & kv.DEV_BAD_PAGE
+    assert np.all(np.isfinite(g.output()))

@@ -103,24 +103,30 @@ def test_entry_points_reject_bad_arguments_before_cuda(kv):
     assert kv.lib().kv_nvfp4_status_string(-1) == b"invalid argument"
 
 
-@pytest.mark.parametrize("lens,q_len,causal,chunk,ctas", [
-    ([131073] * 4, 1, True, 64, 152), ([131073] * 4, 1, True, 1024, 152),
-    ([5, 70, 1000, 200000], 1, True, 1024, 152), ([100008] * 4, 8, True, 1024, 152),
-    ([3], 1, True, 64, 152), ([600064], 8192, True, 64, 152), ([2000, 37], 8, False, 256, 7),
+@pytest.mark.parametrize("lens,q_len,causal,chunk,ctas,Hq,Hkv", [
+    ([131073] * 4, 1, True, 64, 152, 24, 4), ([131073] * 4, 1, True, 1024, 152, 24, 4),
+    ([5, 70, 1000, 200000], 1, True, 1024, 152, 24, 4), ([100008] * 4, 8, True, 1024, 152, 24, 4),
+    ([3], 1, True, 64, 152, 24, 4), ([600064], 8192, True, 64, 152, 24, 4),
+    ([2000, 37], 8, False, 256, 7, 24, 4), ([900, 3000], 5, True, 128, 11, 9, 3),
+    ([70, 4000], 3, True, 64, 20, 8, 1), ([500], 1, True, 64, 9, 9, 3),
 ])
-def test_plan_covers_every_visible_page_once_and_balances(kv, lens, q_len, causal, chunk, ctas):
-    L = kv.make_layout()
+def test_plan_covers_every_visible_page_once_and_balances(kv, lens, q_len, causal, chunk, ctas,
+                                                          Hq, Hkv):
+    L = kv.make_layout(Hq, Hkv)
     info, groups, segs, cta, split = kv.kv_nvfp4_plan_host(L, lens, q_len, causal, chunk, ctas)
-    G = 6
-    n_rg = (G * q_len + 7) // 8
-    assert info.num_groups == len(lens) * n_rg == len(groups)
+    G = Hq // Hkv
+    # at most 8 rows per KV head: 8-row tiles over every head; more: 64-row tiles per head pair
+    tile_rows, n_pairs = (8, 1) if G * q_len <= 8 else (64, (Hkv + 1) // 2)
+    n_rg = (G * q_len + tile_rows - 1) // tile_rows
+    assert info.num_row_groups == n_rg
+    assert info.num_groups == len(lens) * n_pairs * n_rg == len(groups)
     # expected visited pages per group: up to the last key any row of the tile can see
     gi = np.arange(len(groups))
-    s_, rg_ = groups[:, 0], groups[:, 2]
-    assert np.all(groups[:, 1] == 0)
-    assert np.array_equal(gi, s_ * n_rg + rg_)
+    s_, pr_, rg_ = groups[:, 0], groups[:, 1], groups[:, 2]
+    assert np.all((pr_ >= 0) & (pr_ < n_pairs))
+    assert np.array_equal(gi, (s_ * n_pairs + pr_) * n_rg + rg_)
     assert np.array_equal(groups[:, 3], np.asarray(lens)[s_])
-    last_row = np.minimum(G * q_len - 1, 8 * rg_ + 7)
+    last_row = np.minimum(G * q_len - 1, tile_rows * rg_ + tile_rows - 1)
     vis = (groups[:, 3] - q_len + last_row // G + 1) if causal else groups[:, 3]
     assert np.array_equal(groups[:, 6], (vis + 63) // 64)
     # segments tile each group's [0, pages) exactly, in order, cut only at chunk boundaries
@@ -197,3 +203,19 @@ def test_comparator_sizes_and_rejections_before_cuda(kv):
                                   1, 256, 1, 256, None, None) == EINVAL
     n = kv.kv_cmp_plan_workspace_bytes(L, [131073] * 4, 1, True, 64)
     assert n > 0
+
+
+def test_noalloc_buffer_size_matches_the_header(kv):
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                            "kv_nvfp4.h")).read()
+    m = re.search(r"#define KV_NVFP4_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", hdr)
+    assert m is not None
+    assert int(m.group(1)) << int(m.group(2)) == kv.NOALLOC_SCRATCH_BYTES
+    # on a 152-SM GPU the 64-row-tile plans of the verify shape (4 x 100,008 tokens, 8 new each)
+    # and of the 600k prefill chunk fit the buffer
+    L = kv.make_layout()
+    for lens, q_len in (([100008] * 4, 8), ([600064], 8192)):
+        info = kv.kv_nvfp4_plan_host(L, lens, q_len, True, 1024, 152)[0]
+        assert info.workspace_bytes <= kv.NOALLOC_SCRATCH_BYTES
