@@ -52,15 +52,15 @@ struct AppendParams {
 struct RowTarget {
   const uint16_t* src;  // bf16 row
   uint8_t* codes;       // code destination, or nullptr to skip the row
-  uint8_t* scales;      // 8-byte destination (K rows: blocks 0..3 here, 4..7 at scales_hi)
-  uint8_t* scales_hi;
+  uint8_t* scales;      // scales of blocks 0..3; blocks 4..7 at scales + hi_step
+  int32_t hi_step;      // 4, or for K rows the distance to the second 64-dim half's scales
   int32_t pos;          // position, for RoPE
   bool rotate;
   bool tiled;           // K codes: 16-byte pieces 128 bytes apart (tensor-core tile order)
 };
 
 __device__ __forceinline__ RowTarget locate_row(const AppendParams& p, int64_t row, int lane) {
-  RowTarget r{nullptr, nullptr, nullptr, nullptr, 0, false, false};
+  RowTarget r{nullptr, nullptr, nullptr, 4, 0, false, false};
   const int32_t per_tok = p.Hq + 2 * p.Hkv;
   const int64_t t = row / per_tok;
   const int32_t w = (int32_t)(row - t * per_tok);
@@ -81,7 +81,6 @@ __device__ __forceinline__ RowTarget locate_row(const AppendParams& p, int64_t r
     r.src = p.q + (t * p.Hq + w) * kHeadDim;
     r.codes = p.q_codes + (t * p.Hq + w) * kCodeBytes;
     r.scales = p.q_scales + (t * p.Hq + w) * kScaleBytes;
-    r.scales_hi = r.scales + 4;
     r.rotate = true;
   } else {
     const int32_t kv = w - p.Hq;
@@ -100,11 +99,10 @@ __device__ __forceinline__ RowTarget locate_row(const AppendParams& p, int64_t r
     if (is_k) {
       r.codes = blk + h * 4096 + (k >> 3) * 512 + (k & 7) * 16;  // + chunk * 128 + byte % 16
       r.scales = blk + kscale_offset(p.Hkv, h, k, 0);
-      r.scales_hi = blk + kscale_offset(p.Hkv, h, k, 1);
+      r.hi_step = kscale_offset(p.Hkv, h, k, 1) - kscale_offset(p.Hkv, h, k, 0);
     } else {
       r.codes = blk + p.Hkv * 4608 + h * 4096 + k * 64;
       r.scales = blk + p.Hkv * 8704 + h * 512 + k * 8;
-      r.scales_hi = r.scales + 4;
     }
     r.tiled = is_k;
     r.rotate = is_k;
@@ -127,11 +125,11 @@ __device__ __forceinline__ void quantize_store_row(float (&x)[4], const RowTarge
     // lane l holds code bytes 2l, 2l+1 of the row: 16-byte piece l / 8, offset (2l) % 16
     uint8_t* dst = r.tiled ? r.codes + (lane >> 3) * 128 + ((2 * lane) & 15) : r.codes + 2 * lane;
     *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
-    if ((lane & 3) == 0) (lane < 16 ? r.scales : r.scales_hi)[(lane >> 2) & 3] = (uint8_t)sc;
+    if ((lane & 3) == 0) r.scales[(lane < 16 ? 0 : r.hi_step) + ((lane >> 2) & 3)] = (uint8_t)sc;
   }
 }
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) append_kernel(const AppendParams p) {
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, 4) append_kernel(const AppendParams p) {
   // Launched as a programmatic dependent of the previous kernel on the stream (e.g. the attention
   // of the previous step, which reads the pool): wait for it before touching memory, then let the
   // next kernel (the attention of this step) start its launch while this one runs; that kernel
