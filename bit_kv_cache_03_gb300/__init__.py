@@ -72,6 +72,10 @@ _SIG = {
                               ctypes.c_float, _P, _I32, _P, _I32, _P, _P, _P], _I32),
     "kv_nvfp4_decode_step": ([ctypes.POINTER(Layout), ctypes.POINTER(PlanInfo), _P, _P, _P, _P, _P,
                               _I32, _P, _I32, _I32, _P, _P, _P, ctypes.c_float, _P, _P, _P], _I32),
+    "kv_nvfp4_decode_step_host": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32, _P,
+                                   ctypes.c_size_t, _P, _P, _P, _P, _P, _P, _P, _I32, _P, _I32,
+                                   _I32, _P, ctypes.c_float, _P, _P, _P, ctypes.POINTER(PlanInfo),
+                                   _P], _I32),
     "kv_nvfp4_decode_attn_noalloc": ([ctypes.POINTER(Layout), _P, _I32, _I32, _I32, _I32, _P, _P,
                                       ctypes.c_float, _P, _I32, _P, _I32, _P, _P, _P], _I32),
     "kv_cmp_page_bytes": ([ctypes.POINTER(Layout), _I32], ctypes.c_size_t),
@@ -251,6 +255,24 @@ def kv_nvfp4_decode_step(layout, plan: PlanInfo, workspace, q, k, v, rope, rope_
         _ptr(rope), rope_max_pos, _ptr(block_table), max_pages, num_pages, _ptr(pool),
         _ptr(q_codes_out), _ptr(q_scales_out), float(sm_scale), _ptr(out), _ptr(status),
         _stream(stream)), "kv_nvfp4_decode_step")
+
+
+def kv_nvfp4_decode_step_host(layout, seq_lens, q_len, causal, chunk_tokens, workspace, ws_bytes,
+                              h_q, h_k, h_v, d_q, d_k, d_v, rope, rope_max_pos, block_table,
+                              max_pages, num_pages, pool, sm_scale, d_out, h_out, status=None,
+                              stream=None, plan_out=None):
+    """One decode step from host buffers (see the header). seq_lens: int32 host lengths; h_*:
+    host tensors (page-locked for asynchronous copies); d_*: device tensors."""
+    import numpy as np
+    sl = seq_lens if (isinstance(seq_lens, np.ndarray) and seq_lens.dtype == np.int32 and
+                      seq_lens.flags.c_contiguous) else np.ascontiguousarray(seq_lens, np.int32)
+    _check(lib().kv_nvfp4_decode_step_host(
+        ctypes.byref(layout), sl.ctypes.data, len(sl), q_len, int(causal), chunk_tokens,
+        _ptr(workspace), ws_bytes, _ptr(h_q), _ptr(h_k), _ptr(h_v), _ptr(d_q), _ptr(d_k),
+        _ptr(d_v), _ptr(rope), rope_max_pos, _ptr(block_table), max_pages, num_pages, _ptr(pool),
+        float(sm_scale), _ptr(d_out), _ptr(h_out), _ptr(status),
+        ctypes.byref(plan_out) if plan_out is not None else None, _stream(stream)),
+        "kv_nvfp4_decode_step_host")
 
 
 # ---- comparator formats (bf16, int8, NVFP4 K + fp16 V) ----

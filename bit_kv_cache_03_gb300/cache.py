@@ -9,9 +9,9 @@ import math
 import numpy as np
 import torch
 
-from . import (kv_nvfp4_append, kv_nvfp4_decode_attn, kv_nvfp4_decode_step, kv_nvfp4_plan,
-               kv_nvfp4_plan_workspace_bytes, kv_nvfp4_pool_bytes, kv_nvfp4_rope_table_init,
-               make_layout)
+from . import (kv_nvfp4_append, kv_nvfp4_decode_attn, kv_nvfp4_decode_step,
+               kv_nvfp4_decode_step_host, kv_nvfp4_plan, kv_nvfp4_plan_workspace_bytes,
+               kv_nvfp4_pool_bytes, kv_nvfp4_rope_table_init, make_layout)
 
 
 class PagedNVFP4Cache:
@@ -74,3 +74,17 @@ class PagedNVFP4Cache:
         kv_nvfp4_decode_step(self.layout, self.plan_info, self.workspace, q, k, v, self.rope,
                              self.max_pos, self.block_table, self.max_pages, self.num_pages,
                              self.pool, q_codes, q_scales, sm_scale, out, self.status, stream)
+
+    # -- one decode step from host buffers -------------------------------------------------------
+    def decode_step_host(self, seq_lens, q_len, h_q, h_k, h_v, d_q, d_k, d_v, d_out, h_out,
+                         causal=True, chunk_tokens=1024, sm_scale=None, stream=None):
+        """Plan, host-to-device copies of the new tokens, the fused step and the device-to-host
+        copy of the output, enqueued by one library call (the workspace must already be large
+        enough: call plan() once with the same shape first)."""
+        if sm_scale is None:
+            sm_scale = 1.0 / math.sqrt(128)
+        kv_nvfp4_decode_step_host(self.layout, seq_lens, q_len, causal, chunk_tokens,
+                                  self.workspace, self.workspace.numel(), h_q, h_k, h_v, d_q, d_k,
+                                  d_v, self.rope, self.max_pos, self.block_table, self.max_pages,
+                                  self.num_pages, self.pool, sm_scale, d_out, h_out, self.status,
+                                  stream)

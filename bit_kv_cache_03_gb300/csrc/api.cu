@@ -556,6 +556,47 @@ kv_nvfp4_status kv_nvfp4_decode_step(const kv_nvfp4_layout* L, const kv_nvfp4_pl
 }
 
 
+kv_nvfp4_status kv_nvfp4_decode_step_host(
+    const kv_nvfp4_layout* L, const int32_t* h_seq_lens, int32_t num_seqs, int32_t q_len,
+    int32_t causal, int32_t chunk_tokens, void* d_workspace, size_t ws_bytes, const void* h_q,
+    const void* h_k, const void* h_v, void* d_q, void* d_k, void* d_v, const float* d_rope_table,
+    int32_t rope_max_pos, const int32_t* d_block_table, int32_t max_pages, int32_t num_pages,
+    uint8_t* pool, float sm_scale, float* d_out, float* h_out, int32_t* d_status,
+    kv_nvfp4_plan_info* plan_out, void* stream) {
+  if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || h_seq_lens == nullptr || num_seqs <= 0 ||
+      q_len <= 0)
+    return KV_NVFP4_EINVAL;
+  if (!h_q || !h_k || !h_v || !d_q || !d_k || !d_v || !h_out || !d_out || !d_workspace ||
+      !aligned16(d_workspace))
+    return KV_NVFP4_EINVAL;
+  // the same checks as the fused step, before anything is enqueued
+  if (L->num_kv_heads > kMaxAttnKvHeads ||
+      (int64_t)(L->num_q_heads / L->num_kv_heads) * q_len > kRowsPerItem)
+    return KV_NVFP4_EINVAL;
+  const int num_sms = num_sms_current_device();
+  if (num_sms <= 0) return cuda_status(cudaErrorNoDevice);
+  const cudaStream_t st = (cudaStream_t)stream;
+  const size_t rows = (size_t)num_seqs * (size_t)q_len;
+  const size_t qb = rows * (size_t)L->num_q_heads * 256, kb = rows * (size_t)L->num_kv_heads * 256;
+  const size_t ob = rows * (size_t)L->num_q_heads * 128 * 4;
+  cudaError_t e = cudaMemcpyAsync(d_q, h_q, qb, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(d_k, h_k, kb, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(d_v, h_v, kb, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  kv_nvfp4_plan_info info;
+  kv_nvfp4_status s = plan_upload(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_sms,
+                                  false, d_workspace, ws_bytes, &info, stream);
+  if (s != KV_NVFP4_OK) return s;
+  s = kv_nvfp4_decode_step(L, &info, d_workspace, d_q, d_k, d_v, d_rope_table, rope_max_pos,
+                           d_block_table, max_pages, num_pages, pool, nullptr, nullptr, sm_scale,
+                           d_out, d_status, stream);
+  if (s != KV_NVFP4_OK) return s;
+  e = cudaMemcpyAsync(h_out, d_out, ob, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (plan_out != nullptr) *plan_out = info;
+  return KV_NVFP4_OK;
+}
+
 // ---- comparator formats -----------------------------------------------------------------------
 size_t kv_cmp_page_bytes(const kv_nvfp4_layout* L, int32_t fmt) {
   if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || fmt < KV_CMP_BF16 || fmt > KV_CMP_K4V16) return 0;

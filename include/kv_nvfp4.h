@@ -259,6 +259,34 @@ kv_nvfp4_status kv_nvfp4_decode_step(const kv_nvfp4_layout *layout,
                                      uint8_t *q_scales_out, float sm_scale, float *out,
                                      int32_t *d_status, void *stream);
 
+/* ---- One decode step from host buffers ------------------------------------------------------
+ * No counterpart in the pages: kv_nvfp4_plan followed by kv_nvfp4_decode_step, with the step's
+ * new tokens and its output in HOST memory, enqueued on `stream` by one call: the host-to-device
+ * copies of q, k and v into the caller's device buffers, the plan build and its upload, the
+ * fused step's launches, and the device-to-host copy of the output. For a serving loop that
+ * drives the library from host code once per step.
+ *   h_seq_lens, num_seqs, q_len, causal, chunk_tokens: as for kv_nvfp4_plan (HOST lengths
+ *              including the new tokens); (num_q_heads / num_kv_heads) * q_len <= 8
+ *   d_workspace, ws_bytes: at least kv_nvfp4_plan_workspace_bytes bytes (DEVICE, 16-byte aligned)
+ *   h_q, h_k, h_v: HOST bf16 rows laid out as q, k, v of kv_nvfp4_decode_step; page-locked
+ *              memory makes the copies asynchronous (pageable memory is copied before return)
+ *   d_q, d_k, d_v: DEVICE buffers of the same sizes (16-byte aligned) that receive them
+ *   d_rope_table, rope_max_pos, d_block_table, max_pages, num_pages, pool, sm_scale, d_status:
+ *              as for kv_nvfp4_decode_step
+ *   d_out:     DEVICE fp32 output [num_seqs * q_len][num_q_heads][128]
+ *   h_out:     HOST copy of it (page-locked for an asynchronous copy), complete when the stream
+ *              reaches the end of this call's work
+ *   plan_out:  optional HOST copy of the plan info (may be null)
+ * Returns once everything is enqueued; EINVAL before any copy for the argument checks above, or
+ * the first error of the calls it makes. */
+kv_nvfp4_status kv_nvfp4_decode_step_host(
+    const kv_nvfp4_layout *layout, const int32_t *h_seq_lens, int32_t num_seqs, int32_t q_len,
+    int32_t causal, int32_t chunk_tokens, void *d_workspace, size_t ws_bytes, const void *h_q,
+    const void *h_k, const void *h_v, void *d_q, void *d_k, void *d_v, const float *d_rope_table,
+    int32_t rope_max_pos, const int32_t *d_block_table, int32_t max_pages, int32_t num_pages,
+    uint8_t *pool, float sm_scale, float *d_out, float *h_out, int32_t *d_status,
+    kv_nvfp4_plan_info *plan_out, void *stream);
+
 /* ---- Comparator KV formats [NVFP4 "Result": 144 B per token per KV head vs 264 int8 vs 512 bf16;
  * upstream NVFP4 K with fp16 V and no rotation] -------------------------------------------------
  * prismix.dev/news/833001997676, section "NVFP4 KV cache (from scratch)". Decode attention over

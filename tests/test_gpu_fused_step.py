@@ -64,3 +64,27 @@ def test_fused_step_flags_a_page_outside_the_pool():
     torch.cuda.synchronize()
     assert g.status() & kv.DEV_BAD_PAGE
     g.cache.block_table.copy_(bt)
+
+
+def test_decode_step_from_host_buffers_matches_device_step():
+    # kv_nvfp4_decode_step_host (H2D copies, plan, fused step, D2H in one call) against the
+    # device-buffer step on the same inputs: every code byte as the oracle's, identical output
+    w = synth.Workload("host_step", [700, 64, 3000], q_len=1, seed=21, chunk_tokens=128)
+    ref = GpuRun(w)
+    ref.step_fused()
+    torch.cuda.synchronize()
+    g = GpuRun(w)
+    g.cache.plan(w.seq_lens, w.q_len, w.causal, 128)  # sizes the workspace
+    q, k, v, *_ = w.new_tokens()
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
+    h_q, h_k, h_v = pin(q), pin(k), pin(v)
+    d_q, d_k, d_v = (torch.empty_like(t, device="cuda") for t in (h_q, h_k, h_v))
+    h_out = torch.full((g.out.numel(),), float("nan"), dtype=torch.float32).pin_memory()
+    g.cache.decode_step_host(np.asarray(w.seq_lens, np.int32), w.q_len, h_q, h_k, h_v, d_q, d_k,
+                             d_v, g.out, h_out, causal=w.causal, chunk_tokens=128,
+                             sm_scale=w.sm_scale)
+    torch.cuda.synchronize()
+    assert g.status() == 0 and ref.status() == 0
+    bad = compare_pool(g, OracleRun(w))
+    assert all(v == 0 for v in bad.values()), bad
+    assert np.array_equal(h_out.numpy(), ref.out.cpu().numpy())

@@ -219,3 +219,23 @@ def test_noalloc_buffer_size_matches_the_header(kv):
     for lens, q_len in (([100008] * 4, 8), ([600064], 8192)):
         info = kv.kv_nvfp4_plan_host(L, lens, q_len, True, 1024, 152)[0]
         assert info.workspace_bytes <= kv.NOALLOC_SCRATCH_BYTES
+
+
+def test_decode_step_host_rejects_bad_arguments_before_cuda(kv):
+    lib = kv.lib()
+    L = kv.make_layout()
+    sl = np.array([100, 200], np.int32)
+    info = kv.PlanInfo()
+    args = lambda q_len, hq: (ctypes.byref(L), sl.ctypes.data, 2, q_len, 1, 64, 256, 1 << 20, hq,
+                              512, 768, 1024, 1280, 1536, 1792, 1000, 2048, 4, 8, 2304, 0.0, 2560,
+                              2816, None, ctypes.byref(info), None)
+    EINVAL = kv.KV_NVFP4_EINVAL
+    assert lib.kv_nvfp4_decode_step_host(*args(1, None)) == EINVAL      # no host Q
+    assert lib.kv_nvfp4_decode_step_host(*args(2, 256)) == EINVAL       # 12 rows per KV head
+    bad = kv.Layout(24, 4, 64, 64, 32)
+    a = list(args(1, 256))
+    a[0] = ctypes.byref(bad)
+    assert lib.kv_nvfp4_decode_step_host(*a) == EINVAL                  # head_dim 64
+    a = list(args(1, 256))
+    a[6] = 264                                                         # misaligned workspace
+    assert lib.kv_nvfp4_decode_step_host(*a) == EINVAL
