@@ -9,13 +9,16 @@ step's new tokens (Q, K, V: RoPE, Hadamard rotation, NVFP4), stores their K/V ro
 and runs the split-K decode attention over the whole cache (two kernel launches: the attention
 kernel with the append inside it, and the split-K merge). The step re-appends the same positions,
 so every step sees the same cache. The same step as two calls (kv_nvfp4_append, then
-kv_nvfp4_decode_attn: three launches) and the attention call alone are timed beside it. The KV read per step (302 MB)
-is larger than L2 (129 MB), so no L2 flush is needed between steps.
+kv_nvfp4_decode_attn: three launches) and the attention call alone are timed beside it. The KV
+read per step (302 MB) is larger than L2 (129 MB), so no L2 flush is needed between steps.
 
-`value` is device time with inputs resident in HBM; `e2e` adds, every step, the host->device
-copy of the new tokens from pinned memory, the split-K plan upload, and the device->host copy of
-the attention output. `roofline` covers the step call (attention kernel + merge kernel), timed
-with CUDA events around the back-to-back steps.
+`value` is device time with inputs resident in HBM; `e2e` is one kv_nvfp4_decode_step_host call
+per step, which adds the host->device copy of the new tokens from pinned memory, the split-K plan
+upload and the device->host copy of the attention output. `roofline` covers the step call
+(attention kernel + merge kernel), timed with CUDA events around the back-to-back steps.
+Beside the headline line's decode workload, the many-row shapes that run on the tile kernel are
+timed too (`tile_workloads`: the speculative verify step and the 600k prefill chunk), as are the
+comparator KV formats (`comparators`) and the page spill / restore path (`spill`).
 `--impl reference` times the CPU oracle on a bounded sample of the same workload.
 
 Multi-GPU: the path has no exchange step, so N GPUs run N independent replicas (weak scaling);
