@@ -994,9 +994,11 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
                           const uint16_t* v_new, const float* rope, int32_t rope_max_pos,
                           int32_t rot_dim, uint8_t* pool_w, uint8_t* q_codes_out,
                           uint8_t* q_scales_out, cudaStream_t stream) {
-  // the attribute belongs to each instantiation, set once per process
-  static bool attr_done = false;
-  if (!attr_done) {
+  // the attribute belongs to each instantiation and each device: set once per device
+  static bool attr_done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
     cudaError_t e = cudaSuccess;
     const void* kernels[] = {(const void*)decode_kernel<8, false>, (const void*)decode_kernel<6, false>,
                              (const void*)decode_kernel<8, true>, (const void*)decode_kernel<6, true>};
@@ -1004,7 +1006,7 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
       if (e == cudaSuccess)
         e = cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
   if (Hkv < 1 || Hkv > kMaxHkv) return cudaErrorInvalidValue;
   DecodeParams p;

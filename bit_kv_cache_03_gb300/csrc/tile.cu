@@ -745,13 +745,16 @@ cudaError_t launch_tile(const uint8_t* q_codes, const uint8_t* q_scales, const u
                         const int32_t* split_groups, int32_t num_split, float* partials,
                         float* out, int32_t* status, int32_t Hq, int32_t Hkv, int32_t q_len,
                         int32_t causal, int32_t grid, float sm_scale, cudaStream_t stream) {
-  static bool attr_done = false;
-  if (!attr_done) {
+  // the attribute belongs to each device: set once per device
+  static bool attr_done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
     const cudaError_t e = cudaFuncSetAttribute(tile_kernel,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                kTSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
   if (Hkv < 1 || Hkv > 4) return cudaErrorInvalidValue;
   TileParams p;
