@@ -163,6 +163,11 @@ def test_plan_covers_every_visible_page_once_and_balances(kv, lens, q_len, causa
     assert np.array_equal(split, np.flatnonzero(groups[:, 4] > 1))
     assert info.num_split_groups == len(split)
     assert info.off_split % 16 == 0 and info.off_partials % 16 == 0
+    # one (m, l, O) partial per slot: rows x (128 + 2) floats for every KV head the group covers
+    heads = 2 if tile_rows == 64 else Hkv
+    part_bytes = heads * tile_rows * 130 * 4
+    assert info.workspace_bytes >= info.off_partials + info.num_partials * part_bytes
+    assert info.workspace_bytes < info.off_partials + info.num_partials * part_bytes + 256
 
 
 def test_spill_restore_reject_bad_arguments_before_cuda(kv):
