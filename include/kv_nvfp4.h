@@ -70,7 +70,7 @@ typedef int32_t kv_nvfp4_status;
 #define KV_NVFP4_DEV_BAD_ROPE 0x8     /* position >= rope_max_pos for a rotated row */
 #define KV_NVFP4_DEV_TIMEOUT 0x10     /* an internal barrier wait hit its time limit */
 
-/* Model geometry of one attention layer. This build supports head_dim = 128 and
+/* Model geometry of one attention layer. The library supports head_dim = 128 and
  * page_size = 64; num_q_heads must be a multiple of num_kv_heads with a group of at most 8;
  * rot_dim is even, a multiple of 8 and at most 128 (0 disables RoPE). */
 typedef struct kv_nvfp4_layout {
