@@ -2,7 +2,9 @@
 
 Attention is checked against closed forms (one key, equal scores, two keys), against
 torch's scaled_dot_product_attention in float64 on the oracle's own dequantised arrays (GQA head
-mapping, causal offsets, scale), and the joint-rotation invariance of Q.K^T.
+mapping, causal offsets, scale), and the joint-rotation invariance of Q.K^T. The unquantised
+reference (the baseline of the cosine report) is checked against torch float64 SDPA on rows rotated
+by an independent float64 RoPE, and for the relative-position property of the key rotation.
 """
 import math
 
@@ -172,3 +174,108 @@ def test_paged_gather_layout(H):
     bt2 = np.array([[4, 9]], np.int32)
     *_, bad = oracle.paged_gather(pool, P, H, bt2, 0, 0, 100)
     assert bad == (100 - 64) * H
+
+
+def _rope64(x, pos, rot_dim, theta, pos_scale):
+    """RoPE written independently in float64 with torch: pairs (i, i + rot_dim/2) rotated by
+    (pos / pos_scale) * theta^(-2i/rot_dim). x [n, 128], pos [n]."""
+    half = rot_dim // 2
+    i = torch.arange(half, dtype=torch.float64)
+    inv = theta ** (-2.0 * i / rot_dim)
+    ang = (pos.to(torch.float64)[:, None] / pos_scale) * inv[None, :]
+    c, s = torch.cos(ang), torch.sin(ang)
+    a, b = x[:, :half], x[:, half:rot_dim]
+    return torch.cat([a * c - b * s, b * c + a * s, x[:, rot_dim:]], dim=1)
+
+
+@pytest.mark.parametrize("rot_dim,pos_scale,causal", [(32, 1.0, 1), (32, 600000 / 262144, 1),
+                                                       (32, 1.0, 0), (128, 1.0, 1), (0, 1.0, 1)])
+def test_unquantized_reference_matches_torch_sdpa(rot_dim, pos_scale, causal):
+    # The unquantised attention behind the cosine report: bf16 q/k/v widened exactly, RoPE on q at
+    # its own position (len - q_len + i) and on key t at position t, GQA head h -> kv head
+    # h // group, causal offsets; against torch float64 SDPA on rows rotated by an independent
+    # float64 RoPE. The oracle's fp32 table and products differ by rounding only (~1e-7).
+    Hq, Hkv, q_len, theta = 12, 4, 3, 1e7
+    seq_lens = [5, 70, 23]
+    T = sum(seq_lens)
+    q = synth.normal_bf16(5, 1, 0, 0, len(seq_lens) * q_len, Hq)
+    k = synth.normal_bf16(5, 2, 0, 0, T, Hkv)
+    v = synth.normal_bf16(5, 3, 0, 0, T, Hkv)
+    max_pos = max(seq_lens)
+    table = oracle.rope_table(max_pos, rot_dim, theta, pos_scale) if rot_dim else \
+        np.zeros(1, np.float32)
+    sl = np.asarray(seq_lens, np.int32)
+    tok_off = np.concatenate([[0], np.cumsum(sl)[:-1]]).astype(np.int64)
+    rows = [(s, i, h) for s in range(len(seq_lens)) for i in range(q_len) for h in range(Hq)]
+    rs, rt, rh = (np.array(x, np.int32) for x in zip(*rows))
+    sm = 1.0 / math.sqrt(128)
+    out = oracle.attention_ref_rows(Hq, Hkv, q_len, causal, sm, sl, tok_off,
+                                    q.reshape(-1, 128), k.reshape(-1, 128), v.reshape(-1, 128),
+                                    table, rot_dim, rs, rt, rh)
+    f64 = lambda a: torch.from_numpy(synth.bf16_bits_to_float(a).astype(np.float64))
+    Q, K, V = f64(q), f64(k), f64(v)          # [S*q_len, Hq, D], [T, Hkv, D]
+    ref = []
+    off = 0
+    for s, L in enumerate(seq_lens):
+        qpos = torch.arange(L - q_len, L)
+        kpos = torch.arange(L)
+        qs = Q[s * q_len:(s + 1) * q_len]   # [q_len, Hq, D]
+        ks, vs = K[off:off + L], V[off:off + L]
+        if rot_dim:
+            qs = _rope64(qs.reshape(-1, 128), qpos.repeat_interleave(Hq), rot_dim, theta,
+                         pos_scale).reshape(q_len, Hq, 128)
+            ks = _rope64(ks.reshape(-1, 128), kpos.repeat_interleave(Hkv), rot_dim, theta,
+                         pos_scale).reshape(L, Hkv, 128)
+        mask = (kpos[None, :] <= qpos[:, None]) if causal else torch.ones(q_len, L, dtype=torch.bool)
+        o = torch.nn.functional.scaled_dot_product_attention(
+            qs.permute(1, 0, 2)[None], ks.permute(1, 0, 2)[None], vs.permute(1, 0, 2)[None],
+            attn_mask=mask, scale=sm, enable_gqa=True)
+        ref.append(o[0].permute(1, 0, 2).reshape(-1, 128).numpy())
+        off += L
+    ref = np.concatenate(ref)
+    assert np.allclose(out, ref, rtol=0, atol=2e-5), np.abs(out - ref).max()
+
+
+def test_unquantized_reference_key_positions_are_relative():
+    # RoPE makes a score depend on the query and key positions only through their difference.
+    # Sequence B repeats sequence A's keys and values D positions later, after D keys of zeros
+    # (score 0) whose values are zero; the query rows are the same bf16 rows, so B's query sits D
+    # positions after A's. With the real keys' scores far above 0 the filler keys get weight
+    # below e^-40, so the outputs agree to fp32 rounding if and only if every key is rotated at
+    # its own position t and the query at len - q_len + i.
+    Hq, Hkv, q_len, D, L = 4, 1, 2, 37, 9
+    q = np.zeros((2 * q_len, Hq, 128), np.uint16)
+    k = np.zeros((L + L + D, Hkv, 128), np.uint16)
+    v = np.zeros_like(k)
+    rng = np.random.default_rng(3)
+    bf = lambda x: (np.asarray(x, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    # q and k both large along the rotary dims' partner pairs and a non-rotary dim, so that
+    # every score is large and positive and depends on the relative position
+    qa = np.zeros((q_len, Hq, 128), np.float32)
+    qa[..., 0] = 8.0; qa[..., 16] = 8.0; qa[..., 100] = 24.0
+    ka = np.zeros((L, Hkv, 128), np.float32)
+    ka[..., 0] = rng.uniform(2, 4, (L, Hkv)); ka[..., 16] = rng.uniform(2, 4, (L, Hkv))
+    ka[..., 100] = rng.uniform(3, 5, (L, Hkv))
+    va = rng.standard_normal((L, Hkv, 128)).astype(np.float32)
+    q[:q_len] = bf(qa); q[q_len:] = bf(qa)
+    k[:L] = bf(ka); k[L + D:] = bf(ka)
+    v[:L] = bf(va); v[L + D:] = bf(va)
+    sl = np.array([L, L + D], np.int32)
+    tok_off = np.array([0, L], np.int64)
+    table = oracle.rope_table(L + D, 32, 1e7, 1.0)
+    rows = [(s, i, h) for s in range(2) for i in range(q_len) for h in range(Hq)]
+    rs, rt, rh = (np.array(x, np.int32) for x in zip(*rows))
+    out = oracle.attention_ref_rows(Hq, Hkv, q_len, 1, 1.0, sl, tok_off, q.reshape(-1, 128),
+                                    k.reshape(-1, 128), v.reshape(-1, 128), table, 32, rs, rt, rh)
+    a, b = out[:q_len * Hq], out[q_len * Hq:]
+    assert np.allclose(a, b, rtol=0, atol=1e-5), np.abs(a - b).max()
+    # the positions matter: with both sequences' keys at the same absolute positions (no shift)
+    # the two would differ, so the agreement above is not a trivial one
+    t2 = oracle.rope_table(L + D, 32, 1e7, 1.0 / 64)
+    out2 = oracle.attention_ref_rows(Hq, Hkv, q_len, 1, 1.0, sl, tok_off, q.reshape(-1, 128),
+                                     k.reshape(-1, 128), v.reshape(-1, 128), t2, 32, rs, rt, rh)
+    assert np.allclose(out2[:q_len * Hq], out2[q_len * Hq:], rtol=0, atol=1e-5)
+    c = oracle.attention_ref_rows(Hq, Hkv, q_len, 1, 1.0, sl[:1], tok_off[:1], q[:q_len].reshape(-1, 128),
+                                  k[:L].reshape(-1, 128), v[:L].reshape(-1, 128), t2, 32,
+                                  rs[:q_len * Hq], rt[:q_len * Hq], rh[:q_len * Hq])
+    assert not np.allclose(c, out[:q_len * Hq], rtol=0, atol=1e-3)
