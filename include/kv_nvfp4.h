@@ -376,8 +376,10 @@ kv_nvfp4_status kv_nvfp4_restore_pages(const kv_nvfp4_layout *layout, const uint
  *   the rest: as for kv_nvfp4_decode_attn
  * Returns KV_NVFP4_ENOSPACE, before any GPU work, when the plan's workspace
  * (kv_nvfp4_plan_workspace_bytes) exceeds the buffer; callers then use the workspace path.
- * The first call on a device looks up the buffer's device address (with that device current)
- * and keeps it; make that first call before any stream capture. Every call shares the buffer:
+ * The first call on a device (in each of its contexts) looks up the buffer's device address with
+ * that device current and keeps it for the later calls. Each call builds its work list in host
+ * memory and uploads it, so the call cannot be recorded into a CUDA graph: while `stream` is
+ * capturing it returns KV_NVFP4_EINVAL before enqueuing anything. Every call shares the buffer:
  * each rewrites its work list before its kernels read it and nothing in it has to start at zero,
  * but calls whose kernels overlap on the GPU (other streams, other host threads) corrupt each
  * other's results and must be serialised by the caller. */

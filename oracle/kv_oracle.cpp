@@ -208,8 +208,8 @@ void orc_quantize_rows(const uint16_t* rows, int64_t n_rows, const int32_t* pos,
                        const float* rope_table, int32_t rot_dim, uint8_t* codes, uint8_t* scales,
                        int32_t nthreads) {
 #ifdef _OPENMP
-  if (nthreads > 0) omp_set_num_threads(nthreads);
-#pragma omp parallel for schedule(static)
+  const int nt_used = nthreads > 0 ? nthreads : omp_get_max_threads();  // global setting kept
+#pragma omp parallel for num_threads(nt_used) schedule(static)
 #endif
   for (int64_t r = 0; r < n_rows; ++r) {
     float x[128];
@@ -307,8 +307,8 @@ void orc_attention_rows(int32_t q_heads, int32_t kv_heads, int32_t q_len, int32_
                         const int32_t* row_head, float* out, int32_t nthreads) {
   const int32_t group = q_heads / kv_heads;
 #ifdef _OPENMP
-  if (nthreads > 0) omp_set_num_threads(nthreads);
-#pragma omp parallel for schedule(dynamic, 1)
+  const int nt_used = nthreads > 0 ? nthreads : omp_get_max_threads();  // global setting kept
+#pragma omp parallel for num_threads(nt_used) schedule(dynamic, 1)
 #endif
   for (int64_t r = 0; r < n_rows; ++r) {
     const int32_t s = row_seq[r], i = row_tok[r], head = row_head[r];
@@ -352,8 +352,8 @@ void orc_attention_ref_rows(int32_t q_heads, int32_t kv_heads, int32_t q_len, in
                             const int32_t* row_head, float* out, int32_t nthreads) {
   const int32_t group = q_heads / kv_heads;
 #ifdef _OPENMP
-  if (nthreads > 0) omp_set_num_threads(nthreads);
-#pragma omp parallel for schedule(dynamic, 1)
+  const int nt_used = nthreads > 0 ? nthreads : omp_get_max_threads();  // global setting kept
+#pragma omp parallel for num_threads(nt_used) schedule(dynamic, 1)
 #endif
   for (int64_t r = 0; r < n_rows; ++r) {
     const int32_t s = row_seq[r], i = row_tok[r], head = row_head[r];
@@ -638,8 +638,8 @@ void orc_attention_f64_rows(int32_t q_heads, int32_t kv_heads, int32_t q_len, in
                             const int32_t* row_head, float* out, int32_t nthreads) {
   const int32_t group = q_heads / kv_heads;
 #ifdef _OPENMP
-  if (nthreads > 0) omp_set_num_threads(nthreads);
-#pragma omp parallel for schedule(dynamic, 1)
+  const int nt_used = nthreads > 0 ? nthreads : omp_get_max_threads();  // global setting kept
+#pragma omp parallel for num_threads(nt_used) schedule(dynamic, 1)
 #endif
   for (int64_t r = 0; r < n_rows; ++r) {
     const int32_t s = row_seq[r], i = row_tok[r], head = row_head[r];

@@ -67,8 +67,8 @@ void synth_normal_bf16(uint64_t seed, uint64_t stream, int32_t seq, int32_t pos0
   for (int k = 0; k < n_outliers; ++k)
     if (outliers[k] >= 0 && outliers[k] < dim) mult[outliers[k]] = outlier_mult;
 #ifdef _OPENMP
-  if (nthreads > 0) omp_set_num_threads(nthreads);
-#pragma omp parallel for schedule(static)
+  const int nt_used = nthreads > 0 ? nthreads : omp_get_max_threads();  // global setting kept
+#pragma omp parallel for num_threads(nt_used) schedule(static)
 #endif
   for (int64_t t = 0; t < (int64_t)n_tok; ++t) {
     const uint64_t pos = (uint64_t)(pos0 + t);

@@ -1,8 +1,15 @@
-"""Parity on the five full-size workloads, in the launch configuration the benchmark times (GPU).
+"""Parity on the five full-size workloads, in the launch configurations the benchmark times (GPU).
 
 Every K/V row of every cached and appended token is compared bit-exactly with the oracle's
 quantisation; attention is compared on every output row (decode and verify workloads) or on a
-seeded row sample (the 600k prefill chunk, 196,608 rows)."""
+seeded row sample (the 600k prefill chunk, 196,608 rows). Each workload runs through the call and
+the split-K chunk size that bench.py times for it:
+  tiny / steady / ragged decode: kv_nvfp4_decode_step (the append inside the attention launch),
+      chunks of 64 tokens (tiny, steady) and 1024 tokens (ragged), so the split-K merge runs;
+  speculative verify and the 600k prefill chunk: kv_nvfp4_append + kv_nvfp4_decode_attn on the
+      tile kernel, chunks of 1024 tokens, so the tile kernel's merge runs as well.
+The decode workloads are also run through the two-call path with the workload's own chunk size.
+"""
 import numpy as np
 import pytest
 
@@ -13,18 +20,20 @@ from kvrun import (MAX_ABS_TOL, REL_L2_TOL, GpuRun, OracleRun, attention_errors,
 torch = pytest.importorskip("torch")
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
+# the split-K chunk each workload is timed with in bench.py
+BENCH_CHUNK = {"tiny_decode_4k": 64, "steady_decode_4x128k": 64, "ragged_decode_8seq": 1024,
+               "spec_verify_4x100k_q8": 1024, "prefill_chunk_600k": 1024}
 
-def _run(w, rows=None, chunk=None):
-    g = GpuRun(w)
-    g.step(chunk_tokens=chunk)
+
+def _check(g, o, w, rows, label):
     torch.cuda.synchronize()
-    assert g.status() == 0
-    o = OracleRun(w)
+    assert g.status() == 0, (label, g.status())
     bad = compare_pool(g, o)
-    assert all(v == 0 for v in bad.values()), bad
+    assert all(v == 0 for v in bad.values()), (label, bad)
     qc, qs = g.q_quant()
-    assert np.array_equal(qc, o.qc) and np.array_equal(qs, o.qs)
+    assert np.array_equal(qc, o.qc) and np.array_equal(qs, o.qs), label
     out = g.output()
+    assert np.all(np.isfinite(out)), label
     if rows is None:
         ref = o.attention().reshape(out.shape)
         got = out
@@ -33,36 +42,60 @@ def _run(w, rows=None, chunk=None):
         rs, rt, rh = rows
         got = out.reshape(w.num_seqs, w.q_len, w.q_heads, 128)[rs, rt, rh]
     max_abs, rel = attention_errors(got, ref)
-    print(f"{w.name}: max_abs={max_abs:.3e} rel_l2={rel:.3e}")
-    assert max_abs <= MAX_ABS_TOL and rel <= REL_L2_TOL, (max_abs, rel)
-    assert np.all(np.isfinite(out))
-    return g, o, got, ref
+    print(f"{w.name} [{label}]: max_abs={max_abs:.3e} rel_l2={rel:.3e}")
+    assert max_abs <= MAX_ABS_TOL and rel <= REL_L2_TOL, (label, max_abs, rel)
+    return got
+
+
+def _decode(w):
+    """The benchmarked fused step (bench chunk), then the two-call path (workload chunk)."""
+    g = GpuRun(w)
+    o = OracleRun(w)
+    chunk = BENCH_CHUNK[w.name]
+    g.step_fused(chunk_tokens=chunk)
+    assert g.cache.plan_info.num_split_groups > 0  # the merge launch ran
+    got = _check(g, o, w, None, f"decode_step chunk {chunk}")
+    g.out.zero_()
+    g.step(chunk_tokens=w.chunk_tokens)
+    _check(g, o, w, None, f"append + decode_attn chunk {w.chunk_tokens}")
+    return g, o, got
 
 
 def test_tiny_decode_4k():
     w = synth.tiny_decode()
-    g, o, got, ref = _run(w)
-    rows = o.all_rows()
-    unq = o.attention_unquantized(rows)
+    g, o, got = _decode(w)
+    unq = o.attention_unquantized(o.all_rows())
     c = cosine(got, unq)
     print(f"cosine vs unquantised attention: {c:.4f}")
     assert c > 0.5
 
 
 def test_steady_decode_4x128k():
-    _run(synth.steady_decode())
+    _decode(synth.steady_decode())
 
 
 def test_ragged_decode_8seq():
-    _run(synth.ragged_decode())
+    _decode(synth.ragged_decode())
 
 
 def test_spec_verify_4x100k_q8():
-    _run(synth.spec_verify())
+    w = synth.spec_verify()
+    g = GpuRun(w)
+    o = OracleRun(w)
+    g.step(chunk_tokens=BENCH_CHUNK[w.name])
+    assert g.cache.plan_info.num_split_groups > 0  # the tile kernel's merge ran
+    _check(g, o, w, None, "append + decode_attn (tile kernel) chunk 1024")
 
 
 def test_prefill_chunk_600k_sampled():
     w = synth.prefill_chunk()
     rows = sample_rows(w, 256, seed=0)
-    # one chunk per sequence: every (kv head, 8-row tile) item streams the whole cache
-    _run(w, rows=rows, chunk=((w.max_pos + 63) // 64) * 64)
+    g = GpuRun(w)
+    o = OracleRun(w)
+    g.step(chunk_tokens=BENCH_CHUNK[w.name])
+    assert g.cache.plan_info.num_split_groups > 0
+    _check(g, o, w, rows, "append + decode_attn (tile kernel) chunk 1024, sampled rows")
+    # one chunk per sequence (no split-K merge): the same sampled rows
+    g.out.zero_()
+    g.step(chunk_tokens=((w.max_pos + 63) // 64) * 64)
+    _check(g, o, w, rows, "one chunk per sequence, sampled rows")

@@ -53,17 +53,49 @@ def test_noalloc_rejects_a_plan_larger_than_its_buffer():
     g = GpuRun(w)
     c = g.cache
     # 1,000,000 one-token sequences: the group and segment tables alone (48 B a sequence) are
-    # past the buffer. The block table and the output below cover one sequence only, so the call
-    # is safe only because the library refuses it on the host, before any GPU work: check first
-    # that the plan is larger than the buffer (the constant mirrors the header, which a CPU test
-    # keeps in step).
+    # past the buffer, so the call returns ENOSPACE on the host. The output and the block table
+    # are passed as null: were the plan ever to fit, the decode call's pointer checks would refuse
+    # it (EINVAL) before any launch, so no call here can reach a kernel.
     lens = np.ones(1_000_000, np.int32)
     need = kv.kv_nvfp4_plan_workspace_bytes(c.layout, lens, 1, True, 64)
     assert need > kv.NOALLOC_SCRATCH_BYTES
-    out = torch.zeros_like(g.out)
     with pytest.raises(kv.KVNVFP4Error, match=r"\(-3\)"):
         kv.kv_nvfp4_decode_attn_noalloc(c.layout, lens, 1, True, 64, g.q_codes, g.q_scales,
-                                        w.sm_scale, c.pool, c.num_pages, c.block_table,
-                                        c.max_pages, out, c.status)
+                                        w.sm_scale, c.pool, c.num_pages, None, c.max_pages, None,
+                                        c.status)
     torch.cuda.synchronize()
-    assert not out.any()  # rejected before any GPU work
+    assert g.status() == 0
+
+
+def test_noalloc_is_refused_while_the_stream_is_capturing():
+    # the work list is uploaded from host memory that each call rebuilds, so a graph replay would
+    # read stale memory: the entry point refuses a capturing stream before enqueuing anything
+    import bit_kv_cache_03_gb300 as kv
+    w = synth.Workload("noalloc_capture", [500, 90], q_len=1, seed=5, chunk_tokens=64)
+    g = GpuRun(w)
+    g.step(chunk_tokens=64)
+    torch.cuda.synchronize()
+    ref = g.output().copy()
+    out = torch.full_like(g.out, float("nan"))
+    side = torch.zeros(16, device="cuda")
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    refused = None
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            side.add_(1.0)
+            try:
+                _noalloc(g, out)
+            except kv.KVNVFP4Error as e:
+                refused = str(e)
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    assert refused is not None and "(-1)" in refused, refused
+    assert torch.isnan(out).all()  # nothing was enqueued, into the graph or otherwise
+    # the same call outside the capture runs as usual
+    _noalloc(g, out)
+    torch.cuda.synchronize()
+    max_abs, rel = attention_errors(out.view(g.T, w.q_heads, 128).cpu().numpy(), ref)
+    assert max_abs <= MAX_ABS_TOL and rel <= REL_L2_TOL, (max_abs, rel)
+    assert g.status() == 0
