@@ -8,18 +8,26 @@ A step is one pass of the whole hot path: one kv_nvfp4_decode_step call, which q
 step's new tokens (Q, K, V: RoPE, Hadamard rotation, NVFP4), stores their K/V rows into the pool
 and runs the split-K decode attention over the whole cache (two kernel launches: the attention
 kernel with the append inside it, and the split-K merge). The step re-appends the same positions,
-so every step sees the same cache. The same step as two calls (kv_nvfp4_append, then
-kv_nvfp4_decode_attn: three launches) and the attention call alone are timed beside it. The KV
-read per step (302 MB) is larger than L2 (129 MB), so no L2 flush is needed between steps.
+so every step sees the same cache. The W warm-up steps run directly before the K timed steps. The
+same step as two calls (kv_nvfp4_append, then kv_nvfp4_decode_attn: three launches) and the
+attention call alone are timed beside it. The KV read per step (302 MB) is larger than L2
+(129 MB), so no L2 flush is needed between steps.
 
 `value` is device time with inputs resident in HBM; `e2e` is one kv_nvfp4_decode_step_host call
 per step, which adds the host->device copy of the new tokens from pinned memory, the split-K plan
 upload and the device->host copy of the attention output. `roofline` covers the step call
 (attention kernel + merge kernel), timed with CUDA events around the back-to-back steps.
-Beside the headline line's decode workload, the many-row shapes that run on the tile kernel are
-timed too (`tile_workloads`: the speculative verify step and the 600k prefill chunk), as are the
-comparator KV formats (`comparators`) and the page spill / restore path (`spill`).
-`--impl reference` times the CPU oracle on a bounded sample of the same workload.
+
+`configs` holds every workload of the parity tests in the launch configuration the tests check:
+the tiny and ragged decode workloads (kv_nvfp4_decode_step, back to back), the speculative
+verify step and the 600k prefill chunk (append of the new tokens, then the attention call on the
+tile kernel), each with KV-tokens/s, its HBM fraction and the cosine similarity of its output
+with unquantised attention (bf16 inputs, same RoPE, float64; computed with torch on the GPU for
+the report). The comparator KV formats (`comparators`) and the page spill / restore path
+(`spill`) are timed too. `cpu_baseline` is the oracle on the host's cores: the headline step in
+full on all threads, with rows for quantize-append and every workload on all threads and on one
+(samples extrapolated and marked). `--impl reference` times the CPU oracle on a bounded sample
+of the same workload.
 
 Multi-GPU: the path has no exchange step, so N GPUs run N independent replicas (weak scaling);
 value = units of all ranks / max-over-ranks time.
@@ -154,55 +162,6 @@ def decode_traffic_profile():
     if d.get("decode_cu_sha256_16") != h:
         return None
     return d.get("dram_bytes_per_launch")
-
-
-def oracle_sample(w, reps_target_s=10.0, max_reps=3):
-    """The CPU oracle on a bounded sample of the step: the new token of sequence 0 quantised
-    (Q/K/V) and its 24 heads' attention over all 131,073 keys of that sequence."""
-    import numpy as np
-
-    import oracle
-    import synth
-
-    s = 0
-    L = int(w.seq_lens[s])
-    table = oracle.rope_table(w.max_pos, w.rot_dim, w.theta, w.pos_scale)
-    k = w.k_rows(s, 0, L)
-    v = w.v_rows(s, 0, L)
-    pos = np.repeat(np.arange(L, dtype=np.int32), w.kv_heads)
-    # the cached part is state, not step work: quantised before the clock starts
-    kc, ks = oracle.quantize_rows(k[:-1].reshape(-1, 128), pos[:-w.kv_heads], True, table, w.rot_dim)
-    vc, vs = oracle.quantize_rows(v[:-1].reshape(-1, 128), None, False, None, 0)
-    q = w.q_rows(s, L - 1, 1)
-    nthreads = oracle.num_threads()
-
-    def one():
-        kn, ksn = oracle.quantize_rows(k[-1:].reshape(-1, 128), pos[-w.kv_heads:], True, table,
-                                       w.rot_dim)
-        vn, vsn = oracle.quantize_rows(v[-1:].reshape(-1, 128), None, False, None, 0)
-        qc, qs = oracle.quantize_rows(q.reshape(-1, 128),
-                                      np.full(w.q_heads, L - 1, np.int32), True, table, w.rot_dim)
-        KC = np.concatenate([kc, kn]); KS = np.concatenate([ks, ksn])
-        VC = np.concatenate([vc, vn]); VS = np.concatenate([vs, vsn])
-        rows = (np.zeros(w.q_heads, np.int32), np.zeros(w.q_heads, np.int32),
-                np.arange(w.q_heads, dtype=np.int32))
-        oracle.attention_rows(w.q_heads, w.kv_heads, 1, True, w.sm_scale, np.array([L], np.int32),
-                              np.array([0], np.int64), qc, qs, KC, KS, VC, VS, *rows)
-
-    t0 = time.perf_counter()
-    one()
-    dt = time.perf_counter() - t0
-    reps = 1
-    extra = max(0, min(max_reps - 1, int(reps_target_s / max(dt, 1e-3)) - 1))
-    t0 = time.perf_counter()
-    for _ in range(extra):
-        one()
-    if extra:
-        dt = (time.perf_counter() - t0) / extra
-        reps += extra
-    return {"value": L / dt, "unit": UNIT, "cores": nthreads, "kind": "oracle",
-            "sample": f"1 of 4 sequences ({L} KV tokens, 24 query heads, 1 new token: "
-                      f"quantise + fp64 attention), {reps} reps, {dt:.2f} s each"}
 
 
 def run_reference(args, world, rank):
@@ -373,57 +332,232 @@ def comparators(w, dev, stream, peak, reps=200):
     return res
 
 
-def tile_workloads(dev, stream, peak_gbs):
-    """Attention calls of the many-row shapes, which run on the tile kernel: the speculative
-    verify step (4 x 100,008 keys, 8 new tokens: 48 query rows per KV head) and the 600k prefill
-    chunk (8192 new tokens: 196,608 query rows over up to 600,064 keys). Both are parity cases of
-    the GPU tests; here they are timed (the cache populated by the append kernel first)."""
-    import torch
-
-    import synth
-    from kvrun import GpuRun
-    bf16, bf16_kind = measured_bf16_tflops()
-    res = {}
-    for w, chunk, reps in ((synth.spec_verify(), 1024, 200), (synth.prefill_chunk(), 1024, 5)):
-        g = GpuRun(w, device=dev)
-        g.step(chunk_tokens=chunk)  # append the new tokens with Q, plan, attend
-
-        def call():
-            g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
-
-        for _ in range(3):
-            call()
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            call()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        assert g.status() == 0, f"{w.name}: device status {g.status():#x}"
-        t = e0.elapsed_time(e1) / 1e3 / reps
-        T = w.num_seqs * w.q_len
-        kv_tokens = int(w.seq_lens.sum())
+def decode_step_bytes(w, n_pages=None):
+    """Algorithmic bytes of one kv_nvfp4_decode_step: every cached and new K/V row read (144 B per
+    token and KV head), the new Q/K/V rows read in bf16 and their codes written, the block-table
+    entries of the visited pages, and the fp32 output."""
+    T = w.num_seqs * w.q_len
+    if n_pages is None:
         n_pages = int(sum((int(l) + 63) // 64 for l in w.seq_lens))
-        # (query row, visible key) pairs: Q.K^T and P.V take 2 x 128 flops each per pair
-        vis = 0
-        for L in w.seq_lens:
-            L = int(L)
-            vis += (sum(L - w.q_len + i + 1 for i in range(w.q_len)) if w.causal
-                    else L * w.q_len) * w.q_heads
-        attn_bytes = (kv_tokens * w.kv_heads * 144 + T * w.q_heads * 72 + n_pages * 4 +
-                      T * w.q_heads * 128 * 4)
-        pv_tflops = 2 * 128 * vis / t / 1e12
-        res[w.name] = {
-            "attn_us": t * 1e6, "query_rows": T * w.q_heads, "kv_tokens": kv_tokens,
-            "chunk_tokens": chunk, "kv_tokens_per_s": kv_tokens / t,
-            "hbm_gbs": attn_bytes / t / 1e9, "hbm_frac_of_measured": attn_bytes / t / 1e9 / peak_gbs,
-            "qk_plus_pv_tflops": 2 * pv_tflops, "pv_tflops": pv_tflops,
-            "pv_frac_of_bf16": pv_tflops / bf16, "bf16_peak_tflops": bf16,
-            "bf16_peak_kind": bf16_kind + " (burst)"}
-        del g
-        torch.cuda.empty_cache()
-    return res
+    rows = w.q_heads + 2 * w.kv_heads
+    return (w.kv_tokens * w.kv_heads * 144 + T * rows * 256 + T * rows * 72 + n_pages * 4 +
+            T * w.q_heads * 128 * 4)
+
+
+def attn_call_bytes(w):
+    """Algorithmic bytes of one kv_nvfp4_decode_attn: the cache (144 B per token and KV head),
+    the quantised Q rows, the block-table entries and the fp32 output."""
+    T = w.num_seqs * w.q_len
+    n_pages = int(sum((int(l) + 63) // 64 for l in w.seq_lens))
+    return w.kv_tokens * w.kv_heads * 144 + T * w.q_heads * 72 + n_pages * 4 + T * w.q_heads * 512
+
+
+def unquantized_cosine(g, rows):
+    """Cosine similarity between the step's output rows and unquantised attention of the same rows:
+    the bf16 Q/K/V rows, RoPE with the same fp32 table (each product rounded, then added), no
+    Hadamard rotation and no quantisation, scores, softmax and P.V in float64 (torch on the GPU,
+    for this report only)."""
+    import numpy as np
+    import torch
+    w = g.w
+    dev = g.dev
+    rs, rt, rh = (np.asarray(a) for a in rows)
+    out = g.out.view(w.num_seqs, w.q_len, w.q_heads, 128)
+    rot, half = w.rot_dim, w.rot_dim // 2
+    table = g.cache.rope.view(-1, rot) if rot else None
+
+    def rope(x, pos):
+        if not rot:
+            return x
+        t = table[pos]
+        c, s_ = t[:, :half], t[:, half:rot]
+        a, b = x[:, :half], x[:, half:rot]
+        return torch.cat([a * c - b * s_, b * c + a * s_, x[:, rot:]], 1)
+
+    def f32(a):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+        return t.view(torch.bfloat16).float()
+
+    got, ref = [], []
+    for s in np.unique(rs):
+        L = int(w.seq_lens[s])
+        sel = np.nonzero(rs == s)[0]
+        K = f32(w.k_rows(int(s), 0, L))
+        V = f32(w.v_rows(int(s), 0, L))
+        Q = f32(w.q_rows(int(s), L - w.q_len, w.q_len))
+        kpos = torch.arange(L, device=dev)
+        for kvh in range(w.kv_heads):
+            idx = sel[rh[sel] // w.group == kvh]
+            if len(idx) == 0:
+                continue
+            kr = rope(K[:, kvh], kpos).double()
+            qpos = torch.from_numpy((L - w.q_len + rt[idx]).astype(np.int64)).to(dev)
+            qr = rope(Q[torch.from_numpy(rt[idx].astype(np.int64)).to(dev),
+                        torch.from_numpy(rh[idx].astype(np.int64)).to(dev)], qpos).double()
+            sc = (qr @ kr.T) * w.sm_scale
+            if w.causal:
+                sc = sc.masked_fill(kpos[None, :] > qpos[:, None], float("-inf"))
+            ref.append(torch.softmax(sc, dim=1) @ V[:, kvh].double())
+            got.append(out[int(s)][torch.from_numpy(rt[idx].astype(np.int64)).to(dev),
+                                   torch.from_numpy(rh[idx].astype(np.int64)).to(dev)].double())
+        del K, V
+    a, b = torch.cat(got).ravel(), torch.cat(ref).ravel()
+    return float((a @ b) / (a.norm() * b.norm()))
+
+
+def all_rows(w):
+    import numpy as np
+    rs, rt, rh = np.meshgrid(np.arange(w.num_seqs), np.arange(w.q_len), np.arange(w.q_heads),
+                             indexing="ij")
+    return rs.ravel(), rt.ravel(), rh.ravel()
+
+
+def timed_calls(fn, n, stream, dev):
+    """n calls back to back between two CUDA events on the launching stream: seconds per call."""
+    import torch
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / 1e3 / n
+
+
+def decode_config(w, chunk, dev, stream, steps, warmup, peak):
+    """One decode workload timed as the headline is: kv_nvfp4_decode_step back to back."""
+    from kvrun import GpuRun
+    g = GpuRun(w, device=dev)
+    g.cache.plan(w.seq_lens, w.q_len, w.causal, chunk)
+
+    def step():
+        g.cache.decode_step(g.q, g.k, g.v, g.out, g.q_codes, g.q_scales, sm_scale=w.sm_scale)
+
+    for _ in range(warmup):
+        step()
+    t = timed_calls(step, steps, stream, dev)
+    assert g.status() == 0, f"{w.name}: device status {g.status():#x}"
+    b = decode_step_bytes(w)
+    return g, {"call": "kv_nvfp4_decode_step", "chunk_tokens": chunk, "steps": steps,
+               "step_us": t * 1e6, "kv_tokens": w.kv_tokens, "kv_tokens_per_s": w.kv_tokens / t,
+               "hbm_gbs": b / t / 1e9, "hbm_frac_of_measured": b / t / 1e9 / peak,
+               "algorithmic_bytes": b}
+
+
+def tile_config(w, chunk, dev, stream, reps, peak, bf16):
+    """A many-row workload (speculative verify, prefill chunk): the append of its new tokens (with
+    Q) and the attention call on the tile kernel, each timed back to back."""
+    from kvrun import GpuRun
+    g = GpuRun(w, device=dev)
+    g.step(chunk_tokens=chunk)  # append the new tokens with Q, plan, attend
+
+    def attend():
+        g.cache.attend(g.q_codes, g.q_scales, g.out, sm_scale=w.sm_scale)
+
+    def append():
+        g.cache.append(g.k, g.v, g.sid, g.pos, q=g.q, q_codes=g.q_codes, q_scales=g.q_scales)
+
+    for _ in range(3):
+        append()
+        attend()
+    t_app = timed_calls(append, max(3, min(reps, 50)), stream, dev)
+    t = timed_calls(attend, reps, stream, dev)
+    assert g.status() == 0, f"{w.name}: device status {g.status():#x}"
+    T = w.num_seqs * w.q_len
+    vis = 0  # (query row, visible key) pairs: Q.K^T and P.V take 2 x 128 flops each per pair
+    for L in w.seq_lens:
+        L = int(L)
+        vis += (sum(L - w.q_len + i + 1 for i in range(w.q_len)) if w.causal
+                else L * w.q_len) * w.q_heads
+    ab = attn_call_bytes(w)
+    app_b = T * (w.q_heads + 2 * w.kv_heads) * (256 + 72)
+    pv_tflops = 2 * 128 * vis / t / 1e12
+    return g, {"call": "kv_nvfp4_append (new tokens, with Q) + kv_nvfp4_decode_attn (tile kernel)",
+               "chunk_tokens": chunk, "reps": reps, "append_us": t_app * 1e6,
+               "append_tokens_per_s": T / t_app, "append_gbs": app_b / t_app / 1e9,
+               "attn_us": t * 1e6, "step_us": (t + t_app) * 1e6, "query_rows": T * w.q_heads,
+               "kv_tokens": w.kv_tokens, "kv_tokens_per_s": w.kv_tokens / t,
+               "hbm_gbs": ab / t / 1e9, "hbm_frac_of_measured": ab / t / 1e9 / peak,
+               "qk_plus_pv_tflops": 2 * pv_tflops, "pv_tflops": pv_tflops,
+               "pv_frac_of_bf16": pv_tflops / bf16, "bf16_peak_tflops": bf16}
+
+
+def cpu_baseline_rows():
+    """The oracle, as it stands, on this host's cores: quantize-append tokens/s and the attention
+    step of each workload, on all cores and on one. A full pass is timed where it takes seconds;
+    otherwise a seeded sample of query rows, extrapolated to the whole step and marked so. The
+    cached rows' quantisation is state, not step work: done before the clock starts."""
+    import numpy as np
+
+    import oracle
+    import synth
+    from kvrun import OracleRun
+    allc = oracle.num_threads()
+    res = {"nproc": os.cpu_count(), "threads_all": allc, "rows": []}
+
+    def rows_sample(w, n, seed):
+        """n query rows drawn uniformly (seeded) from all of the step's rows."""
+        return (synth.uniform_int(seed, 300, n, w.num_seqs), synth.uniform_int(seed, 301, n, w.q_len),
+                synth.uniform_int(seed, 302, n, w.q_heads))
+
+    def add(what, threads, unit, value, seconds, extrapolated):
+        res["rows"].append({"what": what, "threads": threads, "unit": unit, "value": value,
+                            "seconds": seconds, "extrapolated": extrapolated})
+
+    # quantize-append: RoPE + Hadamard + NVFP4 of 24 Q and 4 K rows, NVFP4 of 4 V rows per token
+    w = synth.steady_decode()
+    n = 2048
+    table = oracle.rope_table(w.max_pos, w.rot_dim, w.theta, w.pos_scale)
+    q, k, v = w.q_rows(0, 0, n), w.k_rows(0, 0, n), w.v_rows(0, 0, n)
+    qpos = np.repeat(np.arange(n, dtype=np.int32), w.q_heads)
+    kpos = np.repeat(np.arange(n, dtype=np.int32), w.kv_heads)
+    for th in (1, allc):
+        t0 = time.perf_counter()
+        oracle.quantize_rows(q.reshape(-1, 128), qpos, True, table, w.rot_dim, th)
+        oracle.quantize_rows(k.reshape(-1, 128), kpos, True, table, w.rot_dim, th)
+        oracle.quantize_rows(v.reshape(-1, 128), None, False, None, 0, th)
+        dt = time.perf_counter() - t0
+        add(f"quantize-append, {n} tokens x (24 Q + 4 K + 4 V rows)", th, "tokens/s", n / dt, dt,
+            False)
+
+    def step(w, rows, threads, label):
+        o = OracleRun(w, nthreads=allc)  # the cache, quantised before the clock
+        qn, kn, vn, _, pos = w.new_tokens()
+        total = w.num_seqs * w.q_len * w.q_heads
+        rs = rows[0] if rows is not None else None
+        n_rows = total if rows is None else len(rs)
+        t0 = time.perf_counter()
+        oracle.quantize_rows(qn.reshape(-1, 128), np.repeat(pos, w.q_heads), True, o.table,
+                             w.rot_dim, threads)
+        oracle.quantize_rows(kn.reshape(-1, 128), np.repeat(pos, w.kv_heads), True, o.table,
+                             w.rot_dim, threads)
+        oracle.quantize_rows(vn.reshape(-1, 128), None, False, None, 0, threads)
+        t_new = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        o.nthreads = threads
+        o.attention(rows)
+        t_att = time.perf_counter() - t0
+        dt = t_new + t_att * total / n_rows
+        add(f"{label}: quantise the new tokens + fp64 attention of "
+            f"{'all ' if rows is None else ''}{n_rows} of {total} query rows", threads,
+            "KV-tokens/s", w.kv_tokens / dt, t_new + t_att, rows is not None)
+        return w.kv_tokens / dt
+
+    c1 = synth.tiny_decode()
+    step(c1, None, 1, c1.name)
+    step(c1, None, allc, c1.name)
+    c2 = synth.steady_decode()
+    main = step(c2, None, allc, c2.name)
+    step(c2, rows_sample(c2, 1, 0), 1, c2.name)
+    c3 = synth.ragged_decode()
+    step(c3, None, allc, c3.name)
+    step(c3, rows_sample(c3, 1, 0), 1, c3.name)
+    c4 = synth.spec_verify()
+    step(c4, None, allc, c4.name)
+    c5 = synth.prefill_chunk()
+    step(c5, rows_sample(c5, max(16, allc), 0), allc, c5.name)
+    return main, res
 
 
 def run_cuda(args, world, rank, local):
@@ -514,17 +648,20 @@ def run_cuda(args, world, rank, local):
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) / 1e3
 
-    for fn in (two_call_step, attn_only, fused_step):
-        for _ in range(args.warmup):
-            fn()
-    torch.cuda.synchronize(dev)
     side_steps = max(10, min(args.steps, 5000))
     clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the warm-up and the timed region
+    for fn in (two_call_step, attn_only):
+        for _ in range(args.warmup):
+            fn()
+    # the W warm-up steps directly before the timed steps, so the GPU is not idle in between
+    for _ in range(args.warmup):
+        fused_step()
+    torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    clocks.start()
-    time.sleep(0.3)  # let the sampler start before the timed region
     elapsed = back_to_back(fused_step, args.steps)
     two_call_avg = back_to_back(two_call_step, side_steps) / side_steps
     attn_avg = back_to_back(attn_only, side_steps) / side_steps
@@ -569,7 +706,40 @@ def run_cuda(args, world, rank, local):
 
     spill = spill_restore(g, dev, stream)
     cmp = None if args.no_comparators else comparators(w, dev, stream, measured_peaks()[0])
-    tiles = None if args.no_tile_workloads else tile_workloads(dev, stream, measured_peaks()[0])
+
+    # ---- every workload of the parity tests, in the launch configuration timed here ----
+    peak0 = measured_peaks()[0]
+    bf16, _ = measured_bf16_tflops()
+    configs = {}
+    c2 = {"call": "kv_nvfp4_decode_step", "chunk_tokens": CHUNK, "steps": args.steps,
+          "step_us": None, "note": "the headline line's own workload and numbers"}
+    try:
+        c2["cosine_vs_unquantized"] = unquantized_cosine(g, all_rows(w))
+        c2["cosine_rows"] = w.num_seqs * w.q_len * w.q_heads
+    except RuntimeError as e:  # reporting only: never fails the bench
+        c2["cosine_error"] = str(e)[:200]
+    configs[w.name] = c2
+    if not args.no_configs:
+        for wc, chunk in ((synth.tiny_decode(), 64), (synth.ragged_decode(), 1024)):
+            gc, r = decode_config(wc, chunk, dev, stream, max(args.steps, 20), args.warmup, peak0)
+            r["cosine_vs_unquantized"] = unquantized_cosine(gc, all_rows(wc))
+            r["cosine_rows"] = wc.num_seqs * wc.q_len * wc.q_heads
+            if wc.name == "tiny_decode_4k":
+                r["note"] = "2.4 MB of KV: L2-resident, so this is a latency figure"
+            configs[wc.name] = r
+            del gc
+            torch.cuda.empty_cache()
+    if not args.no_tile_workloads:
+        from kvrun import sample_rows
+        for wc, chunk, reps, n_cos in ((synth.spec_verify(), 1024, 200, None),
+                                       (synth.prefill_chunk(), 1024, 5, 64)):
+            gc, r = tile_config(wc, chunk, dev, stream, reps, peak0, bf16)
+            rows = all_rows(wc) if n_cos is None else sample_rows(wc, n_cos, seed=0)
+            r["cosine_vs_unquantized"] = unquantized_cosine(gc, rows)
+            r["cosine_rows"] = len(rows[0])
+            configs[wc.name] = r
+            del gc
+            torch.cuda.empty_cache()
 
     elapsed, e2e_elapsed = max_over_ranks([elapsed, e2e_elapsed], dev)
     if rank != 0:
@@ -590,6 +760,9 @@ def run_cuda(args, world, rank, local):
     achieved = step_bytes / step_avg / 1e9
     attn_gbs = attn_bytes / attn_avg / 1e9
     traffic = decode_traffic_profile()
+    c2.update({"step_us": step_avg * 1e6, "kv_tokens": kv_tokens,
+               "kv_tokens_per_s": kv_tokens / step_avg, "hbm_gbs": achieved,
+               "hbm_frac_of_measured": achieved / peak, "algorithmic_bytes": step_bytes})
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
@@ -622,10 +795,16 @@ def run_cuda(args, world, rank, local):
         "gpu_launches": 2 * args.steps,  # per timed step: the attention kernel, split-K merge
         "spill": spill,
         "comparators": cmp,
-        "tile_workloads": tiles,
+        "configs": configs,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = oracle_sample(w)
+        main_value, detail = cpu_baseline_rows()
+        line["cpu_baseline"] = {
+            "value": main_value, "unit": UNIT, "cores": detail["threads_all"], "kind": "oracle",
+            "sample": "the headline step in full on all host threads: the 4 new tokens quantised "
+                      "(Q, K, V) and the fp64 attention of all 96 query rows over 524,292 keys; "
+                      "the cached rows are quantised before the clock",
+            "nproc": detail["nproc"], "rows": detail["rows"]}
     print(json.dumps(line), flush=True)
 
 
@@ -640,6 +819,8 @@ def main():
                     help="short run of the verify or prefill-chunk attention call (profiling)")
     ap.add_argument("--no-tile-workloads", action="store_true",
                     help="skip timing the verify and prefill-chunk shapes (tile kernel)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip timing the tiny and ragged decode workloads")
     ap.add_argument("--no-comparators", action="store_true",
                     help="skip the bf16 / int8 / NVFP4 K + fp16 V comparator timings")
     ap.add_argument("--seqs", type=int, default=4, help="sequences of 131072 tokens (profiling)")

@@ -12,7 +12,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD, "libkvnvfp4.so")
 SOURCES = ["api.cu", "append.cu", "decode.cu", "tile.cu", "decode_noalloc.cu", "spill.cu",
-           "compare.cu"]
+           "compare.cu", "host_step.cu"]
 HEADERS = ["nvfp4_device.cuh"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

@@ -18,7 +18,7 @@ cudaError_t launch_append(const uint16_t* q, const uint16_t* k, const uint16_t* 
                           const int32_t* block_table, int32_t num_seqs, int32_t max_pages,
                           int32_t num_pages, uint8_t* pool, uint8_t* q_codes,
                           uint8_t* q_scales, int32_t Hq, int32_t Hkv, int32_t* status,
-                          cudaStream_t stream);
+                          int32_t num_sms, cudaStream_t stream);
 cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const uint8_t* pool,
                           const int32_t* block_table, int32_t max_pages, int32_t num_pages,
                           const void* groups, const void* segments, const int32_t* cta_seg,
@@ -28,7 +28,7 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
                           float sm_scale, const uint16_t* q_new, const uint16_t* k_new,
                           const uint16_t* v_new, const float* rope, int32_t rope_max_pos,
                           int32_t rot_dim, uint8_t* pool_w, uint8_t* q_codes_out,
-                          uint8_t* q_scales_out, cudaStream_t stream);
+                          uint8_t* q_scales_out, bool late_tables, cudaStream_t stream);
 int cmp_chunk_bytes(int fmt);
 cudaError_t launch_cmp_append(int fmt, const uint16_t* q, const uint16_t* k, const uint16_t* v,
                               const int32_t* seq_ids, const int32_t* positions, int64_t T,
@@ -51,6 +51,10 @@ cudaError_t launch_tile(const uint8_t* q_codes, const uint8_t* q_scales, const u
 cudaError_t launch_page_copy(bool spill, const uint8_t* src, uint8_t* dst, const int32_t* ids,
                              int32_t n, int32_t num_pages, uint32_t page_bytes, int sms,
                              int32_t* status, cudaStream_t stream);
+cudaError_t launch_step_inputs(const void* const src[3], void* const dst[3],
+                               const uint32_t n16[3], const void* plan, uint32_t plan_bytes,
+                               void* workspace, cudaStream_t stream);
+int inline_plan_bytes();
 }  // namespace kvnvfp4
 
 namespace {
@@ -249,6 +253,20 @@ namespace {
 
 // Build the plan for num_ctas CTAs and upload its tables (everything before the partials) into
 // the device workspace with one copy on the stream.
+// The host image of a plan's tables (groups, segments, per-CTA segment ranges, split-group list;
+// everything before info.off_partials), as the workspace holds them.
+std::vector<int32_t> plan_image(const PlanBuild& pb) {
+  const kv_nvfp4_plan_info& pi = pb.info;
+  std::vector<int32_t> host((size_t)(pi.off_partials / 4), 0);
+  std::memcpy(host.data() + pi.off_groups / 4, pb.groups.data(), pb.groups.size() * 4);
+  std::memcpy(host.data() + pi.off_segments / 4, pb.segments.data(), pb.segments.size() * 4);
+  std::memcpy(host.data() + pi.off_cta / 4, pb.cta_seg.data(), pb.cta_seg.size() * 4);
+  std::memcpy(host.data() + pi.off_split / 4, pb.split.data(), pb.split.size() * 4);
+  return host;
+}
+
+// Build the plan for num_ctas CTAs and upload its tables (everything before the partials) into
+// the device workspace with one copy on the stream.
 kv_nvfp4_status plan_upload(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, int32_t num_seqs,
                             int32_t q_len, int32_t causal, int32_t chunk_tokens, int num_ctas,
                             bool tile, void* d_workspace, size_t ws_bytes,
@@ -259,11 +277,7 @@ kv_nvfp4_status plan_upload(const kv_nvfp4_layout* L, const int32_t* h_seq_lens,
   if (s != KV_NVFP4_OK) return s;
   const kv_nvfp4_plan_info& pi = pb.info;
   if (ws_bytes < pi.workspace_bytes) return KV_NVFP4_ENOSPACE;
-  std::vector<int32_t> host((size_t)(pi.off_partials / 4), 0);
-  std::memcpy(host.data() + pi.off_groups / 4, pb.groups.data(), pb.groups.size() * 4);
-  std::memcpy(host.data() + pi.off_segments / 4, pb.segments.data(), pb.segments.size() * 4);
-  std::memcpy(host.data() + pi.off_cta / 4, pb.cta_seg.data(), pb.cta_seg.size() * 4);
-  std::memcpy(host.data() + pi.off_split / 4, pb.split.data(), pb.split.size() * 4);
+  const std::vector<int32_t> host = plan_image(pb);
   const cudaError_t e = cudaMemcpyAsync(d_workspace, host.data(), host.size() * 4,
                                         cudaMemcpyHostToDevice, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e);
@@ -271,7 +285,16 @@ kv_nvfp4_status plan_upload(const kv_nvfp4_layout* L, const int32_t* h_seq_lens,
   return KV_NVFP4_OK;
 }
 
-
+// Device address of page-locked host memory (its mapping into the GPU's address space), or null
+// for any other kind of memory. Clears the error a failed query leaves behind.
+const void* mapped_host_address(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
 
 // Device address of an arena: page-locked host memory (its mapped device address) or device
 // memory. Pageable host memory, which the GPU cannot address on every system, is refused.
@@ -314,6 +337,49 @@ kv_nvfp4_status page_copy(const kv_nvfp4_layout* L, bool spill, const uint8_t* p
 }
 
 }  // namespace
+
+// The fused decode step; late_tables: the plan tables are written by a kernel of the same step
+// (the merge reads them only after its wait).
+static kv_nvfp4_status decode_step_impl(const kv_nvfp4_layout* L, const kv_nvfp4_plan_info* plan,
+                                     void* d_workspace, const void* q, const void* k,
+                                     const void* v, const float* d_rope_table,
+                                     int32_t rope_max_pos, const int32_t* d_block_table,
+                                     int32_t max_pages, int32_t num_pages, uint8_t* pool,
+                                     uint8_t* q_codes_out, uint8_t* q_scales_out, float sm_scale,
+                                     float* out, int32_t* d_status, bool late_tables,
+                                     void* stream) {
+  if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || plan == nullptr) return KV_NVFP4_EINVAL;
+  if (L->num_kv_heads > kMaxAttnKvHeads) return KV_NVFP4_EINVAL;
+  if (plan->num_kv_heads != L->num_kv_heads || plan->num_seqs <= 0 || plan->q_len <= 0 ||
+      plan->grid <= 0)
+    return KV_NVFP4_EINVAL;
+  // one row tile per sequence: each new row is encoded and stored by exactly one CTA
+  if ((int64_t)(L->num_q_heads / L->num_kv_heads) * plan->q_len > kRowsPerItem)
+    return KV_NVFP4_EINVAL;
+  if (!d_workspace || !q || !k || !v || !pool || !d_block_table || !out || num_pages <= 0 ||
+      max_pages <= 0)
+    return KV_NVFP4_EINVAL;
+  if ((q_codes_out == nullptr) != (q_scales_out == nullptr)) return KV_NVFP4_EINVAL;
+  if (L->rot_dim > 0 && (!d_rope_table || rope_max_pos <= 0 || !aligned16(d_rope_table)))
+    return KV_NVFP4_EINVAL;
+  if ((int64_t)plan->max_seq_len > (int64_t)max_pages * L->page_size) return KV_NVFP4_EINVAL;
+  const void* ptrs[] = {d_workspace, q, k, v, pool, out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return KV_NVFP4_EINVAL;
+  if (!(sm_scale > 0.0f)) sm_scale = 1.0f / std::sqrt((float)L->head_dim);
+  char* ws = (char*)d_workspace;
+  const cudaError_t e = kvnvfp4::launch_decode(
+      nullptr, nullptr, pool, d_block_table, max_pages, num_pages, ws + plan->off_groups,
+      ws + plan->off_segments, (const int32_t*)(ws + plan->off_cta),
+      (const int32_t*)(ws + plan->off_split), plan->num_split_groups,
+      (float*)(ws + plan->off_partials), out, d_status,
+      L->num_q_heads, L->num_kv_heads, plan->q_len, plan->causal, plan->grid, sm_scale,
+      (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, d_rope_table, rope_max_pos,
+      L->rot_dim, pool, q_codes_out, q_scales_out, late_tables, (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
+
 
 extern "C" {
 
@@ -416,7 +482,7 @@ kv_nvfp4_status kv_nvfp4_append(const kv_nvfp4_layout* L, const void* q, const v
       (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, d_seq_ids, d_positions, T,
       d_rope_table, rope_max_pos, L->rot_dim, d_block_table, num_seqs, max_pages, num_pages,
       pool, q_codes, q_scales, L->num_q_heads, L->num_kv_heads,
-      d_status, (cudaStream_t)stream);
+      d_status, num_sms_current_device(), (cudaStream_t)stream);
   return cuda_status(e);
 }
 
@@ -511,7 +577,7 @@ kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout* L, const kv_nvfp4_pl
         (const int32_t*)(ws + plan->off_split), plan->num_split_groups,
         (float*)(ws + plan->off_partials), out, d_status,
         L->num_q_heads, L->num_kv_heads, plan->q_len, plan->causal, plan->grid, sm_scale,
-        nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, nullptr, nullptr,
+        nullptr, nullptr, nullptr, nullptr, 0, 0, nullptr, nullptr, nullptr, false,
         (cudaStream_t)stream);
   }
   return cuda_status(e);
@@ -524,37 +590,10 @@ kv_nvfp4_status kv_nvfp4_decode_step(const kv_nvfp4_layout* L, const kv_nvfp4_pl
                                      int32_t max_pages, int32_t num_pages, uint8_t* pool,
                                      uint8_t* q_codes_out, uint8_t* q_scales_out, float sm_scale,
                                      float* out, int32_t* d_status, void* stream) {
-  if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || plan == nullptr) return KV_NVFP4_EINVAL;
-  if (L->num_kv_heads > kMaxAttnKvHeads) return KV_NVFP4_EINVAL;
-  if (plan->num_kv_heads != L->num_kv_heads || plan->num_seqs <= 0 || plan->q_len <= 0 ||
-      plan->grid <= 0)
-    return KV_NVFP4_EINVAL;
-  // one row tile per sequence: each new row is encoded and stored by exactly one CTA
-  if ((int64_t)(L->num_q_heads / L->num_kv_heads) * plan->q_len > kRowsPerItem)
-    return KV_NVFP4_EINVAL;
-  if (!d_workspace || !q || !k || !v || !pool || !d_block_table || !out || num_pages <= 0 ||
-      max_pages <= 0)
-    return KV_NVFP4_EINVAL;
-  if ((q_codes_out == nullptr) != (q_scales_out == nullptr)) return KV_NVFP4_EINVAL;
-  if (L->rot_dim > 0 && (!d_rope_table || rope_max_pos <= 0 || !aligned16(d_rope_table)))
-    return KV_NVFP4_EINVAL;
-  if ((int64_t)plan->max_seq_len > (int64_t)max_pages * L->page_size) return KV_NVFP4_EINVAL;
-  const void* ptrs[] = {d_workspace, q, k, v, pool, out};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return KV_NVFP4_EINVAL;
-  if (!(sm_scale > 0.0f)) sm_scale = 1.0f / std::sqrt((float)L->head_dim);
-  char* ws = (char*)d_workspace;
-  const cudaError_t e = kvnvfp4::launch_decode(
-      nullptr, nullptr, pool, d_block_table, max_pages, num_pages, ws + plan->off_groups,
-      ws + plan->off_segments, (const int32_t*)(ws + plan->off_cta),
-      (const int32_t*)(ws + plan->off_split), plan->num_split_groups,
-      (float*)(ws + plan->off_partials), out, d_status,
-      L->num_q_heads, L->num_kv_heads, plan->q_len, plan->causal, plan->grid, sm_scale,
-      (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, d_rope_table, rope_max_pos,
-      L->rot_dim, pool, q_codes_out, q_scales_out, (cudaStream_t)stream);
-  return cuda_status(e);
+  return decode_step_impl(L, plan, d_workspace, q, k, v, d_rope_table, rope_max_pos,
+                          d_block_table, max_pages, num_pages, pool, q_codes_out, q_scales_out,
+                          sm_scale, out, d_status, false, stream);
 }
-
 
 kv_nvfp4_status kv_nvfp4_decode_step_host(
     const kv_nvfp4_layout* L, const int32_t* h_seq_lens, int32_t num_seqs, int32_t q_len,
@@ -579,20 +618,51 @@ kv_nvfp4_status kv_nvfp4_decode_step_host(
   const size_t rows = (size_t)num_seqs * (size_t)q_len;
   const size_t qb = rows * (size_t)L->num_q_heads * 256, kb = rows * (size_t)L->num_kv_heads * 256;
   const size_t ob = rows * (size_t)L->num_q_heads * 128 * 4;
-  cudaError_t e = cudaMemcpyAsync(d_q, h_q, qb, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(d_k, h_k, kb, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(d_v, h_v, kb, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return cuda_status(e);
-  kv_nvfp4_plan_info info;
-  kv_nvfp4_status s = plan_upload(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_sms,
-                                  false, d_workspace, ws_bytes, &info, stream);
+  PlanBuild pb;
+  kv_nvfp4_status s = plan_build(L, h_seq_lens, num_seqs, q_len, causal, chunk_tokens, num_sms,
+                                 false, &pb);
   if (s != KV_NVFP4_OK) return s;
-  s = kv_nvfp4_decode_step(L, &info, d_workspace, d_q, d_k, d_v, d_rope_table, rope_max_pos,
-                           d_block_table, max_pages, num_pages, pool, nullptr, nullptr, sm_scale,
-                           d_out, d_status, stream);
+  const kv_nvfp4_plan_info& info = pb.info;
+  if (ws_bytes < info.workspace_bytes) return KV_NVFP4_ENOSPACE;
+  const std::vector<int32_t> image = plan_image(pb);
+  // Page-locked host buffers (16-byte aligned): the GPU reads the new rows and writes the output
+  // over the host link itself, with no copy-engine operation in the step. Otherwise: copies.
+  const void* mq = aligned16(h_q) ? mapped_host_address(h_q) : nullptr;
+  const void* mk = aligned16(h_k) ? mapped_host_address(h_k) : nullptr;
+  const void* mv = aligned16(h_v) ? mapped_host_address(h_v) : nullptr;
+  const void* mo = aligned16(h_out) ? mapped_host_address(h_out) : nullptr;
+  const bool zero_copy = mq && mk && mv && mo && aligned16(d_q) && aligned16(d_k) &&
+                         aligned16(d_v) && qb / 16 <= 0xFFFFFFFFull;
+  cudaError_t e = cudaSuccess;
+  if (zero_copy) {
+    const size_t img_bytes = image.size() * 4;
+    const bool inline_plan = img_bytes <= (size_t)kvnvfp4::inline_plan_bytes();
+    if (!inline_plan)
+      e = cudaMemcpyAsync(d_workspace, image.data(), img_bytes, cudaMemcpyHostToDevice, st);
+    const void* src[3] = {mq, mk, mv};
+    void* dst[3] = {d_q, d_k, d_v};
+    const uint32_t n16[3] = {(uint32_t)(qb / 16), (uint32_t)(kb / 16), (uint32_t)(kb / 16)};
+    if (e == cudaSuccess)
+      e = kvnvfp4::launch_step_inputs(src, dst, n16, inline_plan ? image.data() : nullptr,
+                                      inline_plan ? (uint32_t)img_bytes : 0u, d_workspace, st);
+    if (e != cudaSuccess) return cuda_status(e);
+  } else {
+    e = cudaMemcpyAsync(d_q, h_q, qb, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(d_k, h_k, kb, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(d_v, h_v, kb, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(d_workspace, image.data(), image.size() * 4, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  float* out = zero_copy ? static_cast<float*>(const_cast<void*>(mo)) : d_out;
+  s = decode_step_impl(L, &info, d_workspace, d_q, d_k, d_v, d_rope_table, rope_max_pos,
+                       d_block_table, max_pages, num_pages, pool, nullptr, nullptr, sm_scale, out,
+                       d_status, zero_copy, stream);
   if (s != KV_NVFP4_OK) return s;
-  e = cudaMemcpyAsync(h_out, d_out, ob, cudaMemcpyDeviceToHost, st);
-  if (e != cudaSuccess) return cuda_status(e);
+  if (!zero_copy) {
+    e = cudaMemcpyAsync(h_out, d_out, ob, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   if (plan_out != nullptr) *plan_out = info;
   return KV_NVFP4_OK;
 }

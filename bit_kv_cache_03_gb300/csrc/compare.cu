@@ -41,7 +41,7 @@ namespace kvnvfp4 {
 cudaError_t launch_split_merge(const void* groups, const int32_t* split_groups,
                                const float* partials, float* out, int32_t Hq, int32_t Hkv,
                                int32_t G, int32_t q_len, float c2, int32_t num_split,
-                               cudaStream_t stream);
+                               bool late_tables, cudaStream_t stream);
 
 namespace {
 
@@ -666,7 +666,7 @@ cudaError_t launch_cmp_decode(int fmt, const uint16_t* q, const uint8_t* pool,
     if (e != cudaSuccess) return e;
   }
   return launch_split_merge(groups, split_groups, partials, out, Hq, Hkv, p.G, q_len, p.c2,
-                            num_split, stream);
+                            num_split, false, stream);
 }
 
 }  // namespace kvnvfp4

@@ -916,17 +916,21 @@ struct MergeParams {
   float c2;
 };
 
+// LATE_TABLES: the plan tables were written by a kernel earlier in the same step (not by a copy
+// before the attention launch), so they are read only after the wait as well.
+template <bool LATE_TABLES>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
   __shared__ float s_m[8], s_l[8];
   __shared__ float4 s_o[8][32];
   asm volatile("griddepcontrol.launch_dependents;");  // the next kernel may begin its launch
+  // launched as a programmatic dependent of the attention kernel: its partials are visible only
+  // after this wait (which returns when that grid has completed and flushed)
+  if (LATE_TABLES) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int gi = p.split[blockIdx.x];  // plan tables: written before the attention launch
   const int h = blockIdx.y / kRows, i = blockIdx.y % kRows;
   const int4 g0 = p.groups[2 * gi], g1 = p.groups[2 * gi + 1];
   const int r = g0.z * kRows + i;
-  // launched as a programmatic dependent of the attention kernel: its partials are visible only
-  // after this wait (which returns when that grid has completed and flushed)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!LATE_TABLES) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (r >= p.G * p.q_len) return;  // padding row of the last tile (uniform over the CTA)
   const int n_seg = g1.x;
   const int slice = threadIdx.x >> 5, d4 = threadIdx.x & 31;
@@ -982,7 +986,7 @@ int decode_smem_bytes() { return kSmemBytes; }
 cudaError_t launch_split_merge(const void* groups, const int32_t* split_groups,
                                const float* partials, float* out, int32_t Hq, int32_t Hkv,
                                int32_t G, int32_t q_len, float c2, int32_t num_split,
-                               cudaStream_t stream);
+                               bool late_tables, cudaStream_t stream);
 
 cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const uint8_t* pool,
                           const int32_t* block_table, int32_t max_pages, int32_t num_pages,
@@ -993,7 +997,7 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
                           float sm_scale, const uint16_t* q_new, const uint16_t* k_new,
                           const uint16_t* v_new, const float* rope, int32_t rope_max_pos,
                           int32_t rot_dim, uint8_t* pool_w, uint8_t* q_codes_out,
-                          uint8_t* q_scales_out, cudaStream_t stream) {
+                          uint8_t* q_scales_out, bool late_tables, cudaStream_t stream) {
   // the attribute belongs to each instantiation and each device: set once per device
   static bool attr_done[64] = {};
   int dev = 0;
@@ -1048,7 +1052,7 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || num_split <= 0) return e;
   return launch_split_merge(p.groups, split_groups, partials, out, Hq, Hkv, p.G, q_len, p.c2,
-                            num_split, stream);
+                            num_split, late_tables, stream);
 }
 
 // The split-K merge launch (also used by the comparator decode): one CTA per (split group, KV
@@ -1057,7 +1061,7 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
 cudaError_t launch_split_merge(const void* groups, const int32_t* split_groups,
                                const float* partials, float* out, int32_t Hq, int32_t Hkv,
                                int32_t G, int32_t q_len, float c2, int32_t num_split,
-                               cudaStream_t stream) {
+                               bool late_tables, cudaStream_t stream) {
   if (num_split <= 0) return cudaSuccess;
   MergeParams mp;
   mp.groups = static_cast<const int4*>(groups); mp.split = split_groups; mp.partials = partials;
@@ -1072,7 +1076,8 @@ cudaError_t launch_split_merge(const void* groups, const int32_t* split_groups,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, merge_kernel, mp);
+  return late_tables ? cudaLaunchKernelEx(&cfg, merge_kernel<true>, mp)
+                     : cudaLaunchKernelEx(&cfg, merge_kernel<false>, mp);
 }
 
 }  // namespace kvnvfp4

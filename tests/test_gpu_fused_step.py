@@ -66,25 +66,41 @@ def test_fused_step_flags_a_page_outside_the_pool():
     g.cache.block_table.copy_(bt)
 
 
-def test_decode_step_from_host_buffers_matches_device_step():
-    # kv_nvfp4_decode_step_host (H2D copies, plan, fused step, D2H in one call) against the
-    # device-buffer step on the same inputs: every code byte as the oracle's, identical output
+@pytest.mark.parametrize("pinned", [True, False])
+def test_decode_step_from_host_buffers_matches_device_step(pinned):
+    # kv_nvfp4_decode_step_host (new rows in, output out, plan, fused step in one call) against the
+    # device-buffer step on the same inputs, three steps in a row with different new rows each
+    # step: every pool byte and every output value identical. Page-locked host buffers take the
+    # path where the GPU reads the rows and writes the output over the host link itself;
+    # pageable ones take the copy path.
     w = synth.Workload("host_step", [700, 64, 3000], q_len=1, seed=21, chunk_tokens=128)
     ref = GpuRun(w)
-    ref.step_fused()
-    torch.cuda.synchronize()
     g = GpuRun(w)
     g.cache.plan(w.seq_lens, w.q_len, w.causal, 128)  # sizes the workspace
-    q, k, v, *_ = w.new_tokens()
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
-    h_q, h_k, h_v = pin(q), pin(k), pin(v)
+    q0, k0, v0, *_ = w.new_tokens()
+    host = (lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()) \
+        if pinned else (lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16).copy()))
+    h_q, h_k, h_v = host(q0), host(k0), host(v0)
     d_q, d_k, d_v = (torch.empty_like(t, device="cuda") for t in (h_q, h_k, h_v))
-    h_out = torch.full((g.out.numel(),), float("nan"), dtype=torch.float32).pin_memory()
-    g.cache.decode_step_host(np.asarray(w.seq_lens, np.int32), w.q_len, h_q, h_k, h_v, d_q, d_k,
-                             d_v, g.out, h_out, causal=w.causal, chunk_tokens=128,
-                             sm_scale=w.sm_scale)
-    torch.cuda.synchronize()
-    assert g.status() == 0 and ref.status() == 0
-    bad = compare_pool(g, OracleRun(w))
-    assert all(v == 0 for v in bad.values()), bad
-    assert np.array_equal(h_out.numpy(), ref.out.cpu().numpy())
+    h_out = torch.full((g.out.numel(),), float("nan"), dtype=torch.float32)
+    if pinned:
+        h_out = h_out.pin_memory()
+    for step in range(3):
+        # this step's new rows: the workload's own rows for step 0, other seeded rows after
+        ws = synth.Workload("host_step", [700, 64, 3000], q_len=1, seed=21 + 100 * step)
+        q, k, v, *_ = ws.new_tokens()
+        for t, a in ((h_q, q), (h_k, k), (h_v, v)):
+            t.copy_(torch.from_numpy(np.ascontiguousarray(a).view(np.int16)))
+        for t, a in ((ref.q, q), (ref.k, k), (ref.v, v)):
+            t.copy_(torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16))
+        ref.step_fused(chunk_tokens=128)
+        g.cache.decode_step_host(np.asarray(w.seq_lens, np.int32), w.q_len, h_q, h_k, h_v, d_q,
+                                 d_k, d_v, g.out, h_out, causal=w.causal, chunk_tokens=128,
+                                 sm_scale=w.sm_scale)
+        torch.cuda.synchronize()
+        assert g.status() == 0 and ref.status() == 0
+        assert np.array_equal(h_out.numpy(), ref.out.cpu().numpy()), step
+        assert torch.equal(g.cache.pool, ref.cache.pool), step
+        if step == 0:  # the workload's own new rows: every code byte as the oracle's
+            bad = compare_pool(g, OracleRun(w))
+            assert all(v == 0 for v in bad.values()), bad
