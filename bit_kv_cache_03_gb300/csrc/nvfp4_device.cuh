@@ -70,6 +70,31 @@ __device__ __forceinline__ float div_rn_by(float x, float b, float r) {
   return __fmaf_rn(res, r, q0);
 }
 
+// x / b rounded to nearest, sign of x kept (a negative zero stays negative), from r = the correctly
+// rounded 1 / b: the same Markstein step as div_rn_by with the residual's sign flipped,
+// q0 = x r, e = q0 b - x (exact), q = q0 - e r. For x = -0 the last step adds -0 to -0, so the
+// quotient is -0 and needs no separate sign fix. Correctly rounded whenever the quotient is normal.
+__device__ __forceinline__ float quot_rn(float x, float b, float r) {
+  const float q0 = __fmul_rn(x, r);
+  const float e = __fmaf_rn(q0, b, -x);
+  return __fmaf_rn(-e, r, q0);
+}
+
+// Eight f32 -> eight E2M1 codes (element 0 in the low nibble) with the hardware converter, packed
+// into one word.
+__device__ __forceinline__ uint32_t e2m1x8_from_f32(const float (&q)[8]) {
+  uint32_t r;
+  asm("{\n.reg .b8 b0, b1, b2, b3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      "mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(r)
+      : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+  return r;
+}
+
 // This lane's RoPE factors for a row at angle-table row `rope_row` (cos of its 4 dims, then sin):
 // lanes below rot/4 hold dims of a rotated pair, the others (and a null row) get zeros. Kept apart
 // from the encode so that a caller can issue the loads of several rows before any arithmetic.
@@ -178,7 +203,7 @@ __device__ __forceinline__ void nvfp4_encode_rows(float (&x)[R][4], bool rotate,
     const float rs = __frcp_rn(sd);
     float q[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) q[e] = copysignf(div_rn_by(x[r][e], sd, rs), x[r][e]);
+    for (int e = 0; e < 4; ++e) q[e] = quot_rn(x[r][e], sd, rs);
     const uint32_t pk = e2m1x2_from_f32(q[1], q[0]) | (e2m1x2_from_f32(q[3], q[2]) << 8);
     packed[r] = sd != 0.0f ? pk : 0u;  // an all-zero block: zero scale, zero codes
   }

@@ -13,7 +13,9 @@
 //      non-negative finite amax;
 //   4. div_rn_by(x, s, 1/s) against __fdiv_rn(x, s) (bits and E2M1 code) for all 126 positive
 //      E4M3 scales s and every x in [s / 16, 32 s), plus signed zeros and tiny values;
-//   5. nvfp4_encode_rows<4> against four calls of nvfp4_encode_rows<1> on random rows.
+//   5. nvfp4_encode_rows<4> against four calls of nvfp4_encode_rows<1> on random rows;
+//   6. quot_rn(x, s, 1/s), the quotient that keeps the sign of x, against __fdiv_rn(x, s) for x and
+//      -x over the inputs of check 4, and its E2M1 code for signed zeros and tiny values.
 // Prints one "name mismatches N" line per check; exit status 0 when the checks ran.
 #include <cstdint>
 #include <cstdio>
@@ -50,8 +52,9 @@ __device__ uint32_t e2m1_by_definition(float x) {
   return c | ((__float_as_uint(x) >> 28) & 8u);
 }
 
-__device__ unsigned long long g_bad[9];
-__device__ unsigned long long g_first[9];
+constexpr int kChecks = 11;
+__device__ unsigned long long g_bad[kChecks];
+__device__ unsigned long long g_first[kChecks];
 
 __device__ void bad(int slot, unsigned long long v) {
   if (atomicAdd(&g_bad[slot], 1ull) == 0ull) g_first[slot] = v;
@@ -103,6 +106,10 @@ __global__ void check_quotient(unsigned long long per_scale) {
     const unsigned long long tag = ((unsigned long long)code << 32) | b;
     if (__float_as_uint(ref) != __float_as_uint(got)) bad(5, tag);
     if (e2m1_by_definition(ref) != (e2m1x2_from_f32(got, 0.0f) >> 4)) bad(6, tag);
+    const float rs = __frcp_rn(s);
+    if (__float_as_uint(quot_rn(x, s, rs)) != __float_as_uint(ref) ||
+        __float_as_uint(quot_rn(-x, s, rs)) != __float_as_uint(__fdiv_rn(-x, s)))
+      bad(9, tag);
   }
 }
 
@@ -114,6 +121,9 @@ __global__ void check_zeros() {
       const float q = copysignf(div_rn_by(xs[k], s, r), xs[k]);
       if (e2m1_by_definition(__fdiv_rn(xs[k], s)) != (e2m1x2_from_f32(q, 0.0f) >> 4))
         bad(7, code * 8 + k);
+      if (e2m1_by_definition(__fdiv_rn(xs[k], s)) !=
+          (e2m1x2_from_f32(quot_rn(xs[k], s, r), 0.0f) >> 4))
+        bad(10, code * 8 + k);
     }
   }
 }
@@ -148,7 +158,7 @@ __global__ void check_rows(const float* in, const float* rope, int nwarps) {
 }  // namespace
 
 int main() {
-  const unsigned long long zero[9] = {};
+  const unsigned long long zero[kChecks] = {};
   if (cudaMemcpyToSymbol(g_bad, zero, sizeof(zero)) != cudaSuccess) return 2;
   check_e2m1<<<1216, 256>>>(1ull << 32);
   check_e4m3<<<1216, 256>>>(1ull << 31);
@@ -180,12 +190,13 @@ int main() {
     printf("cuda error %s\n", cudaGetErrorString(e));
     return 2;
   }
-  unsigned long long nb[9], fi[9];
+  unsigned long long nb[kChecks], fi[kChecks];
   cudaMemcpyFromSymbol(nb, g_bad, sizeof(nb));
   cudaMemcpyFromSymbol(fi, g_first, sizeof(fi));
-  const char* names[9] = {"e2m1_hi", "e2m1_lo", "e4m3_hi", "e4m3_lo", "scale_code",
-                          "quotient_bits", "quotient_code", "zeros_sign", "rows4_vs_rows1"};
-  for (int i = 0; i < 9; ++i)
+  const char* names[kChecks] = {"e2m1_hi", "e2m1_lo", "e4m3_hi", "e4m3_lo", "scale_code",
+                                "quotient_bits", "quotient_code", "zeros_sign", "rows4_vs_rows1",
+                                "signed_quotient_bits", "signed_quotient_zeros"};
+  for (int i = 0; i < kChecks; ++i)
     printf("%s mismatches %llu first %#llx\n", names[i], nb[i], nb[i] ? fi[i] : 0ull);
   cudaFree(d);
   cudaFree(dr);

@@ -80,7 +80,8 @@ def _append_crafted(Hq, Hkv, T, seed, rot_dim=32):
 
 @pytest.mark.parametrize("Hq,Hkv,T,rot", [(24, 4, 77, 32), (8, 8, 130, 32), (6, 1, 64, 128),
                                           (0, 4, 1, 32), (24, 4, 200, 0), (24, 4, 65, 64),
-                                          (24, 4, 33, 48), (4, 2, 70, 8), (3, 3, 1000, 120)])
+                                          (24, 4, 33, 48), (4, 2, 70, 8), (3, 3, 1000, 120),
+                                          (24, 4, 300, 32), (8, 2, 700, 64), (0, 4, 1100, 32)])
 def test_append_crafted_rows_bitexact(Hq, Hkv, T, rot):
     _append_crafted(Hq, Hkv, T, seed=T + Hq, rot_dim=rot)
 

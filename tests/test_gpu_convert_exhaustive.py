@@ -23,5 +23,5 @@ def test_encode_helpers_match_the_definitions_on_every_input(tmp_path):
                    check=True)
     out = subprocess.run([exe], check=True, capture_output=True, text=True, timeout=300).stdout
     counts = dict(re.findall(r"^(\w+) mismatches (\d+)", out, flags=re.M))
-    assert len(counts) == 9, out
+    assert len(counts) == 11, out
     assert all(v == "0" for v in counts.values()), out
