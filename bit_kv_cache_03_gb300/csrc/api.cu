@@ -66,11 +66,14 @@ constexpr int kPartHeadFloats = kRowsPerItem * 128 + 2 * kRowsPerItem;  // O[8][
 constexpr int kTileRows = 64;
 constexpr int kTilePartFloats = 2 * (kTileRows * 128 + 2 * kTileRows);
 
-// The attention kernel a (layout, q_len) pair runs on: more than 8 rows per KV head -> tile kernel.
+constexpr int kMaxAttnKvHeads = 4;  // the decode kernel stages every head of a page
+
+// The attention kernel a (layout, q_len) pair runs on: more than 8 rows per KV head, or more KV
+// heads than the decode kernel stages per page, -> the tile kernel (which works per KV-head pair).
 bool tile_mode(const kv_nvfp4_layout* L, int32_t q_len) {
-  return (int64_t)(L->num_q_heads / L->num_kv_heads) * q_len > kRowsPerItem;
+  return (int64_t)(L->num_q_heads / L->num_kv_heads) * q_len > kRowsPerItem ||
+         L->num_kv_heads > kMaxAttnKvHeads;
 }
-constexpr int kMaxAttnKvHeads = 4;  // the attention kernel stages every head of a page
 constexpr int kMaxGridForSizing = 1024;  // workspace sizing when no device is visible
 
 thread_local cudaError_t g_last_cuda_error = cudaSuccess;
@@ -415,7 +418,7 @@ kv_nvfp4_status kv_nvfp4_layout_check(const kv_nvfp4_layout* L) {
   if (L->head_dim != 128 || L->page_size != 64) return KV_NVFP4_EINVAL;
   if (L->num_kv_heads <= 0 || L->num_q_heads <= 0) return KV_NVFP4_EINVAL;
   if (L->num_q_heads % L->num_kv_heads != 0) return KV_NVFP4_EINVAL;
-  if (L->num_q_heads / L->num_kv_heads > 8) return KV_NVFP4_EINVAL;
+  if (L->num_q_heads > 4096) return KV_NVFP4_EINVAL;
   if (L->rot_dim < 0 || L->rot_dim > 128 || L->rot_dim % 8 != 0) return KV_NVFP4_EINVAL;
   return KV_NVFP4_OK;
 }
@@ -542,7 +545,6 @@ kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout* L, const kv_nvfp4_pl
                                      int32_t max_pages, float* out, int32_t* d_status,
                                      void* stream) {
   if (kv_nvfp4_layout_check(L) != KV_NVFP4_OK || plan == nullptr) return KV_NVFP4_EINVAL;
-  if (L->num_kv_heads > kMaxAttnKvHeads) return KV_NVFP4_EINVAL;
   if (plan->num_kv_heads != L->num_kv_heads || plan->num_seqs <= 0 || plan->q_len <= 0 ||
       plan->grid <= 0)
     return KV_NVFP4_EINVAL;

@@ -30,15 +30,23 @@ __global__ void __launch_bounds__(256) step_inputs_kernel(const __grid_constant_
   // the attention kernel of this step may be scheduled now; it waits for this grid to complete
   // before it reads the work list or the new rows
   asm volatile("griddepcontrol.launch_dependents;");
+  const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
+  const uint32_t nt = gridDim.x * blockDim.x;
+  // this thread's first unit of each buffer is read from host memory before the wait, so the
+  // host-link latency overlaps the previous kernel's tail (the host wrote the rows before the call)
+  uint4 first[3];
+#pragma unroll
+  for (int b = 0; b < 3; ++b)
+    if (tid < p.n16[b]) first[b] = p.src[b][tid];
   // the previous kernel on the stream (the last step's attention or merge) reads the workspace
   // and the device row buffers: overwrite them only after it has completed
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const uint32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
-  const uint32_t nt = gridDim.x * blockDim.x;
   for (uint32_t i = tid; i < p.plan_n16; i += nt) p.plan_dst[i] = p.plan[i];
 #pragma unroll
-  for (int b = 0; b < 3; ++b)
-    for (uint32_t i = tid; i < p.n16[b]; i += nt) p.dst[b][i] = p.src[b][i];
+  for (int b = 0; b < 3; ++b) {
+    if (tid < p.n16[b]) p.dst[b][tid] = first[b];
+    for (uint32_t i = tid + nt; i < p.n16[b]; i += nt) p.dst[b][i] = p.src[b][i];
+  }
 }
 
 }  // namespace
@@ -62,7 +70,8 @@ cudaError_t launch_step_inputs(const void* const src[3], void* const dst[3],
   p.plan_dst = static_cast<uint4*>(workspace);
   const uint4* pl = static_cast<const uint4*>(plan);
   for (uint32_t i = 0; i < p.plan_n16; ++i) p.plan[i] = pl[i];
-  // one 16-byte unit per thread of the largest buffer: every load is in flight at once
+  // one 16-byte unit per thread of the largest buffer (up to 256 KB): every load is in flight at
+  // once, and before the wait
   uint32_t grid = (total + 255) / 256;
   grid = grid < 1 ? 1 : (grid > 64 ? 64 : grid);
   cudaLaunchConfig_t cfg = {};

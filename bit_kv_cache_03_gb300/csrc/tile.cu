@@ -756,7 +756,7 @@ cudaError_t launch_tile(const uint8_t* q_codes, const uint8_t* q_scales, const u
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  if (Hkv < 1 || Hkv > 4) return cudaErrorInvalidValue;
+  if (Hkv < 1) return cudaErrorInvalidValue;
   TileParams p;
   p.q_codes = q_codes; p.q_scales = q_scales; p.pool = pool;
   p.block_table = block_table; p.max_pages = max_pages; p.num_pages = num_pages;

@@ -71,8 +71,8 @@ typedef int32_t kv_nvfp4_status;
 #define KV_NVFP4_DEV_TIMEOUT 0x10     /* an internal barrier wait hit its time limit */
 
 /* Model geometry of one attention layer. The library supports head_dim = 128 and
- * page_size = 64; num_q_heads must be a multiple of num_kv_heads with a group of at most 8;
- * rot_dim is even, a multiple of 8 and at most 128 (0 disables RoPE). */
+ * page_size = 64; num_q_heads (at most 4096) must be a multiple of num_kv_heads; rot_dim is a
+ * multiple of 8 and at most 128 (0 disables RoPE). */
 typedef struct kv_nvfp4_layout {
   int32_t num_q_heads;  /* 24 in the pages' model */
   int32_t num_kv_heads; /* 4 */
@@ -219,14 +219,14 @@ kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout *layout, const int32_t *h_se
  *   sm_scale:       softmax scale; <= 0 selects 1/sqrt(head_dim)
  *   pool, num_pages, d_block_table, max_pages: as for kv_nvfp4_append
  *   out:            DEVICE fp32 [num_seqs * q_len][num_q_heads][128]
- * Supports num_kv_heads <= 4 (every head of a page is staged together). Two kernel launches on
- * `stream`: the attention kernel (one persistent CTA per SM), then, when the plan has split groups,
- * the merge of their partials (one CTA per split group, KV head and row). With at most 8 rows per
- * KV head the attention kernel is the decode kernel (Q.K^T block-scaled on the tensor cores, P.V
- * on the warp-level tensor path); with more rows it is the tile kernel (64 rows of each head of a
- * KV-head pair per tile; Q.K^T block-scaled and P.V in f16, both on the tcgen05 tensor cores, O
- * accumulated in tensor memory). The workspace may be reused by the next call on the same stream;
- * calls that overlap on one workspace race. */
+ * Two kernel launches on `stream`: the attention kernel (one persistent CTA per SM), then, when
+ * the plan has split groups, the merge of their partials (one CTA per split group, KV head and
+ * row). With at most 8 rows per KV head and at most 4 KV heads the attention kernel is the decode
+ * kernel (every head of a page staged together; Q.K^T block-scaled on the tensor cores, P.V on the
+ * warp-level tensor path); otherwise it is the tile kernel (64 rows of each head of a KV-head pair
+ * per tile; Q.K^T block-scaled and P.V in f16, both on the tcgen05 tensor cores, O accumulated in
+ * tensor memory), which takes any number of KV heads and any group size. The workspace may be
+ * reused by the next call on the same stream; calls that overlap on one workspace race. */
 kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout *layout,
                                      const kv_nvfp4_plan_info *plan, void *d_workspace,
                                      const uint8_t *q_codes, const uint8_t *q_scales,
@@ -246,8 +246,9 @@ kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout *layout,
  *   q_codes_out, q_scales_out: optional (both or neither) DEVICE copy of the encoded Q rows,
  *              [num_seqs * q_len][num_q_heads][64 | 8]
  *   sm_scale, out, d_status: as for kv_nvfp4_decode_attn
- * Requires (num_q_heads / num_kv_heads) * q_len <= 8 (one 8-row tile per sequence: decode with
- * GQA groups up to 8); larger verify or prefill steps use the two calls. Status bits as for both
+ * Requires (num_q_heads / num_kv_heads) * q_len <= 8 and num_kv_heads <= 4 (one 8-row tile per
+ * sequence on the decode kernel: decode with GQA groups up to 8); larger verify or prefill steps,
+ * wider groups and more KV heads use the two calls. Status bits as for both
  * calls (a bad page or position skips the row). One kernel launch, plus the split-K merge launch
  * when the plan has split groups. */
 kv_nvfp4_status kv_nvfp4_decode_step(const kv_nvfp4_layout *layout,
@@ -266,17 +267,24 @@ kv_nvfp4_status kv_nvfp4_decode_step(const kv_nvfp4_layout *layout,
  * fused step's launches, and the device-to-host copy of the output. For a serving loop that
  * drives the library from host code once per step.
  *   h_seq_lens, num_seqs, q_len, causal, chunk_tokens: as for kv_nvfp4_plan (HOST lengths
- *              including the new tokens); (num_q_heads / num_kv_heads) * q_len <= 8
+ *              including the new tokens); (num_q_heads / num_kv_heads) * q_len <= 8 and
+ *              num_kv_heads <= 4
  *   d_workspace, ws_bytes: at least kv_nvfp4_plan_workspace_bytes bytes (DEVICE, 16-byte aligned)
- *   h_q, h_k, h_v: HOST bf16 rows laid out as q, k, v of kv_nvfp4_decode_step; page-locked
- *              memory makes the copies asynchronous (pageable memory is copied before return)
+ *   h_q, h_k, h_v: HOST bf16 rows laid out as q, k, v of kv_nvfp4_decode_step; keep them
+ *              unchanged until the stream has passed this call's work
  *   d_q, d_k, d_v: DEVICE buffers of the same sizes (16-byte aligned) that receive them
  *   d_rope_table, rope_max_pos, d_block_table, max_pages, num_pages, pool, sm_scale, d_status:
  *              as for kv_nvfp4_decode_step
- *   d_out:     DEVICE fp32 output [num_seqs * q_len][num_q_heads][128]
- *   h_out:     HOST copy of it (page-locked for an asynchronous copy), complete when the stream
- *              reaches the end of this call's work
+ *   d_out:     DEVICE fp32 buffer [num_seqs * q_len][num_q_heads][128]
+ *   h_out:     HOST fp32 output of the same shape, complete when the stream reaches the end of
+ *              this call's work
  *   plan_out:  optional HOST copy of the plan info (may be null)
+ * When h_q, h_k, h_v and h_out are page-locked and 16-byte aligned, no copy-engine operation is
+ * enqueued: a small kernel reads the new rows over the host link into d_q, d_k, d_v and writes
+ * the work list (passed inline when it is at most 8 KB, else copied), and the attention and merge
+ * kernels write the output rows straight into h_out (d_out is not written). Otherwise the rows and
+ * the work list are copied in, the output goes to d_out and is copied to h_out (pageable memory is
+ * staged by the runtime, which may wait for the stream's earlier work).
  * Returns once everything is enqueued; EINVAL before any copy for the argument checks above, or
  * the first error of the calls it makes. */
 kv_nvfp4_status kv_nvfp4_decode_step_host(

@@ -47,6 +47,26 @@ def test_attention_other_group_sizes(Hq, Hkv):
     _check(w, chunk=256)
 
 
+@pytest.mark.parametrize("Hq,Hkv,q_len", [
+    (24, 8, 1), (48, 8, 1),     # 8 KV heads, GQA 3 and 6: the tile kernel (per KV-head pair)
+    (48, 4, 1), (64, 4, 1),     # GQA 12 and 16: 12 and 16 rows per KV head
+    (24, 8, 3), (40, 5, 2),     # more than one new token; an odd number of KV heads above 4
+])
+def test_attention_more_kv_heads_and_larger_groups(Hq, Hkv, q_len):
+    w = synth.Workload("wide", [0, 700, 2100], q_len=q_len, seed=Hq + Hkv + q_len, q_heads=Hq,
+                       kv_heads=Hkv, chunk_tokens=256)
+    _check(w, chunk=256)
+
+
+def test_fused_step_refuses_more_than_four_kv_heads():
+    import bit_kv_cache_03_gb300 as kv
+    w = synth.Workload("wide_fused", [300], q_len=1, seed=2, q_heads=24, kv_heads=8)
+    g = GpuRun(w)
+    g.cache.plan(w.seq_lens, w.q_len, w.causal, 256)
+    with pytest.raises(kv.KVNVFP4Error, match=r"\(-1\)"):
+        g.step_fused(plan=False)
+
+
 def test_attention_position_scaling_and_full_rotation():
     w = synth.Workload("scaled", [3000], q_len=4, seed=5, rot_dim=128,
                        pos_scale=600000.0 / 262144.0, chunk_tokens=512)

@@ -43,8 +43,8 @@ def test_page_and_pool_bytes(kv):
 
 
 @pytest.mark.parametrize("bad", [dict(head_dim=64), dict(page_size=32), dict(num_q_heads=10),
-                                 dict(num_q_heads=72, num_kv_heads=4), dict(rot_dim=30),
-                                 dict(rot_dim=136)])
+                                 dict(num_q_heads=8192, num_kv_heads=4), dict(rot_dim=30),
+                                 dict(rot_dim=136), dict(num_kv_heads=0)])
 def test_layout_rejected(kv, bad):
     args = dict(num_q_heads=24, num_kv_heads=4, head_dim=128, page_size=64, rot_dim=32)
     args.update(bad)
@@ -109,14 +109,17 @@ def test_entry_points_reject_bad_arguments_before_cuda(kv):
     ([3], 1, True, 64, 152, 24, 4), ([600064], 8192, True, 64, 152, 24, 4),
     ([2000, 37], 8, False, 256, 7, 24, 4), ([900, 3000], 5, True, 128, 11, 9, 3),
     ([70, 4000], 3, True, 64, 20, 8, 1), ([500], 1, True, 64, 9, 9, 3),
+    ([3000, 70], 1, True, 128, 30, 24, 8), ([3000, 70], 1, True, 128, 30, 64, 4),
+    ([900], 2, True, 64, 13, 40, 5),
 ])
 def test_plan_covers_every_visible_page_once_and_balances(kv, lens, q_len, causal, chunk, ctas,
                                                           Hq, Hkv):
     L = kv.make_layout(Hq, Hkv)
     info, groups, segs, cta, split = kv.kv_nvfp4_plan_host(L, lens, q_len, causal, chunk, ctas)
     G = Hq // Hkv
-    # at most 8 rows per KV head: 8-row tiles over every head; more: 64-row tiles per head pair
-    tile_rows, n_pairs = (8, 1) if G * q_len <= 8 else (64, (Hkv + 1) // 2)
+    # at most 8 rows per KV head and at most 4 KV heads: 8-row tiles over every head; otherwise
+    # 64-row tiles per head pair
+    tile_rows, n_pairs = (8, 1) if G * q_len <= 8 and Hkv <= 4 else (64, (Hkv + 1) // 2)
     n_rg = (G * q_len + tile_rows - 1) // tile_rows
     assert info.num_row_groups == n_rg
     assert info.num_groups == len(lens) * n_pairs * n_rg == len(groups)
