@@ -62,14 +62,14 @@ namespace {
 constexpr int kRowsPerItem = 8;   // query rows per KV head in one decode work group
 constexpr int kPartHeadFloats = kRowsPerItem * 128 + 2 * kRowsPerItem;  // O[8][128], m[8], l[8]
 // Tiles of more rows (speculative verify, prefill chunks) go to the tile kernel: groups of one
-// KV-head pair and 64 rows per head, partials of both heads of the pair per segment.
-constexpr int kTileRows = 64;
-constexpr int kTilePartFloats = 2 * (kTileRows * 128 + 2 * kTileRows);
+// KV head and 128 rows, one partial (O, m, l of the tile's rows) per segment.
+constexpr int kTileRows = 128;
+constexpr int kTilePartFloats = kTileRows * 128 + 2 * kTileRows;
 
 constexpr int kMaxAttnKvHeads = 4;  // the decode kernel stages every head of a page
 
 // The attention kernel a (layout, q_len) pair runs on: more than 8 rows per KV head, or more KV
-// heads than the decode kernel stages per page, -> the tile kernel (which works per KV-head pair).
+// heads than the decode kernel stages per page, -> the tile kernel (which works per KV head).
 bool tile_mode(const kv_nvfp4_layout* L, int32_t q_len) {
   return (int64_t)(L->num_q_heads / L->num_kv_heads) * q_len > kRowsPerItem ||
          L->num_kv_heads > kMaxAttnKvHeads;
@@ -100,7 +100,7 @@ int num_sms_current_device() {
 uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 // The split-K work list. Groups are (sequence, 8-row query tile) over every KV head for the
-// decode kernel, or (sequence, KV-head pair, 64-row tile) for the tile kernel, in that order; each
+// decode kernel, or (sequence, KV head, 128-row tile) for the tile kernel, in that order; each
 // group's visited pages are cut into chunks of chunk_pages, and the chunk stream of all groups is
 // dealt out to `grid` CTAs in contiguous ranges of about total_pages / grid pages each.
 struct PlanBuild {
@@ -122,7 +122,7 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
   const int64_t rows = (int64_t)G * q_len;
   const int64_t tile_rows = tile ? kTileRows : kRowsPerItem;
   const int64_t n_rg = (rows + tile_rows - 1) / tile_rows;
-  const int64_t n_pairs = tile ? (L->num_kv_heads + 1) / 2 : 1;  // groups per (sequence, tile)
+  const int64_t n_pairs = tile ? L->num_kv_heads : 1;  // groups per (sequence, row tile)
   const int32_t chunk_pages = chunk_tokens / P;
   const int64_t n_groups = (int64_t)num_seqs * n_pairs * n_rg;
   if (n_groups > (1 << 26)) return KV_NVFP4_EINVAL;

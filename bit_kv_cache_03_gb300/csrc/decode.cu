@@ -89,7 +89,8 @@ constexpr int kBarQkDone = kBarStageEmpty + kStages;   // [kSBufs]
 constexpr int kBarSFree = kBarQkDone + kSBufs;         // [kSBufs]
 constexpr int kBarQReady = kBarSFree + kSBufs;
 constexpr int kBarKvReady = kBarQReady + 1;  // fused append: the segment's new K/V rows are written
-constexpr int kNumBars = kBarKvReady + 1;
+constexpr int kBarDrain = kBarKvReady + 1;   // every tcgen05 op of the CTA complete
+constexpr int kNumBars = kBarDrain + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 // misc: stage page ids, tmem base
 constexpr int kOffStagePid = kOffMisc;
@@ -875,6 +876,7 @@ __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodePa
     }
     mbar_init(bars + 8 * kBarQReady, kAttnWarps);
     mbar_init(bars + 8 * kBarKvReady, 1);
+    mbar_init(bars + 8 * kBarDrain, 1);
     fence_mbar_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(smem + kOffTmemSlot), kTmemCols);
@@ -895,6 +897,15 @@ __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodePa
     attention_warps<NR, FUSED>(p, smem, tbase, warp, lane);
   }
 
+  if (warp == kWarpMma) {
+    // tensor memory is freed only once no tcgen05 op of this CTA is in flight (after a timeout
+    // some may still be; the wait is bounded like every other)
+    if (lane == 0) mma_commit(bars + 8 * kBarDrain);
+    __syncwarp();
+    bool to = false;
+    wait_bar(bars + 8 * kBarDrain, 0, to);
+    if (to && lane == 0) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

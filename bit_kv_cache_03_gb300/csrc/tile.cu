@@ -6,34 +6,37 @@
 // product. The tile decomposition, the lazily raised running max and the split-K merge are this
 // library's design; the pages say nothing about the kernel's decomposition.
 //
-// Work decomposition. A group is (sequence, KV-head pair, tile of 64 query rows per head), a row
+// Work decomposition. A group is (sequence, KV head, tile of 128 query rows of that head), a row
 // being (query token, head in the GQA group) as in the decode kernel. The plan lays the groups'
 // pages end to end and gives each persistent CTA a contiguous, page-balanced share (segments); a
-// group spread over several CTAs leaves one (m, l, O) partial per segment and head, merged by a
-// second launch.
+// group spread over several CTAs leaves one (m, l, O) partial per segment, merged by a second
+// launch. Keys are taken in blocks of 128 (two pages of the head; the last block of a segment may
+// hold one).
 //
-// Per page (64 keys of the pair's two heads, 18 KB in four bulk copies):
-//   Q.K^T: tcgen05.mma kind::mxf4nvf4 block_scale.scale_vec::4X, M = 128 query rows (64 of head
-//     2p, then 64 of head 2p + 1), N = 128 keys (64 of each head), K = 64 per instruction. The
-//     cross terms (rows of one head against keys of the other) are computed and ignored; in return
-//     the K codes and scales are used exactly as the pool stores them (tensor-core tile order,
-//     scale-copy order) and the K scales go to TMEM with one copy per k-half.
-//   Softmax: four warps, one query row per thread (TMEM lane = row), fp32 online softmax. The
-//     running max m of a row is raised only when a page's max exceeds it by more than 2^8 in the
-//     exp2 domain (then the whole O tile is rescaled in TMEM, all rows at once), so
-//     P = exp2((s - m) c2) <= 2^8 fits f16 and O, l use the same m; the result O / l is unchanged.
-//   V: two warps dequantise the page's V rows (E2M1 x E4M3 is exact in f16), two key rows of one
-//     head per thread, into an MN-major f16 tile.
-//   P.V: tcgen05.mma kind::f16, transposed per head: O^T[dims][rows] += V^T P^T with M = 128 dims
-//     (A = the dequantised V tile), N = 64 rows (B = P, K-major), K = 16 keys per instruction. O^T
-//     stays in TMEM for the whole segment.
-// Two S buffers, two P tiles and three V tiles: the Q.K^T of page j + 2 and the P.V of page j - 1
-// run on the tensor pipe while the softmax of page j runs.
+// Per block (the head's part of two pages, 19 KB in eight bulk copies):
+//   Q.K^T: tcgen05.mma kind::mxf4nvf4 block_scale.scale_vec::4X, M = 128 query rows, N = 128
+//     keys, K = 64 per instruction (two per 128-dim row) into one of two S buffers in tensor
+//     memory. The K codes are used as the pool stores them (tensor-core tile order); the MMA warp
+//     gathers the head's K scales of the two pages into the scale-factor copy's row order.
+//   Softmax: four warps, one query row per thread (tensor-memory lane = row), fp32 online softmax
+//     over the row's 128 scores. The running max m of a row is raised only when a block's max
+//     exceeds it by more than 2^8 in the exp2 domain (the warp then rescales its rows of O in
+//     tensor memory), so P = exp2((s - m) c2) <= 2^8 fits f16. P is written in f16 back into the
+//     S buffer it came from, where the P.V product reads it as its A operand.
+//   V: four warps dequantise the block's V rows (E2M1 x E4M3 is exact in f16), one key row per
+//     thread, into an MN-major f16 tile in shared memory.
+//   P.V: tcgen05.mma kind::f16, O[rows][dims] += P V with M = 128 rows (A = P in tensor memory),
+//     N = 144 (B = the dequantised V tile: the 128 head dims, a column of ones and 15 of zeros),
+//     K = 16 keys per instruction (eight per block). The column of ones makes the tensor core
+//     accumulate each row's sum of P (the softmax denominator l) beside O, in fp32, from the very
+//     f16 P values the product uses; O and l stay in tensor memory for the whole segment.
+// Two S buffers and two V tiles: the Q.K^T and the dequantisation of block j + 1 run while the
+// softmax and the P.V of block j do.
 //
-// Warp roles (256 threads): warp 0 bulk-copy producer, warp 1 MMA issuer and TMEM owner, warps
-// 2..5 softmax and epilogue (TMEM lane quadrants 2, 3, 0, 1), warps 6, 7 V dequantisation. Every
-// wait is an mbarrier wait bounded in time; on a timeout the kernel records KV_NVFP4_DEV_TIMEOUT
-// and carries on, so it cannot hang.
+// Warp roles (320 threads): warp 0 bulk-copy producer, warp 1 MMA issuer and tensor-memory owner,
+// warps 2..5 softmax and epilogue (tensor-memory lane quadrants 2, 3, 0, 1), warps 6..9 V
+// dequantisation. Every wait is an mbarrier wait bounded in time; on a timeout the kernel records
+// KV_NVFP4_DEV_TIMEOUT and carries on, so it cannot hang.
 
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -44,19 +47,21 @@ namespace kvnvfp4 {
 
 namespace {
 
-constexpr int kTRows = 64;                  // query rows per head in a tile
-constexpr int kTStages = 4;
-// one page of a head pair in a stage: K codes (both heads, tile order), K scales (scale-copy
-// order), V codes, V scales
-constexpr int kStK = 0, kStKs = 8192, kStV = 9216, kStVs = 17408;
-constexpr int kTStageBytes = 18432;
-constexpr int kVtHeadBytes = 16384;         // dequantised V of one head: 64 keys x 128 dims, f16
-constexpr int kPHeadBytes = 8192;           // P of one head: 64 rows x 64 keys, f16
-constexpr int kTPartHeadFloats = kTRows * 128 + 2 * kTRows;  // O[64][128], m[64], l[64]
+constexpr int kTRows = 128;                 // query rows of one KV head in a tile
+constexpr int kTStages = 4;                 // key blocks in flight
+// one block in a stage: the head's K codes of both pages (tile order, adjacent so that the 128
+// keys form one B operand), the K scales of the head's pair (or lone head) per page, V codes,
+// V scales
+constexpr int kStK = 0, kStKs = 8192, kStV = 10240, kStVs = 18432;
+constexpr int kTStageBytes = 19456;
+constexpr int kVtCols = 144;                // B operand columns: 128 dims, ones, 15 zeros
+constexpr int kVtGroupBytes = kVtCols * 16; // one 8-key group of the V tile: 18 chunks of 8 x 8
+constexpr int kVtBytes = 16 * kVtGroupBytes;  // dequantised V of a block: 128 keys, f16
+constexpr int kTVtBufs = 2;
+constexpr int kTPartFloats = kTRows * 128 + 2 * kTRows;  // a partial: O[rows][128], m[], l[]
 
 constexpr int kTWarpProducer = 0, kTWarpMma = 1, kTWarpSoft0 = 2, kTWarpDeq0 = 6;
-constexpr int kTDeqWarps = 2;              // on the sub-partitions without the producer / MMA warp
-constexpr int kTVtBufs = 3;                // dequantised V tiles
+constexpr int kTDeqWarps = 4;
 constexpr int kTThreads = (kTWarpDeq0 + kTDeqWarps) * 32;
 constexpr uint32_t kNbSoft = 1;             // named barrier of the four softmax warps
 constexpr float kLazyMax = 8.0f;            // raise the running max only past 2^8 (exp2 domain)
@@ -64,43 +69,40 @@ constexpr float kLazyMax = 8.0f;            // raise the running max only past 2
 // shared memory map
 constexpr int kTOffStage = 0;
 constexpr int kTOffQ = kTOffStage + kTStages * kTStageBytes;  // [128 rows][64 B], tile order
-constexpr int kTOffVt = kTOffQ + 8192;                         // [kTVtBufs][2 heads]
-constexpr int kTOffP = kTOffVt + kTVtBufs * 2 * kVtHeadBytes;  // [2 buffers][2 heads]
-constexpr int kTOffSfw = kTOffP + 2 * 2 * kPHeadBytes;         // lone head's K scales widened
-constexpr int kTOffQsc = kTOffSfw + 2 * 1024;                  // Q scales [128 rows][8]
-constexpr int kTOffAlpha = kTOffQsc + 128 * 8;                 // rescale factors [128 rows]
-constexpr int kTOffMl = kTOffAlpha + 128 * 4;                  // m [128], l [128]
-constexpr int kTOffBars = kTOffMl + 2 * 128 * 4;
+constexpr int kTOffVt = kTOffQ + 8192;                         // [kTVtBufs] V tiles
+constexpr int kTOffSfk = kTOffVt + kTVtBufs * kVtBytes;        // [2 S buffers][2 k-halves][512 B]
+constexpr int kTOffQsc = kTOffSfk + 2 * 1024;                  // Q scales [128 rows][8]
+constexpr int kTOffBars = kTOffQsc + 128 * 8;
 // barrier indices
 constexpr int kTbStageFull = 0;
 constexpr int kTbStageEmpty = kTbStageFull + kTStages;
 constexpr int kTbSFull = kTbStageEmpty + kTStages;  // [2]
-constexpr int kTbSFree = kTbSFull + 2;              // [2]
-constexpr int kTbPFull = kTbSFree + 2;              // [2]
-constexpr int kTbVtFull = kTbPFull + 2;             // [kTVtBufs]
+constexpr int kTbPFull = kTbSFull + 2;              // [2]
+constexpr int kTbPvDone = kTbPFull + 2;             // [2]
+constexpr int kTbVtFull = kTbPvDone + 2;            // [kTVtBufs]
 constexpr int kTbVtFree = kTbVtFull + kTVtBufs;     // [kTVtBufs]
-constexpr int kTbPvDone = kTbVtFree + kTVtBufs;     // [2]
-constexpr int kTbQReady = kTbPvDone + 2;
+constexpr int kTbQReady = kTbVtFree + kTVtBufs;
 constexpr int kTbOFree = kTbQReady + 1;
-constexpr int kTNumBars = kTbOFree + 1;
-constexpr int kTOffPid = kTOffBars + kTNumBars * 8;
-constexpr int kTOffTmemSlot = kTOffPid + 8 * 4;
+constexpr int kTbDrain = kTbOFree + 1;              // every tcgen05 op of the CTA complete
+constexpr int kTNumBars = kTbDrain + 1;
+constexpr int kTOffPid = kTOffBars + kTNumBars * 8;            // [kTStages][2] page ids or -1
+constexpr int kTOffTmemSlot = kTOffPid + kTStages * 2 * 4;
 constexpr int kTSmemBytes = kTOffTmemSlot + 16;
-static_assert(kTStages <= 8, "stage page-id slots");
 static_assert(kTSmemBytes <= 227 * 1024, "shared memory budget");
 
 // TMEM columns
-constexpr uint32_t kTColS = 0;      // [2 buffers][128 keys]
-constexpr uint32_t kTColO = 256;    // O^T: [2 heads][64 rows]
-constexpr uint32_t kTColSfa = 384;  // Q scales: [2 k-halves][4]
-constexpr uint32_t kTColSfb = 392;  // K scales: [2 buffers][2 k-halves][4]
+constexpr uint32_t kTColS = 0;      // [2 buffers][128 keys]; P (f16 pairs) over columns 0..63
+constexpr uint32_t kTColO = 256;    // O: [128 dims], then l, then 15 zero columns
+constexpr uint32_t kTColSfa = 400;  // Q scales: [2 k-halves][4]
+constexpr uint32_t kTColSfb = 408;  // K scales: [2 buffers][2 k-halves][4]
 constexpr uint32_t kTTmemCols = 512;
 
 // instruction descriptors (dense, no negation):
 //   Q.K^T: A, B = E2M1 K-major, scale type UE4M3, N = 128, M = 128
-//   P.V:   D = f32, A = B = f16, A MN-major, B K-major, N = 64, M = 128
-constexpr uint32_t kIdescQKT = (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
-constexpr uint32_t kIdescPVT = (1u << 4) | (1u << 15) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+//   P.V:   D = f32, A = B = f16, A K-major (tensor memory), B MN-major, N = 144, M = 128
+constexpr uint32_t kIdescQK = (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdescPV =
+    (1u << 4) | (1u << 16) | (((uint32_t)kVtCols >> 3) << 17) | ((128u >> 4) << 24);
 
 struct TileParams {
   const uint8_t* q_codes;
@@ -109,10 +111,10 @@ struct TileParams {
   const int32_t* block_table;
   int32_t max_pages;
   int32_t num_pages;
-  const int4* groups;      // 2 x int4 per group: {seq, pair, rg, len}, {n_seg, first_part, pages, 0}
+  const int4* groups;      // 2 x int4 per group: {seq, kv head, rg, len}, {n_seg, first_part, pages, 0}
   const int4* segments;    // {group, page_lo, page_hi, part_slot or -1}
   const int32_t* cta_seg;  // [grid + 1]
-  float* partials;         // [num_partials][2][kTPartHeadFloats]
+  float* partials;         // [num_partials][kTPartFloats]
   float* out;
   int32_t* status;
   int32_t Hq, Hkv, G, q_len, causal;
@@ -120,8 +122,7 @@ struct TileParams {
 };
 
 struct TSeg {
-  int seq, pair, rg, len, n_seg, first_part, lo, hi, part;
-  bool two;  // the pair has both heads (false for the last head of an odd head count)
+  int seq, head, rg, len, n_seg, first_part, lo, hi, part;
 };
 
 __device__ __forceinline__ TSeg t_load_seg(const TileParams& p, int s) {
@@ -130,17 +131,20 @@ __device__ __forceinline__ TSeg t_load_seg(const TileParams& p, int s) {
   const int4 g1 = p.groups[2 * seg.x + 1];
   TSeg r;
   r.lo = seg.y; r.hi = seg.z; r.part = seg.w;
-  r.seq = g0.x; r.pair = g0.y; r.rg = g0.z; r.len = g0.w;
+  r.seq = g0.x; r.head = g0.y; r.rg = g0.z; r.len = g0.w;
   r.n_seg = g1.x; r.first_part = g1.y;
-  r.two = 2 * r.pair + 1 < p.Hkv;
   return r;
 }
 
 __device__ __forceinline__ uint32_t tbar(uint32_t bars, int i) { return bars + 8u * (uint32_t)i; }
 
+// key blocks (two pages each) of a segment
+__device__ __forceinline__ int seg_blocks(const TSeg& sg) { return (sg.hi - sg.lo + 1) >> 1; }
+
 // --------------------------------------------------------------------------------------------
-// Producer warp: lane 0 streams the pair's part of each page (K codes, K scales, V codes, V
-// scales: four bulk copies) into a kTStages ring; the other lanes load page ids 32 at a time.
+// Producer warp: lane 0 streams the head's part of each page (K codes, K scales, V codes, V
+// scales: four bulk copies per page) into the kTStages ring, two pages per stage; the other lanes
+// load page ids 32 at a time.
 // --------------------------------------------------------------------------------------------
 __device__ void t_producer(const TileParams& p, uint8_t* smem, int lane) {
   const uint32_t sbase = smem_u32(smem);
@@ -152,33 +156,45 @@ __device__ void t_producer(const TileParams& p, uint8_t* smem, int lane) {
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
   for (int s = s_begin; s < s_end; ++s) {
     const TSeg sg = t_load_seg(p, s);
-    const uint32_t kb = sg.two ? 8192u : 4096u, sb = sg.two ? 1024u : 512u;
-    const int64_t offK = (int64_t)sg.pair * 8192, offKs = (int64_t)p.Hkv * 4096 + sg.pair * 1024;
-    const int64_t offV = (int64_t)p.Hkv * 4608 + sg.pair * 8192;
-    const int64_t offVs = (int64_t)p.Hkv * 8704 + sg.pair * 1024;
-    for (int p0 = sg.lo; p0 < sg.hi; p0 += 32) {
+    const bool lone = (sg.head | 1) >= p.Hkv;  // the last head of an odd count has no partner
+    const uint32_t ksb = lone ? 512u : 1024u;
+    const int64_t offK = (int64_t)sg.head * 4096;
+    const int64_t offKs = (int64_t)p.Hkv * 4096 + (sg.head >> 1) * 1024;
+    const int64_t offV = (int64_t)p.Hkv * 4608 + sg.head * 4096;
+    const int64_t offVs = (int64_t)p.Hkv * 8704 + sg.head * 512;
+    const uint32_t per_page = 4096u + ksb + 4096u + 512u;
+    for (int p0 = sg.lo; p0 < sg.hi; p0 += 32) {  // 32 pages: a whole number of blocks
       const int n = min(32, sg.hi - p0);
       const int32_t mine =
           (lane < n) ? p.block_table[(int64_t)sg.seq * p.max_pages + p0 + lane] : -1;
-      for (int j = 0; j < n; ++j, ++k) {
-        const int32_t pid = __shfl_sync(0xffffffffu, mine, j);
+      for (int j = 0; j < n; j += 2, ++k) {
+        const int32_t pid0 = __shfl_sync(0xffffffffu, mine, j);
+        const int32_t pid1 = __shfl_sync(0xffffffffu, mine, min(j + 1, 31));
         if (lane == 0) {
           const uint32_t st = k % kTStages;
           if (k >= kTStages)
             wait_bar(tbar(bars, kTbStageEmpty + st), ((k / kTStages) - 1) & 1, to);
-          const bool valid = pid >= 0 && pid < p.num_pages;
-          stage_pid[st] = valid ? pid : -1;
+          const bool has1 = j + 1 < n;
+          const bool v0 = pid0 >= 0 && pid0 < p.num_pages;
+          const bool v1 = has1 && pid1 >= 0 && pid1 < p.num_pages;
+          if (!v0 || (has1 && !v1)) flag_status(p.status, KV_NVFP4_DEV_BAD_PAGE);  // skipped
+          stage_pid[2 * st] = v0 ? pid0 : -1;
+          stage_pid[2 * st + 1] = v1 ? pid1 : -1;
           const uint32_t full = tbar(bars, kTbStageFull + st);
-          if (valid) {
-            const uint8_t* src = p.pool + (int64_t)pid * blk;
+          const uint32_t bytes = (v0 ? per_page : 0u) + (v1 ? per_page : 0u);
+          if (bytes > 0u) {
+            mbar_arrive_expect_tx(full, bytes);
             const uint32_t dst = sbase + kTOffStage + st * kTStageBytes;
-            mbar_arrive_expect_tx(full, 2u * (kb + sb));
-            bulk_g2s(dst + kStK, src + offK, kb, full);
-            bulk_g2s(dst + kStKs, src + offKs, sb, full);
-            bulk_g2s(dst + kStV, src + offV, kb, full);
-            bulk_g2s(dst + kStVs, src + offVs, sb, full);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              if (!(q == 0 ? v0 : v1)) continue;
+              const uint8_t* src = p.pool + (int64_t)(q == 0 ? pid0 : pid1) * blk;
+              bulk_g2s(dst + kStK + q * 4096, src + offK, 4096u, full);
+              bulk_g2s(dst + kStKs + q * 1024, src + offKs, ksb, full);
+              bulk_g2s(dst + kStV + q * 4096, src + offV, 4096u, full);
+              bulk_g2s(dst + kStVs + q * 512, src + offVs, 512u, full);
+            }
           } else {
-            flag_status(p.status, KV_NVFP4_DEV_BAD_PAGE);  // the page is skipped (P = 0, V = 0)
             mbar_arrive(full);
           }
         }
@@ -197,76 +213,64 @@ __device__ void t_producer(const TileParams& p, uint8_t* smem, int lane) {
 }
 
 // --------------------------------------------------------------------------------------------
-// MMA warp. A tcgen05 instruction takes this warp tens of cycles to issue, so the Q.K^T of a page
-// is issued two pages ahead of its softmax: per segment, Q.K^T of its first two pages, then for
-// each page k the Q.K^T of page k + 2 (into the S buffer whose scores the softmax of page k has
-// read, first thing) followed by the P.V of page k (it waits for that page's P and V tiles). A segment's first P.V
-// overwrites O^T; it waits until the previous segment's epilogue has read O^T. The shared-memory
-// descriptors are built once and advanced by adding the byte offset / 16 to the address field.
+// MMA warp. Per segment: the Q.K^T of its first two blocks, then per block j the P.V of block j
+// (it waits for that block's P and V tiles) and, once that P.V has completed (its P lives in the
+// S buffer), the Q.K^T of block j + 2 into the same buffer. A segment's first P.V overwrites O; it
+// waits until the previous segment's epilogue has read O.
 // --------------------------------------------------------------------------------------------
-struct MmaDescs {
-  uint64_t q, k, vt, p, sfk, sfw;  // descriptors of offset 0 of each region
-};
-
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
   return d + (uint64_t)(bytes >> 4);  // start-address field: addresses stay below 2^18
 }
 
-// Q.K^T of page kq: K scales to TMEM, two MMAs (k-halves) into S buffer kq % 2.
-__device__ __forceinline__ void t_issue_qk(const MmaDescs& D, uint32_t sbase, uint32_t bars,
-                                           uint32_t tbase, uint32_t kq, bool two, int lane,
-                                           bool& to) {
-  const uint32_t st = kq % kTStages, b = kq & 1u;
-  wait_bar(tbar(bars, kTbStageFull + st), (kq / kTStages) & 1, to);
-  // S buffer b free: the softmax warps have read S of page kq - 2
-  if (kq >= 2) wait_bar(tbar(bars, kTbSFree + b), ((kq >> 1) - 1) & 1, to);
-  const uint32_t soff = kTOffStage + st * kTStageBytes;
-  if (!two) {  // a lone head's 8-byte scale rows widened to 16 (the absent head's half 0)
-    const uint32_t sfw = sbase + kTOffSfw + b * 1024;
+// Q.K^T of block kb (this warp's lanes first gather the head's K scales of the block's two pages
+// into the scale-factor copy's rows: row r = page 0's keys r and r + 32, then page 1's, per
+// k-half; the scale-factor and the key index of the B operand are then 64 page + key).
+__device__ __forceinline__ void t_issue_qk(uint64_t dq, uint64_t dk, uint64_t dsf, uint32_t sbase,
+                                           uint32_t bars, uint32_t tbase, uint32_t kb, int head,
+                                           bool lone, int lane, bool& to) {
+  const uint32_t st = kb % kTStages, b = kb & 1u;
+  wait_bar(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
+  const uint32_t stage = sbase + kTOffStage + st * kTStageBytes;
+  const uint32_t sfk = sbase + kTOffSfk + b * 1024;
 #pragma unroll
-    for (int kh = 0; kh < 2; ++kh) {
-      const uint2 v = lds64(sbase + soff + kStKs + kh * 256 + lane * 8);
-      sts128(sfw + kh * 512 + lane * 16, v.x, v.y, 0u, 0u);
-    }
-    fence_async_smem();
+  for (int kh = 0; kh < 2; ++kh) {
+    uint2 v[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)  // a missing second page leaves stale scales: its keys are masked
+      v[q] = lone ? lds64(stage + kStKs + q * 1024 + kh * 256 + lane * 8)
+                  : lds64(stage + kStKs + q * 1024 + kh * 512 + lane * 16 + (head & 1) * 8);
+    sts128(sfk + kh * 512 + lane * 16, v[0].x, v[0].y, v[1].x, v[1].y);
   }
+  fence_async_smem();
   __syncwarp();
   if (lane == 0) {
     tc_fence_after();
-    const uint64_t sf = two ? desc_add(D.sfk, soff) : desc_add(D.sfw, b * 1024);
-    tmem_cp_32x128b_x4(tbase + kTColSfb + b * 8, sf);
-    tmem_cp_32x128b_x4(tbase + kTColSfb + b * 8 + 4, desc_add(sf, 512));
-    const uint64_t kd = desc_add(D.k, soff);
-    mma_nvf4_ss(tbase + kTColS + b * 128, D.q, kd, kIdescQKT, tbase + kTColSfa,
+    tmem_cp_32x128b_x4(tbase + kTColSfb + b * 8, desc_add(dsf, b * 1024));
+    tmem_cp_32x128b_x4(tbase + kTColSfb + b * 8 + 4, desc_add(dsf, b * 1024 + 512));
+    const uint64_t kd = desc_add(dk, kTOffStage + st * kTStageBytes);
+    mma_nvf4_ss(tbase + kTColS + b * 128, dq, kd, kIdescQK, tbase + kTColSfa,
                 tbase + kTColSfb + b * 8, 0u);
-    mma_nvf4_ss(tbase + kTColS + b * 128, desc_add(D.q, 256), desc_add(kd, 256), kIdescQKT,
+    mma_nvf4_ss(tbase + kTColS + b * 128, desc_add(dq, 256), desc_add(kd, 256), kIdescQK,
                 tbase + kTColSfa + 4, tbase + kTColSfb + b * 8 + 4, 1u);
-    // (the stage's K is released by the softmax warps, which arrive on its empty barrier after
-    // S is complete)
     mma_commit(tbar(bars, kTbSFull + b));
+    mma_commit(tbar(bars, kTbStageEmpty + st));  // K codes and scales consumed
   }
   __syncwarp();
 }
 
-// P.V of page kk: per head, four MMAs (16 keys each) into O^T.
-__device__ __forceinline__ void t_issue_pv(const MmaDescs& D, uint32_t bars, uint32_t tbase,
-                                           uint32_t kk, bool first, bool two, int lane,
-                                           bool& to) {
-  const uint32_t b = kk & 1u, v = kk % kTVtBufs;
-  wait_bar(tbar(bars, kTbPFull + b), (kk >> 1) & 1, to);
-  wait_bar(tbar(bars, kTbVtFull + v), (kk / kTVtBufs) & 1, to);
+// P.V of block kb: eight MMAs (16 keys each) into O, A = P in the S buffer.
+__device__ __forceinline__ void t_issue_pv(uint64_t dv, uint32_t bars, uint32_t tbase, uint32_t kb,
+                                           bool first, int lane, bool& to) {
+  const uint32_t b = kb & 1u, v = kb % kTVtBufs;
+  wait_bar(tbar(bars, kTbPFull + b), (kb >> 1) & 1, to);
+  wait_bar(tbar(bars, kTbVtFull + v), (kb / kTVtBufs) & 1, to);
   if (lane == 0) {
     tc_fence_after();
+    const uint64_t bd = desc_add(dv, v * kVtBytes);
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      if (hh == 1 && !two) break;
-      const uint64_t ad = desc_add(D.vt, (v * 2 + hh) * kVtHeadBytes);
-      const uint64_t bd = desc_add(D.p, (b * 2 + hh) * kPHeadBytes);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)  // 16 keys per instruction
-        mma_f16_ss(tbase + kTColO + hh * 64, desc_add(ad, ks * 4096), desc_add(bd, ks * 256),
-                   kIdescPVT, (first && ks == 0) ? 0u : 1u);
-    }
+    for (int ks = 0; ks < 8; ++ks)  // P: two f16 keys per column, 8 columns per 16 keys
+      mma_f16_ts(tbase + kTColO, tbase + kTColS + b * 128 + ks * 8,
+                 desc_add(bd, ks * 2 * kVtGroupBytes), kIdescPV, (first && ks == 0) ? 0u : 1u);
     mma_commit(tbar(bars, kTbPvDone + b));
     mma_commit(tbar(bars, kTbVtFree + v));
   }
@@ -276,105 +280,101 @@ __device__ __forceinline__ void t_issue_pv(const MmaDescs& D, uint32_t bars, uin
 __device__ void t_mma(const TileParams& p, uint8_t* smem, uint32_t tbase, int lane) {
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kTOffBars;
-  MmaDescs D;
-  D.q = smem_desc(sbase + kTOffQ, 128, 512);
-  D.k = smem_desc(sbase + kStK, 128, 512);          // + stage offset
-  D.sfk = smem_desc(sbase + kStKs, 16, 128);        // + stage offset
-  D.sfw = smem_desc(sbase + kTOffSfw, 16, 128);
-  D.vt = smem_desc(sbase + kTOffVt, 2048, 128);
-  D.p = smem_desc(sbase + kTOffP, 128, 1024);
-  uint32_t k = 0, sgi = 0;
+  const uint64_t dq = smem_desc(sbase + kTOffQ, 128, 512);
+  const uint64_t dk = smem_desc(sbase + kStK, 128, 512);   // + stage offset
+  const uint64_t dsf = smem_desc(sbase + kTOffSfk, 16, 128);
+  const uint64_t dv = smem_desc(sbase + kTOffVt, kVtGroupBytes, 128);
+  uint32_t kb = 0, sgi = 0;
   bool to = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
   for (int s = s_begin; s < s_end; ++s, ++sgi) {
     const TSeg sg = t_load_seg(p, s);
-    const int n = sg.hi - sg.lo;
+    const int n = seg_blocks(sg);
+    const bool lone = (sg.head | 1) >= p.Hkv;
     wait_bar(tbar(bars, kTbQReady), sgi & 1, to);  // this segment's Q tile and its scales
-    t_issue_qk(D, sbase, bars, tbase, k, sg.two, lane, to);
-    if (n > 1) t_issue_qk(D, sbase, bars, tbase, k + 1, sg.two, lane, to);
-    for (int j = 0; j < n; ++j) {
-      // S buffer of page k + j + 2 is free once the softmax of page k + j has read its scores,
-      // early in that softmax; its P.V waits for the end of it
-      if (j + 2 < n) t_issue_qk(D, sbase, bars, tbase, k + j + 2, sg.two, lane, to);
-      if (j == 0 && sgi > 0) wait_bar(tbar(bars, kTbOFree), (sgi - 1) & 1, to);
-      t_issue_pv(D, bars, tbase, k + j, j == 0, sg.two, lane, to);
+    for (int j = 0; j < 2 && j < n; ++j) {
+      // the S buffer of block kb + j is free once the P.V of block kb + j - 2 (which read its P)
+      // has completed
+      const uint32_t kq = kb + j;
+      if (kq >= 2) wait_bar(tbar(bars, kTbPvDone + (kq & 1u)), ((kq - 2) >> 1) & 1, to);
+      t_issue_qk(dq, dk, dsf, sbase, bars, tbase, kq, sg.head, lone, lane, to);
     }
-    k += n;
+    for (int j = 0; j < n; ++j) {
+      if (j == 0 && sgi > 0) wait_bar(tbar(bars, kTbOFree), (sgi - 1) & 1, to);
+      t_issue_pv(dv, bars, tbase, kb + j, j == 0, lane, to);
+      if (j + 2 < n) {
+        wait_bar(tbar(bars, kTbPvDone + ((kb + j) & 1u)), ((kb + j) >> 1) & 1, to);
+        t_issue_qk(dq, dk, dsf, sbase, bars, tbase, kb + j + 2, sg.head, lone, lane, to);
+      }
+    }
+    kb += n;
+    if (to) break;  // a lost signal: issue nothing more (the drain below still runs)
   }
   if (to) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
 
 // --------------------------------------------------------------------------------------------
-// V dequantisation warps: warp hh converts head hh of the pair, lane l the key rows l and l + 32
-// (64 code bytes and 8 scales each) into 128 f16 values of the MN-major tile (core matrix = 8 keys
-// x 8 dims, dims contiguous); zeros for a key past the sequence end or on a skipped page. The
-// 16-byte loads of a row are rotated by key so that the eight keys of a quarter-warp read distinct
-// banks. The two warps sit on the sub-partitions that hold neither the producer nor the MMA warp.
+// V dequantisation warps: thread t of the four warps converts key t of the block (64 code bytes
+// and 8 scales) into 128 f16 values of the MN-major tile (core matrix = 8 keys x 8 dims, dims
+// contiguous; per 8-key group 16 chunks of dims, then the chunk holding the column of ones and a
+// chunk of zeros, written once at the start); zeros for a key past the sequence end or on a
+// skipped page. The 16-byte loads of a row are rotated by key so that the eight keys of a
+// quarter-warp read distinct banks.
 // --------------------------------------------------------------------------------------------
-// One key row's loads: 64 code bytes (rotated 16-byte pieces) and 8 scales.
-struct VRow {
-  uint4 cw[4];
-  uint2 sc8;
-};
-
-__device__ __forceinline__ void t_vrow_load(uint32_t stage, int hh, int key, VRow& r) {
-  const int rot = (key >> 1) & 3;
-  r.sc8 = lds64(stage + kStVs + hh * 512 + key * 8);
-#pragma unroll
-  for (int qq = 0; qq < 4; ++qq)
-    r.cw[qq] = lds128(stage + kStV + hh * 4096 + key * 64 + 16 * ((qq + rot) & 3));
-}
-
-__device__ __forceinline__ void t_vrow_store(const VRow& r, uint32_t dst_tile, int key, bool ok) {
-  const uint32_t dst = dst_tile + (key >> 3) * 2048 + (key & 7) * 16;
-  const int rot = (key >> 1) & 3;
-#pragma unroll
-  for (int qq = 0; qq < 4; ++qq) {
-    const int q4 = (qq + rot) & 3;  // 16 code bytes = dims 32 q4 .. 32 q4 + 31
-    // scales of blocks 2 q4 (dims 32 q4 ..) and 2 q4 + 1 (dims 32 q4 + 16 ..); 0 past the end
-    const uint32_t two_sc = ok ? ((q4 < 2 ? r.sc8.x : r.sc8.y) >> (16 * (q4 & 1))) & 0xFFFFu : 0u;
-    const uint32_t sh = cvt_e4m3x2_f16(two_sc);
-    const uint32_t s0 = dup_lo(sh), s1 = dup_hi(sh);
-    const uint32_t words[4] = {r.cw[qq].x, r.cw[qq].y, r.cw[qq].z, r.cw[qq].w};
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {  // word w: dims 32 q4 + 8 w .. + 7 (byte = dims 2i, 2i + 1)
-      uint32_t r0, r1, r2, r3;
-      cvt_e2m1x8_f16(words[w], r0, r1, r2, r3);
-      const uint32_t sc = w < 2 ? s0 : s1;
-      sts128(dst + (4 * q4 + w) * 128, hmul2(r0, sc), hmul2(r1, sc), hmul2(r2, sc),
-             hmul2(r3, sc));
-    }
-  }
-}
-
 __device__ void t_dequant(const TileParams& p, uint8_t* smem, int warp, int lane) {
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kTOffBars;
   const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kTOffPid);
-  const int hh = warp - kTWarpDeq0;
-  uint32_t k = 0;
+  const int key = (warp - kTWarpDeq0) * 32 + lane;  // 0..127 within the block
+  const int pg = key >> 6, slot = key & 63;
+  const int rot = (key >> 1) & 3;
+  // this key's row of the two extra chunks in both tiles: dim 128 = 1, dims 129 .. 143 = 0 (the
+  // P.V product then accumulates each row's sum of P in column 128 of O)
+#pragma unroll
+  for (int v = 0; v < kTVtBufs; ++v) {
+    const uint32_t row = sbase + kTOffVt + v * kVtBytes + (key >> 3) * kVtGroupBytes + (key & 7) * 16;
+    sts128(row + 16 * 128, 0x3C00u, 0u, 0u, 0u);  // f16 1.0 in the low half of the first word
+    sts128(row + 17 * 128, 0u, 0u, 0u, 0u);
+  }
+  fence_async_smem();
+  uint32_t kb = 0;
   bool to = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
   for (int s = s_begin; s < s_end; ++s) {
     const TSeg sg = t_load_seg(p, s);
-    const bool head_ok = hh == 0 || sg.two;
-    for (int page = sg.lo; page < sg.hi; ++page, ++k) {
-      const uint32_t st = k % kTStages, v = k % kTVtBufs;
-      wait_bar(tbar(bars, kTbStageFull + st), (k / kTStages) & 1, to);
-      // V tile v free once the P.V of page k - kTVtBufs is complete
-      if (k >= kTVtBufs) wait_bar(tbar(bars, kTbVtFree + v), ((k / kTVtBufs) - 1) & 1, to);
-      if (head_ok) {
-        const bool pvalid = stage_pid[st] >= 0;
-        const uint32_t stage = sbase + kTOffStage + st * kTStageBytes;
-        const uint32_t tile = sbase + kTOffVt + (v * 2 + hh) * kVtHeadBytes;
-        // both rows' loads first, then the conversions (the stores would otherwise order each
-        // load after the previous row piece's stores). A key past the sequence end or on a
-        // skipped page gets scale 0: its stale code bytes turn into zeros.
-        VRow r0, r1;
-        t_vrow_load(stage, hh, lane, r0);
-        t_vrow_load(stage, hh, lane + 32, r1);
-        t_vrow_store(r0, tile, lane, pvalid && page * kPage + lane < sg.len);
-        t_vrow_store(r1, tile, lane + 32, pvalid && page * kPage + lane + 32 < sg.len);
+    const int n = seg_blocks(sg);
+    for (int j = 0; j < n; ++j, ++kb) {
+      const uint32_t st = kb % kTStages, v = kb % kTVtBufs;
+      wait_bar(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
+      // V tile v free once the P.V of block kb - 2 is complete
+      if (kb >= kTVtBufs) wait_bar(tbar(bars, kTbVtFree + v), ((kb / kTVtBufs) - 1) & 1, to);
+      const int page = sg.lo + 2 * j + pg;
+      const bool ok = page < sg.hi && stage_pid[2 * st + pg] >= 0 && page * kPage + slot < sg.len;
+      const uint32_t stage = sbase + kTOffStage + st * kTStageBytes;
+      uint4 cw[4];
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq)
+        cw[qq] = lds128(stage + kStV + pg * 4096 + slot * 64 + 16 * ((qq + rot) & 3));
+      const uint2 sc8 = lds64(stage + kStVs + pg * 512 + slot * 8);
+      const uint32_t dst =
+          sbase + kTOffVt + v * kVtBytes + (key >> 3) * kVtGroupBytes + (key & 7) * 16;
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        const int q4 = (qq + rot) & 3;  // 16 code bytes = dims 32 q4 .. 32 q4 + 31
+        // scales of blocks 2 q4 (dims 32 q4 ..) and 2 q4 + 1 (dims 32 q4 + 16 ..); 0 for a key
+        // with no data (its stale code bytes turn into zeros)
+        const uint32_t two_sc = ok ? ((q4 < 2 ? sc8.x : sc8.y) >> (16 * (q4 & 1))) & 0xFFFFu : 0u;
+        const uint32_t sh = cvt_e4m3x2_f16(two_sc);
+        const uint32_t s0 = dup_lo(sh), s1 = dup_hi(sh);
+        const uint32_t words[4] = {cw[qq].x, cw[qq].y, cw[qq].z, cw[qq].w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {  // word w: dims 32 q4 + 8 w .. + 7 (byte = dims 2i, 2i + 1)
+          uint32_t r0, r1, r2, r3;
+          cvt_e2m1x8_f16(words[w], r0, r1, r2, r3);
+          const uint32_t sc = w < 2 ? s0 : s1;
+          sts128(dst + (4 * q4 + w) * 128, hmul2(r0, sc), hmul2(r1, sc), hmul2(r2, sc),
+                 hmul2(r3, sc));
+        }
       }
       fence_async_smem();
       __syncwarp();
@@ -388,23 +388,21 @@ __device__ void t_dequant(const TileParams& p, uint8_t* smem, int warp, int lane
 }
 
 // --------------------------------------------------------------------------------------------
-// Softmax warps. Thread (quadrant q, lane) owns tile row r = 32 q + lane (TMEM lane r of S): head
-// 2 pair + r / 64, tile row r % 64; in the epilogue and the O rescale the same thread owns head
-// dimension r (TMEM lane r of O^T).
+// Softmax warps. Thread (quadrant q, lane) owns tile row r = 32 q + lane (tensor-memory lane r of
+// S and O).
 // --------------------------------------------------------------------------------------------
-// The segment's Q tile: codes into the A operand tile (tile order), scales into TMEM in the
-// replicated scale-factor layout (lane i, column w of a k-half: scales of rows 32 w + i).
+// The segment's Q tile: codes into the A operand tile (tile order), scales into tensor memory in
+// the replicated scale-factor layout (lane i, column w of a k-half: scales of rows 32 w + i).
 __device__ __forceinline__ void t_load_q(const TileParams& p, const TSeg& sg, uint8_t* smem,
                                          uint32_t sbase, uint32_t tbase, uint32_t lane_base, int r,
                                          int lane) {
-  const int hh = r >> 6, i = r & 63;
-  const int head = 2 * sg.pair + hh, gr = sg.rg * kTRows + i;
+  const int gr = sg.rg * kTRows + r;
   uint4 c[4];
   uint2 sc = make_uint2(0u, 0u);
 #pragma unroll
   for (int ch = 0; ch < 4; ++ch) c[ch] = make_uint4(0u, 0u, 0u, 0u);
-  if (head < p.Hkv && gr < p.G * p.q_len) {
-    const int64_t qrow = ((int64_t)sg.seq * p.q_len + gr / p.G) * p.Hq + head * p.G + gr % p.G;
+  if (gr < p.G * p.q_len) {
+    const int64_t qrow = ((int64_t)sg.seq * p.q_len + gr / p.G) * p.Hq + sg.head * p.G + gr % p.G;
     const uint4* src = reinterpret_cast<const uint4*>(p.q_codes + qrow * kCodeBytes);
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch) c[ch] = src[ch];
@@ -427,7 +425,19 @@ __device__ __forceinline__ void t_load_q(const TileParams& p, const TSeg& sg, ui
   tmem_wait_st();
   fence_async_smem();
   tc_fence_before();
-  __syncwarp();
+  named_barrier_sync(kNbSoft, 128);  // the staging rows are read before the next tile rewrites them
+}
+
+// 32 consecutive tensor-memory columns of this warp's lanes.
+__device__ __forceinline__ void ld32_at(uint32_t taddr, uint32_t* dst) {
+  tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(dst));
+}
+
+// max(a, b, c)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, int warp,
@@ -435,15 +445,13 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kTOffBars;
   const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kTOffPid);
-  float* alpha_s = reinterpret_cast<float*>(smem + kTOffAlpha);
-  float* ml_s = reinterpret_cast<float*>(smem + kTOffMl);
   const int q = warp & 3;
   const int r = 32 * q + lane;
-  const int hh = r >> 6, i = r & 63;
   const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+  const uint32_t ocol = tbase + lane_base + kTColO;
   const float c2 = p.c2;
   const int rows_total = p.G * p.q_len;
-  uint32_t k = 0, sgi = 0;
+  uint32_t kb = 0, sgi = 0;
   bool to = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
   if (s_begin < s_end) {
@@ -452,109 +460,108 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
   }
   for (int s = s_begin; s < s_end; ++s, ++sgi) {
     const TSeg sg = t_load_seg(p, s);
-    const int n = sg.hi - sg.lo;
-    const int head = 2 * sg.pair + hh, gr = sg.rg * kTRows + i;
-    const bool row_ok = head < p.Hkv && gr < rows_total;
+    const int n = seg_blocks(sg);
+    const int gr = sg.rg * kTRows + r;
+    const bool row_ok = gr < rows_total;
+    // a warp whose 32 rows are all padding computes nothing (it still takes part in every
+    // barrier); its rows of P and O are never read into a result
+    const bool warp_live = sg.rg * kTRows + 32 * q < rows_total;
     // largest visible key position of this row (-1: no key)
     const int limit = row_ok ? (p.causal ? sg.len - p.q_len + gr / p.G : sg.len - 1) : -1;
-    float m = -INFINITY, l = 0.f;
-    for (int j = 0; j < n; ++j, ++k) {
-      const uint32_t b = k & 1u, st = k % kTStages;
-      wait_bar(tbar(bars, kTbSFull + b), (k >> 1) & 1, to);
+    float m = -INFINITY;
+    for (int j = 0; j < n; ++j, ++kb) {
+      const uint32_t b = kb & 1u, st = kb % kTStages;
+      wait_bar(tbar(bars, kTbSFull + b), (kb >> 1) & 1, to);
       tc_fence_after();
-      uint32_t s_lo[32], s_hi[32];  // scores of keys 0..31, 32..63 of this row's head
-      {
-        const uint32_t col = tbase + lane_base + kTColS + b * 128 + hh * 64;
-        tmem_ld32(col, s_lo);
-        tmem_ld32(col + 32, s_hi);
-        tmem_wait_ld_regs32(s_lo);
-        tmem_wait_ld_regs32(s_hi);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tbar(bars, kTbSFree + b));
-      // the page id, published before the stage's full barrier completed; S complete means the
-      // Q.K^T MMAs have read the stage's K, which this warp's arrival releases with the page id
-      wait_bar(tbar(bars, kTbStageFull + st), (k / kTStages) & 1, to);
-      const bool pvalid = stage_pid[st] >= 0;
+      // page ids of the block, published before its stage's full barrier completed
+      wait_bar(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
+      const int page0 = sg.lo + 2 * j;
+      const bool v0 = stage_pid[2 * st] >= 0;
+      const bool v1 = page0 + 1 < sg.hi && stage_pid[2 * st + 1] >= 0;
       __syncwarp();
       if (lane == 0) mbar_arrive(tbar(bars, kTbStageEmpty + st));
-      const int kp0 = (sg.lo + j) * kPage;
-      const int nvis = pvalid ? max(0, min(kPage, limit - kp0 + 1)) : 0;  // keys c < nvis visible
-      const bool full = nvis == kPage;
-      // page max of the row: eight independent chains, then a tree
-      float mx[8];
+      if (warp_live) {
+        const uint32_t scol = tbase + lane_base + kTColS + b * 128;
+        const int kp0 = page0 * kPage;
+        // keys c < n0 of page 0 and 64 <= c < 64 + n1 of page 1 are visible to this row
+        const int n0 = v0 ? max(0, min(kPage, limit - kp0 + 1)) : 0;
+        const int n1 = v1 ? max(0, min(kPage, limit - kp0 - kPage + 1)) : 0;
+        uint32_t sv[128];
+        ld32_at(scol, &sv[0]);
+        ld32_at(scol + 32, &sv[32]);
+        ld32_at(scol + 64, &sv[64]);
+        ld32_at(scol + 96, &sv[96]);
+        tmem_wait_ld_regs32(*reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_wait_ld_regs32(*reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_wait_ld_regs32(*reinterpret_cast<uint32_t(*)[32]>(&sv[64]));
+        tmem_wait_ld_regs32(*reinterpret_cast<uint32_t(*)[32]>(&sv[96]));
+        if (__any_sync(0xffffffffu, n0 != kPage || n1 != kPage)) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
-      if (full) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(s_lo[c]));
-          mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(s_hi[c]));
+          for (int c = 0; c < 128; ++c) {
+            const bool vis = c < 64 ? c < n0 : c - 64 < n1;
+            sv[c] = vis ? sv[c] : __float_as_uint(-INFINITY);
+          }
         }
-      } else {
+        // block max of the row: eight independent chains of three-input maxima, then a tree
+        float mx[8];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          mx[c & 7] = fmaxf(mx[c & 7], c < nvis ? __uint_as_float(s_lo[c]) : -INFINITY);
-          mx[c & 7] = fmaxf(mx[c & 7], c + 32 < nvis ? __uint_as_float(s_hi[c]) : -INFINITY);
-        }
-      }
-      const float pmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float mc = fmaxf(m, pmax);
-      if (j == 0) {
-        m = mc;  // nothing accumulated yet in this segment
-      } else {
-        const bool need = mc > m && (m == -INFINITY || (mc - m) * c2 > kLazyMax);
-        if (named_barrier_any(kNbSoft, 128, need)) {
-          // all P.V MMAs so far complete before O^T is rescaled
-          wait_bar(tbar(bars, kTbPvDone + ((k - 1) & 1u)), ((k - 1) >> 1) & 1, to);
-          tc_fence_after();
-          const float alpha = (mc == m) ? 1.f : fast_exp2((m - mc) * c2);  // 0 when m was -inf
-          l *= alpha;
+        for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sv[e]);
+#pragma unroll
+        for (int c = 8; c < 120; c += 16)
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            mx[e] = fmax3(mx[e], __uint_as_float(sv[c + e]), __uint_as_float(sv[c + 8 + e]));
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], __uint_as_float(sv[120 + e]));
+        const float pmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                 fmaxf(mx[6], mx[7]));
+        const float mc = fmaxf(m, pmax);
+        float alpha = 1.f;
+        bool need = false;
+        if (j == 0) {
+          m = mc;  // nothing accumulated yet in this segment
+        } else if (mc > m && (m == -INFINITY || (mc - m) * c2 > kLazyMax)) {
+          need = true;
+          alpha = m == -INFINITY ? 0.f : fast_exp2((m - mc) * c2);
           m = mc;
-          alpha_s[r] = alpha;
-          named_barrier_sync(kNbSoft, 128);
+        }
+        // rows whose max was raised: their row of O (and l beside it) is rescaled once the
+        // previous block's P.V has completed; the loads and stores are warp-wide
+        if (__any_sync(0xffffffffu, need)) {
+          wait_bar(tbar(bars, kTbPvDone + ((kb - 1) & 1u)), ((kb - 1) >> 1) & 1, to);
+          tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < (sg.two ? 4 : 2); ++cc) {  // O^T columns 32 cc .. (rows of the tile)
+          for (int cc = 0; cc < 4; ++cc) {
             uint32_t o[32];
-            const uint32_t col = tbase + lane_base + kTColO + cc * 32;
-            tmem_ld32(col, o);
+            tmem_ld32(ocol + 32 * cc, o);
             tmem_wait_ld_regs32(o);
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              const float4 a = *reinterpret_cast<const float4*>(alpha_s + cc * 32 + e);
-              o[e] = __float_as_uint(__uint_as_float(o[e]) * a.x);
-              o[e + 1] = __float_as_uint(__uint_as_float(o[e + 1]) * a.y);
-              o[e + 2] = __float_as_uint(__uint_as_float(o[e + 2]) * a.z);
-              o[e + 3] = __float_as_uint(__uint_as_float(o[e + 3]) * a.w);
-            }
-            tmem_st32(col, o);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(ocol + 32 * cc, o);
           }
+          uint32_t o8[8];
+          tmem_ld8(ocol + 128, o8);
+          tmem_wait_ld_regs(o8);
+          o8[0] = __float_as_uint(__uint_as_float(o8[0]) * alpha);  // l
+          tmem_st8(ocol + 128, o8);
           tmem_wait_st();
         }
-      }
-      // P tile b free once the P.V of page k - 2 is complete
-      if (k >= 2) wait_bar(tbar(bars, kTbPvDone + b), ((k >> 1) - 1) & 1, to);
-      const float mc2 = m * c2;
-      const uint32_t prow = sbase + kTOffP + (b * 2 + hh) * kPHeadBytes + (i >> 3) * 1024 + (i & 7) * 16;
-      float ls[8];  // row-sum partials, one per 8 keys
+        // P = exp2(s c2 - m c2) <= 2^8 in f16 pairs over the first 64 columns of the S buffer; a
+        // masked key (-inf) gives 0, also while m is still -inf (then the offset is taken as 0)
+        const float mc2 = m == -INFINITY ? 0.f : m * c2;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        float pv[8];
+        for (int hf = 0; hf < 2; ++hf) {  // keys 64 hf .. 64 hf + 63 -> columns 32 hf .. + 31
+          uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int c = 8 * c8 + e;
-          const float x = __uint_as_float(c < 32 ? s_lo[c & 31] : s_hi[c & 31]);
-          const float pe = fast_exp2(fmaf(x, c2, -mc2));
-          pv[e] = (full || c < nvis) ? pe : 0.f;
+          for (int c = 0; c < 64; c += 2) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sv[64 * hf + c]), c2, -mc2));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sv[64 * hf + c + 1]), c2, -mc2));
+            pk[c >> 1] = pack_f16x2(p0, p1);
+          }
+          tmem_st32(scol + 32 * hf, pk);
         }
-        ls[c8] = ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
-        sts128(prow + c8 * 128, pack_f16x2(pv[0], pv[1]), pack_f16x2(pv[2], pv[3]),
-               pack_f16x2(pv[4], pv[5]), pack_f16x2(pv[6], pv[7]));
+        tmem_wait_st();
       }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-      fence_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tbar(bars, kTbPFull + b));
@@ -566,41 +573,45 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
       t_load_q(p, t_load_seg(p, s + 1), smem, sbase, tbase, lane_base, r, lane);
       if (lane == 0) mbar_arrive(tbar(bars, kTbQReady));
     }
-    const uint32_t kl = k - 1;
+    const uint32_t kl = kb - 1;
     wait_bar(tbar(bars, kTbPvDone + (kl & 1u)), (kl >> 1) & 1, to);
     tc_fence_after();
-    named_barrier_sync(kNbSoft, 128);  // the previous epilogue's reads of m, l are done
-    ml_s[r] = m;
-    ml_s[128 + r] = l;
-    named_barrier_sync(kNbSoft, 128);
     const bool split = sg.n_seg > 1;
-    const int d = r;  // this thread's head dimension in O^T
-    float* part = split ? p.partials + (int64_t)sg.part * 2 * kTPartHeadFloats : nullptr;
+    if (warp_live) {
+      uint32_t o8[8];
+      tmem_ld8(ocol + 128, o8);
+      tmem_wait_ld_regs(o8);
+      const float l = __uint_as_float(o8[0]);  // the row's sum of P, accumulated by the P.V MMAs
+      float* part = split ? p.partials + (int64_t)sg.part * kTPartFloats : nullptr;
+      const int tok = gr / p.G, qh = sg.head * p.G + gr % p.G;
+      float* orow = p.out + (((int64_t)sg.seq * p.q_len + tok) * p.Hq + qh) * 128;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-    for (int cc = 0; cc < (sg.two ? 4 : 2); ++cc) {
-      uint32_t o[32];
-      tmem_ld32(tbase + lane_base + kTColO + cc * 32, o);
-      tmem_wait_ld_regs32(o);
-      const int h2 = cc >> 1;
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(ocol + 32 * cc, o);
+        tmem_wait_ld_regs32(o);
+        if (row_ok) {
+          if (split) {
+            float4* dst = reinterpret_cast<float4*>(part + r * 128 + 32 * cc);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int i2 = (cc & 1) * 32 + e, g2 = sg.rg * kTRows + i2;
-        if (g2 >= rows_total) continue;
-        const float v = __uint_as_float(o[e]);
-        if (split) {
-          part[h2 * kTPartHeadFloats + i2 * 128 + d] = v;
-        } else {
-          const float l2 = ml_s[128 + h2 * 64 + i2];
-          if (l2 > 0.f) {
-            const int tok = g2 / p.G, qh = (2 * sg.pair + h2) * p.G + g2 % p.G;
-            p.out[(((int64_t)sg.seq * p.q_len + tok) * p.Hq + qh) * 128 + d] = v / l2;
+            for (int e = 0; e < 32; e += 4)
+              dst[e >> 2] = make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                                        __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+          } else if (l > 0.f) {
+            float4* dst = reinterpret_cast<float4*>(orow + 32 * cc);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              dst[e >> 2] = make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
+                                        __uint_as_float(o[e + 2]) * inv,
+                                        __uint_as_float(o[e + 3]) * inv);
           }
         }
       }
-    }
-    if (split && row_ok) {
-      part[hh * kTPartHeadFloats + kTRows * 128 + i] = m;
-      part[hh * kTPartHeadFloats + kTRows * 128 + kTRows + i] = l;
+      if (row_ok && split) {
+        part[kTRows * 128 + r] = m;
+        part[kTRows * 128 + kTRows + r] = l;
+      }
     }
     tc_fence_before();
     __syncwarp();
@@ -619,12 +630,11 @@ __global__ void __launch_bounds__(kTThreads, 1) tile_kernel(const TileParams p) 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTStages; ++s) {
       mbar_init(tbar(bars, kTbStageFull + s), 1);
-      // dequant warps (V read), softmax warps (S complete, so K read; page id read)
-      mbar_init(tbar(bars, kTbStageEmpty + s), kTDeqWarps + 4);
+      // Q.K^T commit (K read), dequant warps (V read), softmax warps (page ids read)
+      mbar_init(tbar(bars, kTbStageEmpty + s), 1 + kTDeqWarps + 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tbar(bars, kTbSFull + b), 1);
-      mbar_init(tbar(bars, kTbSFree + b), 4);
       mbar_init(tbar(bars, kTbPFull + b), 4);
       mbar_init(tbar(bars, kTbPvDone + b), 1);
     }
@@ -634,6 +644,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tile_kernel(const TileParams p) 
     }
     mbar_init(tbar(bars, kTbQReady), 4);
     mbar_init(tbar(bars, kTbOFree), 4);
+    mbar_init(tbar(bars, kTbDrain), 1);
     fence_mbar_init();
   }
   if (warp == kTWarpMma) tmem_alloc(smem_u32(smem + kTOffTmemSlot), kTTmemCols);
@@ -656,6 +667,15 @@ __global__ void __launch_bounds__(kTThreads, 1) tile_kernel(const TileParams p) 
     t_dequant(p, smem, warp, lane);
   }
 
+  if (warp == kTWarpMma) {
+    // tensor memory is freed only once no tcgen05 op of this CTA is in flight (after a timeout
+    // some may still be; the wait is bounded like every other)
+    if (lane == 0) mma_commit(tbar(bars, kTbDrain));
+    __syncwarp();
+    bool to = false;
+    wait_bar(tbar(bars, kTbDrain), 0, to);
+    if (to && lane == 0) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -663,16 +683,16 @@ __global__ void __launch_bounds__(kTThreads, 1) tile_kernel(const TileParams p) 
 }
 
 // --------------------------------------------------------------------------------------------
-// Split-K merge of the tile kernel's partials (second launch): one CTA per (split group, head of
-// the pair, row of the tile); its 256 threads are 8 slices of the group's partials x 32 four-dim
-// columns:  M = max_q m_q,  L = sum_q 2^((m_q - M) c2) l_q,  o = sum_q 2^((m_q - M) c2) O_q / L.
+// Split-K merge of the tile kernel's partials (second launch): one CTA per (split group, row of
+// the tile); its 256 threads are 8 slices of the group's partials x 32 four-dim columns:
+//   M = max_q m_q,  L = sum_q 2^((m_q - M) c2) l_q,  o = sum_q 2^((m_q - M) c2) O_q / L.
 // --------------------------------------------------------------------------------------------
 struct TMergeParams {
   const int4* groups;
   const int32_t* split;    // [num_split] group indices
-  const float* partials;   // [num_partials][2][kTPartHeadFloats]
+  const float* partials;   // [num_partials][kTPartFloats]
   float* out;
-  int32_t Hq, Hkv, G, q_len;
+  int32_t Hq, G, q_len;
   float c2;
 };
 
@@ -681,21 +701,20 @@ __global__ void __launch_bounds__(256) tile_merge_kernel(const TMergeParams p) {
   __shared__ float4 s_o[8][32];
   asm volatile("griddepcontrol.launch_dependents;");
   const int gi = p.split[blockIdx.x];  // plan tables: written before the attention launch
-  const int hh = blockIdx.y / kTRows, i = blockIdx.y % kTRows;
+  const int i = blockIdx.y;
   const int4 g0 = p.groups[2 * gi], g1 = p.groups[2 * gi + 1];
-  const int r = g0.z * kTRows + i, head = 2 * g0.y + hh;
+  const int r = g0.z * kTRows + i, head = g0.y;
   // the partials are visible only after the attention grid has completed and flushed
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (head >= p.Hkv || r >= p.G * p.q_len) return;  // uniform over the CTA
+  if (r >= p.G * p.q_len) return;  // uniform over the CTA
   const int n_seg = g1.x;
   const int slice = threadIdx.x >> 5, d4 = threadIdx.x & 31;
-  const int64_t stride = 2 * (int64_t)kTPartHeadFloats;
-  const float* base = p.partials + (int64_t)g1.y * stride + hh * kTPartHeadFloats;
+  const float* base = p.partials + (int64_t)g1.y * kTPartFloats;
   float M = -INFINITY, L = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
   for (int q = slice; q < n_seg; q += 8) {
-    const float* pq = base + q * stride;
+    const float* pq = base + (int64_t)q * kTPartFloats;
     const float mq = __ldcg(pq + kTRows * 128 + i);
     const float lq = __ldcg(pq + kTRows * 128 + kTRows + i);
     const float4 ov = __ldcg(reinterpret_cast<const float4*>(pq + i * 128) + d4);
@@ -737,8 +756,8 @@ __global__ void __launch_bounds__(256) tile_merge_kernel(const TMergeParams p) {
 
 int tile_smem_bytes() { return kTSmemBytes; }
 
-// Attention for tiles of 64 rows per head of a KV-head pair (see the top of this file), then the
-// merge of the split groups' partials; both launched as programmatic dependents on the stream.
+// Attention for tiles of 128 rows of one KV head (see the top of this file), then the merge of the
+// split groups' partials; both launched as programmatic dependents on the stream.
 cudaError_t launch_tile(const uint8_t* q_codes, const uint8_t* q_scales, const uint8_t* pool,
                         const int32_t* block_table, int32_t max_pages, int32_t num_pages,
                         const void* groups, const void* segments, const int32_t* cta_seg,
@@ -785,9 +804,10 @@ cudaError_t launch_tile(const uint8_t* q_codes, const uint8_t* q_scales, const u
   if (e != cudaSuccess || num_split <= 0) return e;
   TMergeParams mp;
   mp.groups = p.groups; mp.split = split_groups; mp.partials = partials; mp.out = out;
-  mp.Hq = Hq; mp.Hkv = Hkv; mp.G = p.G; mp.q_len = q_len; mp.c2 = p.c2;
+  mp.Hq = Hq; mp.G = p.G; mp.q_len = q_len; mp.c2 = p.c2;
+  const int rows_total = p.G * q_len;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)num_split, 2u * kTRows);
+  cfg.gridDim = dim3((unsigned)num_split, (unsigned)(rows_total < kTRows ? rows_total : kTRows));
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

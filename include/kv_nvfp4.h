@@ -83,9 +83,10 @@ typedef struct kv_nvfp4_layout {
 
 /* Filled by kv_nvfp4_plan; passed unchanged to kv_nvfp4_decode_attn. A row is (query token, head
  * within the GQA group): row = token * group + head_in_group, group * q_len rows per KV head.
- * With at most 8 rows per KV head (decode) a group is one (sequence, tile of 8 rows), covering
- * every KV head; with more (speculative verify, prefill chunks) a group is one (sequence, KV-head
- * pair, tile of 64 rows per head), run by the tile kernel. A group's pages are split into chunks
+ * With at most 8 rows per KV head and at most 4 KV heads (decode) a group is one (sequence, tile
+ * of 8 rows), covering every KV head; otherwise (speculative verify, prefill chunks, wider layouts)
+ * a group is one (sequence, KV head, tile of 128 rows), run by the tile kernel. A group's pages
+ * are split into chunks
  * of chunk_pages pages, and the chunks of all groups are shared out over `grid` CTAs in
  * contiguous, page-balanced ranges (one range may hold several chunks of a group, which the CTA
  * combines as it goes). */
@@ -97,9 +98,8 @@ typedef struct kv_nvfp4_plan_info {
   int32_t chunk_pages;     /* split-K granularity, in pages */
   int32_t num_kv_heads;
   int32_t num_row_groups;  /* row tiles per sequence: ceil(group * q_len / 8), or
-                              ceil(group * q_len / 64) when group * q_len > 8 */
-  int32_t num_groups;      /* num_seqs * num_row_groups, times ceil(num_kv_heads / 2) head
-                              pairs when group * q_len > 8 */
+                              ceil(group * q_len / 128) on the tile kernel */
+  int32_t num_groups;      /* num_seqs * num_row_groups, times num_kv_heads on the tile kernel */
   int32_t num_segments;    /* contiguous (group, page range) pieces over all CTAs */
   int32_t num_partials;    /* partial-result slots (segments of groups split over CTAs) */
   int32_t grid;            /* CTAs of the attention launch, at most the SM count */
@@ -180,7 +180,7 @@ kv_nvfp4_status kv_nvfp4_append(const kv_nvfp4_layout *layout, const void *q, co
  * decode; 64 lets the plan balance the CTAs to the page. The workspace holds the group and
  * segment tables, the list of split groups (those that span more than one CTA), and one
  * (m, l, O) partial per segment of every split group: 4160 bytes per KV head for 8-row tiles,
- * 2 x 33,280 bytes (both heads of the pair) for 64-row tiles. */
+ * 66,560 bytes for the tile kernel's 128-row tiles. */
 kv_nvfp4_status kv_nvfp4_plan_workspace_bytes(const kv_nvfp4_layout *layout,
                                               const int32_t *h_seq_lens, int32_t num_seqs,
                                               int32_t q_len, int32_t causal,
@@ -223,9 +223,10 @@ kv_nvfp4_status kv_nvfp4_plan(const kv_nvfp4_layout *layout, const int32_t *h_se
  * the plan has split groups, the merge of their partials (one CTA per split group, KV head and
  * row). With at most 8 rows per KV head and at most 4 KV heads the attention kernel is the decode
  * kernel (every head of a page staged together; Q.K^T block-scaled on the tensor cores, P.V on the
- * warp-level tensor path); otherwise it is the tile kernel (64 rows of each head of a KV-head pair
- * per tile; Q.K^T block-scaled and P.V in f16, both on the tcgen05 tensor cores, O accumulated in
- * tensor memory), which takes any number of KV heads and any group size. The workspace may be
+ * warp-level tensor path); otherwise it is the tile kernel (128 rows of one KV head per tile, keys
+ * in blocks of 128; Q.K^T block-scaled and P.V in f16 with P in tensor memory, both on the tcgen05
+ * tensor cores, O accumulated in tensor memory), which takes any number of KV heads and any group
+ * size. The workspace may be
  * reused by the next call on the same stream; calls that overlap on one workspace race. */
 kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout *layout,
                                      const kv_nvfp4_plan_info *plan, void *d_workspace,

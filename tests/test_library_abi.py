@@ -118,8 +118,8 @@ def test_plan_covers_every_visible_page_once_and_balances(kv, lens, q_len, causa
     info, groups, segs, cta, split = kv.kv_nvfp4_plan_host(L, lens, q_len, causal, chunk, ctas)
     G = Hq // Hkv
     # at most 8 rows per KV head and at most 4 KV heads: 8-row tiles over every head; otherwise
-    # 64-row tiles per head pair
-    tile_rows, n_pairs = (8, 1) if G * q_len <= 8 and Hkv <= 4 else (64, (Hkv + 1) // 2)
+    # 128-row tiles per KV head
+    tile_rows, n_pairs = (8, 1) if G * q_len <= 8 and Hkv <= 4 else (128, Hkv)
     n_rg = (G * q_len + tile_rows - 1) // tile_rows
     assert info.num_row_groups == n_rg
     assert info.num_groups == len(lens) * n_pairs * n_rg == len(groups)
@@ -167,7 +167,7 @@ def test_plan_covers_every_visible_page_once_and_balances(kv, lens, q_len, causa
     assert info.num_split_groups == len(split)
     assert info.off_split % 16 == 0 and info.off_partials % 16 == 0
     # one (m, l, O) partial per slot: rows x (128 + 2) floats for every KV head the group covers
-    heads = 2 if tile_rows == 64 else Hkv
+    heads = 1 if tile_rows == 128 else Hkv
     part_bytes = heads * tile_rows * 130 * 4
     assert info.workspace_bytes >= info.off_partials + info.num_partials * part_bytes
     assert info.workspace_bytes < info.off_partials + info.num_partials * part_bytes + 256
@@ -221,7 +221,7 @@ def test_noalloc_buffer_size_matches_the_header(kv):
     m = re.search(r"#define KV_NVFP4_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", hdr)
     assert m is not None
     assert int(m.group(1)) << int(m.group(2)) == kv.NOALLOC_SCRATCH_BYTES
-    # on a 152-SM GPU the 64-row-tile plans of the verify shape (4 x 100,008 tokens, 8 new each)
+    # on a 152-SM GPU the tile-kernel plans of the verify shape (4 x 100,008 tokens, 8 new each)
     # and of the 600k prefill chunk fit the buffer
     L = kv.make_layout()
     for lens, q_len in (([100008] * 4, 8), ([600064], 8192)):
