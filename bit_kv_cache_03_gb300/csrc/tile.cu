@@ -17,12 +17,15 @@
 //   Q.K^T: tcgen05.mma kind::mxf4nvf4 block_scale.scale_vec::4X, M = 128 query rows, N = 128
 //     keys, K = 64 per instruction (two per 128-dim row) into one of two S buffers in tensor
 //     memory. The K codes are used as the pool stores them (tensor-core tile order); the MMA warp
-//     gathers the head's K scales of the two pages into the scale-factor copy's row order.
-//   Softmax: four warps, one query row per thread (tensor-memory lane = row), fp32 online softmax
-//     over the row's 128 scores. The running max m of a row is raised only when a block's max
-//     exceeds it by more than 2^8 in the exp2 domain (the warp then rescales its rows of O in
-//     tensor memory), so P = exp2((s - m) c2) <= 2^8 fits f16. P is written in f16 back into the
-//     S buffer it came from, where the P.V product reads it as its A operand.
+//     gathers the head's K scales of the two pages into the scale-factor copy's row order while
+//     the previous block's P.V runs.
+//   Softmax: eight warps, two per tensor-memory lane quadrant: one query row per thread (lane =
+//     row) and 64 of the block's 128 keys per warp, fp32 online softmax. The two warps of a
+//     quadrant exchange their partial row maxima through shared memory. The running max m of a
+//     row is raised only when a block's max exceeds it by more than 2^8 in the exp2 domain (the
+//     warps then rescale their halves of the row of O in tensor memory), so P = exp2((s - m) c2)
+//     <= 2^8 fits f16. Each warp writes its 64 P values in f16 pairs over the first 32 of its own
+//     64 S columns, where the P.V product reads them as its A operand.
 //   V: four warps dequantise the block's V rows (E2M1 x E4M3 is exact in f16), one key row per
 //     thread, into an MN-major f16 tile in shared memory.
 //   P.V: tcgen05.mma kind::f16, O[rows][dims] += P V with M = 128 rows (A = P in tensor memory),
@@ -33,10 +36,17 @@
 // Two S buffers and two V tiles: the Q.K^T and the dequantisation of block j + 1 run while the
 // softmax and the P.V of block j do.
 //
-// Warp roles (320 threads): warp 0 bulk-copy producer, warp 1 MMA issuer and tensor-memory owner,
-// warps 2..5 softmax and epilogue (tensor-memory lane quadrants 2, 3, 0, 1), warps 6..9 V
-// dequantisation. Every wait is an mbarrier wait bounded in time; on a timeout the kernel records
-// KV_NVFP4_DEV_TIMEOUT and carries on, so it cannot hang.
+// Warp roles (448 threads): warp 0 bulk-copy producer, warp 1 MMA issuer and tensor-memory owner,
+// warps 2..9 softmax and epilogue (warp w: lane quadrant w mod 4, key half (w - 2) / 4), warps
+// 10..13 V dequantisation. Every wait is an mbarrier wait bounded in time; on a timeout the kernel
+// records KV_NVFP4_DEV_TIMEOUT and carries on, so it cannot hang.
+//
+// Barriers per block kb (S buffer and V tile b = kb mod 2, stage kb mod 4):
+//   StageFull   producer copies landed            -> MMA warp (K scales), softmax (page ids), V
+//   SFull[b]    Q.K^T complete (commit)           -> softmax
+//   StageEmpty  softmax (after SFull: Q.K^T read the K codes) and V warps done with the stage
+//   PFull[b]    softmax wrote P, V warps wrote V  -> MMA warp issues P.V
+//   PvDone[b]   P.V complete (commit)             -> S buffer b and V tile b free; O readable
 
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -57,31 +67,30 @@ constexpr int kTStageBytes = 19456;
 constexpr int kVtCols = 144;                // B operand columns: 128 dims, ones, 15 zeros
 constexpr int kVtGroupBytes = kVtCols * 16; // one 8-key group of the V tile: 18 chunks of 8 x 8
 constexpr int kVtBytes = 16 * kVtGroupBytes;  // dequantised V of a block: 128 keys, f16
-constexpr int kTVtBufs = 2;
 constexpr int kTPartFloats = kTRows * 128 + 2 * kTRows;  // a partial: O[rows][128], m[], l[]
 
-constexpr int kTWarpProducer = 0, kTWarpMma = 1, kTWarpSoft0 = 2, kTWarpDeq0 = 6;
-constexpr int kTDeqWarps = 4;
+constexpr int kTWarpProducer = 0, kTWarpMma = 1, kTWarpSoft0 = 2, kTSoftWarps = 8;
+constexpr int kTWarpDeq0 = kTWarpSoft0 + kTSoftWarps, kTDeqWarps = 4;
 constexpr int kTThreads = (kTWarpDeq0 + kTDeqWarps) * 32;
-constexpr uint32_t kNbSoft = 1;             // named barrier of the four softmax warps
+constexpr uint32_t kNbQ = 1;                // named barrier: the four softmax warps that load Q
+constexpr uint32_t kNbPair = 2;             // named barriers 2..5: the two warps of a quadrant
 constexpr float kLazyMax = 8.0f;            // raise the running max only past 2^8 (exp2 domain)
 
 // shared memory map
 constexpr int kTOffStage = 0;
 constexpr int kTOffQ = kTOffStage + kTStages * kTStageBytes;  // [128 rows][64 B], tile order
-constexpr int kTOffVt = kTOffQ + 8192;                         // [kTVtBufs] V tiles
-constexpr int kTOffSfk = kTOffVt + kTVtBufs * kVtBytes;        // [2 S buffers][2 k-halves][512 B]
+constexpr int kTOffVt = kTOffQ + 8192;                         // [2] V tiles
+constexpr int kTOffSfk = kTOffVt + 2 * kVtBytes;               // [2 S buffers][2 k-halves][512 B]
 constexpr int kTOffQsc = kTOffSfk + 2 * 1024;                  // Q scales [128 rows][8]
-constexpr int kTOffBars = kTOffQsc + 128 * 8;
+constexpr int kTOffRed = kTOffQsc + 128 * 8;                   // [2 parities][2 halves][128] f32
+constexpr int kTOffBars = kTOffRed + 2 * 2 * 128 * 4;
 // barrier indices
 constexpr int kTbStageFull = 0;
 constexpr int kTbStageEmpty = kTbStageFull + kTStages;
 constexpr int kTbSFull = kTbStageEmpty + kTStages;  // [2]
 constexpr int kTbPFull = kTbSFull + 2;              // [2]
 constexpr int kTbPvDone = kTbPFull + 2;             // [2]
-constexpr int kTbVtFull = kTbPvDone + 2;            // [kTVtBufs]
-constexpr int kTbVtFree = kTbVtFull + kTVtBufs;     // [kTVtBufs]
-constexpr int kTbQReady = kTbVtFree + kTVtBufs;
+constexpr int kTbQReady = kTbPvDone + 2;
 constexpr int kTbOFree = kTbQReady + 1;
 constexpr int kTbDrain = kTbOFree + 1;              // every tcgen05 op of the CTA complete
 constexpr int kTNumBars = kTbDrain + 1;
@@ -91,7 +100,7 @@ constexpr int kTSmemBytes = kTOffTmemSlot + 16;
 static_assert(kTSmemBytes <= 227 * 1024, "shared memory budget");
 
 // TMEM columns
-constexpr uint32_t kTColS = 0;      // [2 buffers][128 keys]; P (f16 pairs) over columns 0..63
+constexpr uint32_t kTColS = 0;      // [2 buffers][128 keys]; P (f16 pairs) at 0..31 and 64..95
 constexpr uint32_t kTColO = 256;    // O: [128 dims], then l, then 15 zero columns
 constexpr uint32_t kTColSfa = 400;  // Q scales: [2 k-halves][4]
 constexpr uint32_t kTColSfb = 408;  // K scales: [2 buffers][2 k-halves][4]
@@ -214,20 +223,21 @@ __device__ void t_producer(const TileParams& p, uint8_t* smem, int lane) {
 
 // --------------------------------------------------------------------------------------------
 // MMA warp. Per segment: the Q.K^T of its first two blocks, then per block j the P.V of block j
-// (it waits for that block's P and V tiles) and, once that P.V has completed (its P lives in the
-// S buffer), the Q.K^T of block j + 2 into the same buffer. A segment's first P.V overwrites O; it
-// waits until the previous segment's epilogue has read O.
+// (once its P and V tile are written), the gathering of block j + 2's K scales while that P.V
+// runs, and, once the P.V has completed (its P lives in the S buffer), the Q.K^T of block j + 2
+// into the same buffer. A segment's first P.V overwrites O; it waits until the previous segment's
+// epilogue has read O.
 // --------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
   return d + (uint64_t)(bytes >> 4);  // start-address field: addresses stay below 2^18
 }
 
-// Q.K^T of block kb (this warp's lanes first gather the head's K scales of the block's two pages
-// into the scale-factor copy's rows: row r = page 0's keys r and r + 32, then page 1's, per
-// k-half; the scale-factor and the key index of the B operand are then 64 page + key).
-__device__ __forceinline__ void t_issue_qk(uint64_t dq, uint64_t dk, uint64_t dsf, uint32_t sbase,
-                                           uint32_t bars, uint32_t tbase, uint32_t kb, int head,
-                                           bool lone, int lane, bool& to) {
+// The head's K scales of block kb's two pages, gathered by the warp's lanes into the
+// scale-factor copy's rows (row r = page 0's keys r and r + 32, then page 1's, per k-half; the
+// scale-factor and the key index of the B operand are then 64 page + key). The previous reader
+// of the buffer, the Q.K^T of block kb - 2, completed before that block's P.V was issued.
+__device__ __forceinline__ void t_gather_kscales(uint32_t sbase, uint32_t bars, uint32_t kb,
+                                                 int head, bool lone, int lane, bool& to) {
   const uint32_t st = kb % kTStages, b = kb & 1u;
   wait_bar(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
   const uint32_t stage = sbase + kTOffStage + st * kTStageBytes;
@@ -243,6 +253,12 @@ __device__ __forceinline__ void t_issue_qk(uint64_t dq, uint64_t dk, uint64_t ds
   }
   fence_async_smem();
   __syncwarp();
+}
+
+// Q.K^T of block kb (its K scales gathered, its S buffer free).
+__device__ __forceinline__ void t_issue_qk(uint64_t dq, uint64_t dk, uint64_t dsf, uint32_t bars,
+                                           uint32_t tbase, uint32_t kb, int lane) {
+  const uint32_t st = kb % kTStages, b = kb & 1u;
   if (lane == 0) {
     tc_fence_after();
     tmem_cp_32x128b_x4(tbase + kTColSfb + b * 8, desc_add(dsf, b * 1024));
@@ -253,26 +269,24 @@ __device__ __forceinline__ void t_issue_qk(uint64_t dq, uint64_t dk, uint64_t ds
     mma_nvf4_ss(tbase + kTColS + b * 128, desc_add(dq, 256), desc_add(kd, 256), kIdescQK,
                 tbase + kTColSfa + 4, tbase + kTColSfb + b * 8 + 4, 1u);
     mma_commit(tbar(bars, kTbSFull + b));
-    mma_commit(tbar(bars, kTbStageEmpty + st));  // K codes and scales consumed
   }
   __syncwarp();
 }
 
-// P.V of block kb: eight MMAs (16 keys each) into O, A = P in the S buffer.
+// P.V of block kb: eight MMAs (16 keys each) into O; A = P in the S buffer (keys 0..63 in
+// columns 0..31, keys 64..127 in columns 64..95).
 __device__ __forceinline__ void t_issue_pv(uint64_t dv, uint32_t bars, uint32_t tbase, uint32_t kb,
                                            bool first, int lane, bool& to) {
-  const uint32_t b = kb & 1u, v = kb % kTVtBufs;
+  const uint32_t b = kb & 1u;
   wait_bar(tbar(bars, kTbPFull + b), (kb >> 1) & 1, to);
-  wait_bar(tbar(bars, kTbVtFull + v), (kb / kTVtBufs) & 1, to);
   if (lane == 0) {
     tc_fence_after();
-    const uint64_t bd = desc_add(dv, v * kVtBytes);
+    const uint64_t bd = desc_add(dv, b * kVtBytes);
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks)  // P: two f16 keys per column, 8 columns per 16 keys
-      mma_f16_ts(tbase + kTColO, tbase + kTColS + b * 128 + ks * 8,
+    for (int ks = 0; ks < 8; ++ks)
+      mma_f16_ts(tbase + kTColO, tbase + kTColS + b * 128 + 64 * (ks >> 2) + 8 * (ks & 3),
                  desc_add(bd, ks * 2 * kVtGroupBytes), kIdescPV, (first && ks == 0) ? 0u : 1u);
     mma_commit(tbar(bars, kTbPvDone + b));
-    mma_commit(tbar(bars, kTbVtFree + v));
   }
   __syncwarp();
 }
@@ -296,15 +310,18 @@ __device__ void t_mma(const TileParams& p, uint8_t* smem, uint32_t tbase, int la
       // the S buffer of block kb + j is free once the P.V of block kb + j - 2 (which read its P)
       // has completed
       const uint32_t kq = kb + j;
+      t_gather_kscales(sbase, bars, kq, sg.head, lone, lane, to);
       if (kq >= 2) wait_bar(tbar(bars, kTbPvDone + (kq & 1u)), ((kq - 2) >> 1) & 1, to);
-      t_issue_qk(dq, dk, dsf, sbase, bars, tbase, kq, sg.head, lone, lane, to);
+      t_issue_qk(dq, dk, dsf, bars, tbase, kq, lane);
     }
     for (int j = 0; j < n; ++j) {
       if (j == 0 && sgi > 0) wait_bar(tbar(bars, kTbOFree), (sgi - 1) & 1, to);
       t_issue_pv(dv, bars, tbase, kb + j, j == 0, lane, to);
       if (j + 2 < n) {
-        wait_bar(tbar(bars, kTbPvDone + ((kb + j) & 1u)), ((kb + j) >> 1) & 1, to);
-        t_issue_qk(dq, dk, dsf, sbase, bars, tbase, kb + j + 2, sg.head, lone, lane, to);
+        const uint32_t kq = kb + j + 2;
+        t_gather_kscales(sbase, bars, kq, sg.head, lone, lane, to);
+        wait_bar(tbar(bars, kTbPvDone + (kq & 1u)), ((kq - 2) >> 1) & 1, to);
+        t_issue_qk(dq, dk, dsf, bars, tbase, kq, lane);
       }
     }
     kb += n;
@@ -331,7 +348,7 @@ __device__ void t_dequant(const TileParams& p, uint8_t* smem, int warp, int lane
   // this key's row of the two extra chunks in both tiles: dim 128 = 1, dims 129 .. 143 = 0 (the
   // P.V product then accumulates each row's sum of P in column 128 of O)
 #pragma unroll
-  for (int v = 0; v < kTVtBufs; ++v) {
+  for (int v = 0; v < 2; ++v) {
     const uint32_t row = sbase + kTOffVt + v * kVtBytes + (key >> 3) * kVtGroupBytes + (key & 7) * 16;
     sts128(row + 16 * 128, 0x3C00u, 0u, 0u, 0u);  // f16 1.0 in the low half of the first word
     sts128(row + 17 * 128, 0u, 0u, 0u, 0u);
@@ -344,10 +361,10 @@ __device__ void t_dequant(const TileParams& p, uint8_t* smem, int warp, int lane
     const TSeg sg = t_load_seg(p, s);
     const int n = seg_blocks(sg);
     for (int j = 0; j < n; ++j, ++kb) {
-      const uint32_t st = kb % kTStages, v = kb % kTVtBufs;
+      const uint32_t st = kb % kTStages, v = kb & 1u;
       wait_bar(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
-      // V tile v free once the P.V of block kb - 2 is complete
-      if (kb >= kTVtBufs) wait_bar(tbar(bars, kTbVtFree + v), ((kb / kTVtBufs) - 1) & 1, to);
+      // V tile v is free once the P.V of block kb - 2 is complete
+      if (kb >= 2) wait_bar(tbar(bars, kTbPvDone + v), ((kb - 2) >> 1) & 1, to);
       const int page = sg.lo + 2 * j + pg;
       const bool ok = page < sg.hi && stage_pid[2 * st + pg] >= 0 && page * kPage + slot < sg.len;
       const uint32_t stage = sbase + kTOffStage + st * kTStageBytes;
@@ -379,7 +396,7 @@ __device__ void t_dequant(const TileParams& p, uint8_t* smem, int warp, int lane
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(tbar(bars, kTbVtFull + v));
+        mbar_arrive(tbar(bars, kTbPFull + v));
         mbar_arrive(tbar(bars, kTbStageEmpty + st));
       }
     }
@@ -389,10 +406,11 @@ __device__ void t_dequant(const TileParams& p, uint8_t* smem, int warp, int lane
 
 // --------------------------------------------------------------------------------------------
 // Softmax warps. Thread (quadrant q, lane) owns tile row r = 32 q + lane (tensor-memory lane r of
-// S and O).
+// S and O); warp half h takes keys 64 h .. 64 h + 63 of each block and dims 64 h .. 64 h + 63 of O.
 // --------------------------------------------------------------------------------------------
-// The segment's Q tile: codes into the A operand tile (tile order), scales into tensor memory in
-// the replicated scale-factor layout (lane i, column w of a k-half: scales of rows 32 w + i).
+// The segment's Q tile (loaded by the four warps of half 0): codes into the A operand tile (tile
+// order), scales into tensor memory in the replicated scale-factor layout (lane i, column w of a
+// k-half: scales of rows 32 w + i).
 __device__ __forceinline__ void t_load_q(const TileParams& p, const TSeg& sg, uint8_t* smem,
                                          uint32_t sbase, uint32_t tbase, uint32_t lane_base, int r,
                                          int lane) {
@@ -413,7 +431,7 @@ __device__ __forceinline__ void t_load_q(const TileParams& p, const TSeg& sg, ui
     sts128(sbase + kTOffQ + (r >> 3) * 512 + ch * 128 + (r & 7) * 16, c[ch].x, c[ch].y, c[ch].z,
            c[ch].w);
   *reinterpret_cast<uint2*>(smem + kTOffQsc + r * 8) = sc;
-  named_barrier_sync(kNbSoft, 128);
+  named_barrier_sync(kNbQ, 128);
   uint32_t sf[8];
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
@@ -425,7 +443,7 @@ __device__ __forceinline__ void t_load_q(const TileParams& p, const TSeg& sg, ui
   tmem_wait_st();
   fence_async_smem();
   tc_fence_before();
-  named_barrier_sync(kNbSoft, 128);  // the staging rows are read before the next tile rewrites them
+  named_barrier_sync(kNbQ, 128);  // the staging rows are read before the next tile rewrites them
 }
 
 // 32 consecutive tensor-memory columns of this warp's lanes.
@@ -440,12 +458,24 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// Multiplies 32 columns of O (this thread's row) by alpha in tensor memory.
+__device__ __forceinline__ void t_scale_o32(uint32_t taddr, float alpha) {
+  uint32_t o[32];
+  tmem_ld32(taddr, o);
+  tmem_wait_ld_regs32(o);
+#pragma unroll
+  for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+  tmem_st32(taddr, o);
+}
+
 __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, int warp,
                           int lane) {
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kTOffBars;
   const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kTOffPid);
+  float* red = reinterpret_cast<float*>(smem + kTOffRed);
   const int q = warp & 3;
+  const int h = (warp - kTWarpSoft0) >> 2;
   const int r = 32 * q + lane;
   const uint32_t lane_base = (uint32_t)(32 * q) << 16;
   const uint32_t ocol = tbase + lane_base + kTColO;
@@ -454,7 +484,7 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
   uint32_t kb = 0, sgi = 0;
   bool to = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
-  if (s_begin < s_end) {
+  if (h == 0 && s_begin < s_end) {
     t_load_q(p, t_load_seg(p, s_begin), smem, sbase, tbase, lane_base, r, lane);
     if (lane == 0) mbar_arrive(tbar(bars, kTbQReady));
   }
@@ -463,58 +493,55 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
     const int n = seg_blocks(sg);
     const int gr = sg.rg * kTRows + r;
     const bool row_ok = gr < rows_total;
-    // a warp whose 32 rows are all padding computes nothing (it still takes part in every
-    // barrier); its rows of P and O are never read into a result
+    // a quadrant whose 32 rows are all padding computes nothing (its two warps still take part
+    // in every mbarrier); its rows of P and O are never read into a result
     const bool warp_live = sg.rg * kTRows + 32 * q < rows_total;
     // largest visible key position of this row (-1: no key)
     const int limit = row_ok ? (p.causal ? sg.len - p.q_len + gr / p.G : sg.len - 1) : -1;
     float m = -INFINITY;
     for (int j = 0; j < n; ++j, ++kb) {
       const uint32_t b = kb & 1u, st = kb % kTStages;
-      wait_bar(tbar(bars, kTbSFull + b), (kb >> 1) & 1, to);
-      tc_fence_after();
       // page ids of the block, published before its stage's full barrier completed
       wait_bar(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
-      const int page0 = sg.lo + 2 * j;
-      const bool v0 = stage_pid[2 * st] >= 0;
-      const bool v1 = page0 + 1 < sg.hi && stage_pid[2 * st + 1] >= 0;
+      const int page = sg.lo + 2 * j + h;
+      const bool valid = page < sg.hi && stage_pid[2 * st + h] >= 0;
+      wait_bar(tbar(bars, kTbSFull + b), (kb >> 1) & 1, to);
+      tc_fence_after();
       __syncwarp();
+      // the Q.K^T (complete) read the stage's K codes; this warp is done with its page ids
       if (lane == 0) mbar_arrive(tbar(bars, kTbStageEmpty + st));
       if (warp_live) {
-        const uint32_t scol = tbase + lane_base + kTColS + b * 128;
-        const int kp0 = page0 * kPage;
-        // keys c < n0 of page 0 and 64 <= c < 64 + n1 of page 1 are visible to this row
-        const int n0 = v0 ? max(0, min(kPage, limit - kp0 + 1)) : 0;
-        const int n1 = v1 ? max(0, min(kPage, limit - kp0 - kPage + 1)) : 0;
-        uint32_t sv[128];
+        const uint32_t scol = tbase + lane_base + kTColS + b * 128 + 64 * h;
+        // keys c < nv of this warp's page are visible to this row
+        const int nv = valid ? max(0, min(kPage, limit - page * kPage + 1)) : 0;
+        uint32_t sv[64];
         ld32_at(scol, &sv[0]);
         ld32_at(scol + 32, &sv[32]);
-        ld32_at(scol + 64, &sv[64]);
-        ld32_at(scol + 96, &sv[96]);
         tmem_wait_ld_regs32(*reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
         tmem_wait_ld_regs32(*reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        tmem_wait_ld_regs32(*reinterpret_cast<uint32_t(*)[32]>(&sv[64]));
-        tmem_wait_ld_regs32(*reinterpret_cast<uint32_t(*)[32]>(&sv[96]));
-        if (__any_sync(0xffffffffu, n0 != kPage || n1 != kPage)) {
+        if (__any_sync(0xffffffffu, nv != kPage)) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const bool vis = c < 64 ? c < n0 : c - 64 < n1;
-            sv[c] = vis ? sv[c] : __float_as_uint(-INFINITY);
-          }
+          for (int c = 0; c < 64; ++c) sv[c] = c < nv ? sv[c] : __float_as_uint(-INFINITY);
         }
-        // block max of the row: eight independent chains of three-input maxima, then a tree
+        // this half's max of the row: eight chains of three-input maxima, then a tree
         float mx[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sv[e]);
 #pragma unroll
-        for (int c = 8; c < 120; c += 16)
+        for (int c = 8; c < 56; c += 16)
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             mx[e] = fmax3(mx[e], __uint_as_float(sv[c + e]), __uint_as_float(sv[c + 8 + e]));
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], __uint_as_float(sv[120 + e]));
-        const float pmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                 fmaxf(mx[6], mx[7]));
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], __uint_as_float(sv[56 + e]));
+        float pmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                           fmaxf(mx[6], mx[7]));
+        // the other half's max of the row (buffers alternate by block, so a slow partner still
+        // reads this block's value after this warp has moved on)
+        red[(b * 2 + h) * 128 + r] = pmax;
+        named_barrier_sync(kNbPair + q, 64);
+        pmax = fmaxf(pmax, red[(b * 2 + (h ^ 1)) * 128 + r]);
+        // both warps of the quadrant hold the same row maxima, so they take the same decisions
         const float mc = fmaxf(m, pmax);
         float alpha = 1.f;
         bool need = false;
@@ -525,40 +552,32 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
           alpha = m == -INFINITY ? 0.f : fast_exp2((m - mc) * c2);
           m = mc;
         }
-        // rows whose max was raised: their row of O (and l beside it) is rescaled once the
-        // previous block's P.V has completed; the loads and stores are warp-wide
+        // P = exp2(s c2 - m c2) <= 2^8 in f16 pairs over the first 32 of this warp's columns; a
+        // masked key (-inf) gives 0, also while m is still -inf (then the offset is taken as 0)
+        const float mc2 = m == -INFINITY ? 0.f : m * c2;
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), c2, -mc2));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc2));
+          pk[c >> 1] = pack_f16x2(p0, p1);
+        }
+        tmem_st32(scol, pk);
+        // rows whose max was raised: this warp's half of their row of O (half 0 also l) is
+        // rescaled once the previous block's P.V has completed (after the P stores, so that the
+        // scores are no longer held); the loads and stores are warp-wide
         if (__any_sync(0xffffffffu, need)) {
           wait_bar(tbar(bars, kTbPvDone + ((kb - 1) & 1u)), ((kb - 1) >> 1) & 1, to);
           tc_fence_after();
-#pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(ocol + 32 * cc, o);
-            tmem_wait_ld_regs32(o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(ocol + 32 * cc, o);
+          t_scale_o32(ocol + 64 * h, alpha);
+          t_scale_o32(ocol + 64 * h + 32, alpha);
+          if (h == 0) {
+            uint32_t o8[8];
+            tmem_ld8(ocol + 128, o8);
+            tmem_wait_ld_regs(o8);
+            o8[0] = __float_as_uint(__uint_as_float(o8[0]) * alpha);  // l
+            tmem_st8(ocol + 128, o8);
           }
-          uint32_t o8[8];
-          tmem_ld8(ocol + 128, o8);
-          tmem_wait_ld_regs(o8);
-          o8[0] = __float_as_uint(__uint_as_float(o8[0]) * alpha);  // l
-          tmem_st8(ocol + 128, o8);
-          tmem_wait_st();
-        }
-        // P = exp2(s c2 - m c2) <= 2^8 in f16 pairs over the first 64 columns of the S buffer; a
-        // masked key (-inf) gives 0, also while m is still -inf (then the offset is taken as 0)
-        const float mc2 = m == -INFINITY ? 0.f : m * c2;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {  // keys 64 hf .. 64 hf + 63 -> columns 32 hf .. + 31
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sv[64 * hf + c]), c2, -mc2));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sv[64 * hf + c + 1]), c2, -mc2));
-            pk[c >> 1] = pack_f16x2(p0, p1);
-          }
-          tmem_st32(scol + 32 * hf, pk);
         }
         tmem_wait_st();
       }
@@ -569,7 +588,7 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
 
     // ---- segment end: the next segment's Q tile (every Q.K^T of this one is complete), then
     // the epilogue of this one ----
-    if (s + 1 < s_end) {
+    if (h == 0 && s + 1 < s_end) {
       t_load_q(p, t_load_seg(p, s + 1), smem, sbase, tbase, lane_base, r, lane);
       if (lane == 0) mbar_arrive(tbar(bars, kTbQReady));
     }
@@ -587,7 +606,7 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
       float* orow = p.out + (((int64_t)sg.seq * p.q_len + tok) * p.Hq + qh) * 128;
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 2 * h; cc < 2 * h + 2; ++cc) {
         uint32_t o[32];
         tmem_ld32(ocol + 32 * cc, o);
         tmem_wait_ld_regs32(o);
@@ -608,7 +627,7 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
           }
         }
       }
-      if (row_ok && split) {
+      if (row_ok && split && h == 0) {
         part[kTRows * 128 + r] = m;
         part[kTRows * 128 + kTRows + r] = l;
       }
@@ -630,20 +649,16 @@ __global__ void __launch_bounds__(kTThreads, 1) tile_kernel(const TileParams p) 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTStages; ++s) {
       mbar_init(tbar(bars, kTbStageFull + s), 1);
-      // Q.K^T commit (K read), dequant warps (V read), softmax warps (page ids read)
-      mbar_init(tbar(bars, kTbStageEmpty + s), 1 + kTDeqWarps + 4);
+      // softmax warps (page ids read, after the Q.K^T that read the K codes) and V warps
+      mbar_init(tbar(bars, kTbStageEmpty + s), kTSoftWarps + kTDeqWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tbar(bars, kTbSFull + b), 1);
-      mbar_init(tbar(bars, kTbPFull + b), 4);
+      mbar_init(tbar(bars, kTbPFull + b), kTSoftWarps + kTDeqWarps);
       mbar_init(tbar(bars, kTbPvDone + b), 1);
     }
-    for (int v = 0; v < kTVtBufs; ++v) {
-      mbar_init(tbar(bars, kTbVtFull + v), kTDeqWarps);
-      mbar_init(tbar(bars, kTbVtFree + v), 1);
-    }
     mbar_init(tbar(bars, kTbQReady), 4);
-    mbar_init(tbar(bars, kTbOFree), 4);
+    mbar_init(tbar(bars, kTbOFree), kTSoftWarps);
     mbar_init(tbar(bars, kTbDrain), 1);
     fence_mbar_init();
   }
@@ -681,6 +696,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tile_kernel(const TileParams p) 
   tc_fence_after();
   if (warp == kTWarpMma) tmem_dealloc(tbase, kTTmemCols);
 }
+
 
 // --------------------------------------------------------------------------------------------
 // Split-K merge of the tile kernel's partials (second launch): one CTA per (split group, row of
