@@ -16,9 +16,9 @@
 // Per block (the head's part of two pages, 19 KB in eight bulk copies):
 //   Q.K^T: tcgen05.mma kind::mxf4nvf4 block_scale.scale_vec::4X, M = 128 query rows, N = 128
 //     keys, K = 64 per instruction (two per 128-dim row) into one of two S buffers in tensor
-//     memory. The K codes are used as the pool stores them (tensor-core tile order); the MMA warp
-//     gathers the head's K scales of the two pages into the scale-factor copy's row order while
-//     the previous block's P.V runs.
+//     memory. The K codes are used as the pool stores them (tensor-core tile order); the Q.K^T
+//     warp gathers the head's K scales of the two pages into the scale-factor copy's row order
+//     ahead of time.
 //   Softmax: eight warps, two per tensor-memory lane quadrant: one query row per thread (lane =
 //     row) and 64 of the block's 128 keys per warp, fp32 online softmax. The two warps of a
 //     quadrant exchange their partial row maxima through shared memory. The running max m of a
@@ -36,16 +36,18 @@
 // Two S buffers and two V tiles: the Q.K^T and the dequantisation of block j + 1 run while the
 // softmax and the P.V of block j do.
 //
-// Warp roles (448 threads): warp 0 bulk-copy producer, warp 1 MMA issuer and tensor-memory owner,
-// warps 2..9 softmax and epilogue (warp w: lane quadrant w mod 4, key half (w - 2) / 4), warps
-// 10..13 V dequantisation. Every wait is an mbarrier wait bounded in time; on a timeout the kernel
+// Warp roles (480 threads): warp 0 bulk-copy producer, warp 1 Q.K^T issuer and tensor-memory
+// owner, warps 2..9 softmax and epilogue (warp w: lane quadrant w mod 4, key half (w - 2) / 4),
+// warps 10..13 V dequantisation, warp 14 P.V issuer. The two MMA issuers sit on different SM
+// sub-partitions (warp w runs on sub-partition w mod 4), so that issuing one block's P.V and
+// the next block's Q.K^T overlap. Every wait is an mbarrier wait bounded in time; on a timeout the kernel
 // records KV_NVFP4_DEV_TIMEOUT and carries on, so it cannot hang.
 //
 // Barriers per block kb (S buffer and V tile b = kb mod 2, stage kb mod 4):
-//   StageFull   producer copies landed            -> MMA warp (K scales), softmax (page ids), V
+//   StageFull   producer copies landed            -> Q.K^T warp (K scales), softmax (page ids), V
 //   SFull[b]    Q.K^T complete (commit)           -> softmax
 //   StageEmpty  softmax (after SFull: Q.K^T read the K codes) and V warps done with the stage
-//   PFull[b]    softmax wrote P, V warps wrote V  -> MMA warp issues P.V
+//   PFull[b]    softmax wrote P, V warps wrote V  -> P.V warp issues P.V
 //   PvDone[b]   P.V complete (commit)             -> S buffer b and V tile b free; O readable
 
 #include <cstdint>
@@ -71,7 +73,8 @@ constexpr int kTPartFloats = kTRows * 128 + 2 * kTRows;  // a partial: O[rows][1
 
 constexpr int kTWarpProducer = 0, kTWarpMma = 1, kTWarpSoft0 = 2, kTSoftWarps = 8;
 constexpr int kTWarpDeq0 = kTWarpSoft0 + kTSoftWarps, kTDeqWarps = 4;
-constexpr int kTThreads = (kTWarpDeq0 + kTDeqWarps) * 32;
+constexpr int kTWarpPv = kTWarpDeq0 + kTDeqWarps;
+constexpr int kTThreads = (kTWarpPv + 1) * 32;
 constexpr uint32_t kNbQ = 1;                // named barrier: the four softmax warps that load Q
 constexpr uint32_t kNbPair = 2;             // named barriers 2..5: the two warps of a quadrant
 constexpr float kLazyMax = 8.0f;            // raise the running max only past 2^8 (exp2 domain)
@@ -80,8 +83,8 @@ constexpr float kLazyMax = 8.0f;            // raise the running max only past 2
 constexpr int kTOffStage = 0;
 constexpr int kTOffQ = kTOffStage + kTStages * kTStageBytes;  // [128 rows][64 B], tile order
 constexpr int kTOffVt = kTOffQ + 8192;                         // [2] V tiles
-constexpr int kTOffSfk = kTOffVt + 2 * kVtBytes;               // [2 S buffers][2 k-halves][512 B]
-constexpr int kTOffQsc = kTOffSfk + 2 * 1024;                  // Q scales [128 rows][8]
+constexpr int kTOffSfk = kTOffVt + 2 * kVtBytes;               // [kTStages][2 k-halves][512 B]
+constexpr int kTOffQsc = kTOffSfk + kTStages * 1024;           // Q scales [128 rows][8]
 constexpr int kTOffRed = kTOffQsc + 128 * 8;                   // [2 parities][2 halves][128] f32
 constexpr int kTOffBars = kTOffRed + 2 * 2 * 128 * 4;
 // barrier indices
@@ -92,7 +95,7 @@ constexpr int kTbPFull = kTbSFull + 2;              // [2]
 constexpr int kTbPvDone = kTbPFull + 2;             // [2]
 constexpr int kTbQReady = kTbPvDone + 2;
 constexpr int kTbOFree = kTbQReady + 1;
-constexpr int kTbDrain = kTbOFree + 1;              // every tcgen05 op of the CTA complete
+constexpr int kTbDrain = kTbOFree + 1;              // every tcgen05 op of both issuers complete
 constexpr int kTNumBars = kTbDrain + 1;
 constexpr int kTOffPid = kTOffBars + kTNumBars * 8;            // [kTStages][2] page ids or -1
 constexpr int kTOffTmemSlot = kTOffPid + kTStages * 2 * 4;
@@ -222,11 +225,11 @@ __device__ void t_producer(const TileParams& p, uint8_t* smem, int lane) {
 }
 
 // --------------------------------------------------------------------------------------------
-// MMA warp. Per segment: the Q.K^T of its first two blocks, then per block j the P.V of block j
-// (once its P and V tile are written), the gathering of block j + 2's K scales while that P.V
-// runs, and, once the P.V has completed (its P lives in the S buffer), the Q.K^T of block j + 2
-// into the same buffer. A segment's first P.V overwrites O; it waits until the previous segment's
-// epilogue has read O.
+// MMA issuers. The Q.K^T warp, per block: gathers the block's K scales (as soon as its stage has
+// landed), then, once the P.V of block kb - 2 (which read its P from the S buffer) has completed,
+// issues the Q.K^T into that buffer; a segment's first Q.K^T waits for its Q tile. The P.V warp,
+// per block: once the block's P and V tile are written, issues its P.V; a segment's first P.V
+// overwrites O and waits until the previous segment's epilogue has read O.
 // --------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
   return d + (uint64_t)(bytes >> 4);  // start-address field: addresses stay below 2^18
@@ -234,14 +237,15 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
 
 // The head's K scales of block kb's two pages, gathered by the warp's lanes into the
 // scale-factor copy's rows (row r = page 0's keys r and r + 32, then page 1's, per k-half; the
-// scale-factor and the key index of the B operand are then 64 page + key). The previous reader
-// of the buffer, the Q.K^T of block kb - 2, completed before that block's P.V was issued.
+// scale-factor and the key index of the B operand are then 64 page + key), in the ring slot of
+// the block's stage. The slot's previous reader, the Q.K^T of block kb - 4, completed before
+// this warp issued the Q.K^T of block kb - 2 (it waited for the P.V of block kb - 4).
 __device__ __forceinline__ void t_gather_kscales(uint32_t sbase, uint32_t bars, uint32_t kb,
                                                  int head, bool lone, int lane, bool& to) {
-  const uint32_t st = kb % kTStages, b = kb & 1u;
+  const uint32_t st = kb % kTStages;
   wait_bar(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
   const uint32_t stage = sbase + kTOffStage + st * kTStageBytes;
-  const uint32_t sfk = sbase + kTOffSfk + b * 1024;
+  const uint32_t sfk = sbase + kTOffSfk + st * 1024;
 #pragma unroll
   for (int kh = 0; kh < 2; ++kh) {
     uint2 v[2];
@@ -261,8 +265,8 @@ __device__ __forceinline__ void t_issue_qk(uint64_t dq, uint64_t dk, uint64_t ds
   const uint32_t st = kb % kTStages, b = kb & 1u;
   if (lane == 0) {
     tc_fence_after();
-    tmem_cp_32x128b_x4(tbase + kTColSfb + b * 8, desc_add(dsf, b * 1024));
-    tmem_cp_32x128b_x4(tbase + kTColSfb + b * 8 + 4, desc_add(dsf, b * 1024 + 512));
+    tmem_cp_32x128b_x4(tbase + kTColSfb + b * 8, desc_add(dsf, st * 1024));
+    tmem_cp_32x128b_x4(tbase + kTColSfb + b * 8 + 4, desc_add(dsf, st * 1024 + 512));
     const uint64_t kd = desc_add(dk, kTOffStage + st * kTStageBytes);
     mma_nvf4_ss(tbase + kTColS + b * 128, dq, kd, kIdescQK, tbase + kTColSfa,
                 tbase + kTColSfb + b * 8, 0u);
@@ -273,31 +277,12 @@ __device__ __forceinline__ void t_issue_qk(uint64_t dq, uint64_t dk, uint64_t ds
   __syncwarp();
 }
 
-// P.V of block kb: eight MMAs (16 keys each) into O; A = P in the S buffer (keys 0..63 in
-// columns 0..31, keys 64..127 in columns 64..95).
-__device__ __forceinline__ void t_issue_pv(uint64_t dv, uint32_t bars, uint32_t tbase, uint32_t kb,
-                                           bool first, int lane, bool& to) {
-  const uint32_t b = kb & 1u;
-  wait_bar(tbar(bars, kTbPFull + b), (kb >> 1) & 1, to);
-  if (lane == 0) {
-    tc_fence_after();
-    const uint64_t bd = desc_add(dv, b * kVtBytes);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
-      mma_f16_ts(tbase + kTColO, tbase + kTColS + b * 128 + 64 * (ks >> 2) + 8 * (ks & 3),
-                 desc_add(bd, ks * 2 * kVtGroupBytes), kIdescPV, (first && ks == 0) ? 0u : 1u);
-    mma_commit(tbar(bars, kTbPvDone + b));
-  }
-  __syncwarp();
-}
-
-__device__ void t_mma(const TileParams& p, uint8_t* smem, uint32_t tbase, int lane) {
+__device__ void t_mma_qk(const TileParams& p, uint8_t* smem, uint32_t tbase, int lane) {
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kTOffBars;
   const uint64_t dq = smem_desc(sbase + kTOffQ, 128, 512);
   const uint64_t dk = smem_desc(sbase + kStK, 128, 512);   // + stage offset
   const uint64_t dsf = smem_desc(sbase + kTOffSfk, 16, 128);
-  const uint64_t dv = smem_desc(sbase + kTOffVt, kVtGroupBytes, 128);
   uint32_t kb = 0, sgi = 0;
   bool to = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
@@ -305,27 +290,45 @@ __device__ void t_mma(const TileParams& p, uint8_t* smem, uint32_t tbase, int la
     const TSeg sg = t_load_seg(p, s);
     const int n = seg_blocks(sg);
     const bool lone = (sg.head | 1) >= p.Hkv;
-    wait_bar(tbar(bars, kTbQReady), sgi & 1, to);  // this segment's Q tile and its scales
-    for (int j = 0; j < 2 && j < n; ++j) {
-      // the S buffer of block kb + j is free once the P.V of block kb + j - 2 (which read its P)
-      // has completed
-      const uint32_t kq = kb + j;
-      t_gather_kscales(sbase, bars, kq, sg.head, lone, lane, to);
-      if (kq >= 2) wait_bar(tbar(bars, kTbPvDone + (kq & 1u)), ((kq - 2) >> 1) & 1, to);
-      t_issue_qk(dq, dk, dsf, bars, tbase, kq, lane);
+    for (int j = 0; j < n; ++j, ++kb) {
+      t_gather_kscales(sbase, bars, kb, sg.head, lone, lane, to);
+      if (j == 0) wait_bar(tbar(bars, kTbQReady), sgi & 1, to);  // the segment's Q tile, scales
+      // S buffer kb & 1 is free once the P.V of block kb - 2 (which read its P) has completed
+      if (kb >= 2) wait_bar(tbar(bars, kTbPvDone + (kb & 1u)), ((kb - 2) >> 1) & 1, to);
+      t_issue_qk(dq, dk, dsf, bars, tbase, kb, lane);
     }
-    for (int j = 0; j < n; ++j) {
-      if (j == 0 && sgi > 0) wait_bar(tbar(bars, kTbOFree), (sgi - 1) & 1, to);
-      t_issue_pv(dv, bars, tbase, kb + j, j == 0, lane, to);
-      if (j + 2 < n) {
-        const uint32_t kq = kb + j + 2;
-        t_gather_kscales(sbase, bars, kq, sg.head, lone, lane, to);
-        wait_bar(tbar(bars, kTbPvDone + (kq & 1u)), ((kq - 2) >> 1) & 1, to);
-        t_issue_qk(dq, dk, dsf, bars, tbase, kq, lane);
-      }
-    }
-    kb += n;
     if (to) break;  // a lost signal: issue nothing more (the drain below still runs)
+  }
+  if (to) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
+}
+
+// P.V of block kb: eight MMAs (16 keys each) into O; A = P in the S buffer (keys 0..63 in
+// columns 0..31, keys 64..127 in columns 64..95).
+__device__ void t_mma_pv(const TileParams& p, uint8_t* smem, uint32_t tbase, int lane) {
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + kTOffBars;
+  const uint64_t dv = smem_desc(sbase + kTOffVt, kVtGroupBytes, 128);
+  uint32_t kb = 0, sgi = 0;
+  bool to = false;
+  const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
+  for (int s = s_begin; s < s_end; ++s, ++sgi) {
+    const int n = seg_blocks(t_load_seg(p, s));
+    if (sgi > 0) wait_bar(tbar(bars, kTbOFree), (sgi - 1) & 1, to);
+    for (int j = 0; j < n; ++j, ++kb) {
+      const uint32_t b = kb & 1u;
+      wait_bar(tbar(bars, kTbPFull + b), (kb >> 1) & 1, to);
+      if (lane == 0) {
+        tc_fence_after();
+        const uint64_t bd = desc_add(dv, b * kVtBytes);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_f16_ts(tbase + kTColO, tbase + kTColS + b * 128 + 64 * (ks >> 2) + 8 * (ks & 3),
+                     desc_add(bd, ks * 2 * kVtGroupBytes), kIdescPV, (j == 0 && ks == 0) ? 0u : 1u);
+        mma_commit(tbar(bars, kTbPvDone + b));
+      }
+      __syncwarp();
+    }
+    if (to) break;
   }
   if (to) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
@@ -659,7 +662,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tile_kernel(const TileParams p) 
     }
     mbar_init(tbar(bars, kTbQReady), 4);
     mbar_init(tbar(bars, kTbOFree), kTSoftWarps);
-    mbar_init(tbar(bars, kTbDrain), 1);
+    mbar_init(tbar(bars, kTbDrain), 2);  // one commit per issuer
     fence_mbar_init();
   }
   if (warp == kTWarpMma) tmem_alloc(smem_u32(smem + kTOffTmemSlot), kTTmemCols);
@@ -675,14 +678,16 @@ __global__ void __launch_bounds__(kTThreads, 1) tile_kernel(const TileParams p) 
   if (warp == kTWarpProducer) {
     t_producer(p, smem, lane);
   } else if (warp == kTWarpMma) {
-    t_mma(p, smem, tbase, lane);
+    t_mma_qk(p, smem, tbase, lane);
   } else if (warp >= kTWarpSoft0 && warp < kTWarpDeq0) {
     t_softmax(p, smem, tbase, warp, lane);
-  } else {
+  } else if (warp < kTWarpPv) {
     t_dequant(p, smem, warp, lane);
+  } else {
+    t_mma_pv(p, smem, tbase, lane);
   }
 
-  if (warp == kTWarpMma) {
+  if (warp == kTWarpMma || warp == kTWarpPv) {
     // tensor memory is freed only once no tcgen05 op of this CTA is in flight (after a timeout
     // some may still be; the wait is bounded like every other)
     if (lane == 0) mma_commit(tbar(bars, kTbDrain));
