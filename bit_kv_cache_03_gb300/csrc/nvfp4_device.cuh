@@ -360,6 +360,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete asks to be suspended for up to
+// hint_ns (it resumes as soon as the phase completes), so that waiting warps do not poll the
+// barrier and take issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -385,6 +400,22 @@ __device__ __forceinline__ void wait_bar(uint32_t bar, uint32_t parity, bool& ti
     return;
   }
   if (!mbar_wait_bounded(bar, parity)) timed_out = true;
+}
+
+// wait_bar whose tries suspend the thread (up to 1 ms each) instead of returning at once.
+__device__ __forceinline__ void wait_bar_sleep(uint32_t bar, uint32_t parity, bool& timed_out) {
+  if (timed_out) {
+    (void)mbar_try_wait(bar, parity);
+    return;
+  }
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait_suspend(bar, parity, 1000000u)) {
+    if (global_timer_ns() - t0 > 2000000000ull) {
+      timed_out = true;
+      return;
+    }
+  }
 }
 
 // Bulk (non-tensor) async copy global -> shared, completing on an mbarrier. Both addresses

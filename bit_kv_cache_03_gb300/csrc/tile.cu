@@ -22,9 +22,9 @@
 //   Softmax: eight warps, two per tensor-memory lane quadrant: one query row per thread (lane =
 //     row) and 64 of the block's 128 keys per warp, fp32 online softmax. The two warps of a
 //     quadrant exchange their partial row maxima through shared memory. The running max m of a
-//     row is raised only when a block's max exceeds it by more than 2^8 in the exp2 domain (the
+//     row is raised only when a block's max exceeds it by more than 2^15 in the exp2 domain (the
 //     warps then rescale their halves of the row of O in tensor memory), so P = exp2((s - m) c2)
-//     <= 2^8 fits f16. Each warp writes its 64 P values in f16 pairs over the first 32 of its own
+//     <= 2^15 fits f16 (largest finite value 65504). Each warp writes its 64 P values in f16 pairs over the first 32 of its own
 //     64 S columns, where the P.V product reads them as its A operand.
 //   V: four warps dequantise the block's V rows (E2M1 x E4M3 is exact in f16), one key row per
 //     thread, into an MN-major f16 tile in shared memory.
@@ -77,7 +77,7 @@ constexpr int kTWarpPv = kTWarpDeq0 + kTDeqWarps;
 constexpr int kTThreads = (kTWarpPv + 1) * 32;
 constexpr uint32_t kNbQ = 1;                // named barrier: the four softmax warps that load Q
 constexpr uint32_t kNbPair = 2;             // named barriers 2..5: the two warps of a quadrant
-constexpr float kLazyMax = 8.0f;            // raise the running max only past 2^8 (exp2 domain)
+constexpr float kLazyMax = 15.0f;           // raise the running max only past 2^15 (exp2 domain)
 
 // shared memory map
 constexpr int kTOffStage = 0;
@@ -185,7 +185,7 @@ __device__ void t_producer(const TileParams& p, uint8_t* smem, int lane) {
         if (lane == 0) {
           const uint32_t st = k % kTStages;
           if (k >= kTStages)
-            wait_bar(tbar(bars, kTbStageEmpty + st), ((k / kTStages) - 1) & 1, to);
+            wait_bar_sleep(tbar(bars, kTbStageEmpty + st), ((k / kTStages) - 1) & 1, to);
           const bool has1 = j + 1 < n;
           const bool v0 = pid0 >= 0 && pid0 < p.num_pages;
           const bool v1 = has1 && pid1 >= 0 && pid1 < p.num_pages;
@@ -218,7 +218,7 @@ __device__ void t_producer(const TileParams& p, uint8_t* smem, int lane) {
     // no copy into this CTA's shared memory may still be in flight at exit
     for (uint32_t st = 0; st < kTStages && st < k; ++st) {
       const uint32_t last = k - 1 - ((k - 1 - st) % kTStages);
-      wait_bar(tbar(bars, kTbStageFull + st), (last / kTStages) & 1, to);
+      wait_bar_sleep(tbar(bars, kTbStageFull + st), (last / kTStages) & 1, to);
     }
     if (to) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
   }
@@ -243,7 +243,7 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
 __device__ __forceinline__ void t_gather_kscales(uint32_t sbase, uint32_t bars, uint32_t kb,
                                                  int head, bool lone, int lane, bool& to) {
   const uint32_t st = kb % kTStages;
-  wait_bar(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
+  wait_bar_sleep(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
   const uint32_t stage = sbase + kTOffStage + st * kTStageBytes;
   const uint32_t sfk = sbase + kTOffSfk + st * 1024;
 #pragma unroll
@@ -292,9 +292,9 @@ __device__ void t_mma_qk(const TileParams& p, uint8_t* smem, uint32_t tbase, int
     const bool lone = (sg.head | 1) >= p.Hkv;
     for (int j = 0; j < n; ++j, ++kb) {
       t_gather_kscales(sbase, bars, kb, sg.head, lone, lane, to);
-      if (j == 0) wait_bar(tbar(bars, kTbQReady), sgi & 1, to);  // the segment's Q tile, scales
+      if (j == 0) wait_bar_sleep(tbar(bars, kTbQReady), sgi & 1, to);  // the segment's Q tile, scales
       // S buffer kb & 1 is free once the P.V of block kb - 2 (which read its P) has completed
-      if (kb >= 2) wait_bar(tbar(bars, kTbPvDone + (kb & 1u)), ((kb - 2) >> 1) & 1, to);
+      if (kb >= 2) wait_bar_sleep(tbar(bars, kTbPvDone + (kb & 1u)), ((kb - 2) >> 1) & 1, to);
       t_issue_qk(dq, dk, dsf, bars, tbase, kb, lane);
     }
     if (to) break;  // a lost signal: issue nothing more (the drain below still runs)
@@ -313,10 +313,10 @@ __device__ void t_mma_pv(const TileParams& p, uint8_t* smem, uint32_t tbase, int
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
   for (int s = s_begin; s < s_end; ++s, ++sgi) {
     const int n = seg_blocks(t_load_seg(p, s));
-    if (sgi > 0) wait_bar(tbar(bars, kTbOFree), (sgi - 1) & 1, to);
+    if (sgi > 0) wait_bar_sleep(tbar(bars, kTbOFree), (sgi - 1) & 1, to);
     for (int j = 0; j < n; ++j, ++kb) {
       const uint32_t b = kb & 1u;
-      wait_bar(tbar(bars, kTbPFull + b), (kb >> 1) & 1, to);
+      wait_bar_sleep(tbar(bars, kTbPFull + b), (kb >> 1) & 1, to);
       if (lane == 0) {
         tc_fence_after();
         const uint64_t bd = desc_add(dv, b * kVtBytes);
@@ -365,9 +365,9 @@ __device__ void t_dequant(const TileParams& p, uint8_t* smem, int warp, int lane
     const int n = seg_blocks(sg);
     for (int j = 0; j < n; ++j, ++kb) {
       const uint32_t st = kb % kTStages, v = kb & 1u;
-      wait_bar(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
+      wait_bar_sleep(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
       // V tile v is free once the P.V of block kb - 2 is complete
-      if (kb >= 2) wait_bar(tbar(bars, kTbPvDone + v), ((kb - 2) >> 1) & 1, to);
+      if (kb >= 2) wait_bar_sleep(tbar(bars, kTbPvDone + v), ((kb - 2) >> 1) & 1, to);
       const int page = sg.lo + 2 * j + pg;
       const bool ok = page < sg.hi && stage_pid[2 * st + pg] >= 0 && page * kPage + slot < sg.len;
       const uint32_t stage = sbase + kTOffStage + st * kTStageBytes;
@@ -505,18 +505,19 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
     for (int j = 0; j < n; ++j, ++kb) {
       const uint32_t b = kb & 1u, st = kb % kTStages;
       // page ids of the block, published before its stage's full barrier completed
-      wait_bar(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
+      wait_bar_sleep(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
       const int page = sg.lo + 2 * j + h;
       const bool valid = page < sg.hi && stage_pid[2 * st + h] >= 0;
-      wait_bar(tbar(bars, kTbSFull + b), (kb >> 1) & 1, to);
+      wait_bar_sleep(tbar(bars, kTbSFull + b), (kb >> 1) & 1, to);
       tc_fence_after();
       __syncwarp();
       // the Q.K^T (complete) read the stage's K codes; this warp is done with its page ids
       if (lane == 0) mbar_arrive(tbar(bars, kTbStageEmpty + st));
       if (warp_live) {
         const uint32_t scol = tbase + lane_base + kTColS + b * 128 + 64 * h;
-        // keys c < nv of this warp's page are visible to this row
-        const int nv = valid ? max(0, min(kPage, limit - page * kPage + 1)) : 0;
+        // keys c < nv of this warp's page are visible to this row; a padding row (no query) is
+        // left unmasked: its P and O are never read, and its scores are finite or its own
+        const int nv = !row_ok ? kPage : valid ? max(0, min(kPage, limit - page * kPage + 1)) : 0;
         uint32_t sv[64];
         ld32_at(scol, &sv[0]);
         ld32_at(scol + 32, &sv[32]);
@@ -555,7 +556,7 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
           alpha = m == -INFINITY ? 0.f : fast_exp2((m - mc) * c2);
           m = mc;
         }
-        // P = exp2(s c2 - m c2) <= 2^8 in f16 pairs over the first 32 of this warp's columns; a
+        // P = exp2(s c2 - m c2) <= 2^15 in f16 pairs over the first 32 of this warp's columns; a
         // masked key (-inf) gives 0, also while m is still -inf (then the offset is taken as 0)
         const float mc2 = m == -INFINITY ? 0.f : m * c2;
         uint32_t pk[32];
@@ -570,7 +571,7 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
         // rescaled once the previous block's P.V has completed (after the P stores, so that the
         // scores are no longer held); the loads and stores are warp-wide
         if (__any_sync(0xffffffffu, need)) {
-          wait_bar(tbar(bars, kTbPvDone + ((kb - 1) & 1u)), ((kb - 1) >> 1) & 1, to);
+          wait_bar_sleep(tbar(bars, kTbPvDone + ((kb - 1) & 1u)), ((kb - 1) >> 1) & 1, to);
           tc_fence_after();
           t_scale_o32(ocol + 64 * h, alpha);
           t_scale_o32(ocol + 64 * h + 32, alpha);
@@ -596,7 +597,7 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
       if (lane == 0) mbar_arrive(tbar(bars, kTbQReady));
     }
     const uint32_t kl = kb - 1;
-    wait_bar(tbar(bars, kTbPvDone + (kl & 1u)), (kl >> 1) & 1, to);
+    wait_bar_sleep(tbar(bars, kTbPvDone + (kl & 1u)), (kl >> 1) & 1, to);
     tc_fence_after();
     const bool split = sg.n_seg > 1;
     if (warp_live) {
@@ -693,7 +694,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tile_kernel(const TileParams p) 
     if (lane == 0) mma_commit(tbar(bars, kTbDrain));
     __syncwarp();
     bool to = false;
-    wait_bar(tbar(bars, kTbDrain), 0, to);
+    wait_bar_sleep(tbar(bars, kTbDrain), 0, to);
     if (to && lane == 0) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
   }
   tc_fence_before();
