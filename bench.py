@@ -585,6 +585,25 @@ def run_cuda(args, world, rank, local):
         assert gt.status() == 0
         print(json.dumps({"profile_run": True, "workload": wt.name, "steps": args.steps}))
         return
+    if args.profile_append:
+        # short run of the bulk append (16,384 tokens with Q, K, V) for the profiler
+        wa = synth.steady_decode()
+        Ta = 16384
+        qa = torch.randn(Ta, wa.q_heads, 128, device=dev).to(torch.bfloat16)
+        ka = torch.randn(Ta, wa.kv_heads, 128, device=dev).to(torch.bfloat16)
+        va = torch.randn(Ta, wa.kv_heads, 128, device=dev).to(torch.bfloat16)
+        sida = torch.zeros(Ta, dtype=torch.int32, device=dev)
+        posa = torch.arange(Ta, dtype=torch.int32, device=dev)
+        ca = kv.PagedNVFP4Cache(Ta // 64, np.arange(Ta // 64, dtype=np.int32)[None], Ta,
+                                wa.q_heads, wa.kv_heads, wa.rot_dim, device=dev)
+        qca, qsa = ca.quantized_q_buffers(Ta)
+        for _ in range(args.warmup + args.steps):
+            ca.append(ka, va, sida, posa, q=qa, q_codes=qca, q_scales=qsa)
+        torch.cuda.synchronize(dev)
+        assert int(ca.status.item()) == 0
+        print(json.dumps({"profile_run": True, "workload": "append_16384_tokens",
+                          "steps": args.steps}))
+        return
     w = synth.steady_decode()
     if args.seqs != 4:
         w = synth.Workload(f"steady_decode_{args.seqs}x128k", [131072] * args.seqs, q_len=1,
@@ -817,6 +836,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-tile", choices=["verify", "prefill"], default=None,
                     help="short run of the verify or prefill-chunk attention call (profiling)")
+    ap.add_argument("--profile-append", action="store_true",
+                    help="short run of the 16,384-token bulk append (profiling)")
     ap.add_argument("--no-tile-workloads", action="store_true",
                     help="skip timing the verify and prefill-chunk shapes (tile kernel)")
     ap.add_argument("--no-configs", action="store_true",
