@@ -138,6 +138,9 @@ struct DecodeParams {
   uint8_t* pool_w;         // the pool, receiving the new K/V rows
   uint8_t* q_codes_out;    // optional copy of the encoded Q rows, or null
   uint8_t* q_scales_out;
+  // 1 when the plan tables (cta_seg, segments, groups) were written before the launch (not by the
+  // kernel this one depends on), so that they may be read before the dependency wait
+  int32_t early_tables;
 };
 
 struct SegInfo {
@@ -365,7 +368,7 @@ __device__ __forceinline__ void s_issue(AttnCtx& c, uint32_t kk, uint32_t (&sr)[
   tmem_ld8(c.tbase + c.lane_base + kColS + b * 32 + c.pr * 16 + c.half * 8, sr);
 }
 
-// Finish loading page kk's scores, release the S buffer, and turn the scores into P in the P tile
+// Finish loading page kk's scores and turn them into P in the P tile
 // at pt: page max per row over the warp's 32 keys (warp reductions), running max and row-sum
 // update, P = exp2((s - m) c2) <= 1 in f16. Returns whether a max grew (then alpha_a and
 // alpha_b are the factors for rows 2t and 2t + 1 of the accumulator). kv_lim: keys of the page
@@ -376,9 +379,6 @@ __device__ __forceinline__ bool s_softmax(AttnCtx& c, uint32_t kk, uint32_t kst,
                                           float (&lp)[kRows], uint32_t pt, int t, float c2,
                                           float& alpha_a, float& alpha_b, int& kv_lim) {
   tmem_wait_ld_regs(sr);
-  tc_fence_before();
-  __syncwarp();
-  if (c.lane == 0) mbar_arrive(c.bars + 8 * (kBarSFree + kk % kSBufs));
   const uint32_t st = kst % kStages;
   // the Q.K^T warp saw this stage land; waiting here as well makes the V bytes and the page id
   // visible to this warp (the wait returns at once)
@@ -551,9 +551,10 @@ __device__ __forceinline__ void new_kv_store(const DecodeParams& p, const NewKvR
 // step's new K/V rows that fall on the segment's pages stored into the pool. The bf16 rows and
 // RoPE rows come from the step slot, which the producer filled ahead of the segment; the one
 // global load left is the page id of a new row (while the other CTAs stream the cache, a global
-// load takes about a microsecond, and the segment's first QK waits for this prologue). Kept out of
-// line: inlined, it made the page loop that follows about 4 % slower (measured).
-__device__ __noinline__ void fused_prologue(const DecodeParams& p, const SegInfo& sg,
+// load takes about a microsecond, and the segment's first QK waits for this prologue). Inlined:
+// out of line, its reads of the kernel parameters and the segment record went through memory and
+// the prologue took about twice as long (a decode step of 4 x 128K tokens 1.8 us longer, measured).
+__device__ __forceinline__ void fused_prologue(const DecodeParams& p, const SegInfo& sg,
                                                uint8_t* smem, const uint8_t* slot, uint32_t sbase,
                                                uint32_t bars, int aw, int lane) {
   const int rows_total = p.G * p.q_len;
@@ -770,8 +771,14 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
         const uint32_t vs = stage + p.Hkv * 8704 + c.head * 512 + g;       // scale of block g
         pv_page(smem, lm_addr, vc - c.sbase, vs - c.sbase, c.key0, kv_lim, vk0, vk1, acc);
       }
+      // the page's S buffer and stage slot are released together (the Q.K^T warp runs pages
+      // ahead, so it seldom waits for an S buffer)
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bars + 8 * (kBarStageEmpty + st));
+      if (lane == 0) {
+        mbar_arrive(c.bars + 8 * (kBarSFree + k % kSBufs));
+        mbar_arrive(c.bars + 8 * (kBarStageEmpty + st));
+      }
     }
 
     // ---- segment end: row sums, then the two warps of each head merge ----
@@ -880,6 +887,17 @@ __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodePa
     fence_mbar_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(smem + kOffTmemSlot), kTmemCols);
+  if (p.early_tables && lane == 0) {
+    // bring this CTA's first segment record into L1 while the previous kernel finishes: every warp
+    // starts by reading it, three dependent loads that otherwise take ~1.5 us under the page
+    // stream of the other CTAs
+    const int s0 = __ldg(p.cta_seg + blockIdx.x), s1 = __ldg(p.cta_seg + blockIdx.x + 1);
+    if (s0 < s1) {
+      const int4 seg = __ldg(p.segments + s0);
+      const int4 g0 = __ldg(p.groups + 2 * seg.x), g1 = __ldg(p.groups + 2 * seg.x + 1);
+      asm volatile("" ::"r"(g0.x), "r"(g1.x));
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1036,6 +1054,7 @@ cudaError_t launch_decode(const uint8_t* q_codes, const uint8_t* q_scales, const
   p.q_new = q_new; p.k_new = k_new; p.v_new = v_new; p.rope = rope;
   p.rope_max_pos = rope_max_pos; p.rot_dim = rot_dim; p.pool_w = pool_w;
   p.q_codes_out = q_codes_out; p.q_scales_out = q_scales_out;
+  p.early_tables = late_tables ? 0 : 1;
   const bool fused = q_new != nullptr;
   if (grid <= 0) return cudaSuccess;
   // programmatic dependent launch: the kernel is set up while the previous kernel on the stream
