@@ -631,11 +631,11 @@ __device__ __forceinline__ void fused_prologue(const DecodeParams& p, const SegI
     new_kv_store(p, kv, lane);
   }
   // the pool rows visible to this CTA's bulk copies (async proxy) before the producer copies their
-  // page; the Q tile and its staged scales complete before the scale factors are read
-  if (nrows > 0) {
-    __threadfence();
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-  }
+  // page: each writer orders its stores before later async-proxy accesses, and the barrier below
+  // plus the producer's wait on the KV-ready barrier carry that order to the copy (the only reader
+  // of those rows in this kernel; a GPU-scope fence here made these CTAs the step's last by
+  // 1-3 us); the Q tile and its staged scales complete before the scale factors are read
+  if (nrows > 0) asm volatile("fence.proxy.async.global;" ::: "memory");
   named_barrier_sync(kNbAttn, 32 * kAttnWarps);
   if (nrows > 0 && aw == 0 && lane == 0) mbar_arrive(bars + 8 * kBarKvReady);
 }
