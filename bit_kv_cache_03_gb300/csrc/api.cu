@@ -64,6 +64,7 @@ constexpr int kPartHeadFloats = kRowsPerItem * 128 + 2 * kRowsPerItem;  // O[8][
 // Tiles of more rows (speculative verify, prefill chunks) go to the tile kernel: groups of one
 // KV head and 128 rows, one partial (O, m, l of the tile's rows) per segment.
 constexpr int kTileRows = 128;
+constexpr int kTailCharge = 2;    // extra pages charged for a decode group's last page
 constexpr int kTilePartFloats = kTileRows * 128 + 2 * kTileRows;
 
 constexpr int kMaxAttnKvHeads = 4;  // the decode kernel stages every head of a page
@@ -102,7 +103,10 @@ uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 // The split-K work list. Groups are (sequence, 8-row query tile) over every KV head for the
 // decode kernel, or (sequence, KV head, 128-row tile) for the tile kernel, in that order; each
 // group's visited pages are cut into chunks of chunk_pages, and the chunk stream of all groups is
-// dealt out to `grid` CTAs in contiguous ranges of about total_pages / grid pages each.
+// dealt out to `grid` CTAs in contiguous ranges of about total_pages / grid pages each. For the
+// decode kernel a group's last page is charged kTailCharge pages more: in the fused decode step
+// the CTA holding it also encodes and stores the step's new K/V rows (measured ~1-2 us, two
+// pages' time), so it gets that many fewer pages.
 struct PlanBuild {
   kv_nvfp4_plan_info info;
   std::vector<int32_t> groups;    // 8 ints per group
@@ -147,6 +151,8 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
       }
   }
   const int64_t grid = std::min<int64_t>(num_sms, total_chunks);
+  const int64_t tail = tile ? 0 : kTailCharge;  // cost of a group's last page beyond one page
+  const int64_t total_cost = total_pages + tail * n_groups;
   pb->groups.assign((size_t)n_groups * 8, 0);
   pb->segments.clear();
   pb->cta_seg.assign((size_t)grid + 1, 0);
@@ -161,17 +167,17 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
       int32_t hi = lo;
       while (hi < pages) {
         hi = std::min(pages, hi + chunk_pages);
-        const int64_t quota = (cta + 1) * total_pages / grid;
-        if (cta < grid - 1 && dealt + (hi - lo) >= quota) break;
+        const int64_t quota = (cta + 1) * total_cost / grid;
+        if (cta < grid - 1 && dealt + (hi - lo) + (hi == pages ? tail : 0) >= quota) break;
       }
       pb->segments.push_back((int32_t)gi);
       pb->segments.push_back(lo);
       pb->segments.push_back(hi);
       pb->segments.push_back(-1);
       seg_count[(size_t)gi] += 1;
-      dealt += hi - lo;
+      dealt += hi - lo + (hi == pages ? tail : 0);
       lo = hi;
-      const int64_t quota = (cta + 1) * total_pages / grid;
+      const int64_t quota = (cta + 1) * total_cost / grid;
       if (cta < grid - 1 && dealt >= quota) {
         ++cta;
         pb->cta_seg[(size_t)cta] = (int32_t)(pb->segments.size() / 4);
