@@ -44,9 +44,9 @@
 // records KV_NVFP4_DEV_TIMEOUT and carries on, so it cannot hang.
 //
 // Barriers per block kb (S buffer and V tile b = kb mod 2, stage kb mod 4):
-//   StageFull   producer copies landed            -> Q.K^T warp (K scales), softmax (page ids), V
+//   StageFull   producer copies landed            -> Q.K^T warp (K scales), V warps
 //   SFull[b]    Q.K^T complete (commit)           -> softmax
-//   StageEmpty  softmax (after SFull: Q.K^T read the K codes) and V warps done with the stage
+//   StageEmpty  Q.K^T complete (commit) and V warps done with the stage
 //   PFull[b]    softmax wrote P, V warps wrote V  -> P.V warp issues P.V
 //   PvDone[b]   P.V complete (commit)             -> S buffer b and V tile b free; O readable
 
@@ -273,6 +273,7 @@ __device__ __forceinline__ void t_issue_qk(uint64_t dq, uint64_t dk, uint64_t ds
     mma_nvf4_ss(tbase + kTColS + b * 128, desc_add(dq, 256), desc_add(kd, 256), kIdescQK,
                 tbase + kTColSfa + 4, tbase + kTColSfb + b * 8 + 4, 1u);
     mma_commit(tbar(bars, kTbSFull + b));
+    mma_commit(tbar(bars, kTbStageEmpty + st));  // K codes and scales consumed
   }
   __syncwarp();
 }
@@ -475,7 +476,6 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
                           int lane) {
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kTOffBars;
-  const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kTOffPid);
   float* red = reinterpret_cast<float*>(smem + kTOffRed);
   const int q = warp & 3;
   const int h = (warp - kTWarpSoft0) >> 2;
@@ -502,17 +502,20 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
     // largest visible key position of this row (-1: no key)
     const int limit = row_ok ? (p.causal ? sg.len - p.q_len + gr / p.G : sg.len - 1) : -1;
     float m = -INFINITY;
+    // this warp's page of each block is skipped (its keys masked) when its id lies outside the
+    // pool, as the producer skips it; the id is read from the block table one block ahead, so that
+    // the block loop touches no shared-memory barrier but the S-full and P-full ones
+    const int32_t* bt = p.block_table + (int64_t)sg.seq * p.max_pages;
+    int32_t pid_next = (sg.lo + h < sg.hi) ? __ldg(bt + sg.lo + h) : -1;
     for (int j = 0; j < n; ++j, ++kb) {
-      const uint32_t b = kb & 1u, st = kb % kTStages;
-      // page ids of the block, published before its stage's full barrier completed
-      wait_bar_sleep(tbar(bars, kTbStageFull + st), (kb / kTStages) & 1, to);
+      const uint32_t b = kb & 1u;
       const int page = sg.lo + 2 * j + h;
-      const bool valid = page < sg.hi && stage_pid[2 * st + h] >= 0;
+      const int32_t pid = pid_next;
+      const bool valid = page < sg.hi && pid >= 0 && pid < p.num_pages;
+      if (page + 2 < sg.hi) pid_next = __ldg(bt + page + 2);
       wait_bar_sleep(tbar(bars, kTbSFull + b), (kb >> 1) & 1, to);
       tc_fence_after();
       __syncwarp();
-      // the Q.K^T (complete) read the stage's K codes; this warp is done with its page ids
-      if (lane == 0) mbar_arrive(tbar(bars, kTbStageEmpty + st));
       if (warp_live) {
         const uint32_t scol = tbase + lane_base + kTColS + b * 128 + 64 * h;
         // keys c < nv of this warp's page are visible to this row; a padding row (no query) is
@@ -653,8 +656,8 @@ __global__ void __launch_bounds__(kTThreads, 1) tile_kernel(const TileParams p) 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kTStages; ++s) {
       mbar_init(tbar(bars, kTbStageFull + s), 1);
-      // softmax warps (page ids read, after the Q.K^T that read the K codes) and V warps
-      mbar_init(tbar(bars, kTbStageEmpty + s), kTSoftWarps + kTDeqWarps);
+      // the Q.K^T (K codes and scales read, by its commit) and the V warps
+      mbar_init(tbar(bars, kTbStageEmpty + s), 1 + kTDeqWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tbar(bars, kTbSFull + b), 1);
