@@ -948,7 +948,7 @@ struct MergeParams {
 // LATE_TABLES: the plan tables were written by a kernel earlier in the same step (not by a copy
 // before the attention launch), so they are read only after the wait as well.
 template <bool LATE_TABLES>
-__global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(256, 4) merge_kernel(const MergeParams p) {
   __shared__ float s_m[8], s_l[8];
   __shared__ float4 s_o[8][32];
   asm volatile("griddepcontrol.launch_dependents;");  // the next kernel may begin its launch
@@ -965,22 +965,37 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeParams p) {
   const int slice = threadIdx.x >> 5, d4 = threadIdx.x & 31;
   const int64_t stride = (int64_t)p.Hkv * kPartHeadFloats;
   const float* base = p.partials + (int64_t)g1.y * stride + h * kPartHeadFloats;
-  // one pass per slice with a running max; slices combined below
+  // one pass per slice with a running max; slices combined below. A slice's partials (up to 4
+  // per round: 32 segments) are all requested before any is used, so that a round costs one
+  // L2 round trip rather than one per partial
   float M = -INFINITY, L = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int q = slice; q < n_seg; q += 8) {
-    const float* pq = base + q * stride;
-    const float mq = __ldcg(pq + kRows * 128 + i);
-    const float lq = __ldcg(pq + kRows * 128 + kRows + i);
-    const float4 ov = __ldcg(reinterpret_cast<const float4*>(pq + i * 128) + d4);
-    if (mq == -INFINITY) continue;  // a segment with no visible key
-    const float mn = fmaxf(M, mq);
-    const float a = fast_exp2((M - mn) * p.c2), f = fast_exp2((mq - mn) * p.c2);  // a = 0 at start
-    M = mn;
-    L = L * a + f * lq;
-    O.x = O.x * a + f * ov.x; O.y = O.y * a + f * ov.y;
-    O.z = O.z * a + f * ov.z; O.w = O.w * a + f * ov.w;
+  for (int q0 = slice; q0 < n_seg; q0 += 32) {
+    float mq[4], lq[4];
+    float4 ov[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = q0 + 8 * u;
+      mq[u] = -INFINITY;
+      lq[u] = 0.f;
+      ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (q < n_seg) {
+        const float* pq = base + q * stride;
+        mq[u] = __ldcg(pq + kRows * 128 + i);
+        lq[u] = __ldcg(pq + kRows * 128 + kRows + i);
+        ov[u] = __ldcg(reinterpret_cast<const float4*>(pq + i * 128) + d4);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (mq[u] == -INFINITY) continue;  // a segment with no visible key, or none at all
+      const float mn = fmaxf(M, mq[u]);
+      const float a = fast_exp2((M - mn) * p.c2), f = fast_exp2((mq[u] - mn) * p.c2);  // a = 0 first
+      M = mn;
+      L = L * a + f * lq[u];
+      O.x = O.x * a + f * ov[u].x; O.y = O.y * a + f * ov[u].y;
+      O.z = O.z * a + f * ov[u].z; O.w = O.w * a + f * ov[u].w;
+    }
   }
   s_o[slice][d4] = O;
   if (d4 == 0) { s_m[slice] = M; s_l[slice] = L; }
