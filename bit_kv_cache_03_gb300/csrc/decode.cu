@@ -257,7 +257,6 @@ template <bool FUSED>
 __device__ void qk_warp(const DecodeParams& p, uint8_t* smem, uint32_t tbase, int lane) {
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kOffBars;
-  const volatile int32_t* stage_pid = reinterpret_cast<const volatile int32_t*>(smem + kOffStagePid);
   const int npairs = (p.Hkv + 1) >> 1;
   uint32_t k = 0, ks = 0, sgi = 0;  // pages (S buffers), stage slots, segments
   bool timed_out = false;
