@@ -578,7 +578,7 @@ def run_cuda(args, world, rank, local):
         from kvrun import GpuRun as _G
         wt = synth.spec_verify() if args.profile_tile == "verify" else synth.prefill_chunk()
         gt = _G(wt, device=dev)
-        gt.step(chunk_tokens=1024)
+        gt.step(chunk_tokens=128 if args.profile_tile == "verify" else 1024)
         for _ in range(args.warmup + args.steps):
             gt.cache.attend(gt.q_codes, gt.q_scales, gt.out, sm_scale=wt.sm_scale)
         torch.cuda.synchronize(dev)
@@ -739,7 +739,9 @@ def run_cuda(args, world, rank, local):
         c2["cosine_error"] = str(e)[:200]
     configs[w.name] = c2
     if not args.no_configs:
-        for wc, chunk in ((synth.tiny_decode(), 64), (synth.ragged_decode(), 1024)):
+        # split-K chunks of one page: the plan then deals every CTA its share to the page (the
+        # ragged lengths with 1024-token chunks left CTAs between 49 and 80 pages)
+        for wc, chunk in ((synth.tiny_decode(), 64), (synth.ragged_decode(), 64)):
             gc, r = decode_config(wc, chunk, dev, stream, max(args.steps, 20), args.warmup, peak0)
             r["cosine_vs_unquantized"] = unquantized_cosine(gc, all_rows(wc))
             r["cosine_rows"] = wc.num_seqs * wc.q_len * wc.q_heads
@@ -750,7 +752,8 @@ def run_cuda(args, world, rank, local):
             torch.cuda.empty_cache()
     if not args.no_tile_workloads:
         from kvrun import sample_rows
-        for wc, chunk, reps, n_cos in ((synth.spec_verify(), 1024, 200, None),
+        # verify: chunks of one key block (two pages) balance the CTAs to the block
+        for wc, chunk, reps, n_cos in ((synth.spec_verify(), 128, 200, None),
                                        (synth.prefill_chunk(), 1024, 5, 64)):
             gc, r = tile_config(wc, chunk, dev, stream, reps, peak0, bf16)
             rows = all_rows(wc) if n_cos is None else sample_rows(wc, n_cos, seed=0)

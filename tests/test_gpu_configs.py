@@ -5,10 +5,12 @@ quantisation; attention is compared on every output row (decode and verify workl
 seeded row sample (the 600k prefill chunk, 196,608 rows). Each workload runs through the call and
 the split-K chunk size that bench.py times for it:
   tiny / steady / ragged decode: kv_nvfp4_decode_step (the append inside the attention launch),
-      chunks of 64 tokens (tiny, steady) and 1024 tokens (ragged), so the split-K merge runs;
+      chunks of 64 tokens, so the split-K merge runs;
   speculative verify and the 600k prefill chunk: kv_nvfp4_append + kv_nvfp4_decode_attn on the
-      tile kernel, chunks of 1024 tokens, so the tile kernel's merge runs as well.
-The decode workloads are also run through the two-call path with the workload's own chunk size.
+      tile kernel, chunks of 128 tokens (verify) and 1024 tokens (prefill), so the tile kernel's
+      merge runs as well.
+The decode workloads are also run through the two-call path with the workload's own chunk size
+(1024 tokens for the ragged workload).
 """
 import numpy as np
 import pytest
@@ -21,8 +23,8 @@ torch = pytest.importorskip("torch")
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 # the split-K chunk each workload is timed with in bench.py
-BENCH_CHUNK = {"tiny_decode_4k": 64, "steady_decode_4x128k": 64, "ragged_decode_8seq": 1024,
-               "spec_verify_4x100k_q8": 1024, "prefill_chunk_600k": 1024}
+BENCH_CHUNK = {"tiny_decode_4k": 64, "steady_decode_4x128k": 64, "ragged_decode_8seq": 64,
+               "spec_verify_4x100k_q8": 128, "prefill_chunk_600k": 1024}
 
 
 def _check(g, o, w, rows, label):
@@ -84,7 +86,7 @@ def test_spec_verify_4x100k_q8():
     o = OracleRun(w)
     g.step(chunk_tokens=BENCH_CHUNK[w.name])
     assert g.cache.plan_info.num_split_groups > 0  # the tile kernel's merge ran
-    _check(g, o, w, None, "append + decode_attn (tile kernel) chunk 1024")
+    _check(g, o, w, None, f"append + decode_attn (tile kernel) chunk {BENCH_CHUNK[w.name]}")
 
 
 def test_prefill_chunk_600k_sampled():
@@ -94,7 +96,8 @@ def test_prefill_chunk_600k_sampled():
     o = OracleRun(w)
     g.step(chunk_tokens=BENCH_CHUNK[w.name])
     assert g.cache.plan_info.num_split_groups > 0
-    _check(g, o, w, rows, "append + decode_attn (tile kernel) chunk 1024, sampled rows")
+    _check(g, o, w, rows,
+           f"append + decode_attn (tile kernel) chunk {BENCH_CHUNK[w.name]}, sampled rows")
     # one chunk per sequence (no split-K merge): the same sampled rows
     g.out.zero_()
     g.step(chunk_tokens=((w.max_pos + 63) // 64) * 64)
