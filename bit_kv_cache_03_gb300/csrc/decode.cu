@@ -172,6 +172,10 @@ __device__ void producer(const DecodeParams& p, uint8_t* smem, int lane) {
   const uint32_t bars = sbase + kOffBars;
   volatile int32_t* stage_pid = reinterpret_cast<volatile int32_t*>(smem + kOffStagePid);
   const uint32_t blk_bytes = (uint32_t)p.Hkv * 9216u;
+  // the pages are read once per call: marked first for eviction, they leave the L2 to what is
+  // read again soon (the split-K partials, which the merge reads after this kernel, the plan
+  // tables and the block table)
+  const uint64_t stream_policy = l2_evict_first_policy();
   uint32_t k = 0, kvr = 0;
   bool timed_out = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
@@ -224,8 +228,8 @@ __device__ void producer(const DecodeParams& p, uint8_t* smem, int lane) {
           const uint32_t full = bars + 8 * (kBarStageFull + st);
           if (valid) {
             mbar_arrive_expect_tx(full, blk_bytes);
-            bulk_g2s(sbase + kOffStage + st * kStageBytes, p.pool + (int64_t)pid * blk_bytes,
-                     blk_bytes, full);
+            bulk_g2s_hint(sbase + kOffStage + st * kStageBytes, p.pool + (int64_t)pid * blk_bytes,
+                          blk_bytes, full, stream_policy);
           } else {
             flag_status(p.status, KV_NVFP4_DEV_BAD_PAGE);  // the page is skipped (P = 0, V = 0)
             mbar_arrive(full);
@@ -944,12 +948,15 @@ struct MergeParams {
   float c2;
 };
 
+constexpr int kMergeSlices = 8;
+constexpr int kMergePerRound = 8;  // partials a slice requests at once (64 per CTA and round)
+
 // LATE_TABLES: the plan tables were written by a kernel earlier in the same step (not by a copy
 // before the attention launch), so they are read only after the wait as well.
 template <bool LATE_TABLES>
-__global__ void __launch_bounds__(256, 4) merge_kernel(const MergeParams p) {
-  __shared__ float s_m[8], s_l[8];
-  __shared__ float4 s_o[8][32];
+__global__ void __launch_bounds__(32 * kMergeSlices, 2) merge_kernel(const MergeParams p) {
+  __shared__ float s_m[kMergeSlices], s_l[kMergeSlices];
+  __shared__ float4 s_o[kMergeSlices][32];
   asm volatile("griddepcontrol.launch_dependents;");  // the next kernel may begin its launch
   // launched as a programmatic dependent of the attention kernel: its partials are visible only
   // after this wait (which returns when that grid has completed and flushed)
@@ -964,17 +971,17 @@ __global__ void __launch_bounds__(256, 4) merge_kernel(const MergeParams p) {
   const int slice = threadIdx.x >> 5, d4 = threadIdx.x & 31;
   const int64_t stride = (int64_t)p.Hkv * kPartHeadFloats;
   const float* base = p.partials + (int64_t)g1.y * stride + h * kPartHeadFloats;
-  // one pass per slice with a running max; slices combined below. A slice's partials (up to 4
-  // per round: 32 segments) are all requested before any is used, so that a round costs one
-  // L2 round trip rather than one per partial
+  // Per round a slice requests its partials q = q0 + 8 u (u < 8) all at once, so that a round
+  // costs one L2 round trip (a group of up to 64 segments takes one round); they are then
+  // combined with independent maxima and weights rather than one dependent step per partial.
   float M = -INFINITY, L = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int q0 = slice; q0 < n_seg; q0 += 32) {
-    float mq[4], lq[4];
-    float4 ov[4];
+  for (int q0 = slice; q0 < n_seg; q0 += kMergeSlices * kMergePerRound) {
+    float mq[kMergePerRound], lq[kMergePerRound];
+    float4 ov[kMergePerRound];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int q = q0 + 8 * u;
+    for (int u = 0; u < kMergePerRound; ++u) {
+      const int q = q0 + kMergeSlices * u;
       mq[u] = -INFINITY;
       lq[u] = 0.f;
       ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -985,16 +992,21 @@ __global__ void __launch_bounds__(256, 4) merge_kernel(const MergeParams p) {
         ov[u] = __ldcg(reinterpret_cast<const float4*>(pq + i * 128) + d4);
       }
     }
+    float mn = M;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kMergePerRound; ++u) mn = fmaxf(mn, mq[u]);
+    if (mn == -INFINITY) continue;  // no visible key in any partial so far
+    const float a = fast_exp2((M - mn) * p.c2);  // 0 while M is -inf
+    L *= a;
+    O.x *= a; O.y *= a; O.z *= a; O.w *= a;
+#pragma unroll
+    for (int u = 0; u < kMergePerRound; ++u) {
       if (mq[u] == -INFINITY) continue;  // a segment with no visible key, or none at all
-      const float mn = fmaxf(M, mq[u]);
-      const float a = fast_exp2((M - mn) * p.c2), f = fast_exp2((mq[u] - mn) * p.c2);  // a = 0 first
-      M = mn;
-      L = L * a + f * lq[u];
-      O.x = O.x * a + f * ov[u].x; O.y = O.y * a + f * ov[u].y;
-      O.z = O.z * a + f * ov[u].z; O.w = O.w * a + f * ov[u].w;
+      const float f = fast_exp2((mq[u] - mn) * p.c2);
+      L += f * lq[u];
+      O.x += f * ov[u].x; O.y += f * ov[u].y; O.z += f * ov[u].z; O.w += f * ov[u].w;
     }
+    M = mn;
   }
   s_o[slice][d4] = O;
   if (d4 == 0) { s_m[slice] = M; s_l[slice] = L; }
@@ -1002,11 +1014,11 @@ __global__ void __launch_bounds__(256, 4) merge_kernel(const MergeParams p) {
   if (slice == 0) {
     float Mt = s_m[0];
 #pragma unroll
-    for (int j = 1; j < 8; ++j) Mt = fmaxf(Mt, s_m[j]);
+    for (int j = 1; j < kMergeSlices; ++j) Mt = fmaxf(Mt, s_m[j]);
     float Lt = 0.f;
     float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kMergeSlices; ++j) {
       if (s_m[j] == -INFINITY) continue;
       const float f = fast_exp2((s_m[j] - Mt) * p.c2);
       const float4 v = s_o[j][d4];
@@ -1112,7 +1124,7 @@ cudaError_t launch_split_merge(const void* groups, const int32_t* split_groups,
   mp.out = out; mp.Hq = Hq; mp.Hkv = Hkv; mp.G = G; mp.q_len = q_len; mp.c2 = c2;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)num_split, (unsigned)(Hkv * kRows));
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(32 * kMergeSlices);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
