@@ -1029,7 +1029,8 @@ __global__ void __launch_bounds__(32 * kMergeSlices, 2) merge_kernel(const Merge
       const int tok = r / p.G, qh = h * p.G + r % p.G;
       float4* dst = reinterpret_cast<float4*>(
           p.out + (((int64_t)g0.x * p.q_len + tok) * p.Hq + qh) * 128 + 4 * d4);
-      *dst = make_float4(Ot.x / Lt, Ot.y / Lt, Ot.z / Lt, Ot.w / Lt);
+      const float inv = 1.f / Lt;
+      *dst = make_float4(Ot.x * inv, Ot.y * inv, Ot.z * inv, Ot.w * inv);
     }
   }
 }

@@ -163,6 +163,11 @@ __device__ void t_producer(const TileParams& p, uint8_t* smem, int lane) {
   const uint32_t bars = sbase + kTOffBars;
   volatile int32_t* stage_pid = reinterpret_cast<volatile int32_t*>(smem + kTOffPid);
   const int64_t blk = (int64_t)p.Hkv * 9216;
+  // with one row tile per (sequence, KV head) (verify) a page is read once per call: marked first
+  // for eviction it leaves the L2 to the split-K partials the merge reads next; with several tiles
+  // per head (a prefill chunk) the other tiles read the same pages, so they are kept as usual
+  const uint64_t policy =
+      p.G * p.q_len <= kTRows ? l2_evict_first_policy() : l2_evict_normal_policy();
   uint32_t k = 0;
   bool to = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
@@ -201,10 +206,10 @@ __device__ void t_producer(const TileParams& p, uint8_t* smem, int lane) {
             for (int q = 0; q < 2; ++q) {
               if (!(q == 0 ? v0 : v1)) continue;
               const uint8_t* src = p.pool + (int64_t)(q == 0 ? pid0 : pid1) * blk;
-              bulk_g2s(dst + kStK + q * 4096, src + offK, 4096u, full);
-              bulk_g2s(dst + kStKs + q * 1024, src + offKs, ksb, full);
-              bulk_g2s(dst + kStV + q * 4096, src + offV, 4096u, full);
-              bulk_g2s(dst + kStVs + q * 512, src + offVs, 512u, full);
+              bulk_g2s_hint(dst + kStK + q * 4096, src + offK, 4096u, full, policy);
+              bulk_g2s_hint(dst + kStKs + q * 1024, src + offKs, ksb, full, policy);
+              bulk_g2s_hint(dst + kStV + q * 4096, src + offV, 4096u, full, policy);
+              bulk_g2s_hint(dst + kStVs + q * 512, src + offVs, 512u, full, policy);
             }
           } else {
             mbar_arrive(full);
@@ -721,9 +726,12 @@ struct TMergeParams {
   float c2;
 };
 
-__global__ void __launch_bounds__(256) tile_merge_kernel(const TMergeParams p) {
-  __shared__ float s_m[8], s_l[8];
-  __shared__ float4 s_o[8][32];
+constexpr int kTMergeSlices = 8;
+constexpr int kTMergePerRound = 8;  // partials a slice requests at once (64 per CTA and round)
+
+__global__ void __launch_bounds__(32 * kTMergeSlices, 2) tile_merge_kernel(const TMergeParams p) {
+  __shared__ float s_m[kTMergeSlices], s_l[kTMergeSlices];
+  __shared__ float4 s_o[kTMergeSlices][32];
   asm volatile("griddepcontrol.launch_dependents;");
   const int gi = p.split[blockIdx.x];  // plan tables: written before the attention launch
   const int i = blockIdx.y;
@@ -735,21 +743,41 @@ __global__ void __launch_bounds__(256) tile_merge_kernel(const TMergeParams p) {
   const int n_seg = g1.x;
   const int slice = threadIdx.x >> 5, d4 = threadIdx.x & 31;
   const float* base = p.partials + (int64_t)g1.y * kTPartFloats;
+  // per round a slice requests its partials q = q0 + 8 u (u < 8) at once (one L2 round trip for a
+  // group of up to 64 segments) and combines them with independent weights
   float M = -INFINITY, L = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int q = slice; q < n_seg; q += 8) {
-    const float* pq = base + (int64_t)q * kTPartFloats;
-    const float mq = __ldcg(pq + kTRows * 128 + i);
-    const float lq = __ldcg(pq + kTRows * 128 + kTRows + i);
-    const float4 ov = __ldcg(reinterpret_cast<const float4*>(pq + i * 128) + d4);
-    if (mq == -INFINITY) continue;  // a segment with no visible key for this row
-    const float mn = fmaxf(M, mq);
-    const float a = fast_exp2((M - mn) * p.c2), f = fast_exp2((mq - mn) * p.c2);
+  for (int q0 = slice; q0 < n_seg; q0 += kTMergeSlices * kTMergePerRound) {
+    float mq[kTMergePerRound], lq[kTMergePerRound];
+    float4 ov[kTMergePerRound];
+#pragma unroll
+    for (int u = 0; u < kTMergePerRound; ++u) {
+      const int q = q0 + kTMergeSlices * u;
+      mq[u] = -INFINITY;
+      lq[u] = 0.f;
+      ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (q < n_seg) {
+        const float* pq = base + (int64_t)q * kTPartFloats;
+        mq[u] = __ldcg(pq + kTRows * 128 + i);
+        lq[u] = __ldcg(pq + kTRows * 128 + kTRows + i);
+        ov[u] = __ldcg(reinterpret_cast<const float4*>(pq + i * 128) + d4);
+      }
+    }
+    float mn = M;
+#pragma unroll
+    for (int u = 0; u < kTMergePerRound; ++u) mn = fmaxf(mn, mq[u]);
+    if (mn == -INFINITY) continue;  // no visible key for this row in any partial so far
+    const float a = fast_exp2((M - mn) * p.c2);  // 0 while M is -inf
+    L *= a;
+    O.x *= a; O.y *= a; O.z *= a; O.w *= a;
+#pragma unroll
+    for (int u = 0; u < kTMergePerRound; ++u) {
+      if (mq[u] == -INFINITY) continue;  // a segment with no visible key for this row
+      const float f = fast_exp2((mq[u] - mn) * p.c2);
+      L += f * lq[u];
+      O.x += f * ov[u].x; O.y += f * ov[u].y; O.z += f * ov[u].z; O.w += f * ov[u].w;
+    }
     M = mn;
-    L = L * a + f * lq;
-    O.x = O.x * a + f * ov.x; O.y = O.y * a + f * ov.y;
-    O.z = O.z * a + f * ov.z; O.w = O.w * a + f * ov.w;
   }
   s_o[slice][d4] = O;
   if (d4 == 0) { s_m[slice] = M; s_l[slice] = L; }
@@ -757,11 +785,11 @@ __global__ void __launch_bounds__(256) tile_merge_kernel(const TMergeParams p) {
   if (slice == 0) {
     float Mt = s_m[0];
 #pragma unroll
-    for (int j = 1; j < 8; ++j) Mt = fmaxf(Mt, s_m[j]);
+    for (int j = 1; j < kTMergeSlices; ++j) Mt = fmaxf(Mt, s_m[j]);
     float Lt = 0.f;
     float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kTMergeSlices; ++j) {
       if (s_m[j] == -INFINITY) continue;
       const float f = fast_exp2((s_m[j] - Mt) * p.c2);
       const float4 v = s_o[j][d4];
@@ -772,7 +800,8 @@ __global__ void __launch_bounds__(256) tile_merge_kernel(const TMergeParams p) {
       const int tok = r / p.G, qh = head * p.G + r % p.G;
       float4* dst = reinterpret_cast<float4*>(
           p.out + (((int64_t)g0.x * p.q_len + tok) * p.Hq + qh) * 128 + 4 * d4);
-      *dst = make_float4(Ot.x / Lt, Ot.y / Lt, Ot.z / Lt, Ot.w / Lt);
+      const float inv = 1.f / Lt;
+      *dst = make_float4(Ot.x * inv, Ot.y * inv, Ot.z * inv, Ot.w * inv);
     }
   }
 }
@@ -833,7 +862,7 @@ cudaError_t launch_tile(const uint8_t* q_codes, const uint8_t* q_scales, const u
   const int rows_total = p.G * q_len;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)num_split, (unsigned)(rows_total < kTRows ? rows_total : kTRows));
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(32 * kTMergeSlices);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
   cfg.attrs = attr;
