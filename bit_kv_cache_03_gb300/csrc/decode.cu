@@ -99,6 +99,7 @@ constexpr int kOffQsc = kOffTmemSlot + 16;   // fused append: Q scales [2 pairs]
 constexpr int kSmemBytes = kOffQsc + 2 * 16 * 8;
 static_assert(kStages <= 8, "stage page-id slots");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kOffQ % 16 == 0 && kOffQsc % 8 == 0, "Q tile 16-byte, Q scale rows 8-byte aligned");
 
 // TMEM columns
 constexpr uint32_t kColS = 0;                 // [kSBufs][2 pairs][16]
@@ -275,7 +276,6 @@ __device__ void qk_warp(const DecodeParams& p, uint8_t* smem, uint32_t tbase, in
       if (lane == 0) mbar_arrive(bars + 8 * (kBarStageEmpty + st));
       ++ks;
     }
-    wait_bar(bars + 8 * kBarQReady, sgi & 1, timed_out);  // Q tile and its scales for this group
     for (int j = 0; j < sg.hi - sg.lo; ++j, ++k, ++ks) {
       const uint32_t st = ks % kStages, b = k % kSBufs;
       wait_bar(bars + 8 * (kBarStageFull + st), (ks / kStages) & 1, timed_out);
@@ -307,6 +307,15 @@ __device__ void qk_warp(const DecodeParams& p, uint8_t* smem, uint32_t tbase, in
                                      : stage + p.Hkv * 4096 + pr * 1024 + kh * 512;
             tmem_cp_32x128b_x4(tbase + kColSfa + b * 16 + pr * 8 + kh * 4, smem_desc(src, 16, 128));
           }
+      }
+      if (j == 0) {
+        // the segment's Q tile and its scales, awaited only now: the first page's K-scale copies
+        // above were issued while the attention warps encoded Q
+        __syncwarp();
+        wait_bar(bars + 8 * kBarQReady, sgi & 1, timed_out);
+      }
+      if (lane == 0) {
+        tc_fence_after();
         const uint32_t qb = sbase + kOffQ;
         for (int pr = 0; pr < npairs; ++pr) {
           for (int kh = 0; kh < 2; ++kh) {
@@ -322,6 +331,8 @@ __device__ void qk_warp(const DecodeParams& p, uint8_t* smem, uint32_t tbase, in
       }
       __syncwarp();
     }
+    // a segment without pages (the plan makes none) still consumes its Q-ready phase
+    if (sg.hi <= sg.lo) wait_bar(bars + 8 * kBarQReady, sgi & 1, timed_out);
   }
   if (timed_out) flag_status(p.status, KV_NVFP4_DEV_TIMEOUT);
 }
@@ -557,6 +568,7 @@ __device__ __forceinline__ void new_kv_store(const DecodeParams& p, const NewKvR
 // load takes about a microsecond, and the segment's first QK waits for this prologue). Inlined:
 // out of line, its reads of the kernel parameters and the segment record went through memory and
 // the prologue took about twice as long (a decode step of 4 x 128K tokens 1.8 us longer, measured).
+template <int NR>
 __device__ __forceinline__ void fused_prologue(const DecodeParams& p, const SegInfo& sg,
                                                uint8_t* smem, const uint8_t* slot, uint32_t sbase,
                                                uint32_t bars, int aw, int lane) {
@@ -564,16 +576,22 @@ __device__ __forceinline__ void fused_prologue(const DecodeParams& p, const SegI
   const int row0 = sg.rg * kRows;
   const bool q_out = p.q_codes_out != nullptr && (sg.n_seg == 1 || sg.part == sg.first_part);
   uint8_t* qsc = smem + kOffQsc;
-  const int pr = aw >> 2;
-  // tile rows 4 (aw % 4) .. + 3 of pair aw / 4
-  uint2 qraw[4];
-  float4 qc[4], qs[4];
-  int64_t qtrow[4];
-  int qstate[4];  // 0: padding row, 1: row past the RoPE table, 2: row to encode
+  // the tile's rows that can be real: NR per head, 4 NR over the two head pairs, R per warp (rows
+  // NR .. 7 of a head are never computed: their Q tile rows keep the zeros written at the start)
+  constexpr int R = NR / 2;
+  int nrows_of[R], pr_of[R];
+  uint2 qraw[R];
+  float4 qc[R], qs[R];
+  int64_t qtrow[R];
+  int qstate[R];  // 0: padding row, 1: row past the RoPE table, 2: row to encode
 #pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const int nrow = 4 * (aw & 3) + jj;
-    const int hh = 2 * pr + (nrow >> 3), r = row0 + (nrow & 7);
+  for (int jj = 0; jj < R; ++jj) {
+    const int rr = R * aw + jj;          // 0 .. 4 NR - 1
+    const int pr = rr / (2 * NR), hip = (rr % (2 * NR)) / NR;
+    const int nrow = 8 * hip + rr % NR;  // tile row of pair pr
+    nrows_of[jj] = nrow;
+    pr_of[jj] = pr;
+    const int hh = 2 * pr + hip, r = row0 + (nrow & 7);
     qraw[jj] = make_uint2(0u, 0u);
     qc[jj] = qs[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
     qtrow[jj] = 0;
@@ -599,21 +617,21 @@ __device__ __forceinline__ void fused_prologue(const DecodeParams& p, const SegI
   NewKvRow kv;
   if (aw < nrows) new_kv_fetch(p, sg, slot, aw, t0, lane, kv);
 
-  // the four rows in lockstep; a padding row or one past the RoPE table holds zeros and encodes
+  // the warp's rows in lockstep; a padding row or one past the RoPE table holds zeros and encodes
   // to zero codes and a zero scale
-  float qx[4][4];
+  float qx[R][4];
 #pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
+  for (int jj = 0; jj < R; ++jj) {
     qx[jj][0] = __uint_as_float(qraw[jj].x << 16);
     qx[jj][1] = __uint_as_float(qraw[jj].x & 0xFFFF0000u);
     qx[jj][2] = __uint_as_float(qraw[jj].y << 16);
     qx[jj][3] = __uint_as_float(qraw[jj].y & 0xFFFF0000u);
   }
-  uint32_t qpk[4], qsc4[4];
-  nvfp4_encode_rows<4>(qx, true, p.rot_dim > 0, qc, qs, p.rot_dim, lane, qpk, qsc4);
+  uint32_t qpk[R], qsc4[R];
+  nvfp4_encode_rows<R>(qx, true, p.rot_dim > 0, qc, qs, p.rot_dim, lane, qpk, qsc4);
 #pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const int nrow = 4 * (aw & 3) + jj;
+  for (int jj = 0; jj < R; ++jj) {
+    const int nrow = nrows_of[jj], pr = pr_of[jj];
     if (qstate[jj] == 2 && q_out) {
       *reinterpret_cast<uint16_t*>(p.q_codes_out + qtrow[jj] * kCodeBytes + 2 * lane) =
           (uint16_t)qpk[jj];
@@ -696,7 +714,8 @@ __device__ void attention_warps(const DecodeParams& p, uint8_t* smem, uint32_t t
     if (FUSED) {
       const uint32_t st = ks % kStages;
       wait_bar(c.bars + 8 * (kBarStageFull + st), (ks / kStages) & 1, c.timed_out);
-      fused_prologue(p, sg, smem, smem + kOffStage + st * kStageBytes, c.sbase, c.bars, aw, lane);
+      fused_prologue<NR>(p, sg, smem, smem + kOffStage + st * kStageBytes, c.sbase, c.bars, aw,
+                         lane);
       if (lane == 0) mbar_arrive(c.bars + 8 * (kBarStageEmpty + st));  // slot read by this warp
       ++ks;
     } else if (c.gt < 64) {
@@ -890,6 +909,11 @@ __global__ void __launch_bounds__(kBoundThreads, 1) decode_kernel(const DecodePa
     fence_mbar_init();
   }
   if (warp == kWarpMma) tmem_alloc(smem_u32(smem + kOffTmemSlot), kTmemCols);
+  // the fused prologue writes only the rows that can be real: the others stay zero
+  for (int i = threadIdx.x; i < kQBytes / 16; i += kThreads)
+    sts128(smem_u32(smem + kOffQ) + 16 * i, 0u, 0u, 0u, 0u);
+  for (int i = threadIdx.x; i < 2 * 16; i += kThreads)  // 8-byte rows (the area is 8-aligned)
+    *reinterpret_cast<uint2*>(smem + kOffQsc + 8 * i) = make_uint2(0u, 0u);
   if (p.early_tables && lane == 0) {
     // bring this CTA's first segment record into L1 while the previous kernel finishes: every warp
     // starts by reading it, three dependent loads that otherwise take ~1.5 us under the page
