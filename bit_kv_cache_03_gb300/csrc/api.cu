@@ -369,6 +369,7 @@ static kv_nvfp4_status decode_step_impl(const kv_nvfp4_layout* L, const kv_nvfp4
       max_pages <= 0)
     return KV_NVFP4_EINVAL;
   if ((q_codes_out == nullptr) != (q_scales_out == nullptr)) return KV_NVFP4_EINVAL;
+  if (q_codes_out != nullptr && !aligned16(q_codes_out)) return KV_NVFP4_EINVAL;
   if (L->rot_dim > 0 && (!d_rope_table || rope_max_pos <= 0 || !aligned16(d_rope_table)))
     return KV_NVFP4_EINVAL;
   if ((int64_t)plan->max_seq_len > (int64_t)max_pages * L->page_size) return KV_NVFP4_EINVAL;

@@ -568,6 +568,94 @@ __device__ __forceinline__ void new_kv_store(const DecodeParams& p, const NewKvR
 // load takes about a microsecond, and the segment's first QK waits for this prologue). Inlined:
 // out of line, its reads of the kernel parameters and the segment record went through memory and
 // the prologue took about twice as long (a decode step of 4 x 128K tokens 1.8 us longer, measured).
+// One Q row encoded by eight threads (o = lane % 8 holds the row's 16-value block o: elements
+// 16 o .. 16 o + 15), from its bf16 values at `row` in shared memory: RoPE on the first rot dims
+// (the partner of a rotated value read back from the staged row, each product rounded on its own,
+// then added), the Hadamard stages 1 .. 8 in registers and 16, 32, 64 with lanes o ^ 1, o ^ 2,
+// o ^ 4, the normalisation, and NVFP4 of the thread's own block (its amax, scale and codes need
+// no exchange). Every step rounds as the definition states, so the codes and the scale equal those
+// of the warp-per-row encoder bit for bit. All 32 lanes must call it (the exchanges are warp-wide);
+// a lane with `load` false encodes zeros.
+__device__ __forceinline__ void encode_q_octet(uint32_t row, bool load, const float* trow, int rot,
+                                               int o, uint2& codes, uint32_t& scale) {
+  float x[16];
+  {
+    uint4 v0 = make_uint4(0u, 0u, 0u, 0u), v1 = v0;
+    if (load) {
+      v0 = lds128(row + 32 * o);
+      v1 = lds128(row + 32 * o + 16);
+    }
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      x[2 * e] = __uint_as_float(w[e] << 16);
+      x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+    }
+  }
+  if (load && trow != nullptr) {
+    const int half = rot >> 1;
+#pragma unroll
+    for (int k0 = 0; k0 < 16; k0 += 4) {
+      const int e0 = 16 * o + k0;  // dims e0 .. e0 + 3 (rot / 2 is a multiple of 4)
+      if (e0 < rot) {
+        const bool lower = e0 < half;
+        const int i0 = lower ? e0 : e0 - half;
+        const float4 c4 = *reinterpret_cast<const float4*>(trow + i0);
+        const float4 s4 = *reinterpret_cast<const float4*>(trow + half + i0);
+        const uint2 pb = lds64(row + 2 * (lower ? e0 + half : e0 - half));
+        const float part[4] = {__uint_as_float(pb.x << 16), __uint_as_float(pb.x & 0xFFFF0000u),
+                               __uint_as_float(pb.y << 16), __uint_as_float(pb.y & 0xFFFF0000u)};
+        const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+        const float ss[4] = {s4.x, s4.y, s4.z, s4.w};
+        const float sg = lower ? -1.0f : 1.0f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          x[k0 + e] = __fadd_rn(__fmul_rn(x[k0 + e], cc[e]), __fmul_rn(sg * part[e], ss[e]));
+      }
+    }
+  }
+#pragma unroll
+  for (int hs = 1; hs < 16; hs <<= 1) {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      if ((k & hs) == 0) {
+        const float a = x[k], b = x[k + hs];
+        x[k] = __fadd_rn(a, b);
+        x[k + hs] = __fsub_rn(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) {
+    // the lower element of a pair sits in the thread without bit m: it keeps a + b, the other
+    // a - b; (+-1) x is exact, so one fma rounds as the add or subtract does
+    const float sgn = (o & m) != 0 ? -1.0f : 1.0f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float other = __shfl_xor_sync(0xffffffffu, x[k], m);
+      x[k] = __fmaf_rn(sgn, x[k], other);
+    }
+  }
+  const float kNorm = __uint_as_float(0x3DB504F3u);  // rn(2^-3.5) = rn(1/sqrt(128))
+  float amax = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    x[k] = __fmul_rn(x[k], kNorm);
+    amax = fmaxf(amax, fabsf(x[k]));
+  }
+  const float r6 = __frcp_rn(6.0f);
+  scale = e4m3x2_from_f32(0.0f, div_rn_by(amax, 6.0f, r6)) & 0xFFu;
+  const float sd = e4m3_decode_pos(scale);
+  const float rs = __frcp_rn(sd);
+  float q[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) q[k] = quot_rn(x[k], sd, rs);
+  const float(&q0)[8] = *reinterpret_cast<const float(*)[8]>(&q[0]);
+  const float(&q1)[8] = *reinterpret_cast<const float(*)[8]>(&q[8]);
+  codes = sd != 0.0f ? make_uint2(e2m1x8_from_f32(q0), e2m1x8_from_f32(q1))
+                     : make_uint2(0u, 0u);  // an all-zero block: zero scale, zero codes
+}
+
 template <int NR>
 __device__ __forceinline__ void fused_prologue(const DecodeParams& p, const SegInfo& sg,
                                                uint8_t* smem, const uint8_t* slot, uint32_t sbase,
@@ -576,74 +664,52 @@ __device__ __forceinline__ void fused_prologue(const DecodeParams& p, const SegI
   const int row0 = sg.rg * kRows;
   const bool q_out = p.q_codes_out != nullptr && (sg.n_seg == 1 || sg.part == sg.first_part);
   uint8_t* qsc = smem + kOffQsc;
-  // the tile's rows that can be real: NR per head, 4 NR over the two head pairs, R per warp (rows
-  // NR .. 7 of a head are never computed: their Q tile rows keep the zeros written at the start)
-  constexpr int R = NR / 2;
-  int nrows_of[R], pr_of[R];
-  uint2 qraw[R];
-  float4 qc[R], qs[R];
-  int64_t qtrow[R];
-  int qstate[R];  // 0: padding row, 1: row past the RoPE table, 2: row to encode
-#pragma unroll
-  for (int jj = 0; jj < R; ++jj) {
-    const int rr = R * aw + jj;          // 0 .. 4 NR - 1
-    const int pr = rr / (2 * NR), hip = (rr % (2 * NR)) / NR;
-    const int nrow = 8 * hip + rr % NR;  // tile row of pair pr
-    nrows_of[jj] = nrow;
-    pr_of[jj] = pr;
-    const int hh = 2 * pr + hip, r = row0 + (nrow & 7);
-    qraw[jj] = make_uint2(0u, 0u);
-    qc[jj] = qs[jj] = make_float4(0.f, 0.f, 0.f, 0.f);
-    qtrow[jj] = 0;
-    qstate[jj] = 0;
-    if (hh < p.Hkv && r < rows_total) {  // warp-uniform
-      const int tok = r / p.G, qh = hh * p.G + r % p.G;
-      qtrow[jj] = ((int64_t)sg.seq * p.q_len + tok) * p.Hq + qh;
-      const int pos = sg.len - p.q_len + tok;
-      const bool rope_ok = p.rot_dim == 0 || pos < p.rope_max_pos;
-      qstate[jj] = rope_ok ? 2 : 1;
-      if (rope_ok) {
-        qraw[jj] = *reinterpret_cast<const uint2*>(slot + kStepQ + (tok * p.Hq + qh) * 256 + 8 * lane);
-        rope_fetch(p.rot_dim > 0 ? reinterpret_cast<const float*>(slot + kStepRope) + tok * p.rot_dim
-                                 : nullptr,
-                   p.rot_dim, lane, qc[jj], qs[jj]);
-      }
-    }
-  }
   // the step's new K and V rows on this segment's pages; the first one of this warp fetched now
+  // (its page id is a global load), stored after the Q rows are encoded
   const int first_pos = sg.len - p.q_len;
   const int t0 = max(0, sg.lo * kPage - first_pos), t1 = min(p.q_len, sg.hi * kPage - first_pos);
   const int nrows = t1 > t0 ? (t1 - t0) * 2 * p.Hkv : 0;
   NewKvRow kv;
   if (aw < nrows) new_kv_fetch(p, sg, slot, aw, t0, lane, kv);
-
-  // the warp's rows in lockstep; a padding row or one past the RoPE table holds zeros and encodes
-  // to zero codes and a zero scale
-  float qx[R][4];
-#pragma unroll
-  for (int jj = 0; jj < R; ++jj) {
-    qx[jj][0] = __uint_as_float(qraw[jj].x << 16);
-    qx[jj][1] = __uint_as_float(qraw[jj].x & 0xFFFF0000u);
-    qx[jj][2] = __uint_as_float(qraw[jj].y << 16);
-    qx[jj][3] = __uint_as_float(qraw[jj].y & 0xFFFF0000u);
-  }
-  uint32_t qpk[R], qsc4[R];
-  nvfp4_encode_rows<R>(qx, true, p.rot_dim > 0, qc, qs, p.rot_dim, lane, qpk, qsc4);
-#pragma unroll
-  for (int jj = 0; jj < R; ++jj) {
-    const int nrow = nrows_of[jj], pr = pr_of[jj];
-    if (qstate[jj] == 2 && q_out) {
-      *reinterpret_cast<uint16_t*>(p.q_codes_out + qtrow[jj] * kCodeBytes + 2 * lane) =
-          (uint16_t)qpk[jj];
-      if ((lane & 3) == 0) p.q_scales_out[qtrow[jj] * kScaleBytes + (lane >> 2)] = (uint8_t)qsc4[jj];
-    } else if (qstate[jj] == 1) {  // a position past the RoPE table: flagged, the row scores zero
-      if (lane == 0) flag_status(p.status, KV_NVFP4_DEV_BAD_ROPE);
+  // The tile rows that can be real, NR per head (4 NR over the two head pairs), eight threads per
+  // row and four rows per warp: row rr = 4 aw + lane / 8. Rows NR .. 7 of a head are never
+  // computed; their Q tile rows keep the zeros written at the start.
+  {
+    const int o = lane & 7;
+    const int rr = 4 * aw + (lane >> 3);
+    const bool tile_row = rr < 4 * NR;
+    const int pr = rr / (2 * NR), hip = (rr % (2 * NR)) / NR;
+    const int nrow = 8 * hip + rr % NR;  // tile row of pair pr
+    const int hh = 2 * pr + hip, r = row0 + (nrow & 7);
+    int state = 0;  // 0: padding row, 1: row past the RoPE table, 2: row to encode
+    int64_t qtrow = 0;
+    uint32_t rowaddr = 0;
+    const float* trow = nullptr;
+    if (tile_row && hh < p.Hkv && r < rows_total) {
+      const int tok = r / p.G, qh = hh * p.G + r % p.G;
+      qtrow = ((int64_t)sg.seq * p.q_len + tok) * p.Hq + qh;
+      const int pos = sg.len - p.q_len + tok;
+      state = (p.rot_dim == 0 || pos < p.rope_max_pos) ? 2 : 1;
+      rowaddr = smem_u32(slot) + kStepQ + (tok * p.Hq + qh) * 256;
+      if (p.rot_dim > 0) trow = reinterpret_cast<const float*>(slot + kStepRope) + tok * p.rot_dim;
     }
-    // tensor-core tile order: lane l's code bytes 2l, 2l + 1 sit in 16-byte piece l / 8
-    sts16(sbase + kOffQ + pr * 1024 + (nrow >> 3) * 512 + (lane >> 3) * 128 + (nrow & 7) * 16 +
-              ((2 * lane) & 15),
-          qpk[jj]);
-    if ((lane & 3) == 0) qsc[(pr * 16 + nrow) * 8 + (lane >> 2)] = (uint8_t)qsc4[jj];
+    uint2 codes;
+    uint32_t scale;
+    encode_q_octet(rowaddr, state == 2, trow, p.rot_dim, o, codes, scale);
+    if (state == 2 && q_out) {
+      *reinterpret_cast<uint2*>(p.q_codes_out + qtrow * kCodeBytes + 8 * o) = codes;
+      p.q_scales_out[qtrow * kScaleBytes + o] = (uint8_t)scale;
+    } else if (state == 1 && o == 0) {  // a position past the RoPE table: flagged, scores zero
+      flag_status(p.status, KV_NVFP4_DEV_BAD_ROPE);
+    }
+    if (tile_row) {
+      // tensor-core tile order: the row's code bytes 8 o .. 8 o + 7 sit in 16-byte piece o / 2
+      const uint32_t a = sbase + kOffQ + pr * 1024 + (nrow >> 3) * 512 + (o >> 1) * 128 +
+                         (nrow & 7) * 16 + 8 * (o & 1);
+      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(codes.x), "r"(codes.y)
+                   : "memory");
+      qsc[(pr * 16 + nrow) * 8 + o] = (uint8_t)scale;
+    }
   }
   if (aw < nrows) new_kv_store(p, kv, lane);
 #pragma unroll 1

@@ -46,6 +46,29 @@ def test_fused_step_matches_two_calls_and_oracle(lens, q_len, Hq, Hkv, chunk):
     assert np.array_equal(a.output(), b.output()) and b.status() == 0
 
 
+@pytest.mark.parametrize("lens,q_len,Hq,Hkv,rot", [
+    ([300, 1200], 1, 24, 4, 64),    # rotary dims spread over four 16-value blocks of a row
+    ([500], 2, 8, 2, 128),          # every dim rotary
+    ([700, 90], 1, 24, 4, 0),       # no RoPE
+    ([900], 1, 12, 4, 48),          # a rotary width that ends inside a 16-value block
+])
+def test_fused_step_rotary_widths(lens, q_len, Hq, Hkv, rot):
+    w = synth.Workload("fused_rot", lens, q_len=q_len, seed=19 + rot, q_heads=Hq, kv_heads=Hkv,
+                       rot_dim=rot, chunk_tokens=128,
+                       pool_pages=sum((c + q_len + 63) // 64 for c in lens) + 2)
+    a, b = _pair(w, 128)
+    assert a.status() == 0 and b.status() == 0
+    o = OracleRun(w)
+    bad = compare_pool(b, o)
+    assert all(v == 0 for v in bad.values()), bad
+    qa, qb = a.q_quant(), b.q_quant()
+    assert np.array_equal(qa[0], qb[0]) and np.array_equal(qa[1], qb[1])
+    assert np.array_equal(qb[0], o.qc) and np.array_equal(qb[1], o.qs)
+    assert np.array_equal(a.output(), b.output())
+    max_abs, rel = attention_errors(b.output(), o.attention().reshape(b.output().shape))
+    assert max_abs <= MAX_ABS_TOL and rel <= REL_L2_TOL, (max_abs, rel)
+
+
 def test_fused_step_rejects_more_than_one_row_tile():
     import bit_kv_cache_03_gb300 as kv
     w = synth.Workload("fused_bad", [500], q_len=2, seed=3, chunk_tokens=256)  # 2 x GQA 6 = 12 rows
