@@ -245,7 +245,7 @@ kv_nvfp4_status kv_nvfp4_decode_attn(const kv_nvfp4_layout *layout,
  *              row s * q_len + i is new token i of sequence s, at position seq_len_s - q_len + i
  *   d_rope_table, rope_max_pos, d_block_table, max_pages, num_pages, pool: as for the append
  *   q_codes_out, q_scales_out: optional (both or neither) DEVICE copy of the encoded Q rows,
- *              [num_seqs * q_len][num_q_heads][64 | 8]
+ *              [num_seqs * q_len][num_q_heads][64 | 8] (q_codes_out 16-byte aligned, else EINVAL)
  *   sm_scale, out, d_status: as for kv_nvfp4_decode_attn
  * Requires (num_q_heads / num_kv_heads) * q_len <= 8 and num_kv_heads <= 4 (one 8-row tile per
  * sequence on the decode kernel: decode with GQA groups up to 8); larger verify or prefill steps,
