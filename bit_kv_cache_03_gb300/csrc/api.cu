@@ -65,6 +65,7 @@ constexpr int kPartHeadFloats = kRowsPerItem * 128 + 2 * kRowsPerItem;  // O[8][
 // KV head and 128 rows, one partial (O, m, l of the tile's rows) per segment.
 constexpr int kTileRows = 128;
 constexpr int kTailCharge = 2;    // extra pages charged for a decode group's last page
+constexpr int kTileSegCharge = 10;  // pages charged for each segment of the tile kernel
 constexpr int kTilePartFloats = kTileRows * 128 + 2 * kTileRows;
 
 constexpr int kMaxAttnKvHeads = 4;  // the decode kernel stages every head of a page
@@ -106,7 +107,12 @@ uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 // dealt out to `grid` CTAs in contiguous ranges of about total_pages / grid pages each. For the
 // decode kernel a group's last page is charged kTailCharge pages more: in the fused decode step
 // the CTA holding it also encodes and stores the step's new K/V rows (measured ~1-2 us, two
-// pages' time), so it gets that many fewer pages.
+// pages' time), so it gets that many fewer pages. For the tile kernel each segment costs
+// kTileSegCharge pages on top of its pages (its Q load, pipeline start and epilogue take ~5 us,
+// about ten pages' time): a CTA whose range crosses a group boundary runs two segments, and with
+// page-balanced ranges such CTAs ended ~7 us after the median one on the verify workload. The
+// tile plan therefore takes the smallest per-CTA cost cap for which a greedy fill of the chunk
+// stream needs at most `grid` CTAs (a binary search, each probe linear in the groups).
 struct PlanBuild {
   kv_nvfp4_plan_info info;
   std::vector<int32_t> groups;    // 8 ints per group
@@ -114,6 +120,49 @@ struct PlanBuild {
   std::vector<int32_t> cta_seg;   // grid + 1
   std::vector<int32_t> split;     // indices of the groups with more than one segment
 };
+
+// Greedy fill of the chunk stream (groups in order, each cut into chunks of chunk_pages, a
+// group's last chunk possibly shorter) into CTAs of cost at most cap, a segment costing charge
+// plus its pages. Returns the CTAs needed (INT64_MAX when one chunk and a charge exceed the cap);
+// with `out` it also records the segments {group, lo, hi} and each CTA's first segment.
+static int64_t tile_fill(const std::vector<int32_t>& gpages, int32_t chunk_pages, int64_t charge,
+                         int64_t cap, std::vector<int32_t>* segs, std::vector<int32_t>* cta_first) {
+  int64_t ctas = 1, used = 0;
+  if (cta_first) cta_first->assign(1, 0);
+  for (size_t gi = 0; gi < gpages.size(); ++gi) {
+    const int32_t pages = gpages[gi];
+    int32_t lo = 0;
+    while (lo < pages) {
+      const int64_t first = std::min<int64_t>(chunk_pages, pages - lo);
+      if (used + charge + first > cap) {
+        if (used == 0) return INT64_MAX;  // a chunk and its charge alone exceed the cap
+        ++ctas;
+        used = 0;
+        if (cta_first) cta_first->push_back((int32_t)(segs->size() / 4));
+      }
+      used += charge;
+      const int64_t room = cap - used;
+      int64_t take = (int64_t)(pages - lo) <= room ? (int64_t)(pages - lo)
+                                                  : room / chunk_pages * chunk_pages;
+      if (take < first) take = first;
+      const int32_t hi = lo + (int32_t)take;
+      used += take;
+      if (segs) {
+        segs->push_back((int32_t)gi);
+        segs->push_back(lo);
+        segs->push_back(hi);
+        segs->push_back(-1);
+      }
+      lo = hi;
+      if (lo < pages) {  // the CTA is full: the group continues on the next one
+        ++ctas;
+        used = 0;
+        if (cta_first) cta_first->push_back((int32_t)(segs->size() / 4));
+      }
+    }
+  }
+  return ctas;
+}
 
 kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, int32_t num_seqs,
                            int32_t q_len, int32_t causal, int32_t chunk_tokens, int32_t num_sms,
@@ -157,9 +206,27 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
   pb->segments.clear();
   pb->cta_seg.assign((size_t)grid + 1, 0);
   std::vector<int32_t> seg_count((size_t)n_groups, 0);
+  if (tile) {
+    // the smallest cost cap whose greedy fill needs at most `grid` CTAs
+    const int64_t charge = kTileSegCharge;
+    int64_t lo_cap = (total_pages + charge * grid + grid - 1) / grid;
+    int64_t hi_cap = lo_cap;
+    while (tile_fill(gpages, chunk_pages, charge, hi_cap, nullptr, nullptr) > grid) hi_cap *= 2;
+    while (lo_cap < hi_cap) {
+      const int64_t mid = lo_cap + (hi_cap - lo_cap) / 2;
+      if (tile_fill(gpages, chunk_pages, charge, mid, nullptr, nullptr) <= grid) hi_cap = mid;
+      else lo_cap = mid + 1;
+    }
+    std::vector<int32_t> first;
+    tile_fill(gpages, chunk_pages, charge, hi_cap, &pb->segments, &first);
+    for (size_t c = 0; c < first.size() && c <= (size_t)grid; ++c) pb->cta_seg[c] = first[c];
+    const int32_t nseg_t = (int32_t)(pb->segments.size() / 4);
+    for (size_t c = first.size(); c <= (size_t)grid; ++c) pb->cta_seg[c] = nseg_t;
+    for (int32_t si = 0; si < nseg_t; ++si) seg_count[(size_t)pb->segments[(size_t)si * 4]] += 1;
+  }
   // deal chunks to CTAs: CTA c closes once the pages dealt so far reach (c+1) * total / grid
   int64_t cta = 0, dealt = 0;
-  for (int64_t gi = 0; gi < n_groups; ++gi) {
+  for (int64_t gi = 0; !tile && gi < n_groups; ++gi) {
     const int32_t pages = gpages[(size_t)gi];
     int32_t lo = 0;
     while (lo < pages) {
@@ -185,7 +252,8 @@ kv_nvfp4_status plan_build(const kv_nvfp4_layout* L, const int32_t* h_seq_lens, 
     }
   }
   const int64_t n_seg = (int64_t)pb->segments.size() / 4;
-  for (int64_t c = cta + 1; c <= grid; ++c) pb->cta_seg[(size_t)c] = (int32_t)n_seg;
+  if (!tile)
+    for (int64_t c = cta + 1; c <= grid; ++c) pb->cta_seg[(size_t)c] = (int32_t)n_seg;
   // partial slots, contiguous per group in segment order; the split groups, in group order, are
   // the work list of the merge launch
   int64_t parts = 0;
