@@ -85,8 +85,12 @@ constexpr int kTOffQ = kTOffStage + kTStages * kTStageBytes;  // [128 rows][64 B
 constexpr int kTOffVt = kTOffQ + 8192;                         // [2] V tiles
 constexpr int kTOffSfk = kTOffVt + 2 * kVtBytes;               // [kTStages][2 k-halves][512 B]
 constexpr int kTOffQsc = kTOffSfk + kTStages * 1024;           // Q scales [128 rows][8]
-constexpr int kTOffRed = kTOffQsc + 128 * 8;                   // [2 parities][2 halves][128] f32
-constexpr int kTOffBars = kTOffRed + 2 * 2 * 128 * 4;
+// row maxima of the softmax warps: [2 parities][2 halves][128 rows] f32, or in split-page mode
+// [2 parities][4 warps][64 rows]
+constexpr int kTOffRed = kTOffQsc + 128 * 8;
+constexpr int kTOffXch = kTOffRed + 2 * 2 * 128 * 4;           // split-page epilogue: O, l of 64 rows
+constexpr int kTXchOBytes = 64 * 128 * 4;
+constexpr int kTOffBars = kTOffXch + kTXchOBytes + 64 * 4;
 // barrier indices
 constexpr int kTbStageFull = 0;
 constexpr int kTbStageEmpty = kTbStageFull + kTStages;
@@ -101,6 +105,7 @@ constexpr int kTOffPid = kTOffBars + kTNumBars * 8;            // [kTStages][2] 
 constexpr int kTOffTmemSlot = kTOffPid + kTStages * 2 * 4;
 constexpr int kTSmemBytes = kTOffTmemSlot + 16;
 static_assert(kTSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kTOffXch % 16 == 0, "16-byte accesses of the exchange area");
 
 // TMEM columns
 constexpr uint32_t kTColS = 0;      // [2 buffers][128 keys]; P (f16 pairs) at 0..31 and 64..95
@@ -309,11 +314,13 @@ __device__ void t_mma_qk(const TileParams& p, uint8_t* smem, uint32_t tbase, int
 }
 
 // P.V of block kb: eight MMAs (16 keys each) into O; A = P in the S buffer (keys 0..63 in
-// columns 0..31, keys 64..127 in columns 64..95).
+// columns 0..31, keys 64..127 in columns 64..95; in split-page mode keys 32 i .. 32 i + 31 in
+// columns 32 i .. 32 i + 15).
 __device__ void t_mma_pv(const TileParams& p, uint8_t* smem, uint32_t tbase, int lane) {
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kTOffBars;
   const uint64_t dv = smem_desc(sbase + kTOffVt, kVtGroupBytes, 128);
+  const bool dup = p.G * p.q_len <= kTRows / 2;  // split-page mode (see the softmax warps)
   uint32_t kb = 0, sgi = 0;
   bool to = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
@@ -327,9 +334,12 @@ __device__ void t_mma_pv(const TileParams& p, uint8_t* smem, uint32_t tbase, int
         tc_fence_after();
         const uint64_t bd = desc_add(dv, b * kVtBytes);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_f16_ts(tbase + kTColO, tbase + kTColS + b * 128 + 64 * (ks >> 2) + 8 * (ks & 3),
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t acol = dup ? 64 * (ks >> 2) + 32 * ((ks >> 1) & 1) + 8 * (ks & 1)
+                                    : 64 * (ks >> 2) + 8 * (ks & 3);
+          mma_f16_ts(tbase + kTColO, tbase + kTColS + b * 128 + acol,
                      desc_add(bd, ks * 2 * kVtGroupBytes), kIdescPV, (j == 0 && ks == 0) ? 0u : 1u);
+        }
         mma_commit(tbar(bars, kTbPvDone + b));
       }
       __syncwarp();
@@ -414,16 +424,24 @@ __device__ void t_dequant(const TileParams& p, uint8_t* smem, int warp, int lane
 }
 
 // --------------------------------------------------------------------------------------------
-// Softmax warps. Thread (quadrant q, lane) owns tile row r = 32 q + lane (tensor-memory lane r of
-// S and O); warp half h takes keys 64 h .. 64 h + 63 of each block and dims 64 h .. 64 h + 63 of O.
+// Softmax warps. A tile of more than 64 query rows: thread (quadrant q, lane) owns tile row
+// r = 32 q + lane (tensor-memory lane r of S and O); warp half h takes page h of each block (keys
+// 64 h .. 64 h + 63) and dims 64 h .. 64 h + 63 of O. A tile of at most 64 rows (split-page mode,
+// kDup): tile rows 64..127 repeat rows 0..63, so that every lane quadrant holds scores and the
+// exponentials of a block are spread over the four SM sub-partitions (warp w runs on
+// sub-partition w mod 4, and only it reads lane quadrant w mod 4). Quadrants 0, 1 take page 0 of
+// each block and quadrants 2, 3 page 1, warp half h keys 32 h .. 32 h + 31 of the page; lane r of
+// P holds the row's P over its page and zeros over the other, so the P.V accumulates the row's
+// sums over page 0 in lanes 0..63 of O and over page 1 in lanes 64..127, which the epilogue adds.
 // --------------------------------------------------------------------------------------------
 // The segment's Q tile (loaded by the four warps of half 0): codes into the A operand tile (tile
 // order), scales into tensor memory in the replicated scale-factor layout (lane i, column w of a
 // k-half: scales of rows 32 w + i).
+template <bool kDup>
 __device__ __forceinline__ void t_load_q(const TileParams& p, const TSeg& sg, uint8_t* smem,
                                          uint32_t sbase, uint32_t tbase, uint32_t lane_base, int r,
                                          int lane) {
-  const int gr = sg.rg * kTRows + r;
+  const int gr = sg.rg * kTRows + (kDup ? (r & 63) : r);
   uint4 c[4];
   uint2 sc = make_uint2(0u, 0u);
 #pragma unroll
@@ -477,14 +495,22 @@ __device__ __forceinline__ void t_scale_o32(uint32_t taddr, float alpha) {
   tmem_st32(taddr, o);
 }
 
+template <bool kDup>
 __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, int warp,
                           int lane) {
+  constexpr int kNc = kDup ? 32 : 64;  // keys of each block that one warp takes
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + kTOffBars;
   float* red = reinterpret_cast<float*>(smem + kTOffRed);
   const int q = warp & 3;
   const int h = (warp - kTWarpSoft0) >> 2;
-  const int r = 32 * q + lane;
+  const int r = 32 * q + lane;              // tensor-memory lane
+  const int rr = kDup ? (r & 63) : r;       // tile row
+  const int pg = kDup ? (q >> 1) : h;       // page of each block that this warp takes
+  const int kofs = kDup ? 32 * h : 0;       // its first key within the page
+  // the warps that share this thread's row: the quadrant's pair, or (kDup) the two pairs
+  const uint32_t nb_row = kDup ? kNbPair + (q & 1) : kNbPair + q;
+  constexpr uint32_t kRowThreads = kDup ? 128 : 64;
   const uint32_t lane_base = (uint32_t)(32 * q) << 16;
   const uint32_t ocol = tbase + lane_base + kTColO;
   const float c2 = p.c2;
@@ -493,17 +519,17 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
   bool to = false;
   const int s_begin = p.cta_seg[blockIdx.x], s_end = p.cta_seg[blockIdx.x + 1];
   if (h == 0 && s_begin < s_end) {
-    t_load_q(p, t_load_seg(p, s_begin), smem, sbase, tbase, lane_base, r, lane);
+    t_load_q<kDup>(p, t_load_seg(p, s_begin), smem, sbase, tbase, lane_base, r, lane);
     if (lane == 0) mbar_arrive(tbar(bars, kTbQReady));
   }
   for (int s = s_begin; s < s_end; ++s, ++sgi) {
     const TSeg sg = t_load_seg(p, s);
     const int n = seg_blocks(sg);
-    const int gr = sg.rg * kTRows + r;
+    const int gr = sg.rg * kTRows + rr;
     const bool row_ok = gr < rows_total;
     // a quadrant whose 32 rows are all padding computes nothing (its two warps still take part
     // in every mbarrier); its rows of P and O are never read into a result
-    const bool warp_live = sg.rg * kTRows + 32 * q < rows_total;
+    const bool warp_live = sg.rg * kTRows + (rr & ~31) < rows_total;
     // largest visible key position of this row (-1: no key)
     const int limit = row_ok ? (p.causal ? sg.len - p.q_len + gr / p.G : sg.len - 1) : -1;
     float m = -INFINITY;
@@ -511,10 +537,10 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
     // pool, as the producer skips it; the id is read from the block table one block ahead, so that
     // the block loop touches no shared-memory barrier but the S-full and P-full ones
     const int32_t* bt = p.block_table + (int64_t)sg.seq * p.max_pages;
-    int32_t pid_next = (sg.lo + h < sg.hi) ? __ldg(bt + sg.lo + h) : -1;
+    int32_t pid_next = (sg.lo + pg < sg.hi) ? __ldg(bt + sg.lo + pg) : -1;
     for (int j = 0; j < n; ++j, ++kb) {
       const uint32_t b = kb & 1u;
-      const int page = sg.lo + 2 * j + h;
+      const int page = sg.lo + 2 * j + pg;
       const int32_t pid = pid_next;
       const bool valid = page < sg.hi && pid >= 0 && pid < p.num_pages;
       if (page + 2 < sg.hi) pid_next = __ldg(bt + page + 2);
@@ -522,38 +548,48 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
       tc_fence_after();
       __syncwarp();
       if (warp_live) {
-        const uint32_t scol = tbase + lane_base + kTColS + b * 128 + 64 * h;
-        // keys c < nv of this warp's page are visible to this row; a padding row (no query) is
-        // left unmasked: its P and O are never read, and its scores are finite or its own
-        const int nv = !row_ok ? kPage : valid ? max(0, min(kPage, limit - page * kPage + 1)) : 0;
-        uint32_t sv[64];
-        ld32_at(scol, &sv[0]);
-        ld32_at(scol + 32, &sv[32]);
-        tmem_wait_ld_regs32(*reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_wait_ld_regs32(*reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        if (__any_sync(0xffffffffu, nv != kPage)) {
+        const uint32_t sbuf = tbase + lane_base + kTColS + b * 128;
+        const uint32_t scol = sbuf + 64 * pg + kofs;
+        // keys c < nv of this warp's share of its page are visible to this row; a padding row (no
+        // query) is left unmasked: its P and O are never read, and its scores are finite or its own
+        const int nv =
+            !row_ok ? kNc : valid ? max(0, min(kNc, limit - page * kPage - kofs + 1)) : 0;
+        uint32_t sv[kNc];
 #pragma unroll
-          for (int c = 0; c < 64; ++c) sv[c] = c < nv ? sv[c] : __float_as_uint(-INFINITY);
+        for (int c = 0; c < kNc; c += 32) ld32_at(scol + c, &sv[c]);
+#pragma unroll
+        for (int c = 0; c < kNc; c += 32)
+          tmem_wait_ld_regs32(*reinterpret_cast<uint32_t(*)[32]>(&sv[c]));
+        if (__any_sync(0xffffffffu, nv != kNc)) {
+#pragma unroll
+          for (int c = 0; c < kNc; ++c) sv[c] = c < nv ? sv[c] : __float_as_uint(-INFINITY);
         }
-        // this half's max of the row: eight chains of three-input maxima, then a tree
+        // this warp's max of the row: eight chains of three-input maxima, then a tree
         float mx[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sv[e]);
 #pragma unroll
-        for (int c = 8; c < 56; c += 16)
+        for (int c = 8; c < kNc - 8; c += 16)
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             mx[e] = fmax3(mx[e], __uint_as_float(sv[c + e]), __uint_as_float(sv[c + 8 + e]));
 #pragma unroll
-        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], __uint_as_float(sv[56 + e]));
+        for (int e = 0; e < 8; ++e) mx[e] = fmaxf(mx[e], __uint_as_float(sv[kNc - 8 + e]));
         float pmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
                            fmaxf(mx[6], mx[7]));
-        // the other half's max of the row (buffers alternate by block, so a slow partner still
-        // reads this block's value after this warp has moved on)
-        red[(b * 2 + h) * 128 + r] = pmax;
-        named_barrier_sync(kNbPair + q, 64);
-        pmax = fmaxf(pmax, red[(b * 2 + (h ^ 1)) * 128 + r]);
-        // both warps of the quadrant hold the same row maxima, so they take the same decisions
+        // the other warps' maxima of the row (buffers alternate by block, so a slow partner still
+        // reads this block's values after this warp has moved on)
+        if (kDup) {
+          red[(b * 4 + 2 * pg + h) * 64 + rr] = pmax;
+          named_barrier_sync(nb_row, kRowThreads);
+          const float* rb = red + b * 256 + rr;
+          pmax = fmaxf(fmax3(rb[0], rb[64], rb[128]), rb[192]);
+        } else {
+          red[(b * 2 + h) * 128 + r] = pmax;
+          named_barrier_sync(nb_row, kRowThreads);
+          pmax = fmaxf(pmax, red[(b * 2 + (h ^ 1)) * 128 + r]);
+        }
+        // every warp of the row holds the same row maxima, so they take the same decisions
         const float mc = fmaxf(m, pmax);
         float alpha = 1.f;
         bool need = false;
@@ -564,17 +600,24 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
           alpha = m == -INFINITY ? 0.f : fast_exp2((m - mc) * c2);
           m = mc;
         }
-        // P = exp2(s c2 - m c2) <= 2^15 in f16 pairs over the first 32 of this warp's columns; a
-        // masked key (-inf) gives 0, also while m is still -inf (then the offset is taken as 0)
+        // P = exp2(s c2 - m c2) <= 2^15 in f16 pairs over the first kNc / 2 of this warp's
+        // columns; a masked key (-inf) gives 0, also while m is still -inf (then the offset is
+        // taken as 0)
         const float mc2 = m == -INFINITY ? 0.f : m * c2;
-        uint32_t pk[32];
+        uint32_t pk[kNc / 2];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
+        for (int c = 0; c < kNc; c += 2) {
           const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), c2, -mc2));
           const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), c2, -mc2));
           pk[c >> 1] = pack_f16x2(p0, p1);
         }
-        tmem_st32(scol, pk);
+        if constexpr (kDup) {
+          tmem_st16(scol, pk);
+          // zeros over the same keys of the other page (columns no warp of this quadrant reads)
+          tmem_st16_zero(sbuf + 64 * (pg ^ 1) + kofs);
+        } else {
+          tmem_st32(scol, pk);
+        }
         // rows whose max was raised: this warp's half of their row of O (half 0 also l) is
         // rescaled once the previous block's P.V has completed (after the P stores, so that the
         // scores are no longer held); the loads and stores are warp-wide
@@ -601,48 +644,86 @@ __device__ void t_softmax(const TileParams& p, uint8_t* smem, uint32_t tbase, in
     // ---- segment end: the next segment's Q tile (every Q.K^T of this one is complete), then
     // the epilogue of this one ----
     if (h == 0 && s + 1 < s_end) {
-      t_load_q(p, t_load_seg(p, s + 1), smem, sbase, tbase, lane_base, r, lane);
+      t_load_q<kDup>(p, t_load_seg(p, s + 1), smem, sbase, tbase, lane_base, r, lane);
       if (lane == 0) mbar_arrive(tbar(bars, kTbQReady));
     }
     const uint32_t kl = kb - 1;
     wait_bar_sleep(tbar(bars, kTbPvDone + (kl & 1u)), (kl >> 1) & 1, to);
     tc_fence_after();
     const bool split = sg.n_seg > 1;
+    float4* xo = reinterpret_cast<float4*>(smem + kTOffXch);  // [32 dim quads][64 rows]
+    float* xl = reinterpret_cast<float*>(smem + kTOffXch + kTXchOBytes);
     if (warp_live) {
-      uint32_t o8[8];
-      tmem_ld8(ocol + 128, o8);
-      tmem_wait_ld_regs(o8);
-      const float l = __uint_as_float(o8[0]);  // the row's sum of P, accumulated by the P.V MMAs
-      float* part = split ? p.partials + (int64_t)sg.part * kTPartFloats : nullptr;
-      const int tok = gr / p.G, qh = sg.head * p.G + gr % p.G;
-      float* orow = p.out + (((int64_t)sg.seq * p.q_len + tok) * p.Hq + qh) * 128;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (kDup) {
+        // quadrants 2, 3 hand their rows' sums over page 1 (O and l) to quadrants 0, 1
+        if (q >= 2) {
 #pragma unroll 1
-      for (int cc = 2 * h; cc < 2 * h + 2; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(ocol + 32 * cc, o);
-        tmem_wait_ld_regs32(o);
-        if (row_ok) {
-          if (split) {
-            float4* dst = reinterpret_cast<float4*>(part + r * 128 + 32 * cc);
+          for (int cc = 2 * h; cc < 2 * h + 2; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(ocol + 32 * cc, o);
+            tmem_wait_ld_regs32(o);
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-              dst[e >> 2] = make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
-                                        __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
-          } else if (l > 0.f) {
-            float4* dst = reinterpret_cast<float4*>(orow + 32 * cc);
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              dst[e >> 2] = make_float4(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv,
-                                        __uint_as_float(o[e + 2]) * inv,
-                                        __uint_as_float(o[e + 3]) * inv);
+              xo[(cc * 8 + (e >> 2)) * 64 + rr] =
+                  make_float4(__uint_as_float(o[e]), __uint_as_float(o[e + 1]),
+                              __uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+          }
+          if (h == 0) {
+            uint32_t o8[8];
+            tmem_ld8(ocol + 128, o8);
+            tmem_wait_ld_regs(o8);
+            xl[rr] = __uint_as_float(o8[0]);
           }
         }
+        named_barrier_sync(nb_row, kRowThreads);
       }
-      if (row_ok && split && h == 0) {
-        part[kTRows * 128 + r] = m;
-        part[kTRows * 128 + kTRows + r] = l;
+      if (!kDup || q < 2) {
+        uint32_t o8[8];
+        tmem_ld8(ocol + 128, o8);
+        tmem_wait_ld_regs(o8);
+        // the row's sum of P, accumulated by the P.V MMAs
+        const float l = __uint_as_float(o8[0]) + (kDup ? xl[rr] : 0.f);
+        float* part = split ? p.partials + (int64_t)sg.part * kTPartFloats : nullptr;
+        const int tok = gr / p.G, qh = sg.head * p.G + gr % p.G;
+        float* orow = p.out + (((int64_t)sg.seq * p.q_len + tok) * p.Hq + qh) * 128;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+        for (int cc = 2 * h; cc < 2 * h + 2; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(ocol + 32 * cc, o);
+          tmem_wait_ld_regs32(o);
+          float ov[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __uint_as_float(o[e]);
+          if (kDup) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 x = xo[(cc * 8 + (e >> 2)) * 64 + rr];
+              ov[e] += x.x; ov[e + 1] += x.y; ov[e + 2] += x.z; ov[e + 3] += x.w;
+            }
+          }
+          if (row_ok) {
+            if (split) {
+              float4* dst = reinterpret_cast<float4*>(part + rr * 128 + 32 * cc);
+#pragma unroll
+              for (int e = 0; e < 32; e += 4)
+                dst[e >> 2] = make_float4(ov[e], ov[e + 1], ov[e + 2], ov[e + 3]);
+            } else if (l > 0.f) {
+              float4* dst = reinterpret_cast<float4*>(orow + 32 * cc);
+#pragma unroll
+              for (int e = 0; e < 32; e += 4)
+                dst[e >> 2] = make_float4(ov[e] * inv, ov[e + 1] * inv, ov[e + 2] * inv,
+                                          ov[e + 3] * inv);
+            }
+          }
+        }
+        if (row_ok && split && h == 0) {
+          part[kTRows * 128 + rr] = m;
+          part[kTRows * 128 + kTRows + rr] = l;
+        }
       }
+      // the exchange area is read before the next segment's epilogue rewrites it
+      if (kDup) named_barrier_sync(nb_row, kRowThreads);
     }
     tc_fence_before();
     __syncwarp();
@@ -689,7 +770,8 @@ __global__ void __launch_bounds__(kTThreads, 1) tile_kernel(const TileParams p) 
   } else if (warp == kTWarpMma) {
     t_mma_qk(p, smem, tbase, lane);
   } else if (warp >= kTWarpSoft0 && warp < kTWarpDeq0) {
-    t_softmax(p, smem, tbase, warp, lane);
+    if (p.G * p.q_len <= kTRows / 2) t_softmax<true>(p, smem, tbase, warp, lane);
+    else t_softmax<false>(p, smem, tbase, warp, lane);
   } else if (warp < kTWarpPv) {
     t_dequant(p, smem, warp, lane);
   } else {

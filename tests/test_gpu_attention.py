@@ -89,8 +89,8 @@ def test_attention_skips_bad_pages_and_flags_them():
     assert np.all(np.isfinite(g.output()))
 
 
-# More than 8 rows per KV head run on the tile kernel (64 rows of each head of a KV-head pair per
-# tile, both products on the tcgen05 tensor cores).
+# More than 8 rows per KV head run on the tile kernel (tiles of 128 query rows of one KV head, both
+# products on the tcgen05 tensor cores; tiles of at most 64 rows run in split-page mode).
 @pytest.mark.parametrize("lens,q_len,causal,chunk", [
     ([300, 2000], 16, True, 256),        # 96 rows: a full 64-row tile and a ragged one
     ([257, 1000], 12, False, 128),       # 72 rows, every key visible
@@ -104,7 +104,9 @@ def test_tile_kernel_shapes(lens, q_len, causal, chunk):
     _check(w, chunk=chunk, steps=2)
 
 
-@pytest.mark.parametrize("Hq,Hkv,q_len", [(8, 1, 5), (9, 3, 5), (16, 2, 3), (6, 3, 9), (12, 4, 4)])
+@pytest.mark.parametrize("Hq,Hkv,q_len", [(8, 1, 5), (9, 3, 5), (16, 2, 3), (6, 3, 9), (12, 4, 4),
+                                          (32, 4, 8),    # 64 rows: the largest split-page tile
+                                          (13, 1, 5)])   # 65 rows: the smallest full tile
 def test_tile_kernel_group_sizes(Hq, Hkv, q_len):
     # odd head counts leave the last pair with one head
     w = synth.Workload("tile_groups", [200, 1300], q_len=q_len, seed=Hq * 10 + Hkv, q_heads=Hq,
