@@ -97,6 +97,8 @@ def test_attention_skips_bad_pages_and_flags_them():
     ([3000], 256, True, 64),             # 1536 rows, 24 tiles per pair: many segments per CTA
     ([64, 65, 129], 2, True, 64),        # 12 rows; sequences ending on and just past a page
     ([4100], 11, True, 4160),            # one chunk per group: groups not split
+    ([4000] * 4, 8, True, 128),          # split-page mode (48 rows), many blocks and segments per CTA
+    ([3000, 1500], 8, False, 128),       # split-page mode, every key visible
 ])
 def test_tile_kernel_shapes(lens, q_len, causal, chunk):
     w = synth.Workload("tile", lens, q_len=q_len, causal=causal, seed=q_len * 7 + len(lens),
