@@ -24,8 +24,11 @@
 //     quadrant exchange their partial row maxima through shared memory. The running max m of a
 //     row is raised only when a block's max exceeds it by more than 2^15 in the exp2 domain (the
 //     warps then rescale their halves of the row of O in tensor memory), so P = exp2((s - m) c2)
-//     <= 2^15 fits f16 (largest finite value 65504). Each warp writes its 64 P values in f16 pairs over the first 32 of its own
-//     64 S columns, where the P.V product reads them as its A operand.
+//     <= 2^15 fits f16 (largest finite value 65504). Each warp writes its 64 P values in f16
+//     pairs over the first 32 of its own 64 S columns, where the P.V product reads them as its A
+//     operand. Tiles of at most 64 rows (speculative verify) run in split-page mode: the rows are
+//     repeated in lanes 64..127 and each lane set takes one page of the block, 32 keys per warp,
+//     so that the exponentials run on all four SM sub-partitions (see the softmax warps below).
 //   V: four warps dequantise the block's V rows (E2M1 x E4M3 is exact in f16), one key row per
 //     thread, into an MN-major f16 tile in shared memory.
 //   P.V: tcgen05.mma kind::f16, O[rows][dims] += P V with M = 128 rows (A = P in tensor memory),
