@@ -99,6 +99,8 @@ def test_attention_skips_bad_pages_and_flags_them():
     ([4100], 11, True, 4160),            # one chunk per group: groups not split
     ([4000] * 4, 8, True, 128),          # split-page mode (48 rows), many blocks and segments per CTA
     ([3000, 1500], 8, False, 128),       # split-page mode, every key visible
+    ([0, 1, 55, 56], 8, True, 128),      # split-page mode, one ragged page per sequence (no second page)
+    ([0, 57, 120], 8, False, 64),        # the same without the causal mask, one-page chunks
 ])
 def test_tile_kernel_shapes(lens, q_len, causal, chunk):
     w = synth.Workload("tile", lens, q_len=q_len, causal=causal, seed=q_len * 7 + len(lens),
