@@ -86,10 +86,11 @@ typedef struct kv_nvfp4_layout {
  * With at most 8 rows per KV head and at most 4 KV heads (decode) a group is one (sequence, tile
  * of 8 rows), covering every KV head; otherwise (speculative verify, prefill chunks, wider layouts)
  * a group is one (sequence, KV head, tile of 128 rows), run by the tile kernel. A group's pages
- * are split into chunks
- * of chunk_pages pages, and the chunks of all groups are shared out over `grid` CTAs in
- * contiguous, page-balanced ranges (one range may hold several chunks of a group, which the CTA
- * combines as it goes). */
+ * are split into chunks of chunk_pages pages, and the chunks of all groups are shared out over
+ * `grid` CTAs in contiguous ranges (one range may hold several chunks of a group, which the CTA
+ * combines as it goes): page-balanced for the decode kernel, and for the tile kernel balanced on
+ * pages plus a fixed charge of ten pages per segment (the smallest per-CTA cap that `grid` CTAs
+ * can fill, so trailing CTAs may get no work). */
 typedef struct kv_nvfp4_plan_info {
   int32_t num_seqs;
   int32_t q_len;
