@@ -252,3 +252,41 @@ def test_decode_step_host_rejects_bad_arguments_before_cuda(kv):
     a = list(args(1, 256))
     a[6] = 264                                                         # misaligned workspace
     assert lib.kv_nvfp4_decode_step_host(*a) == EINVAL
+
+
+@pytest.mark.parametrize("lens,q_len,causal,chunk,ctas,Hq,Hkv", [
+    ([2000, 37], 8, False, 256, 7, 24, 4), ([900, 3000], 5, True, 128, 11, 9, 3),
+    ([5000, 300, 2100], 8, True, 128, 16, 24, 4), ([700], 16, True, 64, 5, 24, 4),
+    ([4100, 4100], 8, True, 512, 9, 24, 4), ([1500, 20, 640], 12, False, 128, 13, 16, 2),
+])
+def test_tile_plan_minimises_the_largest_cta_cost(kv, lens, q_len, causal, chunk, ctas, Hq, Hkv):
+    # The tile plan's CTAs cover the chunk stream (groups in order, each cut into chunks) in
+    # contiguous ranges; a CTA costs its pages plus ten per segment (one segment per group it
+    # touches). An exact dynamic program over all contiguous splits into at most `grid` ranges
+    # gives the smallest possible largest cost, which the plan must reach.
+    L = kv.make_layout(Hq, Hkv)
+    info, groups, segs, cta, split = kv.kv_nvfp4_plan_host(L, lens, q_len, causal, chunk, ctas)
+    assert (Hq // Hkv) * q_len > 8  # the tile kernel's plan
+    cp = chunk // 64
+    chunks = [(g, min(cp, int(groups[g][6]) - lo))
+              for g in range(len(groups)) for lo in range(0, int(groups[g][6]), cp)]
+    n, grid, inf = len(chunks), int(info.grid), float("inf")
+    # cost[i][j]: one CTA taking chunks i .. j - 1
+    cost = [[0] * (n + 1) for _ in range(n + 1)]
+    for i in range(n):
+        pages, segs_in = 0, 0
+        for j in range(i + 1, n + 1):
+            g, pg = chunks[j - 1]
+            pages += pg
+            segs_in += 1 if (j - 1 == i or chunks[j - 2][0] != g) else 0
+            cost[i][j] = pages + 10 * segs_in
+    best = [0.0] + [inf] * n  # best[j]: chunks[:j] over the CTAs so far
+    for _ in range(grid):
+        nxt = best[:]  # a CTA may stay empty
+        for j in range(1, n + 1):
+            nxt[j] = min(nxt[j], min(max(best[i], cost[i][j]) for i in range(j)))
+        best = nxt
+    seg_cost = (segs[:, 2] - segs[:, 1]).astype(np.int64) + 10
+    csum = np.concatenate([[0], np.cumsum(seg_cost)])
+    plan_max = int((csum[cta[1:]] - csum[cta[:-1]]).max())
+    assert plan_max == best[n], (plan_max, best[n])
